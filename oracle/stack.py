@@ -1,0 +1,49 @@
+"""Layer-stack driver (oracle).
+
+Anchor layers output exact attention and replace the held index sets;
+reuse layers read the held sets unchanged, recomputing attention with their
+own q, K, V (euno.news summary, Key Contributions "Cross-layer Top-k reuse",
+Methodology 2-3). Layers before the first anchor have no sets to reuse and
+run dense (the pages' example anchor list does not start at layer 0).
+"""
+from . import attention as A
+
+
+def run_stack(mode, layers, k, anchors, group_map=None, scale=None, tile=A.TILE):
+    """layers: list of (q, K, V) per layer. Returns (outputs, sets_read).
+
+    ``sets_read[l]`` is the index array layer l consumed (None for anchors and
+    dense layers); anchors' own sets are returned in ``sets_written``.
+    """
+    anchors = set(anchors)
+    held = None
+    outs, sets_read, sets_written = [], [], []
+    for layer, (q, K, V) in enumerate(layers):
+        if mode == "decode":
+            if layer in anchors:
+                o, held, _ = A.anchor_decode(q, K, V, k, group_map, scale)
+                sets_read.append(None)
+                sets_written.append(held)
+            elif held is None:
+                o, _ = A.dense_decode(q, K, V, group_map, scale)
+                sets_read.append(None)
+                sets_written.append(None)
+            else:
+                o = A.sparse_decode(q, K, V, held, group_map, scale)
+                sets_read.append(held)
+                sets_written.append(None)
+        else:
+            if layer in anchors:
+                o, held = A.anchor_prefill(q, K, V, k, group_map, scale, tile)
+                sets_read.append(None)
+                sets_written.append(held)
+            elif held is None:
+                o = A.dense_prefill(q, K, V, group_map, scale, tile)
+                sets_read.append(None)
+                sets_written.append(None)
+            else:
+                o = A.sparse_prefill(q, K, V, held, group_map, scale, tile)
+                sets_read.append(held)
+                sets_written.append(None)
+        outs.append(o)
+    return outs, sets_read, sets_written

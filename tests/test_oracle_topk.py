@@ -1,0 +1,107 @@
+"""Pins for the oracle's Top-k rule (oracle/topk.py).
+
+Checked against: hand cases (tests/golden/topk_hand_cases.json), a brute
+force over all subsets for every small array built from a tricky value set,
+an independent partition-based selection, and hypothesis properties.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle.topk import topk_indices, kth_score
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "topk_hand_cases.json")
+
+
+def _parse(x):
+    return float(x) if not isinstance(x, str) else float(x.replace("inf", "inf"))
+
+
+def test_hand_cases():
+    with open(GOLDEN) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        s = np.array([_parse(x) for x in c["scores"]], dtype=np.float32)
+        assert topk_indices(s, c["k"]).tolist() == c["expected"], c["why"]
+
+
+def _valid_subset(s, S):
+    """Every selected element beats every unselected one: larger, or equal with lower index."""
+    inside = set(S)
+    for i in S:
+        for j in range(len(s)):
+            if j in inside:
+                continue
+            if s[i] > s[j]:
+                continue
+            if s[i] == s[j] and i < j:
+                continue
+            return False
+    return True
+
+
+@pytest.mark.parametrize("values,maxn", [((-0.0, 0.0, 1.0, 2.0, -math.inf), 5),
+                                         ((-0.0, 0.0, 1.0, -math.inf), 6)])
+def test_brute_force_all_small_arrays(values, maxn):
+    for n in range(1, maxn + 1):
+        for arr in itertools.product(values, repeat=n):
+            s = np.array(arr, dtype=np.float32)
+            for k in range(1, n + 1):
+                valid = [S for S in itertools.combinations(range(n), k) if _valid_subset(s, S)]
+                assert len(valid) == 1, (arr, k, valid)
+                assert topk_indices(s, k).tolist() == list(valid[0]), (arr, k)
+
+
+def _partition_topk(s, k):
+    """Independent rule: threshold = k-th largest value; take all strictly above,
+    then the lowest-index elements equal to it."""
+    n = len(s)
+    k = min(k, n)
+    thr = np.partition(s.astype(np.float64), n - k)[n - k]
+    above = [j for j in range(n) if s[j] > thr]
+    eq = [j for j in range(n) if s[j] == thr]
+    return sorted(above + eq[: k - len(above)])
+
+
+def test_matches_partition_rule_random():
+    rng = np.random.default_rng(5)
+    for trial in range(300):
+        n = int(rng.integers(1, 400))
+        # coarse values create many ties; include signed zeros and -inf
+        s = rng.integers(-4, 5, size=n).astype(np.float32)
+        s[rng.random(n) < 0.1] = -0.0
+        s[rng.random(n) < 0.05] = -np.inf
+        k = int(rng.integers(1, n + 1))
+        assert topk_indices(s, k).tolist() == _partition_topk(s, k)
+
+
+def test_nan_rejected():
+    with pytest.raises(ValueError):
+        topk_indices(np.array([1.0, np.nan, 0.0]), 1)
+
+
+def test_kth_score():
+    assert kth_score([3.0, 1.0, 2.0], 2) == 2.0
+
+
+hyp = pytest.importorskip("hypothesis")
+from hypothesis import given, settings, strategies as st  # noqa: E402
+
+
+@settings(max_examples=200, deadline=None)
+@given(st.lists(st.floats(allow_nan=False, width=32), min_size=1, max_size=64),
+       st.integers(min_value=1, max_value=80))
+def test_properties(vals, k):
+    s = np.array(vals, dtype=np.float32)
+    idx = topk_indices(s, k)
+    assert len(idx) == min(k, len(s))
+    assert list(idx) == sorted(set(idx.tolist()))
+    sel = set(idx.tolist())
+    for i in sel:
+        for j in range(len(s)):
+            if j not in sel:
+                assert s[i] > s[j] or (s[i] == s[j] and i < j)
