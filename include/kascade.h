@@ -1,0 +1,192 @@
+/*
+ * kascade.h — C ABI of libkascade: head-aware Top-k sparse attention with
+ * cross-layer index reuse (Kascade) on one GB300 GPU (sm_103a).
+ *
+ * Method (Kascade: A Practical Sparse Attention Method for Long-Context LLM
+ * Inference; euno.news summary, sections Key Contributions and Methodology;
+ * opentrain.ai page, Abstract):
+ *   - anchor layers compute attention exactly and take an exact Top-k of key
+ *     indices per head (Methodology 2, 5);
+ *   - reuse layers recompute attention with their own q, K, V, the softmax
+ *     restricted to the saved indices (Methodology 3);
+ *   - prefill works per query tile (Abstract, "tile-level operations"): one
+ *     index set per (head, 128-row tile), ranked by the tile's summed
+ *     post-softmax weights, capped at the tile's causal prefix;
+ *   - anchors are chosen offline by a DP that maximises cross-layer Top-k
+ *     overlap (Key Contributions, Methodology 4).
+ *
+ * Conventions for every entry point
+ *   - Device pointers are plain CUDA device addresses; the caller owns every
+ *     buffer. The library never allocates or frees device memory.
+ *   - Tensors are dense, row-major ("C-contiguous"), and their base addresses
+ *     are 16-byte aligned. Element type is given by kascade_desc.dtype for q,
+ *     k, v and out (bf16 or fp32); indices are int32; scores are fp32.
+ *   - Layouts (B batch, Hq query heads, Hkv KV heads, N length, d head_dim):
+ *       decode : q [B,Hq,d]   k,v [B,Hkv,N,d]   out [B,Hq,d]
+ *                idx [B,Hq,topk]            ascending key positions
+ *       prefill: q [B,Hq,N,d] k,v [B,Hkv,N,d]   out [B,Hq,N,d]
+ *                idx [B,Hq,nT,topk], nT = ceil(N/128); row t holds
+ *                k_t = min(topk, min(N,128(t+1))) ascending positions, then
+ *                -1 padding.
+ *   - Top-k rule: larger score first, lower index wins a tie, -0 == +0.
+ *     Decode ranks the scaled logits sigma*q.k (the same set as ranking the
+ *     softmax weights); prefill ranks the tile weights
+ *     w_j = sum_{i in tile, i >= j} softmax_i(j).
+ *   - `ws` is a caller-owned device workspace of at least
+ *     kascade_workspace_size() bytes, 256-byte aligned. It must be zeroed
+ *     once (kascade_workspace_init) before first use; afterwards the library
+ *     leaves it in a reusable state. Calls sharing one workspace must be
+ *     ordered (same stream, or synchronised).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). Argument errors are returned before anything is
+ *     launched; launch failures return KASCADE_ERR_CUDA. Faults found on the
+ *     device (NaN scores, an out-of-range index, an expired bounded wait) are
+ *     recorded in the workspace and read by kascade_device_error().
+ *   - No entry point throws, blocks on the device (except
+ *     kascade_device_error) or keeps pointers after it returns.
+ */
+#ifndef KASCADE_H
+#define KASCADE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KASCADE_OK = 0,
+  KASCADE_ERR_INVALID_ARG = 1,  /* bad shape, pointer, alignment, k, schedule */
+  KASCADE_ERR_UNSUPPORTED = 2,  /* valid but not built: head_dim, dtype, group size */
+  KASCADE_ERR_WORKSPACE = 3,    /* workspace missing or too small */
+  KASCADE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
+  KASCADE_ERR_BAD_INPUT = 5,    /* device-detected: NaN score or index out of range */
+  KASCADE_ERR_TIMEOUT = 6       /* device-detected: a bounded wait expired */
+} kascade_status;
+
+typedef enum { KASCADE_F32 = 0, KASCADE_BF16 = 1 } kascade_dtype;
+typedef enum { KASCADE_DECODE = 0, KASCADE_PREFILL = 1 } kascade_mode;
+
+/* Shape and numerics of one attention layer. */
+typedef struct {
+  int32_t batch;        /* B >= 1 */
+  int32_t n_q_heads;    /* Hq, a multiple of n_kv_heads, <= 256 */
+  int32_t n_kv_heads;   /* Hkv >= 1 */
+  int32_t head_dim;     /* d: 64 or 128 */
+  int32_t kv_len;       /* N: cached keys (decode) or sequence length (prefill) */
+  int32_t dtype;        /* kascade_dtype of q, k, v, out; prefill needs BF16 */
+  float scale;          /* sigma; <= 0 selects 1/sqrt(head_dim) */
+  /* Host array [n_q_heads]: KV head read by each query head (GQA), or NULL
+   * for h / (Hq/Hkv). Every KV head must serve exactly Hq/Hkv query heads;
+   * group sizes 1, 2, 4 and 8 are built. Read only during the call. */
+  const int32_t* group_map;
+} kascade_desc;
+
+/* Human-readable name of a status code (static storage). */
+const char* kascade_status_string(kascade_status s);
+
+/* Bytes of workspace the calls below need for this shape, Top-k size and
+ * mode (covers every decode or prefill entry point and kascade_run_stack).
+ * Returns 0 for an invalid descriptor. */
+size_t kascade_workspace_size(const kascade_desc* desc, int32_t topk, int32_t mode);
+
+/* Zero a workspace (cudaMemsetAsync on `stream`). */
+kascade_status kascade_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, then read and clear the device error word of `ws`:
+ * KASCADE_OK, KASCADE_ERR_BAD_INPUT or KASCADE_ERR_TIMEOUT. */
+kascade_status kascade_device_error(void* ws, void* stream);
+
+/* ---------------------------------------------------------------- decode -- */
+
+/* Exact attention for one query per sequence over all N cached keys (the
+ * library's own dense baseline; also the anchor layer's output).
+ * out[b,h] = sum_j softmax_j(sigma q[b,h].k[b,g(h),j]) v[b,g(h),j]. */
+kascade_status kascade_dense_decode(const kascade_desc* desc, const void* q, const void* k,
+                                    const void* v, void* out, void* ws, size_t ws_bytes,
+                                    void* stream);
+
+/* Anchor layer (Methodology 2): exact output as kascade_dense_decode, and the
+ * exact Top-k (1 <= topk <= N) of the scaled logits of every (sequence,
+ * query head) in idx_out [B,Hq,topk], ascending. When scores_out is not NULL
+ * the fp32 logits sigma*q.k are also written there, [B,Hq,N]. */
+kascade_status kascade_anchor_decode(const kascade_desc* desc, const void* q, const void* k,
+                                     const void* v, int32_t topk, void* out, int32_t* idx_out,
+                                     float* scores_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Reuse layer (Methodology 3): out[b,h] = softmax restricted to the saved set
+ * S = idx[b,h,:] (topk ascending, distinct positions in [0,N)), computed with
+ * this layer's q, k, v. Rows of k and v outside the sets are not read. Query
+ * heads of one KV head share one pass over the union of their sets. */
+kascade_status kascade_reuse_decode(const kascade_desc* desc, const void* q, const void* k,
+                                    const void* v, int32_t topk, const int32_t* idx, void* out,
+                                    void* ws, size_t ws_bytes, void* stream);
+
+/* Exact Top-k of fp32 rows: scores [rows, n] (row stride n) -> idx [rows,k]
+ * ascending, 1 <= k <= n. A NaN anywhere sets KASCADE_ERR_BAD_INPUT on the
+ * device. This is the selection the anchor calls use. Needs no workspace
+ * beyond the error word (ws may be any workspace, >= 256 bytes). */
+kascade_status kascade_topk(const float* scores, int32_t rows, int32_t n, int32_t k,
+                            int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
+
+/* --------------------------------------------------------------- prefill -- */
+
+/* Causal exact attention (the library's own dense baseline), bf16 only. */
+kascade_status kascade_dense_prefill(const kascade_desc* desc, const void* q, const void* k,
+                                     const void* v, void* out, void* ws, size_t ws_bytes,
+                                     void* stream);
+
+/* Anchor layer, prefill: exact causal output, then per (sequence, query
+ * head, 128-row tile t) the Top-k_t of the tile weights w_j, k_t =
+ * min(topk, L_t), L_t = min(N, 128(t+1)), into idx_out [B,Hq,nT,topk]
+ * (ascending, -1 padded). */
+kascade_status kascade_anchor_prefill(const kascade_desc* desc, const void* q, const void* k,
+                                      const void* v, int32_t topk, void* out, int32_t* idx_out,
+                                      void* ws, size_t ws_bytes, void* stream);
+
+/* Reuse layer, prefill: row i of tile t attends to S_i = {j in idx[b,h,t,:],
+ * j >= 0, j <= i}; a row whose S_i is empty outputs zeros. */
+kascade_status kascade_reuse_prefill(const kascade_desc* desc, const void* q, const void* k,
+                                     const void* v, int32_t topk, const int32_t* idx, void* out,
+                                     void* ws, size_t ws_bytes, void* stream);
+
+/* ----------------------------------------------------------------- stack -- */
+
+/* Run n_layers layers of one mode. q[l], k[l], v[l], out[l] are host arrays
+ * of device pointers (layouts as above). anchors: host array, strictly
+ * ascending layer numbers in [0, n_layers). Layer l is an anchor when listed;
+ * otherwise it reuses the sets of the most recent anchor <= l, or runs dense
+ * when no anchor precedes it. idx_buf (device, the decode or prefill idx
+ * layout) holds the current sets; on return it holds the last anchor's. The
+ * sets never leave the device. */
+kascade_status kascade_run_stack(const kascade_desc* desc, int32_t mode, int32_t n_layers,
+                                 const void* const* q, const void* const* k,
+                                 const void* const* v, int32_t topk, const int32_t* anchors,
+                                 int32_t n_anchors, void* const* out, int32_t* idx_buf,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------ scheduling -- */
+
+/* Cross-layer Top-k overlap for the anchor DP (Methodology 4). sets: device
+ * int32 [n_layers, units, topk], each row distinct positions in [0, n_bits).
+ * counts_out: device int64 [n_layers, n_layers], counts_out[i][l] =
+ * sum over units of |S_i ∩ S_l| (symmetric). Needs ws of
+ * kascade_overlap_workspace_size bytes. */
+size_t kascade_overlap_workspace_size(int32_t n_layers, int32_t units, int32_t n_bits);
+kascade_status kascade_layer_overlap(const int32_t* sets, int32_t n_layers, int32_t units,
+                                     int32_t topk, int32_t n_bits, int64_t* counts_out,
+                                     void* ws, size_t ws_bytes, void* stream);
+
+/* Host DP: choose n_anchors layers (always including 0) maximising
+ * F(A) = sum_l sim[a(l) * n_layers + l], a(l) = most recent anchor <= l.
+ * sim: host [n_layers * n_layers], row i = anchor layer. Ties go to the
+ * lexicographically smallest list. anchors_out: host [n_anchors],
+ * ascending. objective_out may be NULL. */
+kascade_status kascade_schedule_anchors(const double* sim, int32_t n_layers, int32_t n_anchors,
+                                        int32_t* anchors_out, double* objective_out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KASCADE_H */

@@ -1,0 +1,675 @@
+// decode.cu — decode attention for one query per sequence (Kascade anchor
+// and reuse layers; euno.news summary, Methodology 2-3).
+//
+//   k_decode_dense_bf16   split-K flash-decode over all N keys of one
+//                         (sequence, KV head). A producer warp streams K/V
+//                         tiles into shared memory with TMA (128-byte
+//                         swizzle, mbarrier pipeline); consumer warps run the
+//                         G query heads of the group together as mma.sync
+//                         m16n8k16 tiles (keys x heads), online softmax in
+//                         fp32, and (anchor layers) spill the scaled logits
+//                         sigma*q.k for the Top-k selection.
+//   k_build_union_plan    merges the G per-head index sets of one KV head
+//                         into one ascending list of keys with a head mask.
+//   k_decode_union_bf16   reuse layer: gathers only the planned K/V rows
+//                         (16-byte cp.async into the same swizzled layout)
+//                         and runs the same tile math with per-(key, head)
+//                         masking, so a row shared by several heads of a
+//                         group is read once.
+//   k_decode_generic      CUDA-core path for fp32 inputs.
+// The split kernels finish with a last-arriving-CTA merge of the split
+// partials (log-sum-exp combine), so a layer is one launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kascade {
+
+namespace {
+
+#define kNegInf (-CUDART_INF_F)
+
+// ------------------------------------------------------------------------
+// Consumer math on one 16-key slice held in swizzled shared memory. Thread
+// (gid = lane/4, c4 = lane%4) owns heads 2*c4, 2*c4+1 and keys gid, gid+8 of
+// the slice's score tile, and output dims 16*mt+gid(+8) of those two heads.
+// ------------------------------------------------------------------------
+template <int D>
+struct WarpState {
+  float m[2];
+  float l[2];
+  float o[D / 16][4];
+};
+
+template <int D>
+__device__ __forceinline__ void warp_state_init(WarpState<D>& st) {
+  st.m[0] = st.m[1] = kNegInf;
+  st.l[0] = st.l[1] = 0.f;
+#pragma unroll
+  for (int i = 0; i < D / 16; ++i) st.o[i][0] = st.o[i][1] = st.o[i][2] = st.o[i][3] = 0.f;
+}
+
+// Scores of the 16 keys of a slice against the (up to 8) group heads:
+// sc[0]=(key gid, head 2c4) sc[1]=(gid, 2c4+1) sc[2]=(gid+8, 2c4) sc[3]=(gid+8, 2c4+1).
+template <int D>
+__device__ __forceinline__ void slice_scores(uint32_t kbase, int rows, int row0,
+                                             const uint32_t (&qf)[D / 16][2], float (&sc)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int mi = lane >> 3, r = lane & 7;
+  const int row = row0 + (mi & 1) * 8 + r;
+  float acc0[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(kbase + sw128_offset(rows, row, 2 * kk + (mi >> 1)), a0, a1, a2, a3);
+    if (kk & 1)
+      mma_bf16_16816(acc1, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+    else
+      mma_bf16_16816(acc0, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) sc[i] = acc0[i] + acc1[i];
+}
+
+// Online-softmax update with log2-domain scores x (masked entries -inf),
+// then O^T += V^T P^T on the tensor cores.
+template <int D>
+__device__ __forceinline__ void slice_softmax_pv(WarpState<D>& st, const float (&x)[4],
+                                                 uint32_t vbase, int rows, int row0) {
+  const int lane = threadIdx.x & 31;
+  float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const float mn0 = fmaxf(st.m[0], mx0), mn1 = fmaxf(st.m[1], mx1);
+  const float al0 = (mn0 == kNegInf) ? 1.f : fast_exp2(st.m[0] - mn0);
+  const float al1 = (mn1 == kNegInf) ? 1.f : fast_exp2(st.m[1] - mn1);
+  const float mu0 = (mn0 == kNegInf) ? 0.f : mn0;
+  const float mu1 = (mn1 == kNegInf) ? 0.f : mn1;
+  const float p0 = fast_exp2(x[0] - mu0), p1 = fast_exp2(x[1] - mu1);
+  const float p2 = fast_exp2(x[2] - mu0), p3 = fast_exp2(x[3] - mu1);
+  st.l[0] = st.l[0] * al0 + p0 + p2;
+  st.l[1] = st.l[1] * al1 + p1 + p3;
+  st.m[0] = mn0;
+  st.m[1] = mn1;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    st.o[mt][0] *= al0;
+    st.o[mt][1] *= al1;
+    st.o[mt][2] *= al0;
+    st.o[mt][3] *= al1;
+  }
+  // P (keys x heads) -> P^T fragments (heads x keys) for the B operand.
+  const uint32_t b0 = movmatrix_t(pack_bf16(p0, p1));
+  const uint32_t b1 = movmatrix_t(pack_bf16(p2, p3));
+  const int mi = lane >> 3, r = lane & 7;
+  const int row = row0 + (mi >> 1) * 8 + r;
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_t(vbase + sw128_offset(rows, row, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+    mma_bf16_16816(st.o[mt], a0, a1, a2, a3, b0, b1);
+  }
+}
+
+// q fragments (B operand of keys x heads): qf[kk] = q[head gid][16kk + 2c4 (+8)].
+template <int D>
+__device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g,
+                                             uint32_t (&qf)[D / 16][2]) {
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2, c4 = lane & 3;
+  const bool ok = gid < a.G;
+  const int hq = ok ? a.heads[g * a.G + gid] : 0;
+  const uint32_t* qrow =
+      reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                        (static_cast<size_t>(b) * a.Hq + hq) * D);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    qf[kk][0] = ok ? __ldg(qrow + 8 * kk + c4) : 0u;
+    qf[kk][1] = ok ? __ldg(qrow + 8 * kk + 4 + c4) : 0u;
+  }
+}
+
+// Merge the consumer warps' states through shared memory, write this CTA's
+// partial (or the final output when there is one split), and let the last
+// CTA of the (sequence, KV head) merge all splits. `scratch` must hold
+// (16 + 8*D) * n_consumers + 16 + 8 * S floats.
+template <int D>
+__device__ void finish_cta(const DecodeArgs& a, WarpState<D>& st, int cw, int n_consumers,
+                           float* scratch, int b, int g, int split) {
+  __shared__ unsigned int s_last;
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2, c4 = lane & 3;
+  // sum l across the 8 lanes that share a head pair
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    st.l[0] += __shfl_xor_sync(0xffffffffu, st.l[0], off);
+    st.l[1] += __shfl_xor_sync(0xffffffffu, st.l[1], off);
+  }
+  // scratch layout: m[W][8], l[W][8], o[W][8][D], cm[8], cl[8]
+  float* sm = scratch;
+  float* sl = scratch + n_consumers * 8;
+  float* so = scratch + n_consumers * 16;
+  float* cm = so + n_consumers * 8 * D;
+  float* cl = cm + 8;
+  if (cw >= 0) {
+    if (gid == 0) {
+      sm[cw * 8 + 2 * c4] = st.m[0];
+      sm[cw * 8 + 2 * c4 + 1] = st.m[1];
+      sl[cw * 8 + 2 * c4] = st.l[0];
+      sl[cw * 8 + 2 * c4 + 1] = st.l[1];
+    }
+    float* base = so + (cw * 8) * D;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      base[(2 * c4) * D + 16 * mt + gid] = st.o[mt][0];
+      base[(2 * c4 + 1) * D + 16 * mt + gid] = st.o[mt][1];
+      base[(2 * c4) * D + 16 * mt + gid + 8] = st.o[mt][2];
+      base[(2 * c4 + 1) * D + 16 * mt + gid + 8] = st.o[mt][3];
+    }
+  }
+  __syncthreads();
+  const int G = a.G;
+  const int unit = b * a.Hkv + g;
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
+    float M = kNegInf;
+    for (int w = 0; w < n_consumers; ++w) M = fmaxf(M, sm[w * 8 + h]);
+    float L = 0.f;
+    for (int w = 0; w < n_consumers; ++w) {
+      const float mw = sm[w * 8 + h];
+      if (mw != kNegInf) L += fast_exp2(mw - M) * sl[w * 8 + h];
+    }
+    cm[h] = M;
+    cl[h] = L;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+    const int h = e / D, dd = e % D;
+    const float M = cm[h];
+    float acc = 0.f;
+    for (int w = 0; w < n_consumers; ++w) {
+      const float mw = sm[w * 8 + h];
+      if (mw != kNegInf) acc += fast_exp2(mw - M) * so[(w * 8 + h) * D + dd];
+    }
+    const int hq = a.heads[g * G + h];
+    if (a.S == 1) {
+      const float L = cl[h];
+      const float y = L > 0.f ? acc / L : 0.f;
+      static_cast<__nv_bfloat16*>(a.out)[(static_cast<size_t>(b) * a.Hq + hq) * D + dd] =
+          __float2bfloat16_rn(y);
+    } else {
+      float* pp = a.part + ((static_cast<size_t>(b) * a.Hq + hq) * a.S + split) * (D + 4);
+      pp[4 + dd] = acc;
+      if (dd == 0) {
+        pp[0] = M;
+        pp[1] = cl[h];
+      }
+    }
+  }
+  if (a.S == 1) return;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const unsigned int prev = atomicAdd(&a.counters[unit], 1u);
+    s_last = (prev == static_cast<unsigned int>(a.S - 1)) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // Final merge over splits: weights w_s = 2^(m_s - M) / L per head.
+  float* wts = cl + 8;   // [G][S]
+  if (threadIdx.x < G) {
+    const int h = threadIdx.x;
+    const int hq = a.heads[g * G + h];
+    const float* pp = a.part + (static_cast<size_t>(b) * a.Hq + hq) * a.S * (D + 4);
+    float M = kNegInf;
+    for (int s = 0; s < a.S; ++s) M = fmaxf(M, __ldcg(pp + s * (D + 4)));
+    float L = 0.f;
+    for (int s = 0; s < a.S; ++s) {
+      const float ms = __ldcg(pp + s * (D + 4));
+      const float w = (ms == kNegInf) ? 0.f : fast_exp2(ms - M);
+      wts[h * a.S + s] = w;
+      L += w * __ldcg(pp + s * (D + 4) + 1);
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    for (int s = 0; s < a.S; ++s) wts[h * a.S + s] *= inv;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+    const int h = e / D, dd = e % D;
+    const int hq = a.heads[g * G + h];
+    const float* pp = a.part + (static_cast<size_t>(b) * a.Hq + hq) * a.S * (D + 4);
+    float acc = 0.f;
+    for (int s = 0; s < a.S; ++s) acc += wts[h * a.S + s] * __ldcg(pp + s * (D + 4) + 4 + dd);
+    static_cast<__nv_bfloat16*>(a.out)[(static_cast<size_t>(b) * a.Hq + hq) * D + dd] =
+        __float2bfloat16_rn(acc);
+  }
+  if (threadIdx.x == 0) a.counters[unit] = 0u;   // ready for the next launch
+}
+
+// ------------------------------------------------------------------------
+// Dense / anchor decode, TMA producer warp + NW consumer warps.
+// ------------------------------------------------------------------------
+template <int D, int NW, int STAGES, bool SPILL>
+__global__ void __launch_bounds__((NW + 1) * 32)
+    k_decode_dense_bf16(const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ DecodeArgs a) {
+  constexpr int TK = 16 * NW;
+  constexpr int HALVES = D / 64;
+  constexpr int TILE_BYTES = HALVES * TK * 128;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char* ktile = smem;
+  unsigned char* vtile = smem + STAGES * TILE_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(vtile + STAGES * TILE_BYTES);
+  uint64_t* empty = full + STAGES;
+
+  const int split = blockIdx.x, unit = blockIdx.y;
+  const int b = unit / a.Hkv, g = unit % a.Hkv;
+  const int n0 = split * a.chunk;
+  const int n1 = min(a.N, n0 + a.chunk);
+  const int ntiles = n0 < n1 ? (n1 - n0 + TK - 1) / TK : 0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NW);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  WarpState<D> st;
+  warp_state_init(st);
+  if (warp == NW) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      const int row_base = unit * a.N + n0;
+      int issued = 0;
+      for (int t = 0; t < ntiles; ++t) {
+        const int s = t % STAGES;
+        if (!mbar_wait(&empty[s], ((t / STAGES) & 1) ^ 1, a.err, 0x101)) break;
+        mbar_arrive_expect_tx(&full[s], 2 * TILE_BYTES);
+#pragma unroll
+        for (int hf = 0; hf < HALVES; ++hf) {
+          tma_load_2d(ktile + s * TILE_BYTES + hf * TK * 128, &tmK, &full[s], hf * 64,
+                      row_base + t * TK);
+          tma_load_2d(vtile + s * TILE_BYTES + hf * TK * 128, &tmV, &full[s], hf * 64,
+                      row_base + t * TK);
+        }
+        issued = t + 1;
+      }
+      // Never leave with copies in flight.
+      for (int t = issued > STAGES ? issued - STAGES : 0; t < issued; ++t)
+        mbar_wait(&full[t % STAGES], (t / STAGES) & 1, a.err, 0x102);
+    }
+  } else {
+    // ---------------- consumers ----------------
+    uint32_t qf[D / 16][2];
+    load_q_frags<D>(a, b, g, qf);
+    const int gid = lane >> 2, c4 = lane & 3;
+    const int row0 = warp * 16;
+    const bool hv0 = 2 * c4 < a.G, hv1 = 2 * c4 + 1 < a.G;
+    float* sp0 = nullptr;
+    float* sp1 = nullptr;
+    if (SPILL) {
+      if (hv0) sp0 = a.spill + (static_cast<size_t>(b) * a.Hq + a.heads[g * a.G + 2 * c4]) * a.N;
+      if (hv1)
+        sp1 = a.spill + (static_cast<size_t>(b) * a.Hq + a.heads[g * a.G + 2 * c4 + 1]) * a.N;
+    }
+    for (int t = 0; t < ntiles; ++t) {
+      const int s = t % STAGES;
+      if (!mbar_wait(&full[s], (t / STAGES) & 1, a.err, 0x103)) break;
+      float sc[4];
+      slice_scores<D>(smem_u32(ktile + s * TILE_BYTES), TK, row0, qf, sc);
+      const int key0 = n0 + t * TK + row0 + gid, key1 = key0 + 8;
+      const bool kv0 = key0 < n1, kv1 = key1 < n1;
+      if (SPILL) {
+        if (kv0) {
+          if (hv0) sp0[key0] = sc[0] * a.scale;
+          if (hv1) sp1[key0] = sc[1] * a.scale;
+        }
+        if (kv1) {
+          if (hv0) sp0[key1] = sc[2] * a.scale;
+          if (hv1) sp1[key1] = sc[3] * a.scale;
+        }
+      }
+      float x[4];
+      x[0] = kv0 ? sc[0] * a.scale_log2 : kNegInf;
+      x[1] = kv0 ? sc[1] * a.scale_log2 : kNegInf;
+      x[2] = kv1 ? sc[2] * a.scale_log2 : kNegInf;
+      x[3] = kv1 ? sc[3] * a.scale_log2 : kNegInf;
+      slice_softmax_pv<D>(st, x, smem_u32(vtile + s * TILE_BYTES), TK, row0);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+  }
+  __syncthreads();
+  finish_cta<D>(a, st, warp < NW ? warp : -1, NW, reinterpret_cast<float*>(smem), b, g, split);
+}
+
+// ------------------------------------------------------------------------
+// Union plan: per (sequence, KV head), merge the G ascending per-head sets
+// into one ascending key list; entry = key | (head-slot mask << 24).
+// One 1024-thread CTA per unit, per-slot bitmaps of N bits in shared memory.
+// ------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_build_union_plan(const __grid_constant__ DecodeArgs a,
+                                                           uint32_t* __restrict__ plan,
+                                                           int32_t* __restrict__ plan_count) {
+  extern __shared__ uint32_t bm[];   // [G][words]
+  __shared__ int s_scan[1024];
+  const int unit = blockIdx.x;
+  const int b = unit / a.Hkv, g = unit % a.Hkv;
+  const int G = a.G, N = a.N, topk = a.topk;
+  const int words = (N + 31) / 32;
+  for (int i = threadIdx.x; i < G * words; i += blockDim.x) bm[i] = 0u;
+  __syncthreads();
+  for (int slot = 0; slot < G; ++slot) {
+    const int hq = a.heads[g * G + slot];
+    const int32_t* row = a.idx + (static_cast<size_t>(b) * a.Hq + hq) * topk;
+    for (int j = threadIdx.x; j < topk; j += blockDim.x) {
+      const int key = row[j];
+      if (key < 0 || key >= N) {
+        report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x201);
+        continue;
+      }
+      atomicOr(&bm[slot * words + (key >> 5)], 1u << (key & 31));
+    }
+  }
+  __syncthreads();
+  // each thread owns a contiguous run of words
+  const int per = (words + blockDim.x - 1) / blockDim.x;
+  const int w0 = min(words, static_cast<int>(threadIdx.x) * per), w1 = min(words, w0 + per);
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t u = 0;
+    for (int slot = 0; slot < G; ++slot) u |= bm[slot * words + w];
+    cnt += __popc(u);
+  }
+  s_scan[threadIdx.x] = cnt;
+  __syncthreads();
+  for (int off = 1; off < static_cast<int>(blockDim.x); off <<= 1) {
+    const int v = static_cast<int>(threadIdx.x) >= off ? s_scan[threadIdx.x - off] : 0;
+    __syncthreads();
+    s_scan[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int pos = s_scan[threadIdx.x] - cnt;
+  uint32_t* out = plan + static_cast<size_t>(unit) * a.plan_stride;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t u = 0;
+    for (int slot = 0; slot < G; ++slot) u |= bm[slot * words + w];
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      uint32_t mask = 0;
+      for (int slot = 0; slot < G; ++slot) mask |= ((bm[slot * words + w] >> bit) & 1u) << slot;
+      out[pos++] = static_cast<uint32_t>(w * 32 + bit) | (mask << 24);
+    }
+  }
+  if (threadIdx.x == blockDim.x - 1) plan_count[unit] = s_scan[threadIdx.x];
+}
+
+// ------------------------------------------------------------------------
+// Reuse decode over the union plan; every warp gathers its own 16-row
+// slices through a STAGES-deep cp.async pipeline (no block barriers).
+// ------------------------------------------------------------------------
+template <int D, int NW, int STAGES>
+__global__ void __launch_bounds__(NW * 32)
+    k_decode_union_bf16(const __grid_constant__ DecodeArgs a) {
+  constexpr int SLICE = (D / 64) * 16 * 128;     // bytes of one K (or V) slice
+  constexpr int CHUNKS = D / 8;                   // 16-byte chunks per row
+  constexpr int ROWS_PER_INSTR = 32 / CHUNKS;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* wbuf = smem + warp * STAGES * 2 * SLICE;
+
+  const int split = blockIdx.x, unit = blockIdx.y;
+  const int b = unit / a.Hkv, g = unit % a.Hkv;
+  const int U = a.plan_count[unit];
+  int cs = (U + a.S - 1) / a.S;
+  cs = (cs + 15) & ~15;
+  const int e0 = split * cs;
+  const int e1 = min(U, e0 + cs);
+  const int nslices = e0 < e1 ? (e1 - e0 + 15) / 16 : 0;
+  const int my = warp < nslices ? (nslices - warp + NW - 1) / NW : 0;
+  const uint32_t* plan = a.plan + static_cast<size_t>(unit) * a.plan_stride;
+  const __nv_bfloat16* kbase =
+      static_cast<const __nv_bfloat16*>(a.k) + static_cast<size_t>(unit) * a.N * D;
+  const __nv_bfloat16* vbase =
+      static_cast<const __nv_bfloat16*>(a.v) + static_cast<size_t>(unit) * a.N * D;
+
+  auto issue = [&](int i) {
+    const int sl = warp + i * NW;
+    const int stg = i % STAGES;
+    const int e = e0 + sl * 16 + (lane & 15);
+    const uint32_t ent = (e < e1) ? __ldg(plan + e) : 0u;
+    unsigned char* kd = wbuf + stg * 2 * SLICE;
+    unsigned char* vd = kd + SLICE;
+#pragma unroll
+    for (int it = 0; it < 16 / ROWS_PER_INSTR; ++it) {
+      const int row = it * ROWS_PER_INSTR + lane / CHUNKS;
+      const int ch = lane % CHUNKS;
+      const uint32_t ent_r = __shfl_sync(0xffffffffu, ent, row);
+      const bool ok = (e0 + sl * 16 + row) < e1;
+      const size_t off = static_cast<size_t>(ent_r & 0xFFFFFFu) * D + ch * 8;
+      cp_async16(kd + sw128_offset(16, row, ch), kbase + off, ok ? 16u : 0u);
+      cp_async16(vd + sw128_offset(16, row, ch), vbase + off, ok ? 16u : 0u);
+    }
+  };
+
+  WarpState<D> st;
+  warp_state_init(st);
+  uint32_t qf[D / 16][2];
+  load_q_frags<D>(a, b, g, qf);
+  const int gid = lane >> 2, c4 = lane & 3;
+
+#pragma unroll
+  for (int i = 0; i < STAGES - 1; ++i) {
+    if (i < my) issue(i);
+    cp_async_commit();
+  }
+  for (int i = 0; i < my; ++i) {
+    if (i + STAGES - 1 < my) issue(i + STAGES - 1);
+    cp_async_commit();
+    cp_async_wait<STAGES - 1>();
+    __syncwarp();
+    const int sl = warp + i * NW;
+    const uint32_t kd = smem_u32(wbuf + (i % STAGES) * 2 * SLICE);
+    float sc[4];
+    slice_scores<D>(kd, 16, 0, qf, sc);
+    const int e = e0 + sl * 16 + (lane & 15);
+    const uint32_t ent = (e < e1) ? __ldg(plan + e) : 0u;
+    const uint32_t m0 = __shfl_sync(0xffffffffu, ent, gid) >> 24;
+    const uint32_t m1 = __shfl_sync(0xffffffffu, ent, gid + 8) >> 24;
+    float x[4];
+    x[0] = ((m0 >> (2 * c4)) & 1u) ? sc[0] * a.scale_log2 : kNegInf;
+    x[1] = ((m0 >> (2 * c4 + 1)) & 1u) ? sc[1] * a.scale_log2 : kNegInf;
+    x[2] = ((m1 >> (2 * c4)) & 1u) ? sc[2] * a.scale_log2 : kNegInf;
+    x[3] = ((m1 >> (2 * c4 + 1)) & 1u) ? sc[3] * a.scale_log2 : kNegInf;
+    slice_softmax_pv<D>(st, x, kd + SLICE, 16, 0);
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  finish_cta<D>(a, st, warp, NW, reinterpret_cast<float*>(smem), b, g, split);
+}
+
+// ------------------------------------------------------------------------
+// Generic CUDA-core decode: one CTA per (query head, sequence); fp32 inputs.
+// Logits go to the spill buffer (always present on this path), then a block
+// softmax and a dim-parallel weighted sum of V.
+// ------------------------------------------------------------------------
+__device__ float block_reduce(float v, bool is_max, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
+  }
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  const int nw = blockDim.x >> 5;
+  float r = is_max ? kNegInf : 0.f;
+  for (int w = 0; w < nw; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
+  return r;
+}
+
+__global__ void k_decode_generic_f32(const __grid_constant__ DecodeArgs a, int D, int kind) {
+  extern __shared__ float qs[];   // [D]
+  __shared__ float red[32];
+  const int b = blockIdx.y, hq = blockIdx.x;
+  int g = 0;
+  for (int gg = 0; gg < a.Hkv; ++gg)
+    for (int s = 0; s < a.G; ++s)
+      if (a.heads[gg * a.G + s] == hq) g = gg;
+  const float* q = static_cast<const float*>(a.q) + (static_cast<size_t>(b) * a.Hq + hq) * D;
+  const float* K = static_cast<const float*>(a.k) + (static_cast<size_t>(b) * a.Hkv + g) * a.N * D;
+  const float* V = static_cast<const float*>(a.v) + (static_cast<size_t>(b) * a.Hkv + g) * a.N * D;
+  float* s = a.spill + (static_cast<size_t>(b) * a.Hq + hq) * a.N;
+  const int32_t* sel =
+      (kind == kSparse) ? a.idx + (static_cast<size_t>(b) * a.Hq + hq) * a.topk : nullptr;
+  const int n = (kind == kSparse) ? a.topk : a.N;
+  for (int c = threadIdx.x; c < D; c += blockDim.x) qs[c] = q[c];
+  __syncthreads();
+  float mx = kNegInf;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    int key = j;
+    if (sel) {
+      key = sel[j];
+      if (key < 0 || key >= a.N) {
+        report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x301);
+        key = 0;
+      }
+    }
+    float acc = 0.f;
+    for (int c = 0; c < D; ++c) acc = fmaf(qs[c], K[static_cast<size_t>(key) * D + c], acc);
+    acc *= a.scale;
+    s[j] = acc;              // sparse: slot j of the set; dense: key j
+    mx = fmaxf(mx, acc);
+  }
+  mx = block_reduce(mx, true, red);
+  float sum = 0.f;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) sum += expf(s[j] - mx);
+  sum = block_reduce(sum, false, red);
+  const float inv = 1.f / sum;
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {
+    float acc = 0.f;
+    for (int j = 0; j < n; ++j) {
+      int key = sel ? sel[j] : j;
+      if (key < 0 || key >= a.N) key = 0;
+      acc = fmaf(expf(s[j] - mx), V[static_cast<size_t>(key) * D + c], acc);
+    }
+    static_cast<float*>(a.out)[(static_cast<size_t>(b) * a.Hq + hq) * D + c] = acc * inv;
+  }
+}
+
+template <int D, int NW, int STAGES, bool SPILL>
+cudaError_t launch_dense_t(const DecodeArgs& a, cudaStream_t st) {
+  constexpr int TK = 16 * NW;
+  alignas(64) CUtensorMap tk, tv;
+  const uint64_t rows = static_cast<uint64_t>(a.B) * a.Hkv * a.N;
+  if (!encode_tmap_2d_bf16(&tk, a.k, D, rows, 64, TK, true)) return cudaErrorInvalidValue;
+  if (!encode_tmap_2d_bf16(&tv, a.v, D, rows, 64, TK, true)) return cudaErrorInvalidValue;
+  constexpr int TILE_BYTES = (D / 64) * TK * 128;
+  const size_t smem = 1024 + 2 * STAGES * TILE_BYTES + 2 * STAGES * 8;
+  auto kern = k_decode_dense_bf16<D, NW, STAGES, SPILL>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.S, a.B * a.Hkv);
+  kern<<<grid, (NW + 1) * 32, smem, st>>>(tk, tv, a);
+  return cudaGetLastError();
+}
+
+template <int D, int NW, int STAGES>
+cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
+  constexpr int SLICE = (D / 64) * 16 * 128;
+  const size_t smem = 1024 + static_cast<size_t>(NW) * STAGES * 2 * SLICE;
+  auto kern = k_decode_union_bf16<D, NW, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.S, a.B * a.Hkv);
+  kern<<<grid, NW * 32, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Launch shapes: 4 consumer warps (64-key tiles) per CTA, 2 CTAs per SM;
+// about four waves of CTAs over the 152 SMs.
+constexpr int kDenseNW = 4;
+constexpr int kUnionNW = 4;
+constexpr int kTargetCtas = 152 * 2 * 4;
+
+int decode_chunk_dense(int units, int N) {
+  int s = (kTargetCtas + units - 1) / units;
+  if (s < 1) s = 1;
+  int chunk = (N + s - 1) / s;
+  const int min_chunk = (N + kMaxSplits - 1) / kMaxSplits;
+  if (chunk < min_chunk) chunk = min_chunk;
+  if (chunk < 256) chunk = 256;
+  return (chunk + 63) & ~63;
+}
+
+int decode_splits_union(int units, int G, int topk) {
+  int s = (kTargetCtas + units - 1) / units;
+  const int max_by_len = (G * topk + 255) / 256;
+  if (s > max_by_len) s = max_by_len;
+  if (s > kMaxSplits) s = kMaxSplits;
+  if (s < 1) s = 1;
+  return s;
+}
+
+cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spill,
+                                     cudaStream_t st) {
+  if (head_dim == 128)
+    return spill ? launch_dense_t<128, kDenseNW, 3, true>(a, st)
+                 : launch_dense_t<128, kDenseNW, 3, false>(a, st);
+  if (head_dim == 64)
+    return spill ? launch_dense_t<64, kDenseNW, 6, true>(a, st)
+                 : launch_dense_t<64, kDenseNW, 6, false>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_union_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st) {
+  if (head_dim == 128) return launch_union_t<128, kUnionNW, 3>(a, st);
+  if (head_dim == 64) return launch_union_t<64, kUnionNW, 6>(a, st);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_build_union_plan(const DecodeArgs& a, uint32_t* plan, int32_t* plan_count,
+                                    cudaStream_t st) {
+  const size_t smem = static_cast<size_t>(a.G) * ((a.N + 31) / 32) * 4;
+  cudaError_t e = cudaFuncSetAttribute(k_build_union_plan,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  k_build_union_plan<<<a.B * a.Hkv, 1024, smem, st>>>(a, plan, plan_count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_generic(const DecodeArgs& a, int head_dim, int dtype, DecodeKind kind,
+                                  cudaStream_t st) {
+  if (dtype != KASCADE_F32) return cudaErrorInvalidValue;
+  dim3 grid(a.Hq, a.B);
+  k_decode_generic_f32<<<grid, 256, head_dim * sizeof(float), st>>>(a, head_dim, kind);
+  return cudaGetLastError();
+}
+
+}  // namespace kascade

@@ -1,0 +1,91 @@
+// internal.h — launch interfaces between the C ABI layer (api.cu) and the
+// kernel translation units. Plain structs of device pointers and sizes.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kascade {
+
+constexpr int kMaxQHeads = 256;
+constexpr int kMaxSplits = 128;
+
+// One decode attention layer (dense, anchor or reuse).
+struct DecodeArgs {
+  const void* q;            // [B,Hq,d]
+  const void* k;            // [B,Hkv,N,d]
+  const void* v;            // [B,Hkv,N,d]
+  void* out;                // [B,Hq,d]
+  float* spill;             // [B,Hq,N] scaled logits (anchor), or null
+  float* part;              // [B*Hq][S][d+4]: m (log2 units), l, -, -, o[d]
+  unsigned int* counters;   // [B*Hkv] split arrival counters (self-resetting)
+  unsigned int* err;        // workspace error word
+  const uint32_t* plan;     // union plan [B*Hkv][plan_stride]: key | mask << 24
+  const int32_t* plan_count;  // [B*Hkv]
+  const int32_t* idx;       // per-head sets [B,Hq,topk] (generic sparse path)
+  int plan_stride;          // G * topk
+  int topk;
+  int B, Hq, Hkv, N, G;
+  int S;                    // splits per (sequence, KV head)
+  int chunk;                // keys (dense) per split
+  float scale;              // sigma
+  float scale_log2;         // sigma * log2(e)
+  int16_t heads[kMaxQHeads];  // heads[g*G + slot] = query head of slot in group g
+};
+
+enum DecodeKind { kDense = 0, kAnchor = 1, kSparse = 2 };
+
+// decode.cu
+cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spill,
+                                     cudaStream_t st);
+cudaError_t launch_decode_union_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st);
+cudaError_t launch_build_union_plan(const DecodeArgs& a, uint32_t* plan, int32_t* plan_count,
+                                    cudaStream_t st);
+cudaError_t launch_decode_generic(const DecodeArgs& a, int head_dim, int dtype, DecodeKind kind,
+                                  cudaStream_t st);
+int decode_chunk_dense(int units, int N);        // keys per split (multiple of 64)
+int decode_splits_union(int units, int G, int topk);
+
+// topk.cu
+struct TopkArgs {
+  const float* scores;     // row r starts at scores + row offset (see below)
+  int32_t* idx_out;        // row r at idx_out + r * k_stride
+  unsigned int* err;
+  int rows;
+  int n;                   // plain rows: row length; tile rows: sequence length
+  int k;                   // requested k
+  int k_stride;
+  int prefill_tiles;       // 0: plain rows [rows, n]; >0: packed triangular tile rows
+  int tile;                // prefill tile (128)
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
+
+// prefill.cu
+struct PrefillArgs {
+  const void* q;        // [B,Hq,N,d]
+  const void* k;        // [B,Hkv,N,d]
+  const void* v;        // [B,Hkv,N,d]
+  void* out;            // [B,Hq,N,d]
+  float* lse;           // [B*Hq][N] log2-domain LSE of sigma*log2e*logits (anchor pass 1)
+  float* w;             // packed tile weights [B*Hq][sum_t L_t]
+  const int32_t* idx;   // [B,Hq,nT,topk] (reuse)
+  unsigned int* err;
+  int B, Hq, Hkv, N, G, topk, nT;
+  float scale, scale_log2;
+  int16_t head_kv[kMaxQHeads];   // KV head of each query head
+};
+cudaError_t launch_prefill_dense(const PrefillArgs& a, int head_dim, cudaStream_t st);
+cudaError_t launch_prefill_lse(const PrefillArgs& a, int head_dim, cudaStream_t st);
+cudaError_t launch_prefill_anchor_main(const PrefillArgs& a, int head_dim, cudaStream_t st);
+cudaError_t launch_prefill_reuse(const PrefillArgs& a, int head_dim, cudaStream_t st);
+
+// overlap.cu
+cudaError_t launch_layer_overlap(const int32_t* sets, int L, int units, int topk, int n_bits,
+                                 long long* counts, uint32_t* bitmaps, unsigned int* err,
+                                 cudaStream_t st);
+
+// Encoding of 2-D bf16 tensor maps (api.cu owns the driver entry point).
+bool encode_tmap_2d_bf16(void* tmap, const void* base, uint64_t inner, uint64_t outer,
+                         uint32_t box_inner, uint32_t box_outer, bool swizzle128);
+
+}  // namespace kascade
