@@ -1,0 +1,528 @@
+// api.cu — the C ABI of libkascade (include/kascade.h): argument validation,
+// workspace layout, kernel dispatch and the layer-stack driver.
+//
+// Stack semantics follow the Kascade pages (euno.news summary, Key
+// Contributions "Cross-layer Top-k reuse", Methodology 2-3): an anchor layer
+// computes exact attention and replaces the held index sets; a reuse layer
+// recomputes attention with its own q, K, V over the held sets. The sets
+// stay on the device for the whole stack.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "kascade.h"
+
+namespace kascade {
+
+// ------------------------------------------------------------ tensor maps --
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+}  // namespace
+
+bool encode_tmap_2d_bf16(void* tmap, const void* base, uint64_t inner, uint64_t outer,
+                         uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+  EncodeTiledFn enc = get_encode();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(reinterpret_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Validated shape plus the derived head tables.
+struct Shape {
+  int B, Hq, Hkv, d, N, G, dtype;
+  float scale;
+  int16_t heads[kMaxQHeads];     // heads[g*G + slot]
+  int16_t head_kv[kMaxQHeads];   // KV head of each query head
+};
+
+kascade_status check_desc(const kascade_desc* desc, Shape& s) {
+  if (desc == nullptr) return KASCADE_ERR_INVALID_ARG;
+  s.B = desc->batch;
+  s.Hq = desc->n_q_heads;
+  s.Hkv = desc->n_kv_heads;
+  s.d = desc->head_dim;
+  s.N = desc->kv_len;
+  s.dtype = desc->dtype;
+  if (s.B < 1 || s.Hkv < 1 || s.Hq < 1 || s.N < 1) return KASCADE_ERR_INVALID_ARG;
+  if (s.Hq % s.Hkv != 0 || s.Hq > kMaxQHeads) return KASCADE_ERR_INVALID_ARG;
+  if (s.dtype != KASCADE_F32 && s.dtype != KASCADE_BF16) return KASCADE_ERR_INVALID_ARG;
+  if (s.d != 64 && s.d != 128) return KASCADE_ERR_UNSUPPORTED;
+  s.G = s.Hq / s.Hkv;
+  if (s.G != 1 && s.G != 2 && s.G != 4 && s.G != 8) return KASCADE_ERR_UNSUPPORTED;
+  if (static_cast<long long>(s.B) * s.Hkv * s.N >= (1ll << 31)) return KASCADE_ERR_UNSUPPORTED;
+  if (s.N >= (1 << 24)) return KASCADE_ERR_UNSUPPORTED;
+  s.scale = desc->scale > 0.f ? desc->scale : 1.0f / sqrtf(static_cast<float>(s.d));
+  int fill[kMaxQHeads];
+  for (int g = 0; g < s.Hkv; ++g) fill[g] = 0;
+  for (int h = 0; h < s.Hq; ++h) {
+    const int g = desc->group_map ? desc->group_map[h] : h / s.G;
+    if (g < 0 || g >= s.Hkv) return KASCADE_ERR_INVALID_ARG;
+    if (fill[g] >= s.G) return KASCADE_ERR_INVALID_ARG;   // unbalanced map
+    s.heads[g * s.G + fill[g]++] = static_cast<int16_t>(h);
+    s.head_kv[h] = static_cast<int16_t>(g);
+  }
+  return KASCADE_OK;
+}
+
+inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Workspace layout; offsets in bytes from the workspace base.
+struct Layout {
+  size_t counters, part, spill, plan, plan_count;   // decode
+  size_t lse, w;                                    // prefill
+  size_t total;
+};
+
+Layout layout(const Shape& s, int topk, int mode) {
+  Layout L{};
+  size_t off = sizeof(WsHeader);
+  if (mode == KASCADE_DECODE) {
+    L.counters = off;
+    off = align256(off + static_cast<size_t>(s.B) * s.Hkv * 4);
+    L.part = off;
+    off = align256(off + static_cast<size_t>(s.B) * s.Hq * kMaxSplits * (s.d + 4) * 4);
+    L.spill = off;
+    off = align256(off + static_cast<size_t>(s.B) * s.Hq * s.N * 4);
+    L.plan = off;
+    off = align256(off + static_cast<size_t>(s.B) * s.Hq * topk * 4);
+    L.plan_count = off;
+    off = align256(off + static_cast<size_t>(s.B) * s.Hkv * 4);
+  } else {
+    const size_t nT = (s.N + 127) / 128;
+    const size_t per_bh = 64 * (nT - 1) * nT + s.N;
+    L.lse = off;
+    off = align256(off + static_cast<size_t>(s.B) * s.Hq * s.N * 4);
+    L.w = off;
+    off = align256(off + static_cast<size_t>(s.B) * s.Hq * per_bh * 4);
+  }
+  L.total = off;
+  return L;
+}
+
+kascade_status check_ws(const Shape& s, int topk, int mode, void* ws, size_t ws_bytes,
+                        Layout& L) {
+  L = layout(s, topk, mode);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) != 0) return KASCADE_ERR_WORKSPACE;
+  if (ws_bytes < L.total) return KASCADE_ERR_WORKSPACE;
+  return KASCADE_OK;
+}
+
+inline kascade_status cuda_status(cudaError_t e) {
+  return e == cudaSuccess ? KASCADE_OK : KASCADE_ERR_CUDA;
+}
+
+template <typename T>
+inline T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+void fill_decode_args(DecodeArgs& a, const Shape& s, const void* q, const void* k, const void* v,
+                      void* out, void* ws, const Layout& L, int topk) {
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.spill = at<float>(ws, L.spill);
+  a.part = at<float>(ws, L.part);
+  a.counters = at<unsigned int>(ws, L.counters);
+  a.err = at<unsigned int>(ws, 0);
+  a.plan = at<uint32_t>(ws, L.plan);
+  a.plan_count = at<int32_t>(ws, L.plan_count);
+  a.plan_stride = s.G * topk;
+  a.topk = topk;
+  a.B = s.B;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.N = s.N;
+  a.G = s.G;
+  a.scale = s.scale;
+  a.scale_log2 = s.scale * 1.4426950408889634f;
+  for (int i = 0; i < s.Hq; ++i) a.heads[i] = s.heads[i];
+}
+
+}  // namespace
+}  // namespace kascade
+
+// ------------------------------------------------------- decode dispatch --
+namespace kascade {
+namespace {
+
+kascade_status run_dense_decode(const Shape& s, const void* q, const void* k, const void* v,
+                                void* out, void* ws, const Layout& L, int topk, float* spill,
+                                cudaStream_t st) {
+  DecodeArgs a;
+  fill_decode_args(a, s, q, k, v, out, ws, L, topk);
+  if (spill != nullptr) a.spill = spill;
+  if (s.dtype == KASCADE_F32)
+    return cuda_status(launch_decode_generic(a, s.d, s.dtype, spill ? kAnchor : kDense, st));
+  a.chunk = decode_chunk_dense(s.B * s.Hkv, s.N);
+  a.S = (s.N + a.chunk - 1) / a.chunk;
+  return cuda_status(launch_decode_dense_bf16(a, s.d, spill != nullptr, st));
+}
+
+kascade_status run_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx,
+                             unsigned int* err, cudaStream_t st) {
+  TopkArgs t{};
+  t.scores = scores;
+  t.idx_out = idx;
+  t.err = err;
+  t.rows = rows;
+  t.n = n;
+  t.k = k;
+  t.k_stride = k;
+  t.prefill_tiles = 0;
+  t.tile = 128;
+  return cuda_status(launch_topk(t, st));
+}
+
+kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, const void* v,
+                                 int topk, void* out, int32_t* idx_out, float* scores_out,
+                                 void* ws, const Layout& L, cudaStream_t st) {
+  float* spill = scores_out ? scores_out : at<float>(ws, L.spill);
+  kascade_status r = run_dense_decode(s, q, k, v, out, ws, L, topk, spill, st);
+  if (r != KASCADE_OK) return r;
+  return run_topk_rows(spill, s.B * s.Hq, s.N, topk, idx_out, at<unsigned int>(ws, 0), st);
+}
+
+// Build the per-(sequence, KV head) union of the group's sets (bf16 path).
+kascade_status run_build_plan(const Shape& s, const int32_t* idx, int topk, void* ws,
+                              const Layout& L, cudaStream_t st) {
+  DecodeArgs a;
+  fill_decode_args(a, s, nullptr, nullptr, nullptr, nullptr, ws, L, topk);
+  a.idx = idx;
+  return cuda_status(
+      launch_build_union_plan(a, at<uint32_t>(ws, L.plan), at<int32_t>(ws, L.plan_count), st));
+}
+
+kascade_status run_reuse_decode(const Shape& s, const void* q, const void* k, const void* v,
+                                int topk, const int32_t* idx, void* out, void* ws,
+                                const Layout& L, bool plan_ready, cudaStream_t st) {
+  DecodeArgs a;
+  fill_decode_args(a, s, q, k, v, out, ws, L, topk);
+  a.idx = idx;
+  if (s.dtype == KASCADE_F32) return cuda_status(launch_decode_generic(a, s.d, s.dtype, kSparse, st));
+  if (!plan_ready) {
+    kascade_status r = run_build_plan(s, idx, topk, ws, L, st);
+    if (r != KASCADE_OK) return r;
+  }
+  a.S = decode_splits_union(s.B * s.Hkv, s.G, topk);
+  return cuda_status(launch_decode_union_bf16(a, s.d, st));
+}
+
+kascade_status check_decode_ptrs(const void* q, const void* k, const void* v, const void* out) {
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return KASCADE_ERR_INVALID_ARG;
+  return KASCADE_OK;
+}
+
+}  // namespace
+}  // namespace kascade
+
+using namespace kascade;
+
+extern "C" {
+
+const char* kascade_status_string(kascade_status s) {
+  switch (s) {
+    case KASCADE_OK: return "ok";
+    case KASCADE_ERR_INVALID_ARG: return "invalid argument";
+    case KASCADE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KASCADE_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case KASCADE_ERR_CUDA: return "CUDA error";
+    case KASCADE_ERR_BAD_INPUT: return "bad input detected on the device (NaN or index out of range)";
+    case KASCADE_ERR_TIMEOUT: return "bounded device wait expired";
+  }
+  return "unknown status";
+}
+
+size_t kascade_workspace_size(const kascade_desc* desc, int32_t topk, int32_t mode) {
+  Shape s;
+  if (check_desc(desc, s) != KASCADE_OK) return 0;
+  if (mode != KASCADE_DECODE && mode != KASCADE_PREFILL) return 0;
+  if (topk < 1) topk = 1;
+  return layout(s, topk, mode).total;
+}
+
+kascade_status kascade_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr || ws_bytes < sizeof(WsHeader)) return KASCADE_ERR_WORKSPACE;
+  return cuda_status(cudaMemsetAsync(ws, 0, ws_bytes, static_cast<cudaStream_t>(stream)));
+}
+
+kascade_status kascade_device_error(void* ws, void* stream) {
+  if (ws == nullptr) return KASCADE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KASCADE_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KASCADE_ERR_CUDA;
+  if (word != 0) {
+    const unsigned int zero[2] = {0u, 0u};
+    if (cudaMemcpy(ws, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return KASCADE_ERR_CUDA;
+  }
+  if (word & (1u << KASCADE_ERR_TIMEOUT)) return KASCADE_ERR_TIMEOUT;
+  if (word & (1u << KASCADE_ERR_BAD_INPUT)) return KASCADE_ERR_BAD_INPUT;
+  return KASCADE_OK;
+}
+
+kascade_status kascade_dense_decode(const kascade_desc* desc, const void* q, const void* k,
+                                    const void* v, void* out, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  Shape s;
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if ((r = check_decode_ptrs(q, k, v, out)) != KASCADE_OK) return r;
+  Layout L;
+  if ((r = check_ws(s, 1, KASCADE_DECODE, ws, ws_bytes, L)) != KASCADE_OK) return r;
+  return run_dense_decode(s, q, k, v, out, ws, L, 1, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+kascade_status kascade_anchor_decode(const kascade_desc* desc, const void* q, const void* k,
+                                     const void* v, int32_t topk, void* out, int32_t* idx_out,
+                                     float* scores_out, void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if ((r = check_decode_ptrs(q, k, v, out)) != KASCADE_OK) return r;
+  if (topk < 1 || topk > s.N || !aligned16(idx_out)) return KASCADE_ERR_INVALID_ARG;
+  if (scores_out != nullptr && !aligned16(scores_out)) return KASCADE_ERR_INVALID_ARG;
+  Layout L;
+  if ((r = check_ws(s, topk, KASCADE_DECODE, ws, ws_bytes, L)) != KASCADE_OK) return r;
+  return run_anchor_decode(s, q, k, v, topk, out, idx_out, scores_out, ws, L,
+                           static_cast<cudaStream_t>(stream));
+}
+
+kascade_status kascade_reuse_decode(const kascade_desc* desc, const void* q, const void* k,
+                                    const void* v, int32_t topk, const int32_t* idx, void* out,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if ((r = check_decode_ptrs(q, k, v, out)) != KASCADE_OK) return r;
+  if (topk < 1 || topk > s.N || !aligned16(idx)) return KASCADE_ERR_INVALID_ARG;
+  Layout L;
+  if ((r = check_ws(s, topk, KASCADE_DECODE, ws, ws_bytes, L)) != KASCADE_OK) return r;
+  return run_reuse_decode(s, q, k, v, topk, idx, out, ws, L, false,
+                          static_cast<cudaStream_t>(stream));
+}
+
+kascade_status kascade_topk(const float* scores, int32_t rows, int32_t n, int32_t k,
+                            int32_t* idx_out, void* ws, size_t ws_bytes, void* stream) {
+  if (rows < 0 || n < 1 || k < 1 || k > n) return KASCADE_ERR_INVALID_ARG;
+  if (rows > 0 && (scores == nullptr || idx_out == nullptr)) return KASCADE_ERR_INVALID_ARG;
+  if (ws == nullptr || ws_bytes < sizeof(WsHeader)) return KASCADE_ERR_WORKSPACE;
+  return run_topk_rows(scores, rows, n, k, idx_out, static_cast<unsigned int*>(ws),
+                       static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------ prefill dispatch --
+namespace kascade {
+namespace {
+
+inline kascade_status launch_status(cudaError_t e) {
+  if (e == cudaErrorNotSupported) return KASCADE_ERR_UNSUPPORTED;
+  return cuda_status(e);
+}
+
+void fill_prefill_args(PrefillArgs& a, const Shape& s, const void* q, const void* k,
+                       const void* v, void* out, void* ws, const Layout& L, int topk) {
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = at<float>(ws, L.lse);
+  a.w = at<float>(ws, L.w);
+  a.err = at<unsigned int>(ws, 0);
+  a.B = s.B;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.N = s.N;
+  a.G = s.G;
+  a.topk = topk;
+  a.nT = (s.N + 127) / 128;
+  a.scale = s.scale;
+  a.scale_log2 = s.scale * 1.4426950408889634f;
+  for (int h = 0; h < s.Hq; ++h) a.head_kv[h] = s.head_kv[h];
+}
+
+kascade_status run_dense_prefill(const Shape& s, const void* q, const void* k, const void* v,
+                                 void* out, void* ws, const Layout& L, cudaStream_t st) {
+  PrefillArgs a;
+  fill_prefill_args(a, s, q, k, v, out, ws, L, 1);
+  return launch_status(launch_prefill_dense(a, s.d, st));
+}
+
+kascade_status run_anchor_prefill(const Shape& s, const void* q, const void* k, const void* v,
+                                  int topk, void* out, int32_t* idx_out, void* ws,
+                                  const Layout& L, cudaStream_t st) {
+  PrefillArgs a;
+  fill_prefill_args(a, s, q, k, v, out, ws, L, topk);
+  kascade_status r = launch_status(launch_prefill_lse(a, s.d, st));
+  if (r != KASCADE_OK) return r;
+  if ((r = launch_status(launch_prefill_anchor_main(a, s.d, st))) != KASCADE_OK) return r;
+  TopkArgs t{};
+  t.scores = a.w;
+  t.idx_out = idx_out;
+  t.err = a.err;
+  t.rows = s.B * s.Hq * a.nT;
+  t.n = s.N;
+  t.k = topk;
+  t.k_stride = topk;
+  t.prefill_tiles = a.nT;
+  t.tile = 128;
+  return cuda_status(launch_topk(t, st));
+}
+
+kascade_status run_reuse_prefill(const Shape& s, const void* q, const void* k, const void* v,
+                                 int topk, const int32_t* idx, void* out, void* ws,
+                                 const Layout& L, cudaStream_t st) {
+  PrefillArgs a;
+  fill_prefill_args(a, s, q, k, v, out, ws, L, topk);
+  a.idx = idx;
+  return launch_status(launch_prefill_reuse(a, s.d, st));
+}
+
+kascade_status check_prefill(const kascade_desc* desc, Shape& s, const void* q, const void* k,
+                             const void* v, const void* out) {
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if (s.dtype != KASCADE_BF16) return KASCADE_ERR_UNSUPPORTED;
+  return check_decode_ptrs(q, k, v, out);
+}
+
+}  // namespace
+}  // namespace kascade
+
+extern "C" {
+
+kascade_status kascade_dense_prefill(const kascade_desc* desc, const void* q, const void* k,
+                                     const void* v, void* out, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  Shape s;
+  kascade_status r = check_prefill(desc, s, q, k, v, out);
+  if (r != KASCADE_OK) return r;
+  Layout L;
+  if ((r = check_ws(s, 1, KASCADE_PREFILL, ws, ws_bytes, L)) != KASCADE_OK) return r;
+  return run_dense_prefill(s, q, k, v, out, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+kascade_status kascade_anchor_prefill(const kascade_desc* desc, const void* q, const void* k,
+                                      const void* v, int32_t topk, void* out, int32_t* idx_out,
+                                      void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  kascade_status r = check_prefill(desc, s, q, k, v, out);
+  if (r != KASCADE_OK) return r;
+  if (topk < 1 || topk > s.N || !aligned16(idx_out)) return KASCADE_ERR_INVALID_ARG;
+  Layout L;
+  if ((r = check_ws(s, topk, KASCADE_PREFILL, ws, ws_bytes, L)) != KASCADE_OK) return r;
+  return run_anchor_prefill(s, q, k, v, topk, out, idx_out, ws, L,
+                            static_cast<cudaStream_t>(stream));
+}
+
+kascade_status kascade_reuse_prefill(const kascade_desc* desc, const void* q, const void* k,
+                                     const void* v, int32_t topk, const int32_t* idx, void* out,
+                                     void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  kascade_status r = check_prefill(desc, s, q, k, v, out);
+  if (r != KASCADE_OK) return r;
+  if (topk < 1 || topk > s.N || !aligned16(idx)) return KASCADE_ERR_INVALID_ARG;
+  Layout L;
+  if ((r = check_ws(s, topk, KASCADE_PREFILL, ws, ws_bytes, L)) != KASCADE_OK) return r;
+  return run_reuse_prefill(s, q, k, v, topk, idx, out, ws, L, static_cast<cudaStream_t>(stream));
+}
+
+kascade_status kascade_run_stack(const kascade_desc* desc, int32_t mode, int32_t n_layers,
+                                 const void* const* q, const void* const* k,
+                                 const void* const* v, int32_t topk, const int32_t* anchors,
+                                 int32_t n_anchors, void* const* out, int32_t* idx_buf,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  Shape s;
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if (mode != KASCADE_DECODE && mode != KASCADE_PREFILL) return KASCADE_ERR_INVALID_ARG;
+  if (mode == KASCADE_PREFILL && s.dtype != KASCADE_BF16) return KASCADE_ERR_UNSUPPORTED;
+  if (n_layers < 1 || q == nullptr || k == nullptr || v == nullptr || out == nullptr)
+    return KASCADE_ERR_INVALID_ARG;
+  if (n_anchors < 0 || (n_anchors > 0 && anchors == nullptr)) return KASCADE_ERR_INVALID_ARG;
+  for (int i = 0; i < n_anchors; ++i) {
+    if (anchors[i] < 0 || anchors[i] >= n_layers) return KASCADE_ERR_INVALID_ARG;
+    if (i > 0 && anchors[i] <= anchors[i - 1]) return KASCADE_ERR_INVALID_ARG;
+  }
+  if (n_anchors > 0 && (topk < 1 || topk > s.N || !aligned16(idx_buf)))
+    return KASCADE_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)
+    if ((r = check_decode_ptrs(q[l], k[l], v[l], out[l])) != KASCADE_OK) return r;
+  const int tk = topk < 1 ? 1 : topk;
+  Layout L;
+  if ((r = check_ws(s, tk, mode, ws, ws_bytes, L)) != KASCADE_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bool held = false;
+  int next = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    const bool is_anchor = next < n_anchors && anchors[next] == l;
+    if (is_anchor) ++next;
+    if (mode == KASCADE_DECODE) {
+      if (is_anchor) {
+        r = run_anchor_decode(s, q[l], k[l], v[l], tk, out[l], idx_buf, nullptr, ws, L, st);
+        if (r == KASCADE_OK && s.dtype == KASCADE_BF16) r = run_build_plan(s, idx_buf, tk, ws, L, st);
+        held = true;
+      } else if (held) {
+        r = run_reuse_decode(s, q[l], k[l], v[l], tk, idx_buf, out[l], ws, L, true, st);
+      } else {
+        r = run_dense_decode(s, q[l], k[l], v[l], out[l], ws, L, tk, nullptr, st);
+      }
+    } else {
+      if (is_anchor) {
+        r = run_anchor_prefill(s, q[l], k[l], v[l], tk, out[l], idx_buf, ws, L, st);
+        held = true;
+      } else if (held) {
+        r = run_reuse_prefill(s, q[l], k[l], v[l], tk, idx_buf, out[l], ws, L, st);
+      } else {
+        r = run_dense_prefill(s, q[l], k[l], v[l], out[l], ws, L, st);
+      }
+    }
+    if (r != KASCADE_OK) return r;
+  }
+  return KASCADE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,324 @@
+"""Python binding of libkascade (include/kascade.h).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels. PyTorch supplies device memory (outputs, the
+workspace) and the current CUDA stream. Importing this module loads
+``libkascade.so`` from this package directory and raises if it is missing;
+there is no fallback.
+"""
+import ctypes
+import math
+import os
+from typing import List, Optional, Sequence
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkascade.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("libkascade.so is not built; run python -m long_context_anchor_gb300.build "
+                      "(or __graft_entry__.build())")
+_lib = ctypes.CDLL(LIB_PATH)
+
+OK, INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA, BAD_INPUT, TIMEOUT = range(7)
+F32, BF16 = 0, 1
+DECODE, PREFILL = 0, 1
+TILE = 128
+
+
+class Desc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("kv_len", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("group_map", ctypes.POINTER(ctypes.c_int32))]
+
+
+_vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+_DP = ctypes.POINTER(Desc)
+_SIGS = {
+    "kascade_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kascade_workspace_size": (_sz, [_DP, _i32, _i32]),
+    "kascade_workspace_init": (ctypes.c_int, [_vp, _sz, _vp]),
+    "kascade_device_error": (ctypes.c_int, [_vp, _vp]),
+    "kascade_dense_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "kascade_anchor_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "kascade_reuse_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "kascade_topk": (ctypes.c_int, [_vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "kascade_dense_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "kascade_anchor_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "kascade_reuse_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "kascade_run_stack": (ctypes.c_int, [_DP, _i32, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                         ctypes.POINTER(_vp), _i32, ctypes.POINTER(_i32), _i32,
+                                         ctypes.POINTER(_vp), _vp, _vp, _sz, _vp]),
+    "kascade_overlap_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "kascade_layer_overlap": (ctypes.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "kascade_schedule_anchors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), _i32, _i32,
+                                                ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_double)]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+class KascadeError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__("%s: %s (status %d)" % (where, status_string(status), status))
+        self.status = status
+
+
+def status_string(s: int) -> str:
+    return _lib.kascade_status_string(int(s)).decode()
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise KascadeError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_desc(batch, n_q_heads, n_kv_heads, head_dim, kv_len, dtype, scale=0.0,
+              group_map: Optional[Sequence[int]] = None):
+    d = Desc(batch, n_q_heads, n_kv_heads, head_dim, kv_len, dtype,
+             float(scale or 0.0), None)
+    keep = None
+    if group_map is not None:
+        keep = (ctypes.c_int32 * n_q_heads)(*[int(x) for x in group_map])
+        d.group_map = ctypes.cast(keep, ctypes.POINTER(ctypes.c_int32))
+    d._keep = keep      # keep the host array alive with the descriptor
+    return d
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError("q/k/v must be bfloat16 or float32")
+
+
+def decode_desc(q, k, group_map=None, scale=None):
+    B, Hq, d = q.shape
+    _, Hkv, N, _ = k.shape
+    return make_desc(B, Hq, Hkv, d, N, _dtype_code(q), scale or 0.0, group_map)
+
+
+def prefill_desc(q, k, group_map=None, scale=None):
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    return make_desc(B, Hq, Hkv, d, N, _dtype_code(q), scale or 0.0, group_map)
+
+
+def workspace_size(desc, topk: int, mode: int) -> int:
+    n = _lib.kascade_workspace_size(ctypes.byref(desc), int(topk), int(mode))
+    if n == 0:
+        raise KascadeError(INVALID_ARG, "kascade_workspace_size")
+    return n
+
+
+class Workspace:
+    """Caller-owned device workspace (torch memory), zeroed once when (re)allocated."""
+
+    def __init__(self, device=None):
+        self.device = torch.device(device if device is not None else "cuda")
+        self.buf: Optional[torch.Tensor] = None
+
+    def get(self, nbytes: int, stream=None) -> torch.Tensor:
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+            _check(_lib.kascade_workspace_init(_ptr(self.buf), self.buf.numel(), _stream(stream)),
+                   "kascade_workspace_init")
+        return self.buf
+
+    def device_error(self, stream=None) -> int:
+        """Synchronise and read/clear the device error word (an int status)."""
+        if self.buf is None:
+            return OK
+        return _lib.kascade_device_error(_ptr(self.buf), _stream(stream))
+
+
+_default_ws = {}
+
+
+def default_workspace(device) -> Workspace:
+    dev = torch.device(device)
+    key = dev.index if dev.index is not None else torch.cuda.current_device()
+    if key not in _default_ws:
+        _default_ws[key] = Workspace(torch.device("cuda", key))
+    return _default_ws[key]
+
+
+def _ws(ws, device, nbytes, stream):
+    ws = ws if ws is not None else default_workspace(device)
+    buf = ws.get(nbytes, stream)
+    return ws, buf
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+# ------------------------------------------------------------------ decode --
+
+def dense_decode(q, k, v, group_map=None, scale=None, out=None, ws=None, stream=None):
+    """Exact decode attention: q [B,Hq,d], k/v [B,Hkv,N,d] -> out [B,Hq,d]."""
+    _contig(q, k, v)
+    desc = decode_desc(q, k, group_map, scale)
+    out = torch.empty_like(q) if out is None else out
+    ws, buf = _ws(ws, q.device, workspace_size(desc, 1, DECODE), stream)
+    _check(_lib.kascade_dense_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                     _ptr(buf), buf.numel(), _stream(stream)), "kascade_dense_decode")
+    return out
+
+
+def anchor_decode(q, k, v, topk, group_map=None, scale=None, return_scores=False, out=None,
+                  idx=None, ws=None, stream=None):
+    """Anchor layer: (out [B,Hq,d], idx [B,Hq,topk] int32[, scores [B,Hq,N] fp32])."""
+    _contig(q, k, v)
+    desc = decode_desc(q, k, group_map, scale)
+    B, Hq, _ = q.shape
+    N = k.shape[2]
+    out = torch.empty_like(q) if out is None else out
+    idx = torch.empty(B, Hq, topk, dtype=torch.int32, device=q.device) if idx is None else idx
+    scores = torch.empty(B, Hq, N, dtype=torch.float32, device=q.device) if return_scores else None
+    ws, buf = _ws(ws, q.device, workspace_size(desc, topk, DECODE), stream)
+    _check(_lib.kascade_anchor_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
+                                      _ptr(out), _ptr(idx), _ptr(scores), _ptr(buf), buf.numel(),
+                                      _stream(stream)), "kascade_anchor_decode")
+    return (out, idx, scores) if return_scores else (out, idx)
+
+
+def reuse_decode(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, stream=None):
+    """Reuse layer over saved sets idx [B,Hq,topk] (int32, ascending)."""
+    _contig(q, k, v, idx)
+    desc = decode_desc(q, k, group_map, scale)
+    topk = idx.shape[-1]
+    out = torch.empty_like(q) if out is None else out
+    ws, buf = _ws(ws, q.device, workspace_size(desc, topk, DECODE), stream)
+    _check(_lib.kascade_reuse_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
+                                     _ptr(idx), _ptr(out), _ptr(buf), buf.numel(), _stream(stream)),
+           "kascade_reuse_decode")
+    return out
+
+
+def topk(scores, k, out=None, ws=None, stream=None):
+    """Exact Top-k of fp32 rows [rows, n] -> int32 [rows, k] ascending."""
+    _contig(scores)
+    rows, n = scores.shape
+    out = torch.empty(rows, k, dtype=torch.int32, device=scores.device) if out is None else out
+    ws, buf = _ws(ws, scores.device, 256, stream)
+    _check(_lib.kascade_topk(_ptr(scores), rows, n, int(k), _ptr(out), _ptr(buf), buf.numel(),
+                             _stream(stream)), "kascade_topk")
+    return out
+
+
+# ----------------------------------------------------------------- prefill --
+
+def n_tiles(n: int) -> int:
+    return (n + TILE - 1) // TILE
+
+
+def dense_prefill(q, k, v, group_map=None, scale=None, out=None, ws=None, stream=None):
+    """Causal exact attention: q [B,Hq,N,d], k/v [B,Hkv,N,d] (bf16)."""
+    _contig(q, k, v)
+    desc = prefill_desc(q, k, group_map, scale)
+    out = torch.empty_like(q) if out is None else out
+    ws, buf = _ws(ws, q.device, workspace_size(desc, 1, PREFILL), stream)
+    _check(_lib.kascade_dense_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(out),
+                                      _ptr(buf), buf.numel(), _stream(stream)), "kascade_dense_prefill")
+    return out
+
+
+def anchor_prefill(q, k, v, topk, group_map=None, scale=None, out=None, idx=None, ws=None,
+                   stream=None):
+    """Anchor layer, prefill: (out, idx [B,Hq,nT,topk] int32, -1 padded)."""
+    _contig(q, k, v)
+    desc = prefill_desc(q, k, group_map, scale)
+    B, Hq, N, _ = q.shape
+    out = torch.empty_like(q) if out is None else out
+    if idx is None:
+        idx = torch.empty(B, Hq, n_tiles(N), topk, dtype=torch.int32, device=q.device)
+    ws, buf = _ws(ws, q.device, workspace_size(desc, topk, PREFILL), stream)
+    _check(_lib.kascade_anchor_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
+                                       _ptr(out), _ptr(idx), _ptr(buf), buf.numel(),
+                                       _stream(stream)), "kascade_anchor_prefill")
+    return out, idx
+
+
+def reuse_prefill(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, stream=None):
+    """Reuse layer, prefill, over saved tile sets idx [B,Hq,nT,topk]."""
+    _contig(q, k, v, idx)
+    desc = prefill_desc(q, k, group_map, scale)
+    topk = idx.shape[-1]
+    out = torch.empty_like(q) if out is None else out
+    ws, buf = _ws(ws, q.device, workspace_size(desc, topk, PREFILL), stream)
+    _check(_lib.kascade_reuse_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
+                                      _ptr(idx), _ptr(out), _ptr(buf), buf.numel(),
+                                      _stream(stream)), "kascade_reuse_prefill")
+    return out
+
+
+# ------------------------------------------------------------------- stack --
+
+def run_stack(mode, qs, ks, vs, topk, anchors, group_map=None, scale=None, outs=None,
+              idx_buf=None, ws=None, stream=None):
+    """Run a layer stack; returns (outs, idx_buf). mode: DECODE or PREFILL."""
+    L = len(qs)
+    _contig(*qs, *ks, *vs)
+    if mode == DECODE:
+        desc = decode_desc(qs[0], ks[0], group_map, scale)
+        B, Hq, _ = qs[0].shape
+        shape = (B, Hq, topk)
+    else:
+        desc = prefill_desc(qs[0], ks[0], group_map, scale)
+        B, Hq, N, _ = qs[0].shape
+        shape = (B, Hq, n_tiles(N), topk)
+    dev = qs[0].device
+    outs = [torch.empty_like(q) for q in qs] if outs is None else outs
+    if idx_buf is None:
+        idx_buf = torch.empty(shape, dtype=torch.int32, device=dev)
+    ws, buf = _ws(ws, dev, workspace_size(desc, topk, mode), stream)
+    arr = lambda ts: (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
+    an = (ctypes.c_int32 * max(1, len(anchors)))(*[int(a) for a in anchors])
+    _check(_lib.kascade_run_stack(ctypes.byref(desc), int(mode), L, arr(qs), arr(ks), arr(vs),
+                                  int(topk), an, len(anchors), arr(outs), _ptr(idx_buf),
+                                  _ptr(buf), buf.numel(), _stream(stream)), "kascade_run_stack")
+    return outs, idx_buf
+
+
+# -------------------------------------------------------------- scheduling --
+
+def layer_overlap(sets, n_bits, ws=None, stream=None):
+    """sets: int32 [L, units, topk] on the device -> int64 counts [L, L]."""
+    _contig(sets)
+    L, units, k = sets.shape
+    counts = torch.empty(L, L, dtype=torch.int64, device=sets.device)
+    nbytes = _lib.kascade_overlap_workspace_size(L, units, int(n_bits))
+    ws, buf = _ws(ws, sets.device, nbytes, stream)
+    _check(_lib.kascade_layer_overlap(_ptr(sets), L, units, k, int(n_bits), _ptr(counts),
+                                      _ptr(buf), buf.numel(), _stream(stream)), "kascade_layer_overlap")
+    return counts
+
+
+def schedule_anchors(sim, n_anchors: int):
+    """Host DP over a similarity matrix (sequence of rows); returns (anchors, objective)."""
+    L = len(sim)
+    flat = (ctypes.c_double * (L * L))(*[float(x) for row in sim for x in row])
+    out = (ctypes.c_int32 * n_anchors)()
+    obj = ctypes.c_double()
+    _check(_lib.kascade_schedule_anchors(flat, L, int(n_anchors), out, ctypes.byref(obj)),
+           "kascade_schedule_anchors")
+    return list(out), obj.value

@@ -1,0 +1,101 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; argument validation returns errors before any CUDA call; the host
+DP matches the oracle's DP. No GPU needed."""
+import re
+
+import numpy as np
+import pytest
+
+import __graft_entry__
+from oracle.schedule import schedule_anchors as oracle_dp
+
+HEADER = __graft_entry__.ROOT + "/include/kascade.h"
+
+
+@pytest.fixture(scope="module")
+def K():
+    __graft_entry__.build()
+    from long_context_anchor_gb300 import kascade
+    return kascade
+
+
+def test_exports_every_declared_symbol(K):
+    text = open(HEADER).read()
+    declared = set(re.findall(r"\b(kascade_[a-z_]+)\s*\(", text))
+    assert len(declared) >= 15
+    for name in declared:
+        assert hasattr(K._lib, name), name
+    assert declared == set(K.EXPORTED)
+
+
+def test_validation_before_launch(K):
+    ws_size = K._lib.kascade_workspace_size
+    good = K.make_desc(1, 4, 2, 64, 512, K.BF16)
+    assert K.workspace_size(good, 32, K.DECODE) > 0
+    for bad in [K.make_desc(1, 3, 2, 64, 512, K.BF16),     # Hq % Hkv
+                K.make_desc(0, 4, 2, 64, 512, K.BF16),     # batch
+                K.make_desc(1, 4, 2, 64, 0, K.BF16),       # N
+                K.make_desc(1, 4, 2, 64, 512, 7),          # dtype
+                K.make_desc(1, 4, 2, 64, 512, K.BF16, group_map=[0, 0, 0, 1]),  # unbalanced
+                K.make_desc(1, 4, 2, 64, 512, K.BF16, group_map=[0, 0, 1, 2])]:  # out of range
+        assert ws_size(bad, 32, 0) == 0
+    unsup = K.make_desc(1, 4, 2, 96, 512, K.BF16)
+    assert ws_size(unsup, 32, 0) == 0
+    fake = 1 << 20    # aligned non-null address; never dereferenced on these paths
+    import ctypes
+    p = ctypes.c_void_p(fake)
+    nws = K.workspace_size(good, 32, K.DECODE)
+    # topk out of range
+    assert K._lib.kascade_anchor_decode(ctypes.byref(good), p, p, p, 0, p, p, None, p, nws, None) == K.INVALID_ARG
+    assert K._lib.kascade_anchor_decode(ctypes.byref(good), p, p, p, 513, p, p, None, p, nws, None) == K.INVALID_ARG
+    # misaligned tensor
+    assert K._lib.kascade_dense_decode(ctypes.byref(good), ctypes.c_void_p(fake + 4), p, p, p, p, nws, None) == K.INVALID_ARG
+    # workspace too small / misaligned
+    assert K._lib.kascade_dense_decode(ctypes.byref(good), p, p, p, p, p, 100, None) == K.WORKSPACE
+    assert K._lib.kascade_dense_decode(ctypes.byref(good), p, p, p, p, ctypes.c_void_p(fake + 16), nws, None) == K.WORKSPACE
+    # prefill needs bf16
+    f32 = K.make_desc(1, 4, 2, 64, 512, K.F32)
+    assert K._lib.kascade_dense_prefill(ctypes.byref(f32), p, p, p, p, p, 1 << 30, None) == K.UNSUPPORTED
+    # stack: anchors must be ascending and in range
+    arr = (ctypes.c_void_p * 2)(fake, fake)
+    bad_anchors = (ctypes.c_int32 * 2)(1, 0)
+    assert K._lib.kascade_run_stack(ctypes.byref(good), 0, 2, arr, arr, arr, 32, bad_anchors, 2, arr, p, p, nws, None) == K.INVALID_ARG
+    out_of_range = (ctypes.c_int32 * 1)(2)
+    assert K._lib.kascade_run_stack(ctypes.byref(good), 0, 2, arr, arr, arr, 32, out_of_range, 1, arr, p, p, nws, None) == K.INVALID_ARG
+    assert K._lib.kascade_topk(p, 4, 10, 11, p, p, 256, None) == K.INVALID_ARG
+
+
+def test_status_strings(K):
+    for s in range(7):
+        assert len(K.status_string(s)) > 0
+
+
+def _sim(rng, L):
+    X = rng.random((L, L))
+    M = (X + X.T) / 2
+    np.fill_diagonal(M, 1.0)
+    return M
+
+
+@pytest.mark.parametrize("L,m", [(1, 1), (5, 2), (8, 3), (12, 12), (32, 6), (24, 8)])
+def test_host_dp_matches_oracle(K, L, m):
+    rng = np.random.default_rng(L * 100 + m)
+    for _ in range(4):
+        M = _sim(rng, L)
+        a, f = K.schedule_anchors(M.tolist(), m)
+        ao, fo = oracle_dp(M, m)
+        assert a == ao
+        assert abs(f - fo) < 1e-9
+
+
+def test_host_dp_ties_and_errors(K):
+    a, f = K.schedule_anchors(np.ones((6, 6)).tolist(), 3)
+    assert a == [0, 1, 2] and f == 6.0
+    L = 8
+    M = np.zeros((L, L))
+    M[:4, :4] = 0.9
+    M[4:, 4:] = 0.9
+    np.fill_diagonal(M, 1.0)
+    assert K.schedule_anchors(M.tolist(), 2)[0] == [0, 4]
+    with pytest.raises(K.KascadeError):
+        K.schedule_anchors(np.ones((3, 3)).tolist(), 4)
