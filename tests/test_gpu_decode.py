@@ -1,0 +1,230 @@
+"""GPU parity of the decode path (anchor decode + Top-k, reuse decode, dense
+decode, the stack driver) against the float64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+from long_context_anchor_gb300 import configs
+from long_context_anchor_gb300.workloads import make_layers, group_map as default_gmap
+from oracle import attention as A
+from oracle.topk import topk_indices
+from gpu_helpers import check_index_set, check_out, f64
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module")
+def K():
+    __graft_entry__.build()
+    from long_context_anchor_gb300 import kascade
+    return kascade
+
+
+def _rand_layer(B, Hq, Hkv, N, d, dtype, seed, scale_k=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Hq, d, generator=g)
+    k = torch.randn(B, Hkv, N, d, generator=g) * scale_k
+    v = torch.randn(B, Hkv, N, d, generator=g)
+    return [x.to(dtype).to(DEV) for x in (q, k, v)]
+
+
+# ------------------------------------------------------------------ top-k --
+
+def _topk_cases():
+    rng = np.random.default_rng(0)
+    cases = []
+    for n, k in [(7, 3), (512, 32), (1000, 999), (4096, 512), (32768, 4096), (40000, 5000),
+                 (131072, 8192)]:
+        rows = 6
+        x = rng.standard_normal((rows, n)).astype(np.float32)
+        x[1] = np.round(x[1] * 2) / 2                # heavy ties
+        x[2, ::3] = -0.0
+        x[2, 1::3] = 0.0
+        x[3, rng.random(n) < 0.2] = -np.inf
+        x[4] = 1.0                                   # all equal: candidate overflow path
+        cases.append((x, k))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(7))
+def test_topk_bit_exact_on_identical_scores(K, case):
+    x, k = _topk_cases()[case]
+    got = K.topk(torch.from_numpy(x).to(DEV), k).cpu().numpy()
+    for r in range(x.shape[0]):
+        assert got[r].tolist() == topk_indices(x[r], k).tolist(), (case, r)
+
+
+def test_topk_nan_reported(K):
+    ws = K.Workspace(DEV)
+    x = torch.randn(3, 1000, device=DEV)
+    x[1, 17] = float("nan")
+    K.topk(x, 10, ws=ws)
+    assert ws.device_error() == K.BAD_INPUT
+    K.topk(torch.randn(3, 1000, device=DEV), 10, ws=ws)
+    assert ws.device_error() == K.OK
+
+
+# ------------------------------------------------------------ anchor/dense --
+
+SHAPES = [  # B, Hq, Hkv, N, d, dtype
+    (1, 4, 2, 512, 64, torch.float32),
+    (1, 4, 2, 512, 64, torch.bfloat16),
+    (2, 8, 8, 1000, 128, torch.bfloat16),     # G = 1, ragged N
+    (2, 16, 2, 4097, 64, torch.bfloat16),     # G = 8, ragged tail over many tiles
+    (3, 8, 2, 3000, 128, torch.bfloat16),     # G = 4
+    (1, 4, 2, 70, 128, torch.bfloat16),       # shorter than one split
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_anchor_decode_matches_oracle(K, shape):
+    B, Hq, Hkv, N, d, dt = shape
+    q, k, v = _rand_layer(B, Hq, Hkv, N, d, dt, seed=N + Hq)
+    topk = max(1, N // 8)
+    out, idx, scores = K.anchor_decode(q, k, v, topk, return_scores=True)
+    o_ref, _, s_ref = A.anchor_decode(f64(q), f64(k), f64(v), topk)
+    tight = dt == torch.float32
+    check_out(out, o_ref, *( (1e-4, 1e-5) if tight else (2e-2, 2e-3)))
+    check_out(scores, s_ref, 1e-3, 1e-4, what="scores")
+    got = idx.cpu().numpy()
+    sc = scores.cpu().numpy()
+    for b in range(B):
+        for h in range(Hq):
+            check_index_set(got[b, h], s_ref[b, h], topk)
+            # bit-exact against the oracle rule on the kernel's own fp32 scores
+            assert got[b, h].tolist() == topk_indices(sc[b, h], topk).tolist()
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_dense_decode_matches_oracle_and_anchor(K, shape):
+    B, Hq, Hkv, N, d, dt = shape
+    q, k, v = _rand_layer(B, Hq, Hkv, N, d, dt, seed=3 * N + Hq)
+    out = K.dense_decode(q, k, v)
+    o_ref, _ = A.dense_decode(f64(q), f64(k), f64(v))
+    check_out(out, o_ref, *((1e-4, 1e-5) if dt == torch.float32 else (2e-2, 2e-3)))
+    out_a, _ = K.anchor_decode(q, k, v, max(1, N // 8))
+    assert torch.equal(out, out_a)
+
+
+def test_permuted_group_map(K):
+    gm = [1, 0, 3, 2, 0, 1, 2, 3]
+    q, k, v = _rand_layer(2, 8, 4, 777, 128, torch.bfloat16, seed=5)
+    out, idx, scores = K.anchor_decode(q, k, v, 50, group_map=gm, return_scores=True)
+    o_ref, _, s_ref = A.anchor_decode(f64(q), f64(k), f64(v), 50, gm)
+    check_out(out, o_ref)
+    out_r = K.reuse_decode(q, k, v, idx, group_map=gm)
+    check_out(out_r, A.sparse_decode(f64(q), f64(k), f64(v), idx.cpu().numpy(), gm))
+
+
+# ------------------------------------------------------------------- reuse --
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_reuse_decode_matches_oracle(K, shape):
+    B, Hq, Hkv, N, d, dt = shape
+    q, k, v = _rand_layer(B, Hq, Hkv, N, d, dt, seed=7 * N + Hq)
+    topk = max(1, N // 8)
+    _, idx = K.anchor_decode(q, k, v, topk)
+    q2, k2, v2 = _rand_layer(B, Hq, Hkv, N, d, dt, seed=11 * N + Hq)
+    out = K.reuse_decode(q2, k2, v2, idx)
+    o_ref = A.sparse_decode(f64(q2), f64(k2), f64(v2), idx.cpu().numpy())
+    check_out(out, o_ref, *((1e-4, 1e-5) if dt == torch.float32 else (2e-2, 2e-3)))
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
+def test_reuse_with_all_keys_equals_dense(K, dt):
+    q, k, v = _rand_layer(2, 8, 2, 640, 128 if dt == torch.bfloat16 else 64, dt, seed=9)
+    N = k.shape[2]
+    idx = torch.arange(N, dtype=torch.int32, device=DEV).expand(2, 8, N).contiguous()
+    out_r = K.reuse_decode(q, k, v, idx)
+    out_d = K.dense_decode(q, k, v)
+    tol = 1e-5 if dt == torch.float32 else 1e-2
+    assert (out_r.float() - out_d.float()).abs().max().item() <= tol
+
+
+def test_reuse_poison_unselected_rows(K):
+    B, Hq, Hkv, N, d = 2, 8, 2, 2048, 128
+    q, k, v = _rand_layer(B, Hq, Hkv, N, d, torch.bfloat16, seed=13)
+    _, idx = K.anchor_decode(q, k, v, 200)
+    out = K.reuse_decode(q, k, v, idx)
+    used = torch.zeros(B, Hkv, N, dtype=torch.bool, device=DEV)
+    gm = default_gmap(Hq, Hkv)
+    for h in range(Hq):
+        used[:, gm[h]].scatter_(1, idx[:, h].long(), True)
+    kp, vp = k.clone(), v.clone()
+    kp[~used] = float("nan")
+    vp[~used] = float("nan")
+    out_p = K.reuse_decode(q, kp, vp, idx)
+    assert torch.equal(out, out_p)
+    # a selected row does change the output
+    j = int(idx[0, 0, 0])
+    vp2 = v.clone()
+    vp2[0, 0, j] += 4.0
+    assert not torch.equal(K.reuse_decode(q, k, vp2, idx)[0, 0], out[0, 0])
+
+
+def test_reuse_bad_index_reported(K):
+    ws = K.Workspace(DEV)
+    q, k, v = _rand_layer(1, 4, 2, 256, 64, torch.bfloat16, seed=1)
+    idx = torch.arange(16, dtype=torch.int32, device=DEV).expand(1, 4, 16).contiguous()
+    idx[0, 1, 3] = 999
+    K.reuse_decode(q, k, v, idx, ws=ws)
+    assert ws.device_error() == K.BAD_INPUT
+
+
+# ------------------------------------------------------------------- stack --
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_stack_matches_layer_calls_and_oracle(K, dtype):
+    w = configs.TINY_DECODE.with_(dtype=dtype, n_layers=5, anchors=(1, 3))
+    qs, ks, vs = make_layers(w)
+    dq, dk, dv = ([x.to(DEV) for x in xs] for xs in (qs, ks, vs))
+    outs, idx_buf = K.run_stack(K.DECODE, dq, dk, dv, w.topk, list(w.anchors))
+    # layer by layer through the single-layer entry points
+    o0 = K.dense_decode(dq[0], dk[0], dv[0])
+    o1, i1 = K.anchor_decode(dq[1], dk[1], dv[1], w.topk)
+    o2 = K.reuse_decode(dq[2], dk[2], dv[2], i1)
+    o3, i3 = K.anchor_decode(dq[3], dk[3], dv[3], w.topk)
+    o4 = K.reuse_decode(dq[4], dk[4], dv[4], i3)
+    for a, b in zip(outs, [o0, o1, o2, o3, o4]):
+        assert torch.equal(a, b)
+    assert torch.equal(idx_buf, i3)
+    # against the oracle stack, with reuse layers fed the kernel's own sets
+    f = lambda t: f64(t)
+    check_out(outs[0], A.dense_decode(f(qs[0]), f(ks[0]), f(vs[0]))[0])
+    check_out(outs[2], A.sparse_decode(f(qs[2]), f(ks[2]), f(vs[2]), i1.cpu().numpy()))
+    check_out(outs[4], A.sparse_decode(f(qs[4]), f(ks[4]), f(vs[4]), i3.cpu().numpy()))
+
+
+# -------------------------------------------------------- full-size samples --
+
+@pytest.mark.parametrize("cfg", ["llama8b", "gptoss"])
+def test_full_size_decode_sampled(K, cfg):
+    w = configs.LLAMA8B_DECODE_32K if cfg == "llama8b" else configs.GPTOSS_DECODE_128K
+    w = w.with_(n_layers=2)
+    qs, ks, vs = make_layers(w, device=DEV)
+    outs, idx = K.run_stack(K.DECODE, qs, ks, vs, w.topk, [0])
+    torch.cuda.synchronize()
+    gm = default_gmap(w.n_q_heads, w.n_kv_heads)
+    scale = 1.0 / np.sqrt(w.head_dim)
+    rng = np.random.default_rng(1)
+    units = [(0, 0), (w.batch - 1, w.n_q_heads - 1)] + \
+        [(int(rng.integers(w.batch)), int(rng.integers(w.n_q_heads))) for _ in range(6)]
+    idx_np = idx.cpu().numpy()
+    errs0, errs1 = [], []
+    for b, h in units:
+        g = gm[h]
+        K0, V0 = f64(ks[0][b, g]), f64(vs[0][b, g])
+        q0 = f64(qs[0][b, h])
+        s = scale * (K0 @ q0)
+        p = np.exp(s - s.max())
+        o_ref = (p / p.sum()) @ V0
+        errs0.append(np.abs(f64(outs[0][b, h]) - o_ref).max())
+        check_index_set(idx_np[b, h], s, w.topk)
+        sel = idx_np[b, h].astype(np.int64)
+        K1, V1 = f64(ks[1][b, g])[sel], f64(vs[1][b, g])[sel]
+        s1 = scale * (K1 @ f64(qs[1][b, h]))
+        p1 = np.exp(s1 - s1.max())
+        errs1.append(np.abs(f64(outs[1][b, h]) - (p1 / p1.sum()) @ V1).max())
+    assert max(errs0) < 2e-2 and max(errs1) < 2e-2, (max(errs0), max(errs1))
