@@ -1,0 +1,453 @@
+#!/usr/bin/env python
+"""Benchmark: Kascade decode attention on the Llama-3.1-8B attention shape.
+
+Workload (one step = one pass of the whole decode stack): 32 layers, batch 8,
+32 query / 8 KV heads, head_dim 128, bf16, KV cache N = 32768 per sequence,
+one query per sequence, Top-k k = 4096, anchors {0, 4, ..., 28}; seeded
+synthetic inputs (planted heavy keys, attention sink, cross-layer
+correlation 0.9). Each layer's K/V (1.07 GB) is distinct and far larger than
+L2, so no flush is needed between layers or steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0). `value` is decode attention time per layer in
+microseconds (lower is better) for the Kascade stack; the same line carries
+the library's own dense-attention stack on the same inputs, HBM GB/s, the
+roofline of the dominant kernel, an end-to-end number through the public API
+with host buffers, and the CPU oracle timed on the host cores.
+``--impl reference`` times the CPU oracle itself on a bounded sample.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn µs/layer + HBM GB/s at 32K ctx; prefill attn TFLOP/s; vs own dense"
+UNIT = "us/layer"
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i] == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------- CPU oracle leg --
+
+def _oracle_group(task):
+    """One (sequence, KV head) group of one layer through the float64 oracle.
+
+    task = (kind, q [G,d], K [N,d], V [N,d], idx [G,k] or None, k, scale).
+    Runs in a spawned worker with single-threaded BLAS.
+    """
+    import numpy as np
+    from oracle import attention as A
+    kind, q, Kg, Vg, idx, k, scale = task
+    t0 = time.perf_counter()
+    G = q.shape[0]
+    qd = q[None].astype(np.float64)                    # [1, G, d]
+    Kd = Kg[None, None].astype(np.float64)             # [1, 1, N, d]
+    Vd = Vg[None, None].astype(np.float64)
+    gm = [0] * G
+    if kind == "anchor":
+        A.anchor_decode(qd, Kd, Vd, k, gm, scale)
+    else:
+        A.sparse_decode(qd, Kd, Vd, idx[None], gm, scale)
+    return time.perf_counter() - t0
+
+
+def oracle_sample_tasks(w, layers_dev, n_groups, seed=0):
+    """Host copies of n_groups (sequence, KV head) groups of layer 0 (anchor) and
+    layer 1 (reuse, using the oracle's own layer-0 sets computed in the worker
+    order). Returns (anchor_tasks, reuse_tasks)."""
+    import numpy as np
+    import torch
+    from oracle.topk import topk_indices
+    (q0, k0, v0), (q1, k1, v1) = layers_dev
+    rng = np.random.default_rng(seed)
+    G = w.n_q_heads // w.n_kv_heads
+    scale = 1.0 / np.sqrt(w.head_dim)
+    units = [(int(rng.integers(w.batch)), int(rng.integers(w.n_kv_heads))) for _ in range(n_groups)]
+    f32 = lambda t: t.float().cpu().numpy()
+    at, rt = [], []
+    for b, g in units:
+        hs = list(range(g * G, (g + 1) * G))
+        qa, Ka, Va = f32(q0[b, hs]), f32(k0[b, g]), f32(v0[b, g])
+        at.append(("anchor", qa, Ka, Va, None, w.topk, scale))
+        # sets for the reuse task: oracle Top-k of this group's layer-0 logits
+        s = scale * (Ka.astype(np.float64) @ qa.astype(np.float64).T)   # [N, G]
+        idx = np.stack([topk_indices(s[:, i], w.topk) for i in range(G)])
+        rt.append(("reuse", f32(q1[b, hs]), f32(k1[b, g]), f32(v1[b, g]), idx, w.topk, scale))
+    return at, rt
+
+
+def time_oracle(w, layers_dev, n_groups, reps=1):
+    """Wall time of the oracle on the sample, extrapolated to microseconds per
+    layer of the stack (anchor/reuse mix of the schedule). Returns a dict."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    at, rt = oracle_sample_tasks(w, layers_dev, n_groups)
+    cores = os.cpu_count() or 1
+    old = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in old:
+        os.environ[k] = "1"
+    try:
+        with ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as ex:
+            list(ex.map(_oracle_group, at[:1]))           # start the workers
+            ta, tr = [], []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                list(ex.map(_oracle_group, at))
+                ta.append(time.perf_counter() - t0)
+                t0 = time.perf_counter()
+                list(ex.map(_oracle_group, rt))
+                tr.append(time.perf_counter() - t0)
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    groups_per_layer = w.batch * w.n_kv_heads
+    n_anchor = len(w.anchors)
+    n_reuse = w.n_layers - n_anchor
+    per_a = statistics.median(ta) * groups_per_layer / n_groups
+    per_r = statistics.median(tr) * groups_per_layer / n_groups
+    us = 1e6 * (n_anchor * per_a + n_reuse * per_r) / w.n_layers
+    return {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d of %d (sequence, KV head) groups of one anchor layer and one reuse "
+                      "layer (float64 numpy, one process per core, single-threaded BLAS); "
+                      "extrapolated to the %d-anchor / %d-reuse stack" %
+                      (n_groups, groups_per_layer, n_anchor, n_reuse),
+            "anchor_layer_s": per_a, "reuse_layer_s": per_r}
+
+
+# --------------------------------------------------------------- GPU legs --
+
+def decode_bytes(w, union_rows_per_anchor):
+    """Algorithmic HBM bytes per layer kind (bf16 K/V rows of 2*d bytes each).
+
+    dense  : every K and V row once + q read + out write;
+    anchor : dense + fp32 logits spill written and read back by the Top-k
+             + int32 index sets written (+ read once to build the union plan);
+    reuse  : K and V rows of the union of the group's sets, once each, + one
+             4-byte plan entry per union row + q + out.
+    """
+    d, B, Hq, Hkv, N, k = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads, w.kv_len, w.topk
+    qo = 2 * B * Hq * d * 2
+    dense = B * Hkv * N * 2 * d * 2 + qo
+    reuse = [u * (2 * d * 2 + 4) + qo for u in union_rows_per_anchor]
+    anchor = [dense + 2 * B * Hq * N * 4 + 2 * B * Hq * k * 4 + 4 * u for u in union_rows_per_anchor]
+    return dense, anchor, reuse
+
+
+def union_rows(idx, w):
+    """Rows of the per-(sequence, KV head) union of the group's index sets."""
+    import torch
+    B, Hq, k = idx.shape
+    G = w.n_q_heads // w.n_kv_heads
+    mark = torch.zeros(B, w.n_kv_heads, w.kv_len, dtype=torch.bool, device=idx.device)
+    for h in range(Hq):
+        mark[:, h // G].scatter_(1, idx[:, h].long(), True)
+    return int(mark.sum().item())
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from long_context_anchor_gb300 import configs
+    from long_context_anchor_gb300 import kascade as K
+    from long_context_anchor_gb300.workloads import layers as gen_layers
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    w = configs.LLAMA8B_DECODE_32K
+    L, B, Hq, Hkv, N, d = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.kv_len, w.head_dim
+    # Inputs resident in HBM, stacked so a step's host copies are single transfers.
+    q_all = torch.empty(L, B, Hq, d, dtype=torch.bfloat16, device=dev)
+    k_all = torch.empty(L, B, Hkv, N, d, dtype=torch.bfloat16, device=dev)
+    v_all = torch.empty(L, B, Hkv, N, d, dtype=torch.bfloat16, device=dev)
+    keep01 = []
+    for l, (q, k, v) in enumerate(gen_layers(w, device=dev)):
+        q_all[l].copy_(q)
+        k_all[l].copy_(k)
+        v_all[l].copy_(v)
+        del q, k, v
+    qs, ks, vs = list(q_all), list(k_all), list(v_all)
+    out_all = torch.empty_like(q_all)
+    outs = list(out_all)
+    anchors = list(w.anchors)
+    idx_buf = torch.empty(B, Hq, w.topk, dtype=torch.int32, device=dev)
+    ws = K.Workspace(dev)
+    stream = torch.cuda.current_stream()
+
+    def stack(anch, events=None):
+        K.run_stack(K.DECODE, qs, ks, vs, w.topk, anch, outs=outs, idx_buf=idx_buf, ws=ws,
+                    layer_events=events)
+
+    def timed(anch, steps):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(steps)]
+        for row in evs:
+            for e in row:
+                e.record(stream)        # materialise the event handles
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for s in range(steps):
+            evs[s][0].record(stream)
+            stack(anch, evs[s][1:])
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        total = t0.elapsed_time(t1)
+        per_layer = [[evs[s][l].elapsed_time(evs[s][l + 1]) for l in range(L)] for s in range(steps)]
+        return total, per_layer
+
+    for _ in range(args.warmup):
+        stack(anchors)
+        stack([])
+    torch.cuda.synchronize()
+    assert ws.device_error() == K.OK
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    total_k, pl_k = timed(anchors, args.steps)
+    total_d, pl_d = timed([], args.steps)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([total_k, total_d], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_k, total_d = t.tolist()
+
+    ms_step = total_k / args.steps
+    ms_dense = total_d / args.steps
+    anchor_ms = statistics.mean(pl_k[s][l] for s in range(args.steps) for l in anchors)
+    reuse_layers = [l for l in range(L) if l not in anchors]
+    reuse_ms = statistics.mean(pl_k[s][l] for s in range(args.steps) for l in reuse_layers)
+
+    # Byte accounting from each anchor's own sets (outside the timed region).
+    unions = []
+    for a in anchors:
+        _, ia = K.anchor_decode(qs[a], ks[a], vs[a], w.topk, ws=ws)
+        unions.append(union_rows(ia, w))
+    dense_b, anchor_b, reuse_b = decode_bytes(w, unions)
+    seg_reuse = []
+    for i, a in enumerate(anchors):
+        nxt = anchors[i + 1] if i + 1 < len(anchors) else L
+        seg_reuse += [reuse_b[i]] * (nxt - a - 1)
+    reuse_bytes_mean = statistics.mean(seg_reuse)
+    anchor_bytes_mean = statistics.mean(anchor_b)
+    hbm_peak, tf_peak, peak_src = load_peaks()
+    reuse_gbs = reuse_bytes_mean / (reuse_ms * 1e-3) / 1e9
+    anchor_gbs = anchor_bytes_mean / (anchor_ms * 1e-3) / 1e9
+    dense_gbs = dense_b / (ms_dense / L * 1e-3) / 1e9
+    stack_bytes = sum(anchor_b) + sum(seg_reuse)
+    launches_per_step = 3 * len(anchors) + len(reuse_layers)
+
+    result = {
+        "metric": METRIC, "value": round(1e3 * ms_step / L, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "layers": L, "batch": B, "q_heads": Hq, "kv_heads": Hkv,
+                   "head_dim": d, "kv_len": N, "topk": w.topk, "anchors": anchors,
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "no flush: each layer's K/V (1.07 GB) is distinct and exceeds L2"},
+        "decode": {"kascade_us_per_layer": round(1e3 * ms_step / L, 3),
+                   "anchor_layer_us": round(1e3 * anchor_ms, 3),
+                   "reuse_layer_us": round(1e3 * reuse_ms, 3),
+                   "dense_us_per_layer": round(1e3 * ms_dense / L, 3),
+                   "speedup_vs_own_dense": round(ms_dense / ms_step, 3),
+                   "stack_hbm_gbs": round(stack_bytes / (ms_step * 1e-3) / 1e9, 1),
+                   "reuse_hbm_gbs": round(reuse_gbs, 1), "anchor_hbm_gbs": round(anchor_gbs, 1),
+                   "dense_hbm_gbs": round(dense_gbs, 1),
+                   "reuse_union_rows_per_layer": int(statistics.mean(unions)),
+                   "reuse_bytes_per_layer": int(reuse_bytes_mean),
+                   "anchor_bytes_per_layer": int(anchor_bytes_mean),
+                   "dense_bytes_per_layer": int(dense_b),
+                   "peak_hbm_gbs": hbm_peak, "peak_source": peak_src},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    # Dominant kernel: the reuse-layer union-gather kernel (one launch per
+    # reuse layer) or the anchor layer, whichever holds more of the step.
+    if len(reuse_layers) * reuse_ms >= len(anchors) * anchor_ms:
+        result["roofline"] = {"kernel": "k_decode_union_bf16 (reuse layer)", "bound": "hbm",
+                              "achieved": round(reuse_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                              "frac": round(reuse_gbs / hbm_peak, 4), "traffic": None,
+                              "algorithmic_bytes": int(reuse_bytes_mean),
+                              "peak_source": peak_src}
+    else:
+        result["roofline"] = {"kernel": "anchor layer (k_decode_dense_bf16 + k_topk + plan)",
+                              "bound": "hbm", "achieved": round(anchor_gbs, 1), "peak": hbm_peak,
+                              "unit": "GB/s", "frac": round(anchor_gbs / hbm_peak, 4),
+                              "traffic": None, "algorithmic_bytes": int(anchor_bytes_mean),
+                              "peak_source": peak_src}
+
+    # End to end through the public API with host buffers: each step copies
+    # every layer's new query and the newest K/V row (position N-1) from
+    # pinned host memory, runs the stack and reads all outputs back.
+    q_host = q_all.cpu().pin_memory()
+    knew_host = k_all[:, :, :, N - 1].cpu().pin_memory()
+    vnew_host = v_all[:, :, :, N - 1].cpu().pin_memory()
+    out_host = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
+
+    def e2e_step():
+        q_all.copy_(q_host, non_blocking=True)
+        k_all[:, :, :, N - 1].copy_(knew_host, non_blocking=True)
+        v_all[:, :, :, N - 1].copy_(vnew_host, non_blocking=True)
+        stack(anchors)
+        out_host.copy_(out_all, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = t.item()
+    result["e2e"] = {"value": round(1e3 * e2e_ms / L, 3), "unit": UNIT,
+                     "h2d_bytes_per_step": int(q_host.numel() * 2 + 2 * knew_host.numel() * 2),
+                     "d2h_bytes_per_step": int(out_host.numel() * 2)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
+        result["cpu_baseline"] = time_oracle(w, lay01, n_groups=os.cpu_count() or 1, reps=2)
+    if world > 1:
+        dist.destroy_process_group()
+    return result if rank == 0 else None
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm, on a bounded sample per step."""
+    import torch
+    from long_context_anchor_gb300 import configs
+    from long_context_anchor_gb300.workloads import make_layers
+    rank, world, local = dist_env()
+    if rank != 0:
+        return None
+    w = configs.LLAMA8B_DECODE_32K
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    qs, ks, vs = make_layers(w.with_(n_layers=2), device=dev)
+    lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
+    n = os.cpu_count() or 1
+    for _ in range(args.warmup):
+        time_oracle(w, lay01, n_groups=n, reps=1)
+    vals = [time_oracle(w, lay01, n_groups=n, reps=1) for _ in range(args.steps)]
+    us = statistics.mean(v["value"] for v in vals)
+    cb = dict(vals[0])
+    cb["value"] = us
+    return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(us * w.n_layers / 1e3, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "layers": w.n_layers, "batch": w.batch,
+                       "kv_len": w.kv_len, "topk": w.topk, "anchors": list(w.anchors)},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -166,6 +166,17 @@ kascade_status kascade_run_stack(const kascade_desc* desc, int32_t mode, int32_t
                                  int32_t n_anchors, void* const* out, int32_t* idx_buf,
                                  void* ws, size_t ws_bytes, void* stream);
 
+/* kascade_run_stack, additionally recording layer_events[l] (a cudaEvent_t,
+ * or NULL to skip) on `stream` after the launches of layer l; for per-layer
+ * timing. layer_events: host array [n_layers] or NULL. */
+kascade_status kascade_run_stack_profiled(const kascade_desc* desc, int32_t mode,
+                                          int32_t n_layers, const void* const* q,
+                                          const void* const* k, const void* const* v,
+                                          int32_t topk, const int32_t* anchors,
+                                          int32_t n_anchors, void* const* out, int32_t* idx_buf,
+                                          void* ws, size_t ws_bytes, void* stream,
+                                          void* const* layer_events);
+
 /* ------------------------------------------------------------ scheduling -- */
 
 /* Cross-layer Top-k overlap for the anchor DP (Methodology 4). sets: device

@@ -470,11 +470,13 @@ kascade_status kascade_reuse_prefill(const kascade_desc* desc, const void* q, co
   return run_reuse_prefill(s, q, k, v, topk, idx, out, ws, L, static_cast<cudaStream_t>(stream));
 }
 
-kascade_status kascade_run_stack(const kascade_desc* desc, int32_t mode, int32_t n_layers,
-                                 const void* const* q, const void* const* k,
-                                 const void* const* v, int32_t topk, const int32_t* anchors,
-                                 int32_t n_anchors, void* const* out, int32_t* idx_buf,
-                                 void* ws, size_t ws_bytes, void* stream) {
+kascade_status kascade_run_stack_profiled(const kascade_desc* desc, int32_t mode,
+                                          int32_t n_layers, const void* const* q,
+                                          const void* const* k, const void* const* v,
+                                          int32_t topk, const int32_t* anchors,
+                                          int32_t n_anchors, void* const* out, int32_t* idx_buf,
+                                          void* ws, size_t ws_bytes, void* stream,
+                                          void* const* layer_events) {
   Shape s;
   kascade_status r = check_desc(desc, s);
   if (r != KASCADE_OK) return r;
@@ -521,8 +523,20 @@ kascade_status kascade_run_stack(const kascade_desc* desc, int32_t mode, int32_t
       }
     }
     if (r != KASCADE_OK) return r;
+    if (layer_events != nullptr && layer_events[l] != nullptr &&
+        cudaEventRecord(static_cast<cudaEvent_t>(layer_events[l]), st) != cudaSuccess)
+      return KASCADE_ERR_CUDA;
   }
   return KASCADE_OK;
+}
+
+kascade_status kascade_run_stack(const kascade_desc* desc, int32_t mode, int32_t n_layers,
+                                 const void* const* q, const void* const* k,
+                                 const void* const* v, int32_t topk, const int32_t* anchors,
+                                 int32_t n_anchors, void* const* out, int32_t* idx_buf,
+                                 void* ws, size_t ws_bytes, void* stream) {
+  return kascade_run_stack_profiled(desc, mode, n_layers, q, k, v, topk, anchors, n_anchors,
+                                    out, idx_buf, ws, ws_bytes, stream, nullptr);
 }
 
 }  // extern "C"

@@ -51,6 +51,10 @@ _SIGS = {
     "kascade_run_stack": (ctypes.c_int, [_DP, _i32, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                          ctypes.POINTER(_vp), _i32, ctypes.POINTER(_i32), _i32,
                                          ctypes.POINTER(_vp), _vp, _vp, _sz, _vp]),
+    "kascade_run_stack_profiled": (ctypes.c_int, [_DP, _i32, _i32, ctypes.POINTER(_vp),
+                                                  ctypes.POINTER(_vp), ctypes.POINTER(_vp), _i32,
+                                                  ctypes.POINTER(_i32), _i32, ctypes.POINTER(_vp),
+                                                  _vp, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
     "kascade_overlap_workspace_size": (_sz, [_i32, _i32, _i32]),
     "kascade_layer_overlap": (ctypes.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "kascade_schedule_anchors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), _i32, _i32,
@@ -274,8 +278,11 @@ def reuse_prefill(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, s
 # ------------------------------------------------------------------- stack --
 
 def run_stack(mode, qs, ks, vs, topk, anchors, group_map=None, scale=None, outs=None,
-              idx_buf=None, ws=None, stream=None):
-    """Run a layer stack; returns (outs, idx_buf). mode: DECODE or PREFILL."""
+              idx_buf=None, ws=None, stream=None, layer_events=None):
+    """Run a layer stack; returns (outs, idx_buf). mode: DECODE or PREFILL.
+
+    layer_events: optional list of torch.cuda.Event (timing enabled), one per
+    layer, recorded on the stream after that layer's launches."""
     L = len(qs)
     _contig(*qs, *ks, *vs)
     if mode == DECODE:
@@ -293,9 +300,16 @@ def run_stack(mode, qs, ks, vs, topk, anchors, group_map=None, scale=None, outs=
     ws, buf = _ws(ws, dev, workspace_size(desc, topk, mode), stream)
     arr = lambda ts: (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
     an = (ctypes.c_int32 * max(1, len(anchors)))(*[int(a) for a in anchors])
-    _check(_lib.kascade_run_stack(ctypes.byref(desc), int(mode), L, arr(qs), arr(ks), arr(vs),
-                                  int(topk), an, len(anchors), arr(outs), _ptr(idx_buf),
-                                  _ptr(buf), buf.numel(), _stream(stream)), "kascade_run_stack")
+    if layer_events is None:
+        _check(_lib.kascade_run_stack(ctypes.byref(desc), int(mode), L, arr(qs), arr(ks), arr(vs),
+                                      int(topk), an, len(anchors), arr(outs), _ptr(idx_buf),
+                                      _ptr(buf), buf.numel(), _stream(stream)), "kascade_run_stack")
+    else:
+        ev = (ctypes.c_void_p * L)(*[e.cuda_event for e in layer_events])
+        _check(_lib.kascade_run_stack_profiled(ctypes.byref(desc), int(mode), L, arr(qs), arr(ks),
+                                               arr(vs), int(topk), an, len(anchors), arr(outs),
+                                               _ptr(idx_buf), _ptr(buf), buf.numel(),
+                                               _stream(stream), ev), "kascade_run_stack_profiled")
     return outs, idx_buf
 
 
