@@ -130,6 +130,20 @@ kascade_status kascade_reuse_decode(const kascade_desc* desc, const void* q, con
 kascade_status kascade_topk(const float* scores, int32_t rows, int32_t n, int32_t k,
                             int32_t* idx_out, void* ws, size_t ws_bytes, void* stream);
 
+/* Dense decode (as kascade_dense_decode, bf16 only) for callers that cannot
+ * allocate device memory and so cannot supply a workspace: code whose device
+ * memory is all owned by another allocator, or that runs where cudaMalloc is
+ * not allowed. The paper has no counterpart to this entry point. Its scratch
+ * (split partials, counters, error word) is a fixed 8 MiB device array inside
+ * the library, held by every GPU that loads it until the process exits;
+ * shapes needing more return KASCADE_ERR_WORKSPACE. The first call on a
+ * device looks up the array's device address, so make it before any stream
+ * capture. All calls share the array: calls that overlap on the GPU race
+ * and must be serialised by the caller. Allocates nothing. */
+kascade_status kascade_dense_decode_noalloc(const kascade_desc* desc, const void* q,
+                                            const void* k, const void* v, void* out,
+                                            void* stream);
+
 /* --------------------------------------------------------------- prefill -- */
 
 /* Causal exact attention (the library's own dense baseline), bf16 only. */

@@ -45,6 +45,7 @@ _SIGS = {
     "kascade_anchor_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kascade_reuse_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "kascade_topk": (ctypes.c_int, [_vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
+    "kascade_dense_decode_noalloc": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp]),
     "kascade_dense_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kascade_anchor_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "kascade_reuse_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),

@@ -99,3 +99,23 @@ def test_host_dp_ties_and_errors(K):
     assert K.schedule_anchors(M.tolist(), 2)[0] == [0, 4]
     with pytest.raises(K.KascadeError):
         K.schedule_anchors(np.ones((3, 3)).tolist(), 4)
+
+
+def test_noalloc_rejects_shapes_beyond_its_scratch(K):
+    """The no-allocation dense decode keeps its scratch in a fixed 8 MiB device
+    array; a shape whose split partials need more is refused before any CUDA
+    call. Fake pointers are never dereferenced, so this runs only where no GPU
+    is present."""
+    import ctypes
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("validation-only check with placeholder pointers")
+    # 64 x 256 heads x one split x (128 + 4) floats = 8.65 MB > 8 MiB - 64 KiB
+    desc = K.make_desc(64, 256, 32, 128, 4096, K.BF16)
+    p = ctypes.c_void_p(1 << 20)
+    assert K._lib.kascade_dense_decode_noalloc(ctypes.byref(desc), p, p, p, p, None) == K.WORKSPACE
+    ok = K.make_desc(8, 32, 8, 128, 32768, K.BF16)
+    # a fitting shape passes validation and then needs a device (none here)
+    assert K._lib.kascade_dense_decode_noalloc(ctypes.byref(ok), p, p, p, p, None) == K.CUDA
+    f32 = K.make_desc(8, 32, 8, 128, 32768, K.F32)
+    assert K._lib.kascade_dense_decode_noalloc(ctypes.byref(f32), p, p, p, p, None) == K.UNSUPPORTED
