@@ -208,7 +208,8 @@ kascade_status run_topk_rows(const float* scores, int rows, int n, int k, int32_
   t.k_stride = k;
   t.prefill_tiles = 0;
   t.tile = 128;
-  return cuda_status(launch_topk(t, st));
+  const cudaError_t e = launch_topk(t, st);
+  return e == cudaErrorNotSupported ? KASCADE_ERR_UNSUPPORTED : cuda_status(e);
 }
 
 kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, const void* v,
@@ -242,6 +243,7 @@ kascade_status run_reuse_decode(const Shape& s, const void* q, const void* k, co
     if (r != KASCADE_OK) return r;
   }
   a.S = decode_splits_union(s.B * s.Hkv, s.G, topk);
+  if (a.S < 1) return KASCADE_ERR_UNSUPPORTED;   // G*topk too large for 128 splits
   return cuda_status(launch_decode_union_bf16(a, s.d, st));
 }
 

@@ -31,6 +31,8 @@ namespace kascade {
 
 namespace {
 
+constexpr int kPlanCap = 2048;   // plan entries of one reuse CTA staged in shared memory
+
 #define kNegInf (-CUDART_INF_F)
 
 // ------------------------------------------------------------------------
@@ -376,16 +378,42 @@ __global__ void __launch_bounds__(1024) k_build_union_plan(const __grid_constant
   const int words = (N + 31) / 32;
   for (int i = threadIdx.x; i < G * words; i += blockDim.x) bm[i] = 0u;
   __syncthreads();
-  for (int slot = 0; slot < G; ++slot) {
-    const int hq = a.heads[g * G + slot];
-    const int32_t* row = a.idx + (static_cast<size_t>(b) * a.Hq + hq) * topk;
-    for (int j = threadIdx.x; j < topk; j += blockDim.x) {
-      const int key = row[j];
-      if (key < 0 || key >= N) {
-        report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x201);
-        continue;
+  // Loads are batched (4 x int4 per thread in flight) before any atomics.
+  const bool vec = (topk & 3) == 0;
+  const int per_slot = vec ? topk / 4 : topk;
+  const int total = G * per_slot;
+  for (int i0 = 0; i0 < total; i0 += 4 * blockDim.x) {
+    int4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x + threadIdx.x;
+      v[u] = make_int4(-1, -1, -1, -1);
+      if (i < total) {
+        const int slot = i / per_slot, j = i % per_slot;
+        const int32_t* row =
+            a.idx + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + slot]) * topk;
+        if (vec)
+          v[u] = __ldg(reinterpret_cast<const int4*>(row) + j);
+        else
+          v[u].x = __ldg(row + j);
       }
-      atomicOr(&bm[slot * words + (key >> 5)], 1u << (key & 31));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * blockDim.x + threadIdx.x;
+      if (i >= total) continue;
+      const int slot = i / per_slot;
+      const int keys[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (c > 0 && !vec) break;
+        const int key = keys[c];
+        if (key < 0 || key >= N) {
+          report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x201);
+          continue;
+        }
+        atomicOr(&bm[slot * words + (key >> 5)], 1u << (key & 31));
+      }
     }
   }
   __syncthreads();
@@ -437,6 +465,7 @@ __global__ void __launch_bounds__(NW * 32)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* wbuf = smem + warp * STAGES * 2 * SLICE;
+  uint32_t* s_plan = reinterpret_cast<uint32_t*>(smem + NW * STAGES * 2 * SLICE);
 
   const int split = blockIdx.x, unit = blockIdx.y;
   const int b = unit / a.Hkv, g = unit % a.Hkv;
@@ -445,9 +474,20 @@ __global__ void __launch_bounds__(NW * 32)
   cs = (cs + 15) & ~15;
   const int e0 = split * cs;
   const int e1 = min(U, e0 + cs);
+  if (e1 - e0 > kPlanCap) {   // the host sizes S so this cannot happen
+    if (threadIdx.x == 0) report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x202);
+    return;
+  }
   const int nslices = e0 < e1 ? (e1 - e0 + 15) / 16 : 0;
   const int my = warp < nslices ? (nslices - warp + NW - 1) / NW : 0;
-  const uint32_t* plan = a.plan + static_cast<size_t>(unit) * a.plan_stride;
+  {
+    // this CTA's plan entries, once, coalesced; padded with 0 (mask 0)
+    const uint32_t* plan = a.plan + static_cast<size_t>(unit) * a.plan_stride;
+    const int padded = nslices * 16;
+    for (int i = threadIdx.x; i < padded; i += blockDim.x)
+      s_plan[i] = (e0 + i < e1) ? __ldg(plan + e0 + i) : 0u;
+    __syncthreads();
+  }
   const __nv_bfloat16* kbase =
       static_cast<const __nv_bfloat16*>(a.k) + static_cast<size_t>(unit) * a.N * D;
   const __nv_bfloat16* vbase =
@@ -456,8 +496,7 @@ __global__ void __launch_bounds__(NW * 32)
   auto issue = [&](int i) {
     const int sl = warp + i * NW;
     const int stg = i % STAGES;
-    const int e = e0 + sl * 16 + (lane & 15);
-    const uint32_t ent = (e < e1) ? __ldg(plan + e) : 0u;
+    const uint32_t ent = s_plan[sl * 16 + (lane & 15)];
     unsigned char* kd = wbuf + stg * 2 * SLICE;
     unsigned char* vd = kd + SLICE;
 #pragma unroll
@@ -492,8 +531,7 @@ __global__ void __launch_bounds__(NW * 32)
     const uint32_t kd = smem_u32(wbuf + (i % STAGES) * 2 * SLICE);
     float sc[4];
     slice_scores<D>(kd, 16, 0, qf, sc);
-    const int e = e0 + sl * 16 + (lane & 15);
-    const uint32_t ent = (e < e1) ? __ldg(plan + e) : 0u;
+    const uint32_t ent = s_plan[sl * 16 + (lane & 15)];
     const uint32_t m0 = __shfl_sync(0xffffffffu, ent, gid) >> 24;
     const uint32_t m1 = __shfl_sync(0xffffffffu, ent, gid + 8) >> 24;
     float x[4];
@@ -599,7 +637,7 @@ cudaError_t launch_dense_t(const DecodeArgs& a, cudaStream_t st) {
 template <int D, int NW, int STAGES>
 cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
   constexpr int SLICE = (D / 64) * 16 * 128;
-  const size_t smem = 1024 + static_cast<size_t>(NW) * STAGES * 2 * SLICE;
+  const size_t smem = 1024 + static_cast<size_t>(NW) * STAGES * 2 * SLICE + kPlanCap * 4;
   auto kern = k_decode_union_bf16<D, NW, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
@@ -631,7 +669,10 @@ int decode_splits_union(int units, int G, int topk) {
   int s = (kTargetCtas + units - 1) / units;
   const int max_by_len = (G * topk + 255) / 256;
   if (s > max_by_len) s = max_by_len;
-  if (s > kMaxSplits) s = kMaxSplits;
+  // each split's plan entries must fit the shared staging area
+  const int min_for_cap = (G * topk + kPlanCap - 16 - 1) / (kPlanCap - 16);
+  if (s < min_for_cap) s = min_for_cap;
+  if (s > kMaxSplits) return -1;
   if (s < 1) s = 1;
   return s;
 }

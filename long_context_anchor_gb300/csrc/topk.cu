@@ -3,17 +3,23 @@
 // 5). Rule: larger score first, lower index wins a tie, -0 == +0; output
 // ascending positions.
 //
-// One CTA (32 warps) per row:
-//   1. scores become order-preserving uint32 keys; rows up to 32768 entries
-//      are staged in shared memory once, longer rows are re-read (from L2);
-//   2. radix select on 11/11/10-bit digits with warp-aggregated shared
-//      histograms; as soon as the bin holding the k-th key fits, its members
-//      are compacted into a shared candidate list and the remaining digits
-//      run on the candidates only;
-//   3. with the k-th key T known, the row is split into 32 warp segments;
-//      per-segment counts of keys > T and == T are scanned, and each warp
-//      writes its selected positions in index order using ballots, taking
-//      keys == T in index order until k are selected.
+// One 1024-thread CTA per row, two CTAs per SM; scores become order-
+// preserving uint32 keys on the fly. Typical cost is two coalesced passes
+// over the row (the second mostly from L2):
+//   A. histogram of the top 11 key bits (warp-aggregated shared atomics);
+//      the bin holding the k-th key is found by a block scan. If that bin is
+//      too large for the candidate list, further 11/10-bit digit passes over
+//      the row narrow the prefix first;
+//   B. marking pass: every 32 consecutive positions give one 32-bit word of
+//      "key above the prefix" by a warp ballot (a bitmap, no atomics); keys
+//      inside the prefix are compacted into a shared candidate list (or,
+//      when the prefix is already the full key, marked in an "equal" bitmap);
+//   C. the remaining digits run on the candidates only, giving the k-th key
+//      T; candidates > T join the "above" bitmap, candidates == T the
+//      "equal" bitmap;
+//   D. ordered emission: a block scan over per-thread word runs gives each
+//      thread its output offset; keys == T are taken in position order until
+//      k positions are written.
 // Prefill rows are the packed tile weights of one (sequence, head, tile):
 // length L_t = min(N, 128(t+1)), k_t = min(k, L_t), -1 padding after k_t.
 #include <cuda_runtime.h>
@@ -26,8 +32,8 @@ namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowCap = 32768;   // entries staged in shared memory
-constexpr int kCandCap = 8192;   // candidate (key, position) pairs
+constexpr int kCandCap = 4096;   // candidate (key, position) pairs in shared memory
+constexpr int kUnroll = 8;       // 32-position chunks in flight per warp
 
 struct RowDesc {
   const float* ptr;
@@ -85,93 +91,76 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, bool active, uint32_t b
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ TopkArgs a) {
+// Visit the row in warp-owned blocks of 32*kUnroll consecutive positions;
+// f(pos, valid, key) runs on every lane (warp-uniform control flow).
+template <typename F>
+__device__ __forceinline__ void for_row(const RowDesc& rd, bool& bad, F f) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = warp * 32 * kUnroll; base < rd.len; base += kWarps * 32 * kUnroll) {
+    float x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = base + 32 * u + lane;
+      x[u] = j < rd.len ? __ldg(rd.ptr + j) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = base + 32 * u + lane;
+      const bool valid = j < rd.len;
+      bad |= valid && isnan(x[u]);
+      f(j, valid, float_key(x[u]));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ TopkArgs a,
+                                                      int words_cap) {
   extern __shared__ uint32_t sm[];
   uint32_t* hist = sm;                                                     // [2048]
   uint32_t* cand_key = hist + 2048;                                        // [kCandCap]
   int32_t* cand_pos = reinterpret_cast<int32_t*>(cand_key + kCandCap);     // [kCandCap]
-  uint32_t* row_keys = reinterpret_cast<uint32_t*>(cand_pos + kCandCap);   // [len] if staged
+  uint32_t* above = reinterpret_cast<uint32_t*>(cand_pos + kCandCap);      // [words_cap]
+  uint32_t* eqbm = above + words_cap;                                      // [words_cap]
   __shared__ int warp_tot[32];
-  __shared__ int seg_gt[kWarps], seg_eq[kWarps];
   __shared__ int s_ncand, s_bin, s_above;
 
   const int r = blockIdx.x;
   const RowDesc rd = row_desc(a, r);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   int32_t* out = a.idx_out + static_cast<size_t>(r) * a.k_stride;
 
   if (rd.k >= rd.len) {   // the whole prefix is selected
     for (int j = tid; j < a.k_stride; j += kThreads) out[j] = (j < rd.len) ? j : -1;
     return;
   }
-  const bool staged = a.n <= kRowCap;   // shared memory is sized for a.n >= rd.len
+  const int W = (rd.len + 31) >> 5;
+  for (int w = tid; w < W; w += kThreads) above[w] = eqbm[w] = 0u;
   if (tid == 0) s_ncand = 0;
-  if (staged) {
-    bool bad = false;
-    for (int j = tid; j < rd.len; j += kThreads) {
-      const float f = __ldg(rd.ptr + j);
-      bad |= isnan(f);
-      row_keys[j] = float_key(f);
-    }
-    if (__syncthreads_or(bad) && tid == 0) report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x401);
-  } else {
-    __syncthreads();
-  }
-  auto key_at = [&](int j) -> uint32_t {
-    return staged ? row_keys[j] : float_key(__ldg(rd.ptr + j));
-  };
 
+  // A. digit histograms over the row until the k-th key's bin fits the
+  //    candidate list (usually after the first digit) or the key is complete.
   uint32_t prefix = 0, pmask = 0;
-  int c_gt = 0;
-  bool in_cands = false;
-  const int seg = (((rd.len + kWarps - 1) / kWarps) + 31) & ~31;
-  const int seg0 = warp * seg, seg1 = min(rd.len, seg0 + seg);
-
-  for (int d = 0; d < 3; ++d) {
+  int c_gt = 0, d = 0;
+  bool bad = false;
+  while (true) {
     const int nb = d < 2 ? 2048 : 1024;
     const int sh = d == 0 ? 21 : (d == 1 ? 10 : 0);
     for (int i = tid; i < nb; i += kThreads) hist[i] = 0u;
     __syncthreads();
-    if (in_cands) {
-      const int nc = s_ncand;
-      for (int i = tid; i < nc; i += kThreads) {
-        const uint32_t key = cand_key[i];
-        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
-      }
-    } else {
-      bool bad = false;
-      for (int j0 = 0; j0 < rd.len; j0 += kThreads) {
-        const int j = j0 + tid;
-        uint32_t key = 0;
-        bool act = false;
-        if (j < rd.len) {
-          if (!staged && d == 0) {
-            const float f = __ldg(rd.ptr + j);
-            bad |= isnan(f);
-            key = float_key(f);
-          } else {
-            key = key_at(j);
-          }
-          act = (key & pmask) == prefix;
-        }
-        hist_add(hist, act, (key >> sh) & (nb - 1));
-      }
-      if (bad) report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x402);
-    }
+    for_row(rd, bad, [&](int, bool valid, uint32_t key) {
+      hist_add(hist, valid && (key & pmask) == prefix, (key >> sh) & (nb - 1));
+    });
     __syncthreads();
-    // Locate the bin holding rank `need` counting from the top bin down.
     const int need = rd.k - c_gt;
     const int b_hi = nb - 1 - 2 * tid;   // this thread owns bins b_hi, b_hi-1
-    int h0 = 0, h1 = 0;
-    if (b_hi >= 0) h0 = static_cast<int>(hist[b_hi]);
-    if (b_hi - 1 >= 0) h1 = static_cast<int>(hist[b_hi - 1]);
-    const int incl = block_incl_scan(h0 + h1, warp_tot);
-    const int excl = incl - h0 - h1;
+    const int h0 = b_hi >= 0 ? static_cast<int>(hist[b_hi]) : 0;
+    const int h1 = b_hi >= 1 ? static_cast<int>(hist[b_hi - 1]) : 0;
+    const int excl = block_incl_scan(h0 + h1, warp_tot) - h0 - h1;
     if (b_hi >= 0) {
       if (excl < need && need <= excl + h0) {
         s_bin = b_hi;
         s_above = excl;
-      } else if (b_hi - 1 >= 0 && excl + h0 < need && need <= excl + h0 + h1) {
+      } else if (b_hi >= 1 && excl + h0 < need && need <= excl + h0 + h1) {
         s_bin = b_hi - 1;
         s_above = excl + h0;
       }
@@ -181,98 +170,107 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
     c_gt += s_above;
     prefix |= static_cast<uint32_t>(bin) << sh;
     pmask |= static_cast<uint32_t>(nb - 1) << sh;
-    const int cnt_bin = static_cast<int>(hist[bin]);
+    const int cnt = static_cast<int>(hist[bin]);
+    ++d;
     __syncthreads();
-    if (!in_cands && d < 2 && cnt_bin <= kCandCap) {
-      // Compact the bin's members; count keys above the prefix per segment.
-      int above = 0;
-      for (int j0 = seg0; j0 < seg0 + seg; j0 += 32) {
-        const int j = j0 + lane;
-        uint32_t key = 0;
-        bool is_c = false;
-        if (j < seg1) {
-          key = key_at(j);
-          const uint32_t hi = key & pmask;
-          above += hi > prefix;
-          is_c = hi == prefix;
-        }
-        const unsigned int bal = __ballot_sync(0xffffffffu, is_c);
-        int base = 0;
-        if (lane == 0 && bal) base = atomicAdd(&s_ncand, __popc(bal));
-        base = __shfl_sync(0xffffffffu, base, 0);
-        if (is_c) {
-          const int p = base + __popc(bal & ((1u << lane) - 1u));
-          cand_key[p] = key;
-          cand_pos[p] = j;
+    if (d == 3 || cnt <= kCandCap) break;
+  }
+  if (__syncthreads_or(bad) && tid == 0) report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x401);
+
+  // B. marking pass: ballot bitmaps of keys above the prefix; candidates
+  //    inside it (or, with a complete prefix, the "equal" bitmap).
+  const bool full = d == 3;
+  for_row(rd, bad, [&](int j, bool valid, uint32_t key) {
+    const uint32_t hi = key & pmask;
+    const bool in = valid && hi == prefix;
+    const unsigned int ba = __ballot_sync(0xffffffffu, valid && hi > prefix);
+    const unsigned int bi = __ballot_sync(0xffffffffu, in);
+    if (lane == 0 && j < rd.len) {
+      above[j >> 5] = ba;
+      if (full) eqbm[j >> 5] = bi;
+    }
+    if (!full && bi) {
+      int base = 0;
+      if (lane == 0) base = atomicAdd(&s_ncand, __popc(bi));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      if (in) {
+        const int p = base + __popc(bi & ((1u << lane) - 1u));
+        cand_key[p] = key;
+        cand_pos[p] = j;
+      }
+    }
+  });
+  __syncthreads();
+
+  // C. remaining digits on the candidates; mark them against T.
+  if (!full) {
+    const int nc = s_ncand;
+    for (; d < 3; ++d) {
+      const int nb = d < 2 ? 2048 : 1024;
+      const int sh = d == 1 ? 10 : 0;
+      for (int i = tid; i < nb; i += kThreads) hist[i] = 0u;
+      __syncthreads();
+      for (int i = tid; i < nc; i += kThreads) {
+        const uint32_t key = cand_key[i];
+        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+      }
+      __syncthreads();
+      const int need = rd.k - c_gt;
+      const int b_hi = nb - 1 - 2 * tid;
+      const int h0 = b_hi >= 0 ? static_cast<int>(hist[b_hi]) : 0;
+      const int h1 = b_hi >= 1 ? static_cast<int>(hist[b_hi - 1]) : 0;
+      const int excl = block_incl_scan(h0 + h1, warp_tot) - h0 - h1;
+      if (b_hi >= 0) {
+        if (excl < need && need <= excl + h0) {
+          s_bin = b_hi;
+          s_above = excl;
+        } else if (b_hi >= 1 && excl + h0 < need && need <= excl + h0 + h1) {
+          s_bin = b_hi - 1;
+          s_above = excl + h0;
         }
       }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) above += __shfl_xor_sync(0xffffffffu, above, off);
-      if (lane == 0) seg_gt[warp] = above;
-      in_cands = true;
+      __syncthreads();
+      c_gt += s_above;
+      prefix |= static_cast<uint32_t>(s_bin) << sh;
+      pmask |= static_cast<uint32_t>(nb - 1) << sh;
       __syncthreads();
     }
-  }
-  const uint32_t T = prefix;   // the k-th largest key
-  // Per-segment counts of keys > T and == T.
-  if (in_cands) {
-    if (tid < kWarps) seg_eq[tid] = 0;
-    __syncthreads();
-    const int nc = s_ncand;
     for (int i = tid; i < nc; i += kThreads) {
       const uint32_t key = cand_key[i];
-      const int sgi = cand_pos[i] / seg;
-      if (key > T) atomicAdd(&seg_gt[sgi], 1);
-      else if (key == T) atomicAdd(&seg_eq[sgi], 1);
+      const int p = cand_pos[i];
+      if (key > prefix) atomicOr(&above[p >> 5], 1u << (p & 31));
+      else if (key == prefix) atomicOr(&eqbm[p >> 5], 1u << (p & 31));
     }
-  } else {
-    int gt = 0, eq = 0;
-    for (int j = seg0 + lane; j < seg1; j += 32) {
-      const uint32_t key = key_at(j);
-      gt += key > T;
-      eq += key == T;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      gt += __shfl_xor_sync(0xffffffffu, gt, off);
-      eq += __shfl_xor_sync(0xffffffffu, eq, off);
-    }
-    if (lane == 0) {
-      seg_gt[warp] = gt;
-      seg_eq[warp] = eq;
-    }
+    __syncthreads();
   }
-  __syncthreads();
-  int gt_before = 0, eq_before = 0, gt_total = 0;
-  for (int w = 0; w < kWarps; ++w) {
-    if (w < warp) {
-      gt_before += seg_gt[w];
-      eq_before += seg_eq[w];
-    }
-    gt_total += seg_gt[w];
+
+  // D. ordered emission.
+  const int need_eq = rd.k - c_gt;
+  const int per = (W + kThreads - 1) / kThreads;
+  const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
+  int ca = 0, ce = 0;
+  for (int w = w0; w < w1; ++w) {
+    ca += __popc(above[w]);
+    ce += __popc(eqbm[w]);
   }
-  const int need_eq = rd.k - gt_total;
-  // Ordered write of the selected positions.
-  int run_gt = 0, run_eq = 0;
-  for (int j0 = seg0; j0 < seg0 + seg; j0 += 32) {
-    const int j = j0 + lane;
-    bool gt = false, eq = false;
-    if (j < seg1) {
-      const uint32_t key = key_at(j);
-      gt = key > T;
-      eq = key == T;
+  int pa = block_incl_scan(ca, warp_tot) - ca;
+  int pe = block_incl_scan(ce, warp_tot) - ce;
+  for (int w = w0; w < w1; ++w) {
+    const uint32_t ab = above[w], eb = eqbm[w];
+    uint32_t u = ab | eb;
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      const int pos = w * 32 + bit;
+      if ((ab >> bit) & 1u) {
+        const int o = pa + min(pe, need_eq);
+        if (o < rd.k) out[o] = pos;
+        ++pa;
+      } else {
+        if (pe < need_eq && pa + pe < rd.k) out[pa + pe] = pos;
+        ++pe;
+      }
     }
-    const unsigned int bg = __ballot_sync(0xffffffffu, gt);
-    const unsigned int be = __ballot_sync(0xffffffffu, eq);
-    const unsigned int lt = (1u << lane) - 1u;
-    const int my_gt = gt_before + run_gt + __popc(bg & lt);
-    const int my_eq = eq_before + run_eq + __popc(be & lt);
-    if (gt || (eq && my_eq < need_eq)) {
-      const int pos = my_gt + min(my_eq, need_eq);
-      if (pos < rd.k) out[pos] = j;
-    }
-    run_gt += __popc(bg);
-    run_eq += __popc(be);
   }
   for (int j = rd.k + tid; j < a.k_stride; j += kThreads) out[j] = -1;
 }
@@ -281,12 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_topk(const __grid_constant__ To
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
-  size_t smem = (2048 + 2 * kCandCap) * sizeof(uint32_t);
-  if (a.n <= kRowCap) smem += static_cast<size_t>(a.n) * sizeof(uint32_t);
+  const int words_cap = (a.n + 31) / 32;
+  const size_t smem = (2048 + 2 * kCandCap) * sizeof(uint32_t) +
+                      2 * static_cast<size_t>(words_cap) * sizeof(uint32_t);
+  if (smem > 220 * 1024) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k_topk<<<a.rows, kThreads, smem, st>>>(a);
+  k_topk<<<a.rows, kThreads, smem, st>>>(a, words_cap);
   return cudaGetLastError();
 }
 
