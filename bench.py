@@ -221,6 +221,108 @@ def dist_env():
     return rank, world, local
 
 
+def prefill_flops(w, topk_sizes=None):
+    """Algorithmic FLOPs per layer kind for causal prefill (bf16 MMAs).
+
+    dense : QK^T and PV over the causal pairs, 4 * d * Hq * N(N+1)/2;
+    anchor: dense + one more QK^T pass for the tile weights (1.5 x dense);
+    reuse : QK^T and PV of every 128-row tile against its k_t saved keys,
+            4 * d * Hq * sum_t rows_t * k_t.
+    """
+    N, d, Hq, k, T = w.kv_len, w.head_dim, w.n_q_heads, w.topk, w.tile
+    pairs = N * (N + 1) // 2
+    dense = 4 * d * Hq * pairs * w.batch
+    anchor = dense * 3 // 2
+    nT = (N + T - 1) // T
+    tile_pairs = sum(min(N, T * (t + 1)) - T * t for t in range(nT))
+    reuse = 4 * d * Hq * w.batch * sum((min(N, T * (t + 1)) - T * t) * min(k, min(N, T * (t + 1)))
+                                       for t in range(nT))
+    del tile_pairs
+    return dense, anchor, reuse
+
+
+def run_prefill(args, dev, world, stream):
+    """Prefill stack of the Llama-3.1-8B shape at N = 16384 (32 layers,
+    anchors every 4th layer): Kascade vs the library's own dense prefill."""
+    import torch
+    import torch.distributed as dist
+    from long_context_anchor_gb300 import configs
+    from long_context_anchor_gb300 import kascade as K
+    from long_context_anchor_gb300.workloads import make_layers
+    w = configs.LLAMA8B_PREFILL_16K
+    L = w.n_layers
+    qs, ks, vs = make_layers(w, device=dev)
+    outs = [torch.empty_like(q) for q in qs]
+    nT = (w.kv_len + 127) // 128
+    idx_buf = torch.empty(w.batch, w.n_q_heads, nT, w.topk, dtype=torch.int32, device=dev)
+    ws = K.Workspace(dev)
+    anchors = list(w.anchors)
+
+    def timed(anch, steps):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(steps)]
+        for row in evs:
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        for s in range(steps):
+            evs[s][0].record(stream)
+            K.run_stack(K.PREFILL, qs, ks, vs, w.topk, anch, outs=outs, idx_buf=idx_buf, ws=ws,
+                        layer_events=evs[s][1:])
+        torch.cuda.synchronize()
+        per = [[evs[s][l].elapsed_time(evs[s][l + 1]) for l in range(L)] for s in range(steps)]
+        total = sum(evs[s][0].elapsed_time(evs[s][L]) for s in range(steps))
+        return total, per
+
+    for _ in range(args.warmup):
+        K.run_stack(K.PREFILL, qs, ks, vs, w.topk, anchors, outs=outs, idx_buf=idx_buf, ws=ws)
+        K.run_stack(K.PREFILL, qs, ks, vs, w.topk, [], outs=outs, idx_buf=idx_buf, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.device_error() == K.OK
+    steps = max(1, args.steps // 2)
+    tot_k, per_k = timed(anchors, steps)
+    tot_d, per_d = timed([], steps)
+    if world > 1:
+        t = torch.tensor([tot_k, tot_d], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_k, tot_d = t.tolist()
+    ms_k, ms_d = tot_k / steps, tot_d / steps
+    reuse_layers = [l for l in range(L) if l not in anchors]
+    anchor_ms = statistics.mean(per_k[s][l] for s in range(steps) for l in anchors)
+    reuse_ms = statistics.mean(per_k[s][l] for s in range(steps) for l in reuse_layers)
+    dense_ms = ms_d / L
+    f_dense, f_anchor, f_reuse = prefill_flops(w)
+    _, tf_burst, src = load_peaks()
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tf_sust = float(json.load(f)["bf16_tflops_sustained"])
+    except (OSError, KeyError, ValueError):
+        tf_sust = 1700.0
+    res = {
+        "workload": w.name, "layers": L, "kv_len": w.kv_len, "topk": w.topk, "anchors": anchors,
+        "kascade_ms_per_stack": round(ms_k, 3), "dense_ms_per_stack": round(ms_d, 3),
+        "speedup_vs_own_dense": round(ms_d / ms_k, 3),
+        "anchor_layer_us": round(1e3 * anchor_ms, 1), "reuse_layer_us": round(1e3 * reuse_ms, 1),
+        "dense_layer_us": round(1e3 * dense_ms, 1),
+        "dense_tflops": round(f_dense / (dense_ms * 1e-3) / 1e12, 1),
+        "anchor_tflops": round(f_anchor / (anchor_ms * 1e-3) / 1e12, 1),
+        "reuse_tflops": round(f_reuse / (reuse_ms * 1e-3) / 1e12, 1),
+        "stack_tflops": round((len(anchors) * f_anchor + len(reuse_layers) * f_reuse) /
+                              (ms_k * 1e-3) / 1e12, 1),
+        "flops_per_layer": {"dense": f_dense, "anchor": f_anchor, "reuse": f_reuse},
+        "peak_bf16_tflops_sustained": tf_sust, "peak_bf16_tflops_burst": tf_burst,
+        "peak_source": src,
+    }
+    res["dense_frac_of_sustained"] = round(res["dense_tflops"] / tf_sust, 4)
+    res["anchor_frac_of_sustained"] = round(res["anchor_tflops"] / tf_sust, 4)
+    res["reuse_frac_of_sustained"] = round(res["reuse_tflops"] / tf_sust, 4)
+    launches = steps * (3 * len(anchors) + len(reuse_layers))
+    del qs, ks, vs, outs
+    torch.cuda.empty_cache()
+    return res, launches, ms_k, (anchor_ms, f_anchor, reuse_ms, f_reuse, tf_sust, src)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -396,6 +498,25 @@ def run_ours(args):
     result["e2e"] = {"value": round(1e3 * e2e_ms / L, 3), "unit": UNIT,
                      "h2d_bytes_per_step": int(q_host.numel() * 2 + 2 * knew_host.numel() * 2),
                      "d2h_bytes_per_step": int(out_host.numel() * 2)}
+    # Prefill stack (same step): Llama-3.1-8B shape at N = 16384.
+    if not args.no_prefill:
+        pre, pre_launches, pre_ms, (pa_ms, pa_f, pr_ms, pr_f, tf_sust, tsrc) = \
+            run_prefill(args, dev, world, stream)
+        result["prefill"] = pre
+        result["gpu_launches_prefill"] = pre_launches
+        result["ms_per_step_prefill"] = round(pre_ms, 3)
+        pr_tf = pr_f / (pr_ms * 1e-3) / 1e12
+        result["roofline_prefill_reuse"] = {
+            "kernel": "k_prefill_fa<gather> (reuse layer)", "bound": "tensor",
+            "achieved": round(pr_tf, 1), "peak": tf_sust, "unit": "TFLOP/s",
+            "frac": round(pr_tf / tf_sust, 4), "traffic": None, "algorithmic_flops": int(pr_f),
+            "peak_source": tsrc + " (sustained)"}
+        # The step's dominant single-launch kernel by total time.
+        dec_reuse_total = len(reuse_layers) * reuse_ms
+        pre_reuse_total = (w.n_layers - len(anchors)) * pr_ms
+        if pre_reuse_total > dec_reuse_total:
+            result["roofline_decode_reuse"] = result["roofline"]
+            result["roofline"] = result["roofline_prefill_reuse"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
         result["cpu_baseline"] = time_oracle(w, lay01, n_groups=os.cpu_count() or 1, reps=2)
@@ -441,6 +562,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

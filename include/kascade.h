@@ -35,8 +35,10 @@
  *   - `ws` is a caller-owned device workspace of at least
  *     kascade_workspace_size() bytes, 256-byte aligned. It must be zeroed
  *     once (kascade_workspace_init) before first use; afterwards the library
- *     leaves it in a reusable state. Calls sharing one workspace must be
- *     ordered (same stream, or synchronised).
+ *     leaves it in a reusable state: its first 65,792 bytes (error word and
+ *     split counters) stay zero between calls of any shape or entry point,
+ *     and must not be written by the caller. Calls sharing one workspace must
+ *     be ordered (same stream, or synchronised).
  *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *     default stream). Argument errors are returned before anything is
  *     launched; launch failures return KASCADE_ERR_CUDA. Faults found on the

@@ -85,6 +85,7 @@ kascade_status check_desc(const kascade_desc* desc, Shape& s) {
   s.G = s.Hq / s.Hkv;
   if (s.G != 1 && s.G != 2 && s.G != 4 && s.G != 8) return KASCADE_ERR_UNSUPPORTED;
   if (static_cast<long long>(s.B) * s.Hkv * s.N >= (1ll << 31)) return KASCADE_ERR_UNSUPPORTED;
+  if (s.B * s.Hkv > kMaxCounterUnits) return KASCADE_ERR_UNSUPPORTED;
   if (s.N >= (1 << 24)) return KASCADE_ERR_UNSUPPORTED;
   s.scale = desc->scale > 0.f ? desc->scale : 1.0f / sqrtf(static_cast<float>(s.d));
   int fill[kMaxQHeads];
@@ -110,18 +111,18 @@ struct Layout {
 
 Layout layout(const Shape& s, int topk, int mode) {
   Layout L{};
-  size_t off = sizeof(WsHeader);
+  L.counters = sizeof(WsHeader);
+  size_t off = kWsStateBytes;
   if (mode == KASCADE_DECODE) {
-    L.counters = off;
-    off = align256(off + static_cast<size_t>(s.B) * s.Hkv * 4);
     L.part = off;
     off = align256(off + static_cast<size_t>(s.B) * s.Hq * kMaxSplits * (s.d + 4) * 4);
     L.spill = off;
     off = align256(off + static_cast<size_t>(s.B) * s.Hq * s.N * 4);
+    const size_t chunks = decode_union_chunks(s.B * s.Hkv, s.N);
     L.plan = off;
-    off = align256(off + static_cast<size_t>(s.B) * s.Hq * topk * 4);
+    off = align256(off + static_cast<size_t>(s.B) * s.Hkv * chunks * kPlanCapEntries * 4);
     L.plan_count = off;
-    off = align256(off + static_cast<size_t>(s.B) * s.Hkv * 4);
+    off = align256(off + static_cast<size_t>(s.B) * s.Hkv * chunks * 4);
   } else {
     const size_t nT = (s.N + 127) / 128;
     const size_t per_bh = 64 * (nT - 1) * nT + s.N;
@@ -227,8 +228,9 @@ kascade_status run_build_plan(const Shape& s, const int32_t* idx, int topk, void
   DecodeArgs a;
   fill_decode_args(a, s, nullptr, nullptr, nullptr, nullptr, ws, L, topk);
   a.idx = idx;
-  return cuda_status(
-      launch_build_union_plan(a, at<uint32_t>(ws, L.plan), at<int32_t>(ws, L.plan_count), st));
+  const cudaError_t e =
+      launch_build_union_plan(a, at<uint32_t>(ws, L.plan), at<int32_t>(ws, L.plan_count), st);
+  return e == cudaErrorNotSupported ? KASCADE_ERR_UNSUPPORTED : cuda_status(e);
 }
 
 kascade_status run_reuse_decode(const Shape& s, const void* q, const void* k, const void* v,
@@ -242,8 +244,8 @@ kascade_status run_reuse_decode(const Shape& s, const void* q, const void* k, co
     kascade_status r = run_build_plan(s, idx, topk, ws, L, st);
     if (r != KASCADE_OK) return r;
   }
-  a.S = decode_splits_union(s.B * s.Hkv, s.G, topk);
-  if (a.S < 1) return KASCADE_ERR_UNSUPPORTED;   // G*topk too large for 128 splits
+  a.S = decode_union_chunks(s.B * s.Hkv, s.N);
+  if (a.S > kMaxSplits) return KASCADE_ERR_UNSUPPORTED;   // N too long for 128 chunks
   return cuda_status(launch_decode_union_bf16(a, s.d, st));
 }
 

@@ -19,6 +19,13 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "workspace header is 256 bytes");
 
+// Every workspace layout starts with the header and a fixed region of split
+// arrival counters that kernels leave at zero between calls; shape-dependent
+// regions start after it, so calls of different shapes (or other entry
+// points) sharing one workspace never overwrite the counters.
+constexpr int kMaxCounterUnits = 16384;
+constexpr size_t kWsStateBytes = sizeof(WsHeader) + kMaxCounterUnits * sizeof(unsigned int);
+
 // Spin limit for every mbarrier / flag wait (each try_wait may also suspend
 // in hardware for a short time). Far above any legitimate wait.
 constexpr unsigned int kSpinLimit = 1u << 26;

@@ -31,7 +31,7 @@ namespace kascade {
 
 namespace {
 
-constexpr int kPlanCap = 2048;   // plan entries of one reuse CTA staged in shared memory
+constexpr int kPlanCap = kPlanCapEntries;   // plan entries of one reuse CTA (shared staging)
 
 #define kNegInf (-CUDART_INF_F)
 
@@ -363,67 +363,82 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 }
 
 // ------------------------------------------------------------------------
-// Union plan: per (sequence, KV head), merge the G ascending per-head sets
-// into one ascending key list; entry = key | (head-slot mask << 24).
-// One 1024-thread CTA per unit, per-slot bitmaps of N bits in shared memory.
+// Union plan, one CTA per (key-range chunk c, sequence b, KV head g): the G
+// ascending per-head sets are cut to keys [c*R, (c+1)*R) by a warp-wide
+// 32-ary lower-bound search, marked in per-slot shared bitmaps and emitted as
+// one ascending list of entries key | (head-slot mask << 24) into
+// plan[unit][c][kPlanCap], with its length in plan_count[unit][c]. Reuse
+// CTA (c, unit) consumes exactly chunk c.
 // ------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) k_build_union_plan(const __grid_constant__ DecodeArgs a,
-                                                           uint32_t* __restrict__ plan,
-                                                           int32_t* __restrict__ plan_count) {
-  extern __shared__ uint32_t bm[];   // [G][words]
-  __shared__ int s_scan[1024];
-  const int unit = blockIdx.x;
+__device__ __forceinline__ int warp_lower_bound(const int32_t* row, int n, int v) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = n;   // first index in [lo, hi] with row[i] >= v
+  while (hi - lo > 32) {
+    const int step = (hi - lo + 31) / 32;
+    const int p = lo + (lane + 1) * step - 1;
+    const bool ge = p >= hi || __ldg(row + p) >= v;
+    const unsigned int bal = __ballot_sync(0xffffffffu, ge);
+    if (bal == 0u) return hi;
+    const int f = __ffs(bal) - 1;
+    const int nlo = f == 0 ? lo : lo + f * step;
+    hi = min(hi, lo + (f + 1) * step - 1);
+    lo = nlo;
+  }
+  const int p = lo + lane;
+  const bool ge = p < hi && __ldg(row + p) >= v;
+  const unsigned int bal = __ballot_sync(0xffffffffu, ge);
+  return bal ? lo + __ffs(bal) - 1 : hi;
+}
+
+__global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant__ DecodeArgs a,
+                                                          uint32_t* __restrict__ plan,
+                                                          int32_t* __restrict__ plan_count,
+                                                          int R) {
+  __shared__ uint32_t bm[8][kPlanCap / 32];
+  __shared__ int s_lo[8], s_hi[8];
+  __shared__ int s_scan[256];
+  const int c = blockIdx.x, unit = blockIdx.y, nch = gridDim.x;
   const int b = unit / a.Hkv, g = unit % a.Hkv;
-  const int G = a.G, N = a.N, topk = a.topk;
-  const int words = (N + 31) / 32;
-  for (int i = threadIdx.x; i < G * words; i += blockDim.x) bm[i] = 0u;
-  __syncthreads();
-  // Loads are batched (4 x int4 per thread in flight) before any atomics.
-  const bool vec = (topk & 3) == 0;
-  const int per_slot = vec ? topk / 4 : topk;
-  const int total = G * per_slot;
-  for (int i0 = 0; i0 < total; i0 += 4 * blockDim.x) {
-    int4 v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * blockDim.x + threadIdx.x;
-      v[u] = make_int4(-1, -1, -1, -1);
-      if (i < total) {
-        const int slot = i / per_slot, j = i % per_slot;
-        const int32_t* row =
-            a.idx + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + slot]) * topk;
-        if (vec)
-          v[u] = __ldg(reinterpret_cast<const int4*>(row) + j);
-        else
-          v[u].x = __ldg(row + j);
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * blockDim.x + threadIdx.x;
-      if (i >= total) continue;
-      const int slot = i / per_slot;
-      const int keys[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c > 0 && !vec) break;
-        const int key = keys[c];
-        if (key < 0 || key >= N) {
-          report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x201);
-          continue;
-        }
-        atomicOr(&bm[slot * words + (key >> 5)], 1u << (key & 31));
-      }
+  const int G = a.G, topk = a.topk;
+  const int n0 = c * R, n1 = min(a.N, n0 + R);
+  const int words = (R + 31) / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = threadIdx.x; i < G * words; i += blockDim.x) bm[i / words][i % words] = 0u;
+  if (warp < G) {
+    const int32_t* row = a.idx + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + warp]) * topk;
+    const int lo = warp_lower_bound(row, topk, n0);
+    const int hi = warp_lower_bound(row, topk, n1);
+    if (lane == 0) {
+      s_lo[warp] = lo;
+      s_hi[warp] = hi;
+      // entries below 0 (first chunk) or at/after N (last chunk) are invalid
+      if ((c == 0 && lo > 0) || (c == nch - 1 && hi < topk))
+        report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x201);
     }
   }
   __syncthreads();
-  // each thread owns a contiguous run of words
+  for (int slot = 0; slot < G; ++slot) {
+    const int32_t* row = a.idx + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + slot]) * topk;
+    const int hi = s_hi[slot];
+    for (int i = s_lo[slot] + threadIdx.x; i < hi; i += blockDim.x) {
+      const int raw = __ldg(row + i);
+      const int key = raw - n0;
+      // the sets must be strictly ascending and inside [0, N)
+      if (key < 0 || key >= n1 - n0 || (i + 1 < hi && __ldg(row + i + 1) <= raw)) {
+        report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x202);
+        if (key < 0 || key >= n1 - n0) continue;
+      }
+      atomicOr(&bm[slot][key >> 5], 1u << (key & 31));
+    }
+  }
+  __syncthreads();
+  // contiguous word runs per thread; block scan of union counts
   const int per = (words + blockDim.x - 1) / blockDim.x;
   const int w0 = min(words, static_cast<int>(threadIdx.x) * per), w1 = min(words, w0 + per);
   int cnt = 0;
   for (int w = w0; w < w1; ++w) {
     uint32_t u = 0;
-    for (int slot = 0; slot < G; ++slot) u |= bm[slot * words + w];
+    for (int slot = 0; slot < G; ++slot) u |= bm[slot][w];
     cnt += __popc(u);
   }
   s_scan[threadIdx.x] = cnt;
@@ -435,19 +450,19 @@ __global__ void __launch_bounds__(1024) k_build_union_plan(const __grid_constant
     __syncthreads();
   }
   int pos = s_scan[threadIdx.x] - cnt;
-  uint32_t* out = plan + static_cast<size_t>(unit) * a.plan_stride;
+  uint32_t* out = plan + (static_cast<size_t>(unit) * nch + c) * kPlanCap;
   for (int w = w0; w < w1; ++w) {
     uint32_t u = 0;
-    for (int slot = 0; slot < G; ++slot) u |= bm[slot * words + w];
+    for (int slot = 0; slot < G; ++slot) u |= bm[slot][w];
     while (u) {
       const int bit = __ffs(u) - 1;
       u &= u - 1;
       uint32_t mask = 0;
-      for (int slot = 0; slot < G; ++slot) mask |= ((bm[slot * words + w] >> bit) & 1u) << slot;
-      out[pos++] = static_cast<uint32_t>(w * 32 + bit) | (mask << 24);
+      for (int slot = 0; slot < G; ++slot) mask |= ((bm[slot][w] >> bit) & 1u) << slot;
+      out[pos++] = static_cast<uint32_t>(n0 + w * 32 + bit) | (mask << 24);
     }
   }
-  if (threadIdx.x == blockDim.x - 1) plan_count[unit] = s_scan[threadIdx.x];
+  if (threadIdx.x == blockDim.x - 1) plan_count[unit * nch + c] = s_scan[threadIdx.x];
 }
 
 // ------------------------------------------------------------------------
@@ -469,23 +484,17 @@ __global__ void __launch_bounds__(NW * 32)
 
   const int split = blockIdx.x, unit = blockIdx.y;
   const int b = unit / a.Hkv, g = unit % a.Hkv;
-  const int U = a.plan_count[unit];
-  int cs = (U + a.S - 1) / a.S;
-  cs = (cs + 15) & ~15;
-  const int e0 = split * cs;
-  const int e1 = min(U, e0 + cs);
-  if (e1 - e0 > kPlanCap) {   // the host sizes S so this cannot happen
-    if (threadIdx.x == 0) report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x202);
-    return;
-  }
-  const int nslices = e0 < e1 ? (e1 - e0 + 15) / 16 : 0;
+  // this CTA's chunk of the union plan (keys of one key range)
+  const int e0 = 0;
+  const int e1 = min(kPlanCap, a.plan_count[unit * a.S + split]);
+  const int nslices = (e1 + 15) / 16;
   const int my = warp < nslices ? (nslices - warp + NW - 1) / NW : 0;
   {
-    // this CTA's plan entries, once, coalesced; padded with 0 (mask 0)
-    const uint32_t* plan = a.plan + static_cast<size_t>(unit) * a.plan_stride;
+    // the chunk's entries, once, coalesced; padded with 0 (mask 0)
+    const uint32_t* plan = a.plan + (static_cast<size_t>(unit) * a.S + split) * kPlanCap;
     const int padded = nslices * 16;
     for (int i = threadIdx.x; i < padded; i += blockDim.x)
-      s_plan[i] = (e0 + i < e1) ? __ldg(plan + e0 + i) : 0u;
+      s_plan[i] = (i < e1) ? __ldg(plan + i) : 0u;
     __syncthreads();
   }
   const __nv_bfloat16* kbase =
@@ -665,16 +674,21 @@ int decode_chunk_dense(int units, int N) {
   return (chunk + 63) & ~63;
 }
 
-int decode_splits_union(int units, int G, int topk) {
+// Key-range chunks of the reuse decode: R keys (multiple of 32, at most
+// kPlanCap so a chunk's union fits the shared staging area), about four
+// waves of CTAs over 152 SMs x 2.
+int decode_union_range(int units, int N) {
   int s = (kTargetCtas + units - 1) / units;
-  const int max_by_len = (G * topk + 255) / 256;
-  if (s > max_by_len) s = max_by_len;
-  // each split's plan entries must fit the shared staging area
-  const int min_for_cap = (G * topk + kPlanCap - 16 - 1) / (kPlanCap - 16);
-  if (s < min_for_cap) s = min_for_cap;
-  if (s > kMaxSplits) return -1;
   if (s < 1) s = 1;
-  return s;
+  int R = (N + s - 1) / s;
+  R = (R + 31) & ~31;
+  if (R > kPlanCap) R = kPlanCap;
+  if (R < 256) R = 256;
+  return R;
+}
+int decode_union_chunks(int units, int N) {
+  const int R = decode_union_range(units, N);
+  return (N + R - 1) / R;
 }
 
 cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spill,
@@ -696,12 +710,11 @@ cudaError_t launch_decode_union_bf16(const DecodeArgs& a, int head_dim, cudaStre
 
 cudaError_t launch_build_union_plan(const DecodeArgs& a, uint32_t* plan, int32_t* plan_count,
                                     cudaStream_t st) {
-  const size_t smem = static_cast<size_t>(a.G) * ((a.N + 31) / 32) * 4;
-  cudaError_t e = cudaFuncSetAttribute(k_build_union_plan,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  k_build_union_plan<<<a.B * a.Hkv, 1024, smem, st>>>(a, plan, plan_count);
+  if (a.G > 8) return cudaErrorInvalidValue;
+  const int R = decode_union_range(a.B * a.Hkv, a.N);
+  const int S = (a.N + R - 1) / R;
+  if (S > kMaxSplits) return cudaErrorNotSupported;
+  k_build_union_plan<<<dim3(S, a.B * a.Hkv), 256, 0, st>>>(a, plan, plan_count, R);
   return cudaGetLastError();
 }
 

@@ -20,8 +20,8 @@ struct DecodeArgs {
   float* part;              // [B*Hq][S][d+4]: m (log2 units), l, -, -, o[d]
   unsigned int* counters;   // [B*Hkv] split arrival counters (self-resetting)
   unsigned int* err;        // workspace error word
-  const uint32_t* plan;     // union plan [B*Hkv][plan_stride]: key | mask << 24
-  const int32_t* plan_count;  // [B*Hkv]
+  const uint32_t* plan;     // union plan [B*Hkv][chunks][2048]: key | mask << 24
+  const int32_t* plan_count;  // [B*Hkv][chunks]
   const int32_t* idx;       // per-head sets [B,Hq,topk] (generic sparse path)
   int plan_stride;          // G * topk
   int topk;
@@ -44,7 +44,9 @@ cudaError_t launch_build_union_plan(const DecodeArgs& a, uint32_t* plan, int32_t
 cudaError_t launch_decode_generic(const DecodeArgs& a, int head_dim, int dtype, DecodeKind kind,
                                   cudaStream_t st);
 int decode_chunk_dense(int units, int N);        // keys per split (multiple of 64)
-int decode_splits_union(int units, int G, int topk);
+int decode_union_range(int units, int N);    // keys per reuse chunk
+int decode_union_chunks(int units, int N);   // reuse CTAs per (sequence, KV head)
+constexpr int kPlanCapEntries = 2048;        // union entries per chunk
 
 // topk.cu
 struct TopkArgs {

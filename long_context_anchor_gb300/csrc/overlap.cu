@@ -76,7 +76,7 @@ extern "C" {
 size_t kascade_overlap_workspace_size(int32_t n_layers, int32_t units, int32_t n_bits) {
   if (n_layers < 1 || units < 1 || n_bits < 1) return 0;
   const size_t words = (static_cast<size_t>(n_bits) + 31) / 32;
-  return sizeof(kascade::WsHeader) + static_cast<size_t>(n_layers) * units * words * 4;
+  return kascade::kWsStateBytes + static_cast<size_t>(n_layers) * units * words * 4;
 }
 
 kascade_status kascade_layer_overlap(const int32_t* sets, int32_t n_layers, int32_t units,
@@ -91,7 +91,7 @@ kascade_status kascade_layer_overlap(const int32_t* sets, int32_t n_layers, int3
   char* base = static_cast<char*>(ws);
   cudaError_t e = kascade::launch_layer_overlap(
       sets, n_layers, units, topk, n_bits, reinterpret_cast<long long*>(counts_out),
-      reinterpret_cast<uint32_t*>(base + sizeof(kascade::WsHeader)),
+      reinterpret_cast<uint32_t*>(base + kascade::kWsStateBytes),
       reinterpret_cast<unsigned int*>(base), static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? KASCADE_OK : KASCADE_ERR_CUDA;
 }

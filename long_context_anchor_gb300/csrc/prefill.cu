@@ -3,9 +3,11 @@
 // one index set per (head, 128-query tile)).
 //
 //   k_prefill_fa<REUSE, LSE>  one CTA per (sequence, query head, 128-row tile):
-//       a TMA producer warp streams the Q tile and 128-key K/V tiles (dense:
-//       key tiles 0..t, causal; reuse: the tile's saved keys, gathered four
-//       rows per TMA tile::gather4), one thread issues tcgen05.mma
+//       a TMA producer warp streams the Q tile and, for dense/anchor layers,
+//       the causal 128-key K/V tiles 0..t; for reuse layers two warps gather
+//       the tile's saved K/V rows in 64-key chunks (16-byte cp.async into the
+//       128-byte-swizzled layout, four chunks in flight, then
+//       fence.proxy.async before signalling the MMA); one thread issues tcgen05.mma
 //       S = Q K^T into double-buffered TMEM and O += P V, and a softmax
 //       warpgroup (one thread per query row) runs the online softmax with a
 //       lazy O rescale (only when a row maximum grows by more than 2^8),
@@ -34,25 +36,30 @@ constexpr int kFaThreads = 256;         // warp 0 TMA, warp 1 MMA, warps 4-7 sof
 constexpr float kRescaleLog2 = 8.0f;    // lazy O rescale threshold (factor 256)
 #define kNegInfP (-CUDART_INF_F)
 
-struct FaSmem {
-  // 1024-aligned tile region (offsets from the aligned base)
+// Shared-memory plan of k_prefill_fa for KC-key chunks and an ST-deep K/V ring.
+template <int KC, int ST>
+struct FaCfg {
+  static constexpr int KHALF = KC * 128;          // one 64-dim half of a K (or V) chunk
+  static constexpr int KV_BYTES = 2 * KHALF;      // one K (or V) chunk, 128 dims
+  static constexpr int P_BYTES = kTile * KC * 2;  // P tile, bf16
   static constexpr int Q = 0;
-  static constexpr int K0 = Q + kTileBytes;          // K[2]
-  static constexpr int V0 = K0 + 2 * kTileBytes;     // V[2]
-  static constexpr int P = V0 + 2 * kTileBytes;
-  static constexpr int POS = P + kTileBytes;         // int32 [2][128] key positions
-  static constexpr int BAR = POS + 2 * kTile * 4;    // mbarriers
-  static constexpr int TMEM = BAR + 16 * 8;
+  static constexpr int K0 = Q + kTileBytes;
+  static constexpr int V0 = K0 + ST * KV_BYTES;
+  static constexpr int P = V0 + ST * KV_BYTES;
+  static constexpr int POS = P + P_BYTES;          // int32 [ST][KC] key positions
+  static constexpr int BAR = POS + ST * KC * 4;
+  static constexpr int TMEM = BAR + 32 * 8;
   static constexpr int BYTES = TMEM + 16;
+  static constexpr size_t SMEM = BYTES + 1024;
 };
-constexpr size_t kFaSmemBytes = FaSmem::BYTES + 1024;
 
-// tcgen05 descriptors of the 128x128 tiles (see tc.cuh).
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
-  return sw128_desc(tile + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+// tcgen05 descriptors (see tc.cuh): K-major tiles with `half` bytes per
+// 64-column half; V as an MN-major B operand with `half` bytes per 64 dims.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk, int half = kHalf) {
+  return sw128_desc(tile + (kk >> 2) * half + (kk & 3) * 32, 16, 1024);
 }
-__device__ __forceinline__ uint64_t vmn_desc(uint32_t tile, int kk) {
-  return sw128_desc(tile + kk * 2048, kHalf, 1024);
+__device__ __forceinline__ uint64_t vmn_desc(uint32_t tile, int kk, int half = kHalf) {
+  return sw128_desc(tile + kk * 2048, half, 1024);
 }
 
 // Work order: longest tiles (largest t) first.
@@ -62,25 +69,31 @@ __device__ __forceinline__ void fa_tile_coords(const PrefillArgs& a, int& bh, in
   t = a.nT - 1 - static_cast<int>(blockIdx.x) / BH;
 }
 
-template <bool REUSE, bool LSE>
+// REUSE: keys come from the tile's saved set (gathered by warps 2-3 with
+// 16-byte cp.async into the swizzled layout, then fence.proxy.async);
+// otherwise the causal key tiles 0..t stream in by TMA (warp 0).
+// LSE: also store the row log-sum-exp (log2 units) for the tile weights.
+template <bool REUSE, bool LSE, int KC, int ST>
 __global__ void __launch_bounds__(kFaThreads, 1)
     k_prefill_fa(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillArgs a) {
+  using C = FaCfg<KC, ST>;
+  constexpr int LA = ST / 2;   // cp.async chunks kept in flight before signalling
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  int32_t* s_pos = reinterpret_cast<int32_t*>(sm + FaSmem::POS);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + FaSmem::BAR);
+  int32_t* s_pos = reinterpret_cast<int32_t*>(sm + C::POS);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + C::BAR);
   uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;   // [2]
-  uint64_t* kv_free = bar + 3;   // [2]
-  uint64_t* s_full = bar + 5;    // [2]
-  uint64_t* s_free = bar + 7;    // [2]
-  uint64_t* p_full = bar + 9;
-  uint64_t* pv_done = bar + 10;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + FaSmem::TMEM);
-  const uint32_t sQ = smem_u32(sm + FaSmem::Q), sK0 = smem_u32(sm + FaSmem::K0);
-  const uint32_t sV0 = smem_u32(sm + FaSmem::V0), sP = smem_u32(sm + FaSmem::P);
+  uint64_t* kv_full = bar + 1;          // [ST]
+  uint64_t* kv_free = bar + 1 + ST;     // [ST]
+  uint64_t* s_full = bar + 1 + 2 * ST;  // [2]
+  uint64_t* s_free = s_full + 2;        // [2]
+  uint64_t* p_full = s_free + 2;
+  uint64_t* pv_done = p_full + 1;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + C::TMEM);
+  const uint32_t sQ = smem_u32(sm + C::Q), sK0 = smem_u32(sm + C::K0);
+  const uint32_t sV0 = smem_u32(sm + C::V0), sP = smem_u32(sm + C::P);
 
   int bh, t;
   fa_tile_coords(a, bh, t);
@@ -91,18 +104,21 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   const int32_t* idx_row = nullptr;
   if (REUSE) {
     kt = min(a.topk, L);
-    nkv = (kt + kTile - 1) / kTile;
+    nkv = (kt + KC - 1) / KC;
     idx_row = a.idx + (static_cast<size_t>(bh) * a.nT + t) * a.topk;
   } else {
-    nkv = (L + kTile - 1) / kTile;
+    nkv = (L + KC - 1) / KC;
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kv_row_base = (b * a.Hkv + g) * a.N;
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(kv_full + s, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(kv_full + s, REUSE ? 64 : 1);
       mbar_init(kv_free + s, 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(s_full + s, 1);
       mbar_init(s_free + s, 128);
     }
@@ -118,99 +134,105 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   const uint32_t tS = tmem, tO = tmem + 256;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
-    const int kv_row_base = (b * a.Hkv + g) * a.N;
+    // ------------------------------------------------ TMA: Q, and dense K/V
     if (lane == 0) {
       prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmV);
       mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_2d(sm + FaSmem::Q, &tmQ, q_full, 0, bh * a.N + row0);
-      tma_load_2d(sm + FaSmem::Q + kHalf, &tmQ, q_full, 64, bh * a.N + row0);
+      tma_load_2d(sm + C::Q, &tmQ, q_full, 0, bh * a.N + row0);
+      tma_load_2d(sm + C::Q + kHalf, &tmQ, q_full, 64, bh * a.N + row0);
+      if (!REUSE) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        int issued = 0;
+        for (int j = 0; j < nkv; ++j) {
+          const int s = j % ST;
+          if (!mbar_wait(kv_free + s, ((j / ST) & 1) ^ 1, a.err, 0x601)) break;
+          unsigned char* kd = sm + C::K0 + s * C::KV_BYTES;
+          unsigned char* vd = sm + C::V0 + s * C::KV_BYTES;
+          mbar_arrive_expect_tx(kv_full + s, 2 * C::KV_BYTES);
+          const int y = kv_row_base + j * KC;
+          tma_load_2d(kd, &tmK, kv_full + s, 0, y);
+          tma_load_2d(kd + C::KHALF, &tmK, kv_full + s, 64, y);
+          tma_load_2d(vd, &tmV, kv_full + s, 0, y);
+          tma_load_2d(vd + C::KHALF, &tmV, kv_full + s, 64, y);
+          issued = j + 1;
+        }
+        for (int j = issued > ST ? issued - ST : 0; j < issued; ++j)
+          mbar_wait(kv_full + (j % ST), (j / ST) & 1, a.err, 0x604);
+      }
+      mbar_wait(q_full, 0, a.err, 0x603);   // never leave with copies in flight
     }
+  } else if (REUSE && (warp == 2 || warp == 3)) {
+    // ------------------------------------------------ gather producer (64 threads, one key row each)
+    static_assert(!REUSE || KC == 64, "one gathered row per producer thread");
+    const int pt = threadIdx.x - 64;
+    int p_first = __ldg(idx_row);
+    if (p_first < 0 || p_first >= a.N) p_first = 0;
+    const __nv_bfloat16* kbase = static_cast<const __nv_bfloat16*>(a.k);
+    const __nv_bfloat16* vbase = static_cast<const __nv_bfloat16*>(a.v);
     int issued = 0;
     for (int j = 0; j < nkv; ++j) {
-      const int s = j & 1;
-      int ok = 1;
-      if (lane == 0) ok = mbar_wait(kv_free + s, ((j >> 1) & 1) ^ 1, a.err, 0x601);
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      unsigned char* kd = sm + FaSmem::K0 + s * kTileBytes;
-      unsigned char* vd = sm + FaSmem::V0 + s * kTileBytes;
-      if (!REUSE) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(kv_full + s, 2 * kTileBytes);
-          const int y = kv_row_base + j * kTile;
-          tma_load_2d(kd, &tmK, kv_full + s, 0, y);
-          tma_load_2d(kd + kHalf, &tmK, kv_full + s, 64, y);
-          tma_load_2d(vd, &tmV, kv_full + s, 0, y);
-          tma_load_2d(vd + kHalf, &tmV, kv_full + s, 64, y);
-        }
-      } else {
-        // Padding slots (and invalid entries) gather the tile's first saved
-        // row, which is selected anyway, and are masked in the softmax; rows
-        // outside the saved set are never read.
-        int p_first = __ldg(idx_row);
-        if (p_first < 0 || p_first >= a.N) p_first = 0;
-        int rows[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int e = j * kTile + lane * 4 + u;
-          int p = e < kt ? __ldg(idx_row + e) : -1;
-          if (p >= a.N || (e < kt && p < 0)) {
-            report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x602);
-            p = -1;
-          }
-          s_pos[s * kTile + lane * 4 + u] = p;
-          rows[u] = kv_row_base + (p >= 0 ? p : p_first);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(kv_full + s, 2 * kTileBytes);
-        __syncwarp();
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          tma_gather4(kd + hf * kHalf + lane * 512, &tmK, kv_full + s, hf * 64, rows[0], rows[1],
-                      rows[2], rows[3]);
-          tma_gather4(vd + hf * kHalf + lane * 512, &tmV, kv_full + s, hf * 64, rows[0], rows[1],
-                      rows[2], rows[3]);
-        }
+      const int s = j % ST;
+      if (!mbar_wait(kv_free + s, ((j / ST) & 1) ^ 1, a.err, 0x605)) break;
+      const int e = j * KC + pt;
+      int p = e < kt ? __ldg(idx_row + e) : -1;
+      if (p >= a.N || (e < kt && p < 0)) {
+        report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x602);
+        p = -1;
       }
+      s_pos[s * KC + pt] = p;
+      // padding slots re-read the tile's first saved row (masked later)
+      const size_t row = static_cast<size_t>(kv_row_base) + (p >= 0 ? p : p_first);
+      const __nv_bfloat16* ks = kbase + row * 128;
+      const __nv_bfloat16* vs = vbase + row * 128;
+      unsigned char* kd = sm + C::K0 + s * C::KV_BYTES;
+      unsigned char* vd = sm + C::V0 + s * C::KV_BYTES;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int off = (c >> 3) * C::KHALF + pt * 128 + (((c & 7) ^ (pt & 7)) << 4);
+        cp_async16(kd + off, ks + c * 8, 16);
+        cp_async16(vd + off, vs + c * 8, 16);
+      }
+      cp_async_commit();
       issued = j + 1;
+      if (j >= LA) {
+        cp_async_wait<LA>();
+        fence_proxy_async_smem();
+        mbar_arrive(kv_full + (j - LA) % ST);
+      }
     }
-    // Never leave with copies in flight.
-    if (lane == 0) {
-      mbar_wait(q_full, 0, a.err, 0x603);
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-        mbar_wait(kv_full + (j & 1), (j >> 1) & 1, a.err, 0x604);
-    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    for (int j = issued > LA ? issued - LA : 0; j < issued; ++j) mbar_arrive(kv_full + j % ST);
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idq = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t idq = idesc_bf16_f32(128, KC, 0, 0);
       constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
       bool ok = mbar_wait(q_full, 0, a.err, 0x611);
       auto issue_pv = [&](int jj) {
-        const int s = jj & 1;
+        const int s = jj % ST;
         if (!mbar_wait(p_full, jj & 1, a.err, 0x612)) return false;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma(tO, kmajor_desc(sP, kk), vmn_desc(sV0 + s * kTileBytes, kk), idv,
+        for (int kk = 0; kk < KC / 16; ++kk)
+          tc_mma(tO, kmajor_desc(sP, kk), vmn_desc(sV0 + s * C::KV_BYTES, kk, C::KHALF), idv,
                  (jj > 0 || kk > 0) ? 1u : 0u);
         tc_commit(pv_done);
         tc_commit(kv_free + s);
         return true;
       };
       for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j & 1;
-        ok = mbar_wait(kv_full + s, (j >> 1) & 1, a.err, 0x613) &&
-             mbar_wait(s_free + s, ((j >> 1) & 1) ^ 1, a.err, 0x614);
+        const int s = j % ST, sb = j & 1;
+        ok = mbar_wait(kv_full + s, (j / ST) & 1, a.err, 0x613) &&
+             mbar_wait(s_free + sb, ((j >> 1) & 1) ^ 1, a.err, 0x614);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma(tS + s * 128, kmajor_desc(sQ, kk), kmajor_desc(sK0 + s * kTileBytes, kk), idq,
-                 kk > 0 ? 1u : 0u);
-        tc_commit(s_full + s);
+          tc_mma(tS + sb * 128, kmajor_desc(sQ, kk),
+                 kmajor_desc(sK0 + s * C::KV_BYTES, kk, C::KHALF), idq, kk > 0 ? 1u : 0u);
+        tc_commit(s_full + sb);
         if (j > 0) ok = issue_pv(j - 1);
       }
       if (ok && nkv > 0) issue_pv(nkv - 1);
@@ -223,29 +245,37 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     float m_used = kNegInfP, l = 0.f;
     bool ok = true;
     for (int j = 0; j < nkv; ++j) {
-      const int s = j & 1;
-      ok = mbar_wait(s_full + s, (j >> 1) & 1, a.err, 0x621);
+      const int sb = j & 1, s = j % ST;
+      ok = mbar_wait(s_full + sb, (j >> 1) & 1, a.err, 0x621);
       if (!ok) break;
       tc_fence_after();
-      float x[128];
+      float x[KC];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < KC / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tS + s * 128 + c * 32 + lane_base, v);
+        tmem_ld32(tS + sb * 128 + c * 32 + lane_base, v);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
       }
       tc_fence_before();
-      mbar_arrive(s_free + s);
+      mbar_arrive(s_free + sb);
+      // raw-score maximum; the causal mask is needed only where keys can
+      // exceed this row (dense: the diagonal tile; reuse: every chunk)
+      const bool need_mask = REUSE || (j * KC + KC - 1 > row0);
       float tmax = kNegInfP;
+      if (need_mask) {
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const int kp = REUSE ? s_pos[s * kTile + c] : j * kTile + c;
-        const bool valid = kp >= 0 && kp <= i;
-        x[c] = valid ? x[c] * a.scale_log2 : kNegInfP;
-        tmax = fmaxf(tmax, x[c]);
+        for (int c = 0; c < KC; ++c) {
+          const int kp = REUSE ? s_pos[s * KC + c] : j * KC + c;
+          if (!(kp >= 0 && kp <= i)) x[c] = kNegInfP;
+          tmax = fmaxf(tmax, x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < KC; ++c) tmax = fmaxf(tmax, x[c]);
       }
+      tmax *= a.scale_log2;   // scale > 0: max commutes with scaling
       float alpha = 1.f;
       bool resc = false;
       if (tmax > m_used + kRescaleLog2) {
@@ -257,10 +287,11 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         m_used = tmax;
       }
       const float mu = (m_used == kNegInfP) ? 0.f : m_used;
-      uint32_t pk[64];
+      uint32_t pk[KC / 2];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float p0 = ex2_approx(x[2 * c] - mu), p1 = ex2_approx(x[2 * c + 1] - mu);
+      for (int c = 0; c < KC / 2; ++c) {
+        const float p0 = ex2_approx(fmaf(x[2 * c], a.scale_log2, -mu));
+        const float p1 = ex2_approx(fmaf(x[2 * c + 1], a.scale_log2, -mu));
         l += p0 + p1;
         pk[c] = pack_bf16(p0, p1);
       }
@@ -283,9 +314,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
       }
       // P row -> shared memory, K-major 128-byte-swizzled (A operand of P V)
 #pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        const uint32_t addr =
-            sP + (ch >> 3) * kHalf + r * 128 + ((((ch & 7) ^ (r & 7))) << 4);
+      for (int ch = 0; ch < KC / 8; ++ch) {
+        const uint32_t addr = sP + (ch >> 3) * kHalf + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[4 * ch]),
                      "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
                      : "memory");
@@ -328,6 +358,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     tmem_dealloc(tmem, 512);
   }
 }
+
 
 // ------------------------------------------------------------------------
 // Anchor pass 2: tile weights from S^T = K_j Q_t^T (TMEM lane = key).
@@ -463,26 +494,27 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   }
 }
 
+// Q tiles of 128 rows; K/V tiles of kv_rows rows (2-D maps over all heads).
 bool make_maps(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUtensorMap* tv,
-               bool gather) {
+               int kv_rows) {
   const uint64_t qrows = static_cast<uint64_t>(a.B) * a.Hq * a.N;
   const uint64_t kvrows = static_cast<uint64_t>(a.B) * a.Hkv * a.N;
   if (tq && !encode_tmap_2d_bf16(tq, a.q, 128, qrows, 64, kTile, true)) return false;
-  const uint32_t box_rows = gather ? 1 : kTile;
-  if (tk && !encode_tmap_2d_bf16(tk, a.k, 128, kvrows, 64, box_rows, true)) return false;
-  if (tv && !encode_tmap_2d_bf16(tv, a.v, 128, kvrows, 64, box_rows, true)) return false;
+  if (tk && !encode_tmap_2d_bf16(tk, a.k, 128, kvrows, 64, kv_rows, true)) return false;
+  if (tv && !encode_tmap_2d_bf16(tv, a.v, 128, kvrows, 64, kv_rows, true)) return false;
   return true;
 }
 
-template <bool REUSE, bool LSE>
+template <bool REUSE, bool LSE, int KC, int ST>
 cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
   alignas(64) CUtensorMap tq, tk, tv;
-  if (!make_maps(a, &tq, &tk, &tv, REUSE)) return cudaErrorInvalidValue;
-  auto kern = k_prefill_fa<REUSE, LSE>;
+  if (!make_maps(a, &tq, &tk, &tv, KC)) return cudaErrorInvalidValue;
+  auto kern = k_prefill_fa<REUSE, LSE, KC, ST>;
+  const size_t smem = FaCfg<KC, ST>::SMEM;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(kFaSmemBytes));
+                                       static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<a.B * a.Hq * a.nT, kFaThreads, kFaSmemBytes, st>>>(tq, tk, tv, a);
+  kern<<<a.B * a.Hq * a.nT, kFaThreads, smem, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
@@ -490,18 +522,18 @@ cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
 
 cudaError_t launch_prefill_dense(const PrefillArgs& a, int head_dim, cudaStream_t st) {
   if (head_dim != 128) return cudaErrorNotSupported;
-  return launch_fa<false, false>(a, st);
+  return launch_fa<false, false, 128, 2>(a, st);
 }
 
 cudaError_t launch_prefill_lse(const PrefillArgs& a, int head_dim, cudaStream_t st) {
   if (head_dim != 128) return cudaErrorNotSupported;
-  return launch_fa<false, true>(a, st);   // exact output + row LSE
+  return launch_fa<false, true, 128, 2>(a, st);   // exact output + row LSE
 }
 
 cudaError_t launch_prefill_anchor_main(const PrefillArgs& a, int head_dim, cudaStream_t st) {
   if (head_dim != 128) return cudaErrorNotSupported;
   alignas(64) CUtensorMap tq, tk;
-  if (!make_maps(a, &tq, &tk, nullptr, false)) return cudaErrorInvalidValue;
+  if (!make_maps(a, &tq, &tk, nullptr, kTile)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(k_prefill_weights,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kWtSmemBytes));
@@ -512,7 +544,7 @@ cudaError_t launch_prefill_anchor_main(const PrefillArgs& a, int head_dim, cudaS
 
 cudaError_t launch_prefill_reuse(const PrefillArgs& a, int head_dim, cudaStream_t st) {
   if (head_dim != 128) return cudaErrorNotSupported;
-  return launch_fa<true, false>(a, st);
+  return launch_fa<true, false, 64, 4>(a, st);
 }
 
 }  // namespace kascade

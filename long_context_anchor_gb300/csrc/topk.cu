@@ -4,20 +4,19 @@
 // ascending positions.
 //
 // One 1024-thread CTA per row, two CTAs per SM; scores become order-
-// preserving uint32 keys on the fly. Typical cost is two coalesced passes
-// over the row (the second mostly from L2):
-//   A. histogram of the top 11 key bits (warp-aggregated shared atomics);
-//      the bin holding the k-th key is found by a block scan. If that bin is
-//      too large for the candidate list, further 11/10-bit digit passes over
-//      the row narrow the prefix first;
-//   B. marking pass: every 32 consecutive positions give one 32-bit word of
-//      "key above the prefix" by a warp ballot (a bitmap, no atomics); keys
-//      inside the prefix are compacted into a shared candidate list (or,
-//      when the prefix is already the full key, marked in an "equal" bitmap);
-//   C. the remaining digits run on the candidates only, giving the k-th key
-//      T; candidates > T join the "above" bitmap, candidates == T the
-//      "equal" bitmap;
-//   D. ordered emission: a block scan over per-thread word runs gives each
+// preserving uint32 keys on the fly.
+//   1. bracket: an evenly spaced sample of the row (len/16 keys, 2048..8192)
+//      is staged in shared memory and exact rank selection on it gives two
+//      thresholds t_hi >= (k-th key) >= t_lo with a safety margin of four
+//      binomial standard deviations around the expected sample rank;
+//   2. one coalesced pass over the row: a warp ballot per 32 positions gives
+//      the bitmap of keys above t_hi (no atomics), and keys in [t_lo, t_hi]
+//      are compacted into a shared candidate list;
+//   3. if the bracket holds the k-th key, exact rank selection among the
+//      candidates gives T; candidates > T join the "above" bitmap, == T the
+//      "equal" bitmap. Otherwise (heavy ties, an unlucky sample) the exact
+//      fallback runs 11/11/10-bit radix digit passes over the row;
+//   4. ordered emission: a block scan over per-thread word runs gives each
 //      thread its output offset; keys == T are taken in position order until
 //      k positions are written.
 // Prefill rows are the packed tile weights of one (sequence, head, tile):
@@ -34,6 +33,7 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCandCap = 4096;   // candidate (key, position) pairs in shared memory
 constexpr int kUnroll = 8;       // 32-position chunks in flight per warp
+constexpr int kSampleCap = 8192; // evenly spaced sample used to bracket the k-th key
 
 struct RowDesc {
   const float* ptr;
@@ -113,16 +113,67 @@ __device__ __forceinline__ void for_row(const RowDesc& rd, bool& bad, F f) {
   }
 }
 
+// Bin holding rank `need` (1 = largest) of an nb-bin histogram, counting from
+// the top bin down; returns the bin and the count in the bins above it.
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, int* warp_tot,
+                                         int* s_bin, int* s_above, int& bin, int& above) {
+  const int tid = threadIdx.x;
+  const int b_hi = nb - 1 - 2 * tid;   // this thread owns bins b_hi, b_hi-1
+  const int h0 = b_hi >= 0 ? static_cast<int>(hist[b_hi]) : 0;
+  const int h1 = b_hi >= 1 ? static_cast<int>(hist[b_hi - 1]) : 0;
+  const int excl = block_incl_scan(h0 + h1, warp_tot) - h0 - h1;
+  if (b_hi >= 0) {
+    if (excl < need && need <= excl + h0) {
+      *s_bin = b_hi;
+      *s_above = excl;
+    } else if (b_hi >= 1 && excl + h0 < need && need <= excl + h0 + h1) {
+      *s_bin = b_hi - 1;
+      *s_above = excl + h0;
+    }
+  }
+  __syncthreads();
+  bin = *s_bin;
+  above = *s_above;
+  __syncthreads();
+}
+
+// Exact rank selection on a shared-memory key list: the key of rank `rank`
+// (1 = largest) and the number of list keys strictly greater than it.
+__device__ void select_rank(const uint32_t* list, int n, int rank, uint32_t* hist, int* warp_tot,
+                            int* s_bin, int* s_above, uint32_t& key_out, int& greater) {
+  uint32_t prefix = 0, pmask = 0;
+  int gt = 0;
+  for (int d = 0; d < 3; ++d) {
+    const int nb = d < 2 ? 2048 : 1024;
+    const int sh = d == 0 ? 21 : (d == 1 ? 10 : 0);
+    for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t key = list[i];
+      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    int bin, above;
+    find_bin(hist, nb, rank - gt, warp_tot, s_bin, s_above, bin, above);
+    gt += above;
+    prefix |= static_cast<uint32_t>(bin) << sh;
+    pmask |= static_cast<uint32_t>(nb - 1) << sh;
+  }
+  key_out = prefix;
+  greater = gt;
+}
+
 __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ TopkArgs a,
                                                       int words_cap) {
   extern __shared__ uint32_t sm[];
   uint32_t* hist = sm;                                                     // [2048]
   uint32_t* cand_key = hist + 2048;                                        // [kCandCap]
   int32_t* cand_pos = reinterpret_cast<int32_t*>(cand_key + kCandCap);     // [kCandCap]
-  uint32_t* above = reinterpret_cast<uint32_t*>(cand_pos + kCandCap);      // [words_cap]
+  uint32_t* samp = reinterpret_cast<uint32_t*>(cand_pos + kCandCap);       // [kSampleCap]
+  uint32_t* above = samp + kSampleCap;                                     // [words_cap]
   uint32_t* eqbm = above + words_cap;                                      // [words_cap]
   __shared__ int warp_tot[32];
-  __shared__ int s_ncand, s_bin, s_above;
+  __shared__ int s_ncand, s_nabove, s_bin, s_above;
 
   const int r = blockIdx.x;
   const RowDesc rd = row_desc(a, r);
@@ -135,116 +186,101 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
   }
   const int W = (rd.len + 31) >> 5;
   for (int w = tid; w < W; w += kThreads) above[w] = eqbm[w] = 0u;
-  if (tid == 0) s_ncand = 0;
-
-  // A. digit histograms over the row until the k-th key's bin fits the
-  //    candidate list (usually after the first digit) or the key is complete.
-  uint32_t prefix = 0, pmask = 0;
-  int c_gt = 0, d = 0;
-  bool bad = false;
-  while (true) {
-    const int nb = d < 2 ? 2048 : 1024;
-    const int sh = d == 0 ? 21 : (d == 1 ? 10 : 0);
-    for (int i = tid; i < nb; i += kThreads) hist[i] = 0u;
-    __syncthreads();
-    for_row(rd, bad, [&](int, bool valid, uint32_t key) {
-      hist_add(hist, valid && (key & pmask) == prefix, (key >> sh) & (nb - 1));
-    });
-    __syncthreads();
-    const int need = rd.k - c_gt;
-    const int b_hi = nb - 1 - 2 * tid;   // this thread owns bins b_hi, b_hi-1
-    const int h0 = b_hi >= 0 ? static_cast<int>(hist[b_hi]) : 0;
-    const int h1 = b_hi >= 1 ? static_cast<int>(hist[b_hi - 1]) : 0;
-    const int excl = block_incl_scan(h0 + h1, warp_tot) - h0 - h1;
-    if (b_hi >= 0) {
-      if (excl < need && need <= excl + h0) {
-        s_bin = b_hi;
-        s_above = excl;
-      } else if (b_hi >= 1 && excl + h0 < need && need <= excl + h0 + h1) {
-        s_bin = b_hi - 1;
-        s_above = excl + h0;
-      }
-    }
-    __syncthreads();
-    const int bin = s_bin;
-    c_gt += s_above;
-    prefix |= static_cast<uint32_t>(bin) << sh;
-    pmask |= static_cast<uint32_t>(nb - 1) << sh;
-    const int cnt = static_cast<int>(hist[bin]);
-    ++d;
-    __syncthreads();
-    if (d == 3 || cnt <= kCandCap) break;
+  if (tid == 0) {
+    s_ncand = 0;
+    s_nabove = 0;
   }
-  if (__syncthreads_or(bad) && tid == 0) report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x401);
 
-  // B. marking pass: ballot bitmaps of keys above the prefix; candidates
-  //    inside it (or, with a complete prefix, the "equal" bitmap).
-  const bool full = d == 3;
+  // ---- 1. bracket the k-th key from an evenly spaced sample -------------
+  const int S = min(rd.len, max(2048, min(kSampleCap, rd.len / 16)));
+  for (int u = tid; u < S; u += kThreads) {
+    const int j = static_cast<int>((static_cast<long long>(u) * rd.len) / S);
+    samp[u] = float_key(__ldg(rd.ptr + j));
+  }
+  __syncthreads();
+  const float rc = static_cast<float>(rd.k) * S / rd.len;   // expected sample rank
+  const float margin = 4.f * sqrtf(rc) + 16.f;
+  const int r_hi = static_cast<int>(floorf(rc - margin));
+  const int r_lo = static_cast<int>(ceilf(rc + margin));
+  uint32_t t_hi = 0xFFFFFFFFu, t_lo = 0u;
+  int dummy;
+  if (r_hi >= 1) select_rank(samp, S, r_hi, hist, warp_tot, &s_bin, &s_above, t_hi, dummy);
+  if (r_lo <= S) select_rank(samp, S, r_lo, hist, warp_tot, &s_bin, &s_above, t_lo, dummy);
+
+  // ---- 2. one pass: "above" bitmap by ballot, candidates in [t_lo, t_hi] --
+  bool bad = false;
+  int my_above = 0;
   for_row(rd, bad, [&](int j, bool valid, uint32_t key) {
-    const uint32_t hi = key & pmask;
-    const bool in = valid && hi == prefix;
-    const unsigned int ba = __ballot_sync(0xffffffffu, valid && hi > prefix);
+    const bool ab = valid && key > t_hi;
+    const bool in = valid && key >= t_lo && key <= t_hi;
+    const unsigned int ba = __ballot_sync(0xffffffffu, ab);
     const unsigned int bi = __ballot_sync(0xffffffffu, in);
     if (lane == 0 && j < rd.len) {
       above[j >> 5] = ba;
-      if (full) eqbm[j >> 5] = bi;
+      my_above += __popc(ba);
     }
-    if (!full && bi) {
+    if (bi) {
       int base = 0;
       if (lane == 0) base = atomicAdd(&s_ncand, __popc(bi));
       base = __shfl_sync(0xffffffffu, base, 0);
       if (in) {
         const int p = base + __popc(bi & ((1u << lane) - 1u));
-        cand_key[p] = key;
-        cand_pos[p] = j;
+        if (p < kCandCap) {
+          cand_key[p] = key;
+          cand_pos[p] = j;
+        }
       }
     }
   });
-  __syncthreads();
-
-  // C. remaining digits on the candidates; mark them against T.
-  if (!full) {
-    const int nc = s_ncand;
-    for (; d < 3; ++d) {
-      const int nb = d < 2 ? 2048 : 1024;
-      const int sh = d == 1 ? 10 : 0;
-      for (int i = tid; i < nb; i += kThreads) hist[i] = 0u;
-      __syncthreads();
-      for (int i = tid; i < nc; i += kThreads) {
-        const uint32_t key = cand_key[i];
-        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
-      }
-      __syncthreads();
-      const int need = rd.k - c_gt;
-      const int b_hi = nb - 1 - 2 * tid;
-      const int h0 = b_hi >= 0 ? static_cast<int>(hist[b_hi]) : 0;
-      const int h1 = b_hi >= 1 ? static_cast<int>(hist[b_hi - 1]) : 0;
-      const int excl = block_incl_scan(h0 + h1, warp_tot) - h0 - h1;
-      if (b_hi >= 0) {
-        if (excl < need && need <= excl + h0) {
-          s_bin = b_hi;
-          s_above = excl;
-        } else if (b_hi >= 1 && excl + h0 < need && need <= excl + h0 + h1) {
-          s_bin = b_hi - 1;
-          s_above = excl + h0;
-        }
-      }
-      __syncthreads();
-      c_gt += s_above;
-      prefix |= static_cast<uint32_t>(s_bin) << sh;
-      pmask |= static_cast<uint32_t>(nb - 1) << sh;
-      __syncthreads();
-    }
-    for (int i = tid; i < nc; i += kThreads) {
+  if (lane == 0 && my_above) atomicAdd(&s_nabove, my_above);
+  if (__syncthreads_or(bad) && tid == 0) report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x401);
+  const int n_above = s_nabove, n_cand = s_ncand;
+  int c_gt;
+  if (n_above < rd.k && n_above + n_cand >= rd.k && n_cand <= kCandCap) {
+    // ---- 3. exact k-th key among the candidates -------------------------
+    uint32_t T;
+    int cg;
+    select_rank(cand_key, n_cand, rd.k - n_above, hist, warp_tot, &s_bin, &s_above, T, cg);
+    c_gt = n_above + cg;
+    for (int i = tid; i < n_cand; i += kThreads) {
       const uint32_t key = cand_key[i];
       const int p = cand_pos[i];
-      if (key > prefix) atomicOr(&above[p >> 5], 1u << (p & 31));
-      else if (key == prefix) atomicOr(&eqbm[p >> 5], 1u << (p & 31));
+      if (key > T) atomicOr(&above[p >> 5], 1u << (p & 31));
+      else if (key == T) atomicOr(&eqbm[p >> 5], 1u << (p & 31));
     }
+    __syncthreads();
+  } else {
+    // ---- fallback (heavy ties or an unlucky sample): exact digit passes ---
+    uint32_t prefix = 0, pmask = 0;
+    c_gt = 0;
+    for (int d = 0; d < 3; ++d) {
+      const int nb = d < 2 ? 2048 : 1024;
+      const int sh = d == 0 ? 21 : (d == 1 ? 10 : 0);
+      for (int i = tid; i < nb; i += kThreads) hist[i] = 0u;
+      __syncthreads();
+      for_row(rd, bad, [&](int, bool valid, uint32_t key) {
+        hist_add(hist, valid && (key & pmask) == prefix, (key >> sh) & (nb - 1));
+      });
+      __syncthreads();
+      int bin, ab;
+      find_bin(hist, nb, rd.k - c_gt, warp_tot, &s_bin, &s_above, bin, ab);
+      c_gt += ab;
+      prefix |= static_cast<uint32_t>(bin) << sh;
+      pmask |= static_cast<uint32_t>(nb - 1) << sh;
+    }
+    const uint32_t T = prefix;
+    for_row(rd, bad, [&](int j, bool valid, uint32_t key) {
+      const unsigned int ba = __ballot_sync(0xffffffffu, valid && key > T);
+      const unsigned int be = __ballot_sync(0xffffffffu, valid && key == T);
+      if (lane == 0 && j < rd.len) {
+        above[j >> 5] = ba;
+        eqbm[j >> 5] = be;
+      }
+    });
     __syncthreads();
   }
 
-  // D. ordered emission.
+  // ---- 4. ordered emission ----------------------------------------------
   const int need_eq = rd.k - c_gt;
   const int per = (W + kThreads - 1) / kThreads;
   const int w0 = min(W, tid * per), w1 = min(W, w0 + per);
@@ -280,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
   const int words_cap = (a.n + 31) / 32;
-  const size_t smem = (2048 + 2 * kCandCap) * sizeof(uint32_t) +
+  const size_t smem = (2048 + 2 * kCandCap + kSampleCap) * sizeof(uint32_t) +
                       2 * static_cast<size_t>(words_cap) * sizeof(uint32_t);
   if (smem > 220 * 1024) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -228,3 +228,22 @@ def test_full_size_decode_sampled(K, cfg):
         p1 = np.exp(s1 - s1.max())
         errs1.append(np.abs(f64(outs[1][b, h]) - (p1 / p1.sum()) @ V1).max())
     assert max(errs0) < 2e-2 and max(errs1) < 2e-2, (max(errs0), max(errs1))
+
+
+def test_workspace_shared_across_shapes_and_entry_points(K):
+    """One workspace serves calls of different shapes and the overlap kernel;
+    the split counters they rely on must survive every other call's writes."""
+    ws = K.Workspace(DEV)
+    shapes = [(8, 32, 8, 2048, 128), (2, 8, 2, 3000, 128), (4, 16, 2, 1500, 64)]
+    layers = [_rand_layer(B, Hq, Hkv, N, d, torch.bfloat16, seed=40 + i)
+              for i, (B, Hq, Hkv, N, d) in enumerate(shapes)]
+    sets = torch.randint(0, 4096, (3, 16, 64), device=DEV, dtype=torch.int32)
+    for rep in range(2):
+        for (q, k, v) in layers:
+            out = K.dense_decode(q, k, v, ws=ws)
+            check_out(out, A.dense_decode(f64(q), f64(k), f64(v))[0])
+            _, idx = K.anchor_decode(q, k, v, 64, ws=ws)
+            out_r = K.reuse_decode(q, k, v, idx, ws=ws)
+            check_out(out_r, A.sparse_decode(f64(q), f64(k), f64(v), idx.cpu().numpy()))
+            K.layer_overlap(sets, 4096, ws=ws)
+    assert ws.device_error() == K.OK
