@@ -404,15 +404,18 @@ __global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant_
   const int words = (R + 31) / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int i = threadIdx.x; i < G * words; i += blockDim.x) bm[i / words][i % words] = 0u;
-  if (warp < G) {
-    const int32_t* row = a.idx + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + warp]) * topk;
-    const int lo = warp_lower_bound(row, topk, n0);
-    const int hi = warp_lower_bound(row, topk, n1);
+  // search job j: the chunk start of slot j (j < G) or the chunk end of slot
+  // j - G, spread over the 8 warps so the searches run concurrently
+  for (int job = warp; job < 2 * G; job += 8) {
+    const int slot = job < G ? job : job - G;
+    const bool is_hi = job >= G;
+    const int32_t* row = a.idx + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + slot]) * topk;
+    const int pos = warp_lower_bound(row, topk, is_hi ? n1 : n0);
     if (lane == 0) {
-      s_lo[warp] = lo;
-      s_hi[warp] = hi;
+      if (is_hi) s_hi[slot] = pos;
+      else s_lo[slot] = pos;
       // entries below 0 (first chunk) or at/after N (last chunk) are invalid
-      if ((c == 0 && lo > 0) || (c == nch - 1 && hi < topk))
+      if ((!is_hi && c == 0 && pos > 0) || (is_hi && c == nch - 1 && pos < topk))
         report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x201);
     }
   }

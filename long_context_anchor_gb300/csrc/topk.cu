@@ -6,9 +6,10 @@
 // One 1024-thread CTA per row, two CTAs per SM; scores become order-
 // preserving uint32 keys on the fly.
 //   1. bracket: an evenly spaced sample of the row (len/16 keys, 2048..8192)
-//      is staged in shared memory and exact rank selection on it gives two
-//      thresholds t_hi >= (k-th key) >= t_lo with a safety margin of four
-//      binomial standard deviations around the expected sample rank;
+//      is staged in shared memory; two histogram passes over it give the
+//      22-bit key prefixes at sample ranks rc -/+ margin (rc the expected
+//      rank of the k-th key, margin four binomial standard deviations), i.e.
+//      thresholds t_hi >= (k-th key) >= t_lo with high probability;
 //   2. one coalesced pass over the row: a warp ballot per 32 positions gives
 //      the bitmap of keys above t_hi (no atomics), and keys in [t_lo, t_hi]
 //      are compacted into a shared candidate list;
@@ -163,11 +164,41 @@ __device__ void select_rank(const uint32_t* list, int n, int rank, uint32_t* his
   greater = gt;
 }
 
+// Two sample quantiles at once, to 22-bit key resolution: the 22-bit key
+// prefixes of the r_hi-th and r_lo-th largest sample keys (r_hi <= r_lo),
+// from one 11-bit histogram of the sample and one of each boundary bin.
+__device__ void sample_bracket(const uint32_t* samp, int n, int r_hi, int r_lo, uint32_t* hist,
+                               int* warp_tot, int* s_bin, int* s_above, uint32_t& p_hi,
+                               uint32_t& p_lo) {
+  uint32_t* h2 = hist + 2048;   // second histogram (second digit of the r_lo bin)
+  for (int i = threadIdx.x; i < 4096; i += kThreads) hist[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kThreads) atomicAdd(&hist[samp[i] >> 21], 1u);
+  __syncthreads();
+  int b_hi, a_hi, b_lo, a_lo;
+  find_bin(hist, 2048, r_hi, warp_tot, s_bin, s_above, b_hi, a_hi);
+  find_bin(hist, 2048, r_lo, warp_tot, s_bin, s_above, b_lo, a_lo);
+  for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const uint32_t key = samp[i];
+    const uint32_t top = key >> 21, mid = (key >> 10) & 2047u;
+    if (top == static_cast<uint32_t>(b_hi)) atomicAdd(&hist[mid], 1u);
+    if (top == static_cast<uint32_t>(b_lo)) atomicAdd(&h2[mid], 1u);
+  }
+  __syncthreads();
+  int m_hi, x_hi, m_lo, x_lo;
+  find_bin(hist, 2048, r_hi - a_hi, warp_tot, s_bin, s_above, m_hi, x_hi);
+  find_bin(h2, 2048, r_lo - a_lo, warp_tot, s_bin, s_above, m_lo, x_lo);
+  p_hi = (static_cast<uint32_t>(b_hi) << 11) | static_cast<uint32_t>(m_hi);
+  p_lo = (static_cast<uint32_t>(b_lo) << 11) | static_cast<uint32_t>(m_lo);
+}
+
 __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ TopkArgs a,
                                                       int words_cap) {
   extern __shared__ uint32_t sm[];
-  uint32_t* hist = sm;                                                     // [2048]
-  uint32_t* cand_key = hist + 2048;                                        // [kCandCap]
+  uint32_t* hist = sm;                                                     // [2][2048]
+  uint32_t* cand_key = hist + 4096;                                        // [kCandCap]
   int32_t* cand_pos = reinterpret_cast<int32_t*>(cand_key + kCandCap);     // [kCandCap]
   uint32_t* samp = reinterpret_cast<uint32_t*>(cand_pos + kCandCap);       // [kSampleCap]
   uint32_t* above = samp + kSampleCap;                                     // [words_cap]
@@ -202,10 +233,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
   const float margin = 4.f * sqrtf(rc) + 16.f;
   const int r_hi = static_cast<int>(floorf(rc - margin));
   const int r_lo = static_cast<int>(ceilf(rc + margin));
+  // above: 22-bit prefix > p_hi; candidates: p_lo <= prefix <= p_hi
   uint32_t t_hi = 0xFFFFFFFFu, t_lo = 0u;
-  int dummy;
-  if (r_hi >= 1) select_rank(samp, S, r_hi, hist, warp_tot, &s_bin, &s_above, t_hi, dummy);
-  if (r_lo <= S) select_rank(samp, S, r_lo, hist, warp_tot, &s_bin, &s_above, t_lo, dummy);
+  {
+    uint32_t p_hi, p_lo;
+    sample_bracket(samp, S, max(r_hi, 1), min(r_lo, S), hist, warp_tot, &s_bin, &s_above, p_hi,
+                   p_lo);
+    if (r_hi >= 1) t_hi = (p_hi << 10) | 1023u;
+    if (r_lo <= S) t_lo = p_lo << 10;
+  }
 
   // ---- 2. one pass: "above" bitmap by ballot, candidates in [t_lo, t_hi] --
   bool bad = false;
@@ -316,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
   const int words_cap = (a.n + 31) / 32;
-  const size_t smem = (2048 + 2 * kCandCap + kSampleCap) * sizeof(uint32_t) +
+  const size_t smem = (4096 + 2 * kCandCap + kSampleCap) * sizeof(uint32_t) +
                       2 * static_cast<size_t>(words_cap) * sizeof(uint32_t);
   if (smem > 220 * 1024) return cudaErrorNotSupported;
   cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
