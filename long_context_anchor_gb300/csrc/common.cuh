@@ -160,4 +160,11 @@ __device__ __forceinline__ uint32_t float_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Same order as float_key, in three operations: adding +0 turns -0 into +0,
+// then negative values are bit-inverted and positive ones get the top bit.
+__device__ __forceinline__ uint32_t float_key_fast(float f) {
+  const uint32_t u = __float_as_uint(f + 0.0f);
+  return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
+}
+
 }  // namespace kascade

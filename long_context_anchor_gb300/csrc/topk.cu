@@ -3,7 +3,7 @@
 // 5). Rule: larger score first, lower index wins a tie, -0 == +0; output
 // ascending positions.
 //
-// One 1024-thread CTA per row, two CTAs per SM; scores become order-
+// One 512-thread CTA per row, two CTAs per SM; scores become order-
 // preserving uint32 keys on the fly.
 //   1. bracket: an evenly spaced sample of the row (len/16 keys, 2048..8192)
 //      is staged in shared memory; two histogram passes over it give the
@@ -30,9 +30,10 @@
 namespace kascade {
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kCandCap = 4096;   // candidate (key, position) pairs in shared memory
+constexpr int kWarpCap = kCandCap / kWarps;   // per-warp candidate list
 constexpr int kUnroll = 8;       // 32-position chunks in flight per warp
 constexpr int kSampleCap = 8192; // evenly spaced sample used to bracket the k-th key
 
@@ -115,21 +116,24 @@ __device__ __forceinline__ void for_row(const RowDesc& rd, bool& bad, F f) {
 }
 
 // Bin holding rank `need` (1 = largest) of an nb-bin histogram, counting from
-// the top bin down; returns the bin and the count in the bins above it.
+// the top bin down; returns the bin and the count in the bins above it. Each
+// thread owns nb / kThreads consecutive bins (highest first).
 __device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, int* warp_tot,
                                          int* s_bin, int* s_above, int& bin, int& above) {
-  const int tid = threadIdx.x;
-  const int b_hi = nb - 1 - 2 * tid;   // this thread owns bins b_hi, b_hi-1
-  const int h0 = b_hi >= 0 ? static_cast<int>(hist[b_hi]) : 0;
-  const int h1 = b_hi >= 1 ? static_cast<int>(hist[b_hi - 1]) : 0;
-  const int excl = block_incl_scan(h0 + h1, warp_tot) - h0 - h1;
-  if (b_hi >= 0) {
-    if (excl < need && need <= excl + h0) {
-      *s_bin = b_hi;
-      *s_above = excl;
-    } else if (b_hi >= 1 && excl + h0 < need && need <= excl + h0 + h1) {
-      *s_bin = b_hi - 1;
-      *s_above = excl + h0;
+  const int per = nb / kThreads;
+  const int top = nb - 1 - per * static_cast<int>(threadIdx.x);
+  int local = 0;
+  for (int q = 0; q < per; ++q) local += static_cast<int>(hist[top - q]);
+  int run = block_incl_scan(local, warp_tot) - local;   // count above this thread's bins
+  if (run < need && need <= run + local) {
+    for (int q = 0; q < per; ++q) {
+      const int h = static_cast<int>(hist[top - q]);
+      if (need <= run + h) {
+        *s_bin = top - q;
+        *s_above = run;
+        break;
+      }
+      run += h;
     }
   }
   __syncthreads();
@@ -151,6 +155,34 @@ __device__ void select_rank(const uint32_t* list, int n, int rank, uint32_t* his
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += kThreads) {
       const uint32_t key = list[i];
+      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+    }
+    __syncthreads();
+    int bin, above;
+    find_bin(hist, nb, rank - gt, warp_tot, s_bin, s_above, bin, above);
+    gt += above;
+    prefix |= static_cast<uint32_t>(bin) << sh;
+    pmask |= static_cast<uint32_t>(nb - 1) << sh;
+  }
+  key_out = prefix;
+  greater = gt;
+}
+
+// select_rank over the per-warp candidate lists (list w holds count[w] keys
+// at cand + w * kWarpCap).
+__device__ void select_rank_warp_lists(const uint32_t* cand, const int* count, int rank,
+                                       uint32_t* hist, int* warp_tot, int* s_bin, int* s_above,
+                                       uint32_t& key_out, int& greater) {
+  uint32_t prefix = 0, pmask = 0;
+  int gt = 0;
+  for (int d = 0; d < 3; ++d) {
+    const int nb = d < 2 ? 2048 : 1024;
+    const int sh = d == 0 ? 21 : (d == 1 ? 10 : 0);
+    for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < kWarps * kWarpCap; i += kThreads) {
+      if ((i % kWarpCap) >= count[i / kWarpCap]) continue;
+      const uint32_t key = cand[i];
       if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
     }
     __syncthreads();
@@ -205,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
   uint32_t* eqbm = above + words_cap;                                      // [words_cap]
   __shared__ int warp_tot[32];
   __shared__ int s_ncand, s_nabove, s_bin, s_above;
+  __shared__ int s_wcount[kWarps];
 
   const int r = blockIdx.x;
   const RowDesc rd = row_desc(a, r);
@@ -244,41 +277,62 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
   }
 
   // ---- 2. one pass: "above" bitmap by ballot, candidates in [t_lo, t_hi] --
+  // Each warp owns blocks of 32*kUnroll consecutive positions and appends its
+  // candidates to its own shared list (count kept in a register).
+  const int warp = tid >> 5;
+  uint32_t* wkey = cand_key + warp * kWarpCap;
+  int32_t* wpos = cand_pos + warp * kWarpCap;
+  const uint32_t span = t_hi - t_lo;
+  int wcount = 0, my_above = 0;
   bool bad = false;
-  int my_above = 0;
-  for_row(rd, bad, [&](int j, bool valid, uint32_t key) {
-    const bool ab = valid && key > t_hi;
-    const bool in = valid && key >= t_lo && key <= t_hi;
-    const unsigned int ba = __ballot_sync(0xffffffffu, ab);
-    const unsigned int bi = __ballot_sync(0xffffffffu, in);
-    if (lane == 0 && j < rd.len) {
-      above[j >> 5] = ba;
-      my_above += __popc(ba);
+  for (int base = warp * 32 * kUnroll; base < rd.len; base += kWarps * 32 * kUnroll) {
+    float x[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = base + 32 * u + lane;
+      x[u] = j < rd.len ? __ldg(rd.ptr + j) : 0.f;
     }
-    if (bi) {
-      int base = 0;
-      if (lane == 0) base = atomicAdd(&s_ncand, __popc(bi));
-      base = __shfl_sync(0xffffffffu, base, 0);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int j = base + 32 * u + lane;
+      const bool valid = j < rd.len;
+      bad |= x[u] != x[u];
+      const uint32_t key = float_key_fast(x[u]);
+      const unsigned int ba = __ballot_sync(0xffffffffu, valid && key > t_hi);
+      const bool in = valid && (key - t_lo) <= span;
+      const unsigned int bi = __ballot_sync(0xffffffffu, in);
+      if (lane == 0 && (base + 32 * u) < rd.len) above[(base >> 5) + u] = ba;
+      my_above += __popc(ba);
       if (in) {
-        const int p = base + __popc(bi & ((1u << lane) - 1u));
-        if (p < kCandCap) {
-          cand_key[p] = key;
-          cand_pos[p] = j;
+        const int p = wcount + __popc(bi & ((1u << lane) - 1u));
+        if (p < kWarpCap) {
+          wkey[p] = key;
+          wpos[p] = j;
         }
       }
+      wcount += __popc(bi);
     }
-  });
-  if (lane == 0 && my_above) atomicAdd(&s_nabove, my_above);
+  }
+  if (lane == 0) {
+    s_wcount[warp] = wcount;
+    atomicAdd(&s_nabove, my_above);
+    if (wcount > kWarpCap) atomicAdd(&s_ncand, 1);   // overflow marker
+  }
   if (__syncthreads_or(bad) && tid == 0) report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x401);
-  const int n_above = s_nabove, n_cand = s_ncand;
+  int n_cand = 0;
+  for (int w = 0; w < kWarps; ++w) n_cand += s_wcount[w];
+  const int n_above = s_nabove;
+  const bool overflow = s_ncand != 0;
   int c_gt;
-  if (n_above < rd.k && n_above + n_cand >= rd.k && n_cand <= kCandCap) {
+  if (!overflow && n_above < rd.k && n_above + n_cand >= rd.k) {
     // ---- 3. exact k-th key among the candidates -------------------------
     uint32_t T;
     int cg;
-    select_rank(cand_key, n_cand, rd.k - n_above, hist, warp_tot, &s_bin, &s_above, T, cg);
+    select_rank_warp_lists(cand_key, s_wcount, rd.k - n_above, hist, warp_tot, &s_bin, &s_above,
+                           T, cg);
     c_gt = n_above + cg;
-    for (int i = tid; i < n_cand; i += kThreads) {
+    for (int i = tid; i < kWarps * kWarpCap; i += kThreads) {
+      if ((i % kWarpCap) >= s_wcount[i / kWarpCap]) continue;
       const uint32_t key = cand_key[i];
       const int p = cand_pos[i];
       if (key > T) atomicOr(&above[p >> 5], 1u << (p & 31));
@@ -287,6 +341,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
     __syncthreads();
   } else {
     // ---- fallback (heavy ties or an unlucky sample): exact digit passes ---
+    for (int w = tid; w < W; w += kThreads) above[w] = eqbm[w] = 0u;
     uint32_t prefix = 0, pmask = 0;
     c_gt = 0;
     for (int d = 0; d < 3; ++d) {
