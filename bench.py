@@ -26,6 +26,8 @@ import sys
 import tempfile
 import time
 
+import numpy as np
+
 ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -555,6 +557,82 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_sweep(args):
+    """Schedule sweep: the DP picks the anchors from calibration on synthetic
+    sequences, then decode and prefill stacks run with those anchors against
+    the library's own dense kernels on the same inputs."""
+    import torch
+    from long_context_anchor_gb300 import configs
+    from long_context_anchor_gb300 import kascade as K
+    from long_context_anchor_gb300.workloads import make_layers
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    res = {"impl": "ours", "mode": "sweep", "metric": METRIC, "data": "synthetic", "dtype": "bf16"}
+    # 1. calibration + DP
+    wc = configs.SWEEP_CALIBRATION
+    qs, ks, vs = make_layers(wc, device=dev)
+    t0 = time.perf_counter()
+    sim, _ = K.calibrate(qs, ks, vs, wc.topk)
+    t_cal = time.perf_counter() - t0
+    anchors, obj = K.schedule_anchors(sim, configs.SWEEP_N_ANCHORS)
+    uniform = list(range(0, wc.n_layers, wc.n_layers // configs.SWEEP_N_ANCHORS))[:configs.SWEEP_N_ANCHORS]
+    from oracle.schedule import objective   # objective of a fixed schedule, for context
+    res["calibration"] = {"workload": wc.name, "seconds": round(t_cal, 3), "anchors": anchors,
+                          "objective": round(obj, 4),
+                          "uniform_anchors": uniform,
+                          "uniform_objective": round(objective(np.asarray(sim), uniform), 4),
+                          "sim_adjacent_mean": round(float(np.mean([sim[i][i + 1] for i in range(wc.n_layers - 1)])), 4)}
+    del qs, ks, vs
+    torch.cuda.empty_cache()
+
+    def time_stack(mode, qs, ks, vs, topk, anch, steps, warm):
+        outs = [torch.empty_like(q) for q in qs]
+        ws = K.Workspace(dev)
+        for _ in range(warm):
+            K.run_stack(mode, qs, ks, vs, topk, anch, outs=outs, ws=ws)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            K.run_stack(mode, qs, ks, vs, topk, anch, outs=outs, ws=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert ws.device_error() == K.OK
+        return e0.elapsed_time(e1) / steps
+
+    # 2. decode, batch 16, N = 32768
+    wd = configs.SWEEP_DECODE
+    qs, ks, vs = make_layers(wd, device=dev)
+    ms_k = time_stack(K.DECODE, qs, ks, vs, wd.topk, anchors, args.steps, args.warmup)
+    ms_d = time_stack(K.DECODE, qs, ks, vs, wd.topk, [], args.steps, args.warmup)
+    res["decode"] = {"workload": wd.name, "kascade_us_per_layer": round(1e3 * ms_k / wd.n_layers, 2),
+                     "dense_us_per_layer": round(1e3 * ms_d / wd.n_layers, 2),
+                     "speedup_vs_own_dense": round(ms_d / ms_k, 3)}
+    del qs, ks, vs
+    torch.cuda.empty_cache()
+    # 3. prefill at three lengths
+    res["prefill"] = []
+    for n in configs.SWEEP_PREFILL_LENGTHS:
+        wp = configs.LLAMA8B_PREFILL_16K.with_(name="llama8b_prefill_n%d_k%d" % (n, n // 8),
+                                              kv_len=n, topk=n // 8, rho_range=(0.7, 0.95),
+                                              seed=3004 + n)
+        qs, ks, vs = make_layers(wp, device=dev)
+        steps = max(1, args.steps // 4)
+        ms_k = time_stack(K.PREFILL, qs, ks, vs, wp.topk, anchors, steps, 1)
+        ms_d = time_stack(K.PREFILL, qs, ks, vs, wp.topk, [], steps, 1)
+        f_dense, f_anchor, f_reuse = prefill_flops(wp)
+        flops_k = len(anchors) * f_anchor + (wp.n_layers - len(anchors)) * f_reuse
+        res["prefill"].append({"workload": wp.name, "kascade_ms_per_stack": round(ms_k, 2),
+                               "dense_ms_per_stack": round(ms_d, 2),
+                               "speedup_vs_own_dense": round(ms_d / ms_k, 3),
+                               "kascade_tflops": round(flops_k / (ms_k * 1e-3) / 1e12, 1),
+                               "dense_tflops": round(wp.n_layers * f_dense / (ms_d * 1e-3) / 1e12, 1)})
+        del qs, ks, vs
+        torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -563,10 +641,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="schedule sweep: DP anchors from calibration, decode and prefill vs dense")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
-    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.sweep:
+        res = run_sweep(args)
+    else:
+        res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 

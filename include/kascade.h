@@ -205,6 +205,21 @@ kascade_status kascade_layer_overlap(const int32_t* sets, int32_t n_layers, int3
                                      int32_t topk, int32_t n_bits, int64_t* counts_out,
                                      void* ws, size_t ws_bytes, void* stream);
 
+/* Calibration for the anchor DP (Methodology 4) on decode inputs: runs
+ * every layer l as an anchor (kascade_anchor_decode) writing its exact
+ * Top-k sets to sets_buf + l*B*Hq*topk (device int32 [n_layers, B*Hq,
+ * topk]; also the layer outputs to out[l]), counts the cross-layer overlaps
+ * on the device and returns sim_out[i*n_layers + l] = sum over (sequence,
+ * query head) of |S_i ∩ S_l| / (B*Hq*topk) (host float64 [n_layers^2]).
+ * Synchronises `stream` before returning. ws must hold
+ * kascade_calibrate_workspace_size bytes. */
+size_t kascade_calibrate_workspace_size(const kascade_desc* desc, int32_t topk, int32_t n_layers);
+kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
+                                 const void* const* q, const void* const* k,
+                                 const void* const* v, int32_t topk, void* const* out,
+                                 int32_t* sets_buf, double* sim_out, void* ws, size_t ws_bytes,
+                                 void* stream);
+
 /* Host DP: choose n_anchors layers (always including 0) maximising
  * F(A) = sum_l sim[a(l) * n_layers + l], a(l) = most recent anchor <= l.
  * sim: host [n_layers * n_layers], row i = anchor layer. Ties go to the

@@ -13,6 +13,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <new>
 
 #include "common.cuh"
 #include "internal.h"
@@ -541,6 +542,65 @@ kascade_status kascade_run_stack(const kascade_desc* desc, int32_t mode, int32_t
                                  void* ws, size_t ws_bytes, void* stream) {
   return kascade_run_stack_profiled(desc, mode, n_layers, q, k, v, topk, anchors, n_anchors,
                                     out, idx_buf, ws, ws_bytes, stream, nullptr);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------ calibration --
+extern "C" {
+
+size_t kascade_calibrate_workspace_size(const kascade_desc* desc, int32_t topk, int32_t n_layers) {
+  Shape s;
+  if (check_desc(desc, s) != KASCADE_OK || topk < 1 || n_layers < 1) return 0;
+  const size_t dec = layout(s, topk, KASCADE_DECODE).total;
+  const size_t ov = kascade_overlap_workspace_size(n_layers, s.B * s.Hq, s.N);
+  const size_t counts = static_cast<size_t>(n_layers) * n_layers * 8;
+  return align256(dec > ov ? dec : ov) + align256(counts);
+}
+
+kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
+                                 const void* const* q, const void* const* k,
+                                 const void* const* v, int32_t topk, void* const* out,
+                                 int32_t* sets_buf, double* sim_out, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  Shape s;
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if (n_layers < 1 || q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
+      sim_out == nullptr || !aligned16(sets_buf) || topk < 1 || topk > s.N)
+    return KASCADE_ERR_INVALID_ARG;
+  const size_t need = kascade_calibrate_workspace_size(desc, topk, n_layers);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < need)
+    return KASCADE_ERR_WORKSPACE;
+  Layout L = layout(s, topk, KASCADE_DECODE);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t per_layer = static_cast<size_t>(s.B) * s.Hq * topk;
+  for (int l = 0; l < n_layers; ++l) {
+    if ((r = check_decode_ptrs(q[l], k[l], v[l], out[l])) != KASCADE_OK) return r;
+    r = run_anchor_decode(s, q[l], k[l], v[l], topk, out[l], sets_buf + l * per_layer, nullptr,
+                          ws, L, st);
+    if (r != KASCADE_OK) return r;
+  }
+  const size_t dec = L.total;
+  const size_t ov = kascade_overlap_workspace_size(n_layers, s.B * s.Hq, s.N);
+  long long* counts = reinterpret_cast<long long*>(static_cast<char*>(ws) +
+                                                   align256(dec > ov ? dec : ov));
+  char* base = static_cast<char*>(ws);
+  cudaError_t e = launch_layer_overlap(sets_buf, n_layers, s.B * s.Hq, topk, s.N, counts,
+                                       reinterpret_cast<uint32_t*>(base + kWsStateBytes),
+                                       reinterpret_cast<unsigned int*>(base), st);
+  if (e != cudaSuccess) return KASCADE_ERR_CUDA;
+  const size_t nc = static_cast<size_t>(n_layers) * n_layers;
+  long long* host = new (std::nothrow) long long[nc];
+  if (host == nullptr) return KASCADE_ERR_INVALID_ARG;
+  e = cudaMemcpyAsync(host, counts, nc * 8, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) {
+    const double denom = static_cast<double>(s.B) * s.Hq * topk;
+    for (size_t i = 0; i < nc; ++i) sim_out[i] = static_cast<double>(host[i]) / denom;
+  }
+  delete[] host;
+  return e == cudaSuccess ? KASCADE_OK : KASCADE_ERR_CUDA;
 }
 
 }  // extern "C"

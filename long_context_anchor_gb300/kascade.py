@@ -57,6 +57,10 @@ _SIGS = {
                                                   ctypes.POINTER(_i32), _i32, ctypes.POINTER(_vp),
                                                   _vp, _vp, _sz, _vp, ctypes.POINTER(_vp)]),
     "kascade_overlap_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "kascade_calibrate_workspace_size": (_sz, [_DP, _i32, _i32]),
+    "kascade_calibrate": (ctypes.c_int, [_DP, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                         ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), _vp,
+                                         ctypes.POINTER(ctypes.c_double), _vp, _sz, _vp]),
     "kascade_layer_overlap": (ctypes.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "kascade_schedule_anchors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), _i32, _i32,
                                                 ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_double)]),
@@ -337,3 +341,24 @@ def schedule_anchors(sim, n_anchors: int):
     _check(_lib.kascade_schedule_anchors(flat, L, int(n_anchors), out, ctypes.byref(obj)),
            "kascade_schedule_anchors")
     return list(out), obj.value
+
+
+def calibrate(qs, ks, vs, topk, group_map=None, scale=None, ws=None, stream=None):
+    """Every layer as an anchor; returns (sim [L][L] list of lists, sets [L, B*Hq, topk])."""
+    L = len(qs)
+    _contig(*qs, *ks, *vs)
+    desc = decode_desc(qs[0], ks[0], group_map, scale)
+    B, Hq, _ = qs[0].shape
+    dev = qs[0].device
+    outs = [torch.empty_like(q) for q in qs]
+    sets = torch.empty(L, B * Hq, topk, dtype=torch.int32, device=dev)
+    nbytes = _lib.kascade_calibrate_workspace_size(ctypes.byref(desc), int(topk), L)
+    if nbytes == 0:
+        raise KascadeError(INVALID_ARG, "kascade_calibrate_workspace_size")
+    ws, buf = _ws(ws, dev, nbytes, stream)
+    arr = lambda ts: (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
+    sim = (ctypes.c_double * (L * L))()
+    _check(_lib.kascade_calibrate(ctypes.byref(desc), L, arr(qs), arr(ks), arr(vs), int(topk),
+                                  arr(outs), _ptr(sets), sim, _ptr(buf), buf.numel(),
+                                  _stream(stream)), "kascade_calibrate")
+    return [[sim[i * L + j] for j in range(L)] for i in range(L)], sets

@@ -1,0 +1,63 @@
+"""GPU checks of the anchor-selection path: the cross-layer overlap kernel
+against exact set arithmetic, calibration (every layer as an anchor) against
+the oracle's overlap similarity, and the C DP against the oracle DP."""
+import numpy as np
+import pytest
+import torch
+
+import __graft_entry__
+from long_context_anchor_gb300 import configs
+from long_context_anchor_gb300.workloads import make_layers
+from oracle import attention as A
+from oracle.schedule import overlap_similarity, schedule_anchors as oracle_dp
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
+
+
+@pytest.fixture(scope="module")
+def K():
+    __graft_entry__.build()
+    from long_context_anchor_gb300 import kascade
+    return kascade
+
+
+def test_layer_overlap_exact(K):
+    rng = np.random.default_rng(0)
+    L, U, k, nb = 5, 7, 50, 1000
+    sets = np.stack([np.stack([np.sort(rng.choice(nb, k, replace=False)) for _ in range(U)])
+                     for _ in range(L)]).astype(np.int32)
+    counts = K.layer_overlap(torch.from_numpy(sets).to(DEV), nb).cpu().numpy()
+    for i in range(L):
+        for l in range(L):
+            exp = sum(len(set(sets[i, u]) & set(sets[l, u])) for u in range(U))
+            assert counts[i, l] == exp
+
+
+def test_calibration_and_dp(K):
+    w = configs.SWEEP_CALIBRATION.with_(n_layers=6, batch=2, kv_len=2048, topk=256)
+    qs, ks, vs = make_layers(w, device=DEV)
+    sim, sets = K.calibrate(qs, ks, vs, w.topk)
+    sim = np.array(sim)
+    sets_np = sets.cpu().numpy()
+    # each layer's sets are exactly what the anchor entry point returns
+    for layer in range(w.n_layers):
+        _, idx = K.anchor_decode(qs[layer], ks[layer], vs[layer], w.topk)
+        assert np.array_equal(idx.reshape(-1, w.topk).cpu().numpy(), sets_np[layer])
+    # the similarity is the oracle's overlap of those sets
+    ref = overlap_similarity([sets_np[layer] for layer in range(w.n_layers)], w.topk)
+    np.testing.assert_allclose(sim, ref, atol=1e-12)
+    # and close to the overlap of the oracle's own float64 Top-k sets
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)
+    own = []
+    for layer in range(w.n_layers):
+        _, idx, _ = A.anchor_decode(f64(qs[layer]), f64(ks[layer]), f64(vs[layer]), w.topk)
+        own.append(idx.reshape(-1, w.topk))
+    np.testing.assert_allclose(sim, overlap_similarity(own, w.topk), atol=0.02)
+    # the C DP picks the oracle DP's anchors on this similarity
+    for m in (1, 2, 3, 6):
+        a, f = K.schedule_anchors(sim.tolist(), m)
+        ao, fo = oracle_dp(sim, m)
+        assert a == ao and abs(f - fo) < 1e-9
+    # cross-layer correlation makes neighbours overlap more than distant layers
+    assert sim[0, 1] > sim[0, 5]
