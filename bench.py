@@ -33,6 +33,14 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode attn µs/layer + HBM GB/s at 32K ctx; prefill attn TFLOP/s; vs own dense"
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one
+# ncu capture of the kernel as it stands (profiles/<kernel>_*.md); None when no
+# capture of the current kernel at the bench's size exists.
+TRAFFIC = {
+    "k_decode_union_bf16": 454.833e6,   # profiles/k_decode_union_bf16_llama8b_b8_n32768.md
+    "k_prefill_fa2_reuse": None,
+}
 UNIT = "us/layer"
 
 
@@ -455,7 +463,8 @@ def run_ours(args):
     if len(reuse_layers) * reuse_ms >= len(anchors) * anchor_ms:
         result["roofline"] = {"kernel": "k_decode_union_bf16 (reuse layer)", "bound": "hbm",
                               "achieved": round(reuse_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                              "frac": round(reuse_gbs / hbm_peak, 4), "traffic": None,
+                              "frac": round(reuse_gbs / hbm_peak, 4),
+                              "traffic": TRAFFIC["k_decode_union_bf16"],
                               "algorithmic_bytes": int(reuse_bytes_mean),
                               "peak_source": peak_src}
     else:
@@ -511,7 +520,8 @@ def run_ours(args):
         result["roofline_prefill_reuse"] = {
             "kernel": "k_prefill_fa<gather> (reuse layer)", "bound": "tensor",
             "achieved": round(pr_tf, 1), "peak": tf_sust, "unit": "TFLOP/s",
-            "frac": round(pr_tf / tf_sust, 4), "traffic": None, "algorithmic_flops": int(pr_f),
+            "frac": round(pr_tf / tf_sust, 4), "traffic": TRAFFIC["k_prefill_fa2_reuse"],
+            "algorithmic_flops": int(pr_f),
             "peak_source": tsrc + " (sustained)"}
         # The step's dominant single-launch kernel by total time.
         dec_reuse_total = len(reuse_layers) * reuse_ms
