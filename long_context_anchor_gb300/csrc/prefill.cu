@@ -2,18 +2,19 @@
 // prefill works at tile level; opentrain.ai Abstract "tile-level operations";
 // one index set per (head, 128-query tile)).
 //
-//   k_prefill_fa2<REUSE, LSE>  two independent tile pipelines per CTA, each on
-//       one (sequence, query head, 128-row tile): a producer warp loads the Q
-//       tile by TMA and the keys in 64-key chunks (dense/anchor layers: the
+//   k_prefill_fa2<REUSE, LSE>  one (sequence, query head, 128-row tile) per
+//       CTA, its key chunks split over two pipelines that share the Q tile
+//       and merge their partial softmax states at the end: producer warps load
+//       the Q tile by TMA and the keys in 64-key chunks (dense/anchor layers: the
 //       causal K/V tiles by TMA; reuse layers: the tile's saved K/V rows by
 //       16-byte cp.async into the 128-byte-swizzled layout, then
 //       fence.proxy.async); one thread issues tcgen05.mma S = Q K^T into
-//       double-buffered TMEM and O += P V; a softmax warpgroup (one thread per
-//       query row) runs the online softmax with a lazy O rescale (only when a
-//       row maximum grows by more than 2^8), writes P as bf16 to shared memory
-//       and finally O / l (and, for anchor layers, the row log-sum-exp).
-//       Causal masking is by key position. The two pipelines share the SM's
-//       tensor core, so one's softmax overlaps the other's MMAs.
+//       double-buffered TMEM and O += P V; a softmax warpgroup per pipeline (one
+//       thread per query row) runs the online softmax with a lazy O rescale
+//       (only when a row maximum grows by more than 2^8) and writes P as bf16
+//       into double-buffered shared memory; pipeline 0 finally merges both
+//       partial states and writes O / l (and, for anchor layers, the row
+//       log-sum-exp). Causal masking is by key position.
 //   k_prefill_weights        anchor pass 2: S^T = K Q^T per key tile (TMEM lane
 //       = key), p = 2^(s*sigma*log2e - lse2[query]), and each thread sums its
 //       key's column over the tile's rows: w_j = sum_{i in tile, i >= j} p_ij,
@@ -53,123 +54,137 @@ __device__ __forceinline__ void fa_tile_coords(const PrefillArgs& a, int& bh, in
   t = a.nT - 1 - static_cast<int>(blockIdx.x) / BH;
 }
 
-// Two independent tile pipelines per CTA (pipe p handles work tile 2*blockIdx.x + p):
-// warps 4p..4p+3 run pipe p's softmax, warp 8+p issues its MMAs, warp 10+p
-// is its producer (TMA for Q and dense K/V; 16-byte cp.async gathers of the
-// saved rows for reuse). 64-key chunks, a 2-deep K/V ring per pipe.
-constexpr int kFa2Threads = 384;
-constexpr int kKC = 64;
-constexpr int kST = 2;
+// One query tile per CTA, its key chunks split over two pipelines (pipe p takes
+// chunks p, p+2, ...): warps 4p..4p+3 run pipe p's softmax, warp 8+p issues its
+// MMAs, warp 10+p is its producer (TMA for Q and dense K/V); for reuse, warps
+// 10+p and 12+p gather pipe p's chunks in turn with 16-byte cp.async (each
+// waits for its own copies, so two chunks per pipeline are in flight). The Q tile is shared; every pipe has a
+// 2-deep K/V ring, double-buffered S in TMEM and double-buffered P in shared
+// memory, so a softmax warpgroup never waits for the previous P V product
+// before writing the next P. At the end pipe 1's (m, l, O) is merged into
+// pipe 0's through shared memory and TMEM.
+// Threads: 8 softmax warps, 2 MMA warps, and 2 (dense: TMA) or 4 (reuse:
+// gathers, two warps per pipeline taking turns by chunk) producer warps.
+template <bool REUSE> __host__ __device__ constexpr int fa_threads() { return REUSE ? 448 : 384; }
+template <bool REUSE> __host__ __device__ constexpr int fa_producers() { return REUSE ? 2 : 1; }
 
+// Per-pipeline shared memory for KC-key chunks and an ST-deep K/V ring. The
+// P tile keeps a 128-byte row pitch (K-major, 128-byte swizzle) for any KC.
+template <int KC, int ST>
 struct Fa2Pipe {
-  static constexpr int KHALF = kKC * 128;      // 8 KB
-  static constexpr int KV_BYTES = 2 * KHALF;   // 16 KB
-  static constexpr int Q = 0;
-  static constexpr int K0 = Q + kTileBytes;
-  static constexpr int V0 = K0 + kST * KV_BYTES;
-  static constexpr int P = V0 + kST * KV_BYTES;        // 128 x 64 bf16 = 16 KB
-  static constexpr int BYTES = P + kTile * kKC * 2;    // 112 KB, 1024-aligned
+  static constexpr int KHALF = KC * 128;           // one 64-dim half of a K (or V) chunk
+  static constexpr int KV_BYTES = 2 * KHALF;
+  static constexpr int P_BYTES = kTile * 128;      // 16 KB
+  static constexpr int K0 = 0;
+  static constexpr int V0 = K0 + ST * KV_BYTES;
+  static constexpr int P0 = V0 + ST * KV_BYTES;    // P[2]
+  static constexpr int BYTES = P0 + 2 * P_BYTES;   // 96 KB for (64, 2) and (32, 4)
 };
+template <int KC, int ST>
 struct Fa2Smem {
-  static constexpr int PIPE0 = 0;
-  static constexpr int PIPE1 = Fa2Pipe::BYTES;
-  static constexpr int POS = 2 * Fa2Pipe::BYTES;          // int32 [2 pipes][kST][kKC]
-  static constexpr int BAR = POS + 2 * kST * kKC * 4;     // [2 pipes][16] mbarriers
-  static constexpr int TMEM = BAR + 2 * 16 * 8;
+  using Pp = Fa2Pipe<KC, ST>;
+  static constexpr int Q = 0;
+  static constexpr int PIPE0 = kTileBytes;
+  static constexpr int PIPE1 = PIPE0 + Pp::BYTES;
+  static constexpr int POS = PIPE1 + Pp::BYTES;          // int32 [2 pipes][ST][KC]
+  static constexpr int BAR = POS + 2 * ST * KC * 4;      // [2 pipes][16] mbarriers + q_full
+  static constexpr int TMEM = BAR + (2 * 16 + 1) * 8;
   static constexpr int BYTES = TMEM + 16;
   static constexpr size_t SMEM = BYTES + 1024;
+  static_assert(SMEM <= 232448, "the tile and two pipelines must fit in shared memory");
 };
-static_assert(Fa2Smem::SMEM <= 232448, "two pipelines must fit in shared memory");
+// Dense and anchor layers stream 64-key TMA tiles two deep; reuse layers
+// gather 32-key chunks four deep.
+template <bool REUSE> struct FaShape { static constexpr int KC = 64, ST = 2; };
+template <> struct FaShape<true> { static constexpr int KC = 32, ST = 4; };
 
 template <bool REUSE, bool LSE>
-__global__ void __launch_bounds__(kFa2Threads, 1)
+__global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     k_prefill_fa2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillArgs a) {
-  using C = Fa2Pipe;
+  constexpr int kKC = FaShape<REUSE>::KC, kST = FaShape<REUSE>::ST;
+  constexpr int kProd = fa_producers<REUSE>();
+  using C = Fa2Pipe<kKC, kST>;
+  using SM = Fa2Smem<kKC, kST>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // role and pipe of this warp
   int pipe, role;   // role: 0 softmax, 1 MMA, 2 producer
   if (warp < 8) { pipe = warp >> 2; role = 0; }
   else if (warp < 10) { pipe = warp - 8; role = 1; }
-  else { pipe = warp - 10; role = 2; }
+  else { pipe = (warp - 10) & 1; role = 2; }
+  const int prod = (warp - 10) >> 1;   // producer index within its pipeline
 
-  unsigned char* ps = sm + (pipe ? Fa2Smem::PIPE1 : Fa2Smem::PIPE0);
-  int32_t* s_pos = reinterpret_cast<int32_t*>(sm + Fa2Smem::POS) + pipe * kST * kKC;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + Fa2Smem::BAR) + pipe * 16;
-  uint64_t* q_full = bar + 0;
-  uint64_t* kv_full = bar + 1;          // [kST]
-  uint64_t* kv_free = bar + 1 + kST;    // [kST]
-  uint64_t* s_full = bar + 1 + 2 * kST; // [2]
-  uint64_t* s_free = s_full + 2;        // [2]
-  uint64_t* p_full = s_free + 2;
-  uint64_t* pv_done = p_full + 1;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + Fa2Smem::TMEM);
-  const uint32_t sQ = smem_u32(ps + C::Q), sK0 = smem_u32(ps + C::K0);
-  const uint32_t sV0 = smem_u32(ps + C::V0), sP = smem_u32(ps + C::P);
+  unsigned char* ps = sm + (pipe ? SM::PIPE1 : SM::PIPE0);
+  int32_t* s_pos = reinterpret_cast<int32_t*>(sm + SM::POS) + pipe * kST * kKC;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::BAR);
+  uint64_t* q_full = bars + 32;
+  uint64_t* bar = bars + pipe * 16;
+  uint64_t* kv_full = bar + 0;   // [kST <= 4]
+  uint64_t* kv_free = bar + 4;   // [kST]
+  uint64_t* s_full = bar + 8;    // [2]
+  uint64_t* s_free = bar + 10;   // [2]
+  uint64_t* p_full = bar + 12;   // [2]
+  uint64_t* pv_done = bar + 14;  // [2] PV of the chunk that used P buffer b
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + SM::TMEM);
+  const uint32_t sQ = smem_u32(sm + SM::Q), sK0 = smem_u32(ps + C::K0);
+  const uint32_t sV0 = smem_u32(ps + C::V0), sP0 = smem_u32(ps + C::P0);
 
-  // work tile of this pipe (longest tiles first); pipes past the end idle
   const int BH = a.B * a.Hq;
-  const int item = 2 * static_cast<int>(blockIdx.x) + pipe;
-  const bool active = item < BH * a.nT;
-  const int bh = item % BH;
-  const int t = a.nT - 1 - item / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int t = a.nT - 1 - static_cast<int>(blockIdx.x) / BH;   // longest tiles first
   const int b = bh / a.Hq, h = bh % a.Hq, g = a.head_kv[h];
   const int row0 = t * kTile;
-  const int L = active ? min(a.N, row0 + kTile) : 0;
-  int nkv = 0, kt = 0;
+  const int L = min(a.N, row0 + kTile);
+  int nkv, kt = 0;
   const int32_t* idx_row = nullptr;
-  if (active) {
-    if (REUSE) {
-      kt = min(a.topk, L);
-      nkv = (kt + kKC - 1) / kKC;
-      idx_row = a.idx + (static_cast<size_t>(bh) * a.nT + t) * a.topk;
-    } else {
-      nkv = (L + kKC - 1) / kKC;
-    }
+  if (REUSE) {
+    kt = min(a.topk, L);
+    nkv = (kt + kKC - 1) / kKC;
+    idx_row = a.idx + (static_cast<size_t>(bh) * a.nT + t) * a.topk;
+  } else {
+    nkv = (L + kKC - 1) / kKC;
   }
+  const int np = (nkv - pipe + 1) / 2;   // chunks of this pipe: global chunk 2i + pipe
   const int kv_row_base = (b * a.Hkv + g) * a.N;
 
   if (threadIdx.x < 2) {   // thread p initialises pipe p's barriers
-    uint64_t* pb = reinterpret_cast<uint64_t*>(sm + Fa2Smem::BAR) + threadIdx.x * 16;
-    mbar_init(pb + 0, 1);
+    uint64_t* pb = bars + threadIdx.x * 16;
     for (int s = 0; s < kST; ++s) {
-      mbar_init(pb + 1 + s, REUSE ? 32 : 1);
-      mbar_init(pb + 1 + kST + s, 1);
+      mbar_init(pb + 0 + s, REUSE ? 32 : 1);
+      mbar_init(pb + 4 + s, 1);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(pb + 1 + 2 * kST + s, 1);
-      mbar_init(pb + 3 + 2 * kST + s, 128);
+      mbar_init(pb + 8 + s, 1);
+      mbar_init(pb + 10 + s, 128);
+      mbar_init(pb + 12 + s, 128);
+      mbar_init(pb + 14 + s, 1);
     }
-    mbar_init(pb + 5 + 2 * kST, 128);
-    mbar_init(pb + 6 + 2 * kST, 1);
+    if (threadIdx.x == 0) mbar_init(bars + 32, 1);
     fence_barrier_init();
   }
   if (warp == 8) tmem_alloc(s_tmem, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *s_tmem + pipe * 256;
-  const uint32_t tS = tmem, tO = tmem + 128;   // S[2] at +0 / +64, O at +128
+  const uint32_t tmem_base = *s_tmem;
+  const uint32_t tS = tmem_base + pipe * 256, tO = tS + 128;   // S[2] at +0/+64, O at +128
 
-  if (!active) {
-    // nothing to do for this pipe
-  } else if (role == 2) {
+  if (role == 2) {
     // ------------------------------------------------ producer
-    if (lane == 0) {
+    if (pipe == 0 && prod == 0 && lane == 0) {
       prefetch_tmap(&tmQ);
       mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_2d(ps + C::Q, &tmQ, q_full, 0, bh * a.N + row0);
-      tma_load_2d(ps + C::Q + kHalf, &tmQ, q_full, 64, bh * a.N + row0);
+      tma_load_2d(sm + SM::Q, &tmQ, q_full, 0, bh * a.N + row0);
+      tma_load_2d(sm + SM::Q + kHalf, &tmQ, q_full, 64, bh * a.N + row0);
     }
     if (!REUSE) {
-      if (lane == 0) {
+      if (lane == 0) {   // one TMA producer per pipeline
         int issued = 0;
-        for (int j = 0; j < nkv; ++j) {
-          const int s = j % kST;
-          if (!mbar_wait(kv_free + s, ((j / kST) & 1) ^ 1, a.err, 0x601)) break;
+        for (int i = 0; i < np; ++i) {
+          const int s = i % kST, j = 2 * i + pipe;
+          if (!mbar_wait(kv_free + s, ((i / kST) & 1) ^ 1, a.err, 0x601)) break;
           unsigned char* kd = ps + C::K0 + s * C::KV_BYTES;
           unsigned char* vd = ps + C::V0 + s * C::KV_BYTES;
           mbar_arrive_expect_tx(kv_full + s, 2 * C::KV_BYTES);
@@ -178,25 +193,27 @@ __global__ void __launch_bounds__(kFa2Threads, 1)
           tma_load_2d(kd + C::KHALF, &tmK, kv_full + s, 64, y);
           tma_load_2d(vd, &tmV, kv_full + s, 0, y);
           tma_load_2d(vd + C::KHALF, &tmV, kv_full + s, 64, y);
-          issued = j + 1;
+          issued = i + 1;
         }
-        for (int j = issued > kST ? issued - kST : 0; j < issued; ++j)
-          mbar_wait(kv_full + (j % kST), (j / kST) & 1, a.err, 0x604);
+        for (int i = issued > kST ? issued - kST : 0; i < issued; ++i)
+          mbar_wait(kv_full + (i % kST), (i / kST) & 1, a.err, 0x604);
       }
     } else {
       int p_first = __ldg(idx_row);
       if (p_first < 0 || p_first >= a.N) p_first = 0;
       const __nv_bfloat16* kbase = static_cast<const __nv_bfloat16*>(a.k);
       const __nv_bfloat16* vbase = static_cast<const __nv_bfloat16*>(a.v);
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j % kST;
+      // producer `prod` gathers this pipeline's chunks i = prod, prod + kProd,
+      // ...; each waits for its own copies, so kProd chunks are in flight
+      for (int i = prod; i < np; i += kProd) {
+        const int s = i % kST, j = 2 * i + pipe;
         int ok = 1;
-        if (lane == 0) ok = mbar_wait(kv_free + s, ((j / kST) & 1) ^ 1, a.err, 0x605);
+        if (lane == 0) ok = mbar_wait(kv_free + s, ((i / kST) & 1) ^ 1, a.err, 0x605);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         unsigned char* kd = ps + C::K0 + s * C::KV_BYTES;
         unsigned char* vd = ps + C::V0 + s * C::KV_BYTES;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
+        for (int half = 0; half < kKC / 32; ++half) {
           const int pt = lane + 32 * half;   // key row within the chunk
           const int e = j * kKC + pt;
           int p = e < kt ? __ldg(idx_row + e) : -1;
@@ -207,46 +224,45 @@ __global__ void __launch_bounds__(kFa2Threads, 1)
           s_pos[s * kKC + pt] = p;
           // padding slots re-read the tile's first saved row (masked later)
           const size_t row = static_cast<size_t>(kv_row_base) + (p >= 0 ? p : p_first);
-          const __nv_bfloat16* ks = kbase + row * 128;
-          const __nv_bfloat16* vs = vbase + row * 128;
+          const __nv_bfloat16* ksrc = kbase + row * 128;
+          const __nv_bfloat16* vsrc = vbase + row * 128;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const int off = (c >> 3) * C::KHALF + pt * 128 + (((c & 7) ^ (pt & 7)) << 4);
-            cp_async16(kd + off, ks + c * 8, 16);
-            cp_async16(vd + off, vs + c * 8, 16);
+            cp_async16(kd + off, ksrc + c * 8, 16);
+            cp_async16(vd + off, vsrc + c * 8, 16);
           }
         }
-        // signal as soon as this chunk has landed (the other stage keeps the
-        // tensor core busy meanwhile)
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async_smem();
         mbar_arrive(kv_full + s);
       }
     }
-    if (lane == 0) mbar_wait(q_full, 0, a.err, 0x603);   // never leave with copies in flight
+    if (pipe == 0 && prod == 0 && lane == 0) mbar_wait(q_full, 0, a.err, 0x603);   // no copies left in flight
   } else if (role == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idq = idesc_bf16_f32(128, kKC, 0, 0);
       constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
       bool ok = mbar_wait(q_full, 0, a.err, 0x611);
-      auto issue_pv = [&](int jj) {
-        const int s = jj % kST;
-        if (!mbar_wait(p_full, jj & 1, a.err, 0x612)) return false;
+      auto issue_pv = [&](int ii) {
+        const int s = ii % kST, pb = ii & 1;
+        if (!mbar_wait(p_full + pb, (ii >> 1) & 1, a.err, 0x612)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kKC / 16; ++kk)
-          tc_mma(tO, kmajor_desc(sP, kk), vmn_desc(sV0 + s * C::KV_BYTES, kk, C::KHALF), idv,
-                 (jj > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(pv_done);
+          tc_mma(tO, kmajor_desc(sP0 + pb * C::P_BYTES, kk),
+                 vmn_desc(sV0 + s * C::KV_BYTES, kk, C::KHALF), idv,
+                 (ii > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(pv_done + pb);
         tc_commit(kv_free + s);
         return true;
       };
-      for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % kST, sb = j & 1;
-        ok = mbar_wait(kv_full + s, (j / kST) & 1, a.err, 0x613) &&
-             mbar_wait(s_free + sb, ((j >> 1) & 1) ^ 1, a.err, 0x614);
+      for (int i = 0; ok && i < np; ++i) {
+        const int s = i % kST, sb = i & 1;
+        ok = mbar_wait(kv_full + s, (i / kST) & 1, a.err, 0x613) &&
+             mbar_wait(s_free + sb, ((i >> 1) & 1) ^ 1, a.err, 0x614);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
@@ -254,20 +270,20 @@ __global__ void __launch_bounds__(kFa2Threads, 1)
           tc_mma(tS + sb * kKC, kmajor_desc(sQ, kk),
                  kmajor_desc(sK0 + s * C::KV_BYTES, kk, C::KHALF), idq, kk > 0 ? 1u : 0u);
         tc_commit(s_full + sb);
-        if (j > 0) ok = issue_pv(j - 1);
+        if (i > 0) ok = issue_pv(i - 1);
       }
-      if (ok && nkv > 0) issue_pv(nkv - 1);
+      if (ok && np > 0) issue_pv(np - 1);
     }
   } else {
-    // ------------------------------------------------ softmax warpgroup
+    // ------------------------------------------------ softmax warpgroups
     const int r = (warp & 3) * 32 + lane;
-    const int i = row0 + r;
+    const int row = row0 + r;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float m_used = kNegInfP, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      const int sb = j & 1, s = j % kST;
-      ok = mbar_wait(s_full + sb, (j >> 1) & 1, a.err, 0x621);
+    for (int i = 0; i < np; ++i) {
+      const int sb = i & 1, s = i % kST, j = 2 * i + pipe;
+      ok = mbar_wait(s_full + sb, (i >> 1) & 1, a.err, 0x621);
       if (!ok) break;
       tc_fence_after();
       float x[kKC];
@@ -287,7 +303,7 @@ __global__ void __launch_bounds__(kFa2Threads, 1)
 #pragma unroll
         for (int c = 0; c < kKC; ++c) {
           const int kp = REUSE ? s_pos[s * kKC + c] : j * kKC + c;
-          if (!(kp >= 0 && kp <= i)) x[c] = kNegInfP;
+          if (!(kp >= 0 && kp <= row)) x[c] = kNegInfP;
           tmax = fmaxf(tmax, x[c]);
         }
       } else {
@@ -298,7 +314,7 @@ __global__ void __launch_bounds__(kFa2Threads, 1)
       float alpha = 1.f;
       bool resc = false;
       if (tmax > m_used + kRescaleLog2) {
-        if (j > 0) {
+        if (i > 0) {
           alpha = ex2_approx(m_used - tmax);
           resc = true;
         }
@@ -314,11 +330,14 @@ __global__ void __launch_bounds__(kFa2Threads, 1)
         l += p0 + p1;
         pk[c] = pack_bf16(p0, p1);
       }
-      if (j > 0) {
-        ok = mbar_wait(pv_done, (j - 1) & 1, a.err, 0x622);
+      // P buffer sb was last read by PV(i-2); a rescale of O also needs PV(i-1)
+      if (i >= 2) {
+        ok = mbar_wait(pv_done + sb, ((i >> 1) - 1) & 1, a.err, 0x622);
         if (!ok) break;
       }
       if (__any_sync(0xffffffffu, resc)) {
+        ok = mbar_wait(pv_done + (sb ^ 1), ((i - 1) >> 1) & 1, a.err, 0x624);
+        if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -331,6 +350,7 @@ __global__ void __launch_bounds__(kFa2Threads, 1)
         }
         tmem_wait_st();
       }
+      const uint32_t sP = sP0 + sb * C::P_BYTES;
 #pragma unroll
       for (int ch = 0; ch < kKC / 8; ++ch) {
         const uint32_t addr = sP + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
@@ -340,39 +360,62 @@ __global__ void __launch_bounds__(kFa2Threads, 1)
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(p_full + sb);
     }
-    if (ok && nkv > 0) ok = mbar_wait(pv_done, (nkv - 1) & 1, a.err, 0x623);
+    // wait for this pipe's last P V, then merge pipe 1 into pipe 0
+    if (ok && np > 0) ok = mbar_wait(pv_done + ((np - 1) & 1), ((np - 1) >> 1) & 1, a.err, 0x623);
+    float* xch = reinterpret_cast<float*>(sm + SM::PIPE1 + C::P0);   // pipe 1's P, now free
+    if (pipe == 1) {
+      xch[r] = np > 0 ? m_used : kNegInfP;
+      xch[128 + r] = np > 0 ? l : 0.f;
+    }
+    tc_fence_before();
+    asm volatile("bar.sync 1, 256;" ::: "memory");   // the two softmax warpgroups
     tc_fence_after();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    __nv_bfloat16* orow =
-        static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(bh) * a.N + i) * kTile;
+    if (pipe == 0) {
+      const float m1 = xch[r], l1 = xch[128 + r];
+      const float m0 = np > 0 ? m_used : kNegInfP;
+      const float M = fmaxf(m0, m1);
+      const float a0 = (m0 == kNegInfP) ? 0.f : ex2_approx(m0 - M);
+      const float a1 = (m1 == kNegInfP) ? 0.f : ex2_approx(m1 - M);
+      const float lt = a0 * l + a1 * l1;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const uint32_t tO1 = tmem_base + 256 + 128;
+      __nv_bfloat16* orow =
+          static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(bh) * a.N + row) * kTile;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t o[32];
-      tmem_ld32(tO + c * 32 + lane_base, o);
-      tmem_wait_ld();
-      uint32_t ob[16];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(tO + c * 32 + lane_base, o0);
+        tmem_ld32(tO1 + c * 32 + lane_base, o1);
+        tmem_wait_ld();
+        uint32_t ob[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e)
-        ob[e] = (nkv > 0 && ok) ? pack_bf16(__uint_as_float(o[2 * e]) * inv,
-                                            __uint_as_float(o[2 * e + 1]) * inv)
-                                : 0u;
-      if (i < a.N) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        for (int e = 0; e < 16; ++e) {
+          float y0 = a0 * __uint_as_float(o0[2 * e]);
+          float y1 = a0 * __uint_as_float(o0[2 * e + 1]);
+          if (a1 != 0.f) {
+            y0 += a1 * __uint_as_float(o1[2 * e]);
+            y1 += a1 * __uint_as_float(o1[2 * e + 1]);
+          }
+          ob[e] = ok ? pack_bf16(y0 * inv, y1 * inv) : 0u;
+        }
+        if (row < a.N) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[q] = make_uint4(ob[4 * q], ob[4 * q + 1], ob[4 * q + 2], ob[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(ob[4 * q], ob[4 * q + 1], ob[4 * q + 2], ob[4 * q + 3]);
+        }
       }
+      if (LSE && row < a.N)
+        a.lse[static_cast<size_t>(bh) * a.N + row] = lt > 0.f ? M + __log2f(lt) : kNegInfP;
     }
-    if (LSE && i < a.N)
-      a.lse[static_cast<size_t>(bh) * a.N + i] = l > 0.f ? m_used + __log2f(l) : kNegInfP;
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 8) {
     tc_fence_after();
-    tmem_dealloc(*s_tmem, 512);
+    tmem_dealloc(tmem_base, 512);
   }
 }
 
@@ -523,14 +566,15 @@ bool make_maps(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUtensorM
 
 template <bool REUSE, bool LSE>
 cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
+  constexpr int KC = FaShape<REUSE>::KC, ST = FaShape<REUSE>::ST;
+  using SM = Fa2Smem<KC, ST>;
   alignas(64) CUtensorMap tq, tk, tv;
-  if (!make_maps(a, &tq, &tk, &tv, kKC)) return cudaErrorInvalidValue;
+  if (!make_maps(a, &tq, &tk, &tv, KC)) return cudaErrorInvalidValue;
   auto kern = k_prefill_fa2<REUSE, LSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(Fa2Smem::SMEM));
+                                       static_cast<int>(SM::SMEM));
   if (e != cudaSuccess) return e;
-  const int items = a.B * a.Hq * a.nT;
-  kern<<<(items + 1) / 2, kFa2Threads, Fa2Smem::SMEM, st>>>(tq, tk, tv, a);
+  kern<<<a.B * a.Hq * a.nT, fa_threads<REUSE>(), SM::SMEM, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
