@@ -18,6 +18,7 @@ with host buffers, and the CPU oracle timed on the host cores.
 ``--impl reference`` times the CPU oracle itself on a bounded sample.
 """
 import argparse
+import datetime
 import json
 import os
 import statistics
@@ -47,16 +48,23 @@ UNIT = "us/layer"
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons.
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    The sampler runs from `start()` to `stop()`; `begin()`/`end()` bracket each
+    timed region, and `stop()` keeps only the samples taken inside a region
+    (widened by one sampling period, so that regions shorter than the period
+    still get their nearest sample)."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 100
 
     def __init__(self, index=0):
         self.index = index
         self.proc = None
         self.path = None
+        self.windows = []
 
     def start(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
@@ -64,35 +72,48 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
+        time.sleep(0.3)   # let the first samples arrive before the first region
+
+    def begin(self):
+        self.windows.append([datetime.datetime.now(), None])
+
+    def end(self):
+        self.windows[-1][1] = datetime.datetime.now()
 
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(2 * self.PERIOD_MS / 1e3)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        pad = datetime.timedelta(milliseconds=self.PERIOD_MS)
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                sample = (float(parts[1]), float(parts[2]), parts[5:9])
             except ValueError:
                 continue
+            if any(b - pad <= ts <= e + pad for b, e in self.windows if e is not None):
+                rows.append(sample)
         os.unlink(self.path)
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i] == "Active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows),
-                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows), "reasons": reasons}
+                "sm_max_mhz": max(r[1] for r in rows), "samples": len(rows),
+                "timed_regions": len(self.windows), "reasons": reasons}
 
 
 # ---------------------------------------------------------- CPU oracle leg --
@@ -251,7 +272,7 @@ def prefill_flops(w, topk_sizes=None):
     return dense, anchor, reuse
 
 
-def run_prefill(args, dev, world, stream):
+def run_prefill(args, dev, world, stream, clocks):
     """Prefill stack of the Llama-3.1-8B shape at N = 16384 (32 layers,
     anchors every 4th layer): Kascade vs the library's own dense prefill."""
     import torch
@@ -291,8 +312,10 @@ def run_prefill(args, dev, world, stream):
     torch.cuda.synchronize()
     assert ws.device_error() == K.OK
     steps = max(1, args.steps // 2)
+    clocks.begin()
     tot_k, per_k = timed(anchors, steps)
     tot_d, per_d = timed([], steps)
+    clocks.end()
     if world > 1:
         t = torch.tensor([tot_k, tot_d], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -400,9 +423,10 @@ def run_ours(args):
 
     clocks = ClockSampler(local)
     clocks.start()
+    clocks.begin()
     total_k, pl_k = timed(anchors, args.steps)
     total_d, pl_d = timed([], args.steps)
-    clk = clocks.stop()
+    clocks.end()
     if world > 1:
         t = torch.tensor([total_k, total_d], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -456,7 +480,6 @@ def run_ours(args):
                    "dense_bytes_per_layer": int(dense_b),
                    "peak_hbm_gbs": hbm_peak, "peak_source": peak_src},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
     }
     # Dominant kernel: the reuse-layer union-gather kernel (one launch per
     # reuse layer) or the anchor layer, whichever holds more of the step.
@@ -512,13 +535,13 @@ def run_ours(args):
     # Prefill stack (same step): Llama-3.1-8B shape at N = 16384.
     if not args.no_prefill:
         pre, pre_launches, pre_ms, (pa_ms, pa_f, pr_ms, pr_f, tf_sust, tsrc) = \
-            run_prefill(args, dev, world, stream)
+            run_prefill(args, dev, world, stream, clocks)
         result["prefill"] = pre
         result["gpu_launches_prefill"] = pre_launches
         result["ms_per_step_prefill"] = round(pre_ms, 3)
         pr_tf = pr_f / (pr_ms * 1e-3) / 1e12
         result["roofline_prefill_reuse"] = {
-            "kernel": "k_prefill_fa<gather> (reuse layer)", "bound": "tensor",
+            "kernel": "k_prefill_fa2<reuse> (reuse layer)", "bound": "tensor",
             "achieved": round(pr_tf, 1), "peak": tf_sust, "unit": "TFLOP/s",
             "frac": round(pr_tf / tf_sust, 4), "traffic": TRAFFIC["k_prefill_fa2_reuse"],
             "algorithmic_flops": int(pr_f),
@@ -529,6 +552,7 @@ def run_ours(args):
         if pre_reuse_total > dec_reuse_total:
             result["roofline_decode_reuse"] = result["roofline"]
             result["roofline"] = result["roofline_prefill_reuse"]
+    result["clocks"] = clocks.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
         result["cpu_baseline"] = time_oracle(w, lay01, n_groups=os.cpu_count() or 1, reps=2)

@@ -5,16 +5,17 @@
 //   k_prefill_fa2<REUSE, LSE>  one (sequence, query head, 128-row tile) per
 //       CTA, its key chunks split over two pipelines that share the Q tile
 //       and merge their partial softmax states at the end: producer warps load
-//       the Q tile by TMA and the keys in 64-key chunks (dense/anchor layers: the
-//       causal K/V tiles by TMA; reuse layers: the tile's saved K/V rows by
-//       16-byte cp.async into the 128-byte-swizzled layout, then
-//       fence.proxy.async); one thread issues tcgen05.mma S = Q K^T into
-//       double-buffered TMEM and O += P V; a softmax warpgroup per pipeline (one
-//       thread per query row) runs the online softmax with a lazy O rescale
-//       (only when a row maximum grows by more than 2^8) and writes P as bf16
-//       into double-buffered shared memory; pipeline 0 finally merges both
-//       partial states and writes O / l (and, for anchor layers, the row
-//       log-sum-exp). Causal masking is by key position.
+//       the Q tile by TMA and the keys in chunks (dense/anchor layers: 64-key
+//       causal K/V tiles by TMA; reuse layers: 32-key chunks of the tile's saved
+//       K/V rows by 16-byte cp.async into the 128-byte-swizzled layout, then
+//       fence.proxy.async); one thread per pipeline issues tcgen05.mma
+//       S = Q K^T into rotating TMEM score buffers and O += P V with P read from
+//       TMEM; a softmax warpgroup per pipeline (one thread per query row) runs
+//       the online softmax with a lazy O rescale (only when a row maximum grows
+//       by more than 2^8) and writes P as bf16 over the scores it came from;
+//       pipeline 0 finally merges both partial states and writes O / l (and,
+//       for anchor layers, the row log-sum-exp). Causal masking is by key
+//       position.
 //   k_prefill_weights        anchor pass 2: S^T = K Q^T per key tile (TMEM lane
 //       = key), p = 2^(s*sigma*log2e - lse2[query]), and each thread sums its
 //       key's column over the tile's rows: w_j = sum_{i in tile, i >= j} p_ij,
@@ -58,54 +59,67 @@ __device__ __forceinline__ void fa_tile_coords(const PrefillArgs& a, int& bh, in
 // chunks p, p+2, ...): warps 4p..4p+3 run pipe p's softmax, warp 8+p issues its
 // MMAs, warp 10+p is its producer (TMA for Q and dense K/V); for reuse, warps
 // 10+p and 12+p gather pipe p's chunks in turn with 16-byte cp.async (each
-// waits for its own copies, so two chunks per pipeline are in flight). The Q tile is shared; every pipe has a
-// 2-deep K/V ring, double-buffered S in TMEM and double-buffered P in shared
-// memory, so a softmax warpgroup never waits for the previous P V product
-// before writing the next P. At the end pipe 1's (m, l, O) is merged into
-// pipe 0's through shared memory and TMEM.
+// waits for its own copies, so two chunks per pipeline are in flight).
+// The Q tile is shared. Every pipe has an ST-deep K/V ring in shared memory and
+// NSB score buffers in TMEM; the softmax writes P (bf16) over the scores it has
+// just read, and the P V product takes P straight from TMEM as its A operand,
+// so P never touches shared memory. A score buffer is refilled only after the
+// P V product that read its P has completed. At the end pipe 1's (m, l, O) is
+// merged into pipe 0's through shared memory and TMEM.
 // Threads: 8 softmax warps, 2 MMA warps, and 2 (dense: TMA) or 4 (reuse:
 // gathers, two warps per pipeline taking turns by chunk) producer warps.
 template <bool REUSE> __host__ __device__ constexpr int fa_threads() { return REUSE ? 448 : 384; }
 template <bool REUSE> __host__ __device__ constexpr int fa_producers() { return REUSE ? 2 : 1; }
 
-// Per-pipeline shared memory for KC-key chunks and an ST-deep K/V ring. The
-// P tile keeps a 128-byte row pitch (K-major, 128-byte swizzle) for any KC.
-template <int KC, int ST>
-struct Fa2Pipe {
-  static constexpr int KHALF = KC * 128;           // one 64-dim half of a K (or V) chunk
-  static constexpr int KV_BYTES = 2 * KHALF;
-  static constexpr int P_BYTES = kTile * 128;      // 16 KB
-  static constexpr int K0 = 0;
-  static constexpr int V0 = K0 + ST * KV_BYTES;
-  static constexpr int P0 = V0 + ST * KV_BYTES;    // P[2]
-  static constexpr int BYTES = P0 + 2 * P_BYTES;   // 96 KB for (64, 2) and (32, 4)
-};
-template <int KC, int ST>
+// Chunk shape: KC keys per chunk, ST-deep K/V ring, NSB score buffers per
+// pipeline (NSB * KC + 128 O columns = 256 TMEM columns per pipeline).
+// Dense and anchor layers stream 64-key TMA tiles; reuse layers gather
+// 32-key chunks.
+template <bool REUSE> struct FaShape { static constexpr int KC = 64, ST = 3, NSB = 2; };
+template <> struct FaShape<true> { static constexpr int KC = 32, ST = 6, NSB = 4; };
+
+template <bool REUSE>
 struct Fa2Smem {
-  using Pp = Fa2Pipe<KC, ST>;
+  static constexpr int KC = FaShape<REUSE>::KC, ST = FaShape<REUSE>::ST;
+  static constexpr int NSB = FaShape<REUSE>::NSB;
+  static constexpr int KHALF = KC * 128;             // one 64-dim half of a K (or V) chunk
+  static constexpr int KV_BYTES = 2 * KHALF;
+  static constexpr int K0 = 0;                       // within a pipeline's area
+  static constexpr int V0 = ST * KV_BYTES;
+  static constexpr int PIPE_BYTES = 2 * ST * KV_BYTES;
   static constexpr int Q = 0;
   static constexpr int PIPE0 = kTileBytes;
-  static constexpr int PIPE1 = PIPE0 + Pp::BYTES;
-  static constexpr int POS = PIPE1 + Pp::BYTES;          // int32 [2 pipes][ST][KC]
-  static constexpr int BAR = POS + 2 * ST * KC * 4;      // [2 pipes][16] mbarriers + q_full
-  static constexpr int TMEM = BAR + (2 * 16 + 1) * 8;
-  static constexpr int BYTES = TMEM + 16;
-  static constexpr size_t SMEM = BYTES + 1024;
+  static constexpr int PIPE1 = PIPE0 + PIPE_BYTES;
+  static constexpr int POS = PIPE1 + PIPE_BYTES;     // reuse: int32 [2 pipes][ST][KC]
+  static constexpr int POS_BYTES = REUSE ? 2 * ST * KC * 4 : 0;
+  static constexpr int NB = 2 * ST + 3 * NSB;        // mbarriers per pipeline
+  static constexpr int BAR = POS + POS_BYTES;        // [2 pipes][NB] + q_full
+  static constexpr int TMEM = BAR + (2 * NB + 1) * 8;
+  static constexpr int BYTES = TMEM + 8;
+  static constexpr size_t SMEM = BYTES + 1024;       // + slack for 1024-byte alignment
   static_assert(SMEM <= 232448, "the tile and two pipelines must fit in shared memory");
+  static_assert(NSB * KC + 128 <= 256, "a pipeline owns 256 TMEM columns");
+  static_assert(KC % 32 == 0 && KC <= 64, "softmax reads scores 32 columns at a time");
 };
-// Dense and anchor layers stream 64-key TMA tiles two deep; reuse layers
-// gather 32-key chunks four deep.
-template <bool REUSE> struct FaShape { static constexpr int KC = 64, ST = 2; };
-template <> struct FaShape<true> { static constexpr int KC = 32, ST = 4; };
+
+// P (KC bf16 per row, packed in pairs) into KC/2 TMEM columns of this warp's lanes.
+template <int KC>
+__device__ __forceinline__ void tmem_store_p(uint32_t taddr, const uint32_t (&pk)[KC / 2]) {
+  if constexpr (KC == 64) {
+    tmem_st32(taddr, pk);
+  } else {
+    static_assert(KC == 32, "P chunks are 32 or 64 keys");
+    tmem_st16(taddr, pk);
+  }
+}
 
 template <bool REUSE, bool LSE>
 __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     k_prefill_fa2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillArgs a) {
-  constexpr int kKC = FaShape<REUSE>::KC, kST = FaShape<REUSE>::ST;
+  using SM = Fa2Smem<REUSE>;
+  constexpr int kKC = SM::KC, kST = SM::ST, kNSB = SM::NSB;
   constexpr int kProd = fa_producers<REUSE>();
-  using C = Fa2Pipe<kKC, kST>;
-  using SM = Fa2Smem<kKC, kST>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -119,17 +133,16 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   unsigned char* ps = sm + (pipe ? SM::PIPE1 : SM::PIPE0);
   int32_t* s_pos = reinterpret_cast<int32_t*>(sm + SM::POS) + pipe * kST * kKC;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::BAR);
-  uint64_t* q_full = bars + 32;
-  uint64_t* bar = bars + pipe * 16;
-  uint64_t* kv_full = bar + 0;   // [kST <= 4]
-  uint64_t* kv_free = bar + 4;   // [kST]
-  uint64_t* s_full = bar + 8;    // [2]
-  uint64_t* s_free = bar + 10;   // [2]
-  uint64_t* p_full = bar + 12;   // [2]
-  uint64_t* pv_done = bar + 14;  // [2] PV of the chunk that used P buffer b
+  uint64_t* q_full = bars + 2 * SM::NB;
+  uint64_t* bar = bars + pipe * SM::NB;
+  uint64_t* kv_full = bar;                    // [kST]
+  uint64_t* kv_free = bar + kST;              // [kST]
+  uint64_t* s_full = bar + 2 * kST;           // [kNSB] scores of chunk i in buffer i % kNSB
+  uint64_t* p_full = s_full + kNSB;           // [kNSB] P of chunk i written over them
+  uint64_t* pv_done = p_full + kNSB;          // [kNSB] the P V product of that chunk
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + SM::TMEM);
-  const uint32_t sQ = smem_u32(sm + SM::Q), sK0 = smem_u32(ps + C::K0);
-  const uint32_t sV0 = smem_u32(ps + C::V0), sP0 = smem_u32(ps + C::P0);
+  const uint32_t sQ = smem_u32(sm + SM::Q), sK0 = smem_u32(ps + SM::K0);
+  const uint32_t sV0 = smem_u32(ps + SM::V0);
 
   const int BH = a.B * a.Hq;
   const int bh = static_cast<int>(blockIdx.x) % BH;
@@ -150,18 +163,17 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   const int kv_row_base = (b * a.Hkv + g) * a.N;
 
   if (threadIdx.x < 2) {   // thread p initialises pipe p's barriers
-    uint64_t* pb = bars + threadIdx.x * 16;
+    uint64_t* pb = bars + threadIdx.x * SM::NB;
     for (int s = 0; s < kST; ++s) {
-      mbar_init(pb + 0 + s, REUSE ? 32 : 1);
-      mbar_init(pb + 4 + s, 1);
+      mbar_init(pb + s, REUSE ? 32 : 1);
+      mbar_init(pb + kST + s, 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(pb + 8 + s, 1);
-      mbar_init(pb + 10 + s, 128);
-      mbar_init(pb + 12 + s, 128);
-      mbar_init(pb + 14 + s, 1);
+    for (int s = 0; s < kNSB; ++s) {
+      mbar_init(pb + 2 * kST + s, 1);
+      mbar_init(pb + 2 * kST + kNSB + s, 128);
+      mbar_init(pb + 2 * kST + 2 * kNSB + s, 1);
     }
-    if (threadIdx.x == 0) mbar_init(bars + 32, 1);
+    if (threadIdx.x == 0) mbar_init(q_full, 1);
     fence_barrier_init();
   }
   if (warp == 8) tmem_alloc(s_tmem, 512);
@@ -169,7 +181,7 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
-  const uint32_t tS = tmem_base + pipe * 256, tO = tS + 128;   // S[2] at +0/+64, O at +128
+  const uint32_t tS = tmem_base + pipe * 256, tO = tS + 128;   // S[kNSB] at +0, O at +128
 
   if (role == 2) {
     // ------------------------------------------------ producer
@@ -185,14 +197,14 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
         for (int i = 0; i < np; ++i) {
           const int s = i % kST, j = 2 * i + pipe;
           if (!mbar_wait(kv_free + s, ((i / kST) & 1) ^ 1, a.err, 0x601)) break;
-          unsigned char* kd = ps + C::K0 + s * C::KV_BYTES;
-          unsigned char* vd = ps + C::V0 + s * C::KV_BYTES;
-          mbar_arrive_expect_tx(kv_full + s, 2 * C::KV_BYTES);
+          unsigned char* kd = ps + SM::K0 + s * SM::KV_BYTES;
+          unsigned char* vd = ps + SM::V0 + s * SM::KV_BYTES;
+          mbar_arrive_expect_tx(kv_full + s, 2 * SM::KV_BYTES);
           const int y = kv_row_base + j * kKC;
           tma_load_2d(kd, &tmK, kv_full + s, 0, y);
-          tma_load_2d(kd + C::KHALF, &tmK, kv_full + s, 64, y);
+          tma_load_2d(kd + SM::KHALF, &tmK, kv_full + s, 64, y);
           tma_load_2d(vd, &tmV, kv_full + s, 0, y);
-          tma_load_2d(vd + C::KHALF, &tmV, kv_full + s, 64, y);
+          tma_load_2d(vd + SM::KHALF, &tmV, kv_full + s, 64, y);
           issued = i + 1;
         }
         for (int i = issued > kST ? issued - kST : 0; i < issued; ++i)
@@ -210,8 +222,8 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
         int ok = 1;
         if (lane == 0) ok = mbar_wait(kv_free + s, ((i / kST) & 1) ^ 1, a.err, 0x605);
         if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        unsigned char* kd = ps + C::K0 + s * C::KV_BYTES;
-        unsigned char* vd = ps + C::V0 + s * C::KV_BYTES;
+        unsigned char* kd = ps + SM::K0 + s * SM::KV_BYTES;
+        unsigned char* vd = ps + SM::V0 + s * SM::KV_BYTES;
 #pragma unroll
         for (int half = 0; half < kKC / 32; ++half) {
           const int pt = lane + 32 * half;   // key row within the chunk
@@ -228,7 +240,7 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
           const __nv_bfloat16* vsrc = vbase + row * 128;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
-            const int off = (c >> 3) * C::KHALF + pt * 128 + (((c & 7) ^ (pt & 7)) << 4);
+            const int off = (c >> 3) * SM::KHALF + pt * 128 + (((c & 7) ^ (pt & 7)) << 4);
             cp_async16(kd + off, ksrc + c * 8, 16);
             cp_async16(vd + off, vsrc + c * 8, 16);
           }
@@ -246,29 +258,30 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
       constexpr uint32_t idq = idesc_bf16_f32(128, kKC, 0, 0);
       constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
       bool ok = mbar_wait(q_full, 0, a.err, 0x611);
+      // O += P V with P (A operand) read from the score buffer in TMEM
       auto issue_pv = [&](int ii) {
-        const int s = ii % kST, pb = ii & 1;
-        if (!mbar_wait(p_full + pb, (ii >> 1) & 1, a.err, 0x612)) return false;
+        const int s = ii % kST, pb = ii % kNSB;
+        if (!mbar_wait(p_full + pb, (ii / kNSB) & 1, a.err, 0x612)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kKC / 16; ++kk)
-          tc_mma(tO, kmajor_desc(sP0 + pb * C::P_BYTES, kk),
-                 vmn_desc(sV0 + s * C::KV_BYTES, kk, C::KHALF), idv,
-                 (ii > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tO, tS + pb * kKC + kk * 8, vmn_desc(sV0 + s * SM::KV_BYTES, kk, SM::KHALF),
+                    idv, (ii > 0 || kk > 0) ? 1u : 0u);
         tc_commit(pv_done + pb);
         tc_commit(kv_free + s);
         return true;
       };
       for (int i = 0; ok && i < np; ++i) {
-        const int s = i % kST, sb = i & 1;
-        ok = mbar_wait(kv_full + s, (i / kST) & 1, a.err, 0x613) &&
-             mbar_wait(s_free + sb, ((i >> 1) & 1) ^ 1, a.err, 0x614);
+        const int s = i % kST, sb = i % kNSB;
+        ok = mbar_wait(kv_full + s, (i / kST) & 1, a.err, 0x613);
+        // the buffer's previous P must have been consumed by its P V product
+        if (ok && i >= kNSB) ok = mbar_wait(pv_done + sb, ((i / kNSB) - 1) & 1, a.err, 0x614);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc_mma(tS + sb * kKC, kmajor_desc(sQ, kk),
-                 kmajor_desc(sK0 + s * C::KV_BYTES, kk, C::KHALF), idq, kk > 0 ? 1u : 0u);
+                 kmajor_desc(sK0 + s * SM::KV_BYTES, kk, SM::KHALF), idq, kk > 0 ? 1u : 0u);
         tc_commit(s_full + sb);
         if (i > 0) ok = issue_pv(i - 1);
       }
@@ -282,8 +295,8 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     float m_used = kNegInfP, l = 0.f;
     bool ok = true;
     for (int i = 0; i < np; ++i) {
-      const int sb = i & 1, s = i % kST, j = 2 * i + pipe;
-      ok = mbar_wait(s_full + sb, (i >> 1) & 1, a.err, 0x621);
+      const int sb = i % kNSB, s = i % kST, j = 2 * i + pipe;
+      ok = mbar_wait(s_full + sb, (i / kNSB) & 1, a.err, 0x621);
       if (!ok) break;
       tc_fence_after();
       float x[kKC];
@@ -295,21 +308,22 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
       }
-      tc_fence_before();
-      mbar_arrive(s_free + sb);
       const bool need_mask = REUSE || (j * kKC + kKC - 1 > row0);
-      float tmax = kNegInfP;
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < kKC; ++c) {
           const int kp = REUSE ? s_pos[s * kKC + c] : j * kKC + c;
           if (!(kp >= 0 && kp <= row)) x[c] = kNegInfP;
-          tmax = fmaxf(tmax, x[c]);
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kKC; ++c) tmax = fmaxf(tmax, x[c]);
       }
+      // row maximum as a tree (short dependency chains)
+      float mx[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mx[c] = x[c];
+#pragma unroll
+      for (int c = 8; c < kKC; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       tmax *= a.scale_log2;
       float alpha = 1.f;
       bool resc = false;
@@ -323,21 +337,21 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
       }
       const float mu = (m_used == kNegInfP) ? 0.f : m_used;
       uint32_t pk[kKC / 2];
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kKC / 2; ++c) {
         const float p0 = ex2_approx(fmaf(x[2 * c], a.scale_log2, -mu));
         const float p1 = ex2_approx(fmaf(x[2 * c + 1], a.scale_log2, -mu));
-        l += p0 + p1;
+        ls[c & 3] += p0 + p1;
         pk[c] = pack_bf16(p0, p1);
       }
-      // P buffer sb was last read by PV(i-2); a rescale of O also needs PV(i-1)
-      if (i >= 2) {
-        ok = mbar_wait(pv_done + sb, ((i >> 1) - 1) & 1, a.err, 0x622);
-        if (!ok) break;
-      }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       if (__any_sync(0xffffffffu, resc)) {
-        ok = mbar_wait(pv_done + (sb ^ 1), ((i - 1) >> 1) & 1, a.err, 0x624);
-        if (!ok) break;
+        // O may change only once the previous P V product has landed
+        if (i > 0) {
+          ok = mbar_wait(pv_done + ((i - 1) % kNSB), ((i - 1) / kNSB) & 1, a.err, 0x624);
+          if (!ok) break;
+        }
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -348,23 +362,18 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(tO + c * 32 + lane_base, o);
         }
-        tmem_wait_st();
       }
-      const uint32_t sP = sP0 + sb * C::P_BYTES;
-#pragma unroll
-      for (int ch = 0; ch < kKC / 8; ++ch) {
-        const uint32_t addr = sP + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[4 * ch]),
-                     "r"(pk[4 * ch + 1]), "r"(pk[4 * ch + 2]), "r"(pk[4 * ch + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
+      // P over the first kKC/2 columns of the scores it came from
+      tmem_store_p<kKC>(tS + sb * kKC + lane_base, pk);
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(p_full + sb);
     }
     // wait for this pipe's last P V, then merge pipe 1 into pipe 0
-    if (ok && np > 0) ok = mbar_wait(pv_done + ((np - 1) & 1), ((np - 1) >> 1) & 1, a.err, 0x623);
-    float* xch = reinterpret_cast<float*>(sm + SM::PIPE1 + C::P0);   // pipe 1's P, now free
+    if (ok && np > 0)
+      ok = mbar_wait(pv_done + ((np - 1) % kNSB), ((np - 1) / kNSB) & 1, a.err, 0x623);
+    // pipe 1's K ring is idle once its last P V has completed
+    float* xch = reinterpret_cast<float*>(sm + SM::PIPE1 + SM::K0);
     if (pipe == 1) {
       xch[r] = np > 0 ? m_used : kNegInfP;
       xch[128 + r] = np > 0 ? l : 0.f;
@@ -566,10 +575,9 @@ bool make_maps(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUtensorM
 
 template <bool REUSE, bool LSE>
 cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
-  constexpr int KC = FaShape<REUSE>::KC, ST = FaShape<REUSE>::ST;
-  using SM = Fa2Smem<KC, ST>;
+  using SM = Fa2Smem<REUSE>;
   alignas(64) CUtensorMap tq, tk, tv;
-  if (!make_maps(a, &tq, &tk, &tv, KC)) return cudaErrorInvalidValue;
+  if (!make_maps(a, &tq, &tk, &tv, SM::KC)) return cudaErrorInvalidValue;
   auto kern = k_prefill_fa2<REUSE, LSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SM::SMEM));
