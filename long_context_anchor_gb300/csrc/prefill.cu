@@ -57,19 +57,16 @@ __device__ __forceinline__ void fa_tile_coords(const PrefillArgs& a, int& bh, in
 
 // One query tile per CTA, its key chunks split over two pipelines (pipe p takes
 // chunks p, p+2, ...): warps 4p..4p+3 run pipe p's softmax, warp 8+p issues its
-// MMAs, warp 10+p is its producer (TMA for Q and dense K/V); for reuse, warps
-// 10+p and 12+p gather pipe p's chunks in turn with 16-byte cp.async (each
-// waits for its own copies, so two chunks per pipeline are in flight).
+// MMAs, warp 10+p is its producer (TMA for Q and dense K/V; for reuse, coalesced
+// 16-byte cp.async gathers of the saved rows, several chunks in flight).
 // The Q tile is shared. Every pipe has an ST-deep K/V ring in shared memory and
 // NSB score buffers in TMEM; the softmax writes P (bf16) over the scores it has
 // just read, and the P V product takes P straight from TMEM as its A operand,
 // so P never touches shared memory. A score buffer is refilled only after the
 // P V product that read its P has completed. At the end pipe 1's (m, l, O) is
 // merged into pipe 0's through shared memory and TMEM.
-// Threads: 8 softmax warps, 2 MMA warps, and 2 (dense: TMA) or 4 (reuse:
-// gathers, two warps per pipeline taking turns by chunk) producer warps.
-template <bool REUSE> __host__ __device__ constexpr int fa_threads() { return REUSE ? 448 : 384; }
-template <bool REUSE> __host__ __device__ constexpr int fa_producers() { return REUSE ? 2 : 1; }
+// Threads: 8 softmax warps, 2 MMA warps, 2 producer warps.
+constexpr int kFaThreads = 384;
 
 // Chunk shape: KC keys per chunk, ST-deep K/V ring, NSB score buffers per
 // pipeline (NSB * KC + 128 O columns = 256 TMEM columns per pipeline).
@@ -90,8 +87,8 @@ struct Fa2Smem {
   static constexpr int Q = 0;
   static constexpr int PIPE0 = kTileBytes;
   static constexpr int PIPE1 = PIPE0 + PIPE_BYTES;
-  static constexpr int POS = PIPE1 + PIPE_BYTES;     // reuse: int32 [2 pipes][ST][KC]
-  static constexpr int POS_BYTES = REUSE ? 2 * ST * KC * 4 : 0;
+  static constexpr int POS = PIPE1 + PIPE_BYTES;     // reuse: int32 [2 pipes][ST][KC] + flags [2][ST]
+  static constexpr int POS_BYTES = REUSE ? 2 * ST * (KC + 1) * 4 : 0;
   static constexpr int NB = 2 * ST + 3 * NSB;        // mbarriers per pipeline
   static constexpr int BAR = POS + POS_BYTES;        // [2 pipes][NB] + q_full
   static constexpr int TMEM = BAR + (2 * NB + 1) * 8;
@@ -114,12 +111,11 @@ __device__ __forceinline__ void tmem_store_p(uint32_t taddr, const uint32_t (&pk
 }
 
 template <bool REUSE, bool LSE>
-__global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
+__global__ void __launch_bounds__(kFaThreads, 1)
     k_prefill_fa2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillArgs a) {
   using SM = Fa2Smem<REUSE>;
   constexpr int kKC = SM::KC, kST = SM::ST, kNSB = SM::NSB;
-  constexpr int kProd = fa_producers<REUSE>();
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -127,11 +123,12 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   int pipe, role;   // role: 0 softmax, 1 MMA, 2 producer
   if (warp < 8) { pipe = warp >> 2; role = 0; }
   else if (warp < 10) { pipe = warp - 8; role = 1; }
-  else { pipe = (warp - 10) & 1; role = 2; }
-  const int prod = (warp - 10) >> 1;   // producer index within its pipeline
+  else { pipe = warp - 10; role = 2; }
 
   unsigned char* ps = sm + (pipe ? SM::PIPE1 : SM::PIPE0);
   int32_t* s_pos = reinterpret_cast<int32_t*>(sm + SM::POS) + pipe * kST * kKC;
+  // reuse: 1 if chunk stage s needs no causal mask
+  int32_t* s_flag = reinterpret_cast<int32_t*>(sm + SM::POS) + 2 * kST * kKC + pipe * kST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::BAR);
   uint64_t* q_full = bars + 2 * SM::NB;
   uint64_t* bar = bars + pipe * SM::NB;
@@ -185,7 +182,7 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
 
   if (role == 2) {
     // ------------------------------------------------ producer
-    if (pipe == 0 && prod == 0 && lane == 0) {
+    if (pipe == 0 && lane == 0) {
       prefetch_tmap(&tmQ);
       mbar_arrive_expect_tx(q_full, kTileBytes);
       tma_load_2d(sm + SM::Q, &tmQ, q_full, 0, bh * a.N + row0);
@@ -211,47 +208,97 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
           mbar_wait(kv_full + (i % kST), (i / kST) & 1, a.err, 0x604);
       }
     } else {
+      // One gather warp per pipeline with up to kDepth chunks in flight: a
+      // chunk is released (kv_full) once its copies have landed. Before waiting
+      // for a ring stage that is still busy, the warp releases every chunk it
+      // has in flight, so the MMA issuer never waits on copies held back
+      // behind that wait. Positions are read one chunk ahead.
+      constexpr int kDepth = kST > 1 ? kST - 1 : 1;
       int p_first = __ldg(idx_row);
       if (p_first < 0 || p_first >= a.N) p_first = 0;
       const __nv_bfloat16* kbase = static_cast<const __nv_bfloat16*>(a.k);
       const __nv_bfloat16* vbase = static_cast<const __nv_bfloat16*>(a.v);
-      // producer `prod` gathers this pipeline's chunks i = prod, prod + kProd,
-      // ...; each waits for its own copies, so kProd chunks are in flight
-      for (int i = prod; i < np; i += kProd) {
-        const int s = i % kST, j = 2 * i + pipe;
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(kv_free + s, ((i / kST) & 1) ^ 1, a.err, 0x605);
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        unsigned char* kd = ps + SM::K0 + s * SM::KV_BYTES;
-        unsigned char* vd = ps + SM::V0 + s * SM::KV_BYTES;
+      auto read_pos = [&](int i, int (&pos)[kKC / 32]) {
 #pragma unroll
         for (int half = 0; half < kKC / 32; ++half) {
-          const int pt = lane + 32 * half;   // key row within the chunk
+          const int e = (2 * i + pipe) * kKC + lane + 32 * half;
+          pos[half] = e < kt ? __ldg(idx_row + e) : -1;
+        }
+      };
+      auto release_all = [&](int from, int to) {
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        for (int c = from; c < to; ++c) mbar_arrive(kv_full + c % kST);
+      };
+      int nxt[kKC / 32];
+      if (np > 0) read_pos(0, nxt);
+      int issued = 0, released = 0;
+      for (int i = 0; i < np; ++i) {
+        const int s = i % kST, j = 2 * i + pipe;
+        int pos[kKC / 32];
+#pragma unroll
+        for (int half = 0; half < kKC / 32; ++half) pos[half] = nxt[half];
+        if (i + 1 < np) read_pos(i + 1, nxt);
+        const uint32_t par = ((i / kST) & 1) ^ 1;
+        int ready = lane == 0 ? mbar_test_wait(kv_free + s, par) : 0;
+        if (!__shfl_sync(0xffffffffu, ready, 0)) {
+          release_all(released, issued);
+          released = issued;
+          int ok = 1;
+          if (lane == 0) ok = mbar_wait(kv_free + s, par, a.err, 0x605);
+          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        }
+        unsigned char* kd = ps + SM::K0 + s * SM::KV_BYTES;
+        unsigned char* vd = ps + SM::V0 + s * SM::KV_BYTES;
+        // validate; padding slots (-1) re-read the tile's first saved row and
+        // are masked later
+        int src[kKC / 32], pmax = -1;
+        bool all_valid = true;
+#pragma unroll
+        for (int half = 0; half < kKC / 32; ++half) {
+          const int pt = lane + 32 * half;
           const int e = j * kKC + pt;
-          int p = e < kt ? __ldg(idx_row + e) : -1;
+          int p = pos[half];
           if (p >= a.N || (e < kt && p < 0)) {
             report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x602);
             p = -1;
           }
           s_pos[s * kKC + pt] = p;
-          // padding slots re-read the tile's first saved row (masked later)
-          const size_t row = static_cast<size_t>(kv_row_base) + (p >= 0 ? p : p_first);
-          const __nv_bfloat16* ksrc = kbase + row * 128;
-          const __nv_bfloat16* vsrc = vbase + row * 128;
+          src[half] = p >= 0 ? p : p_first;
+          all_valid = all_valid && p >= 0;
+          pmax = max(pmax, p);
+        }
+        // a chunk of valid keys that all precede the tile's first row needs
+        // no causal mask in any of its rows
+        all_valid = __all_sync(0xffffffffu, all_valid);
+        pmax = __reduce_max_sync(0xffffffffu, pmax);
+        if (lane == 0) s_flag[s] = (all_valid && pmax <= row0) ? 1 : 0;
+        // coalesced copies: a half-warp moves one 256-byte row (16 lanes x 16
+        // bytes), so each instruction fills two rows of K (or V) in full
+        const int sub = lane >> 4, c16 = lane & 15;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const int off = (c >> 3) * SM::KHALF + pt * 128 + (((c & 7) ^ (pt & 7)) << 4);
-            cp_async16(kd + off, ksrc + c * 8, 16);
-            cp_async16(vd + off, vsrc + c * 8, 16);
-          }
+        for (int rr = 0; rr < kKC / 2; ++rr) {
+          const int pt = 2 * rr + sub;
+          const int prow = __shfl_sync(0xffffffffu, src[(2 * rr) >> 5], pt & 31);
+          const size_t off_g = (static_cast<size_t>(kv_row_base) + prow) * 128 + c16 * 8;
+          const int off = (c16 >> 3) * SM::KHALF + pt * 128 + (((c16 & 7) ^ (pt & 7)) << 4);
+          cp_async16(kd + off, kbase + off_g, 16);
+          cp_async16(vd + off, vbase + off_g, 16);
         }
         cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        mbar_arrive(kv_full + s);
+        issued = i + 1;
+        if (issued - released >= kDepth) {   // the oldest chunk in flight has landed
+          cp_async_wait<kDepth - 1>();
+          fence_proxy_async_smem();
+          mbar_arrive(kv_full + released % kST);
+          ++released;
+        }
       }
+      // release what is still in flight (also after an error, so that no copy
+      // outlives the kernel)
+      release_all(released, issued);
     }
-    if (pipe == 0 && prod == 0 && lane == 0) mbar_wait(q_full, 0, a.err, 0x603);   // no copies left in flight
+    if (pipe == 0 && lane == 0) mbar_wait(q_full, 0, a.err, 0x603);   // no copies left in flight
   } else if (role == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -271,21 +318,27 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
         tc_commit(kv_free + s);
         return true;
       };
-      for (int i = 0; ok && i < np; ++i) {
+      // S = Q K^T of chunk i into score buffer i % kNSB, once that buffer's
+      // previous P has been consumed by its P V product
+      auto issue_s = [&](int i) {
         const int s = i % kST, sb = i % kNSB;
-        ok = mbar_wait(kv_full + s, (i / kST) & 1, a.err, 0x613);
-        // the buffer's previous P must have been consumed by its P V product
-        if (ok && i >= kNSB) ok = mbar_wait(pv_done + sb, ((i / kNSB) - 1) & 1, a.err, 0x614);
-        if (!ok) break;
+        if (!mbar_wait(kv_full + s, (i / kST) & 1, a.err, 0x613)) return false;
+        if (i >= kNSB && !mbar_wait(pv_done + sb, ((i / kNSB) - 1) & 1, a.err, 0x614))
+          return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc_mma(tS + sb * kKC, kmajor_desc(sQ, kk),
                  kmajor_desc(sK0 + s * SM::KV_BYTES, kk, SM::KHALF), idq, kk > 0 ? 1u : 0u);
         tc_commit(s_full + sb);
-        if (i > 0) ok = issue_pv(i - 1);
+        return true;
+      };
+      // scores run kNSB - 1 chunks ahead of the P V products
+      for (int i = 0; ok && i < min(np, kNSB - 1); ++i) ok = issue_s(i);
+      for (int i = 0; ok && i < np; ++i) {
+        if (i + kNSB - 1 < np) ok = issue_s(i + kNSB - 1);
+        if (ok) ok = issue_pv(i);
       }
-      if (ok && np > 0) issue_pv(np - 1);
     }
   } else {
     // ------------------------------------------------ softmax warpgroups
@@ -308,7 +361,7 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
       }
-      const bool need_mask = REUSE || (j * kKC + kKC - 1 > row0);
+      const bool need_mask = REUSE ? (s_flag[s] == 0) : (j * kKC + kKC - 1 > row0);
       if (need_mask) {
 #pragma unroll
         for (int c = 0; c < kKC; ++c) {
@@ -582,7 +635,7 @@ cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SM::SMEM));
   if (e != cudaSuccess) return e;
-  kern<<<a.B * a.Hq * a.nT, fa_threads<REUSE>(), SM::SMEM, st>>>(tq, tk, tv, a);
+  kern<<<a.B * a.Hq * a.nT, kFaThreads, SM::SMEM, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
