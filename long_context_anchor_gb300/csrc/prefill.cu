@@ -73,7 +73,7 @@ constexpr int kFaThreads = 384;
 // Dense and anchor layers stream 64-key TMA tiles; reuse layers gather
 // 32-key chunks.
 template <bool REUSE> struct FaShape { static constexpr int KC = 64, ST = 3, NSB = 2; };
-template <> struct FaShape<true> { static constexpr int KC = 32, ST = 6, NSB = 4; };
+template <> struct FaShape<true> { static constexpr int KC = 64, ST = 3, NSB = 2; };
 
 template <bool REUSE>
 struct Fa2Smem {
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
     if (pipe == 0 && lane == 0) mbar_wait(q_full, 0, a.err, 0x603);   // no copies left in flight
   } else if (role == 1) {
     // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t idq = idesc_bf16_f32(128, kKC, 0, 0);
       constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
       bool ok = mbar_wait(q_full, 0, a.err, 0x611);
@@ -562,7 +562,7 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         mbar_wait(k_full + (j & 1), (j >> 1) & 1, a.err, 0x703);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    {
       constexpr uint32_t id = idesc_bf16_f32(128, 128, 0, 0);
       bool ok = mbar_wait(q_full, 0, a.err, 0x711);
       for (int j = 0; ok && j < nkv; ++j) {
