@@ -35,7 +35,7 @@ namespace {
 constexpr int kTile = 128;              // query rows and keys per tile
 constexpr int kHalf = kTile * 128;      // bytes of one 64-column half of a tile
 constexpr int kTileBytes = 2 * kHalf;   // 128 x 128 bf16 = 32 KB
-constexpr int kWtThreads = 256;         // weights kernel: warp 0 TMA, warp 1 MMA, warps 4-7 epilogue
+constexpr int kWtThreads = 384;         // weights kernel: warp 0 TMA, warp 1 MMA, warps 4-11 epilogue
 constexpr float kRescaleLog2 = 8.0f;    // lazy O rescale threshold (factor 256)
 #define kNegInfP (-CUDART_INF_F)
 
@@ -483,16 +483,24 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 
 // ------------------------------------------------------------------------
 // Anchor pass 2: tile weights from S^T = K_j Q_t^T (TMEM lane = key).
+// Warp 0 loads the Q tile once and the key tiles 0..t into a kWtKS-deep ring
+// by TMA; warp 1 issues S^T(j) into TMEM score buffer j % kWtSB; two epilogue
+// warpgroups (warps 4-7 and 8-11) take the key tiles in turn (even / odd j),
+// each thread owning one key of the tile: it sums 2^(s*sigma*log2e - lse2)
+// over the tile's query rows i >= key, with no cross-lane reduction.
 // ------------------------------------------------------------------------
+constexpr int kWtKS = 4;   // key-tile ring stages
+constexpr int kWtSB = 4;   // TMEM score buffers (128 columns each)
 struct WtSmem {
   static constexpr int Q = 0;
-  static constexpr int K0 = Q + kTileBytes;      // K[2]
-  static constexpr int LSE = K0 + 2 * kTileBytes;  // float [128]
-  static constexpr int BAR = LSE + kTile * 4;
-  static constexpr int TMEM = BAR + 16 * 8;
-  static constexpr int BYTES = TMEM + 16;
+  static constexpr int K0 = Q + kTileBytes;            // K[kWtKS]
+  static constexpr int LSE = K0 + kWtKS * kTileBytes;  // float [128]
+  static constexpr int BAR = LSE + kTile * 4;          // q_full, k_full[KS], k_free[KS], s_full[SB], s_free[SB]
+  static constexpr int TMEM = BAR + (1 + 2 * kWtKS + 2 * kWtSB) * 8;
+  static constexpr int BYTES = TMEM + 8;
 };
 constexpr size_t kWtSmemBytes = WtSmem::BYTES + 1024;
+static_assert(kWtSmemBytes <= 232448, "weights kernel shared memory");
 
 __global__ void __launch_bounds__(kWtThreads, 1)
     k_prefill_weights(const __grid_constant__ CUtensorMap tmQ,
@@ -502,11 +510,11 @@ __global__ void __launch_bounds__(kWtThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* s_lse = reinterpret_cast<float*>(sm + WtSmem::LSE);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + WtSmem::BAR);
-  uint64_t* q_full = bar + 0;
-  uint64_t* k_full = bar + 1;   // [2]
-  uint64_t* k_free = bar + 3;   // [2]
-  uint64_t* s_full = bar + 5;   // [2]
-  uint64_t* s_free = bar + 7;   // [2]
+  uint64_t* q_full = bar;
+  uint64_t* k_full = bar + 1;                      // [kWtKS]
+  uint64_t* k_free = k_full + kWtKS;               // [kWtKS]
+  uint64_t* s_full = k_free + kWtKS;               // [kWtSB]
+  uint64_t* s_free = s_full + kWtSB;               // [kWtSB]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + WtSmem::TMEM);
   const uint32_t sQ = smem_u32(sm + WtSmem::Q), sK0 = smem_u32(sm + WtSmem::K0);
 
@@ -520,20 +528,22 @@ __global__ void __launch_bounds__(kWtThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kWtKS; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_free + s, 1);
+    }
+    for (int s = 0; s < kWtSB; ++s) {
       mbar_init(s_full + s, 1);
       mbar_init(s_free + s, 128);
     }
     fence_barrier_init();
   }
-  if (warp >= 4) {
+  if (warp >= 4 && warp < 8) {
     const int r = threadIdx.x - 128;
     const int i = row0 + r;
     s_lse[r] = i < a.N ? a.lse[static_cast<size_t>(bh) * a.N + i] : CUDART_INF_F;
   }
-  if (warp == 2) tmem_alloc(s_tmem, 256);
+  if (warp == 2) tmem_alloc(s_tmem, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -549,8 +559,8 @@ __global__ void __launch_bounds__(kWtThreads, 1)
       tma_load_2d(sm + WtSmem::Q + kHalf, &tmQ, q_full, 64, bh * a.N + row0);
       int issued = 0;
       for (int j = 0; j < nkv; ++j) {
-        const int s = j & 1;
-        if (!mbar_wait(k_free + s, ((j >> 1) & 1) ^ 1, a.err, 0x701)) break;
+        const int s = j % kWtKS;
+        if (!mbar_wait(k_free + s, ((j / kWtKS) & 1) ^ 1, a.err, 0x701)) break;
         unsigned char* kd = sm + WtSmem::K0 + s * kTileBytes;
         mbar_arrive_expect_tx(k_full + s, kTileBytes);
         tma_load_2d(kd, &tmK, k_full + s, 0, kv_row_base + j * kTile);
@@ -558,60 +568,76 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         issued = j + 1;
       }
       mbar_wait(q_full, 0, a.err, 0x702);
-      for (int j = issued > 2 ? issued - 2 : 0; j < issued; ++j)
-        mbar_wait(k_full + (j & 1), (j >> 1) & 1, a.err, 0x703);
+      for (int j = issued > kWtKS ? issued - kWtKS : 0; j < issued; ++j)
+        mbar_wait(k_full + (j % kWtKS), (j / kWtKS) & 1, a.err, 0x703);
     }
   } else if (warp == 1) {
-    {
+    {   // the whole warp runs the loop; one elected lane issues each MMA
       constexpr uint32_t id = idesc_bf16_f32(128, 128, 0, 0);
       bool ok = mbar_wait(q_full, 0, a.err, 0x711);
       for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j & 1;
-        ok = mbar_wait(k_full + s, (j >> 1) & 1, a.err, 0x712) &&
-             mbar_wait(s_free + s, ((j >> 1) & 1) ^ 1, a.err, 0x713);
+        const int s = j % kWtKS, sb = j % kWtSB;
+        ok = mbar_wait(k_full + s, (j / kWtKS) & 1, a.err, 0x712) &&
+             mbar_wait(s_free + sb, ((j / kWtSB) & 1) ^ 1, a.err, 0x713);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma(tmem + s * 128, kmajor_desc(sK0 + s * kTileBytes, kk), kmajor_desc(sQ, kk), id,
+          tc_mma(tmem + sb * 128, kmajor_desc(sK0 + s * kTileBytes, kk), kmajor_desc(sQ, kk), id,
                  kk > 0 ? 1u : 0u);
-        tc_commit(s_full + s);
+        tc_commit(s_full + sb);
         tc_commit(k_free + s);
       }
     }
   } else if (warp >= 4) {
-    const int r = threadIdx.x - 128;   // key lane within the key tile
+    const int grp = (warp - 4) >> 2;   // epilogue group: key tiles j = grp, grp + 2, ...
+    const int r = (warp & 3) * 32 + lane;   // key lane within the key tile
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* wrow = a.w + static_cast<size_t>(bh) * (static_cast<size_t>(64) * (a.nT - 1) * a.nT + a.N) +
                   static_cast<size_t>(64) * t * (t + 1);
-    for (int j = 0; j < nkv; ++j) {
-      const int s = j & 1;
-      if (!mbar_wait(s_full + s, (j >> 1) & 1, a.err, 0x721)) break;
+    for (int j = grp; j < nkv; j += 2) {
+      const int sb = j % kWtSB;
+      if (!mbar_wait(s_full + sb, (j / kWtSB) & 1, a.err, 0x721)) break;
       tc_fence_after();
       const int kj = j * kTile + r;
-      float sum = 0.f;
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      const uint32_t ts = tmem + sb * 128 + lane_base;
+      tmem_ld32(ts, v0);
+      tmem_ld32(ts + 32, v1);
+      tmem_ld32(ts + 64, v2);
+      tmem_ld32(ts + 96, v3);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free + sb);
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};
+      // only the diagonal key tile (j == t) needs the causal mask i >= key
+      const bool diag = (j * kTile + kTile - 1 > row0);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tmem + s * 128 + c * 32 + lane_base, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int q = c * 32 + e;
-          const float p = ex2_approx(__uint_as_float(v[e]) * a.scale_log2 - s_lse[q]);
-          sum += (kj <= row0 + q) ? p : 0.f;
+      for (int e = 0; e < 32; ++e) {
+        const float p0 = ex2_approx(__uint_as_float(v0[e]) * a.scale_log2 - s_lse[e]);
+        const float p1 = ex2_approx(__uint_as_float(v1[e]) * a.scale_log2 - s_lse[32 + e]);
+        const float p2 = ex2_approx(__uint_as_float(v2[e]) * a.scale_log2 - s_lse[64 + e]);
+        const float p3 = ex2_approx(__uint_as_float(v3[e]) * a.scale_log2 - s_lse[96 + e]);
+        if (diag) {
+          sum[0] += (kj <= row0 + e) ? p0 : 0.f;
+          sum[1] += (kj <= row0 + 32 + e) ? p1 : 0.f;
+          sum[2] += (kj <= row0 + 64 + e) ? p2 : 0.f;
+          sum[3] += (kj <= row0 + 96 + e) ? p3 : 0.f;
+        } else {
+          sum[0] += p0;
+          sum[1] += p1;
+          sum[2] += p2;
+          sum[3] += p3;
         }
       }
-      tc_fence_before();
-      mbar_arrive(s_free + s);
-      if (kj < L) wrow[kj] = sum;
+      if (kj < L) wrow[kj] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
