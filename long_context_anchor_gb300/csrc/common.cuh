@@ -113,6 +113,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t 
                "r"(src_bytes)
                : "memory");
 }
+// 16-byte global -> shared copy to a shared-memory address.
+__device__ __forceinline__ void cp_async16_s(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

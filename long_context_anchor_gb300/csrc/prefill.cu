@@ -57,23 +57,23 @@ __device__ __forceinline__ void fa_tile_coords(const PrefillArgs& a, int& bh, in
 
 // One query tile per CTA, its key chunks split over two pipelines (pipe p takes
 // chunks p, p+2, ...): warps 4p..4p+3 run pipe p's softmax, warp 8+p issues its
-// MMAs, warp 10+p is its producer (TMA for Q and dense K/V; for reuse, coalesced
-// 16-byte cp.async gathers of the saved rows, several chunks in flight).
+// MMAs, warp 10+p is its producer (TMA for Q and dense K/V); for reuse, warps
+// 10+p and 12+p gather pipe p's chunks in turn with coalesced 16-byte cp.async,
+// two chunks in flight each.
 // The Q tile is shared. Every pipe has an ST-deep K/V ring in shared memory and
 // NSB score buffers in TMEM; the softmax writes P (bf16) over the scores it has
 // just read, and the P V product takes P straight from TMEM as its A operand,
 // so P never touches shared memory. A score buffer is refilled only after the
 // P V product that read its P has completed. At the end pipe 1's (m, l, O) is
 // merged into pipe 0's through shared memory and TMEM.
-// Threads: 8 softmax warps, 2 MMA warps, 2 producer warps.
-constexpr int kFaThreads = 384;
+// Threads: 8 softmax warps, 2 MMA warps, 2 (dense: TMA) or 4 (reuse: gathers)
+// producer warps.
+template <bool REUSE> __host__ __device__ constexpr int fa_threads() { return REUSE ? 448 : 384; }
 
 // Chunk shape: KC keys per chunk, ST-deep K/V ring, NSB score buffers per
-// pipeline (NSB * KC + 128 O columns = 256 TMEM columns per pipeline).
-// Dense and anchor layers stream 64-key TMA tiles; reuse layers gather
-// 32-key chunks.
+// pipeline (NSB * KC + 128 O columns = 256 TMEM columns per pipeline); the
+// same for streamed (TMA) and gathered chunks.
 template <bool REUSE> struct FaShape { static constexpr int KC = 64, ST = 3, NSB = 2; };
-template <> struct FaShape<true> { static constexpr int KC = 64, ST = 3, NSB = 2; };
 
 template <bool REUSE>
 struct Fa2Smem {
@@ -111,7 +111,7 @@ __device__ __forceinline__ void tmem_store_p(uint32_t taddr, const uint32_t (&pk
 }
 
 template <bool REUSE, bool LSE>
-__global__ void __launch_bounds__(kFaThreads, 1)
+__global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     k_prefill_fa2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillArgs a) {
   using SM = Fa2Smem<REUSE>;
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
   int pipe, role;   // role: 0 softmax, 1 MMA, 2 producer
   if (warp < 8) { pipe = warp >> 2; role = 0; }
   else if (warp < 10) { pipe = warp - 8; role = 1; }
-  else { pipe = warp - 10; role = 2; }
+  else { pipe = (warp - 10) & 1; role = 2; }
 
   unsigned char* ps = sm + (pipe ? SM::PIPE1 : SM::PIPE0);
   int32_t* s_pos = reinterpret_cast<int32_t*>(sm + SM::POS) + pipe * kST * kKC;
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(kFaThreads, 1)
 
   if (role == 2) {
     // ------------------------------------------------ producer
-    if (pipe == 0 && lane == 0) {
+    if (warp == 10 && lane == 0) {
       prefetch_tmap(&tmQ);
       mbar_arrive_expect_tx(q_full, kTileBytes);
       tma_load_2d(sm + SM::Q, &tmQ, q_full, 0, bh * a.N + row0);
@@ -208,16 +208,27 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           mbar_wait(kv_full + (i % kST), (i / kST) & 1, a.err, 0x604);
       }
     } else {
-      // One gather warp per pipeline with up to kDepth chunks in flight: a
+      // kProd gather warps per pipeline take its chunks in turn (i = prod,
+      // prod + kProd, ...), each with up to kDepth of its chunks in flight: a
       // chunk is released (kv_full) once its copies have landed. Before waiting
-      // for a ring stage that is still busy, the warp releases every chunk it
-      // has in flight, so the MMA issuer never waits on copies held back
-      // behind that wait. Positions are read one chunk ahead.
-      constexpr int kDepth = kST > 1 ? kST - 1 : 1;
+      // for a ring stage that is still busy, a warp releases every chunk it has
+      // in flight, so the MMA issuer never waits on copies held back behind
+      // that wait. Positions are read one chunk ahead.
+      constexpr int kProd = 2;
+      constexpr int kDepth = 2;
       int p_first = __ldg(idx_row);
       if (p_first < 0 || p_first >= a.N) p_first = 0;
-      const __nv_bfloat16* kbase = static_cast<const __nv_bfloat16*>(a.k);
-      const __nv_bfloat16* vbase = static_cast<const __nv_bfloat16*>(a.v);
+      const int sub = lane >> 4, c16 = lane & 15;
+      // this lane's 16-byte column of a key row, and its swizzled column in
+      // shared memory for rows congruent to 2u + sub (mod 8)
+      const __nv_bfloat16* kl = static_cast<const __nv_bfloat16*>(a.k) +
+                                static_cast<size_t>(kv_row_base) * 128 + c16 * 8;
+      const __nv_bfloat16* vl = static_cast<const __nv_bfloat16*>(a.v) +
+                                static_cast<size_t>(kv_row_base) * 128 + c16 * 8;
+      uint32_t sw[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        sw[u] = (c16 >> 3) * SM::KHALF + sub * 128 + (((c16 & 7) ^ ((2 * u + sub) & 7)) << 4);
       auto read_pos = [&](int i, int (&pos)[kKC / 32]) {
 #pragma unroll
         for (int half = 0; half < kKC / 32; ++half) {
@@ -225,20 +236,21 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           pos[half] = e < kt ? __ldg(idx_row + e) : -1;
         }
       };
-      auto release_all = [&](int from, int to) {
+      auto release_all = [&](int from, int to) {   // own chunks from, from + kProd, ... < to
         cp_async_wait<0>();
         fence_proxy_async_smem();
-        for (int c = from; c < to; ++c) mbar_arrive(kv_full + c % kST);
+        for (int c = from; c < to; c += kProd) mbar_arrive(kv_full + c % kST);
       };
       int nxt[kKC / 32];
-      if (np > 0) read_pos(0, nxt);
-      int issued = 0, released = 0;
-      for (int i = 0; i < np; ++i) {
+      const int prod = (warp - 10) >> 1;
+      if (prod < np) read_pos(prod, nxt);
+      int issued = prod, released = prod;   // own chunks [released, issued) are in flight
+      for (int i = prod; i < np; i += kProd) {
         const int s = i % kST, j = 2 * i + pipe;
         int pos[kKC / 32];
 #pragma unroll
         for (int half = 0; half < kKC / 32; ++half) pos[half] = nxt[half];
-        if (i + 1 < np) read_pos(i + 1, nxt);
+        if (i + kProd < np) read_pos(i + kProd, nxt);
         const uint32_t par = ((i / kST) & 1) ^ 1;
         int ready = lane == 0 ? mbar_test_wait(kv_free + s, par) : 0;
         if (!__shfl_sync(0xffffffffu, ready, 0)) {
@@ -248,8 +260,8 @@ __global__ void __launch_bounds__(kFaThreads, 1)
           if (lane == 0) ok = mbar_wait(kv_free + s, par, a.err, 0x605);
           if (!__shfl_sync(0xffffffffu, ok, 0)) break;
         }
-        unsigned char* kd = ps + SM::K0 + s * SM::KV_BYTES;
-        unsigned char* vd = ps + SM::V0 + s * SM::KV_BYTES;
+        const uint32_t kd = smem_u32(ps + SM::K0 + s * SM::KV_BYTES);
+        const uint32_t vd = smem_u32(ps + SM::V0 + s * SM::KV_BYTES);
         // validate; padding slots (-1) re-read the tile's first saved row and
         // are masked later
         int src[kKC / 32], pmax = -1;
@@ -275,30 +287,27 @@ __global__ void __launch_bounds__(kFaThreads, 1)
         if (lane == 0) s_flag[s] = (all_valid && pmax <= row0) ? 1 : 0;
         // coalesced copies: a half-warp moves one 256-byte row (16 lanes x 16
         // bytes), so each instruction fills two rows of K (or V) in full
-        const int sub = lane >> 4, c16 = lane & 15;
 #pragma unroll
         for (int rr = 0; rr < kKC / 2; ++rr) {
-          const int pt = 2 * rr + sub;
-          const int prow = __shfl_sync(0xffffffffu, src[(2 * rr) >> 5], pt & 31);
-          const size_t off_g = (static_cast<size_t>(kv_row_base) + prow) * 128 + c16 * 8;
-          const int off = (c16 >> 3) * SM::KHALF + pt * 128 + (((c16 & 7) ^ (pt & 7)) << 4);
-          cp_async16(kd + off, kbase + off_g, 16);
-          cp_async16(vd + off, vbase + off_g, 16);
+          const int prow = __shfl_sync(0xffffffffu, src[(2 * rr) >> 5], (2 * rr + sub) & 31);
+          const uint32_t off = sw[rr & 3] + rr * 256;
+          cp_async16_s(kd + off, kl + static_cast<size_t>(prow) * 128);
+          cp_async16_s(vd + off, vl + static_cast<size_t>(prow) * 128);
         }
         cp_async_commit();
-        issued = i + 1;
-        if (issued - released >= kDepth) {   // the oldest chunk in flight has landed
+        issued = i + kProd;
+        if (issued - released >= kDepth * kProd) {   // the oldest own chunk in flight has landed
           cp_async_wait<kDepth - 1>();
           fence_proxy_async_smem();
           mbar_arrive(kv_full + released % kST);
-          ++released;
+          released += kProd;
         }
       }
       // release what is still in flight (also after an error, so that no copy
       // outlives the kernel)
       release_all(released, issued);
     }
-    if (pipe == 0 && lane == 0) mbar_wait(q_full, 0, a.err, 0x603);   // no copies left in flight
+    if (warp == 10 && lane == 0) mbar_wait(q_full, 0, a.err, 0x603);   // no copies left in flight
   } else if (role == 1) {
     // ------------------------------------------------ MMA issuer
     {
@@ -661,7 +670,7 @@ cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SM::SMEM));
   if (e != cudaSuccess) return e;
-  kern<<<a.B * a.Hq * a.nT, kFaThreads, SM::SMEM, st>>>(tq, tk, tv, a);
+  kern<<<a.B * a.Hq * a.nT, fa_threads<REUSE>(), SM::SMEM, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
