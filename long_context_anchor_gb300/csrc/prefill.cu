@@ -3,16 +3,16 @@
 // one index set per (head, 128-query tile)).
 //
 //   k_prefill_fa2<REUSE, LSE>  one (sequence, query head, 128-row tile) per
-//       CTA, its key chunks split over two pipelines that share the Q tile
+//       CTA, its 64-key chunks split over two pipelines that share the Q tile
 //       and merge their partial softmax states at the end: producer warps load
-//       the Q tile by TMA and the keys in chunks (dense/anchor layers: 64-key
-//       causal K/V tiles by TMA; reuse layers: 32-key chunks of the tile's saved
-//       K/V rows by 16-byte cp.async into the 128-byte-swizzled layout, then
-//       fence.proxy.async); one thread per pipeline issues tcgen05.mma
-//       S = Q K^T into rotating TMEM score buffers and O += P V with P read from
-//       TMEM; a softmax warpgroup per pipeline (one thread per query row) runs
-//       the online softmax with a lazy O rescale (only when a row maximum grows
-//       by more than 2^8) and writes P as bf16 over the scores it came from;
+//       the Q tile by TMA and the keys (dense/anchor layers: causal K/V tiles
+//       by TMA; reuse layers: the tile's saved K/V rows by coalesced 16-byte
+//       cp.async into the 128-byte-swizzled layout, then fence.proxy.async);
+//       Q is copied into TMEM and is the A operand of every S = Q K^T; one
+//       warp per pipeline issues tcgen05.mma S = Q K^T and O += P V with P
+//       read from TMEM; a softmax warpgroup per pipeline (one thread per query
+//       row) runs the online softmax with a lazy O rescale (only when a row
+//       maximum grows by more than 2^8) and writes P as bf16 into TMEM;
 //       pipeline 0 finally merges both partial states and writes O / l (and,
 //       for anchor layers, the row log-sum-exp). Causal masking is by key
 //       position.
@@ -60,25 +60,26 @@ __device__ __forceinline__ void fa_tile_coords(const PrefillArgs& a, int& bh, in
 // MMAs, warp 10+p is its producer (TMA for Q and dense K/V); for reuse, warps
 // 10+p and 12+p gather pipe p's chunks in turn with coalesced 16-byte cp.async,
 // two chunks in flight each.
-// The Q tile is shared. Every pipe has an ST-deep K/V ring in shared memory and
-// NSB score buffers in TMEM; the softmax writes P (bf16) over the scores it has
-// just read, and the P V product takes P straight from TMEM as its A operand,
-// so P never touches shared memory. A score buffer is refilled only after the
-// P V product that read its P has completed. At the end pipe 1's (m, l, O) is
-// merged into pipe 0's through shared memory and TMEM.
+// The Q tile is copied once into TMEM, where it is the A operand of every
+// S = Q K^T of both pipes, so shared memory feeds only K and V to the tensor
+// core. Every pipe has an ST-deep K/V ring in shared memory and its own score,
+// P and O columns in TMEM: the softmax releases the scores as soon as it has
+// read them (so S of the next chunk overlaps its exponentials), writes P as
+// bf16 into the P columns once the previous P V product has landed, and the
+// P V product takes P from TMEM as its A operand, so P never touches shared
+// memory. At the end pipe 1's (m, l, O) is merged into pipe 0's through
+// shared memory and TMEM.
 // Threads: 8 softmax warps, 2 MMA warps, 2 (dense: TMA) or 4 (reuse: gathers)
 // producer warps.
 template <bool REUSE> __host__ __device__ constexpr int fa_threads() { return REUSE ? 448 : 384; }
 
-// Chunk shape: KC keys per chunk, ST-deep K/V ring, NSB score buffers per
-// pipeline (NSB * KC + 128 O columns = 256 TMEM columns per pipeline); the
-// same for streamed (TMA) and gathered chunks.
-template <bool REUSE> struct FaShape { static constexpr int KC = 64, ST = 3, NSB = 2; };
+// Chunk shape: KC keys per chunk and an ST-deep K/V ring per pipeline; the same
+// for streamed (TMA) and gathered chunks.
+template <bool REUSE> struct FaShape { static constexpr int KC = 64, ST = 3; };
 
 template <bool REUSE>
 struct Fa2Smem {
   static constexpr int KC = FaShape<REUSE>::KC, ST = FaShape<REUSE>::ST;
-  static constexpr int NSB = FaShape<REUSE>::NSB;
   static constexpr int KHALF = KC * 128;             // one 64-dim half of a K (or V) chunk
   static constexpr int KV_BYTES = 2 * KHALF;
   static constexpr int K0 = 0;                       // within a pipeline's area
@@ -89,13 +90,18 @@ struct Fa2Smem {
   static constexpr int PIPE1 = PIPE0 + PIPE_BYTES;
   static constexpr int POS = PIPE1 + PIPE_BYTES;     // reuse: int32 [2 pipes][ST][KC] + flags [2][ST]
   static constexpr int POS_BYTES = REUSE ? 2 * ST * (KC + 1) * 4 : 0;
-  static constexpr int NB = 2 * ST + 3 * NSB;        // mbarriers per pipeline
-  static constexpr int BAR = POS + POS_BYTES;        // [2 pipes][NB] + q_full
-  static constexpr int TMEM = BAR + (2 * NB + 1) * 8;
+  static constexpr int NB = 2 * ST + 4;             // mbarriers per pipeline
+  static constexpr int BAR = POS + POS_BYTES;        // [2 pipes][NB] + q_full + q_ready
+  static constexpr int TMEM = BAR + (2 * NB + 2) * 8;
   static constexpr int BYTES = TMEM + 8;
   static constexpr size_t SMEM = BYTES + 1024;       // + slack for 1024-byte alignment
   static_assert(SMEM <= 232448, "the tile and two pipelines must fit in shared memory");
-  static_assert(NSB * KC + 128 <= 256, "a pipeline owns 256 TMEM columns");
+  // TMEM columns: Q (bf16 pairs) [0, 64); pipeline p at 64 + 224 p: scores S
+  // (KC fp32 columns), P (KC / 2 columns of bf16 pairs), O (128 columns)
+  static constexpr int T_PIPE = 64, T_PIPE_COLS = 224;
+  static constexpr int T_S = 0, T_P = 64, T_O = 96;
+  static_assert(KC <= 64 && T_O + 128 == T_PIPE_COLS, "pipeline TMEM columns");
+  static_assert(T_PIPE + 2 * T_PIPE_COLS == 512, "TMEM holds Q and two pipelines");
   static_assert(KC % 32 == 0 && KC <= 64, "softmax reads scores 32 columns at a time");
 };
 
@@ -115,7 +121,7 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     k_prefill_fa2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillArgs a) {
   using SM = Fa2Smem<REUSE>;
-  constexpr int kKC = SM::KC, kST = SM::ST, kNSB = SM::NSB;
+  constexpr int kKC = SM::KC, kST = SM::ST;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -130,13 +136,15 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   // reuse: 1 if chunk stage s needs no causal mask
   int32_t* s_flag = reinterpret_cast<int32_t*>(sm + SM::POS) + 2 * kST * kKC + pipe * kST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::BAR);
-  uint64_t* q_full = bars + 2 * SM::NB;
+  uint64_t* q_full = bars + 2 * SM::NB;       // Q tile landed in shared memory
+  uint64_t* q_ready = q_full + 1;             // Q tile copied into TMEM
   uint64_t* bar = bars + pipe * SM::NB;
   uint64_t* kv_full = bar;                    // [kST]
   uint64_t* kv_free = bar + kST;              // [kST]
-  uint64_t* s_full = bar + 2 * kST;           // [kNSB] scores of chunk i in buffer i % kNSB
-  uint64_t* p_full = s_full + kNSB;           // [kNSB] P of chunk i written over them
-  uint64_t* pv_done = p_full + kNSB;          // [kNSB] the P V product of that chunk
+  uint64_t* s_full = bar + 2 * kST;           // scores of the current chunk
+  uint64_t* s_free = s_full + 1;              // ... read by the softmax
+  uint64_t* p_full = s_full + 2;              // P of the current chunk written
+  uint64_t* pv_done = s_full + 3;             // its P V product completed
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + SM::TMEM);
   const uint32_t sQ = smem_u32(sm + SM::Q), sK0 = smem_u32(ps + SM::K0);
   const uint32_t sV0 = smem_u32(ps + SM::V0);
@@ -165,12 +173,14 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
       mbar_init(pb + s, REUSE ? 32 : 1);
       mbar_init(pb + kST + s, 1);
     }
-    for (int s = 0; s < kNSB; ++s) {
-      mbar_init(pb + 2 * kST + s, 1);
-      mbar_init(pb + 2 * kST + kNSB + s, 128);
-      mbar_init(pb + 2 * kST + 2 * kNSB + s, 1);
+    mbar_init(pb + 2 * kST, 1);         // s_full
+    mbar_init(pb + 2 * kST + 1, 128);   // s_free
+    mbar_init(pb + 2 * kST + 2, 128);   // p_full
+    mbar_init(pb + 2 * kST + 3, 1);     // pv_done
+    if (threadIdx.x == 0) {
+      mbar_init(q_full, 1);
+      mbar_init(q_ready, 128);
     }
-    if (threadIdx.x == 0) mbar_init(q_full, 1);
     fence_barrier_init();
   }
   if (warp == 8) tmem_alloc(s_tmem, 512);
@@ -178,7 +188,9 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *s_tmem;
-  const uint32_t tS = tmem_base + pipe * 256, tO = tS + 128;   // S[kNSB] at +0, O at +128
+  const uint32_t tQ = tmem_base;
+  const uint32_t tS = tmem_base + SM::T_PIPE + pipe * SM::T_PIPE_COLS + SM::T_S;
+  const uint32_t tP = tS - SM::T_S + SM::T_P, tO = tS - SM::T_S + SM::T_O;
 
   if (role == 2) {
     // ------------------------------------------------ producer
@@ -309,43 +321,42 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     }
     if (warp == 10 && lane == 0) mbar_wait(q_full, 0, a.err, 0x603);   // no copies left in flight
   } else if (role == 1) {
-    // ------------------------------------------------ MMA issuer
+    // ------------------------------------------------ MMA issuer (the whole
+    // warp runs the loop; one elected lane issues each MMA)
     {
       constexpr uint32_t idq = idesc_bf16_f32(128, kKC, 0, 0);
       constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
-      bool ok = mbar_wait(q_full, 0, a.err, 0x611);
-      // O += P V with P (A operand) read from the score buffer in TMEM
-      auto issue_pv = [&](int ii) {
-        const int s = ii % kST, pb = ii % kNSB;
-        if (!mbar_wait(p_full + pb, (ii / kNSB) & 1, a.err, 0x612)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kKC / 16; ++kk)
-          tc_mma_ts(tO, tS + pb * kKC + kk * 8, vmn_desc(sV0 + s * SM::KV_BYTES, kk, SM::KHALF),
-                    idv, (ii > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(pv_done + pb);
-        tc_commit(kv_free + s);
-        return true;
-      };
-      // S = Q K^T of chunk i into score buffer i % kNSB, once that buffer's
-      // previous P has been consumed by its P V product
+      bool ok = mbar_wait(q_ready, 0, a.err, 0x611);
+      // S = Q K^T of chunk i (A = Q from TMEM) once the softmax has read S(i-1)
       auto issue_s = [&](int i) {
-        const int s = i % kST, sb = i % kNSB;
+        const int s = i % kST;
         if (!mbar_wait(kv_full + s, (i / kST) & 1, a.err, 0x613)) return false;
-        if (i >= kNSB && !mbar_wait(pv_done + sb, ((i / kNSB) - 1) & 1, a.err, 0x614))
-          return false;
+        if (i > 0 && !mbar_wait(s_free, (i - 1) & 1, a.err, 0x614)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma(tS + sb * kKC, kmajor_desc(sQ, kk),
-                 kmajor_desc(sK0 + s * SM::KV_BYTES, kk, SM::KHALF), idq, kk > 0 ? 1u : 0u);
-        tc_commit(s_full + sb);
+          tc_mma_ts(tS, tQ + kk * 8, kmajor_desc(sK0 + s * SM::KV_BYTES, kk, SM::KHALF), idq,
+                    kk > 0 ? 1u : 0u);
+        tc_commit(s_full);
         return true;
       };
-      // scores run kNSB - 1 chunks ahead of the P V products
-      for (int i = 0; ok && i < min(np, kNSB - 1); ++i) ok = issue_s(i);
+      // O += P V with P (A operand) from its own TMEM columns
+      auto issue_pv = [&](int i) {
+        const int s = i % kST;
+        if (!mbar_wait(p_full, i & 1, a.err, 0x612)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kKC / 16; ++kk)
+          tc_mma_ts(tO, tP + kk * 8, vmn_desc(sV0 + s * SM::KV_BYTES, kk, SM::KHALF), idv,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(pv_done);
+        tc_commit(kv_free + s);
+        return true;
+      };
+      if (ok) tc_fence_after();
+      if (ok && np > 0) ok = issue_s(0);
       for (int i = 0; ok && i < np; ++i) {
-        if (i + kNSB - 1 < np) ok = issue_s(i + kNSB - 1);
+        if (i + 1 < np) ok = issue_s(i + 1);
         if (ok) ok = issue_pv(i);
       }
     }
@@ -354,22 +365,48 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     const int r = (warp & 3) * 32 + lane;
     const int row = row0 + r;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float m_used = kNegInfP, l = 0.f;
     bool ok = true;
-    for (int i = 0; i < np; ++i) {
-      const int sb = i % kNSB, s = i % kST, j = 2 * i + pipe;
-      ok = mbar_wait(s_full + sb, (i / kNSB) & 1, a.err, 0x621);
+    if (pipe == 0) {
+      // the Q tile (128-byte-swizzled halves in shared memory) into TMEM
+      // columns [0, 64) as bf16 pairs, one row per thread
+      ok = mbar_wait(q_full, 0, a.err, 0x620);
+      uint32_t qv[64];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint32_t addr = sQ + hh * kHalf + r * 128 + ((c ^ (r & 7)) << 4);
+          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(qv[hh * 32 + c * 4]), "=r"(qv[hh * 32 + c * 4 + 1]),
+                         "=r"(qv[hh * 32 + c * 4 + 2]), "=r"(qv[hh * 32 + c * 4 + 3])
+                       : "r"(addr));
+        }
+      tmem_st32(tQ + lane_base, *reinterpret_cast<uint32_t(*)[32]>(qv));
+      tmem_st32(tQ + 32 + lane_base, *reinterpret_cast<uint32_t(*)[32]>(qv + 32));
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(q_ready);
+    } else {
+      // pipe 1 reuses the Q staging area at the end: not before Q is in TMEM
+      ok = mbar_wait(q_ready, 0, a.err, 0x625);
+    }
+    float m_used = kNegInfP, l = 0.f;
+    for (int i = 0; ok && i < np; ++i) {
+      const int s = i % kST, j = 2 * i + pipe;
+      ok = mbar_wait(s_full, i & 1, a.err, 0x621);
       if (!ok) break;
       tc_fence_after();
       float x[kKC];
 #pragma unroll
       for (int c = 0; c < kKC / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tS + sb * kKC + c * 32 + lane_base, v);
-        tmem_wait_ld();
+        tmem_ld32(tS + c * 32 + lane_base, v);
 #pragma unroll
         for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
       }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free);   // the score buffer may take S(i+1) now
       const bool need_mask = REUSE ? (s_flag[s] == 0) : (j * kKC + kKC - 1 > row0);
       if (need_mask) {
 #pragma unroll
@@ -408,13 +445,13 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
         pk[c] = pack_bf16(p0, p1);
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      // the P columns and O are free once the previous P V product has landed
+      if (i > 0) {
+        ok = mbar_wait(pv_done, (i - 1) & 1, a.err, 0x622);
+        if (!ok) break;
+      }
+      tc_fence_after();
       if (__any_sync(0xffffffffu, resc)) {
-        // O may change only once the previous P V product has landed
-        if (i > 0) {
-          ok = mbar_wait(pv_done + ((i - 1) % kNSB), ((i - 1) / kNSB) & 1, a.err, 0x624);
-          if (!ok) break;
-        }
-        tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t o[32];
@@ -425,17 +462,15 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
           tmem_st32(tO + c * 32 + lane_base, o);
         }
       }
-      // P over the first kKC/2 columns of the scores it came from
-      tmem_store_p<kKC>(tS + sb * kKC + lane_base, pk);
+      tmem_store_p<kKC>(tP + lane_base, pk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(p_full + sb);
+      mbar_arrive(p_full);
     }
     // wait for this pipe's last P V, then merge pipe 1 into pipe 0
-    if (ok && np > 0)
-      ok = mbar_wait(pv_done + ((np - 1) % kNSB), ((np - 1) / kNSB) & 1, a.err, 0x623);
-    // pipe 1's K ring is idle once its last P V has completed
-    float* xch = reinterpret_cast<float*>(sm + SM::PIPE1 + SM::K0);
+    if (ok && np > 0) ok = mbar_wait(pv_done, (np - 1) & 1, a.err, 0x623);
+    // the Q staging area is idle once Q is in TMEM
+    float* xch = reinterpret_cast<float*>(sm + SM::Q);
     if (pipe == 1) {
       xch[r] = np > 0 ? m_used : kNegInfP;
       xch[128 + r] = np > 0 ? l : 0.f;
@@ -451,7 +486,7 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
       const float a1 = (m1 == kNegInfP) ? 0.f : ex2_approx(m1 - M);
       const float lt = a0 * l + a1 * l1;
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      const uint32_t tO1 = tmem_base + 256 + 128;
+      const uint32_t tO1 = tmem_base + SM::T_PIPE + SM::T_PIPE_COLS + SM::T_O;
       __nv_bfloat16* orow =
           static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(bh) * a.N + row) * kTile;
 #pragma unroll
