@@ -415,14 +415,13 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
           if (!(kp >= 0 && kp <= row)) x[c] = kNegInfP;
         }
       }
-      // row maximum as a tree (short dependency chains)
+      // row maximum: eight chains of three-input maxima
       float mx[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) mx[c] = x[c];
+      for (int c = 0; c < 8; ++c) mx[c] = fmaxf(x[2 * c], x[2 * c + 1]);
 #pragma unroll
-      for (int c = 8; c < kKC; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-      float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 8; c < kKC / 2; ++c) mx[c & 7] = fmax3(mx[c & 7], x[2 * c], x[2 * c + 1]);
+      float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
       tmax *= a.scale_log2;
       float alpha = 1.f;
       bool resc = false;
@@ -435,16 +434,23 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
         m_used = tmax;
       }
       const float mu = (m_used == kNegInfP) ? 0.f : m_used;
+      // exponents and row sums on packed pairs (one FMA / add per two scores)
+      const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nmu2 = f2_pack(-mu, -mu);
       uint32_t pk[kKC / 2];
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
       for (int c = 0; c < kKC / 2; ++c) {
-        const float p0 = ex2_approx(fmaf(x[2 * c], a.scale_log2, -mu));
-        const float p1 = ex2_approx(fmaf(x[2 * c + 1], a.scale_log2, -mu));
-        ls[c & 3] += p0 + p1;
+        float y0, y1;
+        f2_unpack(f2_fma(f2_pack(x[2 * c], x[2 * c + 1]), sc2, nmu2), y0, y1);
+        const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+        ls2[c & 3] = f2_add(ls2[c & 3], f2_pack(p0, p1));
         pk[c] = pack_bf16(p0, p1);
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      {
+        float s0, s1;
+        f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), s0, s1);
+        l += s0 + s1;
+      }
       // the P columns and O are free once the previous P V product has landed
       if (i > 0) {
         ok = mbar_wait(pv_done, (i - 1) & 1, a.err, 0x622);
@@ -585,7 +591,8 @@ __global__ void __launch_bounds__(kWtThreads, 1)
   if (warp >= 4 && warp < 8) {
     const int r = threadIdx.x - 128;
     const int i = row0 + r;
-    s_lse[r] = i < a.N ? a.lse[static_cast<size_t>(bh) * a.N + i] : CUDART_INF_F;
+    // stored negated: the epilogue's FMA adds it
+    s_lse[r] = i < a.N ? -a.lse[static_cast<size_t>(bh) * a.N + i] : -CUDART_INF_F;
   }
   if (warp == 2) tmem_alloc(s_tmem, 512);
   tc_fence_before();
@@ -653,28 +660,35 @@ __global__ void __launch_bounds__(kWtThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(s_free + sb);
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};
-      // only the diagonal key tile (j == t) needs the causal mask i >= key
+      // only the diagonal key tile (j == t) needs the causal mask i >= key;
+      // exponents and sums on packed pairs of query columns
       const bool diag = (j * kTile + kTile - 1 > row0);
+      const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+      const uint64_t* lse2 = reinterpret_cast<const uint64_t*>(s_lse);
+      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      auto cols = [&](const uint32_t (&v)[32], int base, uint64_t& sum2) {
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const float p0 = ex2_approx(__uint_as_float(v0[e]) * a.scale_log2 - s_lse[e]);
-        const float p1 = ex2_approx(__uint_as_float(v1[e]) * a.scale_log2 - s_lse[32 + e]);
-        const float p2 = ex2_approx(__uint_as_float(v2[e]) * a.scale_log2 - s_lse[64 + e]);
-        const float p3 = ex2_approx(__uint_as_float(v3[e]) * a.scale_log2 - s_lse[96 + e]);
-        if (diag) {
-          sum[0] += (kj <= row0 + e) ? p0 : 0.f;
-          sum[1] += (kj <= row0 + 32 + e) ? p1 : 0.f;
-          sum[2] += (kj <= row0 + 64 + e) ? p2 : 0.f;
-          sum[3] += (kj <= row0 + 96 + e) ? p3 : 0.f;
-        } else {
-          sum[0] += p0;
-          sum[1] += p1;
-          sum[2] += p2;
-          sum[3] += p3;
+        for (int e = 0; e < 32; e += 2) {
+          // 2^(s*sigma*log2e - lse2) = 2^(fma(s, c, -lse2))
+          float y0, y1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2,
+                           lse2[(base + e) >> 1]),
+                    y0, y1);
+          float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+          if (diag) {
+            p0 = (kj <= row0 + base + e) ? p0 : 0.f;
+            p1 = (kj <= row0 + base + e + 1) ? p1 : 0.f;
+          }
+          sum2 = f2_add(sum2, f2_pack(p0, p1));
         }
-      }
-      if (kj < L) wrow[kj] = (sum[0] + sum[1]) + (sum[2] + sum[3]);
+      };
+      cols(v0, 0, acc[0]);
+      cols(v1, 32, acc[1]);
+      cols(v2, 64, acc[2]);
+      cols(v3, 96, acc[3]);
+      float s0, s1;
+      f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+      if (kj < L) wrow[kj] = s0 + s1;
     }
   }
   tc_fence_before();
