@@ -706,7 +706,7 @@ cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spi
 }
 
 cudaError_t launch_decode_union_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st) {
-  if (head_dim == 128) return launch_union_t<128, kUnionNW, 3>(a, st);
+  if (head_dim == 128) return launch_union_t<128, kUnionNW, 2>(a, st);
   if (head_dim == 64) return launch_union_t<64, kUnionNW, 6>(a, st);
   return cudaErrorInvalidValue;
 }
