@@ -35,7 +35,8 @@ namespace {
 constexpr int kTile = 128;              // query rows and keys per tile
 constexpr int kHalf = kTile * 128;      // bytes of one 64-column half of a tile
 constexpr int kTileBytes = 2 * kHalf;   // 128 x 128 bf16 = 32 KB
-constexpr int kWtThreads = 384;         // weights kernel: warp 0 TMA, warp 1 MMA, warps 4-11 epilogue
+constexpr int kWtGroups = 3;            // weights kernel: epilogue warpgroups
+constexpr int kWtThreads = 128 + 128 * kWtGroups;   // warp 0 TMA, warp 1 MMA, warps 4.. epilogue
 constexpr float kRescaleLog2 = 8.0f;    // lazy O rescale threshold (factor 256)
 #define kNegInfP (-CUDART_INF_F)
 
@@ -534,8 +535,8 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
 // ------------------------------------------------------------------------
 // Anchor pass 2: tile weights from S^T = K_j Q_t^T (TMEM lane = key).
 // Warp 0 loads the Q tile once and the key tiles 0..t into a kWtKS-deep ring
-// by TMA; warp 1 issues S^T(j) into TMEM score buffer j % kWtSB; two epilogue
-// warpgroups (warps 4-7 and 8-11) take the key tiles in turn (even / odd j),
+// by TMA; warp 1 issues S^T(j) into TMEM score buffer j % kWtSB; kWtGroups
+// epilogue warpgroups (warps 4-7, 8-11, ...) take the key tiles in turn,
 // each thread owning one key of the tile: it sums 2^(s*sigma*log2e - lse2)
 // over the tile's query rows i >= key, with no cross-lane reduction.
 // ------------------------------------------------------------------------
@@ -641,31 +642,24 @@ __global__ void __launch_bounds__(kWtThreads, 1)
       }
     }
   } else if (warp >= 4) {
-    const int grp = (warp - 4) >> 2;   // epilogue group: key tiles j = grp, grp + 2, ...
+    const int grp = (warp - 4) >> 2;   // epilogue group: key tiles j = grp, grp + kWtGroups, ...
     const int r = (warp & 3) * 32 + lane;   // key lane within the key tile
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     float* wrow = a.w + static_cast<size_t>(bh) * (static_cast<size_t>(64) * (a.nT - 1) * a.nT + a.N) +
                   static_cast<size_t>(64) * t * (t + 1);
-    for (int j = grp; j < nkv; j += 2) {
+    for (int j = grp; j < nkv; j += kWtGroups) {
       const int sb = j % kWtSB;
       if (!mbar_wait(s_full + sb, (j / kWtSB) & 1, a.err, 0x721)) break;
       tc_fence_after();
       const int kj = j * kTile + r;
-      uint32_t v0[32], v1[32], v2[32], v3[32];
       const uint32_t ts = tmem + sb * 128 + lane_base;
-      tmem_ld32(ts, v0);
-      tmem_ld32(ts + 32, v1);
-      tmem_ld32(ts + 64, v2);
-      tmem_ld32(ts + 96, v3);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(s_free + sb);
       // only the diagonal key tile (j == t) needs the causal mask i >= key;
-      // exponents and sums on packed pairs of query columns
+      // exponents and sums on packed pairs of query columns, 64 columns at a
+      // time (the score buffer is released after the second load)
       const bool diag = (j * kTile + kTile - 1 > row0);
       const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
       const uint64_t* lse2 = reinterpret_cast<const uint64_t*>(s_lse);
-      uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+      uint64_t acc[2] = {0ull, 0ull};
       auto cols = [&](const uint32_t (&v)[32], int base, uint64_t& sum2) {
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -682,12 +676,21 @@ __global__ void __launch_bounds__(kWtThreads, 1)
           sum2 = f2_add(sum2, f2_pack(p0, p1));
         }
       };
-      cols(v0, 0, acc[0]);
-      cols(v1, 32, acc[1]);
-      cols(v2, 64, acc[2]);
-      cols(v3, 96, acc[3]);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t va[32], vb[32];
+        tmem_ld32(ts + hh * 64, va);
+        tmem_ld32(ts + hh * 64 + 32, vb);
+        tmem_wait_ld();
+        if (hh == 1) {
+          tc_fence_before();
+          mbar_arrive(s_free + sb);
+        }
+        cols(va, hh * 64, acc[0]);
+        cols(vb, hh * 64 + 32, acc[1]);
+      }
       float s0, s1;
-      f2_unpack(f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3])), s0, s1);
+      f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
       if (kj < L) wrow[kj] = s0 + s1;
     }
   }
