@@ -469,9 +469,14 @@ __global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant_
 }
 
 // ------------------------------------------------------------------------
-// Reuse decode over the union plan; every warp gathers its own 16-row
-// slices through a STAGES-deep cp.async pipeline (no block barriers).
+// Reuse decode over the union plan. A CTA takes chunks_per_cta consecutive
+// plan chunks of one (sequence, KV head) as one stream of 16-row slices;
+// every warp gathers its own slices through a STAGES-deep cp.async pipeline
+// (no block barriers), reading each slice's plan entries from global memory
+// one slice ahead. Padding entries (mask 0) are zero-filled, never read.
 // ------------------------------------------------------------------------
+constexpr int kMaxChunksPerCta = 8;
+
 template <int D, int NW, int STAGES>
 __global__ void __launch_bounds__(NW * 32)
     k_decode_union_bf16(const __grid_constant__ DecodeArgs a) {
@@ -481,34 +486,43 @@ __global__ void __launch_bounds__(NW * 32)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ int s_pref[kMaxChunksPerCta + 1];          // slice prefix over the CTA's chunks
+  __shared__ uint32_t s_ent[NW][STAGES][16];            // entries of the slices in flight
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* wbuf = smem + warp * STAGES * 2 * SLICE;
-  uint32_t* s_plan = reinterpret_cast<uint32_t*>(smem + NW * STAGES * 2 * SLICE);
 
   const int split = blockIdx.x, unit = blockIdx.y;
   const int b = unit / a.Hkv, g = unit % a.Hkv;
-  // this CTA's chunk of the union plan (keys of one key range)
-  const int e0 = 0;
-  const int e1 = min(kPlanCap, a.plan_count[unit * a.S + split]);
-  const int nslices = (e1 + 15) / 16;
-  const int my = warp < nslices ? (nslices - warp + NW - 1) / NW : 0;
-  {
-    // the chunk's entries, once, coalesced; padded with 0 (mask 0)
-    const uint32_t* plan = a.plan + (static_cast<size_t>(unit) * a.S + split) * kPlanCap;
-    const int padded = nslices * 16;
-    for (int i = threadIdx.x; i < padded; i += blockDim.x)
-      s_plan[i] = (i < e1) ? __ldg(plan + i) : 0u;
-    __syncthreads();
+  const int c0 = split * a.chunks_per_cta;
+  const int nc = max(0, min(a.plan_chunks - c0, a.chunks_per_cta));
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int c = 0; c < nc; ++c) {
+      s_pref[c] = acc;
+      acc += (min(kPlanCap, a.plan_count[unit * a.plan_chunks + c0 + c]) + 15) / 16;
+    }
+    s_pref[nc] = acc;
   }
+  __syncthreads();
+  const int nslices = s_pref[nc];
+  const int my = warp < nslices ? (nslices - warp + NW - 1) / NW : 0;
+  // this lane's plan entry of slice sl (lanes 16..31 repeat lanes 0..15)
+  auto fetch = [&](int sl) -> uint32_t {
+    int c = 0;
+    while (c + 1 < nc && s_pref[c + 1] <= sl) ++c;
+    const int e = (sl - s_pref[c]) * 16 + (lane & 15);
+    const int cnt = min(kPlanCap, a.plan_count[unit * a.plan_chunks + c0 + c]);
+    return e < cnt ? __ldg(a.plan + (static_cast<size_t>(unit) * a.plan_chunks + c0 + c) * kPlanCap + e)
+                   : 0u;
+  };
   const __nv_bfloat16* kbase =
       static_cast<const __nv_bfloat16*>(a.k) + static_cast<size_t>(unit) * a.N * D;
   const __nv_bfloat16* vbase =
       static_cast<const __nv_bfloat16*>(a.v) + static_cast<size_t>(unit) * a.N * D;
 
-  auto issue = [&](int i) {
-    const int sl = warp + i * NW;
+  auto issue = [&](int i, uint32_t ent) {
     const int stg = i % STAGES;
-    const uint32_t ent = s_plan[sl * 16 + (lane & 15)];
+    if (lane < 16) s_ent[warp][stg][lane] = ent;
     unsigned char* kd = wbuf + stg * 2 * SLICE;
     unsigned char* vd = kd + SLICE;
 #pragma unroll
@@ -516,7 +530,7 @@ __global__ void __launch_bounds__(NW * 32)
       const int row = it * ROWS_PER_INSTR + lane / CHUNKS;
       const int ch = lane % CHUNKS;
       const uint32_t ent_r = __shfl_sync(0xffffffffu, ent, row);
-      const bool ok = (e0 + sl * 16 + row) < e1;
+      const bool ok = (ent_r >> 24) != 0u;   // padding: mask 0
       const size_t off = static_cast<size_t>(ent_r & 0xFFFFFFu) * D + ch * 8;
       cp_async16(kd + sw128_offset(16, row, ch), kbase + off, ok ? 16u : 0u);
       cp_async16(vd + sw128_offset(16, row, ch), vbase + off, ok ? 16u : 0u);
@@ -529,21 +543,29 @@ __global__ void __launch_bounds__(NW * 32)
   load_q_frags<D>(a, b, g, qf);
   const int gid = lane >> 2, c4 = lane & 3;
 
+  uint32_t nxt = my > 0 ? fetch(warp) : 0u;   // entries of the next slice to issue
 #pragma unroll
   for (int i = 0; i < STAGES - 1; ++i) {
-    if (i < my) issue(i);
+    if (i < my) {
+      const uint32_t e = nxt;
+      nxt = (i + 1 < my) ? fetch(warp + (i + 1) * NW) : 0u;
+      issue(i, e);
+    }
     cp_async_commit();
   }
   for (int i = 0; i < my; ++i) {
-    if (i + STAGES - 1 < my) issue(i + STAGES - 1);
+    if (i + STAGES - 1 < my) {
+      const uint32_t e = nxt;
+      nxt = (i + STAGES < my) ? fetch(warp + (i + STAGES) * NW) : 0u;
+      issue(i + STAGES - 1, e);
+    }
     cp_async_commit();
     cp_async_wait<STAGES - 1>();
     __syncwarp();
-    const int sl = warp + i * NW;
     const uint32_t kd = smem_u32(wbuf + (i % STAGES) * 2 * SLICE);
     float sc[4];
     slice_scores<D>(kd, 16, 0, qf, sc);
-    const uint32_t ent = s_plan[sl * 16 + (lane & 15)];
+    const uint32_t ent = s_ent[warp][i % STAGES][lane & 15];
     const uint32_t m0 = __shfl_sync(0xffffffffu, ent, gid) >> 24;
     const uint32_t m1 = __shfl_sync(0xffffffffu, ent, gid + 8) >> 24;
     float x[4];
@@ -646,16 +668,30 @@ cudaError_t launch_dense_t(const DecodeArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+constexpr int kUnionSlots = 152 * 3;   // resident reuse CTAs (three per SM)
+// Plan chunks per reuse CTA: about one wave of resident CTAs.
+int union_chunks_per_cta(int plan_chunks, int units) {
+  const int total = plan_chunks * units;
+  int m = (total + kUnionSlots / 2) / kUnionSlots;
+  if (m < 1) m = 1;
+  if (m > kMaxChunksPerCta) m = kMaxChunksPerCta;
+  return m;
+}
+
 template <int D, int NW, int STAGES>
 cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
   constexpr int SLICE = (D / 64) * 16 * 128;
-  const size_t smem = 1024 + static_cast<size_t>(NW) * STAGES * 2 * SLICE + kPlanCap * 4;
+  const size_t smem = 1024 + static_cast<size_t>(NW) * STAGES * 2 * SLICE;
   auto kern = k_decode_union_bf16<D, NW, STAGES>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  dim3 grid(a.S, a.B * a.Hkv);
-  kern<<<grid, NW * 32, smem, st>>>(a);
+  DecodeArgs u = a;   // a.S plan chunks per unit, regrouped into fewer, longer CTAs
+  u.plan_chunks = a.S;
+  u.chunks_per_cta = union_chunks_per_cta(a.S, a.B * a.Hkv);
+  u.S = (a.S + u.chunks_per_cta - 1) / u.chunks_per_cta;
+  dim3 grid(u.S, a.B * a.Hkv);
+  kern<<<grid, NW * 32, smem, st>>>(u);
   return cudaGetLastError();
 }
 
@@ -666,6 +702,7 @@ cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
 constexpr int kDenseNW = 4;
 constexpr int kUnionNW = 4;
 constexpr int kTargetCtas = 152 * 2 * 4;
+constexpr int kUnionTargetCtas = 152 * 2 * 4;
 
 int decode_chunk_dense(int units, int N) {
   int s = (kTargetCtas + units - 1) / units;
@@ -681,7 +718,7 @@ int decode_chunk_dense(int units, int N) {
 // kPlanCap so a chunk's union fits the shared staging area), about four
 // waves of CTAs over 152 SMs x 2.
 int decode_union_range(int units, int N) {
-  int s = (kTargetCtas + units - 1) / units;
+  int s = (kUnionTargetCtas + units - 1) / units;
   if (s < 1) s = 1;
   int R = (N + s - 1) / s;
   R = (R + 31) & ~31;
