@@ -15,6 +15,9 @@ microseconds (lower is better) for the Kascade stack; the same line carries
 the library's own dense-attention stack on the same inputs, HBM GB/s, the
 roofline of the dominant kernel, an end-to-end number through the public API
 with host buffers, and the CPU oracle timed on the host cores.
+The line also carries the prefill stack (Llama-3.1-8B shape, N=16384) and the
+long-context decode stack (gpt-oss-20b-like shape: 24 layers, 64/8 heads,
+d=64, B=4, N=131072, k=8192), each against the library's own dense kernels.
 ``--impl reference`` times the CPU oracle itself on a bounded sample.
 """
 import argparse
@@ -356,6 +359,87 @@ def run_prefill(args, dev, world, stream, clocks):
     return res, launches, ms_k, (anchor_ms, f_anchor, reuse_ms, f_reuse, tf_sust, src)
 
 
+def run_decode_long(args, dev, world, stream, clocks):
+    """Decode stack of the gpt-oss-20b-like attention shape (24 layers, 64/8
+    heads, d=64, B=4, N=131072, k=8192, anchors every 3rd): Kascade vs the
+    library's own dense decode, per-layer CUDA events, union bytes."""
+    import torch
+    import torch.distributed as dist
+    from long_context_anchor_gb300 import configs
+    from long_context_anchor_gb300 import kascade as K
+    from long_context_anchor_gb300.workloads import make_layers
+    w = configs.GPTOSS_DECODE_128K
+    L = w.n_layers
+    qs, ks, vs = make_layers(w, device=dev)
+    outs = [torch.empty_like(q) for q in qs]
+    idx_buf = torch.empty(w.batch, w.n_q_heads, w.topk, dtype=torch.int32, device=dev)
+    ws = K.Workspace(dev)
+    anchors = list(w.anchors)
+
+    def timed(anch, steps):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(steps)]
+        for row in evs:
+            for e in row:
+                e.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        for st in range(steps):
+            evs[st][0].record(stream)
+            K.run_stack(K.DECODE, qs, ks, vs, w.topk, anch, outs=outs, idx_buf=idx_buf, ws=ws,
+                        layer_events=evs[st][1:])
+        torch.cuda.synchronize()
+        per = [[evs[st][l].elapsed_time(evs[st][l + 1]) for l in range(L)] for st in range(steps)]
+        total = sum(evs[st][0].elapsed_time(evs[st][L]) for st in range(steps))
+        return total, per
+
+    for _ in range(args.warmup):
+        K.run_stack(K.DECODE, qs, ks, vs, w.topk, anchors, outs=outs, idx_buf=idx_buf, ws=ws)
+        K.run_stack(K.DECODE, qs, ks, vs, w.topk, [], outs=outs, idx_buf=idx_buf, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.device_error() == K.OK
+    clocks.begin()
+    tot_k, per_k = timed(anchors, args.steps)
+    tot_d, _ = timed([], args.steps)
+    clocks.end()
+    if world > 1:
+        t = torch.tensor([tot_k, tot_d], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_k, tot_d = t.tolist()
+    ms_k, ms_d = tot_k / args.steps, tot_d / args.steps
+    reuse_layers = [l for l in range(L) if l not in anchors]
+    anchor_ms = statistics.mean(per_k[st][l] for st in range(args.steps) for l in anchors)
+    reuse_ms = statistics.mean(per_k[st][l] for st in range(args.steps) for l in reuse_layers)
+    unions = []
+    for a_ in anchors:
+        _, ia = K.anchor_decode(qs[a_], ks[a_], vs[a_], w.topk, ws=ws)
+        unions.append(union_rows(ia, w))
+    dense_b, anchor_b, reuse_b = decode_bytes(w, unions)
+    seg = []
+    for i, a_ in enumerate(anchors):
+        nxt = anchors[i + 1] if i + 1 < len(anchors) else L
+        seg += [reuse_b[i]] * (nxt - a_ - 1)
+    reuse_gbs = statistics.mean(seg) / (reuse_ms * 1e-3) / 1e9
+    hbm_peak, _, src = load_peaks()
+    res = {
+        "workload": w.name, "layers": L, "batch": w.batch, "q_heads": w.n_q_heads,
+        "kv_heads": w.n_kv_heads, "head_dim": w.head_dim, "kv_len": w.kv_len, "topk": w.topk,
+        "anchors": anchors,
+        "kascade_us_per_layer": round(1e3 * ms_k / L, 3),
+        "dense_us_per_layer": round(1e3 * ms_d / L, 3),
+        "speedup_vs_own_dense": round(ms_d / ms_k, 3),
+        "anchor_layer_us": round(1e3 * anchor_ms, 3), "reuse_layer_us": round(1e3 * reuse_ms, 3),
+        "reuse_hbm_gbs": round(reuse_gbs, 1), "reuse_frac_of_copy": round(reuse_gbs / hbm_peak, 4),
+        "dense_hbm_gbs": round(dense_b / (ms_d / L * 1e-3) / 1e9, 1),
+        "reuse_union_rows_per_layer": int(statistics.mean(unions)),
+        "peak_hbm_gbs": hbm_peak, "peak_source": src,
+    }
+    launches = args.steps * (3 * len(anchors) + len(reuse_layers))
+    del qs, ks, vs, outs
+    torch.cuda.empty_cache()
+    return res, launches
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -552,6 +636,10 @@ def run_ours(args):
         if pre_reuse_total > dec_reuse_total:
             result["roofline_decode_reuse"] = result["roofline"]
             result["roofline"] = result["roofline_prefill_reuse"]
+    if not args.no_long_decode:
+        long_res, long_launches = run_decode_long(args, dev, world, stream, clocks)
+        result["decode_long"] = long_res
+        result["gpu_launches_decode_long"] = long_launches
     result["clocks"] = clocks.stop()
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
@@ -675,6 +763,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-long-decode", action="store_true",
+                    help="skip the gpt-oss-20b-like decode stack (N=131072, d=64)")
     ap.add_argument("--sweep", action="store_true",
                     help="schedule sweep: DP anchors from calibration, decode and prefill vs dense")
     args = ap.parse_args()

@@ -32,8 +32,12 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCandCap = 4096;   // candidate (key, position) pairs in shared memory
-constexpr int kWarpCap = kCandCap / kWarps;   // per-warp candidate list
+// Candidate (key, position) pairs in shared memory: kCandCap for rows up to
+// kShortRow keys (two CTAs per SM); longer rows take a larger pool (one CTA per
+// SM) so that the per-warp lists do not overflow into the exact fallback.
+constexpr int kCandCap = 4096;
+constexpr int kShortRow = 32768;
+constexpr int kMaxCandCap = 16384;
 constexpr int kUnroll = 8;       // 32-position chunks in flight per warp
 constexpr int kSampleCap = 8192; // evenly spaced sample used to bracket the k-th key
 
@@ -169,8 +173,9 @@ __device__ void select_rank(const uint32_t* list, int n, int rank, uint32_t* his
 }
 
 // select_rank over the per-warp candidate lists (list w holds count[w] keys
-// at cand + w * kWarpCap).
-__device__ void select_rank_warp_lists(const uint32_t* cand, const int* count, int rank,
+// at cand + w * warp_cap).
+__device__ void select_rank_warp_lists(const uint32_t* cand, const int* count, int warp_cap,
+                                       int rank,
                                        uint32_t* hist, int* warp_tot, int* s_bin, int* s_above,
                                        uint32_t& key_out, int& greater) {
   uint32_t prefix = 0, pmask = 0;
@@ -180,10 +185,15 @@ __device__ void select_rank_warp_lists(const uint32_t* cand, const int* count, i
     const int sh = d == 0 ? 21 : (d == 1 ? 10 : 0);
     for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0u;
     __syncthreads();
-    for (int i = threadIdx.x; i < kWarps * kWarpCap; i += kThreads) {
-      if ((i % kWarpCap) >= count[i / kWarpCap]) continue;
-      const uint32_t key = cand[i];
-      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
+    // only the filled part of each list; the candidates share a narrow key
+    // range, so bins repeat within a warp: warp-aggregated adds
+    for (int w = 0; w < kWarps; ++w) {
+      const uint32_t* lst = cand + w * warp_cap;
+      for (int i0 = 0; i0 < count[w]; i0 += kThreads) {
+        const int i = i0 + static_cast<int>(threadIdx.x);
+        const uint32_t key = i < count[w] ? lst[i] : 0u;
+        hist_add(hist, i < count[w] && (key & pmask) == prefix, (key >> sh) & (nb - 1));
+      }
     }
     __syncthreads();
     int bin, above;
@@ -226,13 +236,18 @@ __device__ void sample_bracket(const uint32_t* samp, int n, int r_hi, int r_lo, 
   p_lo = (static_cast<uint32_t>(b_lo) << 11) | static_cast<uint32_t>(m_lo);
 }
 
-__global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ TopkArgs a,
-                                                      int words_cap) {
+// UNROLL: 32-position chunks per warp per step of the main pass (the next
+// step's loads are in flight meanwhile); long rows run one CTA per SM with a
+// deeper main pass, short rows two CTAs per SM.
+template <int UNROLL, int MIN_BLOCKS>
+__global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_constant__ TopkArgs a,
+                                                               int words_cap, int cand_cap) {
   extern __shared__ uint32_t sm[];
   uint32_t* hist = sm;                                                     // [2][2048]
-  uint32_t* cand_key = hist + 4096;                                        // [kCandCap]
-  int32_t* cand_pos = reinterpret_cast<int32_t*>(cand_key + kCandCap);     // [kCandCap]
-  uint32_t* samp = reinterpret_cast<uint32_t*>(cand_pos + kCandCap);       // [kSampleCap]
+  const int warp_cap = cand_cap / kWarps;                                  // per-warp list
+  uint32_t* cand_key = hist + 4096;                                        // [cand_cap]
+  int32_t* cand_pos = reinterpret_cast<int32_t*>(cand_key + cand_cap);     // [cand_cap]
+  uint32_t* samp = reinterpret_cast<uint32_t*>(cand_pos + cand_cap);       // [kSampleCap]
   uint32_t* above = samp + kSampleCap;                                     // [words_cap]
   uint32_t* eqbm = above + words_cap;                                      // [words_cap]
   __shared__ int warp_tot[32];
@@ -257,9 +272,27 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
 
   // ---- 1. bracket the k-th key from an evenly spaced sample -------------
   const int S = min(rd.len, max(2048, min(kSampleCap, rd.len / 16)));
-  for (int u = tid; u < S; u += kThreads) {
-    const int j = static_cast<int>((static_cast<long long>(u) * rd.len) / S);
-    samp[u] = float_key(__ldg(rd.ptr + j));
+  // The sample is S / 32 evenly spaced runs of 32 consecutive keys, one
+  // 128-byte line per run, so that sampling costs whole lines rather than one
+  // DRAM sector per sample (the exact selection below does not depend on how
+  // the sample was drawn; a poor sample only costs the fallback).
+  {
+    const int runs = S / 32;
+    const float step = static_cast<float>(rd.len - 32) / static_cast<float>(max(runs - 1, 1));
+    for (int u0 = 0; u0 < S; u0 += 16 * kThreads) {   // 16 loads in flight per thread
+      float v[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int u = u0 + q * kThreads + tid;
+        const int j = min(rd.len - 1, __float2int_rd(static_cast<float>(u >> 5) * step) + (u & 31));
+        v[q] = u < S ? __ldg(rd.ptr + j) : 0.f;
+      }
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const int u = u0 + q * kThreads + tid;
+        if (u < S) samp[u] = float_key(v[q]);
+      }
+    }
   }
   __syncthreads();
   const float rc = static_cast<float>(rd.k) * S / rd.len;   // expected sample rank
@@ -277,23 +310,36 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
   }
 
   // ---- 2. one pass: "above" bitmap by ballot, candidates in [t_lo, t_hi] --
-  // Each warp owns blocks of 32*kUnroll consecutive positions and appends its
+  // Each warp owns blocks of 32*UNROLL consecutive positions and appends its
   // candidates to its own shared list (count kept in a register).
   const int warp = tid >> 5;
-  uint32_t* wkey = cand_key + warp * kWarpCap;
-  int32_t* wpos = cand_pos + warp * kWarpCap;
+  uint32_t* wkey = cand_key + warp * warp_cap;
+  int32_t* wpos = cand_pos + warp * warp_cap;
   const uint32_t span = t_hi - t_lo;
   int wcount = 0, my_above = 0;
   bool bad = false;
-  for (int base = warp * 32 * kUnroll; base < rd.len; base += kWarps * 32 * kUnroll) {
-    float x[kUnroll];
+  // the next block's scores are loaded before this block is processed
+  float xn[UNROLL];
+  {
+    const int base = warp * 32 * UNROLL;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       const int j = base + 32 * u + lane;
-      x[u] = j < rd.len ? __ldg(rd.ptr + j) : 0.f;
+      xn[u] = j < rd.len ? __ldg(rd.ptr + j) : 0.f;
+    }
+  }
+  for (int base = warp * 32 * UNROLL; base < rd.len; base += kWarps * 32 * UNROLL) {
+    float x[UNROLL];
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) x[u] = xn[u];
+    const int nbase = base + kWarps * 32 * UNROLL;
+#pragma unroll
+    for (int u = 0; u < UNROLL; ++u) {
+      const int j = nbase + 32 * u + lane;
+      xn[u] = j < rd.len ? __ldg(rd.ptr + j) : 0.f;
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       const int j = base + 32 * u + lane;
       const bool valid = j < rd.len;
       bad |= x[u] != x[u];
@@ -305,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
       my_above += __popc(ba);
       if (in) {
         const int p = wcount + __popc(bi & ((1u << lane) - 1u));
-        if (p < kWarpCap) {
+        if (p < warp_cap) {
           wkey[p] = key;
           wpos[p] = j;
         }
@@ -316,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
   if (lane == 0) {
     s_wcount[warp] = wcount;
     atomicAdd(&s_nabove, my_above);
-    if (wcount > kWarpCap) atomicAdd(&s_ncand, 1);   // overflow marker
+    if (wcount > warp_cap) atomicAdd(&s_ncand, 1);   // overflow marker
   }
   if (__syncthreads_or(bad) && tid == 0) report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x401);
   int n_cand = 0;
@@ -328,15 +374,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
     // ---- 3. exact k-th key among the candidates -------------------------
     uint32_t T;
     int cg;
-    select_rank_warp_lists(cand_key, s_wcount, rd.k - n_above, hist, warp_tot, &s_bin, &s_above,
-                           T, cg);
+    select_rank_warp_lists(cand_key, s_wcount, warp_cap, rd.k - n_above, hist, warp_tot, &s_bin,
+                           &s_above, T, cg);
     c_gt = n_above + cg;
-    for (int i = tid; i < kWarps * kWarpCap; i += kThreads) {
-      if ((i % kWarpCap) >= s_wcount[i / kWarpCap]) continue;
-      const uint32_t key = cand_key[i];
-      const int p = cand_pos[i];
-      if (key > T) atomicOr(&above[p >> 5], 1u << (p & 31));
-      else if (key == T) atomicOr(&eqbm[p >> 5], 1u << (p & 31));
+    for (int w = 0; w < kWarps; ++w) {
+      for (int i = tid; i < s_wcount[w]; i += kThreads) {
+        const uint32_t key = cand_key[w * warp_cap + i];
+        const int p = cand_pos[w * warp_cap + i];
+        if (key > T) atomicOr(&above[p >> 5], 1u << (p & 31));
+        else if (key == T) atomicOr(&eqbm[p >> 5], 1u << (p & 31));
+      }
     }
     __syncthreads();
   } else {
@@ -407,13 +454,22 @@ __global__ void __launch_bounds__(kThreads, 2) k_topk(const __grid_constant__ To
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
   const int words_cap = (a.n + 31) / 32;
-  const size_t smem = (4096 + 2 * kCandCap + kSampleCap) * sizeof(uint32_t) +
-                      2 * static_cast<size_t>(words_cap) * sizeof(uint32_t);
-  if (smem > 220 * 1024) return cudaErrorNotSupported;
-  cudaError_t e = cudaFuncSetAttribute(k_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  constexpr size_t kSmemCap = 220 * 1024;
+  const size_t fixed = (4096 + kSampleCap) * sizeof(uint32_t) +
+                       2 * static_cast<size_t>(words_cap) * sizeof(uint32_t);
+  int cand_cap = kCandCap;
+  if (a.n > kShortRow && fixed < kSmemCap) {
+    const size_t room = (kSmemCap - fixed) / (2 * sizeof(uint32_t));
+    cand_cap = static_cast<int>(room < kMaxCandCap ? room : kMaxCandCap) / 512 * 512;
+    if (cand_cap < kCandCap) cand_cap = kCandCap;
+  }
+  const size_t smem = fixed + 2 * static_cast<size_t>(cand_cap) * sizeof(uint32_t);
+  if (smem > kSmemCap) return cudaErrorNotSupported;
+  auto kern = a.n > kShortRow ? k_topk<32, 1> : k_topk<kUnroll, 2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  k_topk<<<a.rows, kThreads, smem, st>>>(a, words_cap);
+  kern<<<a.rows, kThreads, smem, st>>>(a, words_cap, cand_cap);
   return cudaGetLastError();
 }
 
