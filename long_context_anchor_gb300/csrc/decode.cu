@@ -668,11 +668,12 @@ cudaError_t launch_dense_t(const DecodeArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-constexpr int kUnionSlots = 152 * 3;   // resident reuse CTAs (three per SM)
-// Plan chunks per reuse CTA: about one wave of resident CTAs.
-int union_chunks_per_cta(int plan_chunks, int units) {
-  const int total = plan_chunks * units;
-  int m = (total + kUnionSlots / 2) / kUnionSlots;
+// Plan chunks per reuse CTA: the fewest that fit all CTAs in one wave of
+// resident CTAs (`slots`); a second, partial wave costs more than CTAs that
+// leave some slots idle.
+int union_chunks_per_cta(int plan_chunks, int units, int slots) {
+  const int ctas_per_unit = slots / units > 1 ? slots / units : 1;
+  int m = (plan_chunks + ctas_per_unit - 1) / ctas_per_unit;
   if (m < 1) m = 1;
   if (m > kMaxChunksPerCta) m = kMaxChunksPerCta;
   return m;
@@ -686,9 +687,21 @@ cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
+  // resident CTAs of this kernel (queried once per device)
+  static int cached_dev = -1, cached_slots = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
+  if (dev != cached_dev) {
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, NW * 32, smem) != cudaSuccess)
+      return cudaErrorInvalidValue;
+    cached_slots = max(1, sms * per_sm);
+    cached_dev = dev;
+  }
   DecodeArgs u = a;   // a.S plan chunks per unit, regrouped into fewer, longer CTAs
   u.plan_chunks = a.S;
-  u.chunks_per_cta = union_chunks_per_cta(a.S, a.B * a.Hkv);
+  u.chunks_per_cta = union_chunks_per_cta(a.S, a.B * a.Hkv, cached_slots);
   u.S = (a.S + u.chunks_per_cta - 1) / u.chunks_per_cta;
   dim3 grid(u.S, a.B * a.Hkv);
   kern<<<grid, NW * 32, smem, st>>>(u);
@@ -744,7 +757,7 @@ cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spi
 
 cudaError_t launch_decode_union_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st) {
   if (head_dim == 128) return launch_union_t<128, kUnionNW, 2>(a, st);
-  if (head_dim == 64) return launch_union_t<64, kUnionNW, 6>(a, st);
+  if (head_dim == 64) return launch_union_t<64, kUnionNW, 3>(a, st);
   return cudaErrorInvalidValue;
 }
 
