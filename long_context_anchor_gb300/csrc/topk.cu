@@ -172,37 +172,46 @@ __device__ void select_rank(const uint32_t* list, int n, int rank, uint32_t* his
   greater = gt;
 }
 
-// select_rank over the per-warp candidate lists (list w holds count[w] keys
-// at cand + w * warp_cap).
-__device__ void select_rank_warp_lists(const uint32_t* cand, const int* count, int warp_cap,
-                                       int rank,
+// Candidate i of the per-warp lists (list w holds count[w] keys at
+// cand + w * warp_cap) in list order; pre[w] = keys in lists before w.
+__device__ __forceinline__ int cand_slot(const int* pre, int warp_cap, int i) {
+  int w = 0;
+#pragma unroll
+  for (int q = 1; q < kWarps; ++q) w += (i >= pre[q]) ? 1 : 0;
+  return w * warp_cap + (i - pre[w]);
+}
+
+// select_rank over the per-warp candidate lists: all candidates lie in
+// [t_lo, t_lo + span], so the digits are those of key - t_lo, from the top
+// bit of span down in passes of at most 11 bits (one or two passes for a
+// narrow bracket), each histogram built by one flat loop over the candidates.
+__device__ void select_rank_warp_lists(const uint32_t* cand, const int* pre, int total,
+                                       int warp_cap, uint32_t t_lo, uint32_t span, int rank,
                                        uint32_t* hist, int* warp_tot, int* s_bin, int* s_above,
                                        uint32_t& key_out, int& greater) {
+  const int nbits = span == 0u ? 1 : 32 - __clz(span);
   uint32_t prefix = 0, pmask = 0;
   int gt = 0;
-  for (int d = 0; d < 3; ++d) {
-    const int nb = d < 2 ? 2048 : 1024;
-    const int sh = d == 0 ? 21 : (d == 1 ? 10 : 0);
-    for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0u;
+  for (int top = nbits; top > 0;) {
+    const int width = top > 11 ? 11 : top;
+    const int sh = top - width;
+    const int nb = 1 << width;
+    for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0u;
     __syncthreads();
-    // only the filled part of each list; the candidates share a narrow key
-    // range, so bins repeat within a warp: warp-aggregated adds
-    for (int w = 0; w < kWarps; ++w) {
-      const uint32_t* lst = cand + w * warp_cap;
-      for (int i0 = 0; i0 < count[w]; i0 += kThreads) {
-        const int i = i0 + static_cast<int>(threadIdx.x);
-        const uint32_t key = i < count[w] ? lst[i] : 0u;
-        hist_add(hist, i < count[w] && (key & pmask) == prefix, (key >> sh) & (nb - 1));
-      }
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+      const uint32_t rel = cand[cand_slot(pre, warp_cap, i)] - t_lo;
+      if ((rel & pmask) == prefix) atomicAdd(&hist[(rel >> sh) & (nb - 1)], 1u);
     }
     __syncthreads();
     int bin, above;
-    find_bin(hist, nb, rank - gt, warp_tot, s_bin, s_above, bin, above);
+    find_bin(hist, nb < kThreads ? kThreads : nb, rank - gt, warp_tot, s_bin, s_above, bin,
+             above);
     gt += above;
     prefix |= static_cast<uint32_t>(bin) << sh;
     pmask |= static_cast<uint32_t>(nb - 1) << sh;
+    top = sh;
   }
-  key_out = prefix;
+  key_out = t_lo + prefix;
   greater = gt;
 }
 
@@ -374,16 +383,25 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_cons
     // ---- 3. exact k-th key among the candidates -------------------------
     uint32_t T;
     int cg;
-    select_rank_warp_lists(cand_key, s_wcount, warp_cap, rd.k - n_above, hist, warp_tot, &s_bin,
-                           &s_above, T, cg);
-    c_gt = n_above + cg;
-    for (int w = 0; w < kWarps; ++w) {
-      for (int i = tid; i < s_wcount[w]; i += kThreads) {
-        const uint32_t key = cand_key[w * warp_cap + i];
-        const int p = cand_pos[w * warp_cap + i];
-        if (key > T) atomicOr(&above[p >> 5], 1u << (p & 31));
-        else if (key == T) atomicOr(&eqbm[p >> 5], 1u << (p & 31));
+    __shared__ int s_pre[kWarps + 1];
+    if (tid == 0) {
+      int acc = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        s_pre[w] = acc;
+        acc += s_wcount[w];
       }
+      s_pre[kWarps] = acc;
+    }
+    __syncthreads();
+    select_rank_warp_lists(cand_key, s_pre, n_cand, warp_cap, t_lo, span, rd.k - n_above, hist,
+                           warp_tot, &s_bin, &s_above, T, cg);
+    c_gt = n_above + cg;
+    for (int i = tid; i < n_cand; i += kThreads) {
+      const int slot = cand_slot(s_pre, warp_cap, i);
+      const uint32_t key = cand_key[slot];
+      const int p = cand_pos[slot];
+      if (key > T) atomicOr(&above[p >> 5], 1u << (p & 31));
+      else if (key == T) atomicOr(&eqbm[p >> 5], 1u << (p & 31));
     }
     __syncthreads();
   } else {
