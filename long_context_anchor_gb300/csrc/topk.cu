@@ -256,8 +256,9 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_cons
   const int warp_cap = cand_cap / kWarps;                                  // per-warp list
   uint32_t* cand_key = hist + 4096;                                        // [cand_cap]
   int32_t* cand_pos = reinterpret_cast<int32_t*>(cand_key + cand_cap);     // [cand_cap]
-  uint32_t* samp = reinterpret_cast<uint32_t*>(cand_pos + cand_cap);       // [kSampleCap]
-  uint32_t* above = samp + kSampleCap;                                     // [words_cap]
+  // the sample is only used before the candidates exist: it shares their space
+  uint32_t* samp = cand_key;                                               // [kSampleCap]
+  uint32_t* above = hist + 4096 + max(2 * cand_cap, kSampleCap);          // [words_cap]
   uint32_t* eqbm = above + words_cap;                                      // [words_cap]
   __shared__ int warp_tot[32];
   __shared__ int s_ncand, s_nabove, s_bin, s_above;
@@ -472,18 +473,34 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_cons
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;
   const int words_cap = (a.n + 31) / 32;
-  constexpr size_t kSmemCap = 220 * 1024;
-  const size_t fixed = (4096 + kSampleCap) * sizeof(uint32_t) +
-                       2 * static_cast<size_t>(words_cap) * sizeof(uint32_t);
+  // shared memory: histogram, candidate pool (also holding the sample first),
+  // two row bitmaps. Long rows first try a pool that keeps two CTAs per SM,
+  // else take one CTA per SM with a larger pool.
+  const size_t fixed = 4096 * sizeof(uint32_t) + 2 * static_cast<size_t>(words_cap) * sizeof(uint32_t);
+  auto smem_for = [&](int cap) {
+    const int region = 2 * cap > kSampleCap ? 2 * cap : kSampleCap;
+    return fixed + static_cast<size_t>(region) * sizeof(uint32_t);
+  };
+  constexpr size_t kTwoPerSm = 110 * 1024, kOnePerSm = 220 * 1024;
   int cand_cap = kCandCap;
-  if (a.n > kShortRow && fixed < kSmemCap) {
-    const size_t room = (kSmemCap - fixed) / (2 * sizeof(uint32_t));
-    cand_cap = static_cast<int>(room < kMaxCandCap ? room : kMaxCandCap) / 512 * 512;
+  bool one_per_sm = false;
+  if (a.n > kShortRow) {
+    auto fit = [&](size_t budget) {
+      int cap = 0;
+      if (budget > fixed) cap = static_cast<int>((budget - fixed) / (2 * sizeof(uint32_t)));
+      cap = (cap < kMaxCandCap ? cap : kMaxCandCap) / 512 * 512;
+      return cap;
+    };
+    cand_cap = fit(kTwoPerSm);
+    if (cand_cap < 6144) {   // 384 per warp: room for the long-row bracket
+      cand_cap = fit(kOnePerSm);
+      one_per_sm = true;
+    }
     if (cand_cap < kCandCap) cand_cap = kCandCap;
   }
-  const size_t smem = fixed + 2 * static_cast<size_t>(cand_cap) * sizeof(uint32_t);
-  if (smem > kSmemCap) return cudaErrorNotSupported;
-  auto kern = a.n > kShortRow ? k_topk<32, 1> : k_topk<kUnroll, 2>;
+  const size_t smem = smem_for(cand_cap);
+  if (smem > kOnePerSm) return cudaErrorNotSupported;
+  auto kern = one_per_sm ? k_topk<32, 1> : k_topk<kUnroll, 2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
