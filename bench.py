@@ -248,6 +248,19 @@ def load_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
+def max_over_ranks(values, world, device=None):
+    """Element-wise maximum of a list of floats over all ranks (one all_reduce);
+    the list itself when there is one rank."""
+    values = [float(v) for v in values]
+    if world <= 1:
+        return values
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -319,10 +332,7 @@ def run_prefill(args, dev, world, stream, clocks):
     tot_k, per_k = timed(anchors, steps)
     tot_d, per_d = timed([], steps)
     clocks.end()
-    if world > 1:
-        t = torch.tensor([tot_k, tot_d], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_k, tot_d = t.tolist()
+    tot_k, tot_d = max_over_ranks([tot_k, tot_d], world, dev)
     ms_k, ms_d = tot_k / steps, tot_d / steps
     reuse_layers = [l for l in range(L) if l not in anchors]
     anchor_ms = statistics.mean(per_k[s][l] for s in range(steps) for l in anchors)
@@ -402,10 +412,7 @@ def run_decode_long(args, dev, world, stream, clocks):
     tot_k, per_k = timed(anchors, args.steps)
     tot_d, _ = timed([], args.steps)
     clocks.end()
-    if world > 1:
-        t = torch.tensor([tot_k, tot_d], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_k, tot_d = t.tolist()
+    tot_k, tot_d = max_over_ranks([tot_k, tot_d], world, dev)
     ms_k, ms_d = tot_k / args.steps, tot_d / args.steps
     reuse_layers = [l for l in range(L) if l not in anchors]
     anchor_ms = statistics.mean(per_k[st][l] for st in range(args.steps) for l in anchors)
@@ -511,10 +518,7 @@ def run_ours(args):
     total_k, pl_k = timed(anchors, args.steps)
     total_d, pl_d = timed([], args.steps)
     clocks.end()
-    if world > 1:
-        t = torch.tensor([total_k, total_d], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_k, total_d = t.tolist()
+    total_k, total_d = max_over_ranks([total_k, total_d], world, dev)
 
     ms_step = total_k / args.steps
     ms_dense = total_d / args.steps
@@ -609,10 +613,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = t.item()
+    e2e_ms = max_over_ranks([e2e_ms], world, dev)[0]
     result["e2e"] = {"value": round(1e3 * e2e_ms / L, 3), "unit": UNIT,
                      "h2d_bytes_per_step": int(q_host.numel() * 2 + 2 * knew_host.numel() * 2),
                      "d2h_bytes_per_step": int(out_host.numel() * 2)}
