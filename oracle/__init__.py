@@ -19,7 +19,10 @@ Contributions* and *Methodology*; opentrain.ai page, *Abstract*):
   set per (head, 128-row tile) ranked by the tile's summed post-softmax
   weights;
 * anchors are chosen by a dynamic programme maximising cross-layer Top-k
-  overlap (Key Contributions; Methodology 4).
+  overlap (Key Contributions; Methodology 4);
+* optionally (GQA-pooled sets) one set per (sequence, KV head), ranked by
+  the sum of the group's query heads' post-softmax (or tile) weights: a
+  reading for GQA models, whose head granularity the pages leave open.
 
 Modules: ``attention`` (dense / sparse decode and prefill), ``topk`` (the
 selection rule), ``schedule`` (overlap similarity and the anchor DP),

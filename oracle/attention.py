@@ -267,3 +267,93 @@ def sparse_prefill(Q, K, V, idx, group_map=None, scale=None, tile=TILE):
                 o[b, h, r0:r1] = sparse_prefill_tile(Q, K, V, idx[b, h, t], b, h, t,
                                                      group_map, scale, tile)[0]
     return o
+
+
+# ---------------------------------------------------- GQA-pooled index sets --
+#
+# One index set per (sequence, KV head) instead of per query head. The pages
+# give each attention head its own Top-k list (euno.news summary,
+# Methodology 5) and run GQA models (Llama-3.1-8B: 32 query heads over 8 KV
+# heads); they leave open how a group's heads would share one list. The
+# reading taken here: the score of key j for KV head g is the sum over the
+# group's query heads h (g(h) = g) of their post-softmax weights p_hj in
+# decode, and of the tile weights w_{t,h,j} in prefill. The selection rule is
+# unchanged; every query head of a group then attends over the group's set.
+
+def pooled_decode_weights(s, group_map, n_kv_heads):
+    """w[b, g, j] = sum over heads h with g(h) = g of softmax(s[b, h])_j -> [B, Hkv, N]."""
+    p = softmax(s)
+    B, Hq, N = p.shape
+    w = np.zeros((B, n_kv_heads, N))
+    for h in range(Hq):
+        w[:, group_map[h]] += p[:, h]
+    return w
+
+
+def anchor_decode_pooled(q, K, V, k, group_map=None, scale=None):
+    """Anchor layer with one set per (sequence, KV head).
+
+    Returns (o [B,Hq,d], idx [B,Hkv,min(k,N)] ascending int64, w [B,Hkv,N]).
+    """
+    B, Hq, _ = np.shape(q)
+    Hkv = np.shape(K)[1]
+    group_map = group_map if group_map is not None else default_group_map(Hq, Hkv)
+    o, s = dense_decode(q, K, V, group_map, scale)
+    w = pooled_decode_weights(s, group_map, Hkv)
+    kk = min(k, w.shape[2])
+    idx = np.empty((B, Hkv, kk), dtype=np.int64)
+    for b in range(B):
+        for g in range(Hkv):
+            idx[b, g] = topk_indices(w[b, g], kk)
+    return o, idx, w
+
+
+def expand_pooled_sets(idx, group_map):
+    """Per-query-head view of per-KV-head sets: out[:, h] = idx[:, g(h)]."""
+    return np.asarray(idx)[:, list(group_map)]
+
+
+def sparse_decode_pooled(q, K, V, idx, group_map=None, scale=None):
+    """Reuse layer over per-KV-head sets idx [B,Hkv,k]: head h attends over S_{g(h)}."""
+    Hq, Hkv = np.shape(q)[1], np.shape(K)[1]
+    group_map = group_map if group_map is not None else default_group_map(Hq, Hkv)
+    return sparse_decode(q, K, V, expand_pooled_sets(idx, group_map), group_map, scale)
+
+
+def tile_weights_pooled(Q, K, b, g, t, group_map, scale, tile=TILE):
+    """sum over heads h with g(h) = g of the tile weights w_{t,h,j}, j < L_t."""
+    heads = [h for h in range(len(group_map)) if group_map[h] == g]
+    w = None
+    for h in heads:
+        wh = tile_weights(Q, K, b, h, t, group_map, scale, tile)
+        w = wh if w is None else w + wh
+    return w
+
+
+def anchor_prefill_pooled(Q, K, V, k, group_map=None, scale=None, tile=TILE):
+    """Anchor layer, prefill, one set per (sequence, KV head, tile).
+
+    Returns (o [B,Hq,N,d], idx [B,Hkv,nT,k] int64 ascending, -1 padded
+    beyond k_t = min(k, L_t)).
+    """
+    B, Hq, N, d = np.shape(Q)
+    Hkv = np.shape(K)[1]
+    group_map = group_map if group_map is not None else default_group_map(Hq, Hkv)
+    scale = default_scale(d) if scale is None else scale
+    o = dense_prefill(Q, K, V, group_map, scale, tile)
+    nT = n_tiles(N, tile)
+    idx = np.full((B, Hkv, nT, k), -1, dtype=np.int64)
+    for b in range(B):
+        for g in range(Hkv):
+            for t in range(nT):
+                w = tile_weights_pooled(Q, K, b, g, t, group_map, scale, tile)
+                it = topk_indices(w, min(k, w.shape[0]))
+                idx[b, g, t, :it.shape[0]] = it
+    return o, idx
+
+
+def sparse_prefill_pooled(Q, K, V, idx, group_map=None, scale=None, tile=TILE):
+    """Reuse layer, prefill, over per-KV-head tile sets idx [B,Hkv,nT,k]."""
+    Hq, Hkv = np.shape(Q)[1], np.shape(K)[1]
+    group_map = group_map if group_map is not None else default_group_map(Hq, Hkv)
+    return sparse_prefill(Q, K, V, expand_pooled_sets(idx, group_map), group_map, scale, tile)

@@ -9,19 +9,24 @@ run dense (the pages' example anchor list does not start at layer 0).
 from . import attention as A
 
 
-def run_stack(mode, layers, k, anchors, group_map=None, scale=None, tile=A.TILE):
-    """layers: list of (q, K, V) per layer. Returns (outputs, sets_read).
+def run_stack(mode, layers, k, anchors, group_map=None, scale=None, tile=A.TILE, pooled=False):
+    """layers: list of (q, K, V) per layer. Returns (outputs, sets_read, sets_written).
 
     ``sets_read[l]`` is the index array layer l consumed (None for anchors and
-    dense layers); anchors' own sets are returned in ``sets_written``.
+    dense layers); anchors' own sets are returned in ``sets_written``. With
+    ``pooled`` the sets are per (sequence, KV head) (GQA-pooled scores).
     """
+    anchor_d = A.anchor_decode_pooled if pooled else A.anchor_decode
+    sparse_d = A.sparse_decode_pooled if pooled else A.sparse_decode
+    anchor_p = A.anchor_prefill_pooled if pooled else A.anchor_prefill
+    sparse_p = A.sparse_prefill_pooled if pooled else A.sparse_prefill
     anchors = set(anchors)
     held = None
     outs, sets_read, sets_written = [], [], []
     for layer, (q, K, V) in enumerate(layers):
         if mode == "decode":
             if layer in anchors:
-                o, held, _ = A.anchor_decode(q, K, V, k, group_map, scale)
+                o, held, _ = anchor_d(q, K, V, k, group_map, scale)
                 sets_read.append(None)
                 sets_written.append(held)
             elif held is None:
@@ -29,12 +34,12 @@ def run_stack(mode, layers, k, anchors, group_map=None, scale=None, tile=A.TILE)
                 sets_read.append(None)
                 sets_written.append(None)
             else:
-                o = A.sparse_decode(q, K, V, held, group_map, scale)
+                o = sparse_d(q, K, V, held, group_map, scale)
                 sets_read.append(held)
                 sets_written.append(None)
         else:
             if layer in anchors:
-                o, held = A.anchor_prefill(q, K, V, k, group_map, scale, tile)
+                o, held = anchor_p(q, K, V, k, group_map, scale, tile)
                 sets_read.append(None)
                 sets_written.append(held)
             elif held is None:
@@ -42,7 +47,7 @@ def run_stack(mode, layers, k, anchors, group_map=None, scale=None, tile=A.TILE)
                 sets_read.append(None)
                 sets_written.append(None)
             else:
-                o = A.sparse_prefill(q, K, V, held, group_map, scale, tile)
+                o = sparse_p(q, K, V, held, group_map, scale, tile)
                 sets_read.append(held)
                 sets_written.append(None)
         outs.append(o)

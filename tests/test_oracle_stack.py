@@ -41,3 +41,17 @@ def test_prefill_stack_reads_anchor_sets():
     outs, read, written = run_stack("prefill", layers, 16, [0])
     assert read[1] is written[0] and read[2] is written[0]
     np.testing.assert_array_equal(outs[2], A.sparse_prefill(*layers[2], written[0]))
+
+
+def test_pooled_stacks_hold_per_kv_head_sets():
+    rng = np.random.default_rng(2)
+    layers = _layers(rng, 4, "decode")
+    outs, read, written = run_stack("decode", layers, 8, [0, 2], pooled=True)
+    assert written[0].shape == (1, 2, 8)     # [B, Hkv, k]
+    assert read[1] is written[0] and read[3] is written[2]
+    np.testing.assert_array_equal(outs[3], A.sparse_decode_pooled(*layers[3], written[2]))
+    np.testing.assert_array_equal(written[2], A.anchor_decode_pooled(*layers[2], 8)[1])
+    layers = _layers(rng, 2, "prefill", N=200)
+    outs, read, written = run_stack("prefill", layers, 16, [0], pooled=True)
+    assert written[0].shape == (1, 2, 2, 16)  # [B, Hkv, nT, k]
+    np.testing.assert_array_equal(outs[1], A.sparse_prefill_pooled(*layers[1], written[0]))
