@@ -228,6 +228,23 @@ def decode_bytes(w, union_rows_per_anchor):
     return dense, anchor, reuse
 
 
+def pooled_decode_bytes(w):
+    """Algorithmic HBM bytes per layer with one index set per (sequence, KV head).
+
+    anchor: dense + fp32 logits spill written and read back + the pooled
+            weights written and read by the Top-k + index sets written and
+            read once to build the plan;
+    reuse : K and V rows of the group's set (k rows, no union needed) + one
+            4-byte plan entry per row + q + out.
+    """
+    d, B, Hq, Hkv, N, k = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads, w.kv_len, w.topk
+    qo = 2 * B * Hq * d * 2
+    dense = B * Hkv * N * 2 * d * 2 + qo
+    anchor = dense + 2 * B * Hq * N * 4 + 2 * B * Hkv * N * 4 + 2 * B * Hkv * k * 4
+    reuse = B * Hkv * k * (2 * d * 2 + 4) + qo
+    return anchor, reuse
+
+
 def union_rows(idx, w):
     """Rows of the per-(sequence, KV head) union of the group's index sets."""
     import torch
@@ -483,7 +500,7 @@ def run_ours(args):
         K.run_stack(K.DECODE, qs, ks, vs, w.topk, anch, outs=outs, idx_buf=idx_buf, ws=ws,
                     layer_events=events)
 
-    def timed(anch, steps):
+    def timed(anch, steps, run=stack):
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(steps)]
         for row in evs:
             for e in row:
@@ -497,7 +514,7 @@ def run_ours(args):
         t0.record(stream)
         for s in range(steps):
             evs[s][0].record(stream)
-            stack(anch, evs[s][1:])
+            run(anch, evs[s][1:])
         t1.record(stream)
         torch.cuda.synchronize()
         if world > 1:
@@ -617,6 +634,37 @@ def run_ours(args):
     result["e2e"] = {"value": round(1e3 * e2e_ms / L, 3), "unit": UNIT,
                      "h2d_bytes_per_step": int(q_host.numel() * 2 + 2 * knew_host.numel() * 2),
                      "d2h_bytes_per_step": int(out_host.numel() * 2)}
+    # GQA-pooled index sets (one per KV head) on the same resident inputs.
+    if not args.no_pooled:
+        idx_pool = torch.empty(B, Hkv, w.topk, dtype=torch.int32, device=dev)
+
+        def stack_pooled(anch, events=None):
+            K.run_stack(K.DECODE, qs, ks, vs, w.topk, anch, outs=outs, idx_buf=idx_pool, ws=ws,
+                        layer_events=events, pooled=True)
+
+        for _ in range(args.warmup):
+            stack_pooled(anchors)
+        torch.cuda.synchronize()
+        assert ws.device_error() == K.OK
+        clocks.begin()
+        total_p, pl_p = timed(anchors, args.steps, stack_pooled)
+        clocks.end()
+        total_p = max_over_ranks([total_p], world, dev)[0]
+        ms_p = total_p / args.steps
+        anchor_p = statistics.mean(pl_p[s][l] for s in range(args.steps) for l in anchors)
+        reuse_p = statistics.mean(pl_p[s][l] for s in range(args.steps) for l in reuse_layers)
+        pa_b, pr_b = pooled_decode_bytes(w)
+        pr_gbs = pr_b / (reuse_p * 1e-3) / 1e9
+        result["decode_pooled"] = {
+            "index_sets": "one per (sequence, KV head): group sums of softmax weights",
+            "kascade_us_per_layer": round(1e3 * ms_p / L, 3),
+            "anchor_layer_us": round(1e3 * anchor_p, 3),
+            "reuse_layer_us": round(1e3 * reuse_p, 3),
+            "speedup_vs_own_dense": round(ms_dense / ms_p, 3),
+            "reuse_hbm_gbs": round(pr_gbs, 1), "reuse_frac_of_copy": round(pr_gbs / hbm_peak, 4),
+            "reuse_bytes_per_layer": int(pr_b), "anchor_bytes_per_layer": int(pa_b),
+            "anchor_hbm_gbs": round(pa_b / (anchor_p * 1e-3) / 1e9, 1)}
+        result["gpu_launches_decode_pooled"] = args.steps * (5 * len(anchors) + len(reuse_layers))
     # Prefill stack (same step): Llama-3.1-8B shape at N = 16384.
     if not args.no_prefill:
         pre, pre_launches, pre_ms, (pa_ms, pa_f, pr_ms, pr_f, tf_sust, tsrc) = \
@@ -766,6 +814,8 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-long-decode", action="store_true",
                     help="skip the gpt-oss-20b-like decode stack (N=131072, d=64)")
+    ap.add_argument("--no-pooled", action="store_true",
+                    help="skip the decode stack with GQA-pooled index sets")
     ap.add_argument("--sweep", action="store_true",
                     help="schedule sweep: DP anchors from calibration, decode and prefill vs dense")
     args = ap.parse_args()

@@ -70,6 +70,15 @@ typedef enum {
 typedef enum { KASCADE_F32 = 0, KASCADE_BF16 = 1 } kascade_dtype;
 typedef enum { KASCADE_DECODE = 0, KASCADE_PREFILL = 1 } kascade_mode;
 
+/* Granularity of the index sets. The pages give every attention head its own
+ * Top-k list (euno.news summary, Methodology 5); for GQA models the library
+ * also offers one list per KV head ("pooled"): key j's score is the sum over
+ * the group's query heads h of their softmax weights p_hj (decode) or tile
+ * weights w_{t,h,j} (prefill), and every head of the group attends over the
+ * group's set. Index layouts then use Hkv in place of Hq:
+ *   decode idx [B,Hkv,topk], prefill idx [B,Hkv,nT,topk]. */
+typedef enum { KASCADE_IDX_PER_QHEAD = 0, KASCADE_IDX_PER_KVHEAD = 1 } kascade_index_mode;
+
 /* Shape and numerics of one attention layer. */
 typedef struct {
   int32_t batch;        /* B >= 1 */
@@ -83,6 +92,7 @@ typedef struct {
    * for h / (Hq/Hkv). Every KV head must serve exactly Hq/Hkv query heads;
    * group sizes 1, 2, 4 and 8 are built. Read only during the call. */
   const int32_t* group_map;
+  int32_t index_mode;   /* kascade_index_mode; 0 (zero-initialised) = per query head */
 } kascade_desc;
 
 /* Human-readable name of a status code (static storage). */
@@ -112,7 +122,10 @@ kascade_status kascade_dense_decode(const kascade_desc* desc, const void* q, con
 /* Anchor layer (Methodology 2): exact output as kascade_dense_decode, and the
  * exact Top-k (1 <= topk <= N) of the scaled logits of every (sequence,
  * query head) in idx_out [B,Hq,topk], ascending. When scores_out is not NULL
- * the fp32 logits sigma*q.k are also written there, [B,Hq,N]. */
+ * the fp32 logits sigma*q.k are also written there, [B,Hq,N].
+ * Pooled index mode: idx_out [B,Hkv,topk] is the Top-k of the pooled weights
+ * w[b,g,j] = sum_{h: g(h)=g} softmax_j(sigma q[b,h].k[b,g,j]), and
+ * scores_out (when not NULL) receives those fp32 weights, [B,Hkv,N]. */
 kascade_status kascade_anchor_decode(const kascade_desc* desc, const void* q, const void* k,
                                      const void* v, int32_t topk, void* out, int32_t* idx_out,
                                      float* scores_out, void* ws, size_t ws_bytes, void* stream);
@@ -120,7 +133,8 @@ kascade_status kascade_anchor_decode(const kascade_desc* desc, const void* q, co
 /* Reuse layer (Methodology 3): out[b,h] = softmax restricted to the saved set
  * S = idx[b,h,:] (topk ascending, distinct positions in [0,N)), computed with
  * this layer's q, k, v. Rows of k and v outside the sets are not read. Query
- * heads of one KV head share one pass over the union of their sets. */
+ * heads of one KV head share one pass over the union of their sets.
+ * Pooled index mode: S = idx[b,g(h),:], one set per KV head. */
 kascade_status kascade_reuse_decode(const kascade_desc* desc, const void* q, const void* k,
                                     const void* v, int32_t topk, const int32_t* idx, void* out,
                                     void* ws, size_t ws_bytes, void* stream);
@@ -156,13 +170,15 @@ kascade_status kascade_dense_prefill(const kascade_desc* desc, const void* q, co
 /* Anchor layer, prefill: exact causal output, then per (sequence, query
  * head, 128-row tile t) the Top-k_t of the tile weights w_j, k_t =
  * min(topk, L_t), L_t = min(N, 128(t+1)), into idx_out [B,Hq,nT,topk]
- * (ascending, -1 padded). */
+ * (ascending, -1 padded). Pooled index mode: per (sequence, KV head g,
+ * tile) the Top-k_t of sum_{h: g(h)=g} w_{t,h,j}, idx_out [B,Hkv,nT,topk]. */
 kascade_status kascade_anchor_prefill(const kascade_desc* desc, const void* q, const void* k,
                                       const void* v, int32_t topk, void* out, int32_t* idx_out,
                                       void* ws, size_t ws_bytes, void* stream);
 
 /* Reuse layer, prefill: row i of tile t attends to S_i = {j in idx[b,h,t,:],
- * j >= 0, j <= i}; a row whose S_i is empty outputs zeros. */
+ * j >= 0, j <= i}; a row whose S_i is empty outputs zeros. Pooled index
+ * mode: the set is idx[b,g(h),t,:]. */
 kascade_status kascade_reuse_prefill(const kascade_desc* desc, const void* q, const void* k,
                                      const void* v, int32_t topk, const int32_t* idx, void* out,
                                      void* ws, size_t ws_bytes, void* stream);
@@ -174,8 +190,8 @@ kascade_status kascade_reuse_prefill(const kascade_desc* desc, const void* q, co
  * ascending layer numbers in [0, n_layers). Layer l is an anchor when listed;
  * otherwise it reuses the sets of the most recent anchor <= l, or runs dense
  * when no anchor precedes it. idx_buf (device, the decode or prefill idx
- * layout) holds the current sets; on return it holds the last anchor's. The
- * sets never leave the device. */
+ * layout of the descriptor's index mode) holds the current sets; on return
+ * it holds the last anchor's. The sets never leave the device. */
 kascade_status kascade_run_stack(const kascade_desc* desc, int32_t mode, int32_t n_layers,
                                  const void* const* q, const void* const* k,
                                  const void* const* v, int32_t topk, const int32_t* anchors,
@@ -207,10 +223,11 @@ kascade_status kascade_layer_overlap(const int32_t* sets, int32_t n_layers, int3
 
 /* Calibration for the anchor DP (Methodology 4) on decode inputs: runs
  * every layer l as an anchor (kascade_anchor_decode) writing its exact
- * Top-k sets to sets_buf + l*B*Hq*topk (device int32 [n_layers, B*Hq,
- * topk]; also the layer outputs to out[l]), counts the cross-layer overlaps
- * on the device and returns sim_out[i*n_layers + l] = sum over (sequence,
- * query head) of |S_i ∩ S_l| / (B*Hq*topk) (host float64 [n_layers^2]).
+ * Top-k sets to sets_buf + l*B*H*topk (device int32 [n_layers, B*H,
+ * topk], H = Hq, or Hkv in pooled index mode; also the layer outputs to
+ * out[l]), counts the cross-layer overlaps on the device and returns
+ * sim_out[i*n_layers + l] = sum over (sequence, head) of |S_i ∩ S_l| /
+ * (B*H*topk) (host float64 [n_layers^2]).
  * Synchronises `stream` before returning. ws must hold
  * kascade_calibrate_workspace_size bytes. */
 size_t kascade_calibrate_workspace_size(const kascade_desc* desc, int32_t topk, int32_t n_layers);

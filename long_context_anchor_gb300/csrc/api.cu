@@ -66,6 +66,8 @@ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // Validated shape plus the derived head tables.
 struct Shape {
   int B, Hq, Hkv, d, N, G, dtype;
+  int pooled;                    // one index set per KV head (GQA-pooled scores)
+  int H_idx;                     // heads that own an index set: Hq, or Hkv when pooled
   float scale;
   int16_t heads[kMaxQHeads];     // heads[g*G + slot]
   int16_t head_kv[kMaxQHeads];   // KV head of each query head
@@ -89,6 +91,10 @@ kascade_status check_desc(const kascade_desc* desc, Shape& s) {
   if (s.B * s.Hkv > kMaxCounterUnits) return KASCADE_ERR_UNSUPPORTED;
   if (s.N >= (1 << 24)) return KASCADE_ERR_UNSUPPORTED;
   s.scale = desc->scale > 0.f ? desc->scale : 1.0f / sqrtf(static_cast<float>(s.d));
+  if (desc->index_mode != KASCADE_IDX_PER_QHEAD && desc->index_mode != KASCADE_IDX_PER_KVHEAD)
+    return KASCADE_ERR_INVALID_ARG;
+  s.pooled = desc->index_mode == KASCADE_IDX_PER_KVHEAD ? 1 : 0;
+  s.H_idx = s.pooled ? s.Hkv : s.Hq;
   int fill[kMaxQHeads];
   for (int g = 0; g < s.Hkv; ++g) fill[g] = 0;
   for (int h = 0; h < s.Hq; ++h) {
@@ -106,7 +112,8 @@ inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<
 // Workspace layout; offsets in bytes from the workspace base.
 struct Layout {
   size_t counters, part, spill, plan, plan_count;   // decode
-  size_t lse, w;                                    // prefill
+  size_t row_stat, pool;                            // decode, pooled sets
+  size_t lse, w, w_pool;                            // prefill (w_pool: pooled sets)
   size_t total;
 };
 
@@ -124,6 +131,12 @@ Layout layout(const Shape& s, int topk, int mode) {
     off = align256(off + static_cast<size_t>(s.B) * s.Hkv * chunks * kPlanCapEntries * 4);
     L.plan_count = off;
     off = align256(off + static_cast<size_t>(s.B) * s.Hkv * chunks * 4);
+    if (s.pooled) {
+      L.row_stat = off;
+      off = align256(off + static_cast<size_t>(s.B) * s.Hq * 8);
+      L.pool = off;
+      off = align256(off + static_cast<size_t>(s.B) * s.Hkv * s.N * 4);
+    }
   } else {
     const size_t nT = (s.N + 127) / 128;
     const size_t per_bh = 64 * (nT - 1) * nT + s.N;
@@ -131,6 +144,10 @@ Layout layout(const Shape& s, int topk, int mode) {
     off = align256(off + static_cast<size_t>(s.B) * s.Hq * s.N * 4);
     L.w = off;
     off = align256(off + static_cast<size_t>(s.B) * s.Hq * per_bh * 4);
+    if (s.pooled) {
+      L.w_pool = off;
+      off = align256(off + static_cast<size_t>(s.B) * s.Hkv * per_bh * 4);
+    }
   }
   L.total = off;
   return L;
@@ -167,6 +184,7 @@ void fill_decode_args(DecodeArgs& a, const Shape& s, const void* q, const void* 
   a.plan = at<uint32_t>(ws, L.plan);
   a.plan_count = at<int32_t>(ws, L.plan_count);
   a.plan_stride = s.G * topk;
+  a.pooled = s.pooled;
   a.topk = topk;
   a.B = s.B;
   a.Hq = s.Hq;
@@ -217,6 +235,17 @@ kascade_status run_topk_rows(const float* scores, int rows, int n, int k, int32_
 kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, const void* v,
                                  int topk, void* out, int32_t* idx_out, float* scores_out,
                                  void* ws, const Layout& L, cudaStream_t st) {
+  if (s.pooled) {
+    // logits to the workspace, then the group sums of their softmax weights
+    float* spill = at<float>(ws, L.spill);
+    kascade_status r = run_dense_decode(s, q, k, v, out, ws, L, topk, spill, st);
+    if (r != KASCADE_OK) return r;
+    float* pool = scores_out ? scores_out : at<float>(ws, L.pool);
+    r = cuda_status(launch_pool_decode(spill, at<float2>(ws, L.row_stat), pool, s.heads, s.B,
+                                       s.Hq, s.Hkv, s.G, s.N, st));
+    if (r != KASCADE_OK) return r;
+    return run_topk_rows(pool, s.B * s.Hkv, s.N, topk, idx_out, at<unsigned int>(ws, 0), st);
+  }
   float* spill = scores_out ? scores_out : at<float>(ws, L.spill);
   kascade_status r = run_dense_decode(s, q, k, v, out, ws, L, topk, spill, st);
   if (r != KASCADE_OK) return r;
@@ -382,6 +411,7 @@ void fill_prefill_args(PrefillArgs& a, const Shape& s, const void* q, const void
   a.Hkv = s.Hkv;
   a.N = s.N;
   a.G = s.G;
+  a.pooled = s.pooled;
   a.topk = topk;
   a.nT = (s.N + 127) / 128;
   a.scale = s.scale;
@@ -404,11 +434,19 @@ kascade_status run_anchor_prefill(const Shape& s, const void* q, const void* k, 
   kascade_status r = launch_status(launch_prefill_lse(a, s.d, st));
   if (r != KASCADE_OK) return r;
   if ((r = launch_status(launch_prefill_anchor_main(a, s.d, st))) != KASCADE_OK) return r;
+  const float* scores = a.w;
+  if (s.pooled) {
+    const size_t per_bh = static_cast<size_t>(64) * (a.nT - 1) * a.nT + s.N;
+    float* w_pool = at<float>(ws, L.w_pool);
+    r = cuda_status(launch_pool_prefill(a.w, w_pool, s.heads, s.B, s.Hq, s.Hkv, s.G, per_bh, st));
+    if (r != KASCADE_OK) return r;
+    scores = w_pool;
+  }
   TopkArgs t{};
-  t.scores = a.w;
+  t.scores = scores;
   t.idx_out = idx_out;
   t.err = a.err;
-  t.rows = s.B * s.Hq * a.nT;
+  t.rows = s.B * s.H_idx * a.nT;
   t.n = s.N;
   t.k = topk;
   t.k_stride = topk;
@@ -553,7 +591,7 @@ size_t kascade_calibrate_workspace_size(const kascade_desc* desc, int32_t topk, 
   Shape s;
   if (check_desc(desc, s) != KASCADE_OK || topk < 1 || n_layers < 1) return 0;
   const size_t dec = layout(s, topk, KASCADE_DECODE).total;
-  const size_t ov = kascade_overlap_workspace_size(n_layers, s.B * s.Hq, s.N);
+  const size_t ov = kascade_overlap_workspace_size(n_layers, s.B * s.H_idx, s.N);
   const size_t counts = static_cast<size_t>(n_layers) * n_layers * 8;
   return align256(dec > ov ? dec : ov) + align256(counts);
 }
@@ -574,7 +612,7 @@ kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
     return KASCADE_ERR_WORKSPACE;
   Layout L = layout(s, topk, KASCADE_DECODE);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const size_t per_layer = static_cast<size_t>(s.B) * s.Hq * topk;
+  const size_t per_layer = static_cast<size_t>(s.B) * s.H_idx * topk;
   for (int l = 0; l < n_layers; ++l) {
     if ((r = check_decode_ptrs(q[l], k[l], v[l], out[l])) != KASCADE_OK) return r;
     r = run_anchor_decode(s, q[l], k[l], v[l], topk, out[l], sets_buf + l * per_layer, nullptr,
@@ -582,11 +620,11 @@ kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
     if (r != KASCADE_OK) return r;
   }
   const size_t dec = L.total;
-  const size_t ov = kascade_overlap_workspace_size(n_layers, s.B * s.Hq, s.N);
+  const size_t ov = kascade_overlap_workspace_size(n_layers, s.B * s.H_idx, s.N);
   long long* counts = reinterpret_cast<long long*>(static_cast<char*>(ws) +
                                                    align256(dec > ov ? dec : ov));
   char* base = static_cast<char*>(ws);
-  cudaError_t e = launch_layer_overlap(sets_buf, n_layers, s.B * s.Hq, topk, s.N, counts,
+  cudaError_t e = launch_layer_overlap(sets_buf, n_layers, s.B * s.H_idx, topk, s.N, counts,
                                        reinterpret_cast<uint32_t*>(base + kWsStateBytes),
                                        reinterpret_cast<unsigned int*>(base), st);
   if (e != cudaSuccess) return KASCADE_ERR_CUDA;
@@ -596,7 +634,7 @@ kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
   e = cudaMemcpyAsync(host, counts, nc * 8, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e == cudaSuccess) {
-    const double denom = static_cast<double>(s.B) * s.Hq * topk;
+    const double denom = static_cast<double>(s.B) * s.H_idx * topk;
     for (size_t i = 0; i < nc; ++i) sim_out[i] = static_cast<double>(host[i]) / denom;
   }
   delete[] host;

@@ -403,13 +403,20 @@ __global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant_
   const int n0 = c * R, n1 = min(a.N, n0 + R);
   const int words = (R + 31) / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int i = threadIdx.x; i < G * words; i += blockDim.x) bm[i / words][i % words] = 0u;
-  // search job j: the chunk start of slot j (j < G) or the chunk end of slot
-  // j - G, spread over the 8 warps so the searches run concurrently
-  for (int job = warp; job < 2 * G; job += 8) {
-    const int slot = job < G ? job : job - G;
-    const bool is_hi = job >= G;
-    const int32_t* row = a.idx + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + slot]) * topk;
+  // sets of this unit: one per query head of the group, or the group's one
+  // pooled set (whose entries then carry every head of the group)
+  const int nsets = a.pooled ? 1 : G;
+  auto set_row = [&](int slot) {
+    return a.pooled ? a.idx + static_cast<size_t>(unit) * topk
+                    : a.idx + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + slot]) * topk;
+  };
+  for (int i = threadIdx.x; i < nsets * words; i += blockDim.x) bm[i / words][i % words] = 0u;
+  // search job j: the chunk start of set j (j < nsets) or the chunk end of
+  // set j - nsets, spread over the 8 warps so the searches run concurrently
+  for (int job = warp; job < 2 * nsets; job += 8) {
+    const int slot = job < nsets ? job : job - nsets;
+    const bool is_hi = job >= nsets;
+    const int32_t* row = set_row(slot);
     const int pos = warp_lower_bound(row, topk, is_hi ? n1 : n0);
     if (lane == 0) {
       if (is_hi) s_hi[slot] = pos;
@@ -420,8 +427,8 @@ __global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant_
     }
   }
   __syncthreads();
-  for (int slot = 0; slot < G; ++slot) {
-    const int32_t* row = a.idx + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + slot]) * topk;
+  for (int slot = 0; slot < nsets; ++slot) {
+    const int32_t* row = set_row(slot);
     const int hi = s_hi[slot];
     for (int i = s_lo[slot] + threadIdx.x; i < hi; i += blockDim.x) {
       const int raw = __ldg(row + i);
@@ -441,7 +448,7 @@ __global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant_
   int cnt = 0;
   for (int w = w0; w < w1; ++w) {
     uint32_t u = 0;
-    for (int slot = 0; slot < G; ++slot) u |= bm[slot][w];
+    for (int slot = 0; slot < nsets; ++slot) u |= bm[slot][w];
     cnt += __popc(u);
   }
   s_scan[threadIdx.x] = cnt;
@@ -456,12 +463,13 @@ __global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant_
   uint32_t* out = plan + (static_cast<size_t>(unit) * nch + c) * kPlanCap;
   for (int w = w0; w < w1; ++w) {
     uint32_t u = 0;
-    for (int slot = 0; slot < G; ++slot) u |= bm[slot][w];
+    for (int slot = 0; slot < nsets; ++slot) u |= bm[slot][w];
     while (u) {
       const int bit = __ffs(u) - 1;
       u &= u - 1;
-      uint32_t mask = 0;
-      for (int slot = 0; slot < G; ++slot) mask |= ((bm[slot][w] >> bit) & 1u) << slot;
+      uint32_t mask = a.pooled ? (1u << G) - 1u : 0u;
+      if (!a.pooled)
+        for (int slot = 0; slot < G; ++slot) mask |= ((bm[slot][w] >> bit) & 1u) << slot;
       out[pos++] = static_cast<uint32_t>(n0 + w * 32 + bit) | (mask << 24);
     }
   }
@@ -614,7 +622,10 @@ __global__ void k_decode_generic_f32(const __grid_constant__ DecodeArgs a, int D
   const float* V = static_cast<const float*>(a.v) + (static_cast<size_t>(b) * a.Hkv + g) * a.N * D;
   float* s = a.spill + (static_cast<size_t>(b) * a.Hq + hq) * a.N;
   const int32_t* sel =
-      (kind == kSparse) ? a.idx + (static_cast<size_t>(b) * a.Hq + hq) * a.topk : nullptr;
+      (kind == kSparse)
+          ? a.idx + (a.pooled ? static_cast<size_t>(b) * a.Hkv + g
+                              : static_cast<size_t>(b) * a.Hq + hq) * a.topk
+          : nullptr;
   const int n = (kind == kSparse) ? a.topk : a.N;
   for (int c = threadIdx.x; c < D; c += blockDim.x) qs[c] = q[c];
   __syncthreads();

@@ -22,7 +22,8 @@ struct DecodeArgs {
   unsigned int* err;        // workspace error word
   const uint32_t* plan;     // union plan [B*Hkv][chunks][2048]: key | mask << 24
   const int32_t* plan_count;  // [B*Hkv][chunks]
-  const int32_t* idx;       // per-head sets [B,Hq,topk] (generic sparse path)
+  const int32_t* idx;       // sets [B,Hq,topk], or [B,Hkv,topk] when pooled
+  int pooled;               // 1: one set per (sequence, KV head)
   int plan_stride;          // G * topk
   int topk;
   int B, Hq, Hkv, N, G;
@@ -72,7 +73,8 @@ struct PrefillArgs {
   void* out;            // [B,Hq,N,d]
   float* lse;           // [B*Hq][N] log2-domain LSE of sigma*log2e*logits (anchor pass 1)
   float* w;             // packed tile weights [B*Hq][sum_t L_t]
-  const int32_t* idx;   // [B,Hq,nT,topk] (reuse)
+  const int32_t* idx;   // [B,Hq,nT,topk] (reuse), or [B,Hkv,nT,topk] when pooled
+  int pooled;           // 1: one set per (sequence, KV head, tile)
   unsigned int* err;
   int B, Hq, Hkv, N, G, topk, nT;
   float scale, scale_log2;
@@ -82,6 +84,18 @@ cudaError_t launch_prefill_dense(const PrefillArgs& a, int head_dim, cudaStream_
 cudaError_t launch_prefill_lse(const PrefillArgs& a, int head_dim, cudaStream_t st);
 cudaError_t launch_prefill_anchor_main(const PrefillArgs& a, int head_dim, cudaStream_t st);
 cudaError_t launch_prefill_reuse(const PrefillArgs& a, int head_dim, cudaStream_t st);
+
+// pool.cu — GQA-pooled scores (one index set per KV head).
+// Decode: w[b,g,j] = sum over the group's heads h of softmax_j(s[b,h,:]),
+// from the anchor's logit spill s [B,Hq,N]; row_stat [B*Hq] holds each row's
+// (max, 1/sum exp(s - max)).
+cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w,
+                               const int16_t* heads, int B, int Hq, int Hkv, int G, int N,
+                               cudaStream_t st);
+// Prefill: packed tile-weight rows [B*Hq][per_bh] -> [B*Hkv][per_bh], each
+// the sum of its group's rows.
+cudaError_t launch_pool_prefill(const float* w, float* w_pool, const int16_t* heads, int B,
+                                int Hq, int Hkv, int G, size_t per_bh, cudaStream_t st);
 
 // overlap.cu
 cudaError_t launch_layer_overlap(const int32_t* sets, int L, int units, int topk, int n_bits,

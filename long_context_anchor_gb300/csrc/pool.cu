@@ -1,0 +1,161 @@
+// pool.cu — scores of GQA-pooled index sets (one set per KV head).
+//
+// The Kascade pages give every attention head its own Top-k list (euno.news
+// summary, Methodology 5) and run GQA models. In pooled mode the query heads
+// of one KV head share a list, ranked by the sum of their post-softmax
+// weights: decode w[b,g,j] = sum_{h: g(h)=g} softmax_j(s[b,h,:]), prefill the
+// sum of the group's tile weights w_{t,h,j}. Both kernels here are plain
+// HBM/L2 streams over fp32 rows the anchor layer has just written.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace kascade {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+#define kNegInf (__int_as_float(0xff800000u))
+
+struct HeadTable {
+  int16_t heads[kMaxQHeads];   // heads[g*G + slot]
+};
+
+// (max, sum of exp(x - max)) pairs, merged exactly as the online softmax does.
+__device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == kNegInf) return;
+  if (m == kNegInf) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  const float mx = fmaxf(m, m2);
+  s = s * exp2f((m - mx) * kLog2e) + s2 * exp2f((m2 - mx) * kLog2e);
+  m = mx;
+}
+
+// One CTA per logit row: row_stat[r] = (max_j s_rj, 1 / sum_j exp(s_rj - max)).
+// A NaN logit makes the sum NaN, so every pooled weight of its group is NaN
+// and the Top-k that follows reports it.
+__global__ void __launch_bounds__(256) k_row_stat(const float* __restrict__ s, int n,
+                                                  float2* __restrict__ row_stat) {
+  __shared__ float sm[8], ss[8];
+  const float* row = s + static_cast<size_t>(blockIdx.x) * n;
+  float m = kNegInf, sum = 0.f;
+  for (int j = threadIdx.x; j < n; j += blockDim.x) {
+    const float x = __ldg(row + j);
+    if (x > m) {
+      sum = (m == kNegInf) ? 0.f : sum * exp2f((m - x) * kLog2e);
+      m = x;
+    }
+    sum += exp2f((x - m) * kLog2e);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, sum, off);
+    stat_merge(m, sum, m2, s2);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sm[warp] = m;
+    ss[warp] = sum;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = sm[0], S = ss[0];
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) stat_merge(M, S, sm[w], ss[w]);
+    row_stat[blockIdx.x] = make_float2(M, 1.f / S);
+  }
+}
+
+// w[u, j] = sum over the group's slots of exp(s[row, j] - max_row) / sum_row,
+// u = b*Hkv + g, row = b*Hq + heads[g*G + slot]. Block (x, u) covers keys
+// [1024 x, 1024 x + 1024), four per thread, coalesced.
+__global__ void __launch_bounds__(256) k_pool_decode(const float* __restrict__ s,
+                                                     const float2* __restrict__ row_stat,
+                                                     float* __restrict__ w,
+                                                     const __grid_constant__ HeadTable ht,
+                                                     int Hq, int Hkv, int G, int n) {
+  const int u = blockIdx.y, b = u / Hkv, g = u % Hkv;
+  const int j0 = blockIdx.x * 1024 + threadIdx.x;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int slot = 0; slot < G; ++slot) {
+    const int r = b * Hq + ht.heads[g * G + slot];
+    const float2 st = row_stat[r];
+    const float* row = s + static_cast<size_t>(r) * n;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = j0 + 256 * i;
+      if (j < n) acc[i] += exp2f((__ldg(row + j) - st.x) * kLog2e) * st.y;
+    }
+  }
+  float* out = w + static_cast<size_t>(u) * n;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int j = j0 + 256 * i;
+    if (j < n) out[j] = acc[i];
+  }
+}
+
+// w_pool[u][e] = sum over the group's slots of w[b*Hq + heads[g*G + slot]][e].
+__global__ void __launch_bounds__(256) k_pool_prefill(const float* __restrict__ w,
+                                                      float* __restrict__ w_pool,
+                                                      const __grid_constant__ HeadTable ht,
+                                                      int Hq, int Hkv, int G, size_t per_bh) {
+  const int u = blockIdx.y, b = u / Hkv, g = u % Hkv;
+  const size_t e0 = static_cast<size_t>(blockIdx.x) * 1024 + threadIdx.x;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int slot = 0; slot < G; ++slot) {
+    const float* row =
+        w + static_cast<size_t>(b * Hq + ht.heads[g * G + slot]) * per_bh;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const size_t e = e0 + 256 * i;
+      if (e < per_bh) acc[i] += __ldg(row + e);
+    }
+  }
+  float* out = w_pool + static_cast<size_t>(u) * per_bh;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const size_t e = e0 + 256 * i;
+    if (e < per_bh) out[e] = acc[i];
+  }
+}
+
+HeadTable make_table(const int16_t* heads, int Hq) {
+  HeadTable t{};
+  for (int i = 0; i < Hq && i < kMaxQHeads; ++i) t.heads[i] = heads[i];
+  return t;
+}
+
+}  // namespace
+
+cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w,
+                               const int16_t* heads, int B, int Hq, int Hkv, int G, int N,
+                               cudaStream_t st) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || G < 1 || N < 1 || Hq != Hkv * G || Hq > kMaxQHeads)
+    return cudaErrorInvalidValue;
+  const HeadTable ht = make_table(heads, Hq);
+  k_row_stat<<<B * Hq, 256, 0, st>>>(spill, N, row_stat);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_pool_decode<<<dim3((N + 1023) / 1024, B * Hkv), 256, 0, st>>>(spill, row_stat, w, ht, Hq,
+                                                                  Hkv, G, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pool_prefill(const float* w, float* w_pool, const int16_t* heads, int B,
+                                int Hq, int Hkv, int G, size_t per_bh, cudaStream_t st) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || G < 1 || Hq != Hkv * G || Hq > kMaxQHeads || per_bh == 0)
+    return cudaErrorInvalidValue;
+  const size_t blocks = (per_bh + 1023) / 1024;
+  if (blocks > 0x7fffffffu) return cudaErrorInvalidValue;
+  const HeadTable ht = make_table(heads, Hq);
+  k_pool_prefill<<<dim3(static_cast<unsigned int>(blocks), B * Hkv), 256, 0, st>>>(
+      w, w_pool, ht, Hq, Hkv, G, per_bh);
+  return cudaGetLastError();
+}
+
+}  // namespace kascade

@@ -161,7 +161,8 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   if (REUSE) {
     kt = min(a.topk, L);
     nkv = (kt + kKC - 1) / kKC;
-    idx_row = a.idx + (static_cast<size_t>(bh) * a.nT + t) * a.topk;
+    const size_t set = a.pooled ? static_cast<size_t>(b) * a.Hkv + g : static_cast<size_t>(bh);
+    idx_row = a.idx + (set * a.nT + t) * a.topk;
   } else {
     nkv = (L + kKC - 1) / kKC;
   }

@@ -24,6 +24,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 OK, INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA, BAD_INPUT, TIMEOUT = range(7)
 F32, BF16 = 0, 1
 DECODE, PREFILL = 0, 1
+PER_QHEAD, PER_KVHEAD = 0, 1     # kascade_index_mode: per query head, or GQA-pooled
 TILE = 128
 
 
@@ -31,7 +32,8 @@ class Desc(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("kv_len", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("group_map", ctypes.POINTER(ctypes.c_int32))]
+                ("scale", ctypes.c_float), ("group_map", ctypes.POINTER(ctypes.c_int32)),
+                ("index_mode", ctypes.c_int32)]
 
 
 _vp, _i32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
@@ -98,9 +100,9 @@ def _stream(stream=None):
 
 
 def make_desc(batch, n_q_heads, n_kv_heads, head_dim, kv_len, dtype, scale=0.0,
-              group_map: Optional[Sequence[int]] = None):
+              group_map: Optional[Sequence[int]] = None, pooled: bool = False):
     d = Desc(batch, n_q_heads, n_kv_heads, head_dim, kv_len, dtype,
-             float(scale or 0.0), None)
+             float(scale or 0.0), None, PER_KVHEAD if pooled else PER_QHEAD)
     keep = None
     if group_map is not None:
         keep = (ctypes.c_int32 * n_q_heads)(*[int(x) for x in group_map])
@@ -117,16 +119,16 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError("q/k/v must be bfloat16 or float32")
 
 
-def decode_desc(q, k, group_map=None, scale=None):
+def decode_desc(q, k, group_map=None, scale=None, pooled=False):
     B, Hq, d = q.shape
     _, Hkv, N, _ = k.shape
-    return make_desc(B, Hq, Hkv, d, N, _dtype_code(q), scale or 0.0, group_map)
+    return make_desc(B, Hq, Hkv, d, N, _dtype_code(q), scale or 0.0, group_map, pooled)
 
 
-def prefill_desc(q, k, group_map=None, scale=None):
+def prefill_desc(q, k, group_map=None, scale=None, pooled=False):
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
-    return make_desc(B, Hq, Hkv, d, N, _dtype_code(q), scale or 0.0, group_map)
+    return make_desc(B, Hq, Hkv, d, N, _dtype_code(q), scale or 0.0, group_map, pooled)
 
 
 def workspace_size(desc, topk: int, mode: int) -> int:
@@ -194,15 +196,19 @@ def dense_decode(q, k, v, group_map=None, scale=None, out=None, ws=None, stream=
 
 
 def anchor_decode(q, k, v, topk, group_map=None, scale=None, return_scores=False, out=None,
-                  idx=None, ws=None, stream=None):
-    """Anchor layer: (out [B,Hq,d], idx [B,Hq,topk] int32[, scores [B,Hq,N] fp32])."""
+                  idx=None, ws=None, stream=None, pooled=False):
+    """Anchor layer: (out [B,Hq,d], idx [B,H,topk] int32[, scores [B,H,N] fp32]).
+
+    H = Hq: per-head sets, scores = the scaled logits. pooled: H = Hkv, one
+    set per KV head, scores = the group sums of the softmax weights."""
     _contig(q, k, v)
-    desc = decode_desc(q, k, group_map, scale)
+    desc = decode_desc(q, k, group_map, scale, pooled)
     B, Hq, _ = q.shape
-    N = k.shape[2]
+    Hkv, N = k.shape[1], k.shape[2]
+    H = Hkv if pooled else Hq
     out = torch.empty_like(q) if out is None else out
-    idx = torch.empty(B, Hq, topk, dtype=torch.int32, device=q.device) if idx is None else idx
-    scores = torch.empty(B, Hq, N, dtype=torch.float32, device=q.device) if return_scores else None
+    idx = torch.empty(B, H, topk, dtype=torch.int32, device=q.device) if idx is None else idx
+    scores = torch.empty(B, H, N, dtype=torch.float32, device=q.device) if return_scores else None
     ws, buf = _ws(ws, q.device, workspace_size(desc, topk, DECODE), stream)
     _check(_lib.kascade_anchor_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
                                       _ptr(out), _ptr(idx), _ptr(scores), _ptr(buf), buf.numel(),
@@ -210,10 +216,11 @@ def anchor_decode(q, k, v, topk, group_map=None, scale=None, return_scores=False
     return (out, idx, scores) if return_scores else (out, idx)
 
 
-def reuse_decode(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, stream=None):
-    """Reuse layer over saved sets idx [B,Hq,topk] (int32, ascending)."""
+def reuse_decode(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, stream=None,
+                 pooled=False):
+    """Reuse layer over saved sets idx [B,Hq,topk] (pooled: [B,Hkv,topk]; int32, ascending)."""
     _contig(q, k, v, idx)
-    desc = decode_desc(q, k, group_map, scale)
+    desc = decode_desc(q, k, group_map, scale, pooled)
     topk = idx.shape[-1]
     out = torch.empty_like(q) if out is None else out
     ws, buf = _ws(ws, q.device, workspace_size(desc, topk, DECODE), stream)
@@ -252,14 +259,16 @@ def dense_prefill(q, k, v, group_map=None, scale=None, out=None, ws=None, stream
 
 
 def anchor_prefill(q, k, v, topk, group_map=None, scale=None, out=None, idx=None, ws=None,
-                   stream=None):
-    """Anchor layer, prefill: (out, idx [B,Hq,nT,topk] int32, -1 padded)."""
+                   stream=None, pooled=False):
+    """Anchor layer, prefill: (out, idx [B,H,nT,topk] int32, -1 padded), H = Hq or,
+    pooled, Hkv."""
     _contig(q, k, v)
-    desc = prefill_desc(q, k, group_map, scale)
+    desc = prefill_desc(q, k, group_map, scale, pooled)
     B, Hq, N, _ = q.shape
+    H = k.shape[1] if pooled else Hq
     out = torch.empty_like(q) if out is None else out
     if idx is None:
-        idx = torch.empty(B, Hq, n_tiles(N), topk, dtype=torch.int32, device=q.device)
+        idx = torch.empty(B, H, n_tiles(N), topk, dtype=torch.int32, device=q.device)
     ws, buf = _ws(ws, q.device, workspace_size(desc, topk, PREFILL), stream)
     _check(_lib.kascade_anchor_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
                                        _ptr(out), _ptr(idx), _ptr(buf), buf.numel(),
@@ -267,10 +276,11 @@ def anchor_prefill(q, k, v, topk, group_map=None, scale=None, out=None, idx=None
     return out, idx
 
 
-def reuse_prefill(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, stream=None):
-    """Reuse layer, prefill, over saved tile sets idx [B,Hq,nT,topk]."""
+def reuse_prefill(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, stream=None,
+                  pooled=False):
+    """Reuse layer, prefill, over saved tile sets idx [B,Hq,nT,topk] (pooled: [B,Hkv,nT,topk])."""
     _contig(q, k, v, idx)
-    desc = prefill_desc(q, k, group_map, scale)
+    desc = prefill_desc(q, k, group_map, scale, pooled)
     topk = idx.shape[-1]
     out = torch.empty_like(q) if out is None else out
     ws, buf = _ws(ws, q.device, workspace_size(desc, topk, PREFILL), stream)
@@ -283,21 +293,23 @@ def reuse_prefill(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, s
 # ------------------------------------------------------------------- stack --
 
 def run_stack(mode, qs, ks, vs, topk, anchors, group_map=None, scale=None, outs=None,
-              idx_buf=None, ws=None, stream=None, layer_events=None):
+              idx_buf=None, ws=None, stream=None, layer_events=None, pooled=False):
     """Run a layer stack; returns (outs, idx_buf). mode: DECODE or PREFILL.
 
     layer_events: optional list of torch.cuda.Event (timing enabled), one per
-    layer, recorded on the stream after that layer's launches."""
+    layer, recorded on the stream after that layer's launches. pooled: one
+    index set per KV head."""
     L = len(qs)
     _contig(*qs, *ks, *vs)
+    H = ks[0].shape[1] if pooled else qs[0].shape[1]
     if mode == DECODE:
-        desc = decode_desc(qs[0], ks[0], group_map, scale)
-        B, Hq, _ = qs[0].shape
-        shape = (B, Hq, topk)
+        desc = decode_desc(qs[0], ks[0], group_map, scale, pooled)
+        B = qs[0].shape[0]
+        shape = (B, H, topk)
     else:
-        desc = prefill_desc(qs[0], ks[0], group_map, scale)
-        B, Hq, N, _ = qs[0].shape
-        shape = (B, Hq, n_tiles(N), topk)
+        desc = prefill_desc(qs[0], ks[0], group_map, scale, pooled)
+        B, _, N, _ = qs[0].shape
+        shape = (B, H, n_tiles(N), topk)
     dev = qs[0].device
     outs = [torch.empty_like(q) for q in qs] if outs is None else outs
     if idx_buf is None:
@@ -343,15 +355,17 @@ def schedule_anchors(sim, n_anchors: int):
     return list(out), obj.value
 
 
-def calibrate(qs, ks, vs, topk, group_map=None, scale=None, ws=None, stream=None):
-    """Every layer as an anchor; returns (sim [L][L] list of lists, sets [L, B*Hq, topk])."""
+def calibrate(qs, ks, vs, topk, group_map=None, scale=None, ws=None, stream=None, pooled=False):
+    """Every layer as an anchor; returns (sim [L][L] list of lists, sets [L, B*H, topk]),
+    H = Hq, or Hkv when pooled."""
     L = len(qs)
     _contig(*qs, *ks, *vs)
-    desc = decode_desc(qs[0], ks[0], group_map, scale)
+    desc = decode_desc(qs[0], ks[0], group_map, scale, pooled)
     B, Hq, _ = qs[0].shape
+    H = ks[0].shape[1] if pooled else Hq
     dev = qs[0].device
     outs = [torch.empty_like(q) for q in qs]
-    sets = torch.empty(L, B * Hq, topk, dtype=torch.int32, device=dev)
+    sets = torch.empty(L, B * H, topk, dtype=torch.int32, device=dev)
     nbytes = _lib.kascade_calibrate_workspace_size(ctypes.byref(desc), int(topk), L)
     if nbytes == 0:
         raise KascadeError(INVALID_ARG, "kascade_calibrate_workspace_size")

@@ -65,6 +65,27 @@ def test_validation_before_launch(K):
     assert K._lib.kascade_topk(p, 4, 10, 11, p, p, 256, None) == K.INVALID_ARG
 
 
+def test_index_mode_validation_and_workspace(K):
+    import ctypes
+    per_head = K.make_desc(2, 8, 2, 128, 4096, K.BF16)
+    pooled = K.make_desc(2, 8, 2, 128, 4096, K.BF16, pooled=True)
+    assert pooled.index_mode == K.PER_KVHEAD and per_head.index_mode == K.PER_QHEAD
+    # pooled sets need room for the row statistics and the pooled weights
+    # (decode: 8 B per query-head row + 4 B per (KV head, key)), and for the
+    # pooled tile weights (prefill)
+    d_ph, d_po = (K.workspace_size(x, 64, K.DECODE) for x in (per_head, pooled))
+    assert d_po - d_ph >= 2 * 8 * 8 + 2 * 2 * 4096 * 4
+    p_ph, p_po = (K.workspace_size(x, 64, K.PREFILL) for x in (per_head, pooled))
+    nT = 4096 // 128
+    assert p_po - p_ph >= 2 * 2 * (64 * (nT - 1) * nT + 4096) * 4
+    bad = K.make_desc(2, 8, 2, 128, 4096, K.BF16)
+    bad.index_mode = 2
+    assert K._lib.kascade_workspace_size(ctypes.byref(bad), 64, 0) == 0
+    p = ctypes.c_void_p(1 << 20)
+    assert K._lib.kascade_anchor_decode(ctypes.byref(bad), p, p, p, 8, p, p, None, p, 1 << 30,
+                                        None) == K.INVALID_ARG
+
+
 def test_status_strings(K):
     for s in range(7):
         assert len(K.status_string(s)) > 0
