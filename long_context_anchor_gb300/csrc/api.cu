@@ -416,7 +416,10 @@ void fill_prefill_args(PrefillArgs& a, const Shape& s, const void* q, const void
   a.nT = (s.N + 127) / 128;
   a.scale = s.scale;
   a.scale_log2 = s.scale * 1.4426950408889634f;
-  for (int h = 0; h < s.Hq; ++h) a.head_kv[h] = s.head_kv[h];
+  for (int h = 0; h < s.Hq; ++h) {
+    a.head_kv[h] = s.head_kv[h];
+    a.heads[h] = s.heads[h];
+  }
 }
 
 kascade_status run_dense_prefill(const Shape& s, const void* q, const void* k, const void* v,

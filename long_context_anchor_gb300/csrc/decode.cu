@@ -767,7 +767,10 @@ cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spi
 }
 
 cudaError_t launch_decode_union_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st) {
-  if (head_dim == 128) return launch_union_t<128, kUnionNW, 2>(a, st);
+  // pooled sets carry k rows per unit instead of the ~G k / 2 of a union, so
+  // their CTAs are shorter: one more stage in flight per warp pays there
+  if (head_dim == 128)
+    return a.pooled ? launch_union_t<128, kUnionNW, 3>(a, st) : launch_union_t<128, kUnionNW, 2>(a, st);
   if (head_dim == 64) return launch_union_t<64, kUnionNW, 3>(a, st);
   return cudaErrorInvalidValue;
 }

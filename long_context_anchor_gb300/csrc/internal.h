@@ -79,6 +79,7 @@ struct PrefillArgs {
   int B, Hq, Hkv, N, G, topk, nT;
   float scale, scale_log2;
   int16_t head_kv[kMaxQHeads];   // KV head of each query head
+  int16_t heads[kMaxQHeads];     // heads[g*G + slot] = query head of slot in group g
 };
 cudaError_t launch_prefill_dense(const PrefillArgs& a, int head_dim, cudaStream_t st);
 cudaError_t launch_prefill_lse(const PrefillArgs& a, int head_dim, cudaStream_t st);

@@ -36,20 +36,39 @@ __device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s
 }
 
 // One CTA per logit row: row_stat[r] = (max_j s_rj, 1 / sum_j exp(s_rj - max)).
-// A NaN logit makes the sum NaN, so every pooled weight of its group is NaN
-// and the Top-k that follows reports it.
-__global__ void __launch_bounds__(256) k_row_stat(const float* __restrict__ s, int n,
-                                                  float2* __restrict__ row_stat) {
-  __shared__ float sm[8], ss[8];
+// Each thread takes kStatUnroll keys per step with independent loads (the row
+// was just written and mostly sits in L2, so the loop is load-latency bound
+// unless several loads are in flight), then folds them into its running
+// (max, sum). A NaN logit makes the sum NaN, so every pooled weight of its
+// group is NaN and the Top-k that follows reports it.
+constexpr int kStatThreads = 512, kStatUnroll = 8;
+__global__ void __launch_bounds__(kStatThreads) k_row_stat(const float* __restrict__ s, int n,
+                                                           float2* __restrict__ row_stat) {
+  __shared__ float sm[kStatThreads / 32], ss[kStatThreads / 32];
   const float* row = s + static_cast<size_t>(blockIdx.x) * n;
   float m = kNegInf, sum = 0.f;
-  for (int j = threadIdx.x; j < n; j += blockDim.x) {
-    const float x = __ldg(row + j);
-    if (x > m) {
-      sum = (m == kNegInf) ? 0.f : sum * exp2f((m - x) * kLog2e);
-      m = x;
+  for (int j0 = threadIdx.x; j0 < n; j0 += kStatThreads * kStatUnroll) {
+    float x[kStatUnroll];
+#pragma unroll
+    for (int u = 0; u < kStatUnroll; ++u) {
+      const int j = j0 + u * kStatThreads;
+      x[u] = j < n ? __ldg(row + j) : kNegInf;
     }
-    sum += exp2f((x - m) * kLog2e);
+    float lm = x[0];
+#pragma unroll
+    for (int u = 1; u < kStatUnroll; ++u) lm = fmaxf(lm, x[u]);
+    if (lm > m) {
+      sum = (m == kNegInf) ? 0.f : sum * exp2f((m - lm) * kLog2e);
+      m = lm;
+    }
+    if (m != kNegInf) {
+#pragma unroll
+      for (int u = 0; u < kStatUnroll; ++u) sum += exp2f((x[u] - m) * kLog2e);
+    } else {
+#pragma unroll
+      for (int u = 0; u < kStatUnroll; ++u)
+        if (x[u] != kNegInf) sum += exp2f(x[u]);   // NaN reaches the sum
+    }
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -65,7 +84,7 @@ __global__ void __launch_bounds__(256) k_row_stat(const float* __restrict__ s, i
   __syncthreads();
   if (threadIdx.x == 0) {
     float M = sm[0], S = ss[0];
-    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) stat_merge(M, S, sm[w], ss[w]);
+    for (int w = 1; w < kStatThreads / 32; ++w) stat_merge(M, S, sm[w], ss[w]);
     row_stat[blockIdx.x] = make_float2(M, 1.f / S);
   }
 }
@@ -138,7 +157,7 @@ cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w,
   if (B < 1 || Hq < 1 || Hkv < 1 || G < 1 || N < 1 || Hq != Hkv * G || Hq > kMaxQHeads)
     return cudaErrorInvalidValue;
   const HeadTable ht = make_table(heads, Hq);
-  k_row_stat<<<B * Hq, 256, 0, st>>>(spill, N, row_stat);
+  k_row_stat<<<B * Hq, kStatThreads, 0, st>>>(spill, N, row_stat);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   k_pool_decode<<<dim3((N + 1023) / 1024, B * Hkv), 256, 0, st>>>(spill, row_stat, w, ht, Hq,

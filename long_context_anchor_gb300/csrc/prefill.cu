@@ -534,6 +534,365 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
 }
 
 // ------------------------------------------------------------------------
+// Reuse prefill over GQA-pooled sets: the query heads of one KV head read the
+// same saved rows, so a CTA takes two of them (one per pipeline) for one tile
+// and both pipelines consume every gathered chunk. Per FLOP this halves the
+// gathers of the per-head kernel above, whose pipelines split the chunks of
+// one head. Q stays in shared memory (two 128-row tiles) and is the A operand
+// of S = Q K^T; each pipeline keeps its own S, P and O columns in TMEM and
+// writes its own head's rows, so there is no merge. One kPairST-deep ring of
+// K/V chunks is filled by four gather warps (chunks j = w, w + 4, ...) and a
+// stage is freed once both pipelines' P V products that read it completed.
+// Warps: 0-3 softmax of pipe 0, 4-7 softmax of pipe 1, 8/9 MMA of pipe 0/1,
+// 10-13 gathers.
+constexpr int kPairThreads = 448;
+constexpr int kPairST = 5;
+
+struct PairSmem {
+  static constexpr int KC = 64, ST = kPairST;
+  static constexpr int KHALF = KC * 128;              // one 64-dim half of a K (or V) chunk
+  static constexpr int KV_BYTES = 2 * KHALF;          // a K (or V) chunk
+  static constexpr int STAGE = 2 * KV_BYTES;          // K, then V
+  static constexpr int Q = 0;                         // two 128-row Q tiles
+  static constexpr int RING = 2 * kTileBytes;
+  static constexpr int POS = RING + ST * STAGE;       // int32 positions [ST][KC], flags [ST]
+  static constexpr int POS_BYTES = ST * (KC + 1) * 4;
+  static constexpr int NB = 2 * ST + 8 + 1;           // kv_full, kv_free, 4 per pipe, q_full
+  static constexpr int BAR = (POS + POS_BYTES + 7) & ~7;
+  static constexpr int TMEM = BAR + NB * 8;
+  static constexpr int BYTES = TMEM + 8;
+  static constexpr size_t SMEM = BYTES + 1024;        // + slack for 1024-byte alignment
+  static_assert(SMEM <= 232448, "two Q tiles and the ring must fit in shared memory");
+  static_assert(RING % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles are 1024-byte aligned");
+  // TMEM columns of pipeline p at 224 p: S (KC fp32), P (KC / 2 bf16 pairs), O (128)
+  static constexpr int T_PIPE_COLS = 224, T_S = 0, T_P = 64, T_O = 96;
+  static_assert(2 * T_PIPE_COLS <= 512, "two pipelines in TMEM");
+};
+
+__global__ void __launch_bounds__(kPairThreads, 1)
+    k_prefill_pair(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ PrefillArgs a) {
+  using SM = PairSmem;
+  constexpr int kKC = SM::KC, kST = SM::ST;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int pipe, role;   // role: 0 softmax, 1 MMA, 2 gather
+  if (warp < 8) { pipe = warp >> 2; role = 0; }
+  else if (warp < 10) { pipe = warp - 8; role = 1; }
+  else { pipe = 0; role = 2; }
+
+  int32_t* s_pos = reinterpret_cast<int32_t*>(sm + SM::POS);   // [kST][kKC]
+  int32_t* s_flag = s_pos + kST * kKC;                          // [kST]: 1 = no causal mask
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::BAR);
+  uint64_t* kv_full = bars;                   // [kST] chunk landed (32 lanes of its gather warp)
+  uint64_t* kv_free = bars + kST;             // [kST] both pipelines' P V read it
+  uint64_t* pb = bars + 2 * kST + 4 * pipe;
+  uint64_t* s_full = pb;                      // scores of the current chunk
+  uint64_t* s_free = pb + 1;                  // ... read by the softmax
+  uint64_t* p_full = pb + 2;                  // P of the current chunk written
+  uint64_t* pv_done = pb + 3;                 // its P V product completed
+  uint64_t* q_full = bars + 2 * kST + 8;      // both Q tiles landed
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + SM::TMEM);
+
+  const int GP = a.G >> 1;                    // head pairs per KV head
+  const int units = a.B * a.Hkv * GP;
+  const int u = static_cast<int>(blockIdx.x) % units;
+  const int t = a.nT - 1 - static_cast<int>(blockIdx.x) / units;   // longest tiles first
+  const int b = u / (a.Hkv * GP), g = (u / GP) % a.Hkv, hp = u % GP;
+  const int row0 = t * kTile;
+  const int L = min(a.N, row0 + kTile);
+  const int kt = min(a.topk, L);
+  const int nkv = (kt + kKC - 1) / kKC;
+  const int32_t* idx_row = a.idx + ((static_cast<size_t>(b) * a.Hkv + g) * a.nT + t) * a.topk;
+  const int kv_row_base = (b * a.Hkv + g) * a.N;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kST; ++s) {
+      mbar_init(kv_full + s, 32);
+      mbar_init(kv_free + s, 2);
+    }
+    for (int p = 0; p < 2; ++p) {
+      uint64_t* q = bars + 2 * kST + 4 * p;
+      mbar_init(q, 1);         // s_full
+      mbar_init(q + 1, 128);   // s_free
+      mbar_init(q + 2, 128);   // p_full
+      mbar_init(q + 3, 1);     // pv_done
+    }
+    mbar_init(q_full, 1);
+    fence_barrier_init();
+  }
+  if (warp == 8) tmem_alloc(s_tmem, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *s_tmem;
+  const uint32_t tS = tmem_base + pipe * SM::T_PIPE_COLS + SM::T_S;
+  const uint32_t tP = tS - SM::T_S + SM::T_P, tO = tS - SM::T_S + SM::T_O;
+
+  if (role == 2) {
+    // ------------------------------------------------ gathers
+    if (warp == 10 && lane == 0) {
+      prefetch_tmap(&tmQ);
+      mbar_arrive_expect_tx(q_full, 2 * kTileBytes);
+      for (int p = 0; p < 2; ++p) {
+        const int y = (b * a.Hq + a.heads[g * a.G + 2 * hp + p]) * a.N + row0;
+        tma_load_2d(sm + SM::Q + p * kTileBytes, &tmQ, q_full, 0, y);
+        tma_load_2d(sm + SM::Q + p * kTileBytes + kHalf, &tmQ, q_full, 64, y);
+      }
+    }
+    // Warp 10 + w gathers chunks j = w, w + 4, ... with up to kDepth of them
+    // in flight; a chunk is released (kv_full) once its copies have landed.
+    // Before waiting for a ring stage that is still busy a warp releases every
+    // chunk it has in flight, so no pipeline waits on copies held back behind
+    // that wait. Positions are read one chunk ahead.
+    constexpr int kProd = 4, kDepth = 2;
+    const int w0 = warp - 10;
+    int p_first = __ldg(idx_row);
+    if (p_first < 0 || p_first >= a.N) p_first = 0;
+    const int sub = lane >> 4, c16 = lane & 15;
+    const __nv_bfloat16* kl = static_cast<const __nv_bfloat16*>(a.k) +
+                              static_cast<size_t>(kv_row_base) * 128 + c16 * 8;
+    const __nv_bfloat16* vl = static_cast<const __nv_bfloat16*>(a.v) +
+                              static_cast<size_t>(kv_row_base) * 128 + c16 * 8;
+    uint32_t sw[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      sw[q] = (c16 >> 3) * SM::KHALF + sub * 128 + (((c16 & 7) ^ ((2 * q + sub) & 7)) << 4);
+    auto read_pos = [&](int j, int (&pos)[kKC / 32]) {
+#pragma unroll
+      for (int half = 0; half < kKC / 32; ++half) {
+        const int e = j * kKC + lane + 32 * half;
+        pos[half] = e < kt ? __ldg(idx_row + e) : -1;
+      }
+    };
+    auto release_all = [&](int from, int to) {   // own chunks from, from + kProd, ... < to
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      for (int c = from; c < to; c += kProd) mbar_arrive(kv_full + c % kST);
+    };
+    int nxt[kKC / 32];
+    if (w0 < nkv) read_pos(w0, nxt);
+    int issued = w0, released = w0;   // own chunks [released, issued) are in flight
+    for (int j = w0; j < nkv; j += kProd) {
+      const int s = j % kST;
+      int pos[kKC / 32];
+#pragma unroll
+      for (int half = 0; half < kKC / 32; ++half) pos[half] = nxt[half];
+      if (j + kProd < nkv) read_pos(j + kProd, nxt);
+      const uint32_t par = ((j / kST) & 1) ^ 1;
+      int ready = lane == 0 ? mbar_test_wait(kv_free + s, par) : 0;
+      if (!__shfl_sync(0xffffffffu, ready, 0)) {
+        release_all(released, issued);
+        released = issued;
+        int okw = 1;
+        if (lane == 0) okw = mbar_wait(kv_free + s, par, a.err, 0x6a5);
+        if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+      }
+      const uint32_t kd = smem_u32(sm + SM::RING + s * SM::STAGE), vd = kd + SM::KV_BYTES;
+      // validate; padding slots (-1) re-read the tile's first saved row and
+      // are masked later
+      int src[kKC / 32], pmax = -1;
+      bool all_valid = true;
+#pragma unroll
+      for (int half = 0; half < kKC / 32; ++half) {
+        const int pt = lane + 32 * half;
+        const int e = j * kKC + pt;
+        int p = pos[half];
+        if (p >= a.N || (e < kt && p < 0)) {
+          report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x6a2);
+          p = -1;
+        }
+        s_pos[s * kKC + pt] = p;
+        src[half] = p >= 0 ? p : p_first;
+        all_valid = all_valid && p >= 0;
+        pmax = max(pmax, p);
+      }
+      // a chunk of valid keys that all precede the tile's first row needs no
+      // causal mask in any of its rows
+      all_valid = __all_sync(0xffffffffu, all_valid);
+      pmax = __reduce_max_sync(0xffffffffu, pmax);
+      if (lane == 0) s_flag[s] = (all_valid && pmax <= row0) ? 1 : 0;
+      // coalesced copies: a half-warp moves one 256-byte row (16 lanes x 16
+      // bytes), so each instruction fills two rows of K (or V) in full
+#pragma unroll
+      for (int rr = 0; rr < kKC / 2; ++rr) {
+        const int prow = __shfl_sync(0xffffffffu, src[(2 * rr) >> 5], (2 * rr + sub) & 31);
+        const uint32_t off = sw[rr & 3] + rr * 256;
+        cp_async16_s(kd + off, kl + static_cast<size_t>(prow) * 128);
+        cp_async16_s(vd + off, vl + static_cast<size_t>(prow) * 128);
+      }
+      cp_async_commit();
+      issued = j + kProd;
+      if (issued - released >= kDepth * kProd) {   // the oldest own chunk in flight has landed
+        cp_async_wait<kDepth - 1>();
+        fence_proxy_async_smem();
+        mbar_arrive(kv_full + released % kST);
+        released += kProd;
+      }
+    }
+    // release what is still in flight (also after an error, so that no copy
+    // outlives the kernel)
+    release_all(released, issued);
+    if (warp == 10 && lane == 0) mbar_wait(q_full, 0, a.err, 0x6a3);   // no copies left in flight
+  } else if (role == 1) {
+    // ------------------------------------------------ MMA issuer of pipe p
+    constexpr uint32_t idq = idesc_bf16_f32(128, kKC, 0, 0);
+    constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
+    const uint32_t sQp = smem_u32(sm + SM::Q + pipe * kTileBytes);
+    const uint32_t sRing = smem_u32(sm + SM::RING);
+    bool ok = mbar_wait(q_full, 0, a.err, 0x6b1);
+    // S = Q K^T of chunk i once the softmax has read S(i-1)
+    auto issue_s = [&](int i) {
+      const int s = i % kST;
+      if (!mbar_wait(kv_full + s, (i / kST) & 1, a.err, 0x6b3)) return false;
+      if (i > 0 && !mbar_wait(s_free, (i - 1) & 1, a.err, 0x6b4)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma(tS, kmajor_desc(sQp, kk), kmajor_desc(sRing + s * SM::STAGE, kk, SM::KHALF), idq,
+               kk > 0 ? 1u : 0u);
+      tc_commit(s_full);
+      return true;
+    };
+    // O += P V with P (A operand) from TMEM; the stage is freed for both pipes
+    auto issue_pv = [&](int i) {
+      const int s = i % kST;
+      if (!mbar_wait(p_full, i & 1, a.err, 0x6b2)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < kKC / 16; ++kk)
+        tc_mma_ts(tO, tP + kk * 8, vmn_desc(sRing + s * SM::STAGE + SM::KV_BYTES, kk, SM::KHALF),
+                  idv, (i > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(pv_done);
+      tc_commit(kv_free + s);
+      return true;
+    };
+    if (ok) tc_fence_after();
+    if (ok && nkv > 0) ok = issue_s(0);
+    for (int i = 0; ok && i < nkv; ++i) {
+      if (i + 1 < nkv) ok = issue_s(i + 1);
+      if (ok) ok = issue_pv(i);
+    }
+  } else {
+    // ------------------------------------------------ softmax warpgroup of pipe p
+    const int r = (warp & 3) * 32 + lane;
+    const int row = row0 + r;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    bool ok = true;
+    float m_used = kNegInfP, l = 0.f;
+    for (int i = 0; ok && i < nkv; ++i) {
+      const int s = i % kST;
+      ok = mbar_wait(s_full, i & 1, a.err, 0x6c1);
+      if (!ok) break;
+      tc_fence_after();
+      float x[kKC];
+#pragma unroll
+      for (int c = 0; c < kKC / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + c * 32 + lane_base, v);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
+      }
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(s_free);   // the score columns may take S(i+1) now
+      if (s_flag[s] == 0) {
+#pragma unroll
+        for (int c = 0; c < kKC; ++c) {
+          const int kp = s_pos[s * kKC + c];
+          if (!(kp >= 0 && kp <= row)) x[c] = kNegInfP;
+        }
+      }
+      float mx[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) mx[c] = fmaxf(x[2 * c], x[2 * c + 1]);
+#pragma unroll
+      for (int c = 8; c < kKC / 2; ++c) mx[c & 7] = fmax3(mx[c & 7], x[2 * c], x[2 * c + 1]);
+      float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+      tmax *= a.scale_log2;
+      float alpha = 1.f;
+      bool resc = false;
+      if (tmax > m_used + kRescaleLog2) {
+        if (i > 0) {
+          alpha = ex2_approx(m_used - tmax);
+          resc = true;
+        }
+        l *= alpha;
+        m_used = tmax;
+      }
+      const float mu = (m_used == kNegInfP) ? 0.f : m_used;
+      const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nmu2 = f2_pack(-mu, -mu);
+      uint32_t pk[kKC / 2];
+      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+      for (int c = 0; c < kKC / 2; ++c) {
+        float y0, y1;
+        f2_unpack(f2_fma(f2_pack(x[2 * c], x[2 * c + 1]), sc2, nmu2), y0, y1);
+        const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+        ls2[c & 3] = f2_add(ls2[c & 3], f2_pack(p0, p1));
+        pk[c] = pack_bf16(p0, p1);
+      }
+      {
+        float s0, s1;
+        f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), s0, s1);
+        l += s0 + s1;
+      }
+      // the P columns and O are free once the previous P V product has landed
+      if (i > 0) {
+        ok = mbar_wait(pv_done, (i - 1) & 1, a.err, 0x6c2);
+        if (!ok) break;
+      }
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + c * 32 + lane_base, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(tO + c * 32 + lane_base, o);
+        }
+      }
+      tmem_store_p<kKC>(tP + lane_base, pk);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && nkv > 0) ok = mbar_wait(pv_done, (nkv - 1) & 1, a.err, 0x6c3);
+    tc_fence_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    const int hq = a.heads[g * a.G + 2 * hp + pipe];
+    __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(a.out) +
+                          ((static_cast<size_t>(b) * a.Hq + hq) * a.N + row) * kTile;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t o[32];
+      tmem_ld32(tO + c * 32 + lane_base, o);
+      tmem_wait_ld();
+      uint32_t ob[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        ob[e] = ok ? pack_bf16(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv)
+                   : 0u;
+      if (row < a.N) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = make_uint4(ob[4 * q], ob[4 * q + 1], ob[4 * q + 2], ob[4 * q + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+// ------------------------------------------------------------------------
 // Anchor pass 2: tile weights from S^T = K_j Q_t^T (TMEM lane = key).
 // Warp 0 loads the Q tile once and the key tiles 0..t into a kWtKS-deep ring
 // by TMA; warp 1 issues S^T(j) into TMEM score buffer j % kWtSB; kWtGroups
@@ -753,6 +1112,17 @@ cudaError_t launch_prefill_anchor_main(const PrefillArgs& a, int head_dim, cudaS
 
 cudaError_t launch_prefill_reuse(const PrefillArgs& a, int head_dim, cudaStream_t st) {
   if (head_dim != 128) return cudaErrorNotSupported;
+  if (a.pooled && a.G >= 2 && a.G % 2 == 0) {
+    // pooled sets: two query heads of a KV head per CTA, sharing every gather
+    alignas(64) CUtensorMap tq;
+    if (!make_maps(a, &tq, nullptr, nullptr, PairSmem::KC)) return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_prefill_pair,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(PairSmem::SMEM));
+    if (e != cudaSuccess) return e;
+    k_prefill_pair<<<a.B * a.Hkv * (a.G / 2) * a.nT, kPairThreads, PairSmem::SMEM, st>>>(tq, a);
+    return cudaGetLastError();
+  }
   return launch_fa<true, false>(a, st);
 }
 

@@ -195,6 +195,57 @@ def test_pooled_reuse_prefill_matches_oracle(K, shape, topk):
     check_out(out, A.sparse_prefill_pooled(f64(q2), f64(k2), f64(v2), idx.cpu().numpy()))
 
 
+@pytest.mark.parametrize("shape,topk", [((1, 4, 2, 640), 200), ((1, 16, 2, 384), 96),
+                                        ((2, 4, 1, 300), 64)])
+def test_pooled_reuse_prefill_equals_per_head_kernel(K, shape, topk):
+    # the paired-head kernel (two heads of a KV head per CTA, one gather)
+    # against the per-head kernel given each head its group's set
+    B, Hq, Hkv, N = shape
+    q, k, v = _prefill_layer(B, Hq, Hkv, N, seed=11 * N + Hq)
+    _, idx = K.anchor_prefill(q, k, v, topk, pooled=True)
+    out_p = K.reuse_prefill(q, k, v, idx, pooled=True)
+    gm = default_gmap(Hq, Hkv)
+    idx_h = idx[:, gm].contiguous()
+    out_h = K.reuse_prefill(q, k, v, idx_h)
+    assert (out_p.float() - out_h.float()).abs().max().item() <= 1.6e-2
+    check_out(out_p, A.sparse_prefill_pooled(f64(q), f64(k), f64(v), idx.cpu().numpy()))
+
+
+def test_pooled_reuse_prefill_poison_and_empty_rows(K):
+    B, Hq, Hkv, N, topk = 1, 8, 2, 512, 64
+    q, k, v = _prefill_layer(B, Hq, Hkv, N, seed=23)
+    nT = A.n_tiles(N)
+    rng = np.random.default_rng(5)
+    idx = np.full((B, Hkv, nT, topk), -1, dtype=np.int32)
+    for g in range(Hkv):
+        for t in range(nT):
+            L = min(N, 128 * (t + 1))
+            # no saved key below position 30: rows 0..29 see an empty set
+            sel = np.sort(rng.choice(np.arange(30, L), min(topk, L - 30), replace=False))
+            idx[0, g, t, :sel.size] = sel
+    idx_t = torch.from_numpy(idx).to(DEV)
+    out = K.reuse_prefill(q, k, v, idx_t, pooled=True)
+    check_out(out, A.sparse_prefill_pooled(f64(q), f64(k), f64(v), idx))
+    assert float(out[0, :, :30].float().abs().max()) == 0.0
+    used = torch.zeros(B, Hkv, N, dtype=torch.bool, device=DEV)
+    for g in range(Hkv):
+        sel = idx_t[0, g].reshape(-1)
+        used[0, g, sel[sel >= 0].long()] = True
+    kp, vp = k.clone(), v.clone()
+    kp[~used] = float("nan")
+    vp[~used] = float("nan")
+    assert torch.equal(K.reuse_prefill(q, kp, vp, idx_t, pooled=True), out)
+
+
+def test_pooled_reuse_prefill_bad_index_reported(K):
+    ws = K.Workspace(DEV)
+    q, k, v = _prefill_layer(1, 4, 2, 256, seed=29)
+    idx = torch.arange(32, dtype=torch.int32, device=DEV).expand(1, 2, 2, 32).contiguous()
+    idx[0, 1, 1, 7] = 4096
+    K.reuse_prefill(q, k, v, idx, ws=ws, pooled=True)
+    assert ws.device_error() == K.BAD_INPUT
+
+
 def test_pooled_prefill_stack_matches_layer_calls(K):
     w = configs.LLAMA8B_PREFILL_16K.with_(n_layers=3, kv_len=640, topk=80, anchors=(0,))
     qs, ks, vs = make_layers(w, device=DEV)
