@@ -319,10 +319,11 @@ def run_prefill(args, dev, world, stream, clocks):
     outs = [torch.empty_like(q) for q in qs]
     nT = (w.kv_len + 127) // 128
     idx_buf = torch.empty(w.batch, w.n_q_heads, nT, w.topk, dtype=torch.int32, device=dev)
+    idx_pool = torch.empty(w.batch, w.n_kv_heads, nT, w.topk, dtype=torch.int32, device=dev)
     ws = K.Workspace(dev)
     anchors = list(w.anchors)
 
-    def timed(anch, steps):
+    def timed(anch, steps, pooled=False):
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(steps)]
         for row in evs:
             for e in row:
@@ -332,8 +333,9 @@ def run_prefill(args, dev, world, stream, clocks):
             dist.barrier()
         for s in range(steps):
             evs[s][0].record(stream)
-            K.run_stack(K.PREFILL, qs, ks, vs, w.topk, anch, outs=outs, idx_buf=idx_buf, ws=ws,
-                        layer_events=evs[s][1:])
+            K.run_stack(K.PREFILL, qs, ks, vs, w.topk, anch, outs=outs,
+                        idx_buf=idx_pool if pooled else idx_buf, ws=ws,
+                        layer_events=evs[s][1:], pooled=pooled)
         torch.cuda.synchronize()
         per = [[evs[s][l].elapsed_time(evs[s][l + 1]) for l in range(L)] for s in range(steps)]
         total = sum(evs[s][0].elapsed_time(evs[s][L]) for s in range(steps))
@@ -377,6 +379,26 @@ def run_prefill(args, dev, world, stream, clocks):
         "peak_bf16_tflops_sustained": tf_sust, "peak_bf16_tflops_burst": tf_burst,
         "peak_source": src,
     }
+    if not args.no_pooled:
+        # GQA-pooled tile sets (one per KV head) on the same inputs
+        K.run_stack(K.PREFILL, qs, ks, vs, w.topk, anchors, outs=outs, idx_buf=idx_pool, ws=ws,
+                    pooled=True)
+        torch.cuda.synchronize()
+        assert ws.device_error() == K.OK
+        clocks.begin()
+        tot_p, per_p = timed(anchors, steps, pooled=True)
+        clocks.end()
+        tot_p = max_over_ranks([tot_p], world, dev)[0]
+        ms_p = tot_p / steps
+        pa = statistics.mean(per_p[s][l] for s in range(steps) for l in anchors)
+        pr = statistics.mean(per_p[s][l] for s in range(steps) for l in reuse_layers)
+        res["pooled"] = {"index_sets": "one per (KV head, tile): group sums of tile weights",
+                         "kascade_ms_per_stack": round(ms_p, 3),
+                         "speedup_vs_own_dense": round(ms_d / ms_p, 3),
+                         "anchor_layer_us": round(1e3 * pa, 1), "reuse_layer_us": round(1e3 * pr, 1),
+                         "reuse_tflops": round(f_reuse / (pr * 1e-3) / 1e12, 1),
+                         "reuse_frac_of_sustained": round(f_reuse / (pr * 1e-3) / 1e12 / tf_sust, 4),
+                         "gpu_launches": steps * (4 * len(anchors) + len(reuse_layers))}
     res["dense_frac_of_sustained"] = round(res["dense_tflops"] / tf_sust, 4)
     res["anchor_frac_of_sustained"] = round(res["anchor_tflops"] / tf_sust, 4)
     res["reuse_frac_of_sustained"] = round(res["reuse_tflops"] / tf_sust, 4)

@@ -1,13 +1,14 @@
 """Run one attention layer kind a few times on synthetic inputs (for profilers).
 
     python -m long_context_anchor_gb300.runcase KIND [--batch B] [--kv-len N]
-        [--heads HQ HKV] [--head-dim D] [--topk K] [--reps R]
+        [--heads HQ HKV] [--head-dim D] [--topk K] [--reps R] [--pooled]
 
 KIND: dense_decode, anchor_decode, reuse_decode, topk, dense_prefill,
 anchor_prefill, reuse_prefill. Defaults are the Llama-3.1-8B attention shape
 with batch 2 (decode: about 0.5 GB of K/V per layer, larger than L2), so a
 profiler capture of one launch stays small. Inputs are drawn once; every
-repetition runs the same launch sequence.
+repetition runs the same launch sequence. --pooled uses one index set per KV
+head (anchor and reuse kinds).
 """
 import argparse
 
@@ -25,6 +26,7 @@ def main():
     ap.add_argument("--head-dim", type=int, default=128)
     ap.add_argument("--topk", type=int, default=0, help="default kv_len // 8")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--pooled", action="store_true", help="one index set per KV head")
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
     g = torch.Generator(device=dev).manual_seed(7)
@@ -39,10 +41,11 @@ def main():
     v = torch.randn(B, Hkv, N, d, generator=g, device=dev).to(bf)
     ws = K.Workspace(dev)
     idx = None
+    pl = a.pooled
     if a.kind == "reuse_decode":
-        _, idx = K.anchor_decode(q, k, v, k_top, ws=ws)
+        _, idx = K.anchor_decode(q, k, v, k_top, ws=ws, pooled=pl)
     if a.kind == "reuse_prefill":
-        _, idx = K.anchor_prefill(q, k, v, k_top, ws=ws)
+        _, idx = K.anchor_prefill(q, k, v, k_top, ws=ws, pooled=pl)
     scores = None
     if a.kind == "topk":
         scores = torch.randn(B * Hq, N, generator=g, device=dev)
@@ -51,17 +54,17 @@ def main():
         if a.kind == "dense_decode":
             K.dense_decode(q, k, v, ws=ws)
         elif a.kind == "anchor_decode":
-            K.anchor_decode(q, k, v, k_top, ws=ws)
+            K.anchor_decode(q, k, v, k_top, ws=ws, pooled=pl)
         elif a.kind == "reuse_decode":
-            K.reuse_decode(q, k, v, idx, ws=ws)
+            K.reuse_decode(q, k, v, idx, ws=ws, pooled=pl)
         elif a.kind == "topk":
             K.topk(scores, k_top, ws=ws)
         elif a.kind == "dense_prefill":
             K.dense_prefill(q, k, v, ws=ws)
         elif a.kind == "anchor_prefill":
-            K.anchor_prefill(q, k, v, k_top, ws=ws)
+            K.anchor_prefill(q, k, v, k_top, ws=ws, pooled=pl)
         elif a.kind == "reuse_prefill":
-            K.reuse_prefill(q, k, v, idx, ws=ws)
+            K.reuse_prefill(q, k, v, idx, ws=ws, pooled=pl)
         else:
             raise SystemExit("unknown kind " + a.kind)
     torch.cuda.synchronize()
