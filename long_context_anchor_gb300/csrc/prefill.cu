@@ -2,19 +2,21 @@
 // prefill works at tile level; opentrain.ai Abstract "tile-level operations";
 // one index set per (head, 128-query tile)).
 //
-//   k_prefill_fa2<REUSE, LSE>  one (sequence, query head, 128-row tile) per
-//       CTA, its 64-key chunks split over two pipelines that share the Q tile
-//       and merge their partial softmax states at the end: producer warps load
-//       the Q tile by TMA and the keys (dense/anchor layers: causal K/V tiles
-//       by TMA; reuse layers: the tile's saved K/V rows by coalesced 16-byte
-//       cp.async into the 128-byte-swizzled layout, then fence.proxy.async);
-//       Q is copied into TMEM and is the A operand of every S = Q K^T; one
-//       warp per pipeline issues tcgen05.mma S = Q K^T and O += P V with P
-//       read from TMEM; a softmax warpgroup per pipeline (one thread per query
-//       row) runs the online softmax with a lazy O rescale (only when a row
-//       maximum grows by more than 2^8) and writes P as bf16 into TMEM;
-//       pipeline 0 finally merges both partial states and writes O / l (and,
-//       for anchor layers, the row log-sum-exp). Causal masking is by key
+//   k_prefill_fa2<REUSE, LSE>  persistent, one CTA per SM taking (sequence,
+//       query head, 128-row) tiles in turn; a tile's 64-key chunks are split
+//       over two pipelines that share the Q tile and merge their partial
+//       softmax states at the end: a loader warp brings the Q tiles by TMA and
+//       producer warps the keys (dense/anchor layers: causal K/V tiles by TMA;
+//       reuse layers: the tile's saved K/V rows by coalesced 16-byte cp.async
+//       into the 128-byte-swizzled layout, then fence.proxy.async), running
+//       ahead into the next tile; Q is copied into TMEM and is the A operand
+//       of every S = Q K^T; one warp per pipeline issues tcgen05.mma S = Q K^T
+//       and O += P V with P read from TMEM; a softmax warpgroup per pipeline
+//       (one thread per query row) runs the online softmax with a lazy O
+//       rescale (only when a row maximum grows by more than 2^8) and writes P
+//       as bf16 into TMEM; at the end of a tile both pipelines merge the two
+//       partial states (half the output dims each) and write O / l (and, for
+//       anchor layers, the row log-sum-exp). Causal masking is by key
 //       position.
 //   k_prefill_weights        anchor pass 2: S^T = K Q^T per key tile (TMEM lane
 //       = key), p = 2^(s*sigma*log2e - lse2[query]), and each thread sums its
@@ -56,11 +58,19 @@ __device__ __forceinline__ void fa_tile_coords(const PrefillArgs& a, int& bh, in
   t = a.nT - 1 - static_cast<int>(blockIdx.x) / BH;
 }
 
-// One query tile per CTA, its key chunks split over two pipelines (pipe p takes
-// chunks p, p+2, ...): warps 4p..4p+3 run pipe p's softmax, warp 8+p issues its
-// MMAs, warp 10+p is its producer (TMA for Q and dense K/V); for reuse, warps
-// 10+p and 12+p gather pipe p's chunks in turn with coalesced 16-byte cp.async,
-// two chunks in flight each.
+// Persistent tiles: one CTA per SM takes the query tiles tau = blockIdx.x,
+// blockIdx.x + gridDim.x, ... (longest tiles first), each tile's 64-key chunks
+// split over two pipelines (pipe p takes chunks p, p+2, ...) that share the Q
+// tile and merge their partial softmax states at the end of the tile. Every
+// barrier phase and ring stage runs on per-pipeline chunk counters that carry
+// over from tile to tile, so the producers stream the next tile's chunks and
+// a dedicated warp loads its Q tile while the current tile is still being
+// computed; a tile boundary costs only the merge and the copy of the next Q
+// into TMEM.
+// Roles: warps 4p..4p+3 run pipe p's softmax, warp 8+p issues its MMAs, warp
+// 10+p is its producer (dense: TMA; reuse: warps 10+p and 12+p gather its
+// chunks in turn with coalesced 16-byte cp.async, two chunks in flight each),
+// and the last warp loads the Q tiles by TMA.
 // The Q tile is copied once into TMEM, where it is the A operand of every
 // S = Q K^T of both pipes, so shared memory feeds only K and V to the tensor
 // core. Every pipe has an ST-deep K/V ring in shared memory and its own score,
@@ -68,11 +78,11 @@ __device__ __forceinline__ void fa_tile_coords(const PrefillArgs& a, int& bh, in
 // read them (so S of the next chunk overlaps its exponentials), writes P as
 // bf16 into the P columns once the previous P V product has landed, and the
 // P V product takes P from TMEM as its A operand, so P never touches shared
-// memory. At the end pipe 1's (m, l, O) is merged into pipe 0's through
-// shared memory and TMEM.
-// Threads: 8 softmax warps, 2 MMA warps, 2 (dense: TMA) or 4 (reuse: gathers)
-// producer warps.
-template <bool REUSE> __host__ __device__ constexpr int fa_threads() { return REUSE ? 448 : 384; }
+// memory. At the end of a tile pipe 1 hands its (m, l) to pipe 0 through its
+// own (then idle) P columns; pipe 0 copies the next Q into TMEM, so the next
+// tile's first scores overlap the merge, then reads both O accumulators.
+template <bool REUSE> __host__ __device__ constexpr int fa_threads() { return REUSE ? 480 : 416; }
+template <bool REUSE> __host__ __device__ constexpr int fa_q_warp() { return REUSE ? 14 : 12; }
 
 // Chunk shape: KC keys per chunk and an ST-deep K/V ring per pipeline; the same
 // for streamed (TMA) and gathered chunks.
@@ -86,7 +96,7 @@ struct Fa2Smem {
   static constexpr int K0 = 0;                       // within a pipeline's area
   static constexpr int V0 = ST * KV_BYTES;
   static constexpr int PIPE_BYTES = 2 * ST * KV_BYTES;
-  static constexpr int Q = 0;
+  static constexpr int Q = 0;                        // Q staging (TMA target)
   static constexpr int PIPE0 = kTileBytes;
   static constexpr int PIPE1 = PIPE0 + PIPE_BYTES;
   static constexpr int POS = PIPE1 + PIPE_BYTES;     // reuse: int32 [2 pipes][ST][KC] + flags [2][ST]
@@ -117,6 +127,33 @@ __device__ __forceinline__ void tmem_store_p(uint32_t taddr, const uint32_t (&pk
   }
 }
 
+// One query tile of the persistent schedule.
+struct FaTile {
+  int bh, t, b, g, row0, L, nkv, kt;
+};
+template <int KC, bool REUSE>
+__device__ __forceinline__ FaTile fa_tile(const PrefillArgs& a, int tau) {
+  FaTile x;
+  const int BH = a.B * a.Hq;
+  x.bh = tau % BH;
+  x.t = a.nT - 1 - tau / BH;   // longest tiles first
+  x.b = x.bh / a.Hq;
+  x.g = a.head_kv[x.bh % a.Hq];
+  x.row0 = x.t * kTile;
+  x.L = min(a.N, x.row0 + kTile);
+  x.kt = REUSE ? min(a.topk, x.L) : 0;
+  x.nkv = REUSE ? (x.kt + KC - 1) / KC : (x.L + KC - 1) / KC;
+  return x;
+}
+
+// n-th tile of this CTA: rounds of gridDim.x tiles in longest-first order,
+// taken left to right in even rounds and right to left in odd ones, so the
+// CTAs that get a round's longest tile get the next round's shortest.
+__device__ __forceinline__ int fa_tau(int n) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  return n * G + ((n & 1) ? G - 1 - c : c);
+}
+
 template <bool REUSE, bool LSE>
 __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     k_prefill_fa2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -127,18 +164,19 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int pipe, role;   // role: 0 softmax, 1 MMA, 2 producer
+  int pipe, role;   // role: 0 softmax, 1 MMA, 2 producer, 3 Q loader
   if (warp < 8) { pipe = warp >> 2; role = 0; }
   else if (warp < 10) { pipe = warp - 8; role = 1; }
-  else { pipe = (warp - 10) & 1; role = 2; }
+  else if (warp < fa_q_warp<REUSE>()) { pipe = (warp - 10) & 1; role = 2; }
+  else { pipe = 0; role = 3; }
 
   unsigned char* ps = sm + (pipe ? SM::PIPE1 : SM::PIPE0);
   int32_t* s_pos = reinterpret_cast<int32_t*>(sm + SM::POS) + pipe * kST * kKC;
   // reuse: 1 if chunk stage s needs no causal mask
   int32_t* s_flag = reinterpret_cast<int32_t*>(sm + SM::POS) + 2 * kST * kKC + pipe * kST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::BAR);
-  uint64_t* q_full = bars + 2 * SM::NB;       // Q tile landed in shared memory
-  uint64_t* q_ready = q_full + 1;             // Q tile copied into TMEM
+  uint64_t* q_full = bars + 2 * SM::NB;       // the tile's Q landed in shared memory
+  uint64_t* q_ready = q_full + 1;             // ... and was copied into TMEM
   uint64_t* bar = bars + pipe * SM::NB;
   uint64_t* kv_full = bar;                    // [kST]
   uint64_t* kv_free = bar + kST;              // [kST]
@@ -149,25 +187,7 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + SM::TMEM);
   const uint32_t sQ = smem_u32(sm + SM::Q), sK0 = smem_u32(ps + SM::K0);
   const uint32_t sV0 = smem_u32(ps + SM::V0);
-
-  const int BH = a.B * a.Hq;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
-  const int t = a.nT - 1 - static_cast<int>(blockIdx.x) / BH;   // longest tiles first
-  const int b = bh / a.Hq, h = bh % a.Hq, g = a.head_kv[h];
-  const int row0 = t * kTile;
-  const int L = min(a.N, row0 + kTile);
-  int nkv, kt = 0;
-  const int32_t* idx_row = nullptr;
-  if (REUSE) {
-    kt = min(a.topk, L);
-    nkv = (kt + kKC - 1) / kKC;
-    const size_t set = a.pooled ? static_cast<size_t>(b) * a.Hkv + g : static_cast<size_t>(bh);
-    idx_row = a.idx + (set * a.nT + t) * a.topk;
-  } else {
-    nkv = (L + kKC - 1) / kKC;
-  }
-  const int np = (nkv - pipe + 1) / 2;   // chunks of this pipe: global chunk 2i + pipe
-  const int kv_row_base = (b * a.Hkv + g) * a.N;
+  const int total = a.B * a.Hq * a.nT;
 
   if (threadIdx.x < 2) {   // thread p initialises pipe p's barriers
     uint64_t* pb = bars + threadIdx.x * SM::NB;
@@ -194,184 +214,239 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   const uint32_t tS = tmem_base + SM::T_PIPE + pipe * SM::T_PIPE_COLS + SM::T_S;
   const uint32_t tP = tS - SM::T_S + SM::T_P, tO = tS - SM::T_S + SM::T_O;
 
-  if (role == 2) {
-    // ------------------------------------------------ producer
-    if (warp == 10 && lane == 0) {
+  if (role == 3) {
+    // ------------------------------------------------ Q loader: the tile after
+    // next may be loaded once the current Q has been copied into TMEM
+    if (lane == 0) {
       prefetch_tmap(&tmQ);
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_2d(sm + SM::Q, &tmQ, q_full, 0, bh * a.N + row0);
-      tma_load_2d(sm + SM::Q + kHalf, &tmQ, q_full, 64, bh * a.N + row0);
+      int n = 0;
+      for (int tau = fa_tau(0); tau < total; tau = fa_tau(++n)) {
+        if (n > 0 && !mbar_wait(q_ready, (n - 1) & 1, a.err, 0x630)) break;
+        const FaTile x = fa_tile<kKC, REUSE>(a, tau);
+        mbar_arrive_expect_tx(q_full, kTileBytes);
+        tma_load_2d(sm + SM::Q, &tmQ, q_full, 0, x.bh * a.N + x.row0);
+        tma_load_2d(sm + SM::Q + kHalf, &tmQ, q_full, 64, x.bh * a.N + x.row0);
+      }
+      if (n > 0) mbar_wait(q_full, (n - 1) & 1, a.err, 0x631);   // no copy left in flight
     }
+  } else if (role == 2) {
+    // ------------------------------------------------ producers
     if (!REUSE) {
       if (lane == 0) {   // one TMA producer per pipeline
-        int issued = 0;
-        for (int i = 0; i < np; ++i) {
-          const int s = i % kST, j = 2 * i + pipe;
-          if (!mbar_wait(kv_free + s, ((i / kST) & 1) ^ 1, a.err, 0x601)) break;
-          unsigned char* kd = ps + SM::K0 + s * SM::KV_BYTES;
-          unsigned char* vd = ps + SM::V0 + s * SM::KV_BYTES;
-          mbar_arrive_expect_tx(kv_full + s, 2 * SM::KV_BYTES);
-          const int y = kv_row_base + j * kKC;
-          tma_load_2d(kd, &tmK, kv_full + s, 0, y);
-          tma_load_2d(kd + SM::KHALF, &tmK, kv_full + s, 64, y);
-          tma_load_2d(vd, &tmV, kv_full + s, 0, y);
-          tma_load_2d(vd + SM::KHALF, &tmV, kv_full + s, 64, y);
-          issued = i + 1;
+        uint32_t c = 0;   // this pipe's chunks so far, over all tiles
+        bool ok = true;
+        int n = 0;
+        for (int tau = fa_tau(0); ok && tau < total; tau = fa_tau(++n)) {
+          const FaTile x = fa_tile<kKC, REUSE>(a, tau);
+          const int np = (x.nkv - pipe + 1) / 2;
+          const int kv_row_base = (x.b * a.Hkv + x.g) * a.N;
+          for (int i = 0; i < np; ++i) {
+            const uint32_t gi = c + i;
+            const int s = gi % kST;
+            if (!mbar_wait(kv_free + s, ((gi / kST) & 1) ^ 1, a.err, 0x601)) {
+              ok = false;
+              c = gi;
+              break;
+            }
+            unsigned char* kd = ps + SM::K0 + s * SM::KV_BYTES;
+            unsigned char* vd = ps + SM::V0 + s * SM::KV_BYTES;
+            mbar_arrive_expect_tx(kv_full + s, 2 * SM::KV_BYTES);
+            const int y = kv_row_base + (2 * i + pipe) * kKC;
+            tma_load_2d(kd, &tmK, kv_full + s, 0, y);
+            tma_load_2d(kd + SM::KHALF, &tmK, kv_full + s, 64, y);
+            tma_load_2d(vd, &tmV, kv_full + s, 0, y);
+            tma_load_2d(vd + SM::KHALF, &tmV, kv_full + s, 64, y);
+          }
+          if (ok) c += np;
         }
-        for (int i = issued > kST ? issued - kST : 0; i < issued; ++i)
-          mbar_wait(kv_full + (i % kST), (i / kST) & 1, a.err, 0x604);
+        // never leave with copies in flight: the last kST chunks issued
+        for (uint32_t gi = c > kST ? c - kST : 0; gi < c; ++gi)
+          mbar_wait(kv_full + (gi % kST), (gi / kST) & 1, a.err, 0x604);
       }
     } else {
-      // kProd gather warps per pipeline take its chunks in turn (i = prod,
-      // prod + kProd, ...), each with up to kDepth of its chunks in flight: a
-      // chunk is released (kv_full) once its copies have landed. Before waiting
-      // for a ring stage that is still busy, a warp releases every chunk it has
-      // in flight, so the MMA issuer never waits on copies held back behind
-      // that wait. Positions are read one chunk ahead.
+      // kProd gather warps per pipeline take its chunks in turn (global chunk
+      // gi of the pipe goes to warp gi % kProd), each with up to kDepth of its
+      // chunks in flight: a chunk is released (kv_full) once its copies have
+      // landed. Before waiting for a ring stage that is still busy, a warp
+      // releases every chunk it has in flight, so the MMA issuer never waits
+      // on copies held back behind that wait. Within a tile, positions are
+      // read one chunk ahead.
       constexpr int kProd = 2;
       constexpr int kDepth = 2;
-      int p_first = __ldg(idx_row);
-      if (p_first < 0 || p_first >= a.N) p_first = 0;
+      const int prod = (warp - 10) >> 1;
       const int sub = lane >> 4, c16 = lane & 15;
-      // this lane's 16-byte column of a key row, and its swizzled column in
-      // shared memory for rows congruent to 2u + sub (mod 8)
-      const __nv_bfloat16* kl = static_cast<const __nv_bfloat16*>(a.k) +
-                                static_cast<size_t>(kv_row_base) * 128 + c16 * 8;
-      const __nv_bfloat16* vl = static_cast<const __nv_bfloat16*>(a.v) +
-                                static_cast<size_t>(kv_row_base) * 128 + c16 * 8;
+      // this lane's swizzled 16-byte column in shared memory for rows
+      // congruent to 2u + sub (mod 8)
       uint32_t sw[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u)
         sw[u] = (c16 >> 3) * SM::KHALF + sub * 128 + (((c16 & 7) ^ ((2 * u + sub) & 7)) << 4);
-      auto read_pos = [&](int i, int (&pos)[kKC / 32]) {
-#pragma unroll
-        for (int half = 0; half < kKC / 32; ++half) {
-          const int e = (2 * i + pipe) * kKC + lane + 32 * half;
-          pos[half] = e < kt ? __ldg(idx_row + e) : -1;
-        }
-      };
-      auto release_all = [&](int from, int to) {   // own chunks from, from + kProd, ... < to
+      auto release_all = [&](uint32_t from, uint32_t to) {   // own chunks from, from + kProd, ... < to
         cp_async_wait<0>();
         fence_proxy_async_smem();
-        for (int c = from; c < to; c += kProd) mbar_arrive(kv_full + c % kST);
+        for (uint32_t c2 = from; c2 < to; c2 += kProd) mbar_arrive(kv_full + c2 % kST);
       };
-      int nxt[kKC / 32];
-      const int prod = (warp - 10) >> 1;
-      if (prod < np) read_pos(prod, nxt);
-      int issued = prod, released = prod;   // own chunks [released, issued) are in flight
-      for (int i = prod; i < np; i += kProd) {
-        const int s = i % kST, j = 2 * i + pipe;
-        int pos[kKC / 32];
+      uint32_t c = 0;                                   // this pipe's chunks so far
+      uint32_t issued = prod, released = prod;          // own chunks [released, issued) in flight
+      bool ok = true;
+      int n = 0;
+      for (int tau = fa_tau(0); ok && tau < total; tau = fa_tau(++n)) {
+        const FaTile x = fa_tile<kKC, REUSE>(a, tau);
+        const int np = (x.nkv - pipe + 1) / 2;
+        const int32_t* idx_row = a.idx + (static_cast<size_t>(x.bh) * a.nT + x.t) * a.topk;
+        const int kv_row_base = (x.b * a.Hkv + x.g) * a.N;
+        const __nv_bfloat16* kl = static_cast<const __nv_bfloat16*>(a.k) +
+                                  static_cast<size_t>(kv_row_base) * 128 + c16 * 8;
+        const __nv_bfloat16* vl = static_cast<const __nv_bfloat16*>(a.v) +
+                                  static_cast<size_t>(kv_row_base) * 128 + c16 * 8;
+        auto read_pos = [&](int i, int (&pos)[kKC / 32]) {
 #pragma unroll
-        for (int half = 0; half < kKC / 32; ++half) pos[half] = nxt[half];
-        if (i + kProd < np) read_pos(i + kProd, nxt);
-        const uint32_t par = ((i / kST) & 1) ^ 1;
-        int ready = lane == 0 ? mbar_test_wait(kv_free + s, par) : 0;
-        if (!__shfl_sync(0xffffffffu, ready, 0)) {
-          release_all(released, issued);
-          released = issued;
-          int ok = 1;
-          if (lane == 0) ok = mbar_wait(kv_free + s, par, a.err, 0x605);
-          if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        }
-        const uint32_t kd = smem_u32(ps + SM::K0 + s * SM::KV_BYTES);
-        const uint32_t vd = smem_u32(ps + SM::V0 + s * SM::KV_BYTES);
-        // validate; padding slots (-1) re-read the tile's first saved row and
-        // are masked later
-        int src[kKC / 32], pmax = -1;
-        bool all_valid = true;
-#pragma unroll
-        for (int half = 0; half < kKC / 32; ++half) {
-          const int pt = lane + 32 * half;
-          const int e = j * kKC + pt;
-          int p = pos[half];
-          if (p >= a.N || (e < kt && p < 0)) {
-            report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x602);
-            p = -1;
+          for (int half = 0; half < kKC / 32; ++half) {
+            const int e = (2 * i + pipe) * kKC + lane + 32 * half;
+            pos[half] = e < x.kt ? __ldg(idx_row + e) : -1;
           }
-          s_pos[s * kKC + pt] = p;
-          src[half] = p >= 0 ? p : p_first;
-          all_valid = all_valid && p >= 0;
-          pmax = max(pmax, p);
+        };
+        // this warp's first chunk of the tile: global chunk c + i0 = prod (mod kProd)
+        const int i0 = static_cast<int>((prod + kProd - c % kProd) % kProd);
+        int p_first = 0;
+        int nxt[kKC / 32];
+        if (i0 < np) {
+          p_first = __ldg(idx_row);
+          if (p_first < 0 || p_first >= a.N) p_first = 0;
+          read_pos(i0, nxt);
         }
-        // a chunk of valid keys that all precede the tile's first row needs
-        // no causal mask in any of its rows
-        all_valid = __all_sync(0xffffffffu, all_valid);
-        pmax = __reduce_max_sync(0xffffffffu, pmax);
-        if (lane == 0) s_flag[s] = (all_valid && pmax <= row0) ? 1 : 0;
-        // coalesced copies: a half-warp moves one 256-byte row (16 lanes x 16
-        // bytes), so each instruction fills two rows of K (or V) in full
+        for (int i = i0; i < np; i += kProd) {
+          const uint32_t gi = c + i;
+          const int s = gi % kST, j = 2 * i + pipe;
+          int pos[kKC / 32];
 #pragma unroll
-        for (int rr = 0; rr < kKC / 2; ++rr) {
-          const int prow = __shfl_sync(0xffffffffu, src[(2 * rr) >> 5], (2 * rr + sub) & 31);
-          const uint32_t off = sw[rr & 3] + rr * 256;
-          cp_async16_s(kd + off, kl + static_cast<size_t>(prow) * 128);
-          cp_async16_s(vd + off, vl + static_cast<size_t>(prow) * 128);
+          for (int half = 0; half < kKC / 32; ++half) pos[half] = nxt[half];
+          if (i + kProd < np) read_pos(i + kProd, nxt);
+          const uint32_t par = ((gi / kST) & 1) ^ 1;
+          int ready = lane == 0 ? mbar_test_wait(kv_free + s, par) : 0;
+          if (!__shfl_sync(0xffffffffu, ready, 0)) {
+            release_all(released, issued);
+            released = issued;
+            int okw = 1;
+            if (lane == 0) okw = mbar_wait(kv_free + s, par, a.err, 0x605);
+            if (!__shfl_sync(0xffffffffu, okw, 0)) {
+              ok = false;
+              break;
+            }
+          }
+          const uint32_t kd = smem_u32(ps + SM::K0 + s * SM::KV_BYTES);
+          const uint32_t vd = smem_u32(ps + SM::V0 + s * SM::KV_BYTES);
+          // validate; padding slots (-1) re-read the tile's first saved row
+          // and are masked later
+          int src[kKC / 32], pmax = -1;
+          bool all_valid = true;
+#pragma unroll
+          for (int half = 0; half < kKC / 32; ++half) {
+            const int pt = lane + 32 * half;
+            const int e = j * kKC + pt;
+            int p = pos[half];
+            if (p >= a.N || (e < x.kt && p < 0)) {
+              report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x602);
+              p = -1;
+            }
+            s_pos[s * kKC + pt] = p;
+            src[half] = p >= 0 ? p : p_first;
+            all_valid = all_valid && p >= 0;
+            pmax = max(pmax, p);
+          }
+          // a chunk of valid keys that all precede the tile's first row
+          // needs no causal mask in any of its rows
+          all_valid = __all_sync(0xffffffffu, all_valid);
+          pmax = __reduce_max_sync(0xffffffffu, pmax);
+          if (lane == 0) s_flag[s] = (all_valid && pmax <= x.row0) ? 1 : 0;
+          // coalesced copies: a half-warp moves one 256-byte row (16 lanes x
+          // 16 bytes), so each instruction fills two rows of K (or V) in full
+#pragma unroll
+          for (int rr = 0; rr < kKC / 2; ++rr) {
+            const int prow = __shfl_sync(0xffffffffu, src[(2 * rr) >> 5], (2 * rr + sub) & 31);
+            const uint32_t off = sw[rr & 3] + rr * 256;
+            cp_async16_s(kd + off, kl + static_cast<size_t>(prow) * 128);
+            cp_async16_s(vd + off, vl + static_cast<size_t>(prow) * 128);
+          }
+          cp_async_commit();
+          issued = gi + kProd;
+          if (issued - released >= kDepth * kProd) {   // the oldest own chunk in flight has landed
+            cp_async_wait<kDepth - 1>();
+            fence_proxy_async_smem();
+            mbar_arrive(kv_full + released % kST);
+            released += kProd;
+          }
         }
-        cp_async_commit();
-        issued = i + kProd;
-        if (issued - released >= kDepth * kProd) {   // the oldest own chunk in flight has landed
-          cp_async_wait<kDepth - 1>();
-          fence_proxy_async_smem();
-          mbar_arrive(kv_full + released % kST);
-          released += kProd;
-        }
+        c += np;
       }
       // release what is still in flight (also after an error, so that no copy
       // outlives the kernel)
       release_all(released, issued);
     }
-    if (warp == 10 && lane == 0) mbar_wait(q_full, 0, a.err, 0x603);   // no copies left in flight
   } else if (role == 1) {
     // ------------------------------------------------ MMA issuer (the whole
     // warp runs the loop; one elected lane issues each MMA)
-    {
-      constexpr uint32_t idq = idesc_bf16_f32(128, kKC, 0, 0);
-      constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
-      bool ok = mbar_wait(q_ready, 0, a.err, 0x611);
-      // S = Q K^T of chunk i (A = Q from TMEM) once the softmax has read S(i-1)
-      auto issue_s = [&](int i) {
-        const int s = i % kST;
-        if (!mbar_wait(kv_full + s, (i / kST) & 1, a.err, 0x613)) return false;
-        if (i > 0 && !mbar_wait(s_free, (i - 1) & 1, a.err, 0x614)) return false;
-        tc_fence_after();
+    constexpr uint32_t idq = idesc_bf16_f32(128, kKC, 0, 0);
+    constexpr uint32_t idv = idesc_bf16_f32(128, 128, 0, 1);
+    uint32_t c = 0;   // this pipe's chunks so far, over all tiles
+    // S = Q K^T of global chunk gi (A = Q from TMEM) once the softmax has read
+    // the previous scores
+    auto issue_s = [&](uint32_t gi) {
+      const int s = gi % kST;
+      if (!mbar_wait(kv_full + s, (gi / kST) & 1, a.err, 0x613)) return false;
+      if (gi > 0 && !mbar_wait(s_free, (gi - 1) & 1, a.err, 0x614)) return false;
+      tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_ts(tS, tQ + kk * 8, kmajor_desc(sK0 + s * SM::KV_BYTES, kk, SM::KHALF), idq,
-                    kk > 0 ? 1u : 0u);
-        tc_commit(s_full);
-        return true;
-      };
-      // O += P V with P (A operand) from its own TMEM columns
-      auto issue_pv = [&](int i) {
-        const int s = i % kST;
-        if (!mbar_wait(p_full, i & 1, a.err, 0x612)) return false;
-        tc_fence_after();
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma_ts(tS, tQ + kk * 8, kmajor_desc(sK0 + s * SM::KV_BYTES, kk, SM::KHALF), idq,
+                  kk > 0 ? 1u : 0u);
+      tc_commit(s_full);
+      return true;
+    };
+    // O += P V with P (A operand) from its own TMEM columns; the tile's first
+    // product overwrites O
+    auto issue_pv = [&](uint32_t gi, bool first) {
+      const int s = gi % kST;
+      if (!mbar_wait(p_full, gi & 1, a.err, 0x612)) return false;
+      tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < kKC / 16; ++kk)
-          tc_mma_ts(tO, tP + kk * 8, vmn_desc(sV0 + s * SM::KV_BYTES, kk, SM::KHALF), idv,
-                    (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(pv_done);
-        tc_commit(kv_free + s);
-        return true;
-      };
-      if (ok) tc_fence_after();
-      if (ok && np > 0) ok = issue_s(0);
+      for (int kk = 0; kk < kKC / 16; ++kk)
+        tc_mma_ts(tO, tP + kk * 8, vmn_desc(sV0 + s * SM::KV_BYTES, kk, SM::KHALF), idv,
+                  (!first || kk > 0) ? 1u : 0u);
+      tc_commit(pv_done);
+      tc_commit(kv_free + s);
+      return true;
+    };
+    bool ok = true;
+    int n = 0;
+    for (int tau = fa_tau(0); ok && tau < total; tau = fa_tau(++n)) {
+      const FaTile x = fa_tile<kKC, REUSE>(a, tau);
+      const int np = (x.nkv - pipe + 1) / 2;
+      ok = mbar_wait(q_ready, n & 1, a.err, 0x611);   // this tile's Q is in TMEM
+      if (!ok) break;
+      tc_fence_after();
+      if (np > 0) ok = issue_s(c);
       for (int i = 0; ok && i < np; ++i) {
-        if (i + 1 < np) ok = issue_s(i + 1);
-        if (ok) ok = issue_pv(i);
+        if (i + 1 < np) ok = issue_s(c + i + 1);
+        if (ok) ok = issue_pv(c + i, i == 0);
       }
+      c += np;
     }
   } else {
     // ------------------------------------------------ softmax warpgroups
     const int r = (warp & 3) * 32 + lane;
-    const int row = row0 + r;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    // at the end of a tile each pipe's (then idle) P columns carry its (m, l)
+    // to the other pipe; pipe p merges output dims [64 p, 64 p + 64)
+    const uint32_t tXchOwn = tP, tXchOther = tmem_base + SM::T_PIPE +
+                                             (1 - pipe) * SM::T_PIPE_COLS + SM::T_P;
+    const uint32_t tOa = tmem_base + SM::T_PIPE + SM::T_O;                      // pipe 0's O
+    const uint32_t tOb = tmem_base + SM::T_PIPE + SM::T_PIPE_COLS + SM::T_O;    // pipe 1's O
     bool ok = true;
-    if (pipe == 0) {
-      // the Q tile (128-byte-swizzled halves in shared memory) into TMEM
-      // columns [0, 64) as bf16 pairs, one row per thread
-      ok = mbar_wait(q_full, 0, a.err, 0x620);
+    // the Q tile (128-byte-swizzled halves in shared memory) into TMEM columns
+    // [0, 64) as bf16 pairs, one row per thread
+    auto copy_q = [&](int n) {
+      if (ok) ok = mbar_wait(q_full, n & 1, a.err, 0x620);
       uint32_t qv[64];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
@@ -388,141 +463,164 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(q_ready);
-    } else {
-      // pipe 1 reuses the Q staging area at the end: not before Q is in TMEM
-      ok = mbar_wait(q_ready, 0, a.err, 0x625);
-    }
-    float m_used = kNegInfP, l = 0.f;
-    for (int i = 0; ok && i < np; ++i) {
-      const int s = i % kST, j = 2 * i + pipe;
-      ok = mbar_wait(s_full, i & 1, a.err, 0x621);
-      if (!ok) break;
-      tc_fence_after();
-      float x[kKC];
-#pragma unroll
-      for (int c = 0; c < kKC / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + c * 32 + lane_base, v);
-#pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(v[e]);
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(s_free);   // the score buffer may take S(i+1) now
-      const bool need_mask = REUSE ? (s_flag[s] == 0) : (j * kKC + kKC - 1 > row0);
-      if (need_mask) {
-#pragma unroll
-        for (int c = 0; c < kKC; ++c) {
-          const int kp = REUSE ? s_pos[s * kKC + c] : j * kKC + c;
-          if (!(kp >= 0 && kp <= row)) x[c] = kNegInfP;
-        }
-      }
-      // row maximum: eight chains of three-input maxima
-      float mx[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) mx[c] = fmaxf(x[2 * c], x[2 * c + 1]);
-#pragma unroll
-      for (int c = 8; c < kKC / 2; ++c) mx[c & 7] = fmax3(mx[c & 7], x[2 * c], x[2 * c + 1]);
-      float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-      tmax *= a.scale_log2;
-      float alpha = 1.f;
-      bool resc = false;
-      if (tmax > m_used + kRescaleLog2) {
-        if (i > 0) {
-          alpha = ex2_approx(m_used - tmax);
-          resc = true;
-        }
-        l *= alpha;
-        m_used = tmax;
-      }
-      const float mu = (m_used == kNegInfP) ? 0.f : m_used;
-      // exponents and row sums on packed pairs (one FMA / add per two scores)
-      const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nmu2 = f2_pack(-mu, -mu);
-      uint32_t pk[kKC / 2];
-      uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-      for (int c = 0; c < kKC / 2; ++c) {
-        float y0, y1;
-        f2_unpack(f2_fma(f2_pack(x[2 * c], x[2 * c + 1]), sc2, nmu2), y0, y1);
-        const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-        ls2[c & 3] = f2_add(ls2[c & 3], f2_pack(p0, p1));
-        pk[c] = pack_bf16(p0, p1);
-      }
-      {
-        float s0, s1;
-        f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), s0, s1);
-        l += s0 + s1;
-      }
-      // the P columns and O are free once the previous P V product has landed
-      if (i > 0) {
-        ok = mbar_wait(pv_done, (i - 1) & 1, a.err, 0x622);
+    };
+    if (pipe == 0 && fa_tau(0) < total) copy_q(0);
+    uint32_t c = 0;   // this pipe's chunks so far, over all tiles
+    int n = 0;
+    // Every softmax thread walks every tile (also after an error, skipping the
+    // waits), so the two named barriers per tile always pair up.
+    for (int tau = fa_tau(0); tau < total; tau = fa_tau(++n)) {
+      const FaTile x = fa_tile<kKC, REUSE>(a, tau);
+      const int np = (x.nkv - pipe + 1) / 2;
+      const int row = x.row0 + r;
+      float m_used = kNegInfP, l = 0.f;
+      for (int i = 0; ok && i < np; ++i) {
+        const uint32_t gi = c + i;
+        const int s = gi % kST, j = 2 * i + pipe;
+        ok = mbar_wait(s_full, gi & 1, a.err, 0x621);
         if (!ok) break;
-      }
-      tc_fence_after();
-      if (__any_sync(0xffffffffu, resc)) {
+        tc_fence_after();
+        float xv[kKC];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32 + lane_base, o);
-          tmem_wait_ld();
+        for (int cc = 0; cc < kKC / 32; ++cc) {
+          uint32_t v[32];
+          tmem_ld32(tS + cc * 32 + lane_base, v);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + c * 32 + lane_base, o);
+          for (int e = 0; e < 32; ++e) xv[cc * 32 + e] = __uint_as_float(v[e]);
         }
-      }
-      tmem_store_p<kKC>(tP + lane_base, pk);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(p_full);
-    }
-    // wait for this pipe's last P V, then merge pipe 1 into pipe 0
-    if (ok && np > 0) ok = mbar_wait(pv_done, (np - 1) & 1, a.err, 0x623);
-    // the Q staging area is idle once Q is in TMEM
-    float* xch = reinterpret_cast<float*>(sm + SM::Q);
-    if (pipe == 1) {
-      xch[r] = np > 0 ? m_used : kNegInfP;
-      xch[128 + r] = np > 0 ? l : 0.f;
-    }
-    tc_fence_before();
-    asm volatile("bar.sync 1, 256;" ::: "memory");   // the two softmax warpgroups
-    tc_fence_after();
-    if (pipe == 0) {
-      const float m1 = xch[r], l1 = xch[128 + r];
-      const float m0 = np > 0 ? m_used : kNegInfP;
-      const float M = fmaxf(m0, m1);
-      const float a0 = (m0 == kNegInfP) ? 0.f : ex2_approx(m0 - M);
-      const float a1 = (m1 == kNegInfP) ? 0.f : ex2_approx(m1 - M);
-      const float lt = a0 * l + a1 * l1;
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      const uint32_t tO1 = tmem_base + SM::T_PIPE + SM::T_PIPE_COLS + SM::T_O;
-      __nv_bfloat16* orow =
-          static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(bh) * a.N + row) * kTile;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o0[32], o1[32];
-        tmem_ld32(tO + c * 32 + lane_base, o0);
-        tmem_ld32(tO1 + c * 32 + lane_base, o1);
         tmem_wait_ld();
-        uint32_t ob[16];
+        tc_fence_before();
+        mbar_arrive(s_free);   // the score buffer may take the next S now
+        const bool need_mask = REUSE ? (s_flag[s] == 0) : (j * kKC + kKC - 1 > x.row0);
+        if (need_mask) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          float y0 = a0 * __uint_as_float(o0[2 * e]);
-          float y1 = a0 * __uint_as_float(o0[2 * e + 1]);
-          if (a1 != 0.f) {
-            y0 += a1 * __uint_as_float(o1[2 * e]);
-            y1 += a1 * __uint_as_float(o1[2 * e + 1]);
+          for (int cc = 0; cc < kKC; ++cc) {
+            const int kp = REUSE ? s_pos[s * kKC + cc] : j * kKC + cc;
+            if (!(kp >= 0 && kp <= row)) xv[cc] = kNegInfP;
           }
-          ob[e] = ok ? pack_bf16(y0 * inv, y1 * inv) : 0u;
         }
-        if (row < a.N) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+        // row maximum: eight chains of three-input maxima
+        float mx[8];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(ob[4 * q], ob[4 * q + 1], ob[4 * q + 2], ob[4 * q + 3]);
+        for (int cc = 0; cc < 8; ++cc) mx[cc] = fmaxf(xv[2 * cc], xv[2 * cc + 1]);
+#pragma unroll
+        for (int cc = 8; cc < kKC / 2; ++cc) mx[cc & 7] = fmax3(mx[cc & 7], xv[2 * cc], xv[2 * cc + 1]);
+        float tmax = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        tmax *= a.scale_log2;
+        float alpha = 1.f;
+        bool resc = false;
+        if (tmax > m_used + kRescaleLog2) {
+          if (i > 0) {
+            alpha = ex2_approx(m_used - tmax);
+            resc = true;
+          }
+          l *= alpha;
+          m_used = tmax;
         }
+        const float mu = (m_used == kNegInfP) ? 0.f : m_used;
+        // exponents and row sums on packed pairs (one FMA / add per two scores)
+        const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2), nmu2 = f2_pack(-mu, -mu);
+        uint32_t pk[kKC / 2];
+        uint64_t ls2[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+        for (int cc = 0; cc < kKC / 2; ++cc) {
+          float y0, y1;
+          f2_unpack(f2_fma(f2_pack(xv[2 * cc], xv[2 * cc + 1]), sc2, nmu2), y0, y1);
+          const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+          ls2[cc & 3] = f2_add(ls2[cc & 3], f2_pack(p0, p1));
+          pk[cc] = pack_bf16(p0, p1);
+        }
+        {
+          float s0, s1;
+          f2_unpack(f2_add(f2_add(ls2[0], ls2[1]), f2_add(ls2[2], ls2[3])), s0, s1);
+          l += s0 + s1;
+        }
+        // the P columns and O are free once the previous P V product has landed
+        if (gi > 0) {
+          ok = mbar_wait(pv_done, (gi - 1) & 1, a.err, 0x622);
+          if (!ok) break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t o[32];
+            tmem_ld32(tO + cc * 32 + lane_base, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(tO + cc * 32 + lane_base, o);
+          }
+        }
+        tmem_store_p<kKC>(tP + lane_base, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(p_full);
       }
-      if (LSE && row < a.N)
-        a.lse[static_cast<size_t>(bh) * a.N + row] = lt > 0.f ? M + __log2f(lt) : kNegInfP;
+      // wait for this pipe's last P V of the tile (it also covers every S)
+      if (ok && np > 0) ok = mbar_wait(pv_done, (c + np - 1) & 1, a.err, 0x623);
+      c += np;
+      tc_fence_after();
+      {
+        uint32_t xw[16];
+        xw[0] = __float_as_uint(np > 0 ? m_used : kNegInfP);
+        xw[1] = __float_as_uint(np > 0 ? l : 0.f);
+#pragma unroll
+        for (int e = 2; e < 16; ++e) xw[e] = 0u;
+        tmem_st16(tXchOwn + lane_base, xw);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      asm volatile("bar.sync 1, 256;" ::: "memory");   // both pipes done with the tile
+      tc_fence_after();
+      // the next tile's Q into TMEM first, so its scores overlap this merge
+      if (pipe == 0 && fa_tau(n + 1) < total) copy_q(n + 1);
+      {
+        uint32_t xr[32];
+        tmem_ld32(tXchOther + lane_base, xr);
+        tmem_wait_ld();
+        const float mo = __uint_as_float(xr[0]), lo = __uint_as_float(xr[1]);
+        const float mine_m = np > 0 ? m_used : kNegInfP, mine_l = np > 0 ? l : 0.f;
+        const float m0 = pipe == 0 ? mine_m : mo, l0 = pipe == 0 ? mine_l : lo;
+        const float m1 = pipe == 0 ? mo : mine_m, l1 = pipe == 0 ? lo : mine_l;
+        const float M = fmaxf(m0, m1);
+        const float a0 = (m0 == kNegInfP) ? 0.f : ex2_approx(m0 - M);
+        const float a1 = (m1 == kNegInfP) ? 0.f : ex2_approx(m1 - M);
+        const float lt = a0 * l0 + a1 * l1;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        __nv_bfloat16* orow =
+            static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(x.bh) * a.N + row) * kTile;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int cc = 2 * pipe + h2;   // 32-dim block of the output
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tOa + cc * 32 + lane_base, o0);
+          tmem_ld32(tOb + cc * 32 + lane_base, o1);
+          tmem_wait_ld();
+          uint32_t ob[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float y0 = a0 * __uint_as_float(o0[2 * e]);
+            float y1 = a0 * __uint_as_float(o0[2 * e + 1]);
+            if (a1 != 0.f) {
+              y0 += a1 * __uint_as_float(o1[2 * e]);
+              y1 += a1 * __uint_as_float(o1[2 * e + 1]);
+            }
+            ob[e] = ok ? pack_bf16(y0 * inv, y1 * inv) : 0u;
+          }
+          if (row < a.N) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(ob[4 * q], ob[4 * q + 1], ob[4 * q + 2], ob[4 * q + 3]);
+          }
+        }
+        if (LSE && pipe == 0 && row < a.N)
+          a.lse[static_cast<size_t>(x.bh) * a.N + row] = lt > 0.f ? M + __log2f(lt) : kNegInfP;
+      }
+      tc_fence_before();
+      asm volatile("bar.sync 1, 256;" ::: "memory");   // both O and P columns free again
+      tc_fence_after();
     }
   }
   tc_fence_before();
@@ -1073,6 +1171,20 @@ bool make_maps(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUtensorM
   return true;
 }
 
+// Streaming multiprocessors of the current device (queried once per device).
+int sm_count() {
+  static int cached_dev = -1, cached = 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev != cached_dev) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached = n;
+    cached_dev = dev;
+  }
+  return cached;
+}
+
 template <bool REUSE, bool LSE>
 cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
   using SM = Fa2Smem<REUSE>;
@@ -1082,7 +1194,13 @@ cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SM::SMEM));
   if (e != cudaSuccess) return e;
-  kern<<<a.B * a.Hq * a.nT, fa_threads<REUSE>(), SM::SMEM, st>>>(tq, tk, tv, a);
+  // persistent: one CTA per SM (shared memory and TMEM allow one), each
+  // taking every gridDim-th tile
+  const int tiles = a.B * a.Hq * a.nT;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidValue;
+  const int grid = tiles < sms ? tiles : sms;
+  kern<<<grid, fa_threads<REUSE>(), SM::SMEM, st>>>(tq, tk, tv, a);
   return cudaGetLastError();
 }
 
