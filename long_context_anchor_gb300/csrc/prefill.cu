@@ -18,10 +18,11 @@
 //       partial states (half the output dims each) and write O / l (and, for
 //       anchor layers, the row log-sum-exp). Causal masking is by key
 //       position.
-//   k_prefill_weights        anchor pass 2: S^T = K Q^T per key tile (TMEM lane
-//       = key), p = 2^(s*sigma*log2e - lse2[query]), and each thread sums its
-//       key's column over the tile's rows: w_j = sum_{i in tile, i >= j} p_ij,
-//       written to the packed tile-weight rows that the Top-k reads.
+//   k_prefill_weights        anchor pass 2, persistent like the kernel above:
+//       S^T = K Q^T per key tile (TMEM lane = key), p = 2^(s*sigma*log2e -
+//       lse2[query]), and each thread sums its key's column over the tile's
+//       rows: w_j = sum_{i in tile, i >= j} p_ij, written to the packed
+//       tile-weight rows that the Top-k reads.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -49,13 +50,6 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk, int half 
 }
 __device__ __forceinline__ uint64_t vmn_desc(uint32_t tile, int kk, int half = kHalf) {
   return sw128_desc(tile + kk * 2048, half, 1024);
-}
-
-// Work order: longest tiles (largest t) first.
-__device__ __forceinline__ void fa_tile_coords(const PrefillArgs& a, int& bh, int& t) {
-  const int BH = a.B * a.Hq;
-  bh = blockIdx.x % BH;
-  t = a.nT - 1 - static_cast<int>(blockIdx.x) / BH;
 }
 
 // Persistent tiles: one CTA per SM takes the query tiles tau = blockIdx.x,
@@ -992,20 +986,26 @@ __global__ void __launch_bounds__(kPairThreads, 1)
 
 // ------------------------------------------------------------------------
 // Anchor pass 2: tile weights from S^T = K_j Q_t^T (TMEM lane = key).
-// Warp 0 loads the Q tile once and the key tiles 0..t into a kWtKS-deep ring
-// by TMA; warp 1 issues S^T(j) into TMEM score buffer j % kWtSB; kWtGroups
-// epilogue warpgroups (warps 4-7, 8-11, ...) take the key tiles in turn,
-// each thread owning one key of the tile: it sums 2^(s*sigma*log2e - lse2)
-// over the tile's query rows i >= key, with no cross-lane reduction.
+// Persistent: one CTA per SM takes the (sequence, query head, 128-row) tiles
+// in the same snake order as the attention kernel. Warp 0 loads each tile's
+// Q (two buffers, so the next tile's Q and row LSEs land while the current
+// tile is computed) and streams the key tiles 0..t through a kWtKS-deep TMA
+// ring; warp 1 issues S^T(j) into TMEM score buffer kc % kWtSB (kc counts key
+// tiles over all tiles of the CTA); kWtGroups epilogue warpgroups (warps 4-7,
+// 8-11, ...) take the key tiles in turn (key tile kc goes to group
+// kc % kWtGroups), each thread owning one key of the tile: it sums
+// 2^(s*sigma*log2e - lse2) over the tile's query rows i >= key, with no
+// cross-lane reduction.
 // ------------------------------------------------------------------------
 constexpr int kWtKS = 4;   // key-tile ring stages
 constexpr int kWtSB = 4;   // TMEM score buffers (128 columns each)
 struct WtSmem {
-  static constexpr int Q = 0;
-  static constexpr int K0 = Q + kTileBytes;            // K[kWtKS]
-  static constexpr int LSE = K0 + kWtKS * kTileBytes;  // float [128]
-  static constexpr int BAR = LSE + kTile * 4;          // q_full, k_full[KS], k_free[KS], s_full[SB], s_free[SB]
-  static constexpr int TMEM = BAR + (1 + 2 * kWtKS + 2 * kWtSB) * 8;
+  static constexpr int Q = 0;                          // Q[2]
+  static constexpr int K0 = Q + 2 * kTileBytes;        // K[kWtKS]
+  static constexpr int LSE = K0 + kWtKS * kTileBytes;  // float [2][128], negated
+  // q_full[2], q_free[2], k_full[KS], k_free[KS], s_full[SB], s_free[SB]
+  static constexpr int BAR = LSE + 2 * kTile * 4;
+  static constexpr int TMEM = BAR + (4 + 2 * kWtKS + 2 * kWtSB) * 8;
   static constexpr int BYTES = TMEM + 8;
 };
 constexpr size_t kWtSmemBytes = WtSmem::BYTES + 1024;
@@ -1019,24 +1019,24 @@ __global__ void __launch_bounds__(kWtThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* s_lse = reinterpret_cast<float*>(sm + WtSmem::LSE);
   uint64_t* bar = reinterpret_cast<uint64_t*>(sm + WtSmem::BAR);
-  uint64_t* q_full = bar;
-  uint64_t* k_full = bar + 1;                      // [kWtKS]
+  uint64_t* q_full = bar;                          // [2] Q landed (tx) + LSE written (32 lanes)
+  uint64_t* q_free = bar + 2;                      // [2] the tile's MMAs and epilogues are done
+  uint64_t* k_full = bar + 4;                      // [kWtKS]
   uint64_t* k_free = k_full + kWtKS;               // [kWtKS]
   uint64_t* s_full = k_free + kWtKS;               // [kWtSB]
   uint64_t* s_free = s_full + kWtSB;               // [kWtSB]
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + WtSmem::TMEM);
   const uint32_t sQ = smem_u32(sm + WtSmem::Q), sK0 = smem_u32(sm + WtSmem::K0);
-
-  int bh, t;
-  fa_tile_coords(a, bh, t);
-  const int b = bh / a.Hq, h = bh % a.Hq, g = a.head_kv[h];
-  const int row0 = t * kTile;
-  const int L = min(a.N, row0 + kTile);
-  const int nkv = (L + kTile - 1) / kTile;
+  const int total = a.B * a.Hq * a.nT;
+  const int BH = a.B * a.Hq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t per_bh = static_cast<size_t>(64) * (a.nT - 1) * a.nT + a.N;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(q_full + q, 33);
+      mbar_init(q_free + q, 1 + 128 * kWtGroups);
+    }
     for (int s = 0; s < kWtKS; ++s) {
       mbar_init(k_full + s, 1);
       mbar_init(k_free + s, 1);
@@ -1047,12 +1047,6 @@ __global__ void __launch_bounds__(kWtThreads, 1)
     }
     fence_barrier_init();
   }
-  if (warp >= 4 && warp < 8) {
-    const int r = threadIdx.x - 128;
-    const int i = row0 + r;
-    // stored negated: the epilogue's FMA adds it
-    s_lse[r] = i < a.N ? -a.lse[static_cast<size_t>(bh) * a.N + i] : -CUDART_INF_F;
-  }
   if (warp == 2) tmem_alloc(s_tmem, 512);
   tc_fence_before();
   __syncthreads();
@@ -1060,96 +1054,172 @@ __global__ void __launch_bounds__(kWtThreads, 1)
   const uint32_t tmem = *s_tmem;
 
   if (warp == 0) {
+    // ------------------------------------------------ loads (whole warp)
     if (lane == 0) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
-      const int kv_row_base = (b * a.Hkv + g) * a.N;
-      mbar_arrive_expect_tx(q_full, kTileBytes);
-      tma_load_2d(sm + WtSmem::Q, &tmQ, q_full, 0, bh * a.N + row0);
-      tma_load_2d(sm + WtSmem::Q + kHalf, &tmQ, q_full, 64, bh * a.N + row0);
-      int issued = 0;
-      for (int j = 0; j < nkv; ++j) {
-        const int s = j % kWtKS;
-        if (!mbar_wait(k_free + s, ((j / kWtKS) & 1) ^ 1, a.err, 0x701)) break;
-        unsigned char* kd = sm + WtSmem::K0 + s * kTileBytes;
-        mbar_arrive_expect_tx(k_full + s, kTileBytes);
-        tma_load_2d(kd, &tmK, k_full + s, 0, kv_row_base + j * kTile);
-        tma_load_2d(kd + kHalf, &tmK, k_full + s, 64, kv_row_base + j * kTile);
-        issued = j + 1;
+    }
+    uint32_t kc = 0;   // key tiles issued over all tiles of this CTA
+    int n = 0, nq = 0;
+    bool ok = true;
+    for (int tau = fa_tau(0); ok && tau < total; tau = fa_tau(++n)) {
+      const int bh = tau % BH, t = a.nT - 1 - tau / BH;
+      const int b = bh / a.Hq, g = a.head_kv[bh % a.Hq];
+      const int row0 = t * kTile;
+      const int L = min(a.N, row0 + kTile);
+      const int nkv = (L + kTile - 1) / kTile;
+      const int buf = n & 1;
+      // buffer buf is free once tile n - 2 is done with it
+      int okw = 1;
+      if (n >= 2 && lane == 0) okw = mbar_wait(q_free + buf, ((n >> 1) - 1) & 1, a.err, 0x704);
+      if (!__shfl_sync(0xffffffffu, okw, 0)) {
+        ok = false;
+        break;
       }
-      mbar_wait(q_full, 0, a.err, 0x702);
-      for (int j = issued > kWtKS ? issued - kWtKS : 0; j < issued; ++j)
-        mbar_wait(k_full + (j % kWtKS), (j / kWtKS) & 1, a.err, 0x703);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full + buf, kTileBytes);
+        tma_load_2d(sm + WtSmem::Q + buf * kTileBytes, &tmQ, q_full + buf, 0, bh * a.N + row0);
+        tma_load_2d(sm + WtSmem::Q + buf * kTileBytes + kHalf, &tmQ, q_full + buf, 64,
+                    bh * a.N + row0);
+      }
+      // the tile's row LSEs, stored negated (the epilogue's FMA adds them)
+#pragma unroll
+      for (int u = 0; u < kTile / 32; ++u) {
+        const int rr = u * 32 + lane, i = row0 + rr;
+        s_lse[buf * kTile + rr] =
+            i < a.N ? -a.lse[static_cast<size_t>(bh) * a.N + i] : -CUDART_INF_F;
+      }
+      mbar_arrive(q_full + buf);
+      nq = n + 1;
+      if (lane == 0) {
+        const int kv_row_base = (b * a.Hkv + g) * a.N;
+        for (int j = 0; j < nkv; ++j) {
+          const uint32_t gk = kc + j;
+          const int s = gk % kWtKS;
+          if (!mbar_wait(k_free + s, ((gk / kWtKS) & 1) ^ 1, a.err, 0x701)) {
+            okw = 0;
+            kc = gk;
+            break;
+          }
+          unsigned char* kd = sm + WtSmem::K0 + s * kTileBytes;
+          mbar_arrive_expect_tx(k_full + s, kTileBytes);
+          tma_load_2d(kd, &tmK, k_full + s, 0, kv_row_base + j * kTile);
+          tma_load_2d(kd + kHalf, &tmK, k_full + s, 64, kv_row_base + j * kTile);
+        }
+        if (okw) kc += nkv;
+      }
+      kc = __shfl_sync(0xffffffffu, kc, 0);
+      if (!__shfl_sync(0xffffffffu, okw, 0)) ok = false;
+    }
+    // never leave with copies in flight
+    if (lane == 0) {
+      for (int m = nq > 2 ? nq - 2 : 0; m < nq; ++m)
+        mbar_wait(q_full + (m & 1), (m >> 1) & 1, a.err, 0x702);
+      for (uint32_t gk = kc > kWtKS ? kc - kWtKS : 0; gk < kc; ++gk)
+        mbar_wait(k_full + (gk % kWtKS), (gk / kWtKS) & 1, a.err, 0x703);
     }
   } else if (warp == 1) {
-    {   // the whole warp runs the loop; one elected lane issues each MMA
-      constexpr uint32_t id = idesc_bf16_f32(128, 128, 0, 0);
-      bool ok = mbar_wait(q_full, 0, a.err, 0x711);
+    // ------------------------------------------------ MMA issuer (the whole
+    // warp runs the loop; one elected lane issues each MMA)
+    constexpr uint32_t id = idesc_bf16_f32(128, 128, 0, 0);
+    uint32_t kc = 0;
+    int n = 0;
+    bool ok = true;
+    for (int tau = fa_tau(0); ok && tau < total; tau = fa_tau(++n)) {
+      const int t = a.nT - 1 - tau / BH;
+      const int nkv = (min(a.N, t * kTile + kTile) + kTile - 1) / kTile;
+      const int buf = n & 1;
+      ok = mbar_wait(q_full + buf, (n >> 1) & 1, a.err, 0x711);
+      const uint32_t sQb = sQ + buf * kTileBytes;
       for (int j = 0; ok && j < nkv; ++j) {
-        const int s = j % kWtKS, sb = j % kWtSB;
-        ok = mbar_wait(k_full + s, (j / kWtKS) & 1, a.err, 0x712) &&
-             mbar_wait(s_free + sb, ((j / kWtSB) & 1) ^ 1, a.err, 0x713);
+        const uint32_t gk = kc + j;
+        const int s = gk % kWtKS, sb = gk % kWtSB;
+        ok = mbar_wait(k_full + s, (gk / kWtKS) & 1, a.err, 0x712) &&
+             mbar_wait(s_free + sb, ((gk / kWtSB) & 1) ^ 1, a.err, 0x713);
         if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma(tmem + sb * 128, kmajor_desc(sK0 + s * kTileBytes, kk), kmajor_desc(sQ, kk), id,
+          tc_mma(tmem + sb * 128, kmajor_desc(sK0 + s * kTileBytes, kk), kmajor_desc(sQb, kk), id,
                  kk > 0 ? 1u : 0u);
         tc_commit(s_full + sb);
         tc_commit(k_free + s);
       }
+      if (ok) tc_commit(q_free + buf);   // this tile's Q buffer, once its MMAs complete
+      kc += nkv;
     }
   } else if (warp >= 4) {
-    const int grp = (warp - 4) >> 2;   // epilogue group: key tiles j = grp, grp + kWtGroups, ...
+    // ------------------------------------------------ epilogue groups
+    const int grp = (warp - 4) >> 2;
     const int r = (warp & 3) * 32 + lane;   // key lane within the key tile
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    float* wrow = a.w + static_cast<size_t>(bh) * (static_cast<size_t>(64) * (a.nT - 1) * a.nT + a.N) +
-                  static_cast<size_t>(64) * t * (t + 1);
-    for (int j = grp; j < nkv; j += kWtGroups) {
-      const int sb = j % kWtSB;
-      if (!mbar_wait(s_full + sb, (j / kWtSB) & 1, a.err, 0x721)) break;
-      tc_fence_after();
-      const int kj = j * kTile + r;
-      const uint32_t ts = tmem + sb * 128 + lane_base;
-      // only the diagonal key tile (j == t) needs the causal mask i >= key;
-      // exponents and sums on packed pairs of query columns, 64 columns at a
-      // time (the score buffer is released after the second load)
-      const bool diag = (j * kTile + kTile - 1 > row0);
-      const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
-      const uint64_t* lse2 = reinterpret_cast<const uint64_t*>(s_lse);
-      uint64_t acc[2] = {0ull, 0ull};
-      auto cols = [&](const uint32_t (&v)[32], int base, uint64_t& sum2) {
+    const uint64_t sc2 = f2_pack(a.scale_log2, a.scale_log2);
+    uint32_t kc = 0;
+    int n = 0;
+    bool ok = true;
+    for (int tau = fa_tau(0); tau < total; tau = fa_tau(++n)) {
+      const int bh = tau % BH, t = a.nT - 1 - tau / BH;
+      const int row0 = t * kTile;
+      const int L = min(a.N, row0 + kTile);
+      const int nkv = (L + kTile - 1) / kTile;
+      const int buf = n & 1;
+      // this group's key tiles of the tile: global key tile kc + j = grp (mod kWtGroups)
+      const int j0 = static_cast<int>((grp + kWtGroups - kc % kWtGroups) % kWtGroups);
+      // every thread waits for the tile's Q and LSEs, even with no key tile of
+      // its own, so its arrival on q_free below belongs to this use of buf
+      if (ok) ok = mbar_wait(q_full + buf, (n >> 1) & 1, a.err, 0x722);
+      float* wrow = a.w + static_cast<size_t>(bh) * per_bh + static_cast<size_t>(64) * t * (t + 1);
+      const uint64_t* lse2 = reinterpret_cast<const uint64_t*>(s_lse + buf * kTile);
+      for (int j = j0; ok && j < nkv; j += kWtGroups) {
+        const uint32_t gk = kc + j;
+        const int sb = gk % kWtSB;
+        if (!mbar_wait(s_full + sb, (gk / kWtSB) & 1, a.err, 0x721)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int kj = j * kTile + r;
+        const uint32_t ts = tmem + sb * 128 + lane_base;
+        // only the diagonal key tile (j == t) needs the causal mask i >= key;
+        // exponents and sums on packed pairs of query columns, 64 columns at
+        // a time (the score buffer is released after the second load)
+        const bool diag = (j * kTile + kTile - 1 > row0);
+        uint64_t acc[2] = {0ull, 0ull};
+        auto cols = [&](const uint32_t (&v)[32], int base, uint64_t& sum2) {
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          // 2^(s*sigma*log2e - lse2) = 2^(fma(s, c, -lse2))
-          float y0, y1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2,
-                           lse2[(base + e) >> 1]),
-                    y0, y1);
-          float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-          if (diag) {
-            p0 = (kj <= row0 + base + e) ? p0 : 0.f;
-            p1 = (kj <= row0 + base + e + 1) ? p1 : 0.f;
+          for (int e = 0; e < 32; e += 2) {
+            // 2^(s*sigma*log2e - lse2) = 2^(fma(s, c, -lse2))
+            float y0, y1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(v[e]), __uint_as_float(v[e + 1])), sc2,
+                             lse2[(base + e) >> 1]),
+                      y0, y1);
+            float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+            if (diag) {
+              p0 = (kj <= row0 + base + e) ? p0 : 0.f;
+              p1 = (kj <= row0 + base + e + 1) ? p1 : 0.f;
+            }
+            sum2 = f2_add(sum2, f2_pack(p0, p1));
           }
-          sum2 = f2_add(sum2, f2_pack(p0, p1));
-        }
-      };
+        };
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t va[32], vb[32];
-        tmem_ld32(ts + hh * 64, va);
-        tmem_ld32(ts + hh * 64 + 32, vb);
-        tmem_wait_ld();
-        if (hh == 1) {
-          tc_fence_before();
-          mbar_arrive(s_free + sb);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t va[32], vb[32];
+          tmem_ld32(ts + hh * 64, va);
+          tmem_ld32(ts + hh * 64 + 32, vb);
+          tmem_wait_ld();
+          if (hh == 1) {
+            tc_fence_before();
+            mbar_arrive(s_free + sb);
+          }
+          cols(va, hh * 64, acc[0]);
+          cols(vb, hh * 64 + 32, acc[1]);
         }
-        cols(va, hh * 64, acc[0]);
-        cols(vb, hh * 64 + 32, acc[1]);
+        float s0, s1;
+        f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
+        if (kj < L) wrow[kj] = s0 + s1;
       }
-      float s0, s1;
-      f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
-      if (kj < L) wrow[kj] = s0 + s1;
+      mbar_arrive(q_free + buf);   // done with this tile's LSEs
+      kc += nkv;
     }
   }
   tc_fence_before();
@@ -1224,7 +1294,10 @@ cudaError_t launch_prefill_anchor_main(const PrefillArgs& a, int head_dim, cudaS
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(kWtSmemBytes));
   if (e != cudaSuccess) return e;
-  k_prefill_weights<<<a.B * a.Hq * a.nT, kWtThreads, kWtSmemBytes, st>>>(tq, tk, a);
+  const int tiles = a.B * a.Hq * a.nT;
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidValue;
+  k_prefill_weights<<<tiles < sms ? tiles : sms, kWtThreads, kWtSmemBytes, st>>>(tq, tk, a);
   return cudaGetLastError();
 }
 
