@@ -96,3 +96,33 @@ def schedule_anchors(M, m: int, rel_tol: float = 1e-12):
                 cur = j
                 break
     return anchors, float(best[m][0])
+
+
+def mass_recall_similarity(probs, sets) -> np.ndarray:
+    """Attention-mass recall between layers (an alternative DP similarity).
+
+    The pages call the DP's quantity the "overlap (similarity) of top-k sets"
+    without a formula (euno.news summary, Methodology 4). This variant asks how
+    much of layer l's exact attention a set saved at layer i would keep:
+
+        M[i][l] = mean over units u of sum_{j in S_i(u)} p_l(u)[j]
+
+    with p_l(u) layer l's softmax weights over all keys for unit u (a
+    (sequence, query head) pair) and S_i(u) the set layer i would hand to it.
+    Entries lie in [0, 1]; M[l][l] is the mass a layer's own Top-k keeps. The
+    DP reads M[i][l] only for i <= l. If p_l were uniform on S_l, M[i][l]
+    would be |S_i ∩ S_l| / k, the overlap similarity.
+
+    probs[l][u]: 1-D weights of layer l, unit u; sets[i][u]: index set.
+    """
+    L = len(probs)
+    U = len(probs[0])
+    M = np.zeros((L, L))
+    for i in range(L):
+        for l in range(L):
+            tot = 0.0
+            for u in range(U):
+                sel = np.asarray(sets[i][u], dtype=np.int64)
+                tot += float(np.asarray(probs[l][u], dtype=np.float64)[sel].sum())
+            M[i, l] = tot / U
+    return M

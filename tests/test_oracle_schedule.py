@@ -99,3 +99,62 @@ def test_overlap_similarity_by_hand():
     np.testing.assert_allclose(M[0, 2], (0 + 1) / 8)
     np.testing.assert_allclose(M[1, 2], (0 + 1) / 8)
     assert (M == M.T).all()
+
+
+# ------------------------------------------------- mass-recall similarity --
+
+from oracle.schedule import mass_recall_similarity  # noqa: E402
+from oracle.topk import topk_indices  # noqa: E402
+
+
+def _softmax_rows(rng, L, U, N, scale=2.0):
+    x = scale * rng.standard_normal((L, U, N))
+    e = np.exp(x - x.max(-1, keepdims=True))
+    return e / e.sum(-1, keepdims=True)
+
+
+def test_mass_recall_diagonal_is_topk_mass_and_bounds():
+    rng = np.random.default_rng(31)
+    L, U, N, k = 4, 5, 60, 7
+    p = _softmax_rows(rng, L, U, N)
+    sets = [[topk_indices(p[l, u], k) for u in range(U)] for l in range(L)]
+    M = mass_recall_similarity(p, sets)
+    for l in range(L):
+        # the k largest weights of each unit, summed and averaged
+        top = np.sort(p[l], axis=-1)[:, ::-1][:, :k].sum(-1).mean()
+        np.testing.assert_allclose(M[l, l], top, atol=1e-14)
+        # no other set of k keys keeps more of layer l's mass
+        assert (M[:, l] <= M[l, l] + 1e-14).all()
+    assert (M >= 0).all() and (M <= 1 + 1e-12).all()
+
+
+def test_mass_recall_full_sets_and_uniform_weights_give_overlap():
+    rng = np.random.default_rng(32)
+    L, U, N, k = 3, 4, 40, 9
+    # k = N keeps all mass
+    p = _softmax_rows(rng, L, U, N)
+    full = [[np.arange(N) for _ in range(U)] for _ in range(L)]
+    np.testing.assert_allclose(mass_recall_similarity(p, full), 1.0, atol=1e-12)
+    # weights uniform on the layer's own set: recall is the overlap fraction
+    sets = [[np.sort(rng.choice(N, k, replace=False)) for _ in range(U)] for _ in range(L)]
+    pu = np.zeros((L, U, N))
+    for l in range(L):
+        for u in range(U):
+            pu[l, u, sets[l][u]] = 1.0 / k
+    np.testing.assert_allclose(mass_recall_similarity(pu, sets), overlap_similarity(sets, k),
+                               atol=1e-12)
+
+
+def test_mass_recall_drives_the_dp():
+    # layers 0-2 attend to one key group, 3-5 to another: the recall matrix
+    # is block-structured and two anchors go to 0 and 3
+    N, U, k = 32, 3, 4
+    p = np.full((6, U, N), 1e-4)
+    for l in range(6):
+        keys = [0, 1, 2, 3] if l < 3 else [16, 17, 18, 19]
+        p[l][:, keys] = 1.0
+    p /= p.sum(-1, keepdims=True)
+    sets = [[topk_indices(p[l, u], k) for u in range(U)] for l in range(6)]
+    M = mass_recall_similarity(p, sets)
+    A, _ = schedule_anchors(M, 2)
+    assert A == [0, 3]
