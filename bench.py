@@ -750,6 +750,17 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
+def schedule_objective(sim, anchors):
+    """sum over layers l of sim[a(l)][l], a(l) the latest anchor at or before l."""
+    A = sorted(anchors)
+    total, cur = 0.0, None
+    for layer in range(len(sim)):
+        while A and A[0] <= layer:
+            cur = A.pop(0)
+        total += sim[cur][layer]
+    return total
+
+
 def run_sweep(args):
     """Schedule sweep: the DP picks the anchors from calibration on synthetic
     sequences, then decode and prefill stacks run with those anchors against
@@ -769,12 +780,25 @@ def run_sweep(args):
     t_cal = time.perf_counter() - t0
     anchors, obj = K.schedule_anchors(sim, configs.SWEEP_N_ANCHORS)
     uniform = list(range(0, wc.n_layers, wc.n_layers // configs.SWEEP_N_ANCHORS))[:configs.SWEEP_N_ANCHORS]
-    from oracle.schedule import objective   # objective of a fixed schedule, for context
+    # the same DP on the attention-mass-recall similarity
+    t0 = time.perf_counter()
+    rsim, _ = K.calibrate(qs, ks, vs, wc.topk, similarity="recall")
+    t_rcal = time.perf_counter() - t0
+    r_anchors, r_obj = K.schedule_anchors(rsim, configs.SWEEP_N_ANCHORS)
+    L = wc.n_layers
     res["calibration"] = {"workload": wc.name, "seconds": round(t_cal, 3), "anchors": anchors,
                           "objective": round(obj, 4),
                           "uniform_anchors": uniform,
-                          "uniform_objective": round(objective(np.asarray(sim), uniform), 4),
-                          "sim_adjacent_mean": round(float(np.mean([sim[i][i + 1] for i in range(wc.n_layers - 1)])), 4)}
+                          "uniform_objective": round(schedule_objective(sim, uniform), 4),
+                          "sim_adjacent_mean": round(float(np.mean([sim[i][i + 1] for i in range(L - 1)])), 4)}
+    # mean share of each layer's exact attention mass kept by the set it
+    # reuses, under each schedule (the recall objective / L)
+    res["calibration_recall"] = {
+        "seconds": round(t_rcal, 3), "anchors": r_anchors, "objective": round(r_obj, 4),
+        "mass_kept_recall_anchors": round(r_obj / L, 4),
+        "mass_kept_overlap_anchors": round(schedule_objective(rsim, anchors) / L, 4),
+        "mass_kept_uniform_anchors": round(schedule_objective(rsim, uniform) / L, 4),
+        "mass_kept_own_topk_mean": round(float(np.mean([rsim[l][l] for l in range(L)])), 4)}
     del qs, ks, vs
     torch.cuda.empty_cache()
 

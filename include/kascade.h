@@ -237,6 +237,25 @@ kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
                                  int32_t* sets_buf, double* sim_out, void* ws, size_t ws_bytes,
                                  void* stream);
 
+/* Calibration with the attention-mass-recall similarity, an alternative to
+ * the set overlap of kascade_calibrate (the pages give the DP's similarity no
+ * formula; euno.news summary, Methodology 4). Every layer runs as an anchor
+ * exactly as there (sets_buf and out as there) and
+ *   sim_out[i*n_layers + l] = mean over (sequence, query head) of
+ *                             sum_{j in S_i} softmax_j(layer l's logits),
+ * for i <= l: the share of layer l's exact attention mass that the set layer
+ * i holds for that head (its own set, or its KV head's in pooled index mode)
+ * would keep. Entries with i > l are 0; the anchor DP reads only i <= l.
+ * sim_out: host float64 [n_layers^2]. Synchronises `stream` before
+ * returning. ws must hold kascade_calibrate_recall_workspace_size bytes. */
+size_t kascade_calibrate_recall_workspace_size(const kascade_desc* desc, int32_t topk,
+                                               int32_t n_layers);
+kascade_status kascade_calibrate_recall(const kascade_desc* desc, int32_t n_layers,
+                                        const void* const* q, const void* const* k,
+                                        const void* const* v, int32_t topk, void* const* out,
+                                        int32_t* sets_buf, double* sim_out, void* ws,
+                                        size_t ws_bytes, void* stream);
+
 /* Host DP: choose n_anchors layers (always including 0) maximising
  * F(A) = sum_l sim[a(l) * n_layers + l], a(l) = most recent anchor <= l.
  * sim: host [n_layers * n_layers], row i = anchor layer. Ties go to the

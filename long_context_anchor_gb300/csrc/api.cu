@@ -645,3 +645,78 @@ kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
 }
 
 }  // extern "C"
+
+// -------------------------------------------------- recall calibration --
+namespace {
+// Workspace of kascade_calibrate_recall: the decode layout, then the row
+// statistics of the current layer, the per-row recall partials and the
+// float64 similarity matrix.
+struct RecallLayout {
+  size_t stat, part, sim, total;
+};
+RecallLayout recall_layout(const Shape& s, int topk, int n_layers) {
+  RecallLayout R{};
+  const size_t rows = static_cast<size_t>(s.B) * s.Hq;
+  size_t off = align256(layout(s, topk, KASCADE_DECODE).total);
+  R.stat = off;
+  off = align256(off + rows * 8);
+  R.part = off;
+  off = align256(off + static_cast<size_t>(n_layers) * n_layers * rows * 4);
+  R.sim = off;
+  off = align256(off + static_cast<size_t>(n_layers) * n_layers * 8);
+  R.total = off;
+  return R;
+}
+}  // namespace
+
+extern "C" {
+
+size_t kascade_calibrate_recall_workspace_size(const kascade_desc* desc, int32_t topk,
+                                               int32_t n_layers) {
+  Shape s;
+  if (check_desc(desc, s) != KASCADE_OK || topk < 1 || n_layers < 1) return 0;
+  return recall_layout(s, topk, n_layers).total;
+}
+
+kascade_status kascade_calibrate_recall(const kascade_desc* desc, int32_t n_layers,
+                                        const void* const* q, const void* const* k,
+                                        const void* const* v, int32_t topk, void* const* out,
+                                        int32_t* sets_buf, double* sim_out, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  Shape s;
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if (n_layers < 1 || q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
+      sim_out == nullptr || !aligned16(sets_buf) || topk < 1 || topk > s.N)
+    return KASCADE_ERR_INVALID_ARG;
+  const RecallLayout R = recall_layout(s, topk, n_layers);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < R.total)
+    return KASCADE_ERR_WORKSPACE;
+  Layout L = layout(s, topk, KASCADE_DECODE);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t per_layer = static_cast<size_t>(s.B) * s.H_idx * topk;
+  const int rows = s.B * s.Hq;
+  float* spill = at<float>(ws, L.spill);   // every anchor call leaves its logits here
+  float2* stat = at<float2>(ws, R.stat);
+  float* part = at<float>(ws, R.part);
+  unsigned int* err = at<unsigned int>(ws, 0);
+  for (int l = 0; l < n_layers; ++l) {
+    if ((r = check_decode_ptrs(q[l], k[l], v[l], out[l])) != KASCADE_OK) return r;
+    r = run_anchor_decode(s, q[l], k[l], v[l], topk, out[l], sets_buf + l * per_layer, nullptr,
+                          ws, L, st);
+    if (r != KASCADE_OK) return r;
+    if (launch_row_stat(spill, rows, s.N, stat, st) != cudaSuccess) return KASCADE_ERR_CUDA;
+    if (launch_mass_recall(spill, stat, sets_buf, per_layer, topk, s.B, s.Hq, s.Hkv, s.N,
+                           s.pooled, s.head_kv, l, n_layers, part, err, st) != cudaSuccess)
+      return KASCADE_ERR_CUDA;
+  }
+  double* sim_dev = at<double>(ws, R.sim);
+  if (launch_recall_reduce(part, n_layers, rows, sim_dev, st) != cudaSuccess)
+    return KASCADE_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(sim_out, sim_dev, static_cast<size_t>(n_layers) * n_layers * 8,
+                                  cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return e == cudaSuccess ? KASCADE_OK : KASCADE_ERR_CUDA;
+}
+
+}  // extern "C"

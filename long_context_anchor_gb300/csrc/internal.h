@@ -93,10 +93,23 @@ cudaError_t launch_prefill_reuse(const PrefillArgs& a, int head_dim, cudaStream_
 cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w,
                                const int16_t* heads, int B, int Hq, int Hkv, int G, int N,
                                cudaStream_t st);
+// Row statistics alone: row_stat[r] = (max_j s_rj, 1 / sum_j exp(s_rj - max)).
+cudaError_t launch_row_stat(const float* s, int rows, int n, float2* row_stat, cudaStream_t st);
 // Prefill: packed tile-weight rows [B*Hq][per_bh] -> [B*Hkv][per_bh], each
 // the sum of its group's rows.
 cudaError_t launch_pool_prefill(const float* w, float* w_pool, const int16_t* heads, int B,
                                 int Hq, int Hkv, int G, size_t per_bh, cudaStream_t st);
+
+// recall.cu — attention-mass recall for the anchor DP: part[(l*L + i)*rows + r]
+// = mass of layer l's softmax row r (logits in `spill`, statistics in
+// row_stat) on the set of layer i for that row, i <= l; then the means over
+// rows in float64, sim[i*L + l] (0 for i > l).
+cudaError_t launch_mass_recall(const float* spill, const float2* row_stat, const int32_t* sets,
+                               size_t per_layer, int topk, int B, int Hq, int Hkv, int N,
+                               int pooled, const int16_t* head_kv, int layer, int n_layers,
+                               float* part, unsigned int* err, cudaStream_t st);
+cudaError_t launch_recall_reduce(const float* part, int n_layers, int rows, double* sim,
+                                 cudaStream_t st);
 
 // overlap.cu
 cudaError_t launch_layer_overlap(const int32_t* sets, int L, int units, int topk, int n_bits,

@@ -165,6 +165,12 @@ cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w,
   return cudaGetLastError();
 }
 
+cudaError_t launch_row_stat(const float* s, int rows, int n, float2* row_stat, cudaStream_t st) {
+  if (rows < 1 || n < 1) return cudaErrorInvalidValue;
+  k_row_stat<<<rows, kStatThreads, 0, st>>>(s, n, row_stat);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pool_prefill(const float* w, float* w_pool, const int16_t* heads, int B,
                                 int Hq, int Hkv, int G, size_t per_bh, cudaStream_t st) {
   if (B < 1 || Hq < 1 || Hkv < 1 || G < 1 || Hq != Hkv * G || Hq > kMaxQHeads || per_bh == 0)

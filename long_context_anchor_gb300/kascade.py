@@ -63,6 +63,10 @@ _SIGS = {
     "kascade_calibrate": (ctypes.c_int, [_DP, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                          ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), _vp,
                                          ctypes.POINTER(ctypes.c_double), _vp, _sz, _vp]),
+    "kascade_calibrate_recall_workspace_size": (_sz, [_DP, _i32, _i32]),
+    "kascade_calibrate_recall": (ctypes.c_int, [_DP, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                                ctypes.POINTER(_vp), _i32, ctypes.POINTER(_vp), _vp,
+                                                ctypes.POINTER(ctypes.c_double), _vp, _sz, _vp]),
     "kascade_layer_overlap": (ctypes.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "kascade_schedule_anchors": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double), _i32, _i32,
                                                 ctypes.POINTER(_i32), ctypes.POINTER(ctypes.c_double)]),
@@ -355,9 +359,14 @@ def schedule_anchors(sim, n_anchors: int):
     return list(out), obj.value
 
 
-def calibrate(qs, ks, vs, topk, group_map=None, scale=None, ws=None, stream=None, pooled=False):
+def calibrate(qs, ks, vs, topk, group_map=None, scale=None, ws=None, stream=None, pooled=False,
+              similarity="overlap"):
     """Every layer as an anchor; returns (sim [L][L] list of lists, sets [L, B*H, topk]),
-    H = Hq, or Hkv when pooled."""
+    H = Hq, or Hkv when pooled. similarity: "overlap" (Top-k set overlap) or
+    "recall" (attention mass of layer l kept by layer i's set; 0 for i > l)."""
+    if similarity not in ("overlap", "recall"):
+        raise ValueError("similarity must be 'overlap' or 'recall'")
+    recall = similarity == "recall"
     L = len(qs)
     _contig(*qs, *ks, *vs)
     desc = decode_desc(qs[0], ks[0], group_map, scale, pooled)
@@ -366,13 +375,16 @@ def calibrate(qs, ks, vs, topk, group_map=None, scale=None, ws=None, stream=None
     dev = qs[0].device
     outs = [torch.empty_like(q) for q in qs]
     sets = torch.empty(L, B * H, topk, dtype=torch.int32, device=dev)
-    nbytes = _lib.kascade_calibrate_workspace_size(ctypes.byref(desc), int(topk), L)
+    size_fn = (_lib.kascade_calibrate_recall_workspace_size if recall
+               else _lib.kascade_calibrate_workspace_size)
+    nbytes = size_fn(ctypes.byref(desc), int(topk), L)
     if nbytes == 0:
-        raise KascadeError(INVALID_ARG, "kascade_calibrate_workspace_size")
+        raise KascadeError(INVALID_ARG, "calibration workspace size")
     ws, buf = _ws(ws, dev, nbytes, stream)
     arr = lambda ts: (ctypes.c_void_p * L)(*[t.data_ptr() for t in ts])
     sim = (ctypes.c_double * (L * L))()
-    _check(_lib.kascade_calibrate(ctypes.byref(desc), L, arr(qs), arr(ks), arr(vs), int(topk),
-                                  arr(outs), _ptr(sets), sim, _ptr(buf), buf.numel(),
-                                  _stream(stream)), "kascade_calibrate")
+    fn = _lib.kascade_calibrate_recall if recall else _lib.kascade_calibrate
+    _check(fn(ctypes.byref(desc), L, arr(qs), arr(ks), arr(vs), int(topk), arr(outs), _ptr(sets),
+              sim, _ptr(buf), buf.numel(), _stream(stream)),
+           "kascade_calibrate_recall" if recall else "kascade_calibrate")
     return [[sim[i * L + j] for j in range(L)] for i in range(L)], sets

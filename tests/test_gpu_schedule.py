@@ -61,3 +61,46 @@ def test_calibration_and_dp(K):
         assert a == ao and abs(f - fo) < 1e-9
     # cross-layer correlation makes neighbours overlap more than distant layers
     assert sim[0, 1] > sim[0, 5]
+
+
+@pytest.mark.parametrize("pooled", [False, True])
+def test_recall_calibration_matches_oracle(K, pooled):
+    from oracle.schedule import mass_recall_similarity, objective
+    w = configs.SWEEP_CALIBRATION.with_(n_layers=6, batch=2, kv_len=2048, topk=256)
+    qs, ks, vs = make_layers(w, device=DEV)
+    sim, sets = K.calibrate(qs, ks, vs, w.topk, pooled=pooled, similarity="recall")
+    sim = np.array(sim)
+    L, B, Hq, Hkv = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads
+    gm = A.default_group_map(Hq, Hkv)
+    # the sets are the anchor entry point's
+    for layer in (0, L - 1):
+        _, idx = K.anchor_decode(qs[layer], ks[layer], vs[layer], w.topk, pooled=pooled)
+        assert np.array_equal(idx.reshape(-1, w.topk).cpu().numpy(), sets[layer].cpu().numpy())
+    # the oracle, on its own float64 softmax and its own Top-k sets
+    f64 = lambda t: t.float().cpu().numpy().astype(np.float64)
+    probs, own = [], []
+    for layer in range(L):
+        q, k, v = f64(qs[layer]), f64(ks[layer]), f64(vs[layer])
+        if pooled:
+            _, idx, _ = A.anchor_decode_pooled(q, k, v, w.topk)
+            idx = A.expand_pooled_sets(idx, gm)          # per query head
+        else:
+            _, idx, _ = A.anchor_decode(q, k, v, w.topk)
+        _, s = A.dense_decode(q, k, v)
+        probs.append(A.softmax(s).reshape(B * Hq, -1))
+        own.append(idx.reshape(B * Hq, w.topk))
+    ref = mass_recall_similarity(probs, own)
+    for i in range(L):
+        for layer in range(L):
+            if i <= layer:
+                # near-tie set differences move the mass by the tiny gap
+                assert abs(sim[i, layer] - ref[i, layer]) < 2e-3, (i, layer)
+            else:
+                assert sim[i, layer] == 0.0
+    # the recall falls with layer distance; the C DP is near-optimal under
+    # the oracle's matrix
+    assert sim[0, 1] > sim[0, 5]
+    for m in (2, 3):
+        a, _ = K.schedule_anchors(sim.tolist(), m)
+        ao, fo = oracle_dp(ref, m)
+        assert objective(ref, a) >= fo - 1e-2
