@@ -110,6 +110,13 @@ kascade_status kascade_workspace_init(void* ws, size_t ws_bytes, void* stream);
  * KASCADE_OK, KASCADE_ERR_BAD_INPUT or KASCADE_ERR_TIMEOUT. */
 kascade_status kascade_device_error(void* ws, void* stream);
 
+/* Failure path of the bounded device waits, for tests: launches one wait on
+ * an mbarrier that nothing completes. After the library's wait limit (about
+ * two seconds) the device records KASCADE_ERR_TIMEOUT in the workspace's
+ * error word (read it with kascade_device_error) and the kernel returns; the
+ * context stays usable. Uses only the workspace header (>= 256 bytes). */
+kascade_status kascade_check_wait_timeout(void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------- decode -- */
 
 /* Exact attention for one query per sequence over all N cached keys (the

@@ -82,12 +82,25 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wall-clock bound of one wait (a try_wait may suspend the thread for a
+// while, so the spin count alone does not bound the time).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
 // Bounded wait: returns false (and records KASCADE_ERR_TIMEOUT) if the phase
-// never completes.
+// does not complete within kWaitLimitNs (or kSpinLimit tries).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* err,
                                           unsigned int where) {
-  for (unsigned int i = 0; i < kSpinLimit; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (unsigned int i = 0; i < kSpinLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && global_ns() - t0 > kWaitLimitNs) break;
+  }
   report_error(err, KASCADE_ERR_TIMEOUT, where);
   return false;
 }

@@ -43,6 +43,7 @@ _SIGS = {
     "kascade_workspace_size": (_sz, [_DP, _i32, _i32]),
     "kascade_workspace_init": (ctypes.c_int, [_vp, _sz, _vp]),
     "kascade_device_error": (ctypes.c_int, [_vp, _vp]),
+    "kascade_check_wait_timeout": (ctypes.c_int, [_vp, _sz, _vp]),
     "kascade_dense_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kascade_anchor_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kascade_reuse_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
@@ -155,6 +156,13 @@ class Workspace:
             _check(_lib.kascade_workspace_init(_ptr(self.buf), self.buf.numel(), _stream(stream)),
                    "kascade_workspace_init")
         return self.buf
+
+    def check_wait_timeout(self, stream=None) -> int:
+        """Run one device wait that can only time out; returns the device error status."""
+        buf = self.get(256, stream)
+        _check(_lib.kascade_check_wait_timeout(_ptr(buf), buf.numel(), _stream(stream)),
+               "kascade_check_wait_timeout")
+        return self.device_error(stream)
 
     def device_error(self, stream=None) -> int:
         """Synchronise and read/clear the device error word (an int status)."""

@@ -247,3 +247,18 @@ def test_workspace_shared_across_shapes_and_entry_points(K):
             check_out(out_r, A.sparse_decode(f64(q), f64(k), f64(v), idx.cpu().numpy()))
             K.layer_overlap(sets, 4096, ws=ws)
     assert ws.device_error() == K.OK
+
+
+def test_bounded_wait_times_out_and_context_survives(K):
+    """A device wait on a barrier nothing completes gives up after the wait
+    limit, reports KASCADE_ERR_TIMEOUT, and the next launches run normally."""
+    import time
+    ws = K.Workspace(DEV)
+    t0 = time.perf_counter()
+    assert ws.check_wait_timeout() == K.TIMEOUT
+    assert time.perf_counter() - t0 < 30.0
+    assert ws.device_error() == K.OK          # the word was read and cleared
+    q, k, v = _rand_layer(1, 4, 2, 256, 64, torch.bfloat16, seed=3)
+    out = K.dense_decode(q, k, v, ws=ws)
+    check_out(out, A.dense_decode(f64(q), f64(k), f64(v))[0])
+    assert ws.device_error() == K.OK
