@@ -8,6 +8,7 @@ import __graft_entry__
 from long_context_anchor_gb300 import configs
 from long_context_anchor_gb300.workloads import make_layers, group_map as default_gmap
 from oracle import attention as A
+from oracle.stack import run_stack as run_oracle_stack
 from oracle.topk import topk_indices
 from gpu_helpers import check_index_set, check_out, f64
 
@@ -20,6 +21,11 @@ def K():
     __graft_entry__.build()
     from long_context_anchor_gb300 import kascade
     return kascade
+
+
+def _dev_idx(idx):
+    """Oracle index sets as the int32 device tensor the library takes."""
+    return torch.from_numpy(np.ascontiguousarray(idx, dtype=np.int32)).to(DEV)
 
 
 def _rand_layer(B, Hq, Hkv, N, d, dtype, seed, scale_k=1.0):
@@ -112,10 +118,15 @@ def test_permuted_group_map(K):
     gm = [1, 0, 3, 2, 0, 1, 2, 3]
     q, k, v = _rand_layer(2, 8, 4, 777, 128, torch.bfloat16, seed=5)
     out, idx, scores = K.anchor_decode(q, k, v, 50, group_map=gm, return_scores=True)
-    o_ref, _, s_ref = A.anchor_decode(f64(q), f64(k), f64(v), 50, gm)
+    o_ref, idx_ref, s_ref = A.anchor_decode(f64(q), f64(k), f64(v), 50, gm)
     check_out(out, o_ref)
-    out_r = K.reuse_decode(q, k, v, idx, group_map=gm)
-    check_out(out_r, A.sparse_decode(f64(q), f64(k), f64(v), idx.cpu().numpy(), gm))
+    got = idx.cpu().numpy()
+    for b in range(2):
+        for h in range(8):
+            check_index_set(got[b, h], s_ref[b, h], 50)
+    # the reuse kernel on the oracle's sets, against the oracle on the same sets
+    out_r = K.reuse_decode(q, k, v, _dev_idx(idx_ref), group_map=gm)
+    check_out(out_r, A.sparse_decode(f64(q), f64(k), f64(v), idx_ref, gm))
 
 
 # ------------------------------------------------------------------- reuse --
@@ -125,10 +136,10 @@ def test_reuse_decode_matches_oracle(K, shape):
     B, Hq, Hkv, N, d, dt = shape
     q, k, v = _rand_layer(B, Hq, Hkv, N, d, dt, seed=7 * N + Hq)
     topk = max(1, N // 8)
-    _, idx = K.anchor_decode(q, k, v, topk)
+    _, idx_ref, _ = A.anchor_decode(f64(q), f64(k), f64(v), topk)   # the oracle's sets
     q2, k2, v2 = _rand_layer(B, Hq, Hkv, N, d, dt, seed=11 * N + Hq)
-    out = K.reuse_decode(q2, k2, v2, idx)
-    o_ref = A.sparse_decode(f64(q2), f64(k2), f64(v2), idx.cpu().numpy())
+    out = K.reuse_decode(q2, k2, v2, _dev_idx(idx_ref))
+    o_ref = A.sparse_decode(f64(q2), f64(k2), f64(v2), idx_ref)
     check_out(out, o_ref, *((1e-4, 1e-5) if dt == torch.float32 else (2e-2, 2e-3)))
 
 
@@ -190,11 +201,21 @@ def test_stack_matches_layer_calls_and_oracle(K, dtype):
     for a, b in zip(outs, [o0, o1, o2, o3, o4]):
         assert torch.equal(a, b)
     assert torch.equal(idx_buf, i3)
-    # against the oracle stack, with reuse layers fed the kernel's own sets
-    f = lambda t: f64(t)
-    check_out(outs[0], A.dense_decode(f(qs[0]), f(ks[0]), f(vs[0]))[0])
-    check_out(outs[2], A.sparse_decode(f(qs[2]), f(ks[2]), f(vs[2]), i1.cpu().numpy()))
-    check_out(outs[4], A.sparse_decode(f(qs[4]), f(ks[4]), f(vs[4]), i3.cpu().numpy()))
+    # against the oracle stack, which selects its own float64 sets
+    ref_outs, _, written = run_oracle_stack("decode", [(f64(a_), f64(b_), f64(c_))
+                                                       for a_, b_, c_ in zip(qs, ks, vs)],
+                                            w.topk, list(w.anchors))
+    # (the two sides pick their sets independently, so near-tie keys may
+    # differ between them; the output tolerance absorbs such a swap)
+    for o, r in zip(outs, ref_outs):
+        check_out(o, r)
+    for layer in (1, 3):
+        s_ref = A.decode_logits(f64(qs[layer]), f64(ks[layer]), A.default_group_map(
+            w.n_q_heads, w.n_kv_heads), A.default_scale(w.head_dim))
+        got = (i1 if layer == 1 else i3).cpu().numpy()
+        for b in range(w.batch):
+            for h in range(w.n_q_heads):
+                check_index_set(got[b, h], s_ref[b, h], w.topk)
 
 
 # -------------------------------------------------------- full-size samples --
@@ -222,7 +243,7 @@ def test_full_size_decode_sampled(K, cfg):
         o_ref = (p / p.sum()) @ V0
         errs0.append(np.abs(f64(outs[0][b, h]) - o_ref).max())
         check_index_set(idx_np[b, h], s, w.topk)
-        sel = idx_np[b, h].astype(np.int64)
+        sel = topk_indices(s, w.topk)   # the oracle's own set for the reuse layer
         K1, V1 = f64(ks[1][b, g])[sel], f64(vs[1][b, g])[sel]
         s1 = scale * (K1 @ f64(qs[1][b, h]))
         p1 = np.exp(s1 - s1.max())
@@ -243,8 +264,13 @@ def test_workspace_shared_across_shapes_and_entry_points(K):
             out = K.dense_decode(q, k, v, ws=ws)
             check_out(out, A.dense_decode(f64(q), f64(k), f64(v))[0])
             _, idx = K.anchor_decode(q, k, v, 64, ws=ws)
-            out_r = K.reuse_decode(q, k, v, idx, ws=ws)
-            check_out(out_r, A.sparse_decode(f64(q), f64(k), f64(v), idx.cpu().numpy()))
+            _, idx_ref, s_ref = A.anchor_decode(f64(q), f64(k), f64(v), 64)
+            got = idx.cpu().numpy()
+            for b_ in range(got.shape[0]):
+                for h_ in range(got.shape[1]):
+                    check_index_set(got[b_, h_], s_ref[b_, h_], 64)
+            out_r = K.reuse_decode(q, k, v, _dev_idx(idx_ref), ws=ws)
+            check_out(out_r, A.sparse_decode(f64(q), f64(k), f64(v), idx_ref))
             K.layer_overlap(sets, 4096, ws=ws)
     assert ws.device_error() == K.OK
 

@@ -15,6 +15,7 @@ import __graft_entry__
 from long_context_anchor_gb300 import configs
 from long_context_anchor_gb300.workloads import make_layers, group_map as default_gmap
 from oracle import attention as A
+from oracle.stack import run_stack as run_oracle_stack
 from oracle.topk import topk_indices
 from gpu_helpers import check_index_set, check_out, f64
 
@@ -38,6 +39,11 @@ def _rand_layer(B, Hq, Hkv, N, d, dtype, seed):
     k = torch.randn(B, Hkv, N, d, generator=g)
     v = torch.randn(B, Hkv, N, d, generator=g)
     return [x.to(dtype).to(DEV) for x in (q, k, v)]
+
+
+def _dev_idx(idx):
+    """Oracle index sets as the int32 device tensor the library takes."""
+    return torch.from_numpy(np.ascontiguousarray(idx, dtype=np.int32)).to(DEV)
 
 
 def _prefill_layer(B, Hq, Hkv, N, seed):
@@ -98,10 +104,10 @@ def test_pooled_reuse_decode_matches_oracle(K, shape):
     B, Hq, Hkv, N, d, dt = shape
     q, k, v = _rand_layer(B, Hq, Hkv, N, d, dt, seed=5 * N + Hq)
     topk = max(1, N // 8)
-    _, idx = K.anchor_decode(q, k, v, topk, pooled=True)
+    _, idx_ref, _ = A.anchor_decode_pooled(f64(q), f64(k), f64(v), topk)   # the oracle's sets
     q2, k2, v2 = _rand_layer(B, Hq, Hkv, N, d, dt, seed=13 * N + Hq)
-    out = K.reuse_decode(q2, k2, v2, idx, pooled=True)
-    o_ref = A.sparse_decode_pooled(f64(q2), f64(k2), f64(v2), idx.cpu().numpy())
+    out = K.reuse_decode(q2, k2, v2, _dev_idx(idx_ref), pooled=True)
+    o_ref = A.sparse_decode_pooled(f64(q2), f64(k2), f64(v2), idx_ref)
     check_out(out, o_ref, *((1e-4, 1e-5) if dt == torch.float32 else (2e-2, 2e-3)))
 
 
@@ -116,8 +122,9 @@ def test_pooled_permuted_group_map(K):
     for b in range(2):
         for g in range(4):
             check_index_set(got[b, g], _log(w_ref[b, g]), 50)
-    out_r = K.reuse_decode(q, k, v, idx, group_map=gm, pooled=True)
-    check_out(out_r, A.sparse_decode_pooled(f64(q), f64(k), f64(v), got, gm))
+    _, idx_ref, _ = A.anchor_decode_pooled(f64(q), f64(k), f64(v), 50, gm)
+    out_r = K.reuse_decode(q, k, v, _dev_idx(idx_ref), group_map=gm, pooled=True)
+    check_out(out_r, A.sparse_decode_pooled(f64(q), f64(k), f64(v), idx_ref, gm))
 
 
 def test_pooled_reuse_poison_outside_group_sets(K):
@@ -156,8 +163,12 @@ def test_pooled_decode_stack_matches_layer_calls(K, dtype):
     for a_, b_ in zip(outs, [o0, o1, o2, o3]):
         assert torch.equal(a_, b_)
     assert idx_buf.shape == (w.batch, w.n_kv_heads, w.topk) and torch.equal(idx_buf, i2)
-    check_out(outs[3], A.sparse_decode_pooled(f64(qs[3]), f64(ks[3]), f64(vs[3]),
-                                              i2.cpu().numpy()))
+    # against the oracle stack, which selects its own float64 pooled sets
+    ref_outs, _, _ = run_oracle_stack("decode", [(f64(a_), f64(b_), f64(c_))
+                                                 for a_, b_, c_ in zip(qs, ks, vs)],
+                                      w.topk, list(w.anchors), pooled=True)
+    for o, r in zip(outs, ref_outs):
+        check_out(o, r)
 
 
 # ----------------------------------------------------------------- prefill --
@@ -189,10 +200,10 @@ def test_pooled_anchor_prefill_matches_oracle(K, shape, topk):
 def test_pooled_reuse_prefill_matches_oracle(K, shape, topk):
     B, Hq, Hkv, N = shape
     q, k, v = _prefill_layer(B, Hq, Hkv, N, seed=7 * N + 1)
-    _, idx = K.anchor_prefill(q, k, v, topk, pooled=True)
+    _, idx_ref = A.anchor_prefill_pooled(f64(q), f64(k), f64(v), topk)   # the oracle's sets
     q2, k2, v2 = _prefill_layer(B, Hq, Hkv, N, seed=9 * N + 1)
-    out = K.reuse_prefill(q2, k2, v2, idx, pooled=True)
-    check_out(out, A.sparse_prefill_pooled(f64(q2), f64(k2), f64(v2), idx.cpu().numpy()))
+    out = K.reuse_prefill(q2, k2, v2, _dev_idx(idx_ref), pooled=True)
+    check_out(out, A.sparse_prefill_pooled(f64(q2), f64(k2), f64(v2), idx_ref))
 
 
 @pytest.mark.parametrize("shape,topk", [((1, 4, 2, 640), 200), ((1, 16, 2, 384), 96),
@@ -202,13 +213,14 @@ def test_pooled_reuse_prefill_equals_per_head_kernel(K, shape, topk):
     # against the per-head kernel given each head its group's set
     B, Hq, Hkv, N = shape
     q, k, v = _prefill_layer(B, Hq, Hkv, N, seed=11 * N + Hq)
-    _, idx = K.anchor_prefill(q, k, v, topk, pooled=True)
+    _, idx_ref = A.anchor_prefill_pooled(f64(q), f64(k), f64(v), topk)   # the oracle's sets
+    idx = _dev_idx(idx_ref)
     out_p = K.reuse_prefill(q, k, v, idx, pooled=True)
     gm = default_gmap(Hq, Hkv)
     idx_h = idx[:, gm].contiguous()
     out_h = K.reuse_prefill(q, k, v, idx_h)
     assert (out_p.float() - out_h.float()).abs().max().item() <= 1.6e-2
-    check_out(out_p, A.sparse_prefill_pooled(f64(q), f64(k), f64(v), idx.cpu().numpy()))
+    check_out(out_p, A.sparse_prefill_pooled(f64(q), f64(k), f64(v), idx_ref))
 
 
 def test_pooled_reuse_prefill_poison_and_empty_rows(K):
@@ -256,8 +268,12 @@ def test_pooled_prefill_stack_matches_layer_calls(K):
     for a_, b_ in zip(outs, [o0, o1, o2]):
         assert torch.equal(a_, b_)
     assert torch.equal(idx_buf, i0)
-    check_out(outs[2], A.sparse_prefill_pooled(f64(qs[2]), f64(ks[2]), f64(vs[2]),
-                                               i0.cpu().numpy()))
+    # against the oracle stack, which selects its own float64 pooled tile sets
+    ref_outs, _, _ = run_oracle_stack("prefill", [(f64(a_), f64(b_), f64(c_))
+                                                  for a_, b_, c_ in zip(qs, ks, vs)],
+                                      w.topk, [0], pooled=True)
+    for o, r in zip(outs, ref_outs):
+        check_out(o, r)
 
 
 # -------------------------------------------------------- full-size samples --
@@ -278,7 +294,7 @@ def test_full_size_pooled_decode_sampled(K):
         for g in (0, 3, w.n_kv_heads - 1):
             check_index_set(idx_np[b, g], _log(wp[g]), w.topk, what="pooled set")
         for h in (0, 13, w.n_q_heads - 1):
-            sel = idx_np[b, gm[h]].astype(np.int64)
+            sel = topk_indices(wp[gm[h]], w.topk)   # the oracle's own set for the reuse layer
             o_ref = A.sparse_decode_pooled(f64(qs[1][b:b + 1, h:h + 1]),
                                            f64(ks[1][b:b + 1, gm[h]:gm[h] + 1]),
                                            f64(vs[1][b:b + 1, gm[h]:gm[h] + 1]),
@@ -306,7 +322,7 @@ def test_full_size_pooled_prefill_sampled(K):
         # reuse rows of one head of the group over the group's set
         h = heads[1]
         r0, r1 = A.tile_rows(t, w.kv_len)
-        sel = idx_np[0, g, t]
+        sel = topk_indices(wt, kt)   # the oracle's own set for the reuse layer
         Q1 = qs[1][:, h:h + 1, :L].float().cpu().numpy()
         K1 = ks[1][:, g:g + 1, :L].float().cpu().numpy()
         V1 = vs[1][:, g:g + 1, :L].float().cpu().numpy()

@@ -10,6 +10,8 @@ import __graft_entry__
 from long_context_anchor_gb300 import configs
 from long_context_anchor_gb300.workloads import make_layers, group_map as default_gmap
 from oracle import attention as A
+from oracle.stack import run_stack as run_oracle_stack
+from oracle.topk import topk_indices
 from gpu_helpers import check_index_set, check_out, f64
 
 pytestmark = pytest.mark.gpu
@@ -21,6 +23,11 @@ def K():
     __graft_entry__.build()
     from long_context_anchor_gb300 import kascade
     return kascade
+
+
+def _dev_idx(idx):
+    """Oracle index sets as the int32 device tensor the library takes."""
+    return torch.from_numpy(np.ascontiguousarray(idx, dtype=np.int32)).to(DEV)
 
 
 def _layer(B, Hq, Hkv, N, d, seed):
@@ -81,10 +88,10 @@ def test_anchor_prefill_matches_oracle(K, shape, topk):
 def test_reuse_prefill_matches_oracle(K, shape, topk):
     B, Hq, Hkv, N = shape
     q, k, v = _layer(B, Hq, Hkv, N, 128, seed=7 * N)
-    _, idx = K.anchor_prefill(q, k, v, topk)
+    _, idx_ref = A.anchor_prefill(f64(q), f64(k), f64(v), topk)   # the oracle's tile sets
     q2, k2, v2 = _layer(B, Hq, Hkv, N, 128, seed=9 * N)
-    out = K.reuse_prefill(q2, k2, v2, idx)
-    check_out(out, A.sparse_prefill(f64(q2), f64(k2), f64(v2), idx.cpu().numpy()))
+    out = K.reuse_prefill(q2, k2, v2, _dev_idx(idx_ref))
+    check_out(out, A.sparse_prefill(f64(q2), f64(k2), f64(v2), idx_ref))
 
 
 def test_reuse_prefill_empty_rows_and_all_keys(K):
@@ -139,7 +146,11 @@ def test_prefill_stack_matches_layer_calls(K):
     for a_, b_ in zip(outs, [o0, o1, o2, o3]):
         assert torch.equal(a_, b_)
     assert torch.equal(idx_buf, i1)
-    check_out(outs[3], A.sparse_prefill(f64(qs[3]), f64(ks[3]), f64(vs[3]), i1.cpu().numpy()))
+    # against the oracle stack, which selects its own float64 tile sets
+    ref_outs, _, _ = run_oracle_stack("prefill", [(f64(a_), f64(b_), f64(c_))
+                                                  for a_, b_, c_ in zip(qs, ks, vs)], w.topk, [1])
+    for o, r in zip(outs, ref_outs):
+        check_out(o, r)
 
 
 def test_full_size_prefill_sampled(K):
@@ -169,7 +180,7 @@ def test_full_size_prefill_sampled(K):
         wts = p.sum(0)
         kt = min(w.topk, L)
         check_index_set(idx_np[0, h, t, :kt], wts, kt, what="tile set")
-        sel = idx_np[0, h, t, :kt].astype(np.int64)
+        sel = topk_indices(wts, kt)   # the oracle's own set for the reuse layer
         Q1 = f64(qs[1][0, h, r0:r1])
         K1, V1 = f64(ks[1][0, g])[sel], f64(vs[1][0, g])[sel]
         s1 = scale * Q1 @ K1.T
