@@ -425,7 +425,9 @@ def run_decode_long(args, dev, world, stream, clocks):
     ws = K.Workspace(dev)
     anchors = list(w.anchors)
 
-    def timed(anch, steps):
+    def timed(anch, steps, per_layer=False):
+        # headline without events between layers (see run_ours); per-layer
+        # breakdown from a separate pass
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(steps)]
         for row in evs:
             for e in row:
@@ -433,14 +435,19 @@ def run_decode_long(args, dev, world, stream, clocks):
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
         for st in range(steps):
-            evs[st][0].record(stream)
+            if per_layer:
+                evs[st][0].record(stream)
             K.run_stack(K.DECODE, qs, ks, vs, w.topk, anch, outs=outs, idx_buf=idx_buf, ws=ws,
-                        layer_events=evs[st][1:])
+                        layer_events=evs[st][1:] if per_layer else None)
+        t1.record(stream)
         torch.cuda.synchronize()
-        per = [[evs[st][l].elapsed_time(evs[st][l + 1]) for l in range(L)] for st in range(steps)]
-        total = sum(evs[st][0].elapsed_time(evs[st][L]) for st in range(steps))
-        return total, per
+        per = ([[evs[st][l].elapsed_time(evs[st][l + 1]) for l in range(L)] for st in range(steps)]
+               if per_layer else None)
+        return t0.elapsed_time(t1), per
 
     for _ in range(args.warmup):
         K.run_stack(K.DECODE, qs, ks, vs, w.topk, anchors, outs=outs, idx_buf=idx_buf, ws=ws)
@@ -448,14 +455,16 @@ def run_decode_long(args, dev, world, stream, clocks):
     torch.cuda.synchronize()
     assert ws.device_error() == K.OK
     clocks.begin()
-    tot_k, per_k = timed(anchors, args.steps)
+    tot_k, _ = timed(anchors, args.steps)
     tot_d, _ = timed([], args.steps)
     clocks.end()
     tot_k, tot_d = max_over_ranks([tot_k, tot_d], world, dev)
+    steps_pl = max(2, args.steps // 2)
+    _, per_k = timed(anchors, steps_pl, per_layer=True)
     ms_k, ms_d = tot_k / args.steps, tot_d / args.steps
     reuse_layers = [l for l in range(L) if l not in anchors]
-    anchor_ms = statistics.mean(per_k[st][l] for st in range(args.steps) for l in anchors)
-    reuse_ms = statistics.mean(per_k[st][l] for st in range(args.steps) for l in reuse_layers)
+    anchor_ms = statistics.mean(per_k[st][l] for st in range(steps_pl) for l in anchors)
+    reuse_ms = statistics.mean(per_k[st][l] for st in range(steps_pl) for l in reuse_layers)
     unions = []
     for a_ in anchors:
         _, ia = K.anchor_decode(qs[a_], ks[a_], vs[a_], w.topk, ws=ws)
@@ -522,7 +531,11 @@ def run_ours(args):
         K.run_stack(K.DECODE, qs, ks, vs, w.topk, anch, outs=outs, idx_buf=idx_buf, ws=ws,
                     layer_events=events)
 
-    def timed(anch, steps, run=stack):
+    def timed(anch, steps, run=stack, per_layer=False):
+        # The headline runs the stack without per-layer events: an event
+        # between two layers' kernels would keep the next layer's kernels from
+        # being scheduled early (programmatic dependent launch). The per-layer
+        # breakdown comes from a separate pass with events.
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(steps)]
         for row in evs:
             for e in row:
@@ -535,15 +548,19 @@ def run_ours(args):
         t1 = torch.cuda.Event(enable_timing=True)
         t0.record(stream)
         for s in range(steps):
-            evs[s][0].record(stream)
-            run(anch, evs[s][1:])
+            if per_layer:
+                evs[s][0].record(stream)
+                run(anch, evs[s][1:])
+            else:
+                run(anch)
         t1.record(stream)
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
         total = t0.elapsed_time(t1)
-        per_layer = [[evs[s][l].elapsed_time(evs[s][l + 1]) for l in range(L)] for s in range(steps)]
-        return total, per_layer
+        per = ([[evs[s][l].elapsed_time(evs[s][l + 1]) for l in range(L)] for s in range(steps)]
+               if per_layer else None)
+        return total, per
 
     for _ in range(args.warmup):
         stack(anchors)
@@ -554,16 +571,19 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     clocks.begin()
-    total_k, pl_k = timed(anchors, args.steps)
-    total_d, pl_d = timed([], args.steps)
+    total_k, _ = timed(anchors, args.steps)
+    total_d, _ = timed([], args.steps)
     clocks.end()
     total_k, total_d = max_over_ranks([total_k, total_d], world, dev)
+    # per-layer breakdown (events between layers)
+    steps_pl = max(2, args.steps // 2)
+    _, pl_k = timed(anchors, steps_pl, per_layer=True)
 
     ms_step = total_k / args.steps
     ms_dense = total_d / args.steps
-    anchor_ms = statistics.mean(pl_k[s][l] for s in range(args.steps) for l in anchors)
+    anchor_ms = statistics.mean(pl_k[s][l] for s in range(steps_pl) for l in anchors)
     reuse_layers = [l for l in range(L) if l not in anchors]
-    reuse_ms = statistics.mean(pl_k[s][l] for s in range(args.steps) for l in reuse_layers)
+    reuse_ms = statistics.mean(pl_k[s][l] for s in range(steps_pl) for l in reuse_layers)
 
     # Byte accounting from each anchor's own sets (outside the timed region).
     unions = []
@@ -669,12 +689,13 @@ def run_ours(args):
         torch.cuda.synchronize()
         assert ws.device_error() == K.OK
         clocks.begin()
-        total_p, pl_p = timed(anchors, args.steps, stack_pooled)
+        total_p, _ = timed(anchors, args.steps, stack_pooled)
         clocks.end()
         total_p = max_over_ranks([total_p], world, dev)[0]
+        _, pl_p = timed(anchors, steps_pl, stack_pooled, per_layer=True)
         ms_p = total_p / args.steps
-        anchor_p = statistics.mean(pl_p[s][l] for s in range(args.steps) for l in anchors)
-        reuse_p = statistics.mean(pl_p[s][l] for s in range(args.steps) for l in reuse_layers)
+        anchor_p = statistics.mean(pl_p[s][l] for s in range(steps_pl) for l in anchors)
+        reuse_p = statistics.mean(pl_p[s][l] for s in range(steps_pl) for l in reuse_layers)
         pa_b, pr_b = pooled_decode_bytes(w)
         pr_gbs = pr_b / (reuse_p * 1e-3) / 1e9
         result["decode_pooled"] = {

@@ -37,6 +37,15 @@ __device__ __forceinline__ void report_error(unsigned int* err, unsigned int cod
   if (prev == 0) atomicExch(err + 1, where);
 }
 
+// Programmatic dependent launch (kernels launched with launch_pdl): wait
+// until the previous kernel in the stream has completed and its writes are
+// visible, then let the next kernel's CTAs be scheduled while this one runs
+// (they wait in their own pdl_wait). Both are no-ops for a plain launch.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

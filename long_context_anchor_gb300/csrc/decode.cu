@@ -264,6 +264,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     k_decode_dense_bf16(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ DecodeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int TK = 16 * NW;
   constexpr int HALVES = D / 64;
   constexpr int TILE_BYTES = HALVES * TK * 128;
@@ -394,6 +396,8 @@ __global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant_
                                                           uint32_t* __restrict__ plan,
                                                           int32_t* __restrict__ plan_count,
                                                           int R) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ uint32_t bm[8][kPlanCap / 32];
   __shared__ int s_lo[8], s_hi[8];
   __shared__ int s_scan[256];
@@ -488,6 +492,8 @@ constexpr int kMaxChunksPerCta = 8;
 template <int D, int NW, int STAGES>
 __global__ void __launch_bounds__(NW * 32)
     k_decode_union_bf16(const __grid_constant__ DecodeArgs a) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int SLICE = (D / 64) * 16 * 128;     // bytes of one K (or V) slice
   constexpr int CHUNKS = D / 8;                   // 16-byte chunks per row
   constexpr int ROWS_PER_INSTR = 32 / CHUNKS;
@@ -610,6 +616,8 @@ __device__ float block_reduce(float v, bool is_max, float* red) {
 }
 
 __global__ void k_decode_generic_f32(const __grid_constant__ DecodeArgs a, int D, int kind) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ float qs[];   // [D]
   __shared__ float red[32];
   const int b = blockIdx.y, hq = blockIdx.x;
@@ -675,8 +683,7 @@ cudaError_t launch_dense_t(const DecodeArgs& a, cudaStream_t st) {
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   dim3 grid(a.S, a.B * a.Hkv);
-  kern<<<grid, (NW + 1) * 32, smem, st>>>(tk, tv, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3((NW + 1) * 32), smem, st, tk, tv, a);
 }
 
 // Plan chunks per reuse CTA: the fewest that fit all CTAs in one wave of
@@ -715,8 +722,7 @@ cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
   u.chunks_per_cta = union_chunks_per_cta(a.S, a.B * a.Hkv, cached_slots);
   u.S = (a.S + u.chunks_per_cta - 1) / u.chunks_per_cta;
   dim3 grid(u.S, a.B * a.Hkv);
-  kern<<<grid, NW * 32, smem, st>>>(u);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(NW * 32), smem, st, u);
 }
 
 }  // namespace
@@ -781,16 +787,16 @@ cudaError_t launch_build_union_plan(const DecodeArgs& a, uint32_t* plan, int32_t
   const int R = decode_union_range(a.B * a.Hkv, a.N);
   const int S = (a.N + R - 1) / R;
   if (S > kMaxSplits) return cudaErrorNotSupported;
-  k_build_union_plan<<<dim3(S, a.B * a.Hkv), 256, 0, st>>>(a, plan, plan_count, R);
-  return cudaGetLastError();
+  return launch_pdl(k_build_union_plan, dim3(S, a.B * a.Hkv), dim3(256), 0, st, a, plan,
+                    plan_count, R);
 }
 
 cudaError_t launch_decode_generic(const DecodeArgs& a, int head_dim, int dtype, DecodeKind kind,
                                   cudaStream_t st) {
   if (dtype != KASCADE_F32) return cudaErrorInvalidValue;
   dim3 grid(a.Hq, a.B);
-  k_decode_generic_f32<<<grid, 256, head_dim * sizeof(float), st>>>(a, head_dim, kind);
-  return cudaGetLastError();
+  return launch_pdl(k_decode_generic_f32, grid, dim3(256), head_dim * sizeof(float), st, a,
+                    head_dim, static_cast<int>(kind));
 }
 
 }  // namespace kascade

@@ -5,7 +5,28 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace kascade {
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while the previous kernel of the stream is still running, and must call
+// pdl_wait() before touching memory that kernel writes or reads.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 constexpr int kMaxQHeads = 256;
 constexpr int kMaxSplits = 128;

@@ -44,6 +44,8 @@ __device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s
 constexpr int kStatThreads = 512, kStatUnroll = 8;
 __global__ void __launch_bounds__(kStatThreads) k_row_stat(const float* __restrict__ s, int n,
                                                            float2* __restrict__ row_stat) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float sm[kStatThreads / 32], ss[kStatThreads / 32];
   const float* row = s + static_cast<size_t>(blockIdx.x) * n;
   float m = kNegInf, sum = 0.f;
@@ -97,6 +99,8 @@ __global__ void __launch_bounds__(256) k_pool_decode(const float* __restrict__ s
                                                      float* __restrict__ w,
                                                      const __grid_constant__ HeadTable ht,
                                                      int Hq, int Hkv, int G, int n) {
+  pdl_wait();
+  pdl_trigger();
   const int u = blockIdx.y, b = u / Hkv, g = u % Hkv;
   const int j0 = blockIdx.x * 1024 + threadIdx.x;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -157,12 +161,11 @@ cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w,
   if (B < 1 || Hq < 1 || Hkv < 1 || G < 1 || N < 1 || Hq != Hkv * G || Hq > kMaxQHeads)
     return cudaErrorInvalidValue;
   const HeadTable ht = make_table(heads, Hq);
-  k_row_stat<<<B * Hq, kStatThreads, 0, st>>>(spill, N, row_stat);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(k_row_stat, dim3(B * Hq), dim3(kStatThreads), 0, st, spill, N,
+                             row_stat);
   if (e != cudaSuccess) return e;
-  k_pool_decode<<<dim3((N + 1023) / 1024, B * Hkv), 256, 0, st>>>(spill, row_stat, w, ht, Hq,
-                                                                  Hkv, G, N);
-  return cudaGetLastError();
+  return launch_pdl(k_pool_decode, dim3((N + 1023) / 1024, B * Hkv), dim3(256), 0, st, spill,
+                    static_cast<const float2*>(row_stat), w, ht, Hq, Hkv, G, N);
 }
 
 cudaError_t launch_row_stat(const float* s, int rows, int n, float2* row_stat, cudaStream_t st) {

@@ -251,6 +251,8 @@ __device__ void sample_bracket(const uint32_t* samp, int n, int r_hi, int r_lo, 
 template <int UNROLL, int MIN_BLOCKS>
 __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_constant__ TopkArgs a,
                                                                int words_cap, int cand_cap) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ uint32_t sm[];
   uint32_t* hist = sm;                                                     // [2][2048]
   const int warp_cap = cand_cap / kWarps;                                  // per-warp list
@@ -504,8 +506,7 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  kern<<<a.rows, kThreads, smem, st>>>(a, words_cap, cand_cap);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(a.rows), dim3(kThreads), smem, st, a, words_cap, cand_cap);
 }
 
 }  // namespace kascade
