@@ -42,8 +42,8 @@ METRIC = "decode attn µs/layer + HBM GB/s at 32K ctx; prefill attn TFLOP/s; vs 
 # ncu capture of the kernel as it stands (profiles/<kernel>_*.md); None when no
 # capture of the current kernel at the bench's size exists.
 TRAFFIC = {
-    "k_decode_union_bf16": 451.503e6,   # profiles/k_decode_union_bf16_llama8b_b8_n32768.md
-    "k_prefill_fa2_reuse": 369.797e6,   # profiles/k_prefill_fa2_reuse_n16384.md
+    "k_decode_union_bf16": 451.458e6,   # profiles/k_decode_union_bf16_llama8b_b8_n32768.md
+    "k_prefill_fa2_reuse": 370.687e6,   # profiles/k_prefill_fa2_reuse_n16384.md
 }
 UNIT = "us/layer"
 
@@ -646,36 +646,77 @@ def run_ours(args):
 
     # End to end through the public API with host buffers: each step copies
     # every layer's new query and the newest K/V row (position N-1) from
-    # pinned host memory, runs the stack and reads all outputs back.
+    # pinned host memory, runs the stack and reads all outputs back. The
+    # copies run on a second stream into two sets of device staging buffers,
+    # so step s+1's inputs travel while step s computes and step s's outputs
+    # travel while step s+1 computes; every step's own copies stay inside the
+    # timed region (the first upload and the last download are not hidden).
     q_host = q_all.cpu().pin_memory()
-    knew_host = k_all[:, :, :, N - 1].cpu().pin_memory()
-    vnew_host = v_all[:, :, :, N - 1].cpu().pin_memory()
-    out_host = torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory()
+    knew_host = k_all[:, :, :, N - 1].contiguous().cpu().pin_memory()
+    vnew_host = v_all[:, :, :, N - 1].contiguous().cpu().pin_memory()
+    out_host = [torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory() for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device=dev)
+    q_stage = [torch.empty_like(q_all) for _ in range(2)]
+    kn_stage = [torch.empty(knew_host.shape, dtype=knew_host.dtype, device=dev) for _ in range(2)]
+    vn_stage = [torch.empty(vnew_host.shape, dtype=vnew_host.dtype, device=dev) for _ in range(2)]
+    out_stage = [torch.empty_like(out_all) for _ in range(2)]
+    up_done = [torch.cuda.Event() for _ in range(2)]
+    step_done = [torch.cuda.Event() for _ in range(2)]
+    down_done = [torch.cuda.Event() for _ in range(2)]
+    slot_used = [False, False]
 
-    def e2e_step():
-        q_all.copy_(q_host, non_blocking=True)
-        k_all[:, :, :, N - 1].copy_(knew_host, non_blocking=True)
-        v_all[:, :, :, N - 1].copy_(vnew_host, non_blocking=True)
-        stack(anchors)
-        out_host.copy_(out_all, non_blocking=True)
+    def upload(slot):
+        with torch.cuda.stream(copy_stream):
+            if slot_used[slot]:
+                copy_stream.wait_event(down_done[slot])   # the slot's previous step is done
+            q_stage[slot].copy_(q_host, non_blocking=True)
+            kn_stage[slot].copy_(knew_host, non_blocking=True)
+            vn_stage[slot].copy_(vnew_host, non_blocking=True)
+            up_done[slot].record(copy_stream)
+        slot_used[slot] = True
 
-    for _ in range(args.warmup):
-        e2e_step()
+    def compute(slot):
+        stream.wait_event(up_done[slot])
+        k_all[:, :, :, N - 1].copy_(kn_stage[slot])
+        v_all[:, :, :, N - 1].copy_(vn_stage[slot])
+        K.run_stack(K.DECODE, list(q_stage[slot]), ks, vs, w.topk, anchors,
+                    outs=list(out_stage[slot]), idx_buf=idx_buf, ws=ws)
+        step_done[slot].record(stream)
+
+    def download(slot):
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(step_done[slot])
+            out_host[slot].copy_(out_stage[slot], non_blocking=True)
+            down_done[slot].record(copy_stream)
+
+    def e2e_run(steps):
+        upload(0)
+        for st in range(steps):
+            if st + 1 < steps:
+                upload((st + 1) % 2)
+            compute(st % 2)
+            download(st % 2)
+        stream.wait_event(down_done[(steps - 1) % 2])
+
+    e2e_run(args.warmup)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    copy_stream.wait_event(e0)
+    e2e_run(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
+    # the outputs that came back are the stack's outputs for these inputs
+    assert torch.equal(out_host[(args.steps - 1) % 2], out_stage[(args.steps - 1) % 2].cpu())
     e2e_ms = e0.elapsed_time(e1) / args.steps
     e2e_ms = max_over_ranks([e2e_ms], world, dev)[0]
     result["e2e"] = {"value": round(1e3 * e2e_ms / L, 3), "unit": UNIT,
                      "h2d_bytes_per_step": int(q_host.numel() * 2 + 2 * knew_host.numel() * 2),
-                     "d2h_bytes_per_step": int(out_host.numel() * 2)}
+                     "d2h_bytes_per_step": int(out_host[0].numel() * 2),
+                     "copies": "second stream, double-buffered staging; D2D scatter of the new K/V rows per step"}
     # GQA-pooled index sets (one per KV head) on the same resident inputs.
     if not args.no_pooled:
         idx_pool = torch.empty(B, Hkv, w.topk, dtype=torch.int32, device=dev)
