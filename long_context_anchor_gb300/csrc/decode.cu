@@ -706,7 +706,8 @@ cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
   // resident CTAs of this kernel (queried once per device)
-  static int cached_dev = -1, cached_slots = 0;
+  // per host thread, so concurrent callers never race on the cache
+  thread_local int cached_dev = -1, cached_slots = 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidValue;
   if (dev != cached_dev) {

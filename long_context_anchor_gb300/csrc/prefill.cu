@@ -1243,7 +1243,7 @@ bool make_maps(const PrefillArgs& a, CUtensorMap* tq, CUtensorMap* tk, CUtensorM
 
 // Streaming multiprocessors of the current device (queried once per device).
 int sm_count() {
-  static int cached_dev = -1, cached = 0;
+  thread_local int cached_dev = -1, cached = 0;   // per host thread: no shared state
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (dev != cached_dev) {
