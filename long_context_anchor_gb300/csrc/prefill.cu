@@ -97,7 +97,7 @@ struct Fa2Smem {
   static constexpr int POS_BYTES = REUSE ? 2 * ST * (KC + 1) * 4 : 0;
   static constexpr int NB = 2 * ST + 4;             // mbarriers per pipeline
   static constexpr int BAR = POS + POS_BYTES;        // [2 pipes][NB] + q_full + q_ready
-  static constexpr int TMEM = BAR + (2 * NB + 2) * 8;
+  static constexpr int TMEM = BAR + (2 * NB + 4) * 8;   // + q_full, q_ready, o_ready[2]
   static constexpr int BYTES = TMEM + 8;
   static constexpr size_t SMEM = BYTES + 1024;       // + slack for 1024-byte alignment
   static_assert(SMEM <= 232448, "the tile and two pipelines must fit in shared memory");
@@ -151,7 +151,8 @@ __device__ __forceinline__ int fa_tau(int n) {
 template <bool REUSE, bool LSE>
 __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     k_prefill_fa2(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ PrefillArgs a) {
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                  const __grid_constant__ PrefillArgs a) {
   using SM = Fa2Smem<REUSE>;
   constexpr int kKC = SM::KC, kST = SM::ST;
   extern __shared__ unsigned char smem_raw[];
@@ -170,7 +171,11 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   int32_t* s_flag = reinterpret_cast<int32_t*>(sm + SM::POS) + 2 * kST * kKC + pipe * kST;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + SM::BAR);
   uint64_t* q_full = bars + 2 * SM::NB;       // the tile's Q landed in shared memory
-  uint64_t* q_ready = q_full + 1;             // ... and was copied into TMEM
+  uint64_t* q_ready = q_full + 1;             // ... and was copied into TMEM (both halves)
+  // o_ready[m & 1]: tile m's output is staged where Q was (two barriers, so a
+  // phase is reused only after the Q loader has waited for it: tile m + 2
+  // needs the Q that is loaded after tile m's output left)
+  uint64_t* o_ready = q_full + 2;
   uint64_t* bar = bars + pipe * SM::NB;
   uint64_t* kv_full = bar;                    // [kST]
   uint64_t* kv_free = bar + kST;              // [kST]
@@ -195,7 +200,9 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     mbar_init(pb + 2 * kST + 3, 1);     // pv_done
     if (threadIdx.x == 0) {
       mbar_init(q_full, 1);
-      mbar_init(q_ready, 128);
+      mbar_init(q_ready, 256);
+      mbar_init(o_ready, 256);
+      mbar_init(o_ready + 1, 256);
     }
     fence_barrier_init();
   }
@@ -209,18 +216,41 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
   const uint32_t tP = tS - SM::T_S + SM::T_P, tO = tS - SM::T_S + SM::T_O;
 
   if (role == 3) {
-    // ------------------------------------------------ Q loader: the tile after
-    // next may be loaded once the current Q has been copied into TMEM
+    // ------------------------------------------------ Q loads and output
+    // stores through the Q staging area: Q(m) is loaded once the output of
+    // tile m - 2 (staged there after Q(m - 1) went to TMEM) has been read out
+    // by its TMA store; ragged tiles (past the sequence end) store their rows
+    // themselves.
     if (lane == 0) {
       prefetch_tmap(&tmQ);
-      int n = 0;
-      for (int tau = fa_tau(0); tau < total; tau = fa_tau(++n)) {
-        if (n > 0 && !mbar_wait(q_ready, (n - 1) & 1, a.err, 0x630)) break;
+      prefetch_tmap(&tmO);
+      auto store_out = [&](int m) {   // output of this CTA's tile m
+        if (!mbar_wait(o_ready + (m & 1), (m >> 1) & 1, a.err, 0x632)) return false;
+        const FaTile x = fa_tile<kKC, REUSE>(a, fa_tau(m));
+        if (x.row0 + kTile <= a.N) {
+          tma_store_2d(&tmO, sm + SM::Q, 0, x.bh * a.N + x.row0);
+          tma_store_2d(&tmO, sm + SM::Q + kHalf, 64, x.bh * a.N + x.row0);
+          bulk_commit_group();
+          bulk_wait_group_read0();   // the staging area may take the next Q
+        }
+        return true;
+      };
+      int n = 0, stored = 0;
+      bool ok = true;
+      for (int tau = fa_tau(0); ok && tau < total; tau = fa_tau(++n)) {
+        if (n == 1) ok = mbar_wait(q_ready, 0, a.err, 0x630);
+        if (n >= 2) {
+          ok = store_out(n - 2);
+          stored = n - 1;
+        }
+        if (!ok) break;
         const FaTile x = fa_tile<kKC, REUSE>(a, tau);
         mbar_arrive_expect_tx(q_full, kTileBytes);
         tma_load_2d(sm + SM::Q, &tmQ, q_full, 0, x.bh * a.N + x.row0);
         tma_load_2d(sm + SM::Q + kHalf, &tmQ, q_full, 64, x.bh * a.N + x.row0);
       }
+      for (int m = stored; ok && fa_tau(m) < total; ++m) ok = store_out(m);
+      bulk_wait_group0();   // every output store has landed
       if (n > 0) mbar_wait(q_full, (n - 1) & 1, a.err, 0x631);   // no copy left in flight
     }
   } else if (role == 2) {
@@ -439,26 +469,26 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
     bool ok = true;
     // the Q tile (128-byte-swizzled halves in shared memory) into TMEM columns
     // [0, 64) as bf16 pairs, one row per thread
+    // pipe p copies dims [64p, 64p + 64) of the Q tile (its 128-byte-swizzled
+    // half in shared memory) into TMEM columns [32p, 32p + 32) as bf16 pairs,
+    // one row per thread; later it stages its half of the output there
     auto copy_q = [&](int n) {
       if (ok) ok = mbar_wait(q_full, n & 1, a.err, 0x620);
-      uint32_t qv[64];
+      uint32_t qv[32];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t addr = sQ + hh * kHalf + r * 128 + ((c ^ (r & 7)) << 4);
-          asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(qv[hh * 32 + c * 4]), "=r"(qv[hh * 32 + c * 4 + 1]),
-                         "=r"(qv[hh * 32 + c * 4 + 2]), "=r"(qv[hh * 32 + c * 4 + 3])
-                       : "r"(addr));
-        }
-      tmem_st32(tQ + lane_base, *reinterpret_cast<uint32_t(*)[32]>(qv));
-      tmem_st32(tQ + 32 + lane_base, *reinterpret_cast<uint32_t(*)[32]>(qv + 32));
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t addr = sQ + pipe * kHalf + r * 128 + ((c ^ (r & 7)) << 4);
+        asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(qv[c * 4]), "=r"(qv[c * 4 + 1]), "=r"(qv[c * 4 + 2]),
+                       "=r"(qv[c * 4 + 3])
+                     : "r"(addr));
+      }
+      tmem_st32(tQ + pipe * 32 + lane_base, qv);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(q_ready);
     };
-    if (pipe == 0 && fa_tau(0) < total) copy_q(0);
+    if (fa_tau(0) < total) copy_q(0);
     uint32_t c = 0;   // this pipe's chunks so far, over all tiles
     int n = 0;
     // Every softmax thread walks every tile (also after an error, skipping the
@@ -568,7 +598,7 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
       asm volatile("bar.sync 1, 256;" ::: "memory");   // both pipes done with the tile
       tc_fence_after();
       // the next tile's Q into TMEM first, so its scores overlap this merge
-      if (pipe == 0 && fa_tau(n + 1) < total) copy_q(n + 1);
+      if (fa_tau(n + 1) < total) copy_q(n + 1);
       {
         uint32_t xr[32];
         tmem_ld32(tXchOther + lane_base, xr);
@@ -584,6 +614,7 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
         __nv_bfloat16* orow =
             static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(x.bh) * a.N + row) * kTile;
+        const bool full = x.row0 + kTile <= a.N;   // whole tile inside the sequence: TMA store
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int cc = 2 * pipe + h2;   // 32-dim block of the output
@@ -602,7 +633,16 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
             }
             ob[e] = ok ? pack_bf16(y0 * inv, y1 * inv) : 0u;
           }
-          if (row < a.N) {
+          if (full) {
+            // into this pipe's (128-byte-swizzled) half of the staging area
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t addr = sQ + pipe * kHalf + r * 128 + (((h2 * 4 + q) ^ (r & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(ob[4 * q]),
+                           "r"(ob[4 * q + 1]), "r"(ob[4 * q + 2]), "r"(ob[4 * q + 3])
+                           : "memory");
+            }
+          } else if (row < a.N) {
             uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
@@ -611,6 +651,8 @@ __global__ void __launch_bounds__(fa_threads<REUSE>(), 1)
         }
         if (LSE && pipe == 0 && row < a.N)
           a.lse[static_cast<size_t>(x.bh) * a.N + row] = lt > 0.f ? M + __log2f(lt) : kNegInfP;
+        fence_proxy_async_smem();   // staged rows visible to the TMA store
+        mbar_arrive(o_ready + (n & 1));
       }
       tc_fence_before();
       asm volatile("bar.sync 1, 256;" ::: "memory");   // both O and P columns free again
@@ -1260,6 +1302,10 @@ cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
   using SM = Fa2Smem<REUSE>;
   alignas(64) CUtensorMap tq, tk, tv;
   if (!make_maps(a, &tq, &tk, &tv, SM::KC)) return cudaErrorInvalidValue;
+  alignas(64) CUtensorMap to;
+  if (!encode_tmap_2d_bf16(&to, a.out, 128, static_cast<uint64_t>(a.B) * a.Hq * a.N, 64, kTile,
+                           true))
+    return cudaErrorInvalidValue;
   auto kern = k_prefill_fa2<REUSE, LSE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(SM::SMEM));
@@ -1270,7 +1316,7 @@ cudaError_t launch_fa(const PrefillArgs& a, cudaStream_t st) {
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidValue;
   const int grid = tiles < sms ? tiles : sms;
-  kern<<<grid, fa_threads<REUSE>(), SM::SMEM, st>>>(tq, tk, tv, a);
+  kern<<<grid, fa_threads<REUSE>(), SM::SMEM, st>>>(tq, tk, tv, to, a);
   return cudaGetLastError();
 }
 
