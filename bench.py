@@ -43,7 +43,7 @@ METRIC = "decode attn µs/layer + HBM GB/s at 32K ctx; prefill attn TFLOP/s; vs 
 # capture of the current kernel at the bench's size exists.
 TRAFFIC = {
     "k_decode_union_bf16": 451.458e6,   # profiles/k_decode_union_bf16_llama8b_b8_n32768.md
-    "k_prefill_fa2_reuse": 370.687e6,   # profiles/k_prefill_fa2_reuse_n16384.md
+    "k_prefill_fa2_reuse": 383.524e6,   # profiles/k_prefill_fa2_reuse_n16384.md
 }
 UNIT = "us/layer"
 
