@@ -728,8 +728,9 @@ cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-// Launch shapes: 4 consumer warps (64-key tiles) per CTA, 2 CTAs per SM;
-// about four waves of CTAs over the 152 SMs.
+// Launch shapes: 4 consumer warps (64-key tiles) per CTA. Dense decode runs
+// 152 * 8 split CTAs (three resident per SM, so about 2.7 waves; 152 * 6 and
+// 152 * 12 were both slower); the union gather sizes its CTAs to one wave.
 constexpr int kDenseNW = 4;
 constexpr int kUnionNW = 4;
 constexpr int kTargetCtas = 152 * 2 * 4;
@@ -765,11 +766,15 @@ int decode_union_chunks(int units, int N) {
 cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spill,
                                      cudaStream_t st) {
   if (head_dim == 128)
-    return spill ? launch_dense_t<128, kDenseNW, 3, true>(a, st)
-                 : launch_dense_t<128, kDenseNW, 3, false>(a, st);
+    // two 32 KB stages: 64 KB, three CTAs per SM (three stages at two per SM
+    // were 2% slower)
+    return spill ? launch_dense_t<128, kDenseNW, 2, true>(a, st)
+                 : launch_dense_t<128, kDenseNW, 2, false>(a, st);
   if (head_dim == 64)
-    return spill ? launch_dense_t<64, kDenseNW, 6, true>(a, st)
-                 : launch_dense_t<64, kDenseNW, 6, false>(a, st);
+    // four 16 KB stages: 64 KB, three CTAs per SM (six stages, two per SM, were
+    // 4% slower on 131072-key rows)
+    return spill ? launch_dense_t<64, kDenseNW, 4, true>(a, st)
+                 : launch_dense_t<64, kDenseNW, 4, false>(a, st);
   return cudaErrorInvalidValue;
 }
 
