@@ -141,7 +141,7 @@ __device__ __forceinline__ void load_q_frags(const DecodeArgs& a, int b, int g,
 // Merge the consumer warps' states through shared memory, write this CTA's
 // partial (or the final output when there is one split), and let the last
 // CTA of the (sequence, KV head) merge all splits. `scratch` must hold
-// (16 + 8*D) * n_consumers + 16 + 8 * S floats.
+// (16 + 8*D) * n_consumers + 16 + 24 * S floats.
 template <int D>
 __device__ void finish_cta(const DecodeArgs& a, WarpState<D>& st, int cw, int n_consumers,
                            float* scratch, int b, int g, int split) {
@@ -225,20 +225,29 @@ __device__ void finish_cta(const DecodeArgs& a, WarpState<D>& st, int cw, int n_
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // Final merge over splits: weights w_s = 2^(m_s - M) / L per head.
-  float* wts = cl + 8;   // [G][S]
+  // Final merge over splits: weights w_s = 2^(m_s - M) / L per head. Every
+  // split's (m, l) is loaded by its own thread first (one round of global
+  // loads instead of a chain of them), then summed in split order.
+  float* wts = cl + 8;           // [G][S]
+  float* pm = wts + G * a.S;     // [G][S] split maxima
+  float* pl = pm + G * a.S;      // [G][S] split sums
+  for (int e = threadIdx.x; e < G * a.S; e += blockDim.x) {
+    const int h = e / a.S, s = e % a.S;
+    const float* pp = a.part + ((static_cast<size_t>(b) * a.Hq + a.heads[g * G + h]) * a.S + s) * (D + 4);
+    pm[e] = __ldcg(pp);
+    pl[e] = __ldcg(pp + 1);
+  }
+  __syncthreads();
   if (threadIdx.x < G) {
     const int h = threadIdx.x;
-    const int hq = a.heads[g * G + h];
-    const float* pp = a.part + (static_cast<size_t>(b) * a.Hq + hq) * a.S * (D + 4);
     float M = kNegInf;
-    for (int s = 0; s < a.S; ++s) M = fmaxf(M, __ldcg(pp + s * (D + 4)));
+    for (int s = 0; s < a.S; ++s) M = fmaxf(M, pm[h * a.S + s]);
     float L = 0.f;
     for (int s = 0; s < a.S; ++s) {
-      const float ms = __ldcg(pp + s * (D + 4));
+      const float ms = pm[h * a.S + s];
       const float w = (ms == kNegInf) ? 0.f : fast_exp2(ms - M);
       wts[h * a.S + s] = w;
-      L += w * __ldcg(pp + s * (D + 4) + 1);
+      L += w * pl[h * a.S + s];
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int s = 0; s < a.S; ++s) wts[h * a.S + s] *= inv;
@@ -249,6 +258,7 @@ __device__ void finish_cta(const DecodeArgs& a, WarpState<D>& st, int cw, int n_
     const int hq = a.heads[g * G + h];
     const float* pp = a.part + (static_cast<size_t>(b) * a.Hq + hq) * a.S * (D + 4);
     float acc = 0.f;
+#pragma unroll 4
     for (int s = 0; s < a.S; ++s) acc += wts[h * a.S + s] * __ldcg(pp + s * (D + 4) + 4 + dd);
     static_cast<__nv_bfloat16*>(a.out)[(static_cast<size_t>(b) * a.Hq + hq) * D + dd] =
         __float2bfloat16_rn(acc);
