@@ -42,7 +42,7 @@ METRIC = "decode attn µs/layer + HBM GB/s at 32K ctx; prefill attn TFLOP/s; vs 
 # ncu capture of the kernel as it stands (profiles/<kernel>_*.md); None when no
 # capture of the current kernel at the bench's size exists.
 TRAFFIC = {
-    "k_decode_union_bf16": 451.458e6,   # profiles/k_decode_union_bf16_llama8b_b8_n32768.md
+    "k_decode_union_bf16": 451.340e6,   # profiles/k_decode_union_bf16_llama8b_b8_n32768.md
     "k_prefill_fa2_reuse": 383.524e6,   # profiles/k_prefill_fa2_reuse_n16384.md
 }
 UNIT = "us/layer"
