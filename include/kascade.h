@@ -94,6 +94,9 @@ typedef struct {
   const int32_t* group_map;
   int32_t index_mode;   /* kascade_index_mode; 0 (zero-initialised) = per query head */
 } kascade_desc;
+/* Size limits (KASCADE_ERR_UNSUPPORTED beyond them): N < 2^24;
+ * B*Hkv*N < 2^31; B*Hkv <= 16384; prefill also B*Hq*N < 2^31. Bf16 reuse
+ * decode also needs N <= 262144 (at most 128 key-range chunks of 2048). */
 
 /* Human-readable name of a status code (static storage). */
 const char* kascade_status_string(kascade_status s);

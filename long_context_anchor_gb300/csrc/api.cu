@@ -472,6 +472,9 @@ kascade_status check_prefill(const kascade_desc* desc, Shape& s, const void* q, 
   kascade_status r = check_desc(desc, s);
   if (r != KASCADE_OK) return r;
   if (s.dtype != KASCADE_BF16) return KASCADE_ERR_UNSUPPORTED;
+  // the prefill kernels address rows of q and out (B*Hq*N of them) with
+  // 32-bit tensor-map coordinates
+  if (static_cast<long long>(s.B) * s.Hq * s.N >= (1ll << 31)) return KASCADE_ERR_UNSUPPORTED;
   return check_decode_ptrs(q, k, v, out);
 }
 

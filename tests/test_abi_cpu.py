@@ -56,6 +56,9 @@ def test_validation_before_launch(K):
     # prefill needs bf16
     f32 = K.make_desc(1, 4, 2, 64, 512, K.F32)
     assert K._lib.kascade_dense_prefill(ctypes.byref(f32), p, p, p, p, p, 1 << 30, None) == K.UNSUPPORTED
+    # prefill rows of q and out are 32-bit tensor-map coordinates: B*Hq*N < 2^31
+    big = K.make_desc(8, 64, 8, 128, 1 << 22, K.BF16)
+    assert K._lib.kascade_dense_prefill(ctypes.byref(big), p, p, p, p, p, 1 << 62, None) == K.UNSUPPORTED
     # stack: anchors must be ascending and in range
     arr = (ctypes.c_void_p * 2)(fake, fake)
     bad_anchors = (ctypes.c_int32 * 2)(1, 0)
