@@ -3,8 +3,9 @@
 // 5). Rule: larger score first, lower index wins a tie, -0 == +0; output
 // ascending positions.
 //
-// One 512-thread CTA per row, two CTAs per SM; scores become order-
-// preserving uint32 keys on the fly.
+// One CTA per row (512 threads, two per SM; 256 threads, four per SM, for
+// the many short rows of the prefill tiles); scores become order-preserving
+// uint32 keys on the fly.
 //   1. bracket: an evenly spaced sample of the row (len/16 keys, 2048..8192)
 //      is staged in shared memory; two histogram passes over it give the
 //      22-bit key prefixes at sample ranks rc -/+ margin (rc the expected
@@ -30,8 +31,6 @@
 namespace kascade {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
 // Candidate (key, position) pairs in shared memory: kCandCap for rows up to
 // kShortRow keys (two CTAs per SM); longer rows take a larger pool (one CTA per
 // SM) so that the per-warp lists do not overflow into the exact fallback.
@@ -40,6 +39,7 @@ constexpr int kShortRow = 32768;
 constexpr int kMaxCandCap = 16384;
 constexpr int kUnroll = 8;       // 32-position chunks in flight per warp
 constexpr int kSampleCap = 8192; // evenly spaced sample used to bracket the k-th key
+constexpr int kManyRows = 1024;  // rows from which short rows take 256-thread CTAs
 
 struct RowDesc {
   const float* ptr;
@@ -64,7 +64,8 @@ __device__ __forceinline__ RowDesc row_desc(const TopkArgs& a, int r) {
   return d;
 }
 
-// Inclusive block scan of one int per thread.
+// Inclusive block scan of one int per thread (NT threads).
+template <int NT>
 __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -75,7 +76,7 @@ __device__ __forceinline__ int block_incl_scan(int v, int* warp_tot) {
   if (lane == 31) warp_tot[warp] = v;
   __syncthreads();
   if (warp == 0) {
-    int t = warp_tot[lane];
+    int t = lane < NT / 32 ? warp_tot[lane] : 0;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const int o = __shfl_up_sync(0xffffffffu, t, off);
@@ -99,10 +100,10 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, bool active, uint32_t b
 
 // Visit the row in warp-owned blocks of 32*kUnroll consecutive positions;
 // f(pos, valid, key) runs on every lane (warp-uniform control flow).
-template <typename F>
+template <int NT, typename F>
 __device__ __forceinline__ void for_row(const RowDesc& rd, bool& bad, F f) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int base = warp * 32 * kUnroll; base < rd.len; base += kWarps * 32 * kUnroll) {
+  for (int base = warp * 32 * kUnroll; base < rd.len; base += (NT / 32) * 32 * kUnroll) {
     float x[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -121,14 +122,15 @@ __device__ __forceinline__ void for_row(const RowDesc& rd, bool& bad, F f) {
 
 // Bin holding rank `need` (1 = largest) of an nb-bin histogram, counting from
 // the top bin down; returns the bin and the count in the bins above it. Each
-// thread owns nb / kThreads consecutive bins (highest first).
+// of the NT threads owns nb / NT consecutive bins (highest first).
+template <int NT>
 __device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, int* warp_tot,
                                          int* s_bin, int* s_above, int& bin, int& above) {
-  const int per = nb / kThreads;
+  const int per = nb / NT;
   const int top = nb - 1 - per * static_cast<int>(threadIdx.x);
   int local = 0;
   for (int q = 0; q < per; ++q) local += static_cast<int>(hist[top - q]);
-  int run = block_incl_scan(local, warp_tot) - local;   // count above this thread's bins
+  int run = block_incl_scan<NT>(local, warp_tot) - local;   // count above this thread's bins
   if (run < need && need <= run + local) {
     for (int q = 0; q < per; ++q) {
       const int h = static_cast<int>(hist[top - q]);
@@ -146,38 +148,13 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need,
   __syncthreads();
 }
 
-// Exact rank selection on a shared-memory key list: the key of rank `rank`
-// (1 = largest) and the number of list keys strictly greater than it.
-__device__ void select_rank(const uint32_t* list, int n, int rank, uint32_t* hist, int* warp_tot,
-                            int* s_bin, int* s_above, uint32_t& key_out, int& greater) {
-  uint32_t prefix = 0, pmask = 0;
-  int gt = 0;
-  for (int d = 0; d < 3; ++d) {
-    const int nb = d < 2 ? 2048 : 1024;
-    const int sh = d == 0 ? 21 : (d == 1 ? 10 : 0);
-    for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0u;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      const uint32_t key = list[i];
-      if ((key & pmask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1u);
-    }
-    __syncthreads();
-    int bin, above;
-    find_bin(hist, nb, rank - gt, warp_tot, s_bin, s_above, bin, above);
-    gt += above;
-    prefix |= static_cast<uint32_t>(bin) << sh;
-    pmask |= static_cast<uint32_t>(nb - 1) << sh;
-  }
-  key_out = prefix;
-  greater = gt;
-}
-
 // Candidate i of the per-warp lists (list w holds count[w] keys at
 // cand + w * warp_cap) in list order; pre[w] = keys in lists before w.
+template <int NT>
 __device__ __forceinline__ int cand_slot(const int* pre, int warp_cap, int i) {
   int w = 0;
 #pragma unroll
-  for (int q = 1; q < kWarps; ++q) w += (i >= pre[q]) ? 1 : 0;
+  for (int q = 1; q < NT / 32; ++q) w += (i >= pre[q]) ? 1 : 0;
   return w * warp_cap + (i - pre[w]);
 }
 
@@ -185,6 +162,7 @@ __device__ __forceinline__ int cand_slot(const int* pre, int warp_cap, int i) {
 // [t_lo, t_lo + span], so the digits are those of key - t_lo, from the top
 // bit of span down in passes of at most 11 bits (one or two passes for a
 // narrow bracket), each histogram built by one flat loop over the candidates.
+template <int NT>
 __device__ void select_rank_warp_lists(const uint32_t* cand, const int* pre, int total,
                                        int warp_cap, uint32_t t_lo, uint32_t span, int rank,
                                        uint32_t* hist, int* warp_tot, int* s_bin, int* s_above,
@@ -196,16 +174,15 @@ __device__ void select_rank_warp_lists(const uint32_t* cand, const int* pre, int
     const int width = top > 11 ? 11 : top;
     const int sh = top - width;
     const int nb = 1 << width;
-    for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0u;
+    for (int i = threadIdx.x; i < 2048; i += NT) hist[i] = 0u;
     __syncthreads();
-    for (int i = threadIdx.x; i < total; i += kThreads) {
-      const uint32_t rel = cand[cand_slot(pre, warp_cap, i)] - t_lo;
+    for (int i = threadIdx.x; i < total; i += NT) {
+      const uint32_t rel = cand[cand_slot<NT>(pre, warp_cap, i)] - t_lo;
       if ((rel & pmask) == prefix) atomicAdd(&hist[(rel >> sh) & (nb - 1)], 1u);
     }
     __syncthreads();
     int bin, above;
-    find_bin(hist, nb < kThreads ? kThreads : nb, rank - gt, warp_tot, s_bin, s_above, bin,
-             above);
+    find_bin<NT>(hist, nb < NT ? NT : nb, rank - gt, warp_tot, s_bin, s_above, bin, above);
     gt += above;
     prefix |= static_cast<uint32_t>(bin) << sh;
     pmask |= static_cast<uint32_t>(nb - 1) << sh;
@@ -218,20 +195,21 @@ __device__ void select_rank_warp_lists(const uint32_t* cand, const int* pre, int
 // Two sample quantiles at once, to 22-bit key resolution: the 22-bit key
 // prefixes of the r_hi-th and r_lo-th largest sample keys (r_hi <= r_lo),
 // from one 11-bit histogram of the sample and one of each boundary bin.
+template <int NT>
 __device__ void sample_bracket(const uint32_t* samp, int n, int r_hi, int r_lo, uint32_t* hist,
                                int* warp_tot, int* s_bin, int* s_above, uint32_t& p_hi,
                                uint32_t& p_lo) {
   uint32_t* h2 = hist + 2048;   // second histogram (second digit of the r_lo bin)
-  for (int i = threadIdx.x; i < 4096; i += kThreads) hist[i] = 0u;
+  for (int i = threadIdx.x; i < 4096; i += NT) hist[i] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += kThreads) atomicAdd(&hist[samp[i] >> 21], 1u);
+  for (int i = threadIdx.x; i < n; i += NT) atomicAdd(&hist[samp[i] >> 21], 1u);
   __syncthreads();
   int b_hi, a_hi, b_lo, a_lo;
-  find_bin(hist, 2048, r_hi, warp_tot, s_bin, s_above, b_hi, a_hi);
-  find_bin(hist, 2048, r_lo, warp_tot, s_bin, s_above, b_lo, a_lo);
-  for (int i = threadIdx.x; i < 2048; i += kThreads) hist[i] = 0u;
+  find_bin<NT>(hist, 2048, r_hi, warp_tot, s_bin, s_above, b_hi, a_hi);
+  find_bin<NT>(hist, 2048, r_lo, warp_tot, s_bin, s_above, b_lo, a_lo);
+  for (int i = threadIdx.x; i < 2048; i += NT) hist[i] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += kThreads) {
+  for (int i = threadIdx.x; i < n; i += NT) {
     const uint32_t key = samp[i];
     const uint32_t top = key >> 21, mid = (key >> 10) & 2047u;
     if (top == static_cast<uint32_t>(b_hi)) atomicAdd(&hist[mid], 1u);
@@ -239,18 +217,20 @@ __device__ void sample_bracket(const uint32_t* samp, int n, int r_hi, int r_lo, 
   }
   __syncthreads();
   int m_hi, x_hi, m_lo, x_lo;
-  find_bin(hist, 2048, r_hi - a_hi, warp_tot, s_bin, s_above, m_hi, x_hi);
-  find_bin(h2, 2048, r_lo - a_lo, warp_tot, s_bin, s_above, m_lo, x_lo);
+  find_bin<NT>(hist, 2048, r_hi - a_hi, warp_tot, s_bin, s_above, m_hi, x_hi);
+  find_bin<NT>(h2, 2048, r_lo - a_lo, warp_tot, s_bin, s_above, m_lo, x_lo);
   p_hi = (static_cast<uint32_t>(b_hi) << 11) | static_cast<uint32_t>(m_hi);
   p_lo = (static_cast<uint32_t>(b_lo) << 11) | static_cast<uint32_t>(m_lo);
 }
 
-// UNROLL: 32-position chunks per warp per step of the main pass (the next
-// step's loads are in flight meanwhile); long rows run one CTA per SM with a
-// deeper main pass, short rows two CTAs per SM.
-template <int UNROLL, int MIN_BLOCKS>
-__global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_constant__ TopkArgs a,
-                                                               int words_cap, int cand_cap) {
+// NT threads per row. UNROLL: 32-position chunks per warp per step of the
+// main pass (the next step's loads are in flight meanwhile); long rows run one
+// CTA per SM with a deeper main pass, decode rows two CTAs per SM, the short
+// prefill tile rows four.
+template <int NT, int UNROLL, int MIN_BLOCKS>
+__global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__ TopkArgs a,
+                                                         int words_cap, int cand_cap) {
+  constexpr int kThreads = NT, kWarps = NT / 32;
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint32_t sm[];
@@ -315,8 +295,8 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_cons
   uint32_t t_hi = 0xFFFFFFFFu, t_lo = 0u;
   {
     uint32_t p_hi, p_lo;
-    sample_bracket(samp, S, max(r_hi, 1), min(r_lo, S), hist, warp_tot, &s_bin, &s_above, p_hi,
-                   p_lo);
+    sample_bracket<NT>(samp, S, max(r_hi, 1), min(r_lo, S), hist, warp_tot, &s_bin, &s_above,
+                       p_hi, p_lo);
     if (r_hi >= 1) t_hi = (p_hi << 10) | 1023u;
     if (r_lo <= S) t_lo = p_lo << 10;
   }
@@ -396,11 +376,11 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_cons
       s_pre[kWarps] = acc;
     }
     __syncthreads();
-    select_rank_warp_lists(cand_key, s_pre, n_cand, warp_cap, t_lo, span, rd.k - n_above, hist,
-                           warp_tot, &s_bin, &s_above, T, cg);
+    select_rank_warp_lists<NT>(cand_key, s_pre, n_cand, warp_cap, t_lo, span, rd.k - n_above,
+                               hist, warp_tot, &s_bin, &s_above, T, cg);
     c_gt = n_above + cg;
     for (int i = tid; i < n_cand; i += kThreads) {
-      const int slot = cand_slot(s_pre, warp_cap, i);
+      const int slot = cand_slot<NT>(s_pre, warp_cap, i);
       const uint32_t key = cand_key[slot];
       const int p = cand_pos[slot];
       if (key > T) atomicOr(&above[p >> 5], 1u << (p & 31));
@@ -417,18 +397,18 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_cons
       const int sh = d == 0 ? 21 : (d == 1 ? 10 : 0);
       for (int i = tid; i < nb; i += kThreads) hist[i] = 0u;
       __syncthreads();
-      for_row(rd, bad, [&](int, bool valid, uint32_t key) {
+      for_row<NT>(rd, bad, [&](int, bool valid, uint32_t key) {
         hist_add(hist, valid && (key & pmask) == prefix, (key >> sh) & (nb - 1));
       });
       __syncthreads();
       int bin, ab;
-      find_bin(hist, nb, rd.k - c_gt, warp_tot, &s_bin, &s_above, bin, ab);
+      find_bin<NT>(hist, nb, rd.k - c_gt, warp_tot, &s_bin, &s_above, bin, ab);
       c_gt += ab;
       prefix |= static_cast<uint32_t>(bin) << sh;
       pmask |= static_cast<uint32_t>(nb - 1) << sh;
     }
     const uint32_t T = prefix;
-    for_row(rd, bad, [&](int j, bool valid, uint32_t key) {
+    for_row<NT>(rd, bad, [&](int j, bool valid, uint32_t key) {
       const unsigned int ba = __ballot_sync(0xffffffffu, valid && key > T);
       const unsigned int be = __ballot_sync(0xffffffffu, valid && key == T);
       if (lane == 0 && j < rd.len) {
@@ -448,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, MIN_BLOCKS) k_topk(const __grid_cons
     ca += __popc(above[w]);
     ce += __popc(eqbm[w]);
   }
-  int pa = block_incl_scan(ca, warp_tot) - ca;
-  int pe = block_incl_scan(ce, warp_tot) - ce;
+  int pa = block_incl_scan<NT>(ca, warp_tot) - ca;
+  int pe = block_incl_scan<NT>(ce, warp_tot) - ce;
   for (int w = w0; w < w1; ++w) {
     const uint32_t ab = above[w], eb = eqbm[w];
     uint32_t u = ab | eb;
@@ -502,11 +482,18 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   }
   const size_t smem = smem_for(cand_cap);
   if (smem > kOnePerSm) return cudaErrorNotSupported;
-  auto kern = one_per_sm ? k_topk<32, 1> : k_topk<kUnroll, 2>;
+  // Many short rows (the prefill tiles: 32 heads x 128 tiles at N = 16384)
+  // run many waves of CTAs whose time goes to barriers and load latency, not
+  // to bandwidth: 256-thread CTAs, four per SM (same registers per thread,
+  // 52 KB of shared memory each at N = 16384), keep twice the rows in flight.
+  const bool small = !one_per_sm && a.n <= kShortRow / 2 && a.rows >= kManyRows;
+  auto kern = one_per_sm ? k_topk<512, 32, 1>
+                         : (small ? k_topk<256, kUnroll, 4> : k_topk<512, kUnroll, 2>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(a.rows), dim3(kThreads), smem, st, a, words_cap, cand_cap);
+  return launch_pdl(kern, dim3(a.rows), dim3(small ? 256 : 512), smem, st, a, words_cap,
+                    cand_cap);
 }
 
 }  // namespace kascade

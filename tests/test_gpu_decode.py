@@ -62,6 +62,29 @@ def test_topk_bit_exact_on_identical_scores(K, case):
         assert got[r].tolist() == topk_indices(x[r], k).tolist(), (case, r)
 
 
+def test_topk_many_short_rows_bit_exact(K):
+    """1100 rows of 6000 keys take the 256-thread CTAs (the launch shape of the
+    prefill tile rows); every row pattern of the cases above recurs across them,
+    including the exact fallback (heavy ties, all equal)."""
+    rng = np.random.default_rng(11)
+    rows, n, k = 1100, 6000, 700
+    x = rng.standard_normal((rows, n)).astype(np.float32)
+    for r in range(rows):
+        kind = r % 6
+        if kind == 1:
+            x[r] = np.round(x[r] * 2) / 2
+        elif kind == 2:
+            x[r, ::3] = -0.0
+            x[r, 1::3] = 0.0
+        elif kind == 3:
+            x[r, rng.random(n) < 0.2] = -np.inf
+        elif kind == 4:
+            x[r] = 1.0
+    got = K.topk(torch.from_numpy(x).to(DEV), k).cpu().numpy()
+    for r in range(rows):
+        assert got[r].tolist() == topk_indices(x[r], k).tolist(), r
+
+
 def test_topk_nan_reported(K):
     ws = K.Workspace(DEV)
     x = torch.randn(3, 1000, device=DEV)
