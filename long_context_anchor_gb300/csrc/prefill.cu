@@ -35,6 +35,11 @@
 namespace kascade {
 namespace {
 
+template <bool V>
+struct BoolC {
+  static constexpr bool value = V;
+};
+
 constexpr int kTile = 128;              // query rows and keys per tile
 constexpr int kHalf = kTile * 128;      // bytes of one 64-column half of a tile
 constexpr int kTileBytes = 2 * kHalf;   // 128 x 128 bf16 = 32 KB
@@ -1224,10 +1229,11 @@ __global__ void __launch_bounds__(kWtThreads, 1)
         const uint32_t ts = tmem + sb * 128 + lane_base;
         // only the diagonal key tile (j == t) needs the causal mask i >= key;
         // exponents and sums on packed pairs of query columns, 64 columns at
-        // a time (the score buffer is released after the second load)
+        // a time (the score buffer is released after the second load). The
+        // mask is a compile-time branch: the off-diagonal tiles (all but one
+        // per row tile) carry no per-score compare or select.
         const bool diag = (j * kTile + kTile - 1 > row0);
-        uint64_t acc[2] = {0ull, 0ull};
-        auto cols = [&](const uint32_t (&v)[32], int base, uint64_t& sum2) {
+        auto cols = [&](const uint32_t (&v)[32], int base, uint64_t& sum2, auto masked) {
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             // 2^(s*sigma*log2e - lse2) = 2^(fma(s, c, -lse2))
@@ -1236,29 +1242,34 @@ __global__ void __launch_bounds__(kWtThreads, 1)
                              lse2[(base + e) >> 1]),
                       y0, y1);
             float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
-            if (diag) {
+            if constexpr (decltype(masked)::value) {
               p0 = (kj <= row0 + base + e) ? p0 : 0.f;
               p1 = (kj <= row0 + base + e + 1) ? p1 : 0.f;
             }
             sum2 = f2_add(sum2, f2_pack(p0, p1));
           }
         };
+        auto key_tile = [&](auto masked) {
+          uint64_t acc[2] = {0ull, 0ull};
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t va[32], vb[32];
-          tmem_ld32(ts + hh * 64, va);
-          tmem_ld32(ts + hh * 64 + 32, vb);
-          tmem_wait_ld();
-          if (hh == 1) {
-            tc_fence_before();
-            mbar_arrive(s_free + sb);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t va[32], vb[32];
+            tmem_ld32(ts + hh * 64, va);
+            tmem_ld32(ts + hh * 64 + 32, vb);
+            tmem_wait_ld();
+            if (hh == 1) {
+              tc_fence_before();
+              mbar_arrive(s_free + sb);
+            }
+            cols(va, hh * 64, acc[0], masked);
+            cols(vb, hh * 64 + 32, acc[1], masked);
           }
-          cols(va, hh * 64, acc[0]);
-          cols(vb, hh * 64 + 32, acc[1]);
-        }
-        float s0, s1;
-        f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
-        if (kj < L) wrow[kj] = s0 + s1;
+          float s0, s1;
+          f2_unpack(f2_add(acc[0], acc[1]), s0, s1);
+          return s0 + s1;
+        };
+        const float wsum = diag ? key_tile(BoolC<true>{}) : key_tile(BoolC<false>{});
+        if (kj < L) wrow[kj] = wsum;
       }
       mbar_arrive(q_free + buf);   // done with this tile's LSEs
       kc += nkv;
