@@ -188,17 +188,82 @@ def _ws(ws, device, nbytes, stream):
     return ws, buf
 
 
-def _contig(*ts):
-    for t in ts:
-        if t is not None and not t.is_contiguous():
-            raise ValueError("tensors must be contiguous")
+# The library reads and writes raw device pointers with the extents the
+# descriptor implies, so every tensor is checked against those extents here,
+# before its address is handed over: a wrong shape, dtype or device would
+# otherwise become an out-of-bounds access on the GPU.
+
+def _expect(t, name, shape, dtype):
+    """Shape, dtype and contiguity of one tensor (no device check)."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s: expected a torch.Tensor" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s: shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+    if t.dtype != dtype:
+        raise TypeError("%s: dtype %s, expected %s" % (name, t.dtype, dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s: must be contiguous" % name)
+
+
+_DEVICE_TYPE = "cuda"   # the only device type whose addresses the library takes
+
+
+def _same_cuda_device(named):
+    """All tensors on one CUDA device; returns it."""
+    dev = named[0][1].device
+    if dev.type != _DEVICE_TYPE:
+        raise ValueError("%s: on %s; the library takes CUDA device tensors" % (named[0][0], dev))
+    for name, t in named[1:]:
+        if t.device != dev:
+            raise ValueError("%s: on %s, expected %s" % (name, t.device, dev))
+    return dev
+
+
+def _attn_inputs(q, k, v, prefill: bool):
+    """Validated (B, Hq, Hkv, N, d) of one layer's q, k, v.
+
+    decode: q [B,Hq,d], k/v [B,Hkv,N,d]; prefill: q [B,Hq,N,d], k/v [B,Hkv,N,d].
+    k and v take q's dtype (bf16 or fp32)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError("%s: expected a torch.Tensor" % name)
+    if q.dim() != (4 if prefill else 3) or k.dim() != 4:
+        raise ValueError("q must be %s and k, v [B,Hkv,N,d]; got q %s, k %s"
+                         % ("[B,Hq,N,d]" if prefill else "[B,Hq,d]", tuple(q.shape),
+                            tuple(k.shape)))
+    _dtype_code(q)
+    B, Hq, d = q.shape[0], q.shape[1], q.shape[-1]
+    Hkv, N = k.shape[1], k.shape[2]
+    if prefill and q.shape[2] != N:
+        raise ValueError("q: %d rows, k: %d keys; prefill needs both equal" % (q.shape[2], N))
+    _expect(q, "q", q.shape, q.dtype)
+    _expect(k, "k", (B, Hkv, N, d), q.dtype)
+    _expect(v, "v", (B, Hkv, N, d), q.dtype)
+    return B, Hq, Hkv, N, d
+
+
+def _layers(qs, ks, vs, prefill: bool):
+    """Validated stack inputs: every layer has layer 0's shapes; returns layer 0's sizes."""
+    L = len(qs)
+    if L < 1 or len(ks) != L or len(vs) != L:
+        raise ValueError("qs, ks, vs: one tensor per layer each (got %d, %d, %d)"
+                         % (len(qs), len(ks), len(vs)))
+    sizes = _attn_inputs(qs[0], ks[0], vs[0], prefill)
+    for l in range(1, L):
+        _expect(qs[l], "qs[%d]" % l, qs[0].shape, qs[0].dtype)
+        _expect(ks[l], "ks[%d]" % l, ks[0].shape, qs[0].dtype)
+        _expect(vs[l], "vs[%d]" % l, ks[0].shape, qs[0].dtype)
+    return sizes
 
 
 # ------------------------------------------------------------------ decode --
 
 def dense_decode(q, k, v, group_map=None, scale=None, out=None, ws=None, stream=None):
     """Exact decode attention: q [B,Hq,d], k/v [B,Hkv,N,d] -> out [B,Hq,d]."""
-    _contig(q, k, v)
+    _attn_inputs(q, k, v, prefill=False)
+    if out is not None:
+        _expect(out, "out", q.shape, q.dtype)
+    _same_cuda_device([("q", q), ("k", k), ("v", v)] + ([("out", out)] if out is not None else []))
     desc = decode_desc(q, k, group_map, scale)
     out = torch.empty_like(q) if out is None else out
     ws, buf = _ws(ws, q.device, workspace_size(desc, 1, DECODE), stream)
@@ -213,11 +278,17 @@ def anchor_decode(q, k, v, topk, group_map=None, scale=None, return_scores=False
 
     H = Hq: per-head sets, scores = the scaled logits. pooled: H = Hkv, one
     set per KV head, scores = the group sums of the softmax weights."""
-    _contig(q, k, v)
-    desc = decode_desc(q, k, group_map, scale, pooled)
-    B, Hq, _ = q.shape
-    Hkv, N = k.shape[1], k.shape[2]
+    B, Hq, Hkv, N, _ = _attn_inputs(q, k, v, prefill=False)
     H = Hkv if pooled else Hq
+    extra = []
+    if out is not None:
+        _expect(out, "out", q.shape, q.dtype)
+        extra.append(("out", out))
+    if idx is not None:
+        _expect(idx, "idx", (B, H, topk), torch.int32)
+        extra.append(("idx", idx))
+    _same_cuda_device([("q", q), ("k", k), ("v", v)] + extra)
+    desc = decode_desc(q, k, group_map, scale, pooled)
     out = torch.empty_like(q) if out is None else out
     idx = torch.empty(B, H, topk, dtype=torch.int32, device=q.device) if idx is None else idx
     scores = torch.empty(B, H, N, dtype=torch.float32, device=q.device) if return_scores else None
@@ -231,9 +302,17 @@ def anchor_decode(q, k, v, topk, group_map=None, scale=None, return_scores=False
 def reuse_decode(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, stream=None,
                  pooled=False):
     """Reuse layer over saved sets idx [B,Hq,topk] (pooled: [B,Hkv,topk]; int32, ascending)."""
-    _contig(q, k, v, idx)
-    desc = decode_desc(q, k, group_map, scale, pooled)
+    B, Hq, Hkv, _, _ = _attn_inputs(q, k, v, prefill=False)
+    if not isinstance(idx, torch.Tensor) or idx.dim() != 3:
+        raise ValueError("idx: expected an int32 tensor [B,H,topk]")
     topk = idx.shape[-1]
+    _expect(idx, "idx", (B, Hkv if pooled else Hq, topk), torch.int32)
+    extra = [("idx", idx)]
+    if out is not None:
+        _expect(out, "out", q.shape, q.dtype)
+        extra.append(("out", out))
+    _same_cuda_device([("q", q), ("k", k), ("v", v)] + extra)
+    desc = decode_desc(q, k, group_map, scale, pooled)
     out = torch.empty_like(q) if out is None else out
     ws, buf = _ws(ws, q.device, workspace_size(desc, topk, DECODE), stream)
     _check(_lib.kascade_reuse_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
@@ -244,8 +323,15 @@ def reuse_decode(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, st
 
 def topk(scores, k, out=None, ws=None, stream=None):
     """Exact Top-k of fp32 rows [rows, n] -> int32 [rows, k] ascending."""
-    _contig(scores)
+    if not isinstance(scores, torch.Tensor) or scores.dim() != 2:
+        raise ValueError("scores: expected an fp32 tensor [rows, n]")
     rows, n = scores.shape
+    _expect(scores, "scores", (rows, n), torch.float32)
+    named = [("scores", scores)]
+    if out is not None:
+        _expect(out, "out", (rows, int(k)), torch.int32)
+        named.append(("out", out))
+    _same_cuda_device(named)
     out = torch.empty(rows, k, dtype=torch.int32, device=scores.device) if out is None else out
     ws, buf = _ws(ws, scores.device, 256, stream)
     _check(_lib.kascade_topk(_ptr(scores), rows, n, int(k), _ptr(out), _ptr(buf), buf.numel(),
@@ -261,7 +347,10 @@ def n_tiles(n: int) -> int:
 
 def dense_prefill(q, k, v, group_map=None, scale=None, out=None, ws=None, stream=None):
     """Causal exact attention: q [B,Hq,N,d], k/v [B,Hkv,N,d] (bf16)."""
-    _contig(q, k, v)
+    _attn_inputs(q, k, v, prefill=True)
+    if out is not None:
+        _expect(out, "out", q.shape, q.dtype)
+    _same_cuda_device([("q", q), ("k", k), ("v", v)] + ([("out", out)] if out is not None else []))
     desc = prefill_desc(q, k, group_map, scale)
     out = torch.empty_like(q) if out is None else out
     ws, buf = _ws(ws, q.device, workspace_size(desc, 1, PREFILL), stream)
@@ -274,10 +363,17 @@ def anchor_prefill(q, k, v, topk, group_map=None, scale=None, out=None, idx=None
                    stream=None, pooled=False):
     """Anchor layer, prefill: (out, idx [B,H,nT,topk] int32, -1 padded), H = Hq or,
     pooled, Hkv."""
-    _contig(q, k, v)
+    B, Hq, Hkv, N, _ = _attn_inputs(q, k, v, prefill=True)
+    H = Hkv if pooled else Hq
+    extra = []
+    if out is not None:
+        _expect(out, "out", q.shape, q.dtype)
+        extra.append(("out", out))
+    if idx is not None:
+        _expect(idx, "idx", (B, H, n_tiles(N), topk), torch.int32)
+        extra.append(("idx", idx))
+    _same_cuda_device([("q", q), ("k", k), ("v", v)] + extra)
     desc = prefill_desc(q, k, group_map, scale, pooled)
-    B, Hq, N, _ = q.shape
-    H = k.shape[1] if pooled else Hq
     out = torch.empty_like(q) if out is None else out
     if idx is None:
         idx = torch.empty(B, H, n_tiles(N), topk, dtype=torch.int32, device=q.device)
@@ -291,9 +387,17 @@ def anchor_prefill(q, k, v, topk, group_map=None, scale=None, out=None, idx=None
 def reuse_prefill(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, stream=None,
                   pooled=False):
     """Reuse layer, prefill, over saved tile sets idx [B,Hq,nT,topk] (pooled: [B,Hkv,nT,topk])."""
-    _contig(q, k, v, idx)
-    desc = prefill_desc(q, k, group_map, scale, pooled)
+    B, Hq, Hkv, N, _ = _attn_inputs(q, k, v, prefill=True)
+    if not isinstance(idx, torch.Tensor) or idx.dim() != 4:
+        raise ValueError("idx: expected an int32 tensor [B,H,nT,topk]")
     topk = idx.shape[-1]
+    _expect(idx, "idx", (B, Hkv if pooled else Hq, n_tiles(N), topk), torch.int32)
+    extra = [("idx", idx)]
+    if out is not None:
+        _expect(out, "out", q.shape, q.dtype)
+        extra.append(("out", out))
+    _same_cuda_device([("q", q), ("k", k), ("v", v)] + extra)
+    desc = prefill_desc(q, k, group_map, scale, pooled)
     out = torch.empty_like(q) if out is None else out
     ws, buf = _ws(ws, q.device, workspace_size(desc, topk, PREFILL), stream)
     _check(_lib.kascade_reuse_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
@@ -311,18 +415,31 @@ def run_stack(mode, qs, ks, vs, topk, anchors, group_map=None, scale=None, outs=
     layer_events: optional list of torch.cuda.Event (timing enabled), one per
     layer, recorded on the stream after that layer's launches. pooled: one
     index set per KV head."""
+    if mode not in (DECODE, PREFILL):
+        raise ValueError("mode must be DECODE or PREFILL")
     L = len(qs)
-    _contig(*qs, *ks, *vs)
-    H = ks[0].shape[1] if pooled else qs[0].shape[1]
+    B, Hq, Hkv, N, _ = _layers(qs, ks, vs, prefill=(mode == PREFILL))
+    H = Hkv if pooled else Hq
     if mode == DECODE:
         desc = decode_desc(qs[0], ks[0], group_map, scale, pooled)
-        B = qs[0].shape[0]
         shape = (B, H, topk)
     else:
         desc = prefill_desc(qs[0], ks[0], group_map, scale, pooled)
-        B, _, N, _ = qs[0].shape
         shape = (B, H, n_tiles(N), topk)
-    dev = qs[0].device
+    named = [("qs[%d]" % l, qs[l]) for l in range(L)] + [("ks[%d]" % l, ks[l]) for l in range(L)]
+    named += [("vs[%d]" % l, vs[l]) for l in range(L)]
+    if outs is not None:
+        if len(outs) != L:
+            raise ValueError("outs: one tensor per layer (got %d for %d layers)" % (len(outs), L))
+        for l in range(L):
+            _expect(outs[l], "outs[%d]" % l, qs[0].shape, qs[0].dtype)
+            named.append(("outs[%d]" % l, outs[l]))
+    if idx_buf is not None:
+        _expect(idx_buf, "idx_buf", shape, torch.int32)
+        named.append(("idx_buf", idx_buf))
+    if layer_events is not None and len(layer_events) != L:
+        raise ValueError("layer_events: one event per layer")
+    dev = _same_cuda_device(named)
     outs = [torch.empty_like(q) for q in qs] if outs is None else outs
     if idx_buf is None:
         idx_buf = torch.empty(shape, dtype=torch.int32, device=dev)
@@ -346,8 +463,11 @@ def run_stack(mode, qs, ks, vs, topk, anchors, group_map=None, scale=None, outs=
 
 def layer_overlap(sets, n_bits, ws=None, stream=None):
     """sets: int32 [L, units, topk] on the device -> int64 counts [L, L]."""
-    _contig(sets)
+    if not isinstance(sets, torch.Tensor) or sets.dim() != 3:
+        raise ValueError("sets: expected an int32 tensor [L, units, topk]")
     L, units, k = sets.shape
+    _expect(sets, "sets", (L, units, k), torch.int32)
+    _same_cuda_device([("sets", sets)])
     counts = torch.empty(L, L, dtype=torch.int64, device=sets.device)
     nbytes = _lib.kascade_overlap_workspace_size(L, units, int(n_bits))
     ws, buf = _ws(ws, sets.device, nbytes, stream)
@@ -376,11 +496,12 @@ def calibrate(qs, ks, vs, topk, group_map=None, scale=None, ws=None, stream=None
         raise ValueError("similarity must be 'overlap' or 'recall'")
     recall = similarity == "recall"
     L = len(qs)
-    _contig(*qs, *ks, *vs)
+    B, Hq, Hkv, _, _ = _layers(qs, ks, vs, prefill=False)
+    dev = _same_cuda_device([("qs[%d]" % l, qs[l]) for l in range(L)]
+                            + [("ks[%d]" % l, ks[l]) for l in range(L)]
+                            + [("vs[%d]" % l, vs[l]) for l in range(L)])
     desc = decode_desc(qs[0], ks[0], group_map, scale, pooled)
-    B, Hq, _ = qs[0].shape
-    H = ks[0].shape[1] if pooled else Hq
-    dev = qs[0].device
+    H = Hkv if pooled else Hq
     outs = [torch.empty_like(q) for q in qs]
     sets = torch.empty(L, B * H, topk, dtype=torch.int32, device=dev)
     size_fn = (_lib.kascade_calibrate_recall_workspace_size if recall
