@@ -13,7 +13,6 @@
 #include <string.h>
 
 #include <mutex>
-#include <new>
 
 #include "common.cuh"
 #include "internal.h"
@@ -613,6 +612,8 @@ kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
   if (n_layers < 1 || q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
       sim_out == nullptr || !aligned16(sets_buf) || topk < 1 || topk > s.N)
     return KASCADE_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)   // every layer's pointers before any launch
+    if ((r = check_decode_ptrs(q[l], k[l], v[l], out[l])) != KASCADE_OK) return r;
   const size_t need = kascade_calibrate_workspace_size(desc, topk, n_layers);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < need)
     return KASCADE_ERR_WORKSPACE;
@@ -620,7 +621,6 @@ kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t per_layer = static_cast<size_t>(s.B) * s.H_idx * topk;
   for (int l = 0; l < n_layers; ++l) {
-    if ((r = check_decode_ptrs(q[l], k[l], v[l], out[l])) != KASCADE_OK) return r;
     r = run_anchor_decode(s, q[l], k[l], v[l], topk, out[l], sets_buf + l * per_layer, nullptr,
                           ws, L, st);
     if (r != KASCADE_OK) return r;
@@ -634,17 +634,20 @@ kascade_status kascade_calibrate(const kascade_desc* desc, int32_t n_layers,
                                        reinterpret_cast<uint32_t*>(base + kWsStateBytes),
                                        reinterpret_cast<unsigned int*>(base), st);
   if (e != cudaSuccess) return KASCADE_ERR_CUDA;
+  // the int64 counts land in the caller's float64 array (same element size)
+  // and are turned into means in place
   const size_t nc = static_cast<size_t>(n_layers) * n_layers;
-  long long* host = new (std::nothrow) long long[nc];
-  if (host == nullptr) return KASCADE_ERR_INVALID_ARG;
-  e = cudaMemcpyAsync(host, counts, nc * 8, cudaMemcpyDeviceToHost, st);
+  static_assert(sizeof(long long) == sizeof(double), "in-place count conversion");
+  e = cudaMemcpyAsync(sim_out, counts, nc * 8, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-  if (e == cudaSuccess) {
-    const double denom = static_cast<double>(s.B) * s.H_idx * topk;
-    for (size_t i = 0; i < nc; ++i) sim_out[i] = static_cast<double>(host[i]) / denom;
+  if (e != cudaSuccess) return KASCADE_ERR_CUDA;
+  const double denom = static_cast<double>(s.B) * s.H_idx * topk;
+  for (size_t i = 0; i < nc; ++i) {
+    long long c;
+    memcpy(&c, sim_out + i, sizeof(c));
+    sim_out[i] = static_cast<double>(c) / denom;
   }
-  delete[] host;
-  return e == cudaSuccess ? KASCADE_OK : KASCADE_ERR_CUDA;
+  return KASCADE_OK;
 }
 
 }  // extern "C"
@@ -692,6 +695,8 @@ kascade_status kascade_calibrate_recall(const kascade_desc* desc, int32_t n_laye
   if (n_layers < 1 || q == nullptr || k == nullptr || v == nullptr || out == nullptr ||
       sim_out == nullptr || !aligned16(sets_buf) || topk < 1 || topk > s.N)
     return KASCADE_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)   // every layer's pointers before any launch
+    if ((r = check_decode_ptrs(q[l], k[l], v[l], out[l])) != KASCADE_OK) return r;
   const RecallLayout R = recall_layout(s, topk, n_layers);
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < R.total)
     return KASCADE_ERR_WORKSPACE;
@@ -704,7 +709,6 @@ kascade_status kascade_calibrate_recall(const kascade_desc* desc, int32_t n_laye
   float* part = at<float>(ws, R.part);
   unsigned int* err = at<unsigned int>(ws, 0);
   for (int l = 0; l < n_layers; ++l) {
-    if ((r = check_decode_ptrs(q[l], k[l], v[l], out[l])) != KASCADE_OK) return r;
     r = run_anchor_decode(s, q[l], k[l], v[l], topk, out[l], sets_buf + l * per_layer, nullptr,
                           ws, L, st);
     if (r != KASCADE_OK) return r;

@@ -68,6 +68,28 @@ def test_validation_before_launch(K):
     assert K._lib.kascade_topk(p, 4, 10, 11, p, p, 256, None) == K.INVALID_ARG
 
 
+def test_calibration_checks_every_layer_before_launching(K):
+    """A misaligned pointer in the last layer is reported as an argument error
+    before layer 0 launches (with no GPU here, a launch would fail with a CUDA
+    error instead)."""
+    import ctypes
+    desc = K.make_desc(1, 4, 2, 64, 512, K.BF16)
+    fake = 1 << 20
+    good = [fake, fake]
+    bad = [fake, fake + 8]
+    arr = lambda xs: (ctypes.c_void_p * 2)(*xs)
+    sim = (ctypes.c_double * 4)()
+    p = ctypes.c_void_p(fake)
+    for fn, size_fn in ((K._lib.kascade_calibrate, K._lib.kascade_calibrate_workspace_size),
+                        (K._lib.kascade_calibrate_recall,
+                         K._lib.kascade_calibrate_recall_workspace_size)):
+        nws = size_fn(ctypes.byref(desc), 32, 2)
+        assert nws > 0
+        for qs, ks in ((bad, good), (good, bad)):
+            assert fn(ctypes.byref(desc), 2, arr(qs), arr(ks), arr(good), 32, arr(good), p, sim,
+                      p, nws, None) == K.INVALID_ARG
+
+
 def test_index_mode_validation_and_workspace(K):
     import ctypes
     per_head = K.make_desc(2, 8, 2, 128, 4096, K.BF16)
