@@ -812,17 +812,6 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
-def schedule_objective(sim, anchors):
-    """sum over layers l of sim[a(l)][l], a(l) the latest anchor at or before l."""
-    A = sorted(anchors)
-    total, cur = 0.0, None
-    for layer in range(len(sim)):
-        while A and A[0] <= layer:
-            cur = A.pop(0)
-        total += sim[cur][layer]
-    return total
-
-
 def run_sweep(args):
     """Schedule sweep: the DP picks the anchors from calibration on synthetic
     sequences, then decode and prefill stacks run with those anchors against
@@ -830,6 +819,8 @@ def run_sweep(args):
     import torch
     from long_context_anchor_gb300 import configs
     from long_context_anchor_gb300 import kascade as K
+    from long_context_anchor_gb300.schedule_file import objective as schedule_objective
+    from long_context_anchor_gb300.schedule_file import save_schedule
     from long_context_anchor_gb300.workloads import make_layers
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
@@ -861,6 +852,13 @@ def run_sweep(args):
         "mass_kept_overlap_anchors": round(schedule_objective(rsim, anchors) / L, 4),
         "mass_kept_uniform_anchors": round(schedule_objective(rsim, uniform) / L, 4),
         "mass_kept_own_topk_mean": round(float(np.mean([rsim[l][l] for l in range(L)])), 4)}
+    if args.save_schedule:
+        meta = {"workload": wc.name, "topk": wc.topk, "batch": wc.batch, "kv_len": wc.kv_len,
+                "n_q_heads": wc.n_q_heads, "n_kv_heads": wc.n_kv_heads, "data": "synthetic"}
+        save_schedule(args.save_schedule, anchors, sim, "overlap", meta)
+        root, ext = os.path.splitext(args.save_schedule)
+        save_schedule(root + "_recall" + (ext or ".json"), r_anchors, rsim, "recall", meta)
+        res["schedule_files"] = [args.save_schedule, root + "_recall" + (ext or ".json")]
     del qs, ks, vs
     torch.cuda.empty_cache()
 
@@ -926,6 +924,8 @@ def main():
                     help="skip the decode stack with GQA-pooled index sets")
     ap.add_argument("--sweep", action="store_true",
                     help="schedule sweep: DP anchors from calibration, decode and prefill vs dense")
+    ap.add_argument("--save-schedule", default="",
+                    help="with --sweep: write the DP schedules (overlap, and recall beside it) as JSON")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
