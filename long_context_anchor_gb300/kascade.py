@@ -459,6 +459,22 @@ def run_stack(mode, qs, ks, vs, topk, anchors, group_map=None, scale=None, outs=
     return outs, idx_buf
 
 
+def kascade_attention(qs, ks, vs, topk, anchors, group_map=None, scale=None, pooled=False,
+                      ws=None, stream=None):
+    """One call over a layer stack, in the form the Kascade pages describe
+    (euno.news summary, Practical Implications): per-layer lists qs, ks, vs,
+    the Top-k size and the anchor layers. 3-D queries [B,Hq,d] are decode,
+    4-D [B,Hq,N,d] causal prefill. Anchor layers compute exact attention and
+    refresh the index sets, the layers after them reuse those sets, and
+    layers before the first anchor run dense. Returns the per-layer outputs."""
+    if len(qs) == 0:
+        raise ValueError("qs: at least one layer")
+    mode = DECODE if qs[0].dim() == 3 else PREFILL
+    outs, _ = run_stack(mode, qs, ks, vs, topk, list(anchors), group_map=group_map, scale=scale,
+                        ws=ws, stream=stream, pooled=pooled)
+    return outs
+
+
 # -------------------------------------------------------------- scheduling --
 
 def layer_overlap(sets, n_bits, ws=None, stream=None):

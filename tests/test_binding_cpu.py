@@ -139,3 +139,24 @@ def test_host_tensors_are_refused(K, monkeypatch):
     with pytest.raises(ValueError, match="CUDA"):
         K.topk(torch.zeros(3, 10), 2)
     assert rec.calls == []
+
+
+def test_kascade_attention_dispatches_on_query_rank(K, fake, monkeypatch):
+    seen = []
+    real = K.run_stack
+
+    def spy(mode, *a, **kw):
+        seen.append(mode)
+        return real(mode, *a, **kw)
+
+    monkeypatch.setattr(K, "run_stack", spy)
+    ws = K.Workspace("cpu")
+    qd, kd, vd = _decode()
+    outs = K.kascade_attention([qd, qd], [kd, kd], [vd, vd], 16, [1], ws=ws)
+    assert len(outs) == 2 and outs[0].shape == qd.shape
+    qp, kp, vp = _prefill()
+    K.kascade_attention([qp], [kp], [vp], 40, (0,), ws=ws)
+    assert seen == [K.DECODE, K.PREFILL]
+    with pytest.raises(ValueError):
+        K.kascade_attention([], [], [], 16, [0])
+
