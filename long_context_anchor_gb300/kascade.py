@@ -242,18 +242,29 @@ def _attn_inputs(q, k, v, prefill: bool):
     return B, Hq, Hkv, N, d
 
 
+def _all_like(ts, name, shape, dtype, dev):
+    """Every tensor of a per-layer list has this shape, dtype and device and is
+    contiguous (one fast pass; the first mismatch gets a detailed error)."""
+    for l, t in enumerate(ts):
+        if not (isinstance(t, torch.Tensor) and t.shape == shape and t.dtype == dtype
+                and t.device == dev and t.is_contiguous()):
+            _expect(t, "%s[%d]" % (name, l), shape, dtype)
+            raise ValueError("%s[%d]: on %s, expected %s" % (name, l, t.device, dev))
+
+
 def _layers(qs, ks, vs, prefill: bool):
-    """Validated stack inputs: every layer has layer 0's shapes; returns layer 0's sizes."""
+    """Validated stack inputs: every layer has layer 0's shapes, dtype and
+    device; returns (B, Hq, Hkv, N, d) and the device."""
     L = len(qs)
     if L < 1 or len(ks) != L or len(vs) != L:
         raise ValueError("qs, ks, vs: one tensor per layer each (got %d, %d, %d)"
                          % (len(qs), len(ks), len(vs)))
     sizes = _attn_inputs(qs[0], ks[0], vs[0], prefill)
-    for l in range(1, L):
-        _expect(qs[l], "qs[%d]" % l, qs[0].shape, qs[0].dtype)
-        _expect(ks[l], "ks[%d]" % l, ks[0].shape, qs[0].dtype)
-        _expect(vs[l], "vs[%d]" % l, ks[0].shape, qs[0].dtype)
-    return sizes
+    dev = _same_cuda_device([("qs[0]", qs[0]), ("ks[0]", ks[0]), ("vs[0]", vs[0])])
+    _all_like(qs, "qs", qs[0].shape, qs[0].dtype, dev)
+    _all_like(ks, "ks", ks[0].shape, qs[0].dtype, dev)
+    _all_like(vs, "vs", ks[0].shape, qs[0].dtype, dev)
+    return sizes, dev
 
 
 # ------------------------------------------------------------------ decode --
@@ -418,7 +429,7 @@ def run_stack(mode, qs, ks, vs, topk, anchors, group_map=None, scale=None, outs=
     if mode not in (DECODE, PREFILL):
         raise ValueError("mode must be DECODE or PREFILL")
     L = len(qs)
-    B, Hq, Hkv, N, _ = _layers(qs, ks, vs, prefill=(mode == PREFILL))
+    (B, Hq, Hkv, N, _), dev = _layers(qs, ks, vs, prefill=(mode == PREFILL))
     H = Hkv if pooled else Hq
     if mode == DECODE:
         desc = decode_desc(qs[0], ks[0], group_map, scale, pooled)
@@ -426,20 +437,15 @@ def run_stack(mode, qs, ks, vs, topk, anchors, group_map=None, scale=None, outs=
     else:
         desc = prefill_desc(qs[0], ks[0], group_map, scale, pooled)
         shape = (B, H, n_tiles(N), topk)
-    named = [("qs[%d]" % l, qs[l]) for l in range(L)] + [("ks[%d]" % l, ks[l]) for l in range(L)]
-    named += [("vs[%d]" % l, vs[l]) for l in range(L)]
     if outs is not None:
         if len(outs) != L:
             raise ValueError("outs: one tensor per layer (got %d for %d layers)" % (len(outs), L))
-        for l in range(L):
-            _expect(outs[l], "outs[%d]" % l, qs[0].shape, qs[0].dtype)
-            named.append(("outs[%d]" % l, outs[l]))
+        _all_like(outs, "outs", qs[0].shape, qs[0].dtype, dev)
     if idx_buf is not None:
         _expect(idx_buf, "idx_buf", shape, torch.int32)
-        named.append(("idx_buf", idx_buf))
+        _same_cuda_device([("qs[0]", qs[0]), ("idx_buf", idx_buf)])
     if layer_events is not None and len(layer_events) != L:
         raise ValueError("layer_events: one event per layer")
-    dev = _same_cuda_device(named)
     outs = [torch.empty_like(q) for q in qs] if outs is None else outs
     if idx_buf is None:
         idx_buf = torch.empty(shape, dtype=torch.int32, device=dev)
@@ -512,10 +518,7 @@ def calibrate(qs, ks, vs, topk, group_map=None, scale=None, ws=None, stream=None
         raise ValueError("similarity must be 'overlap' or 'recall'")
     recall = similarity == "recall"
     L = len(qs)
-    B, Hq, Hkv, _, _ = _layers(qs, ks, vs, prefill=False)
-    dev = _same_cuda_device([("qs[%d]" % l, qs[l]) for l in range(L)]
-                            + [("ks[%d]" % l, ks[l]) for l in range(L)]
-                            + [("vs[%d]" % l, vs[l]) for l in range(L)])
+    (B, Hq, Hkv, _, _), dev = _layers(qs, ks, vs, prefill=False)
     desc = decode_desc(qs[0], ks[0], group_map, scale, pooled)
     H = Hkv if pooled else Hq
     outs = [torch.empty_like(q) for q in qs]
