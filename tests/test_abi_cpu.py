@@ -134,6 +134,17 @@ def test_host_dp_matches_oracle(K, L, m):
         assert abs(f - fo) < 1e-9
 
 
+@pytest.mark.parametrize("L,m", [(6, 2), (8, 4), (10, 4), (16, 5)])
+def test_host_dp_matches_oracle_on_ties(K, L, m):
+    rng = np.random.default_rng(7 * L + m)
+    for _ in range(10):
+        M = rng.integers(0, 3, size=(L, L)) / 2.0
+        np.fill_diagonal(M, 1.0)
+        a, f = K.schedule_anchors(M.tolist(), m)
+        ao, fo = oracle_dp(M, m)
+        assert a == ao and f == fo
+
+
 def test_host_dp_ties_and_errors(K):
     a, f = K.schedule_anchors(np.ones((6, 6)).tolist(), 3)
     assert a == [0, 1, 2] and f == 6.0

@@ -40,6 +40,24 @@ def test_dp_equals_exhaustive_small(L, m):
         np.testing.assert_allclose(objective(M, A), f, atol=1e-10)
 
 
+@pytest.mark.parametrize("L,m", [(6, 2), (7, 3), (8, 4), (9, 3), (10, 4)])
+def test_dp_ties_pick_the_lexicographically_smallest_set(L, m):
+    """Entries in {0, 1/2, 1} sum exactly in float64, so many anchor sets tie
+    for the optimum; the DP must return the first of them in lexicographic
+    order, as exhaustive enumeration does."""
+    rng = np.random.default_rng(100 + L * 10 + m)
+    n_tied = 0
+    for _ in range(20):
+        M = rng.integers(0, 3, size=(L, L)) / 2.0
+        np.fill_diagonal(M, 1.0)
+        A, f = schedule_anchors(M, m)
+        Ae, fe = _exhaustive(M, m)
+        assert A == Ae and f == fe
+        vals = [objective(M, (0,) + rest) for rest in itertools.combinations(range(1, L), m - 1)]
+        n_tied += sum(v == fe for v in vals) > 1
+    assert n_tied > 0   # the cases do exercise ties
+
+
 def test_dp_equals_exhaustive_L32_m6():
     """All C(31, 5) = 169,911 anchor sets of a 32-layer stack, vectorised."""
     rng = np.random.default_rng(32)
