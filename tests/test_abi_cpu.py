@@ -90,6 +90,19 @@ def test_calibration_checks_every_layer_before_launching(K):
                       p, nws, None) == K.INVALID_ARG
 
 
+def test_documented_size_limits(K):
+    """The header's limits: N < 2^24, B*Hkv*N < 2^31, B*Hkv <= 16384 (a
+    descriptor beyond one has no workspace size)."""
+    ws = K._lib.kascade_workspace_size
+    assert ws(K.make_desc(1, 4, 2, 64, (1 << 24) - 1, K.BF16), 32, 0) > 0
+    assert ws(K.make_desc(1, 4, 2, 64, 1 << 24, K.BF16), 32, 0) == 0
+    assert ws(K.make_desc(64, 8, 8, 64, 1 << 22, K.BF16), 32, 0) == 0       # B*Hkv*N = 2^31
+    assert ws(K.make_desc(64, 8, 8, 64, (1 << 22) - 1, K.BF16), 32, 0) > 0
+    assert ws(K.make_desc(2048, 8, 8, 64, 16, K.BF16), 32, 0) > 0           # B*Hkv = 16384
+    assert ws(K.make_desc(2049, 8, 8, 64, 16, K.BF16), 32, 0) == 0
+    assert ws(K.make_desc(1, 264, 33, 64, 512, K.BF16), 32, 0) == 0         # Hq > 256
+
+
 def test_index_mode_validation_and_workspace(K):
     import ctypes
     per_head = K.make_desc(2, 8, 2, 128, 4096, K.BF16)
