@@ -162,13 +162,24 @@ kascade_status kascade_topk(const float* scores, int32_t rows, int32_t n, int32_
  * not allowed. The paper has no counterpart to this entry point. Its scratch
  * (split partials, counters, error word) is a fixed 8 MiB device array inside
  * the library, held by every GPU that loads it until the process exits;
- * shapes needing more return KASCADE_ERR_WORKSPACE. The first call on a
- * device looks up the array's device address, so make it before any stream
- * capture. All calls share the array: calls that overlap on the GPU race
- * and must be serialised by the caller. Allocates nothing. */
+ * shapes needing more return KASCADE_ERR_WORKSPACE (the descriptor limits
+ * above apply as for every entry point). The first call on a device looks
+ * up the array's device address, so make it before any stream capture, and
+ * do not use the library across a cudaDeviceReset. All calls share the
+ * array: calls that overlap on the GPU race and must be serialised by the
+ * caller. Allocates nothing. Faults found on the device (an expired bounded
+ * wait) are recorded in the array's error word; kascade_noalloc_device_error
+ * is the only way to read them. */
 kascade_status kascade_dense_decode_noalloc(const kascade_desc* desc, const void* q,
                                             const void* k, const void* v, void* out,
                                             void* stream);
+
+/* Synchronise `stream`, then read and clear the error word of the
+ * no-allocation scratch array on the current device: KASCADE_OK,
+ * KASCADE_ERR_BAD_INPUT or KASCADE_ERR_TIMEOUT. Faults of every
+ * kascade_dense_decode_noalloc call since the last read accumulate there.
+ * The paper has no counterpart to this entry point. Allocates nothing. */
+kascade_status kascade_noalloc_device_error(void* stream);
 
 /* --------------------------------------------------------------- prefill -- */
 
@@ -181,10 +192,17 @@ kascade_status kascade_dense_prefill(const kascade_desc* desc, const void* q, co
  * head, 128-row tile t) the Top-k_t of the tile weights w_j, k_t =
  * min(topk, L_t), L_t = min(N, 128(t+1)), into idx_out [B,Hq,nT,topk]
  * (ascending, -1 padded). Pooled index mode: per (sequence, KV head g,
- * tile) the Top-k_t of sum_{h: g(h)=g} w_{t,h,j}, idx_out [B,Hkv,nT,topk]. */
+ * tile) the Top-k_t of sum_{h: g(h)=g} w_{t,h,j}, idx_out [B,Hkv,nT,topk].
+ * When weights_out is not NULL (16-byte aligned) the fp32 tile weights the
+ * selection ranked are also written there, packed per (sequence, head):
+ * [B, H, P] with P = 64*(nT-1)*nT + N (the sum of the L_t), tile t's L_t
+ * weights w_0..w_{L_t-1} starting at offset 64*t*(t+1) of its (b, h) row;
+ * H = Hq, or Hkv in pooled index mode (then the group sums). Feeding one
+ * packed row to kascade_topk's rule reproduces idx_out exactly. */
 kascade_status kascade_anchor_prefill(const kascade_desc* desc, const void* q, const void* k,
                                       const void* v, int32_t topk, void* out, int32_t* idx_out,
-                                      void* ws, size_t ws_bytes, void* stream);
+                                      float* weights_out, void* ws, size_t ws_bytes,
+                                      void* stream);
 
 /* Reuse layer, prefill: row i of tile t attends to S_i = {j in idx[b,h,t,:],
  * j >= 0, j <= i}; a row whose S_i is empty outputs zeros. Pooled index

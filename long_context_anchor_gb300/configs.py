@@ -30,7 +30,9 @@ GPTOSS_DECODE_128K = Workload(
     sink=True, rho=0.85, seed=1003)
 
 # Schedule sweep: calibration on 4 sequences with per-layer rho ~ U[0.7, 0.95],
-# 6 anchors chosen by the DP, then evaluation at the lengths below.
+# 6 anchors chosen by the DP, then evaluation at the lengths below. The
+# evaluation inputs are fresh sequences (their own seeds) on the same
+# per-layer rhos as the calibration (rho_seed).
 SWEEP_CALIBRATION = Workload(
     name="llama8b_calibration_b4_n32768_k4096", mode="decode", n_layers=32, batch=4,
     n_q_heads=32, n_kv_heads=8, head_dim=128, kv_len=32768, topk=4096,
@@ -39,7 +41,14 @@ SWEEP_CALIBRATION = Workload(
 SWEEP_N_ANCHORS = 6
 SWEEP_PREFILL_LENGTHS = (4096, 16384, 65536)
 SWEEP_DECODE = SWEEP_CALIBRATION.with_(name="llama8b_decode_b16_n32768_k4096", batch=16,
-                                       seed=2004)
+                                       seed=2004, rho_seed=SWEEP_CALIBRATION.seed)
+
+
+def sweep_prefill(n: int) -> Workload:
+    """Sweep evaluation prefill at length n (k = n/8), 32 layers of the 8B shape."""
+    return LLAMA8B_PREFILL_16K.with_(name="llama8b_prefill_n%d_k%d" % (n, n // 8), kv_len=n,
+                                     topk=n // 8, rho_range=(0.7, 0.95), seed=3004 + n,
+                                     rho_seed=SWEEP_CALIBRATION.seed)
 
 ALL = [TINY_DECODE, LLAMA8B_DECODE_32K, LLAMA8B_PREFILL_16K, GPTOSS_DECODE_128K,
        SWEEP_CALIBRATION]

@@ -58,20 +58,8 @@ bool encode_tmap_2d_bf16(void* tmap, const void* base, uint64_t inner, uint64_t 
   return r == CUDA_SUCCESS;
 }
 
-namespace {
-
-inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
-
-// Validated shape plus the derived head tables.
-struct Shape {
-  int B, Hq, Hkv, d, N, G, dtype;
-  int pooled;                    // one index set per KV head (GQA-pooled scores)
-  int H_idx;                     // heads that own an index set: Hq, or Hkv when pooled
-  float scale;
-  int16_t heads[kMaxQHeads];     // heads[g*G + slot]
-  int16_t head_kv[kMaxQHeads];   // KV head of each query head
-};
-
+// Validation of a descriptor (declared in internal.h; the no-allocation
+// entry point uses it too).
 kascade_status check_desc(const kascade_desc* desc, Shape& s) {
   if (desc == nullptr) return KASCADE_ERR_INVALID_ARG;
   s.B = desc->batch;
@@ -105,6 +93,11 @@ kascade_status check_desc(const kascade_desc* desc, Shape& s) {
   }
   return KASCADE_OK;
 }
+
+
+namespace {
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -429,17 +422,21 @@ kascade_status run_dense_prefill(const Shape& s, const void* q, const void* k, c
 }
 
 kascade_status run_anchor_prefill(const Shape& s, const void* q, const void* k, const void* v,
-                                  int topk, void* out, int32_t* idx_out, void* ws,
-                                  const Layout& L, cudaStream_t st) {
+                                  int topk, void* out, int32_t* idx_out, float* weights_out,
+                                  void* ws, const Layout& L, cudaStream_t st) {
   PrefillArgs a;
   fill_prefill_args(a, s, q, k, v, out, ws, L, topk);
+  // per-head weights go to the caller's buffer when it asked for them (and
+  // the selection reads them there); pooled sets keep the per-head weights
+  // in the workspace and hand out the group sums
+  if (weights_out != nullptr && !s.pooled) a.w = weights_out;
   kascade_status r = launch_status(launch_prefill_lse(a, s.d, st));
   if (r != KASCADE_OK) return r;
   if ((r = launch_status(launch_prefill_anchor_main(a, s.d, st))) != KASCADE_OK) return r;
   const float* scores = a.w;
   if (s.pooled) {
     const size_t per_bh = static_cast<size_t>(64) * (a.nT - 1) * a.nT + s.N;
-    float* w_pool = at<float>(ws, L.w_pool);
+    float* w_pool = weights_out != nullptr ? weights_out : at<float>(ws, L.w_pool);
     r = cuda_status(launch_pool_prefill(a.w, w_pool, s.heads, s.B, s.Hq, s.Hkv, s.G, per_bh, st));
     if (r != KASCADE_OK) return r;
     scores = w_pool;
@@ -495,14 +492,16 @@ kascade_status kascade_dense_prefill(const kascade_desc* desc, const void* q, co
 
 kascade_status kascade_anchor_prefill(const kascade_desc* desc, const void* q, const void* k,
                                       const void* v, int32_t topk, void* out, int32_t* idx_out,
-                                      void* ws, size_t ws_bytes, void* stream) {
+                                      float* weights_out, void* ws, size_t ws_bytes,
+                                      void* stream) {
   Shape s;
   kascade_status r = check_prefill(desc, s, q, k, v, out);
   if (r != KASCADE_OK) return r;
   if (topk < 1 || topk > s.N || !aligned16(idx_out)) return KASCADE_ERR_INVALID_ARG;
+  if (weights_out != nullptr && !aligned16(weights_out)) return KASCADE_ERR_INVALID_ARG;
   Layout L;
   if ((r = check_ws(s, topk, KASCADE_PREFILL, ws, ws_bytes, L)) != KASCADE_OK) return r;
-  return run_anchor_prefill(s, q, k, v, topk, out, idx_out, ws, L,
+  return run_anchor_prefill(s, q, k, v, topk, out, idx_out, weights_out, ws, L,
                             static_cast<cudaStream_t>(stream));
 }
 
@@ -562,7 +561,7 @@ kascade_status kascade_run_stack_profiled(const kascade_desc* desc, int32_t mode
       }
     } else {
       if (is_anchor) {
-        r = run_anchor_prefill(s, q[l], k[l], v[l], tk, out[l], idx_buf, ws, L, st);
+        r = run_anchor_prefill(s, q[l], k[l], v[l], tk, out[l], idx_buf, nullptr, ws, L, st);
         held = true;
       } else if (held) {
         r = run_reuse_prefill(s, q[l], k[l], v[l], tk, idx_buf, out[l], ws, L, st);

@@ -7,6 +7,8 @@
 
 #include <utility>
 
+#include "kascade.h"
+
 namespace kascade {
 
 // Launch with programmatic stream serialization: the kernel may be scheduled
@@ -58,6 +60,21 @@ struct DecodeArgs {
 };
 
 enum DecodeKind { kDense = 0, kAnchor = 1, kSparse = 2 };
+
+// A validated descriptor plus the derived head tables.
+struct Shape {
+  int B, Hq, Hkv, d, N, G, dtype;
+  int pooled;                    // one index set per KV head (GQA-pooled scores)
+  int H_idx;                     // heads that own an index set: Hq, or Hkv when pooled
+  float scale;
+  int16_t heads[kMaxQHeads];     // heads[g*G + slot]
+  int16_t head_kv[kMaxQHeads];   // KV head of each query head
+};
+
+// Checks a descriptor against the library's limits and fills the derived
+// tables (api.cu): KASCADE_OK, KASCADE_ERR_INVALID_ARG or
+// KASCADE_ERR_UNSUPPORTED.
+kascade_status check_desc(const kascade_desc* desc, Shape& s);
 
 // decode.cu
 cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spill,

@@ -12,13 +12,17 @@
 // The array's name is only a host-side stand-in in host code; its device
 // address is fetched once per device with cudaGetSymbolAddress, on the first
 // call made while that device is current, and cached. That first call
-// should therefore come before any stream capture. Every call shares the
-// one array, and it keeps the last call's contents: each call clears the
-// counters and the error word it needs (cudaMemsetAsync, no allocation), and
-// calls that overlap on the GPU (concurrent streams) race on the array and
-// must be serialised by the caller.
+// should therefore come before any stream capture. The cache is keyed by the
+// device ordinal, so the library must not be used across a cudaDeviceReset
+// (the module, and with it the array, may be loaded at another address).
+//
+// Every call shares the one array, and it keeps the last call's contents:
+// each call clears the split counters it needs (cudaMemsetAsync, no
+// allocation), and calls that overlap on the GPU (concurrent streams) race on
+// the array and must be serialised by the caller. The error word is not
+// cleared by the calls: device faults accumulate there until
+// kascade_noalloc_device_error reads and clears it.
 #include <cuda_runtime.h>
-#include <math.h>
 #include <string.h>
 
 #include <mutex>
@@ -66,32 +70,22 @@ extern "C" kascade_status kascade_dense_decode_noalloc(const kascade_desc* desc,
                                                        const void* k, const void* v, void* out,
                                                        void* stream) {
   using namespace kascade;
-  if (desc == nullptr) return KASCADE_ERR_INVALID_ARG;
-  const int B = desc->batch, Hq = desc->n_q_heads, Hkv = desc->n_kv_heads;
-  const int d = desc->head_dim, N = desc->kv_len;
-  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || Hq % Hkv != 0 || Hq > kMaxQHeads)
-    return KASCADE_ERR_INVALID_ARG;
-  if (desc->dtype != KASCADE_BF16 || (d != 64 && d != 128)) return KASCADE_ERR_UNSUPPORTED;
-  const int G = Hq / Hkv;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return KASCADE_ERR_UNSUPPORTED;
-  if (static_cast<long long>(B) * Hkv * N >= (1ll << 31)) return KASCADE_ERR_UNSUPPORTED;
+  Shape s;
+  kascade_status r = check_desc(desc, s);   // the same limits as every other entry point
+  if (r != KASCADE_OK) return r;
+  if (s.dtype != KASCADE_BF16) return KASCADE_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return KASCADE_ERR_INVALID_ARG;
 
   DecodeArgs a;
   memset(&a, 0, sizeof(a));
-  int fill[kMaxQHeads] = {};
-  for (int h = 0; h < Hq; ++h) {
-    const int g = desc->group_map ? desc->group_map[h] : h / G;
-    if (g < 0 || g >= Hkv || fill[g] >= G) return KASCADE_ERR_INVALID_ARG;
-    a.heads[g * G + fill[g]++] = static_cast<int16_t>(h);
-  }
-  const int units = B * Hkv;
-  a.chunk = decode_chunk_dense(units, N);
-  a.S = (N + a.chunk - 1) / a.chunk;
+  for (int i = 0; i < s.Hq; ++i) a.heads[i] = s.heads[i];
+  const int units = s.B * s.Hkv;
+  a.chunk = decode_chunk_dense(units, s.N);
+  a.S = (s.N + a.chunk - 1) / a.chunk;
   // Size check against the fixed scratch: header + counters, then partials.
   const size_t counters = static_cast<size_t>(units) * sizeof(unsigned int);
-  const size_t partials = static_cast<size_t>(B) * Hq * a.S * (d + 4) * sizeof(float);
+  const size_t partials = static_cast<size_t>(s.B) * s.Hq * a.S * (s.d + 4) * sizeof(float);
   if (sizeof(WsHeader) + counters > kCounterBytes ||
       kCounterBytes + partials > kNoAllocScratchBytes)
     return KASCADE_ERR_WORKSPACE;   // shape needs more than the 8 MiB scratch
@@ -99,10 +93,11 @@ extern "C" kascade_status kascade_dense_decode_noalloc(const kascade_desc* desc,
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return KASCADE_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // Counters and the error word must start at zero; partials are overwritten.
-  if (cudaMemsetAsync(scratch, 0, sizeof(WsHeader) + counters, st) != cudaSuccess)
-    return KASCADE_ERR_CUDA;
   char* base = static_cast<char*>(scratch);
+  // The split counters must start at zero (a call cut short by a bounded wait
+  // may have left some set); partials are overwritten; the error word stays.
+  if (cudaMemsetAsync(base + sizeof(WsHeader), 0, counters, st) != cudaSuccess)
+    return KASCADE_ERR_CUDA;
   a.q = q;
   a.k = k;
   a.v = v;
@@ -110,13 +105,34 @@ extern "C" kascade_status kascade_dense_decode_noalloc(const kascade_desc* desc,
   a.err = reinterpret_cast<unsigned int*>(base);
   a.counters = reinterpret_cast<unsigned int*>(base + sizeof(WsHeader));
   a.part = reinterpret_cast<float*>(base + kCounterBytes);
-  a.B = B;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.N = N;
-  a.G = G;
+  a.B = s.B;
+  a.Hq = s.Hq;
+  a.Hkv = s.Hkv;
+  a.N = s.N;
+  a.G = s.G;
   a.topk = 1;
-  a.scale = desc->scale > 0.f ? desc->scale : 1.0f / sqrtf(static_cast<float>(d));
-  a.scale_log2 = a.scale * 1.4426950408889634f;
-  return launch_decode_dense_bf16(a, d, false, st) == cudaSuccess ? KASCADE_OK : KASCADE_ERR_CUDA;
+  a.scale = s.scale;
+  a.scale_log2 = s.scale * 1.4426950408889634f;
+  return launch_decode_dense_bf16(a, s.d, false, st) == cudaSuccess ? KASCADE_OK
+                                                                     : KASCADE_ERR_CUDA;
+}
+
+extern "C" kascade_status kascade_noalloc_device_error(void* stream) {
+  using namespace kascade;
+  void* scratch = nullptr;
+  if (scratch_address(&scratch) != cudaSuccess) return KASCADE_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return KASCADE_ERR_CUDA;
+  unsigned int word[2] = {0u, 0u};
+  // plain copies from and to the array: nothing is allocated
+  if (cudaMemcpy(word, scratch, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return KASCADE_ERR_CUDA;
+  if (word[0] != 0) {
+    const unsigned int zero[2] = {0u, 0u};
+    if (cudaMemcpy(scratch, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return KASCADE_ERR_CUDA;
+  }
+  if (word[0] & (1u << KASCADE_ERR_TIMEOUT)) return KASCADE_ERR_TIMEOUT;
+  if (word[0] & (1u << KASCADE_ERR_BAD_INPUT)) return KASCADE_ERR_BAD_INPUT;
+  return KASCADE_OK;
 }

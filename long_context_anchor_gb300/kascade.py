@@ -49,8 +49,10 @@ _SIGS = {
     "kascade_reuse_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "kascade_topk": (ctypes.c_int, [_vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "kascade_dense_decode_noalloc": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp]),
+    "kascade_noalloc_device_error": (ctypes.c_int, [_vp]),
     "kascade_dense_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "kascade_anchor_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "kascade_anchor_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _sz,
+                                              _vp]),
     "kascade_reuse_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "kascade_run_stack": (ctypes.c_int, [_DP, _i32, _i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                          ctypes.POINTER(_vp), _i32, ctypes.POINTER(_i32), _i32,
@@ -370,10 +372,23 @@ def dense_prefill(q, k, v, group_map=None, scale=None, out=None, ws=None, stream
     return out
 
 
+def packed_tile_len(n: int) -> int:
+    """Length of one (sequence, head) row of packed tile weights: sum_t L_t."""
+    nt = n_tiles(n)
+    return 64 * (nt - 1) * nt + n
+
+
+def packed_tile_offset(t: int) -> int:
+    """Offset of tile t's weights in a packed row (64 t (t + 1))."""
+    return 64 * t * (t + 1)
+
+
 def anchor_prefill(q, k, v, topk, group_map=None, scale=None, out=None, idx=None, ws=None,
-                   stream=None, pooled=False):
+                   stream=None, pooled=False, return_weights=False):
     """Anchor layer, prefill: (out, idx [B,H,nT,topk] int32, -1 padded), H = Hq or,
-    pooled, Hkv."""
+    pooled, Hkv. With return_weights, also the fp32 tile weights the selection
+    ranked, packed [B,H,packed_tile_len(N)] (tile t at packed_tile_offset(t),
+    L_t = min(N, 128(t+1)) entries): (out, idx, weights)."""
     B, Hq, Hkv, N, _ = _attn_inputs(q, k, v, prefill=True)
     H = Hkv if pooled else Hq
     extra = []
@@ -388,11 +403,13 @@ def anchor_prefill(q, k, v, topk, group_map=None, scale=None, out=None, idx=None
     out = torch.empty_like(q) if out is None else out
     if idx is None:
         idx = torch.empty(B, H, n_tiles(N), topk, dtype=torch.int32, device=q.device)
+    wts = (torch.empty(B, H, packed_tile_len(N), dtype=torch.float32, device=q.device)
+           if return_weights else None)
     ws, buf = _ws(ws, q.device, workspace_size(desc, topk, PREFILL), stream)
     _check(_lib.kascade_anchor_prefill(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
-                                       _ptr(out), _ptr(idx), _ptr(buf), buf.numel(),
+                                       _ptr(out), _ptr(idx), _ptr(wts), _ptr(buf), buf.numel(),
                                        _stream(stream)), "kascade_anchor_prefill")
-    return out, idx
+    return (out, idx, wts) if return_weights else (out, idx)
 
 
 def reuse_prefill(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, stream=None,

@@ -52,6 +52,9 @@ class Workload:
     rho: float = 0.9
     rho_range: Optional[Tuple[float, float]] = None   # per-layer rho ~ U[a, b] when set
     seed: int = 1000
+    # seed of the per-layer rho draw when it differs from `seed`: evaluation
+    # sequences of a schedule are fresh draws on the calibration's rhos
+    rho_seed: Optional[int] = None
     tile: int = 128
 
     @property
@@ -76,7 +79,8 @@ def layer_rhos(w: Workload) -> list:
     """Per-layer chain coefficients; rho_0 is unused."""
     if w.rho_range is None:
         return [w.rho] * w.n_layers
-    gen = torch.Generator(device="cpu").manual_seed(w.seed + 7919)
+    gen = torch.Generator(device="cpu").manual_seed(
+        (w.seed if w.rho_seed is None else w.rho_seed) + 7919)
     a, b = w.rho_range
     u = torch.rand(w.n_layers, generator=gen, dtype=torch.float64)
     return [float(a + (b - a) * x) for x in u]

@@ -189,3 +189,11 @@ def test_noalloc_rejects_shapes_beyond_its_scratch(K):
     assert K._lib.kascade_dense_decode_noalloc(ctypes.byref(ok), p, p, p, p, None) == K.CUDA
     f32 = K.make_desc(8, 32, 8, 128, 32768, K.F32)
     assert K._lib.kascade_dense_decode_noalloc(ctypes.byref(f32), p, p, p, p, None) == K.UNSUPPORTED
+    # the descriptor limits are the library's, as for every other entry point
+    long_n = K.make_desc(1, 8, 8, 128, 1 << 24, K.BF16)
+    assert K._lib.kascade_dense_decode_noalloc(ctypes.byref(long_n), p, p, p, p, None) == K.UNSUPPORTED
+    bad_mode = K.make_desc(1, 8, 8, 128, 4096, K.BF16)
+    bad_mode.index_mode = 7
+    assert K._lib.kascade_dense_decode_noalloc(ctypes.byref(bad_mode), p, p, p, p, None) == K.INVALID_ARG
+    # the error-word reader needs a device too
+    assert K._lib.kascade_noalloc_device_error(None) == K.CUDA

@@ -73,6 +73,12 @@ def test_documented_layouts_pass(K, fake):
     K.dense_prefill(q, k, v, ws=ws)
     out, idx = K.anchor_prefill(q, k, v, 40, ws=ws)
     assert idx.shape == (1, 4, 3, 40)
+    out, idx, wts = K.anchor_prefill(q, k, v, 40, ws=ws, return_weights=True)
+    # packed tile rows: L_0 + L_1 + L_2 = 128 + 256 + 300
+    assert wts.shape == (1, 4, 684) and K.packed_tile_len(300) == 684
+    assert [K.packed_tile_offset(t) for t in range(3)] == [0, 128, 384]
+    _, _, wts = K.anchor_prefill(q, k, v, 40, ws=ws, return_weights=True, pooled=True)
+    assert wts.shape == (1, 2, 684)
     K.reuse_prefill(q, k, v, torch.zeros(1, 2, 3, 40, dtype=torch.int32), pooled=True, ws=ws)
     qs, ks, vs = [list(t) for t in (q.expand(3, *q.shape).contiguous(),
                                     k.expand(3, *k.shape).contiguous(),

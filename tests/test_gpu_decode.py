@@ -10,7 +10,7 @@ from long_context_anchor_gb300.workloads import make_layers, group_map as defaul
 from oracle import attention as A
 from oracle.stack import run_stack as run_oracle_stack
 from oracle.topk import topk_indices
-from gpu_helpers import check_index_set, check_out, f64
+from gpu_helpers import check_index_set, check_out, check_topk_exact, f64
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
@@ -245,33 +245,38 @@ def test_stack_matches_layer_calls_and_oracle(K, dtype):
 
 @pytest.mark.parametrize("cfg", ["llama8b", "gptoss"])
 def test_full_size_decode_sampled(K, cfg):
+    """The 8B (B=8, N=32768, k=4096) and gpt-oss-20b-like (B=4, N=131072,
+    k=8192, d=64) decode shapes through the stack call, on sampled (sequence,
+    head) units including the first and last: the anchor output and set
+    against the oracle's decode_unit, the Top-k bit-exact on the kernel's own
+    fp32 logits, and the reuse output over the oracle's own set."""
     w = configs.LLAMA8B_DECODE_32K if cfg == "llama8b" else configs.GPTOSS_DECODE_128K
     w = w.with_(n_layers=2)
     qs, ks, vs = make_layers(w, device=DEV)
     outs, idx = K.run_stack(K.DECODE, qs, ks, vs, w.topk, [0])
+    # the anchor entry point with the logits buffer gives the stack's sets
+    _, idx_a, s_gpu = K.anchor_decode(qs[0], ks[0], vs[0], w.topk, return_scores=True)
     torch.cuda.synchronize()
+    assert torch.equal(idx, idx_a)
     gm = default_gmap(w.n_q_heads, w.n_kv_heads)
     scale = 1.0 / np.sqrt(w.head_dim)
     rng = np.random.default_rng(1)
     units = [(0, 0), (w.batch - 1, w.n_q_heads - 1)] + \
         [(int(rng.integers(w.batch)), int(rng.integers(w.n_q_heads))) for _ in range(6)]
     idx_np = idx.cpu().numpy()
-    errs0, errs1 = [], []
     for b, h in units:
         g = gm[h]
-        K0, V0 = f64(ks[0][b, g]), f64(vs[0][b, g])
-        q0 = f64(qs[0][b, h])
-        s = scale * (K0 @ q0)
-        p = np.exp(s - s.max())
-        o_ref = (p / p.sum()) @ V0
-        errs0.append(np.abs(f64(outs[0][b, h]) - o_ref).max())
-        check_index_set(idx_np[b, h], s, w.topk)
-        sel = topk_indices(s, w.topk)   # the oracle's own set for the reuse layer
-        K1, V1 = f64(ks[1][b, g])[sel], f64(vs[1][b, g])[sel]
-        s1 = scale * (K1 @ f64(qs[1][b, h]))
-        p1 = np.exp(s1 - s1.max())
-        errs1.append(np.abs(f64(outs[1][b, h]) - (p1 / p1.sum()) @ V1).max())
-    assert max(errs0) < 2e-2 and max(errs1) < 2e-2, (max(errs0), max(errs1))
+        # one sequence and KV head on the host, mapped to index 0
+        q0, K0, V0 = (f64(x[b:b + 1, sl]) for x, sl in
+                      ((qs[0], slice(h, h + 1)), (ks[0], slice(g, g + 1)), (vs[0], slice(g, g + 1))))
+        o_ref, sel, s_ref = A.decode_unit(q0, K0, V0, 0, 0, w.topk, [0], scale)
+        check_out(outs[0][b, h], o_ref, what=("anchor out", b, h))
+        check_topk_exact(idx_np[b, h], s_gpu[b, h].cpu().numpy(), w.topk, what=("top-k", b, h))
+        check_index_set(idx_np[b, h], s_ref, w.topk, what=("set", b, h))
+        q1, K1, V1 = (f64(x[b:b + 1, sl]) for x, sl in
+                      ((qs[1], slice(h, h + 1)), (ks[1], slice(g, g + 1)), (vs[1], slice(g, g + 1))))
+        o1_ref = A.decode_unit(q1, K1, V1, 0, 0, w.topk, [0], scale, idx=sel)
+        check_out(outs[1][b, h], o1_ref, what=("reuse out", b, h))
 
 
 def test_workspace_shared_across_shapes_and_entry_points(K):

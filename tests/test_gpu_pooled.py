@@ -17,7 +17,8 @@ from long_context_anchor_gb300.workloads import make_layers, group_map as defaul
 from oracle import attention as A
 from oracle.stack import run_stack as run_oracle_stack
 from oracle.topk import topk_indices
-from gpu_helpers import check_index_set, check_out, f64
+from gpu_helpers import (check_index_set, check_out, check_topk_exact, check_weights, f64,
+                         packed_tile)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
@@ -178,22 +179,26 @@ def test_pooled_decode_stack_matches_layer_calls(K, dtype):
 def test_pooled_anchor_prefill_matches_oracle(K, shape, topk):
     B, Hq, Hkv, N = shape
     q, k, v = _prefill_layer(B, Hq, Hkv, N, seed=3 * N + topk)
-    out, idx = K.anchor_prefill(q, k, v, topk, pooled=True)
+    out, idx, wts = K.anchor_prefill(q, k, v, topk, pooled=True, return_weights=True)
     nT = A.n_tiles(N)
     assert idx.shape == (B, Hkv, nT, topk)
+    assert wts.shape == (B, Hkv, K.packed_tile_len(N))
     Q, Kh, V = f64(q), f64(k), f64(v)
     gm = A.default_group_map(Hq, Hkv)
     check_out(out, A.dense_prefill(Q, Kh, V))
     got = idx.cpu().numpy()
+    w_gpu = wts.cpu().numpy()
     scale = 1.0 / np.sqrt(128)
     for b in range(B):
         for g in range(Hkv):
             for t in range(nT):
                 w = A.tile_weights_pooled(Q, Kh, b, g, t, gm, scale)
+                w_row = packed_tile(w_gpu[b, g], t, N)
+                check_weights(w_row, w, what=("pooled tile weights", b, g, t))
                 kt = min(topk, w.shape[0])
                 row = got[b, g, t]
-                assert (row[kt:] == -1).all()
-                check_index_set(row[:kt], w, kt)
+                check_topk_exact(row, w_row, kt, what=("pooled tile top-k", b, g, t))
+                check_index_set(row[:kt], _log(w), kt, what=("pooled tile set", b, g, t))
 
 
 @pytest.mark.parametrize("shape,topk", [((1, 4, 2, 300), 64), ((2, 8, 2, 520), 130)])
@@ -306,7 +311,10 @@ def test_full_size_pooled_prefill_sampled(K):
     w = configs.LLAMA8B_PREFILL_16K.with_(n_layers=2)
     qs, ks, vs = make_layers(w, device=DEV)
     outs, idx = K.run_stack(K.PREFILL, qs, ks, vs, w.topk, [0], pooled=True)
+    _, idx_a, wts = K.anchor_prefill(qs[0], ks[0], vs[0], w.topk, pooled=True,
+                                     return_weights=True)
     torch.cuda.synchronize()
+    assert torch.equal(idx, idx_a)
     gm = default_gmap(w.n_q_heads, w.n_kv_heads)
     scale = 1.0 / np.sqrt(w.head_dim)
     nT = A.n_tiles(w.kv_len)
@@ -317,8 +325,11 @@ def test_full_size_pooled_prefill_sampled(K):
         Qg = qs[0][:, heads, :L].float().cpu().numpy()
         Kg = ks[0][:, g:g + 1, :L].float().cpu().numpy()
         wt = A.tile_weights_pooled(Qg, Kg, 0, 0, t, [0] * len(heads), scale)
+        w_row = packed_tile(wts[0, g].cpu().numpy(), t, w.kv_len)
+        check_weights(w_row, wt, what=("pooled tile weights", g, t))
         kt = min(w.topk, L)
-        check_index_set(idx_np[0, g, t, :kt], wt, kt, what="pooled tile set")
+        check_topk_exact(idx_np[0, g, t], w_row, kt, what=("pooled tile top-k", g, t))
+        check_index_set(idx_np[0, g, t, :kt], _log(wt), kt, what="pooled tile set")
         # reuse rows of one head of the group over the group's set
         h = heads[1]
         r0, r1 = A.tile_rows(t, w.kv_len)

@@ -12,7 +12,8 @@ from long_context_anchor_gb300.workloads import make_layers, group_map as defaul
 from oracle import attention as A
 from oracle.stack import run_stack as run_oracle_stack
 from oracle.topk import topk_indices
-from gpu_helpers import check_index_set, check_out, f64
+from gpu_helpers import (check_index_set, check_out, check_topk_exact, check_weights, f64,
+                         log_w, packed_tile)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
@@ -63,25 +64,36 @@ def test_dense_prefill_permuted_map_and_scale(K):
 
 
 @pytest.mark.parametrize("shape,topk", [((1, 4, 2, 300), 64), ((2, 8, 2, 520), 130),
-                                        ((1, 8, 1, 1024), 128)])
+                                        ((1, 8, 1, 1024), 128), ((1, 2, 1, 1000), 1000)])
 def test_anchor_prefill_matches_oracle(K, shape, topk):
+    """Every (sequence, head, tile): the kernel's tile weights against the
+    oracle's element by element, its packed-row Top-k bit-exact against the
+    oracle rule on those identical fp32 weights, and its set against the
+    oracle's own float64 set (near-ties judged on log-weights)."""
     B, Hq, Hkv, N = shape
     q, k, v = _layer(B, Hq, Hkv, N, 128, seed=5 * N + topk)
-    out, idx = K.anchor_prefill(q, k, v, topk)
+    out, idx, wts = K.anchor_prefill(q, k, v, topk, return_weights=True)
+    assert wts.shape == (B, Hq, K.packed_tile_len(N))
     Q, Kh, V = f64(q), f64(k), f64(v)
     gm = A.default_group_map(Hq, Hkv)
     scale = 1.0 / np.sqrt(128)
     check_out(out, A.dense_prefill(Q, Kh, V))
     got = idx.cpu().numpy()
+    w_gpu = wts.cpu().numpy()
     nT = A.n_tiles(N)
     for b in range(B):
         for h in range(Hq):
             for t in range(nT):
-                w = A.tile_weights(Q, Kh, b, h, t, gm, scale)
-                kt = min(topk, w.shape[0])
+                w_ref = A.tile_weights(Q, Kh, b, h, t, gm, scale)
+                w_row = packed_tile(w_gpu[b, h], t, N)
+                check_weights(w_row, w_ref, what=("tile weights", b, h, t))
+                kt = min(topk, w_ref.shape[0])
                 row = got[b, h, t]
-                assert (row[kt:] == -1).all()
-                check_index_set(row[:kt], w, kt)
+                check_topk_exact(row, w_row, kt, what=("tile top-k", b, h, t))
+                check_index_set(row[:kt], log_w(w_ref), kt, what=("tile set", b, h, t))
+    # the weights buffer is optional: without it the sets are the same
+    _, idx2 = K.anchor_prefill(q, k, v, topk)
+    assert torch.equal(idx, idx2)
 
 
 @pytest.mark.parametrize("shape,topk", [((1, 4, 2, 300), 64), ((2, 8, 2, 520), 130)])
@@ -154,10 +166,17 @@ def test_prefill_stack_matches_layer_calls(K):
 
 
 def test_full_size_prefill_sampled(K):
+    """The Llama-3.1-8B prefill shape at N = 16384 (k = 2048) through the stack
+    call, on sampled (head, tile) units including the first and last tiles:
+    anchor rows, tile weights, the bit-exact packed-row Top-k and the tile set
+    against the oracle, and the reuse rows over the oracle's own set."""
     w = configs.LLAMA8B_PREFILL_16K.with_(n_layers=2)
     qs, ks, vs = make_layers(w, device=DEV)
     outs, idx = K.run_stack(K.PREFILL, qs, ks, vs, w.topk, [0])
+    # the anchor entry point with the weights buffer gives the stack's sets
+    _, idx_a, wts = K.anchor_prefill(qs[0], ks[0], vs[0], w.topk, return_weights=True)
     torch.cuda.synchronize()
+    assert torch.equal(idx, idx_a)
     gm = default_gmap(w.n_q_heads, w.n_kv_heads)
     scale = 1.0 / np.sqrt(w.head_dim)
     nT = A.n_tiles(w.kv_len)
@@ -165,26 +184,19 @@ def test_full_size_prefill_sampled(K):
     units = [(0, 0), (w.n_q_heads - 1, nT - 1), (5, 20)] + \
         [(int(rng.integers(w.n_q_heads)), int(rng.integers(nT))) for _ in range(3)]
     idx_np = idx.cpu().numpy()
+    # host copies of the sampled heads' rows only
+    Q0, Q1 = f64(qs[0]), f64(qs[1])
+    K0, V0, K1, V1 = f64(ks[0]), f64(vs[0]), f64(ks[1]), f64(vs[1])
     for h, t in units:
-        g = gm[h]
         r0, r1 = A.tile_rows(t, w.kv_len)
-        L = A.prefix_len(t, w.kv_len)
-        Q0 = f64(qs[0][0, h, r0:r1])
-        K0, V0 = f64(ks[0][0, g, :L]), f64(vs[0][0, g, :L])
-        s = scale * Q0 @ K0.T
-        rows = np.arange(r0, r1)[:, None]
-        s[np.arange(L)[None, :] > rows] = -np.inf
-        p = np.exp(s - s.max(1, keepdims=True))
-        p /= p.sum(1, keepdims=True)
-        check_out(outs[0][0, h, r0:r1], p @ V0, what="anchor rows")
-        wts = p.sum(0)
-        kt = min(w.topk, L)
-        check_index_set(idx_np[0, h, t, :kt], wts, kt, what="tile set")
-        sel = topk_indices(wts, kt)   # the oracle's own set for the reuse layer
-        Q1 = f64(qs[1][0, h, r0:r1])
-        K1, V1 = f64(ks[1][0, g])[sel], f64(vs[1][0, g])[sel]
-        s1 = scale * Q1 @ K1.T
-        s1[sel[None, :] > rows] = -np.inf
-        p1 = np.exp(s1 - s1.max(1, keepdims=True))
-        p1 /= p1.sum(1, keepdims=True)
-        check_out(outs[1][0, h, r0:r1], p1 @ V1, what="reuse rows")
+        o_ref, _ = A.dense_prefill_tile(Q0, K0, V0, 0, h, t, gm, scale)
+        check_out(outs[0][0, h, r0:r1], o_ref, what=("anchor rows", h, t))
+        w_ref = A.tile_weights(Q0, K0, 0, h, t, gm, scale)
+        w_row = packed_tile(wts[0, h].cpu().numpy(), t, w.kv_len)
+        check_weights(w_row, w_ref, what=("tile weights", h, t))
+        kt = min(w.topk, w_ref.shape[0])
+        check_topk_exact(idx_np[0, h, t], w_row, kt, what=("tile top-k", h, t))
+        check_index_set(idx_np[0, h, t, :kt], log_w(w_ref), kt, what=("tile set", h, t))
+        sel = topk_indices(w_ref, kt)   # the oracle's own set for the reuse layer
+        o1_ref, _ = A.sparse_prefill_tile(Q1, K1, V1, sel, 0, h, t, gm, scale)
+        check_out(outs[1][0, h, r0:r1], o1_ref, what=("reuse rows", h, t))

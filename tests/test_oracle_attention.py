@@ -244,3 +244,38 @@ def test_anchor_prefill_small_tiles_select_prefix_and_reuse_equals_dense():
     # k >= N: every tile keeps its full prefix, reuse equals dense everywhere
     o_a2, idx2 = A.anchor_prefill(Q, K, V, N)
     np.testing.assert_allclose(A.sparse_prefill(Q, K, V, idx2), o_a2, atol=1e-12)
+
+
+@pytest.mark.parametrize("gname", list(GMAPS))
+def test_decode_unit_matches_sdpa_and_brute_force(gname):
+    """decode_unit, the one-(sequence, head) form the full-size GPU checks use:
+    its dense output equals the library routine on that head alone, its set
+    is the brute-force Top-k of the head's logits under the tie rule (largest
+    first, lower index on ties), and its sparse output equals the library
+    routine with a mask holding only the given set."""
+    rng = np.random.default_rng(31)
+    B, Hq, Hkv, N, d, k = 2, 6, 2, 41, 8, 7
+    gmap = GMAPS[gname]
+    q, K, V = _rand(rng, B, Hq, d), _rand(rng, B, Hkv, N, d), _rand(rng, B, Hkv, N, d)
+    K[1, 0, 5] = K[1, 0, 9]                      # an exact logit tie inside the set
+    for b, h in [(0, 0), (1, 3), (1, 4)]:
+        g = gmap[h]
+        o, idx, s = A.decode_unit(q, K, V, b, h, k, gmap, 0.4)
+        ref = _sdpa(q[b, h][None, None, None], K[b, g][None, None], V[b, g][None, None],
+                    scale=0.4)[0, 0, 0]
+        np.testing.assert_allclose(o, ref, rtol=0, atol=1e-12)
+        # brute force: every key outside the set loses to every key inside it
+        sel = set(idx.tolist())
+        assert len(sel) == k and list(idx) == sorted(sel)
+        for i in sel:
+            for j in range(N):
+                if j not in sel:
+                    assert s[i] > s[j] or (s[i] == s[j] and i < j)
+        # sparse form on an arbitrary set
+        subset = np.sort(rng.choice(N, 9, replace=False))
+        mask = np.zeros((1, 1, 1, N), dtype=bool)
+        mask[..., subset] = True
+        o_s = A.decode_unit(q, K, V, b, h, k, gmap, 0.4, idx=subset)
+        ref_s = _sdpa(q[b, h][None, None, None], K[b, g][None, None], V[b, g][None, None],
+                      mask=mask, scale=0.4)[0, 0, 0]
+        np.testing.assert_allclose(o_s, ref_s, rtol=0, atol=1e-12)

@@ -70,3 +70,15 @@ def test_rho_range():
     r = layer_rhos(configs.SWEEP_CALIBRATION)
     assert len(r) == 32 and all(0.7 <= x <= 0.95 for x in r)
     assert r == layer_rhos(configs.SWEEP_CALIBRATION)
+
+
+def test_sweep_evaluation_shares_calibration_rhos():
+    """The sweep's evaluation sequences are fresh draws (other seeds) on the
+    calibration's per-layer chain coefficients."""
+    cal = layer_rhos(configs.SWEEP_CALIBRATION)
+    assert layer_rhos(configs.SWEEP_DECODE) == cal
+    for n in configs.SWEEP_PREFILL_LENGTHS:
+        w = configs.sweep_prefill(n)
+        assert layer_rhos(w) == cal and w.seed != configs.SWEEP_CALIBRATION.seed
+        assert w.topk == n // 8 and w.kv_len == n
+    assert configs.SWEEP_DECODE.seed != configs.SWEEP_CALIBRATION.seed
