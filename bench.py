@@ -17,8 +17,11 @@ roofline of the dominant kernel, an end-to-end number through the public API
 with host buffers, and the CPU oracle timed on the host cores.
 The line also carries the prefill stack (Llama-3.1-8B shape, N=16384) and the
 long-context decode stack (gpt-oss-20b-like shape: 24 layers, 64/8 heads,
-d=64, B=4, N=131072, k=8192), each against the library's own dense kernels.
-``--impl reference`` times the CPU oracle itself on a bounded sample.
+d=64, B=4, N=131072, k=8192), each against the library's own dense kernels
+with its own roofline, end-to-end pass and oracle sample, and the schedule
+sweep: six anchors chosen by the DP from calibration on four sequences, then
+decode at batch 16 and prefill at N = 4096, 16384 and 65536 with those
+anchors. ``--impl reference`` times the CPU oracle itself on a bounded sample.
 """
 import argparse
 import datetime
@@ -201,11 +204,90 @@ def time_oracle(w, layers_dev, n_groups, reps=1):
     per_a = statistics.median(ta) * groups_per_layer / n_groups
     per_r = statistics.median(tr) * groups_per_layer / n_groups
     us = 1e6 * (n_anchor * per_a + n_reuse * per_r) / w.n_layers
-    return {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle", "extrapolated": True,
             "sample": "%d of %d (sequence, KV head) groups of one anchor layer and one reuse "
                       "layer (float64 numpy, one process per core, single-threaded BLAS); "
                       "extrapolated to the %d-anchor / %d-reuse stack" %
                       (n_groups, groups_per_layer, n_anchor, n_reuse),
+            "anchor_layer_s": per_a, "reuse_layer_s": per_r}
+
+
+def _oracle_prefill_unit(task):
+    """One (head, 128-row tile) unit of one prefill layer through the float64
+    oracle, in a spawned worker with single-threaded BLAS.
+
+    task = (kind, Q [L_t, d], K [L_t, d], V [L_t, d], t, k or set, scale): the
+    causal prefix up to the tile's last row. Returns (seconds, set or None)."""
+    import numpy as np
+    from oracle import attention as A
+    kind, Q, Kt, Vt, t, arg, scale = task
+    t0 = time.perf_counter()
+    q4, k4, v4 = (x[None, None].astype(np.float64) for x in (Q, Kt, Vt))
+    if kind == "anchor":
+        _, idx, _ = A.anchor_prefill_tile(q4, k4, v4, 0, 0, t, arg, [0], scale)
+    else:
+        A.sparse_prefill_tile(q4, k4, v4, arg, 0, 0, t, [0], scale)
+        idx = None
+    return time.perf_counter() - t0, idx
+
+
+def time_oracle_prefill(w, layers_dev, n_units, reps=1, seed=0):
+    """Wall time of the oracle on a seed-fixed sample of (head, tile) units of
+    one anchor prefill layer (exact rows, tile weights, Top-k) and one reuse
+    layer (over the oracle's own sets), always including the first and the
+    last tile, one process per host core; extrapolated by unit count to
+    milliseconds per stack of the schedule."""
+    import multiprocessing as mp
+    from concurrent.futures import ProcessPoolExecutor
+    (q0, k0, v0), (q1, k1, v1) = layers_dev
+    N, T = w.kv_len, w.tile
+    nT = (N + T - 1) // T
+    G = w.n_q_heads // w.n_kv_heads
+    scale = 1.0 / np.sqrt(w.head_dim)
+    rng = np.random.default_rng(seed)
+    units = [(0, 0), (w.n_q_heads - 1, nT - 1)] + \
+        [(int(rng.integers(w.n_q_heads)), int(rng.integers(nT))) for _ in range(n_units - 2)]
+    f32 = lambda x: x.float().cpu().numpy()
+    at, rq = [], []
+    for h, t in units:
+        L = min(N, T * (t + 1))
+        g = h // G
+        at.append(("anchor", f32(q0[0, h, :L]), f32(k0[0, g, :L]), f32(v0[0, g, :L]), t, w.topk,
+                   scale))
+        rq.append((f32(q1[0, h, :L]), f32(k1[0, g, :L]), f32(v1[0, g, :L]), t))
+    cores = os.cpu_count() or 1
+    old = {k: os.environ.get(k) for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in old:
+        os.environ[k] = "1"
+    try:
+        with ProcessPoolExecutor(max_workers=cores, mp_context=mp.get_context("spawn")) as ex:
+            list(ex.map(_oracle_prefill_unit, at[:1]))        # start the workers
+            ta, tr = [], []
+            for _ in range(reps):
+                t0 = time.perf_counter()
+                sets = [r[1] for r in ex.map(_oracle_prefill_unit, at)]
+                ta.append(time.perf_counter() - t0)
+                rt = [("reuse", Q, Kt, Vt, t, sel, scale) for (Q, Kt, Vt, t), sel in zip(rq, sets)]
+                t0 = time.perf_counter()
+                list(ex.map(_oracle_prefill_unit, rt))
+                tr.append(time.perf_counter() - t0)
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    units_per_layer = w.batch * w.n_q_heads * nT
+    n_anchor = len(w.anchors)
+    n_reuse = w.n_layers - n_anchor
+    per_a = statistics.median(ta) * units_per_layer / n_units
+    per_r = statistics.median(tr) * units_per_layer / n_units
+    return {"value": 1e3 * (n_anchor * per_a + n_reuse * per_r), "unit": "ms/stack",
+            "cores": cores, "kind": "oracle", "extrapolated": True,
+            "sample": "%d of %d (query head, 128-row tile) units, first and last tile included, "
+                      "of one anchor layer and one reuse layer (float64 numpy, one process per "
+                      "core, single-threaded BLAS); extrapolated by unit count to the "
+                      "%d-anchor / %d-reuse stack" % (n_units, units_per_layer, n_anchor, n_reuse),
             "anchor_layer_s": per_a, "reuse_layer_s": per_r}
 
 
@@ -303,6 +385,172 @@ def prefill_flops(w, topk_sizes=None):
                                        for t in range(nT))
     del tile_pairs
     return dense, anchor, reuse
+
+
+# ---------------------------------------------------------- end to end legs --
+
+def decode_e2e(K, w, q_all, k_all, v_all, out_all, anchors, idx_buf, ws, stream, steps, warmup,
+               world, dev):
+    """Decode stack end to end through kascade_run_stack with host buffers.
+
+    Each step copies every layer's new query and the newest K/V row
+    (position N-1) from pinned host memory, runs the stack and reads all
+    outputs back. The copies run on a second stream into two sets of device
+    staging buffers, so step s+1's inputs travel while step s computes and
+    step s's outputs travel while step s+1 computes; every step's own copies
+    stay inside the timed region (the first upload and the last download are
+    not hidden)."""
+    import torch
+    L, N = w.n_layers, w.kv_len
+    q_host = q_all.cpu().pin_memory()
+    knew_host = k_all[:, :, :, N - 1].contiguous().cpu().pin_memory()
+    vnew_host = v_all[:, :, :, N - 1].contiguous().cpu().pin_memory()
+    out_host = [torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory() for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device=dev)
+    q_stage = [torch.empty_like(q_all) for _ in range(2)]
+    kn_stage = [torch.empty(knew_host.shape, dtype=knew_host.dtype, device=dev) for _ in range(2)]
+    vn_stage = [torch.empty(vnew_host.shape, dtype=vnew_host.dtype, device=dev) for _ in range(2)]
+    out_stage = [torch.empty_like(out_all) for _ in range(2)]
+    ks, vs = list(k_all), list(v_all)
+    up_done = [torch.cuda.Event() for _ in range(2)]
+    step_done = [torch.cuda.Event() for _ in range(2)]
+    down_done = [torch.cuda.Event() for _ in range(2)]
+    slot_used = [False, False]
+
+    def upload(slot):
+        with torch.cuda.stream(copy_stream):
+            if slot_used[slot]:
+                copy_stream.wait_event(down_done[slot])   # the slot's previous step is done
+            q_stage[slot].copy_(q_host, non_blocking=True)
+            kn_stage[slot].copy_(knew_host, non_blocking=True)
+            vn_stage[slot].copy_(vnew_host, non_blocking=True)
+            up_done[slot].record(copy_stream)
+        slot_used[slot] = True
+
+    def compute(slot):
+        stream.wait_event(up_done[slot])
+        k_all[:, :, :, N - 1].copy_(kn_stage[slot])
+        v_all[:, :, :, N - 1].copy_(vn_stage[slot])
+        K.run_stack(K.DECODE, list(q_stage[slot]), ks, vs, w.topk, anchors,
+                    outs=list(out_stage[slot]), idx_buf=idx_buf, ws=ws)
+        step_done[slot].record(stream)
+
+    def download(slot):
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(step_done[slot])
+            out_host[slot].copy_(out_stage[slot], non_blocking=True)
+            down_done[slot].record(copy_stream)
+
+    def run(n):
+        upload(0)
+        for st in range(n):
+            if st + 1 < n:
+                upload((st + 1) % 2)
+            compute(st % 2)
+            download(st % 2)
+        stream.wait_event(down_done[(n - 1) % 2])
+
+    run(warmup)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    copy_stream.wait_event(e0)
+    run(steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    # the outputs that came back are the stack's outputs for these inputs
+    assert torch.equal(out_host[(steps - 1) % 2], out_stage[(steps - 1) % 2].cpu())
+    assert ws.device_error() == K.OK
+    ms = max_over_ranks([e0.elapsed_time(e1) / steps], world, dev)[0]
+    return {"value": round(1e3 * ms / L, 3), "unit": UNIT,
+            "h2d_bytes_per_step": int(q_host.numel() * 2 + 2 * knew_host.numel() * 2),
+            "d2h_bytes_per_step": int(out_host[0].numel() * 2),
+            "copies": "second stream, double-buffered staging; D2D scatter of the new K/V rows "
+                      "per step"}
+
+
+def prefill_e2e(K, w, qs, ks, vs, anchors, ws, stream, steps, warmup, world, dev):
+    """Prefill stack end to end through kascade_run_stack with host buffers.
+
+    Each step copies every layer's Q, K and V (the whole prompt) from pinned
+    host memory, runs the stack and reads every layer's output back; a second
+    stream and two sets of device staging buffers overlap step s+1's upload
+    and step s-1's download with step s's compute, and every step's own
+    copies stay inside the timed region."""
+    import torch
+    L = w.n_layers
+    stack_h = lambda ts: torch.stack(ts).cpu().pin_memory()
+    q_host, k_host, v_host = stack_h(qs), stack_h(ks), stack_h(vs)
+    out_host = [torch.empty(q_host.shape, dtype=q_host.dtype).pin_memory() for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device=dev)       # host -> device
+    down_stream = torch.cuda.Stream(device=dev)       # device -> host, concurrently
+    stage = [[torch.empty(h.shape, dtype=h.dtype, device=dev) for h in (q_host, k_host, v_host)]
+             for _ in range(2)]
+    out_stage = [torch.empty(q_host.shape, dtype=q_host.dtype, device=dev) for _ in range(2)]
+    up_done = [torch.cuda.Event() for _ in range(2)]
+    step_done = [torch.cuda.Event() for _ in range(2)]
+    down_done = [torch.cuda.Event() for _ in range(2)]
+    slot_used = [False, False]
+    nT = (w.kv_len + w.tile - 1) // w.tile
+    idx_buf = torch.empty(w.batch, w.n_q_heads, nT, w.topk, dtype=torch.int32, device=dev)
+
+    def upload(slot):
+        with torch.cuda.stream(copy_stream):
+            if slot_used[slot]:
+                copy_stream.wait_event(down_done[slot])
+            for dst, src in zip(stage[slot], (q_host, k_host, v_host)):
+                dst.copy_(src, non_blocking=True)
+            up_done[slot].record(copy_stream)
+        slot_used[slot] = True
+
+    def compute(slot):
+        stream.wait_event(up_done[slot])
+        qd, kd, vd = stage[slot]
+        K.run_stack(K.PREFILL, list(qd), list(kd), list(vd), w.topk, anchors,
+                    outs=list(out_stage[slot]), idx_buf=idx_buf, ws=ws)
+        step_done[slot].record(stream)
+
+    def download(slot):
+        with torch.cuda.stream(down_stream):
+            down_stream.wait_event(step_done[slot])
+            out_host[slot].copy_(out_stage[slot], non_blocking=True)
+            down_done[slot].record(down_stream)
+
+    def run(n):
+        upload(0)
+        for st in range(n):
+            if st + 1 < n:
+                upload((st + 1) % 2)
+            compute(st % 2)
+            download(st % 2)
+        stream.wait_event(down_done[(n - 1) % 2])
+
+    run(warmup)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    copy_stream.wait_event(e0)
+    down_stream.wait_event(e0)
+    run(steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host[(steps - 1) % 2], out_stage[(steps - 1) % 2].cpu())
+    assert ws.device_error() == K.OK
+    ms = max_over_ranks([e0.elapsed_time(e1) / steps], world, dev)[0]
+    h2d = sum(h.numel() * h.element_size() for h in (q_host, k_host, v_host))
+    res = {"value": round(ms, 3), "unit": "ms/stack", "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(out_host[0].numel() * out_host[0].element_size()),
+           "copies": "upload and download streams, double-buffered staging of every layer's Q, K, "
+                     "V and output"}
+    del stage, out_stage, out_host, q_host, k_host, v_host
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_prefill(args, dev, world, stream, clocks):
@@ -403,24 +651,62 @@ def run_prefill(args, dev, world, stream, clocks):
     res["anchor_frac_of_sustained"] = round(res["anchor_tflops"] / tf_sust, 4)
     res["reuse_frac_of_sustained"] = round(res["reuse_tflops"] / tf_sust, 4)
     launches = steps * (3 * len(anchors) + len(reuse_layers))
-    del qs, ks, vs, outs
+    res["gpu_launches"] = launches
+    # the dominant kernel of the Kascade prefill stack by total time: the
+    # reuse-layer attention (24 launches per stack, one per reuse layer)
+    pr_tf = f_reuse / (reuse_ms * 1e-3) / 1e12
+    res["roofline"] = {"kernel": "k_prefill_fa2<reuse> (reuse layer)", "bound": "tensor",
+                       "achieved": round(pr_tf, 1), "peak": tf_sust, "unit": "TFLOP/s",
+                       "frac": round(pr_tf / tf_sust, 4), "traffic": TRAFFIC["k_prefill_fa2_reuse"],
+                       "algorithmic_flops": int(f_reuse), "peak_source": src + " (sustained)"}
+    del outs
+    torch.cuda.empty_cache()
+    clocks.begin()
+    res["e2e"] = prefill_e2e(K, w, qs, ks, vs, anchors, ws, stream, steps, 1, world, dev)
+    clocks.end()
+    res["e2e"]["dense_ms_per_stack"] = res["dense_ms_per_stack"]
+    rank = int(os.environ.get("RANK", "0"))
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = time_oracle_prefill(w, [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])],
+                                                  n_units=2 * (os.cpu_count() or 1))
+    del qs, ks, vs
     torch.cuda.empty_cache()
     return res, launches, ms_k, (anchor_ms, f_anchor, reuse_ms, f_reuse, tf_sust, src)
+
+
+def stacked_layers(w, dev):
+    """The workload's layers stacked into [L, ...] tensors (a step's host
+    copies are then single transfers)."""
+    import torch
+    from long_context_anchor_gb300.workloads import layers as gen_layers
+    B, Hq, Hkv, N, d, L = w.batch, w.n_q_heads, w.n_kv_heads, w.kv_len, w.head_dim, w.n_layers
+    q_all = torch.empty(L, B, Hq, d, dtype=torch.bfloat16, device=dev)
+    k_all = torch.empty(L, B, Hkv, N, d, dtype=torch.bfloat16, device=dev)
+    v_all = torch.empty(L, B, Hkv, N, d, dtype=torch.bfloat16, device=dev)
+    for l, (q, k, v) in enumerate(gen_layers(w, device=dev)):
+        q_all[l].copy_(q)
+        k_all[l].copy_(k)
+        v_all[l].copy_(v)
+        del q, k, v
+    return q_all, k_all, v_all
 
 
 def run_decode_long(args, dev, world, stream, clocks):
     """Decode stack of the gpt-oss-20b-like attention shape (24 layers, 64/8
     heads, d=64, B=4, N=131072, k=8192, anchors every 3rd): Kascade vs the
-    library's own dense decode, per-layer CUDA events, union bytes."""
+    library's own dense decode, per-layer CUDA events, union bytes, the
+    reuse kernel's roofline, an end-to-end pass with host buffers and the
+    oracle on a sample."""
     import torch
     import torch.distributed as dist
     from long_context_anchor_gb300 import configs
     from long_context_anchor_gb300 import kascade as K
-    from long_context_anchor_gb300.workloads import make_layers
     w = configs.GPTOSS_DECODE_128K
     L = w.n_layers
-    qs, ks, vs = make_layers(w, device=dev)
-    outs = [torch.empty_like(q) for q in qs]
+    q_all, k_all, v_all = stacked_layers(w, dev)
+    qs, ks, vs = list(q_all), list(k_all), list(v_all)
+    out_all = torch.empty_like(q_all)
+    outs = list(out_all)
     idx_buf = torch.empty(w.batch, w.n_q_heads, w.topk, dtype=torch.int32, device=dev)
     ws = K.Workspace(dev)
     anchors = list(w.anchors)
@@ -474,7 +760,8 @@ def run_decode_long(args, dev, world, stream, clocks):
     for i, a_ in enumerate(anchors):
         nxt = anchors[i + 1] if i + 1 < len(anchors) else L
         seg += [reuse_b[i]] * (nxt - a_ - 1)
-    reuse_gbs = statistics.mean(seg) / (reuse_ms * 1e-3) / 1e9
+    reuse_bytes = statistics.mean(seg)
+    reuse_gbs = reuse_bytes / (reuse_ms * 1e-3) / 1e9
     hbm_peak, _, src = load_peaks()
     res = {
         "workload": w.name, "layers": L, "batch": w.batch, "q_heads": w.n_q_heads,
@@ -488,9 +775,25 @@ def run_decode_long(args, dev, world, stream, clocks):
         "dense_hbm_gbs": round(dense_b / (ms_d / L * 1e-3) / 1e9, 1),
         "reuse_union_rows_per_layer": int(statistics.mean(unions)),
         "peak_hbm_gbs": hbm_peak, "peak_source": src,
+        # the reuse-layer union gather: 16 of the 24 launches' layers, the
+        # largest share of the Kascade stack's time
+        "roofline": {"kernel": "k_decode_union_bf16 (reuse layer)", "bound": "hbm",
+                     "achieved": round(reuse_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(reuse_gbs / hbm_peak, 4),
+                     "traffic": TRAFFIC.get("k_decode_union_bf16_long"),
+                     "algorithmic_bytes": int(reuse_bytes), "peak_source": src},
     }
     launches = args.steps * (3 * len(anchors) + len(reuse_layers))
-    del qs, ks, vs, outs
+    res["gpu_launches"] = launches
+    clocks.begin()
+    res["e2e"] = decode_e2e(K, w, q_all, k_all, v_all, out_all, anchors, idx_buf, ws, stream,
+                            args.steps, args.warmup, world, dev)
+    clocks.end()
+    rank = int(os.environ.get("RANK", "0"))
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
+        res["cpu_baseline"] = time_oracle(w, lay01, n_groups=os.cpu_count() or 1, reps=1)
+    del qs, ks, vs, outs, q_all, k_all, v_all, out_all
     torch.cuda.empty_cache()
     return res, launches
 
@@ -500,7 +803,6 @@ def run_ours(args):
     import torch.distributed as dist
     from long_context_anchor_gb300 import configs
     from long_context_anchor_gb300 import kascade as K
-    from long_context_anchor_gb300.workloads import layers as gen_layers
 
     rank, world, local = dist_env()
     torch.cuda.set_device(local)
@@ -510,15 +812,7 @@ def run_ours(args):
     w = configs.LLAMA8B_DECODE_32K
     L, B, Hq, Hkv, N, d = w.n_layers, w.batch, w.n_q_heads, w.n_kv_heads, w.kv_len, w.head_dim
     # Inputs resident in HBM, stacked so a step's host copies are single transfers.
-    q_all = torch.empty(L, B, Hq, d, dtype=torch.bfloat16, device=dev)
-    k_all = torch.empty(L, B, Hkv, N, d, dtype=torch.bfloat16, device=dev)
-    v_all = torch.empty(L, B, Hkv, N, d, dtype=torch.bfloat16, device=dev)
-    keep01 = []
-    for l, (q, k, v) in enumerate(gen_layers(w, device=dev)):
-        q_all[l].copy_(q)
-        k_all[l].copy_(k)
-        v_all[l].copy_(v)
-        del q, k, v
+    q_all, k_all, v_all = stacked_layers(w, dev)
     qs, ks, vs = list(q_all), list(k_all), list(v_all)
     out_all = torch.empty_like(q_all)
     outs = list(out_all)
@@ -628,95 +922,25 @@ def run_ours(args):
                    "peak_hbm_gbs": hbm_peak, "peak_source": peak_src},
         "gpu_launches": launches_per_step * args.steps,
     }
-    # Dominant kernel: the reuse-layer union-gather kernel (one launch per
-    # reuse layer) or the anchor layer, whichever holds more of the step.
-    if len(reuse_layers) * reuse_ms >= len(anchors) * anchor_ms:
-        result["roofline"] = {"kernel": "k_decode_union_bf16 (reuse layer)", "bound": "hbm",
-                              "achieved": round(reuse_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
-                              "frac": round(reuse_gbs / hbm_peak, 4),
-                              "traffic": TRAFFIC["k_decode_union_bf16"],
-                              "algorithmic_bytes": int(reuse_bytes_mean),
-                              "peak_source": peak_src}
-    else:
-        result["roofline"] = {"kernel": "anchor layer (k_decode_dense_bf16 + k_topk + plan)",
-                              "bound": "hbm", "achieved": round(anchor_gbs, 1), "peak": hbm_peak,
-                              "unit": "GB/s", "frac": round(anchor_gbs / hbm_peak, 4),
-                              "traffic": None, "algorithmic_bytes": int(anchor_bytes_mean),
-                              "peak_source": peak_src}
+    # Dominant kernel of the headline decode step: the reuse-layer union
+    # gather (24 launches per step, 1.9 ms of the 3.6 ms step; the anchor
+    # layers' dense read with the logit spill takes 8 launches).
+    result["roofline"] = {"kernel": "k_decode_union_bf16 (reuse layer)", "bound": "hbm",
+                          "achieved": round(reuse_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                          "frac": round(reuse_gbs / hbm_peak, 4),
+                          "traffic": TRAFFIC["k_decode_union_bf16"],
+                          "algorithmic_bytes": int(reuse_bytes_mean),
+                          "peak_source": peak_src}
+    result["roofline_decode_anchor_layer"] = {
+        "kernel": "anchor layer (k_decode_dense_bf16 with logit spill + k_topk + plan)",
+        "bound": "hbm", "achieved": round(anchor_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+        "frac": round(anchor_gbs / hbm_peak, 4), "traffic": None,
+        "algorithmic_bytes": int(anchor_bytes_mean), "peak_source": peak_src}
 
-    # End to end through the public API with host buffers: each step copies
-    # every layer's new query and the newest K/V row (position N-1) from
-    # pinned host memory, runs the stack and reads all outputs back. The
-    # copies run on a second stream into two sets of device staging buffers,
-    # so step s+1's inputs travel while step s computes and step s's outputs
-    # travel while step s+1 computes; every step's own copies stay inside the
-    # timed region (the first upload and the last download are not hidden).
-    q_host = q_all.cpu().pin_memory()
-    knew_host = k_all[:, :, :, N - 1].contiguous().cpu().pin_memory()
-    vnew_host = v_all[:, :, :, N - 1].contiguous().cpu().pin_memory()
-    out_host = [torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory() for _ in range(2)]
-    copy_stream = torch.cuda.Stream(device=dev)
-    q_stage = [torch.empty_like(q_all) for _ in range(2)]
-    kn_stage = [torch.empty(knew_host.shape, dtype=knew_host.dtype, device=dev) for _ in range(2)]
-    vn_stage = [torch.empty(vnew_host.shape, dtype=vnew_host.dtype, device=dev) for _ in range(2)]
-    out_stage = [torch.empty_like(out_all) for _ in range(2)]
-    up_done = [torch.cuda.Event() for _ in range(2)]
-    step_done = [torch.cuda.Event() for _ in range(2)]
-    down_done = [torch.cuda.Event() for _ in range(2)]
-    slot_used = [False, False]
-
-    def upload(slot):
-        with torch.cuda.stream(copy_stream):
-            if slot_used[slot]:
-                copy_stream.wait_event(down_done[slot])   # the slot's previous step is done
-            q_stage[slot].copy_(q_host, non_blocking=True)
-            kn_stage[slot].copy_(knew_host, non_blocking=True)
-            vn_stage[slot].copy_(vnew_host, non_blocking=True)
-            up_done[slot].record(copy_stream)
-        slot_used[slot] = True
-
-    def compute(slot):
-        stream.wait_event(up_done[slot])
-        k_all[:, :, :, N - 1].copy_(kn_stage[slot])
-        v_all[:, :, :, N - 1].copy_(vn_stage[slot])
-        K.run_stack(K.DECODE, list(q_stage[slot]), ks, vs, w.topk, anchors,
-                    outs=list(out_stage[slot]), idx_buf=idx_buf, ws=ws)
-        step_done[slot].record(stream)
-
-    def download(slot):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(step_done[slot])
-            out_host[slot].copy_(out_stage[slot], non_blocking=True)
-            down_done[slot].record(copy_stream)
-
-    def e2e_run(steps):
-        upload(0)
-        for st in range(steps):
-            if st + 1 < steps:
-                upload((st + 1) % 2)
-            compute(st % 2)
-            download(st % 2)
-        stream.wait_event(down_done[(steps - 1) % 2])
-
-    e2e_run(args.warmup)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    copy_stream.wait_event(e0)
-    e2e_run(args.steps)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    # the outputs that came back are the stack's outputs for these inputs
-    assert torch.equal(out_host[(args.steps - 1) % 2], out_stage[(args.steps - 1) % 2].cpu())
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    e2e_ms = max_over_ranks([e2e_ms], world, dev)[0]
-    result["e2e"] = {"value": round(1e3 * e2e_ms / L, 3), "unit": UNIT,
-                     "h2d_bytes_per_step": int(q_host.numel() * 2 + 2 * knew_host.numel() * 2),
-                     "d2h_bytes_per_step": int(out_host[0].numel() * 2),
-                     "copies": "second stream, double-buffered staging; D2D scatter of the new K/V rows per step"}
+    clocks.begin()
+    result["e2e"] = decode_e2e(K, w, q_all, k_all, v_all, out_all, anchors, idx_buf, ws, stream,
+                               args.steps, args.warmup, world, dev)
+    clocks.end()
     # GQA-pooled index sets (one per KV head) on the same resident inputs.
     if not args.no_pooled:
         idx_pool = torch.empty(B, Hkv, w.topk, dtype=torch.int32, device=dev)
@@ -749,34 +973,26 @@ def run_ours(args):
             "reuse_bytes_per_layer": int(pr_b), "anchor_bytes_per_layer": int(pa_b),
             "anchor_hbm_gbs": round(pa_b / (anchor_p * 1e-3) / 1e9, 1)}
         result["gpu_launches_decode_pooled"] = args.steps * (5 * len(anchors) + len(reuse_layers))
-    # Prefill stack (same step): Llama-3.1-8B shape at N = 16384.
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
+        result["cpu_baseline"] = time_oracle(w, lay01, n_groups=os.cpu_count() or 1, reps=2)
+    del qs, ks, vs, outs, q_all, k_all, v_all, out_all, idx_buf, ws
+    torch.cuda.empty_cache()
+    # Prefill stack: Llama-3.1-8B shape at N = 16384.
     if not args.no_prefill:
-        pre, pre_launches, pre_ms, (pa_ms, pa_f, pr_ms, pr_f, tf_sust, tsrc) = \
-            run_prefill(args, dev, world, stream, clocks)
+        pre, pre_launches, pre_ms, _ = run_prefill(args, dev, world, stream, clocks)
         result["prefill"] = pre
         result["gpu_launches_prefill"] = pre_launches
         result["ms_per_step_prefill"] = round(pre_ms, 3)
-        pr_tf = pr_f / (pr_ms * 1e-3) / 1e12
-        result["roofline_prefill_reuse"] = {
-            "kernel": "k_prefill_fa2<reuse> (reuse layer)", "bound": "tensor",
-            "achieved": round(pr_tf, 1), "peak": tf_sust, "unit": "TFLOP/s",
-            "frac": round(pr_tf / tf_sust, 4), "traffic": TRAFFIC["k_prefill_fa2_reuse"],
-            "algorithmic_flops": int(pr_f),
-            "peak_source": tsrc + " (sustained)"}
-        # The step's dominant single-launch kernel by total time.
-        dec_reuse_total = len(reuse_layers) * reuse_ms
-        pre_reuse_total = (w.n_layers - len(anchors)) * pr_ms
-        if pre_reuse_total > dec_reuse_total:
-            result["roofline_decode_reuse"] = result["roofline"]
-            result["roofline"] = result["roofline_prefill_reuse"]
     if not args.no_long_decode:
         long_res, long_launches = run_decode_long(args, dev, world, stream, clocks)
         result["decode_long"] = long_res
         result["gpu_launches_decode_long"] = long_launches
+    # Schedule sweep: DP anchors from calibration, then decode B16 and
+    # prefill at three lengths against the library's own dense kernels.
+    if not args.no_sweep:
+        result["sweep"] = run_sweep(args, clocks=clocks, world=world, dev=dev)
     result["clocks"] = clocks.stop()
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
-        result["cpu_baseline"] = time_oracle(w, lay01, n_groups=os.cpu_count() or 1, reps=2)
     if world > 1:
         dist.destroy_process_group()
     return result if rank == 0 else None
@@ -812,45 +1028,49 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
 
 
-def run_sweep(args):
-    """Schedule sweep: the DP picks the anchors from calibration on synthetic
-    sequences, then decode and prefill stacks run with those anchors against
-    the library's own dense kernels on the same inputs."""
+def run_sweep(args, clocks=None, world=1, dev=None):
+    """Schedule sweep (the 32-layer 8B shape): the DP picks six anchors from
+    calibration on four synthetic sequences (overlap similarity, and the
+    mass-recall similarity beside it), then the decode stack at batch 16 and
+    the prefill stack at N = 4096, 16384 and 65536 run with those anchors
+    against the library's own dense kernels on the same inputs."""
     import torch
     from long_context_anchor_gb300 import configs
     from long_context_anchor_gb300 import kascade as K
     from long_context_anchor_gb300.schedule_file import objective as schedule_objective
     from long_context_anchor_gb300.schedule_file import save_schedule
     from long_context_anchor_gb300.workloads import make_layers
-    dev = torch.device("cuda", 0)
+    dev = dev if dev is not None else torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
-    res = {"impl": "ours", "mode": "sweep", "metric": METRIC, "data": "synthetic", "dtype": "bf16"}
+    res = {"data": "synthetic", "dtype": "bf16"}
     # 1. calibration + DP
     wc = configs.SWEEP_CALIBRATION
     qs, ks, vs = make_layers(wc, device=dev)
+    torch.cuda.synchronize()
     t0 = time.perf_counter()
     sim, _ = K.calibrate(qs, ks, vs, wc.topk)
     t_cal = time.perf_counter() - t0
-    anchors, obj = K.schedule_anchors(sim, configs.SWEEP_N_ANCHORS)
-    uniform = list(range(0, wc.n_layers, wc.n_layers // configs.SWEEP_N_ANCHORS))[:configs.SWEEP_N_ANCHORS]
+    m = configs.SWEEP_N_ANCHORS
+    anchors, obj = K.schedule_anchors(sim, m)
+    L = wc.n_layers
+    uniform = list(range(0, L, L // m))[:m]
     # the same DP on the attention-mass-recall similarity
     t0 = time.perf_counter()
     rsim, _ = K.calibrate(qs, ks, vs, wc.topk, similarity="recall")
     t_rcal = time.perf_counter() - t0
-    r_anchors, r_obj = K.schedule_anchors(rsim, configs.SWEEP_N_ANCHORS)
-    L = wc.n_layers
+    r_anchors, r_obj = K.schedule_anchors(rsim, m)
     res["calibration"] = {"workload": wc.name, "seconds": round(t_cal, 3), "anchors": anchors,
                           "objective": round(obj, 4),
                           "uniform_anchors": uniform,
-                          "uniform_objective": round(schedule_objective(sim, uniform), 4),
+                          "uniform_objective": round(schedule_objective(uniform, sim), 4),
                           "sim_adjacent_mean": round(float(np.mean([sim[i][i + 1] for i in range(L - 1)])), 4)}
     # mean share of each layer's exact attention mass kept by the set it
     # reuses, under each schedule (the recall objective / L)
     res["calibration_recall"] = {
         "seconds": round(t_rcal, 3), "anchors": r_anchors, "objective": round(r_obj, 4),
         "mass_kept_recall_anchors": round(r_obj / L, 4),
-        "mass_kept_overlap_anchors": round(schedule_objective(rsim, anchors) / L, 4),
-        "mass_kept_uniform_anchors": round(schedule_objective(rsim, uniform) / L, 4),
+        "mass_kept_overlap_anchors": round(schedule_objective(anchors, rsim) / L, 4),
+        "mass_kept_uniform_anchors": round(schedule_objective(uniform, rsim) / L, 4),
         "mass_kept_own_topk_mean": round(float(np.mean([rsim[l][l] for l in range(L)])), 4)}
     if args.save_schedule:
         meta = {"workload": wc.name, "topk": wc.topk, "batch": wc.batch, "kv_len": wc.kv_len,
@@ -868,39 +1088,46 @@ def run_sweep(args):
         for _ in range(warm):
             K.run_stack(mode, qs, ks, vs, topk, anch, outs=outs, ws=ws)
         torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        if clocks is not None:
+            clocks.begin()
         e0.record(stream)
         for _ in range(steps):
             K.run_stack(mode, qs, ks, vs, topk, anch, outs=outs, ws=ws)
         e1.record(stream)
         torch.cuda.synchronize()
+        if clocks is not None:
+            clocks.end()
         assert ws.device_error() == K.OK
-        return e0.elapsed_time(e1) / steps
+        return max_over_ranks([e0.elapsed_time(e1) / steps], world, dev)[0]
 
     # 2. decode, batch 16, N = 32768
     wd = configs.SWEEP_DECODE
     qs, ks, vs = make_layers(wd, device=dev)
-    ms_k = time_stack(K.DECODE, qs, ks, vs, wd.topk, anchors, args.steps, args.warmup)
-    ms_d = time_stack(K.DECODE, qs, ks, vs, wd.topk, [], args.steps, args.warmup)
-    res["decode"] = {"workload": wd.name, "kascade_us_per_layer": round(1e3 * ms_k / wd.n_layers, 2),
+    warm = max(3, args.warmup)
+    ms_k = time_stack(K.DECODE, qs, ks, vs, wd.topk, anchors, args.steps, warm)
+    ms_d = time_stack(K.DECODE, qs, ks, vs, wd.topk, [], args.steps, warm)
+    res["decode"] = {"workload": wd.name, "anchors": anchors, "steps": args.steps,
+                     "kascade_us_per_layer": round(1e3 * ms_k / wd.n_layers, 2),
                      "dense_us_per_layer": round(1e3 * ms_d / wd.n_layers, 2),
                      "speedup_vs_own_dense": round(ms_d / ms_k, 3)}
     del qs, ks, vs
     torch.cuda.empty_cache()
-    # 3. prefill at three lengths
+    # 3. prefill at three lengths (fewer steps as N grows)
     res["prefill"] = []
     for n in configs.SWEEP_PREFILL_LENGTHS:
-        wp = configs.LLAMA8B_PREFILL_16K.with_(name="llama8b_prefill_n%d_k%d" % (n, n // 8),
-                                              kv_len=n, topk=n // 8, rho_range=(0.7, 0.95),
-                                              seed=3004 + n)
+        wp = configs.sweep_prefill(n)
         qs, ks, vs = make_layers(wp, device=dev)
-        steps = max(1, args.steps // 4)
+        steps = max(2, args.steps * 4096 // (4 * n))
         ms_k = time_stack(K.PREFILL, qs, ks, vs, wp.topk, anchors, steps, 1)
         ms_d = time_stack(K.PREFILL, qs, ks, vs, wp.topk, [], steps, 1)
         f_dense, f_anchor, f_reuse = prefill_flops(wp)
         flops_k = len(anchors) * f_anchor + (wp.n_layers - len(anchors)) * f_reuse
-        res["prefill"].append({"workload": wp.name, "kascade_ms_per_stack": round(ms_k, 2),
+        res["prefill"].append({"workload": wp.name, "steps": steps,
+                               "kascade_ms_per_stack": round(ms_k, 2),
                                "dense_ms_per_stack": round(ms_d, 2),
                                "speedup_vs_own_dense": round(ms_d / ms_k, 3),
                                "kascade_tflops": round(flops_k / (ms_k * 1e-3) / 1e12, 1),
@@ -923,14 +1150,18 @@ def main():
     ap.add_argument("--no-pooled", action="store_true",
                     help="skip the decode stack with GQA-pooled index sets")
     ap.add_argument("--sweep", action="store_true",
-                    help="schedule sweep: DP anchors from calibration, decode and prefill vs dense")
+                    help="only the schedule sweep: DP anchors from calibration, decode and "
+                         "prefill vs dense")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the schedule sweep leg of the default run")
     ap.add_argument("--save-schedule", default="",
                     help="with --sweep: write the DP schedules (overlap, and recall beside it) as JSON")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     if args.sweep:
-        res = run_sweep(args)
+        res = {"impl": "ours", "mode": "sweep", "metric": METRIC}
+        res.update(run_sweep(args))
     else:
         res = run_reference(args) if args.impl == "reference" else run_ours(args)
     if res is not None:

@@ -758,14 +758,18 @@ int decode_chunk_dense(int units, int N) {
 
 // Key-range chunks of the reuse decode: R keys (multiple of 32, at most
 // kPlanCap so a chunk's union fits the shared staging area), about four
-// waves of CTAs over 152 SMs x 2.
+// waves of CTAs over 152 SMs x 2, and at most kMaxSplits chunks per (sequence,
+// KV head) (the split merge holds that many partials): few units on long
+// rows take longer chunks, up to N = kMaxSplits * kPlanCap.
 int decode_union_range(int units, int N) {
   int s = (kUnionTargetCtas + units - 1) / units;
   if (s < 1) s = 1;
   int R = (N + s - 1) / s;
   R = (R + 31) & ~31;
-  if (R > kPlanCap) R = kPlanCap;
   if (R < 256) R = 256;
+  const int r_min = ((N + kMaxSplits - 1) / kMaxSplits + 31) & ~31;
+  if (R < r_min) R = r_min;
+  if (R > kPlanCap) R = kPlanCap;
   return R;
 }
 int decode_union_chunks(int units, int N) {

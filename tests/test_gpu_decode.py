@@ -279,6 +279,28 @@ def test_full_size_decode_sampled(K, cfg):
         check_out(outs[1][b, h], o1_ref, what=("reuse out", b, h))
 
 
+@pytest.mark.parametrize("shape", [(1, 64, 8, 131072, 64, 8192), (1, 32, 8, 65536, 128, 8192),
+                                   (2, 8, 1, 200000, 64, 4096)])
+def test_few_units_long_rows(K, shape):
+    """Few (sequence, KV head) units over a long cache: the reuse kernel takes
+    long key-range chunks (its split limit), the dense kernel long splits. The
+    anchor layer against the oracle (output, bit-exact Top-k on its own
+    logits, sets by the near-tie rule), the reuse layer on the oracle's sets."""
+    B, Hq, Hkv, N, d, k = shape
+    q, kk, v = _rand_layer(B, Hq, Hkv, N, d, torch.bfloat16, seed=N + d)
+    out, idx, s_gpu = K.anchor_decode(q, kk, v, k, return_scores=True)
+    o_ref, idx_ref, s_ref = A.anchor_decode(f64(q), f64(kk), f64(v), k)
+    check_out(out, o_ref)
+    got, s_np = idx.cpu().numpy(), s_gpu.cpu().numpy()
+    for b in range(B):
+        for h in range(Hq):
+            check_topk_exact(got[b, h], s_np[b, h], k, what=("top-k", b, h))
+            check_index_set(got[b, h], s_ref[b, h], k, what=("set", b, h))
+    q2, k2, v2 = _rand_layer(B, Hq, Hkv, N, d, torch.bfloat16, seed=N + d + 1)
+    out_r = K.reuse_decode(q2, k2, v2, _dev_idx(idx_ref))
+    check_out(out_r, A.sparse_decode(f64(q2), f64(k2), f64(v2), idx_ref))
+
+
 def test_workspace_shared_across_shapes_and_entry_points(K):
     """One workspace serves calls of different shapes and the overlap kernel;
     the split counters they rely on must survive every other call's writes."""
