@@ -181,6 +181,57 @@ kascade_status kascade_dense_decode_noalloc(const kascade_desc* desc, const void
  * The paper has no counterpart to this entry point. Allocates nothing. */
 kascade_status kascade_noalloc_device_error(void* stream);
 
+/* ------------------------------------------ sequence-sharded anchor decode -- */
+/* Context-parallel form of the anchor decode layer (Methodology 2: exact
+ * attention, then an exact per-head Top-k), for a KV cache split along the
+ * key axis into S contiguous shards in key order (the pages run on one
+ * device and do not shard a sequence). Each shard runs
+ * kascade_anchor_decode_shard on its own keys; one exchange of its partials
+ * (an all-gather across the devices holding the shards) and
+ * kascade_merge_decode_shards give the exact layer output and the exact
+ * global Top-k: every key of the global Top-k is among its own shard's
+ * Top-k, and the merge applies the same rule (larger logit first, lower
+ * global position on ties) to the union. Per query head sets only
+ * (index_mode 0); pooled mode returns KASCADE_ERR_UNSUPPORTED. */
+
+/* One shard: desc->kv_len = N_s, this shard's keys; k, v [B,Hkv,N_s,d] hold
+ * global positions key_offset .. key_offset + N_s - 1 (key_offset >= 0,
+ * key_offset + N_s < 2^31); 1 <= topk <= N_s. Writes
+ *   out         [B,Hq,d] (desc dtype): attention over the shard's keys only;
+ *   lse_out     [B,Hq] fp32: log sum_j exp(s_j) over the shard, s_j = sigma q.k_j;
+ *   cand_idx    [B,Hq,topk] int32: the shard's Top-k as global positions,
+ *               ascending;
+ *   cand_scores [B,Hq,topk] fp32: the logits s_j at those positions (the same
+ *               fp32 values the unsharded anchor layer ranks).
+ * ws: kascade_workspace_size(desc, topk, KASCADE_DECODE) bytes, as for
+ * kascade_anchor_decode. */
+kascade_status kascade_anchor_decode_shard(const kascade_desc* desc, const void* q,
+                                           const void* k, const void* v, int32_t key_offset,
+                                           int32_t topk, void* out, float* lse_out,
+                                           int32_t* cand_idx, float* cand_scores, void* ws,
+                                           size_t ws_bytes, void* stream);
+
+/* Bytes of workspace kascade_merge_decode_shards needs (0 for an invalid
+ * descriptor or sizes). */
+size_t kascade_merge_workspace_size(const kascade_desc* desc, int32_t n_shards, int32_t topk);
+
+/* Merge of n_shards (1..1024) shards' partials, shard s holding keys before
+ * those of shard s + 1: desc describes the whole layer (kv_len = N, the
+ * total keys; B, Hq, head_dim, dtype as the shards'). Inputs, device,
+ * stacked over shards in key order: outs [S,B,Hq,d] (desc dtype), lses
+ * [S,B,Hq] fp32, cand_idx [S,B,Hq,topk] int32, cand_scores [S,B,Hq,topk]
+ * fp32, as kascade_anchor_decode_shard wrote them (S*topk < 2^24). Writes
+ *   out     [B,Hq,d]: sum_s exp(lse_s - LSE) o_s, LSE = log sum_s exp(lse_s);
+ *   idx_out [B,Hq,topk]: the global Top-k, ascending positions.
+ * Candidates out of [0, N) or not ascending across the shards (shards out of
+ * order), and NaN logits, set KASCADE_ERR_BAD_INPUT on the device (read with
+ * kascade_device_error). */
+kascade_status kascade_merge_decode_shards(const kascade_desc* desc, int32_t n_shards,
+                                           const void* outs, const float* lses,
+                                           const int32_t* cand_idx, const float* cand_scores,
+                                           int32_t topk, void* out, int32_t* idx_out, void* ws,
+                                           size_t ws_bytes, void* stream);
+
 /* --------------------------------------------------------------- prefill -- */
 
 /* Causal exact attention (the library's own dense baseline), bf16 only. */

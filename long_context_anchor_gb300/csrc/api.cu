@@ -379,6 +379,84 @@ kascade_status kascade_topk(const float* scores, int32_t rows, int32_t n, int32_
 
 }  // extern "C"
 
+// ------------------------------------------- sequence-sharded anchor decode --
+extern "C" {
+
+kascade_status kascade_anchor_decode_shard(const kascade_desc* desc, const void* q,
+                                           const void* k, const void* v, int32_t key_offset,
+                                           int32_t topk, void* out, float* lse_out,
+                                           int32_t* cand_idx, float* cand_scores, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  Shape s;
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if (s.pooled) return KASCADE_ERR_UNSUPPORTED;
+  if ((r = check_decode_ptrs(q, k, v, out)) != KASCADE_OK) return r;
+  if (topk < 1 || topk > s.N || key_offset < 0 ||
+      static_cast<long long>(key_offset) + s.N > 0x7fffffffll)
+    return KASCADE_ERR_INVALID_ARG;
+  if (!aligned16(lse_out) || !aligned16(cand_idx) || !aligned16(cand_scores))
+    return KASCADE_ERR_INVALID_ARG;
+  Layout L;
+  if ((r = check_ws(s, topk, KASCADE_DECODE, ws, ws_bytes, L)) != KASCADE_OK) return r;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the shard's own anchor layer: exact output, logits in the workspace spill,
+  // local Top-k in cand_idx
+  r = run_anchor_decode(s, q, k, v, topk, out, cand_idx, nullptr, ws, L, st);
+  if (r != KASCADE_OK) return r;
+  const int rows = s.B * s.Hq;
+  // the split partials are free once the attention kernel is done: they hold
+  // the row statistics (max, 1/sum exp) of the logits
+  float2* stat = at<float2>(ws, L.part);
+  const float* spill = at<float>(ws, L.spill);
+  if (launch_row_stat(spill, rows, s.N, stat, st) != cudaSuccess) return KASCADE_ERR_CUDA;
+  return cuda_status(launch_shard_finish(spill, stat, rows, s.N, topk, key_offset, lse_out,
+                                         cand_idx, cand_scores, st));
+}
+
+size_t kascade_merge_workspace_size(const kascade_desc* desc, int32_t n_shards, int32_t topk) {
+  Shape s;
+  if (check_desc(desc, s) != KASCADE_OK || n_shards < 1 || topk < 1) return 0;
+  const size_t rows = static_cast<size_t>(s.B) * s.Hq;
+  return kWsStateBytes + align256(rows * n_shards * topk * 4) + align256(rows * topk * 4);
+}
+
+kascade_status kascade_merge_decode_shards(const kascade_desc* desc, int32_t n_shards,
+                                           const void* outs, const float* lses,
+                                           const int32_t* cand_idx, const float* cand_scores,
+                                           int32_t topk, void* out, int32_t* idx_out, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  Shape s;
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if (s.pooled) return KASCADE_ERR_UNSUPPORTED;
+  if (n_shards < 1 || n_shards > kMaxShards || topk < 1 || topk > s.N ||
+      static_cast<long long>(n_shards) * topk >= (1ll << 24))
+    return KASCADE_ERR_INVALID_ARG;
+  if (!aligned16(outs) || !aligned16(lses) || !aligned16(cand_idx) || !aligned16(cand_scores) ||
+      !aligned16(out) || !aligned16(idx_out))
+    return KASCADE_ERR_INVALID_ARG;
+  const size_t need = kascade_merge_workspace_size(desc, n_shards, topk);
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || ws_bytes < need)
+    return KASCADE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int rows = s.B * s.Hq;
+  const int n = n_shards * topk;
+  float* scores = at<float>(ws, kWsStateBytes);
+  int32_t* pos = at<int32_t>(ws, kWsStateBytes + align256(static_cast<size_t>(rows) * n * 4));
+  unsigned int* err = at<unsigned int>(ws, 0);
+  if ((r = cuda_status(launch_merge_out(outs, lses, n_shards, rows, s.d, s.dtype, out, st))) !=
+      KASCADE_OK)
+    return r;
+  if ((r = cuda_status(launch_merge_scores(cand_idx, cand_scores, n_shards, rows, topk, s.N,
+                                           scores, err, st))) != KASCADE_OK)
+    return r;
+  if ((r = run_topk_rows(scores, rows, n, topk, pos, err, st)) != KASCADE_OK) return r;
+  return cuda_status(launch_merge_emit(pos, cand_idx, rows, topk, idx_out, st));
+}
+
+}  // extern "C"
+
 // ------------------------------------------------------ prefill dispatch --
 namespace kascade {
 namespace {

@@ -32,6 +32,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 constexpr int kMaxQHeads = 256;
 constexpr int kMaxSplits = 128;
+constexpr int kMaxShards = 1024;   // shards one merge call takes
 
 // One decode attention layer (dense, anchor or reuse).
 struct DecodeArgs {
@@ -148,6 +149,23 @@ cudaError_t launch_mass_recall(const float* spill, const float2* row_stat, const
                                float* part, unsigned int* err, cudaStream_t st);
 cudaError_t launch_recall_reduce(const float* part, int n_layers, int rows, double* sim,
                                  cudaStream_t st);
+
+// shard.cu — sequence-sharded anchor decode. A shard's partials: lse_out[r]
+// from row_stat (max, 1/sum exp), and the local Top-k in cand_idx turned into
+// global positions (+ offset) with their logits from the spill [rows][n_s].
+cudaError_t launch_shard_finish(const float* spill, const float2* row_stat, int rows, int n_s,
+                                int topk, int offset, float* lse_out, int32_t* cand_idx,
+                                float* cand_scores, cudaStream_t st);
+// Merge of S shards' partials (outs [S][rows][d] of dtype, lses [S][rows]).
+cudaError_t launch_merge_out(const void* outs, const float* lses, int n_shards, int rows, int d,
+                             int dtype, void* out, cudaStream_t st);
+// scores [rows][S*topk] from cand_scores [S][rows][topk]; checks cand_idx.
+cudaError_t launch_merge_scores(const int32_t* cand_idx, const float* cand_scores, int n_shards,
+                                int rows, int topk, int n_total, float* scores,
+                                unsigned int* err, cudaStream_t st);
+// idx_out[r][i] = cand_idx of candidate pos[r][i] (a position in the row above).
+cudaError_t launch_merge_emit(const int32_t* pos, const int32_t* cand_idx, int rows, int topk,
+                              int32_t* idx_out, cudaStream_t st);
 
 // overlap.cu
 cudaError_t launch_layer_overlap(const int32_t* sets, int L, int units, int topk, int n_bits,

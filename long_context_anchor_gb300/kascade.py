@@ -50,6 +50,11 @@ _SIGS = {
     "kascade_topk": (ctypes.c_int, [_vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "kascade_dense_decode_noalloc": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp]),
     "kascade_noalloc_device_error": (ctypes.c_int, [_vp]),
+    "kascade_anchor_decode_shard": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp,
+                                                   _vp, _vp, _sz, _vp]),
+    "kascade_merge_workspace_size": (_sz, [_DP, _i32, _i32]),
+    "kascade_merge_decode_shards": (ctypes.c_int, [_DP, _i32, _vp, _vp, _vp, _vp, _i32, _vp, _vp,
+                                                   _vp, _sz, _vp]),
     "kascade_dense_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kascade_anchor_prefill": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _sz,
                                               _vp]),
@@ -332,6 +337,67 @@ def reuse_decode(q, k, v, idx, group_map=None, scale=None, out=None, ws=None, st
                                      _ptr(idx), _ptr(out), _ptr(buf), buf.numel(), _stream(stream)),
            "kascade_reuse_decode")
     return out
+
+
+def anchor_decode_shard(q, k, v, key_offset, topk, group_map=None, scale=None, ws=None,
+                        stream=None):
+    """One shard of a KV cache split along the key axis: k/v [B,Hkv,N_s,d] hold
+    global positions key_offset .. key_offset + N_s - 1. Returns the shard's
+    partials (out [B,Hq,d], lse [B,Hq] fp32, cand_idx [B,Hq,topk] int32 global
+    positions ascending, cand_scores [B,Hq,topk] fp32 logits)."""
+    B, Hq, _, N, _ = _attn_inputs(q, k, v, prefill=False)
+    _same_cuda_device([("q", q), ("k", k), ("v", v)])
+    if not (1 <= int(topk) <= N) or int(key_offset) < 0:
+        raise ValueError("topk must lie in [1, N_s] and key_offset must be >= 0")
+    desc = decode_desc(q, k, group_map, scale)
+    out = torch.empty_like(q)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    cand_idx = torch.empty(B, Hq, topk, dtype=torch.int32, device=q.device)
+    cand_scores = torch.empty(B, Hq, topk, dtype=torch.float32, device=q.device)
+    ws, buf = _ws(ws, q.device, workspace_size(desc, topk, DECODE), stream)
+    _check(_lib.kascade_anchor_decode_shard(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v),
+                                            int(key_offset), int(topk), _ptr(out), _ptr(lse),
+                                            _ptr(cand_idx), _ptr(cand_scores), _ptr(buf),
+                                            buf.numel(), _stream(stream)),
+           "kascade_anchor_decode_shard")
+    return out, lse, cand_idx, cand_scores
+
+
+def merge_decode_shards(outs, lses, cand_idx, cand_scores, n_kv_heads=None, kv_len=None,
+                        ws=None, stream=None):
+    """Merge S shards' partials stacked in key order: outs [S,B,Hq,d], lses
+    [S,B,Hq] fp32, cand_idx [S,B,Hq,topk] int32, cand_scores [S,B,Hq,topk]
+    fp32. Returns (out [B,Hq,d], idx [B,Hq,topk] ascending global positions).
+    kv_len (the total keys, for the range check of the candidates) defaults
+    to the largest candidate position + 1; n_kv_heads to Hq (the merge does
+    not read K or V)."""
+    if not isinstance(outs, torch.Tensor) or outs.dim() != 4:
+        raise ValueError("outs: expected a tensor [S,B,Hq,d]")
+    S, B, Hq, d = outs.shape
+    if not isinstance(cand_idx, torch.Tensor) or cand_idx.dim() != 4:
+        raise ValueError("cand_idx: expected an int32 tensor [S,B,Hq,topk]")
+    topk = cand_idx.shape[-1]
+    _expect(lses, "lses", (S, B, Hq), torch.float32)
+    _expect(cand_idx, "cand_idx", (S, B, Hq, topk), torch.int32)
+    _expect(cand_scores, "cand_scores", (S, B, Hq, topk), torch.float32)
+    _expect(outs, "outs", (S, B, Hq, d), outs.dtype)
+    _same_cuda_device([("outs", outs), ("lses", lses), ("cand_idx", cand_idx),
+                       ("cand_scores", cand_scores)])
+    if kv_len is None:
+        kv_len = int(cand_idx.max().item()) + 1
+    hkv = Hq if n_kv_heads is None else int(n_kv_heads)
+    desc = make_desc(B, Hq, hkv, d, int(kv_len), _dtype_code(outs))
+    out = torch.empty(B, Hq, d, dtype=outs.dtype, device=outs.device)
+    idx = torch.empty(B, Hq, topk, dtype=torch.int32, device=outs.device)
+    n = _lib.kascade_merge_workspace_size(ctypes.byref(desc), int(S), int(topk))
+    if n == 0:
+        raise KascadeError(INVALID_ARG, "kascade_merge_workspace_size")
+    ws, buf = _ws(ws, outs.device, n, stream)
+    _check(_lib.kascade_merge_decode_shards(ctypes.byref(desc), int(S), _ptr(outs), _ptr(lses),
+                                            _ptr(cand_idx), _ptr(cand_scores), int(topk),
+                                            _ptr(out), _ptr(idx), _ptr(buf), buf.numel(),
+                                            _stream(stream)), "kascade_merge_decode_shards")
+    return out, idx
 
 
 def topk(scores, k, out=None, ws=None, stream=None):
