@@ -104,6 +104,8 @@ inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<
 // Workspace layout; offsets in bytes from the workspace base.
 struct Layout {
   size_t counters, part, spill, plan, plan_count;   // decode
+  size_t bracket, fcount, flist;                    // decode, fused anchor Top-k
+  int fcap;
   size_t row_stat, pool;                            // decode, pooled sets
   size_t lse, w, w_pool;                            // prefill (w_pool: pooled sets)
   size_t total;
@@ -123,6 +125,18 @@ Layout layout(const Shape& s, int topk, int mode) {
     off = align256(off + static_cast<size_t>(s.B) * s.Hkv * chunks * kPlanCapEntries * 4);
     L.plan_count = off;
     off = align256(off + static_cast<size_t>(s.B) * s.Hkv * chunks * 4);
+    if (!s.pooled && s.dtype == KASCADE_BF16) {
+      // fused anchor Top-k: per logit row a bracket, a list length and a
+      // list of (key, position) pairs
+      const size_t rows = static_cast<size_t>(s.B) * s.Hq;
+      L.fcap = fused_list_cap(s.N, topk);
+      L.bracket = off;
+      off = align256(off + rows * 8);
+      L.fcount = off;
+      off = align256(off + rows * 4);
+      L.flist = off;
+      off = align256(off + rows * static_cast<size_t>(L.fcap) * 8);
+    }
     if (s.pooled) {
       L.row_stat = off;
       off = align256(off + static_cast<size_t>(s.B) * s.Hq * 8);
@@ -239,6 +253,43 @@ kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, c
     return run_topk_rows(pool, s.B * s.Hkv, s.N, topk, idx_out, at<unsigned int>(ws, 0), st);
   }
   float* spill = scores_out ? scores_out : at<float>(ws, L.spill);
+  if (s.dtype == KASCADE_BF16 && topk < s.N) {
+    // fused: a sample bracket per row, then the attention kernel files every
+    // logit at or above the bracket's lower end while it spills, and the
+    // selection reads those lists instead of the rows
+    uint2* bracket = at<uint2>(ws, L.bracket);
+    unsigned int* fcount = at<unsigned int>(ws, L.fcount);
+    uint2* flist = at<uint2>(ws, L.flist);
+    kascade_status r = cuda_status(launch_anchor_bracket(q, k, s.head_kv, s.B, s.Hq, s.Hkv, s.N,
+                                                         s.d, topk, s.scale, bracket, fcount, st));
+    if (r != KASCADE_OK) return r;
+    DecodeArgs a;
+    fill_decode_args(a, s, q, k, v, out, ws, L, topk);
+    a.spill = spill;
+    a.bracket = bracket;
+    a.fcount = fcount;
+    a.flist = flist;
+    a.fcap = L.fcap;
+    a.chunk = decode_chunk_dense(s.B * s.Hkv, s.N);
+    a.S = (s.N + a.chunk - 1) / a.chunk;
+    r = cuda_status(launch_decode_dense_bf16(a, s.d, true, st, true));
+    if (r != KASCADE_OK) return r;
+    TopkArgs t{};
+    t.scores = spill;
+    t.idx_out = idx_out;
+    t.err = at<unsigned int>(ws, 0);
+    t.rows = s.B * s.Hq;
+    t.n = s.N;
+    t.k = topk;
+    t.k_stride = topk;
+    t.tile = 128;
+    t.bracket = bracket;
+    t.fcount = fcount;
+    t.flist = flist;
+    t.fcap = L.fcap;
+    const cudaError_t e = launch_topk(t, st);
+    return e == cudaErrorNotSupported ? KASCADE_ERR_UNSUPPORTED : cuda_status(e);
+  }
   kascade_status r = run_dense_decode(s, q, k, v, out, ws, L, topk, spill, st);
   if (r != KASCADE_OK) return r;
   return run_topk_rows(spill, s.B * s.Hq, s.N, topk, idx_out, at<unsigned int>(ws, 0), st);

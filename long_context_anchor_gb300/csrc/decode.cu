@@ -269,7 +269,19 @@ __device__ void finish_cta(const DecodeArgs& a, WarpState<D>& st, int cw, int n_
 // ------------------------------------------------------------------------
 // Dense / anchor decode, TMA producer warp + NW consumer warps.
 // ------------------------------------------------------------------------
-template <int D, int NW, int STAGES, bool SPILL>
+// Fused anchor decode: a spilled logit v of row `row` whose order-preserving
+// key is >= t_lo joins the row's candidate list (key, position).
+__device__ __forceinline__ void filter_append(const DecodeArgs& a, bool ok, float v,
+                                              uint32_t t_lo, int row, int pos) {
+  const uint32_t key = float_key_fast(v);
+  if (ok && key >= t_lo) {
+    const unsigned int p = atomicAdd(a.fcount + row, 1u);
+    if (p < static_cast<unsigned int>(a.fcap))
+      a.flist[static_cast<size_t>(row) * a.fcap + p] = make_uint2(key, static_cast<uint32_t>(pos));
+  }
+}
+
+template <int D, int NW, int STAGES, bool SPILL, bool FILTER>
 __global__ void __launch_bounds__((NW + 1) * 32)
     k_decode_dense_bf16(const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV,
@@ -338,11 +350,18 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     const bool hv0 = 2 * c4 < a.G, hv1 = 2 * c4 + 1 < a.G;
     float* sp0 = nullptr;
     float* sp1 = nullptr;
+    const int row_h0 = hv0 ? b * a.Hq + a.heads[g * a.G + 2 * c4] : 0;
+    const int row_h1 = hv1 ? b * a.Hq + a.heads[g * a.G + 2 * c4 + 1] : 0;
     if (SPILL) {
-      if (hv0) sp0 = a.spill + (static_cast<size_t>(b) * a.Hq + a.heads[g * a.G + 2 * c4]) * a.N;
-      if (hv1)
-        sp1 = a.spill + (static_cast<size_t>(b) * a.Hq + a.heads[g * a.G + 2 * c4 + 1]) * a.N;
+      if (hv0) sp0 = a.spill + static_cast<size_t>(row_h0) * a.N;
+      if (hv1) sp1 = a.spill + static_cast<size_t>(row_h1) * a.N;
     }
+    uint32_t tlo0 = 0xFFFFFFFFu, tlo1 = 0xFFFFFFFFu;
+    if (FILTER) {
+      if (hv0) tlo0 = a.bracket[row_h0].x;
+      if (hv1) tlo1 = a.bracket[row_h1].x;
+    }
+    bool fbad = false;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % STAGES;
       if (!mbar_wait(&full[s], (t / STAGES) & 1, a.err, 0x103)) break;
@@ -351,13 +370,25 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       const int key0 = n0 + t * TK + row0 + gid, key1 = key0 + 8;
       const bool kv0 = key0 < n1, kv1 = key1 < n1;
       if (SPILL) {
+        const float v0 = sc[0] * a.scale, v1 = sc[1] * a.scale;
+        const float v2 = sc[2] * a.scale, v3 = sc[3] * a.scale;
         if (kv0) {
-          if (hv0) sp0[key0] = sc[0] * a.scale;
-          if (hv1) sp1[key0] = sc[1] * a.scale;
+          if (hv0) sp0[key0] = v0;
+          if (hv1) sp1[key0] = v1;
         }
         if (kv1) {
-          if (hv0) sp0[key1] = sc[2] * a.scale;
-          if (hv1) sp1[key1] = sc[3] * a.scale;
+          if (hv0) sp0[key1] = v2;
+          if (hv1) sp1[key1] = v3;
+        }
+        if (FILTER) {
+          // the same fp32 values the spill holds, so the selection made from
+          // the lists equals the one made from the spill
+          fbad |= (kv0 && ((hv0 && v0 != v0) || (hv1 && v1 != v1))) ||
+                  (kv1 && ((hv0 && v2 != v2) || (hv1 && v3 != v3)));
+          filter_append(a, kv0 && hv0, v0, tlo0, row_h0, key0);
+          filter_append(a, kv0 && hv1, v1, tlo1, row_h1, key0);
+          filter_append(a, kv1 && hv0, v2, tlo0, row_h0, key1);
+          filter_append(a, kv1 && hv1, v3, tlo1, row_h1, key1);
         }
       }
       float x[4];
@@ -369,6 +400,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
+    // a NaN logit: the selection from the lists would not see it
+    if (FILTER && __any_sync(0xffffffffu, fbad) && lane == 0)
+      report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x104);
   }
   __syncthreads();
   finish_cta<D>(a, st, warp < NW ? warp : -1, NW, reinterpret_cast<float*>(smem), b, g, split);
@@ -679,7 +713,7 @@ __global__ void k_decode_generic_f32(const __grid_constant__ DecodeArgs a, int D
   }
 }
 
-template <int D, int NW, int STAGES, bool SPILL>
+template <int D, int NW, int STAGES, bool SPILL, bool FILTER>
 cudaError_t launch_dense_t(const DecodeArgs& a, cudaStream_t st) {
   constexpr int TK = 16 * NW;
   alignas(64) CUtensorMap tk, tv;
@@ -688,7 +722,7 @@ cudaError_t launch_dense_t(const DecodeArgs& a, cudaStream_t st) {
   if (!encode_tmap_2d_bf16(&tv, a.v, D, rows, 64, TK, true)) return cudaErrorInvalidValue;
   constexpr int TILE_BYTES = (D / 64) * TK * 128;
   const size_t smem = 1024 + 2 * STAGES * TILE_BYTES + 2 * STAGES * 8;
-  auto kern = k_decode_dense_bf16<D, NW, STAGES, SPILL>;
+  auto kern = k_decode_dense_bf16<D, NW, STAGES, SPILL, FILTER>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -778,17 +812,20 @@ int decode_union_chunks(int units, int N) {
 }
 
 cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spill,
-                                     cudaStream_t st) {
+                                     cudaStream_t st, bool filter) {
+  if (filter && !spill) return cudaErrorInvalidValue;
   if (head_dim == 128)
     // two 32 KB stages: 64 KB, three CTAs per SM (three stages at two per SM
     // were 2% slower)
-    return spill ? launch_dense_t<128, kDenseNW, 2, true>(a, st)
-                 : launch_dense_t<128, kDenseNW, 2, false>(a, st);
+    return filter  ? launch_dense_t<128, kDenseNW, 2, true, true>(a, st)
+           : spill ? launch_dense_t<128, kDenseNW, 2, true, false>(a, st)
+                   : launch_dense_t<128, kDenseNW, 2, false, false>(a, st);
   if (head_dim == 64)
     // four 16 KB stages: 64 KB, three CTAs per SM (six stages, two per SM, were
     // 4% slower on 131072-key rows)
-    return spill ? launch_dense_t<64, kDenseNW, 4, true>(a, st)
-                 : launch_dense_t<64, kDenseNW, 4, false>(a, st);
+    return filter  ? launch_dense_t<64, kDenseNW, 4, true, true>(a, st)
+           : spill ? launch_dense_t<64, kDenseNW, 4, true, false>(a, st)
+                   : launch_dense_t<64, kDenseNW, 4, false, false>(a, st);
   return cudaErrorInvalidValue;
 }
 

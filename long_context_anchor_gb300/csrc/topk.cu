@@ -24,6 +24,7 @@
 // Prefill rows are the packed tile weights of one (sequence, head, tile):
 // length L_t = min(N, 128(t+1)), k_t = min(k, L_t), -1 padding after k_t.
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 
 #include "common.cuh"
 #include "internal.h"
@@ -261,6 +262,75 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__
     s_ncand = 0;
     s_nabove = 0;
   }
+  const int warp = tid >> 5;
+  int c_gt = 0;
+  bool bad = false;
+  bool fused_ok = false;
+  if (a.flist != nullptr) {
+    // ---- fused anchor decode: select from the list the attention kernel
+    // wrote (every key >= t_lo of the row) instead of reading the row. Keys
+    // above t_hi are selected outright; the k-th key is found among those in
+    // [t_lo, t_hi] (candidates, shared memory). Any miss (list overflow, the
+    // k-th key outside the bracket, too many candidates) takes the full path
+    // below over the row itself.
+    __shared__ int s_fa, s_fc;
+    if (tid == 0) {
+      s_fa = 0;
+      s_fc = 0;
+    }
+    __syncthreads();
+    const unsigned int cnt = a.fcount[r];
+    const uint2 br = a.bracket[r];
+    if (cnt <= static_cast<unsigned int>(a.fcap)) {
+      const uint2* list = a.flist + static_cast<size_t>(r) * a.fcap;
+      int my_above = 0;
+      for (int e = tid; e < static_cast<int>(cnt); e += kThreads) {
+        const uint2 kp = list[e];
+        const int p = static_cast<int>(kp.y);
+        if (kp.x > br.y) {
+          atomicOr(&above[p >> 5], 1u << (p & 31));
+          ++my_above;
+        } else {
+          const int slot = atomicAdd(&s_fc, 1);
+          if (slot < cand_cap) {
+            cand_key[slot] = kp.x;
+            cand_pos[slot] = p;
+          }
+        }
+      }
+      if (my_above) atomicAdd(&s_fa, my_above);
+      __syncthreads();
+      const int n_above = s_fa, n_mid = s_fc;
+      if (n_mid <= cand_cap && n_above < rd.k && n_above + n_mid >= rd.k) {
+        __shared__ int s_fpre[kWarps + 1];
+        for (int w = tid; w <= kWarps; w += kThreads) s_fpre[w] = w == 0 ? 0 : n_mid;
+        __syncthreads();
+        uint32_t T;
+        int cg;
+        // one flat list (list 0 holds every candidate)
+        select_rank_warp_lists<NT>(cand_key, s_fpre, n_mid, cand_cap, br.x, br.y - br.x,
+                                   rd.k - n_above, hist, warp_tot, &s_bin, &s_above, T, cg);
+        c_gt = n_above + cg;
+        for (int i = tid; i < n_mid; i += kThreads) {
+          const uint32_t key = cand_key[i];
+          const int p = cand_pos[i];
+          if (key > T) atomicOr(&above[p >> 5], 1u << (p & 31));
+          else if (key == T) atomicOr(&eqbm[p >> 5], 1u << (p & 31));
+        }
+        fused_ok = true;
+      }
+    }
+    __syncthreads();
+    if (!fused_ok) {
+      for (int w = tid; w < W; w += kThreads) above[w] = 0u;
+      if (tid == 0) {
+        s_ncand = 0;
+        s_nabove = 0;
+      }
+    }
+    __syncthreads();
+  }
+  if (!fused_ok) {
 
   // ---- 1. bracket the k-th key from an evenly spaced sample -------------
   const int S = min(rd.len, max(2048, min(kSampleCap, rd.len / 16)));
@@ -304,12 +374,10 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__
   // ---- 2. one pass: "above" bitmap by ballot, candidates in [t_lo, t_hi] --
   // Each warp owns blocks of 32*UNROLL consecutive positions and appends its
   // candidates to its own shared list (count kept in a register).
-  const int warp = tid >> 5;
   uint32_t* wkey = cand_key + warp * warp_cap;
   int32_t* wpos = cand_pos + warp * warp_cap;
   const uint32_t span = t_hi - t_lo;
   int wcount = 0, my_above = 0;
-  bool bad = false;
   // the next block's scores are loaded before this block is processed
   float xn[UNROLL];
   {
@@ -361,7 +429,6 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__
   for (int w = 0; w < kWarps; ++w) n_cand += s_wcount[w];
   const int n_above = s_nabove;
   const bool overflow = s_ncand != 0;
-  int c_gt;
   if (!overflow && n_above < rd.k && n_above + n_cand >= rd.k) {
     // ---- 3. exact k-th key among the candidates -------------------------
     uint32_t T;
@@ -418,6 +485,7 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__
     });
     __syncthreads();
   }
+  }   // full path
 
   // ---- 4. ordered emission ----------------------------------------------
   const int need_eq = rd.k - c_gt;
@@ -450,7 +518,110 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__
   for (int j = rd.k + tid; j < a.k_stride; j += kThreads) out[j] = -1;
 }
 
+// ------------------------------------------------------------------------
+// Fused anchor decode, step 1: the sample bracket of every logit row, taken
+// before the attention kernel so that it can file each row's candidates as
+// it computes the logits. Row r = (b, h): the same evenly spaced sample of
+// the row as k_topk's (runs of 32 keys), its logits sigma q.k computed here
+// (fp32; only the bracket depends on them, the selection is made on the
+// attention kernel's own values), and the same two sample quantiles.
+// ------------------------------------------------------------------------
+struct BracketArgs {
+  const __nv_bfloat16* q;   // [B,Hq,D]
+  const __nv_bfloat16* k;   // [B,Hkv,N,D]
+  uint2* bracket;           // [B*Hq]
+  unsigned int* fcount;     // [B*Hq]
+  int Hq, Hkv, N, topk;
+  float scale;
+  int16_t head_kv[kMaxQHeads];
+};
+
+constexpr int kBrThreads = 512;
+
+template <int D>
+__global__ void __launch_bounds__(kBrThreads) k_anchor_bracket(const __grid_constant__ BracketArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  extern __shared__ uint32_t sm[];
+  uint32_t* hist = sm;            // [2][2048]
+  uint32_t* samp = sm + 4096;     // [kSampleCap]
+  __shared__ float qs[D];
+  __shared__ int warp_tot[32];
+  __shared__ int s_bin, s_above;
+  const int r = blockIdx.x, tid = threadIdx.x;
+  const int b = r / a.Hq, h = r % a.Hq, g = a.head_kv[h];
+  const int len = a.N, k = min(a.topk, a.N);
+  if (tid == 0) a.fcount[r] = 0u;
+  if (k >= len) {   // every key is selected (k_topk returns early)
+    if (tid == 0) a.bracket[r] = make_uint2(0u, 0xFFFFFFFFu);
+    return;
+  }
+  for (int c = tid; c < D; c += kBrThreads)
+    qs[c] = __bfloat162float(a.q[(static_cast<size_t>(b) * a.Hq + h) * D + c]);
+  __syncthreads();
+  const int S = min(len, max(2048, min(kSampleCap, len / 16)));
+  const int runs = S / 32;
+  const float step = static_cast<float>(len - 32) / static_cast<float>(max(runs - 1, 1));
+  const __nv_bfloat16* kb = a.k + (static_cast<size_t>(b) * a.Hkv + g) * a.N * D;
+  for (int u = tid; u < S; u += kBrThreads) {
+    const int j = min(len - 1, __float2int_rd(static_cast<float>(u >> 5) * step) + (u & 31));
+    const uint4* row = reinterpret_cast<const uint4*>(kb + static_cast<size_t>(j) * D);
+    float acc = 0.f;
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 w = __ldg(row + c);
+      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&wv[e]);
+        const float2 f = __bfloat1622float2(p2);
+        acc = fmaf(f.x, qs[8 * c + 2 * e], acc);
+        acc = fmaf(f.y, qs[8 * c + 2 * e + 1], acc);
+      }
+    }
+    samp[u] = float_key(acc * a.scale);
+  }
+  __syncthreads();
+  const float rc = static_cast<float>(k) * S / len;   // expected sample rank
+  const float margin = 4.f * sqrtf(rc) + 16.f;
+  const int r_hi = static_cast<int>(floorf(rc - margin));
+  const int r_lo = static_cast<int>(ceilf(rc + margin));
+  uint32_t p_hi, p_lo;
+  sample_bracket<kBrThreads>(samp, S, max(r_hi, 1), min(r_lo, S), hist, warp_tot, &s_bin,
+                             &s_above, p_hi, p_lo);
+  if (tid == 0) {
+    const uint32_t t_hi = r_hi >= 1 ? ((p_hi << 10) | 1023u) : 0xFFFFFFFFu;
+    const uint32_t t_lo = r_lo <= S ? (p_lo << 10) : 0u;
+    a.bracket[r] = make_uint2(t_lo, t_hi);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_anchor_bracket(const void* q, const void* k, const int16_t* head_kv, int B,
+                                  int Hq, int Hkv, int N, int d, int topk, float scale,
+                                  uint2* bracket, unsigned int* fcount, cudaStream_t st) {
+  const int rows = B * Hq;
+  if (rows <= 0) return cudaSuccess;
+  BracketArgs a;
+  a.q = static_cast<const __nv_bfloat16*>(q);
+  a.k = static_cast<const __nv_bfloat16*>(k);
+  a.bracket = bracket;
+  a.fcount = fcount;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.N = N;
+  a.topk = topk;
+  a.scale = scale;
+  for (int h = 0; h < Hq; ++h) a.head_kv[h] = head_kv[h];
+  const size_t smem = (4096 + kSampleCap) * sizeof(uint32_t);
+  auto kern = d == 128 ? k_anchor_bracket<128> : k_anchor_bracket<64>;
+  if (d != 128 && d != 64) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(rows), dim3(kBrThreads), smem, st, a);
+}
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   if (a.rows <= 0) return cudaSuccess;

@@ -301,6 +301,50 @@ def test_few_units_long_rows(K, shape):
     check_out(out_r, A.sparse_decode(f64(q2), f64(k2), f64(v2), idx_ref))
 
 
+@pytest.mark.parametrize("kind", ["equal", "ties", "sampled_heavy", "nan"])
+def test_fused_anchor_topk_fallbacks(K, kind):
+    """The anchor decode selects from the candidate lists its attention kernel
+    files against a sample bracket; rows where the bracket misses take the
+    full selection over the spilled logits. Every case must still equal the
+    selection rule on the kernel's own fp32 logits: all logits equal (the
+    lists overflow), a few distinct logits (heavy ties), heavy keys planted
+    only where the sample looks (fewer than k keys reach the bracket), and a
+    NaN key row (reported as bad input)."""
+    B, Hq, Hkv, N, d, k = 2, 8, 2, 32768, 128, 256
+    q, kk, v = _rand_layer(B, Hq, Hkv, N, d, torch.bfloat16, seed=61)
+    if kind == "equal":
+        q = torch.zeros_like(q)
+    elif kind == "ties":
+        rows = kk[:, :, :3].clone()
+        kk = rows[:, :, torch.arange(N, device=DEV) % 3].contiguous()
+    elif kind == "sampled_heavy":
+        # the sample takes 64 evenly spaced runs of 32 keys (about 520 apart):
+        # 100 heavy keys at the starts of 20 runs fill its top ranks, so its
+        # bracket sits above all but about 100 keys of the row
+        pos = torch.tensor([int(i * (N - 32) / 63) + e for i in range(20) for e in range(5)],
+                           device=DEV)
+        qd = q.float() / q.float().norm(dim=-1, keepdim=True)
+        for b in range(B):
+            for g in range(Hkv):
+                u = qd[b, 4 * g:4 * g + 4].sum(0)
+                kk[b, g, pos] = (6.0 * u / u.norm()).to(kk.dtype)
+    elif kind == "nan":
+        kk[1, 0, 777] = float("nan")
+    ws = K.Workspace(DEV)
+    out, idx, s_gpu = K.anchor_decode(q, kk, v, k, return_scores=True, ws=ws)
+    if kind == "nan":
+        assert ws.device_error() == K.BAD_INPUT
+        return
+    assert ws.device_error() == K.OK
+    got, s_np = idx.cpu().numpy(), s_gpu.cpu().numpy()
+    for b in range(B):
+        for h in range(Hq):
+            check_topk_exact(got[b, h], s_np[b, h], k, what=(kind, b, h))
+    if kind == "equal":
+        assert (got == np.arange(k)).all()
+    check_out(out, A.dense_decode(f64(q), f64(kk), f64(v))[0])
+
+
 def test_workspace_shared_across_shapes_and_entry_points(K):
     """One workspace serves calls of different shapes and the overlap kernel;
     the split counters they rely on must survive every other call's writes."""
