@@ -674,6 +674,43 @@ def run_prefill(args, dev, world, stream, clocks):
     return res, launches, ms_k, (anchor_ms, f_anchor, reuse_ms, f_reuse, tf_sust, src)
 
 
+def time_anchor_layers(K, w, qs, ks, vs, ws, stream, reps, fused):
+    """Mean CUDA-event time (us) of one anchor decode layer, taken over the
+    workload's anchor layers in turn (each layer's K/V exceeds L2), with the
+    two-kernel kascade_anchor_decode or the fused kascade_anchor_decode_fused."""
+    import torch
+    anchors = list(w.anchors)
+    idx = torch.empty(w.batch, w.n_q_heads, w.topk, dtype=torch.int32, device=qs[0].device)
+    out = torch.empty_like(qs[0])
+    for a_ in anchors[:2]:
+        K.anchor_decode(qs[a_], ks[a_], vs[a_], w.topk, out=out, idx=idx, ws=ws, fused=fused)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    n = 0
+    for _ in range(reps):
+        for a_ in anchors:
+            K.anchor_decode(qs[a_], ks[a_], vs[a_], w.topk, out=out, idx=idx, ws=ws, fused=fused)
+            n += 1
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert ws.device_error() == K.OK
+    return 1e3 * e0.elapsed_time(e1) / n
+
+
+def fused_anchor_block(K, w, qs, ks, vs, ws, stream, reps, dense_us):
+    """The anchor decode layer alone, two-kernel against fused (NEXT #2)."""
+    two = time_anchor_layers(K, w, qs, ks, vs, ws, stream, reps, False)
+    fused = time_anchor_layers(K, w, qs, ks, vs, ws, stream, reps, True)
+    return {"anchor_layer_us_two_kernel": round(two, 2), "anchor_layer_us_fused": round(fused, 2),
+            "fused_over_two_kernel": round(fused / two, 3),
+            "anchor_over_dense_layer": round(two / dense_us, 3),
+            "note": "kascade_anchor_decode (attention with logit spill, then Top-k) against "
+                    "kascade_anchor_decode_fused (sample bracket, attention filing candidate "
+                    "lists, selection from the lists); identical outputs"}
+
+
 def stacked_layers(w, dev):
     """The workload's layers stacked into [L, ...] tensors (a step's host
     copies are then single transfers)."""
@@ -788,6 +825,8 @@ def run_decode_long(args, dev, world, stream, clocks):
     clocks.begin()
     res["e2e"] = decode_e2e(K, w, q_all, k_all, v_all, out_all, anchors, idx_buf, ws, stream,
                             args.steps, args.warmup, world, dev)
+    res["fused_anchor"] = fused_anchor_block(K, w, qs, ks, vs, ws, stream, max(2, args.steps // 4),
+                                             1e3 * ms_d / L)
     clocks.end()
     rank = int(os.environ.get("RANK", "0"))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -940,6 +979,9 @@ def run_ours(args):
     clocks.begin()
     result["e2e"] = decode_e2e(K, w, q_all, k_all, v_all, out_all, anchors, idx_buf, ws, stream,
                                args.steps, args.warmup, world, dev)
+    result["decode"]["fused_anchor"] = fused_anchor_block(K, w, qs, ks, vs, ws, stream,
+                                                          max(2, args.steps // 4),
+                                                          1e3 * ms_dense / L)
     clocks.end()
     # GQA-pooled index sets (one per KV head) on the same resident inputs.
     if not args.no_pooled:

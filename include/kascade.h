@@ -140,6 +140,24 @@ kascade_status kascade_anchor_decode(const kascade_desc* desc, const void* q, co
                                      const void* v, int32_t topk, void* out, int32_t* idx_out,
                                      float* scores_out, void* ws, size_t ws_bytes, void* stream);
 
+/* The anchor layer of kascade_anchor_decode (bf16, per query head sets; other
+ * modes return KASCADE_ERR_UNSUPPORTED) with the Top-k fused into the
+ * attention kernel (the survey's "fused score spill" with a threshold pass):
+ * a first kernel brackets each row's k-th logit from an evenly spaced sample
+ * of its keys; the attention kernel then files every logit at or above the
+ * bracket's lower end, as (key, position), in per-(row, split, warp) lists
+ * while it spills, and the selection is made from those lists, re-reading a
+ * row's logits only when its bracket missed (all logits equal, heavy ties, an
+ * unrepresentative sample). Outputs and the index sets are identical to
+ * kascade_anchor_decode's (the same fp32 logits under the same rule); on
+ * GB300 the two-kernel kascade_anchor_decode is as fast or faster at the
+ * measured shapes, and kascade_run_stack uses it. Same arguments and
+ * workspace as kascade_anchor_decode. */
+kascade_status kascade_anchor_decode_fused(const kascade_desc* desc, const void* q,
+                                           const void* k, const void* v, int32_t topk, void* out,
+                                           int32_t* idx_out, float* scores_out, void* ws,
+                                           size_t ws_bytes, void* stream);
+
 /* Reuse layer (Methodology 3): out[b,h] = softmax restricted to the saved set
  * S = idx[b,h,:] (topk ascending, distinct positions in [0,N)), computed with
  * this layer's q, k, v. Rows of k and v outside the sets are not read. Query

@@ -104,8 +104,7 @@ inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<
 // Workspace layout; offsets in bytes from the workspace base.
 struct Layout {
   size_t counters, part, spill, plan, plan_count;   // decode
-  size_t bracket, fcount, flist;                    // decode, fused anchor Top-k
-  int fcap;
+  size_t bracket, fcount, flist, fsamp;             // decode, fused anchor Top-k
   size_t row_stat, pool;                            // decode, pooled sets
   size_t lse, w, w_pool;                            // prefill (w_pool: pooled sets)
   size_t total;
@@ -126,16 +125,19 @@ Layout layout(const Shape& s, int topk, int mode) {
     L.plan_count = off;
     off = align256(off + static_cast<size_t>(s.B) * s.Hkv * chunks * 4);
     if (!s.pooled && s.dtype == KASCADE_BF16) {
-      // fused anchor Top-k: per logit row a bracket, a list length and a
-      // list of (key, position) pairs
+      // fused anchor Top-k: per logit row a bracket, and per (row, split,
+      // consumer warp) a sub-list of (key, position) pairs and its length
       const size_t rows = static_cast<size_t>(s.B) * s.Hq;
-      L.fcap = fused_list_cap(s.N, topk);
+      const int chunk = decode_chunk_dense(s.B * s.Hkv, s.N);
+      const int splits = (s.N + chunk - 1) / chunk;
       L.bracket = off;
       off = align256(off + rows * 8);
+      L.fsamp = off;
+      off = align256(off + rows * anchor_sample_stride(s.N) * 4);
       L.fcount = off;
-      off = align256(off + rows * 4);
+      off = align256(off + rows * splits * kDecodeConsumerWarps * 4);
       L.flist = off;
-      off = align256(off + rows * static_cast<size_t>(L.fcap) * 8);
+      off = align256(off + rows * splits * static_cast<size_t>(chunk) * 8);
     }
     if (s.pooled) {
       L.row_stat = off;
@@ -240,7 +242,7 @@ kascade_status run_topk_rows(const float* scores, int rows, int n, int k, int32_
 
 kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, const void* v,
                                  int topk, void* out, int32_t* idx_out, float* scores_out,
-                                 void* ws, const Layout& L, cudaStream_t st) {
+                                 void* ws, const Layout& L, cudaStream_t st, bool fused = false) {
   if (s.pooled) {
     // logits to the workspace, then the group sums of their softmax weights
     float* spill = at<float>(ws, L.spill);
@@ -253,15 +255,16 @@ kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, c
     return run_topk_rows(pool, s.B * s.Hkv, s.N, topk, idx_out, at<unsigned int>(ws, 0), st);
   }
   float* spill = scores_out ? scores_out : at<float>(ws, L.spill);
-  if (s.dtype == KASCADE_BF16 && topk < s.N) {
+  if (fused && topk < s.N) {
     // fused: a sample bracket per row, then the attention kernel files every
     // logit at or above the bracket's lower end while it spills, and the
     // selection reads those lists instead of the rows
     uint2* bracket = at<uint2>(ws, L.bracket);
     unsigned int* fcount = at<unsigned int>(ws, L.fcount);
     uint2* flist = at<uint2>(ws, L.flist);
-    kascade_status r = cuda_status(launch_anchor_bracket(q, k, s.head_kv, s.B, s.Hq, s.Hkv, s.N,
-                                                         s.d, topk, s.scale, bracket, fcount, st));
+    kascade_status r = cuda_status(launch_anchor_bracket(q, k, s.heads, s.B, s.Hq, s.Hkv, s.N,
+                                                         s.d, topk, s.scale,
+                                                         at<uint32_t>(ws, L.fsamp), bracket, st));
     if (r != KASCADE_OK) return r;
     DecodeArgs a;
     fill_decode_args(a, s, q, k, v, out, ws, L, topk);
@@ -269,7 +272,6 @@ kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, c
     a.bracket = bracket;
     a.fcount = fcount;
     a.flist = flist;
-    a.fcap = L.fcap;
     a.chunk = decode_chunk_dense(s.B * s.Hkv, s.N);
     a.S = (s.N + a.chunk - 1) / a.chunk;
     r = cuda_status(launch_decode_dense_bf16(a, s.d, true, st, true));
@@ -286,7 +288,9 @@ kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, c
     t.bracket = bracket;
     t.fcount = fcount;
     t.flist = flist;
-    t.fcap = L.fcap;
+    t.fsplits = a.S;
+    t.fwarps = kDecodeConsumerWarps;
+    t.fchunk = a.chunk;
     const cudaError_t e = launch_topk(t, st);
     return e == cudaErrorNotSupported ? KASCADE_ERR_UNSUPPORTED : cuda_status(e);
   }
@@ -403,6 +407,23 @@ kascade_status kascade_anchor_decode(const kascade_desc* desc, const void* q, co
   if ((r = check_ws(s, topk, KASCADE_DECODE, ws, ws_bytes, L)) != KASCADE_OK) return r;
   return run_anchor_decode(s, q, k, v, topk, out, idx_out, scores_out, ws, L,
                            static_cast<cudaStream_t>(stream));
+}
+
+kascade_status kascade_anchor_decode_fused(const kascade_desc* desc, const void* q,
+                                           const void* k, const void* v, int32_t topk, void* out,
+                                           int32_t* idx_out, float* scores_out, void* ws,
+                                           size_t ws_bytes, void* stream) {
+  Shape s;
+  kascade_status r = check_desc(desc, s);
+  if (r != KASCADE_OK) return r;
+  if (s.pooled || s.dtype != KASCADE_BF16) return KASCADE_ERR_UNSUPPORTED;
+  if ((r = check_decode_ptrs(q, k, v, out)) != KASCADE_OK) return r;
+  if (topk < 1 || topk > s.N || !aligned16(idx_out)) return KASCADE_ERR_INVALID_ARG;
+  if (scores_out != nullptr && !aligned16(scores_out)) return KASCADE_ERR_INVALID_ARG;
+  Layout L;
+  if ((r = check_ws(s, topk, KASCADE_DECODE, ws, ws_bytes, L)) != KASCADE_OK) return r;
+  return run_anchor_decode(s, q, k, v, topk, out, idx_out, scores_out, ws, L,
+                           static_cast<cudaStream_t>(stream), true);
 }
 
 kascade_status kascade_reuse_decode(const kascade_desc* desc, const void* q, const void* k,

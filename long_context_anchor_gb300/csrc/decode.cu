@@ -269,16 +269,14 @@ __device__ void finish_cta(const DecodeArgs& a, WarpState<D>& st, int cw, int n_
 // ------------------------------------------------------------------------
 // Dense / anchor decode, TMA producer warp + NW consumer warps.
 // ------------------------------------------------------------------------
-// Fused anchor decode: a spilled logit v of row `row` whose order-preserving
-// key is >= t_lo joins the row's candidate list (key, position).
-__device__ __forceinline__ void filter_append(const DecodeArgs& a, bool ok, float v,
-                                              uint32_t t_lo, int row, int pos) {
-  const uint32_t key = float_key_fast(v);
-  if (ok && key >= t_lo) {
-    const unsigned int p = atomicAdd(a.fcount + row, 1u);
-    if (p < static_cast<unsigned int>(a.fcap))
-      a.flist[static_cast<size_t>(row) * a.fcap + p] = make_uint2(key, static_cast<uint32_t>(pos));
-  }
+// Fused anchor decode: the lanes of one head (those with the same c4) file
+// the logits of their keys whose order-preserving key is >= t_lo in the
+// warp's own sub-list of the row, at positions from a ballot prefix.
+__device__ __forceinline__ void filter_file(bool in, uint32_t key, int pos, uint32_t group,
+                                            uint32_t below, uint2* list, uint32_t& cnt) {
+  const uint32_t bits = __ballot_sync(0xffffffffu, in) & group;
+  if (in) list[cnt + __popc(bits & below)] = make_uint2(key, static_cast<uint32_t>(pos));
+  cnt += __popc(bits);
 }
 
 template <int D, int NW, int STAGES, bool SPILL, bool FILTER>
@@ -357,9 +355,22 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       if (hv1) sp1 = a.spill + static_cast<size_t>(row_h1) * a.N;
     }
     uint32_t tlo0 = 0xFFFFFFFFu, tlo1 = 0xFFFFFFFFu;
+    uint2* fl0 = nullptr;
+    uint2* fl1 = nullptr;
+    uint32_t fc0 = 0, fc1 = 0;
+    const uint32_t fgroup = 0x11111111u << c4;                 // lanes of this head pair
+    const uint32_t fbelow = fgroup & ((1u << lane) - 1u);
+    const int fsub = (NW > 0) ? a.chunk / NW : 0;               // sub-list capacity
     if (FILTER) {
-      if (hv0) tlo0 = a.bracket[row_h0].x;
-      if (hv1) tlo1 = a.bracket[row_h1].x;
+      const size_t sub = static_cast<size_t>(split) * a.chunk + static_cast<size_t>(warp) * fsub;
+      if (hv0) {
+        tlo0 = a.bracket[row_h0].x;
+        fl0 = a.flist + static_cast<size_t>(row_h0) * a.S * a.chunk + sub;
+      }
+      if (hv1) {
+        tlo1 = a.bracket[row_h1].x;
+        fl1 = a.flist + static_cast<size_t>(row_h1) * a.S * a.chunk + sub;
+      }
     }
     bool fbad = false;
     for (int t = 0; t < ntiles; ++t) {
@@ -385,10 +396,12 @@ __global__ void __launch_bounds__((NW + 1) * 32)
           // the lists equals the one made from the spill
           fbad |= (kv0 && ((hv0 && v0 != v0) || (hv1 && v1 != v1))) ||
                   (kv1 && ((hv0 && v2 != v2) || (hv1 && v3 != v3)));
-          filter_append(a, kv0 && hv0, v0, tlo0, row_h0, key0);
-          filter_append(a, kv0 && hv1, v1, tlo1, row_h1, key0);
-          filter_append(a, kv1 && hv0, v2, tlo0, row_h0, key1);
-          filter_append(a, kv1 && hv1, v3, tlo1, row_h1, key1);
+          const uint32_t f0 = float_key_fast(v0), f1 = float_key_fast(v1);
+          const uint32_t f2 = float_key_fast(v2), f3 = float_key_fast(v3);
+          filter_file(kv0 && hv0 && f0 >= tlo0, f0, key0, fgroup, fbelow, fl0, fc0);
+          filter_file(kv1 && hv0 && f2 >= tlo0, f2, key1, fgroup, fbelow, fl0, fc0);
+          filter_file(kv0 && hv1 && f1 >= tlo1, f1, key0, fgroup, fbelow, fl1, fc1);
+          filter_file(kv1 && hv1 && f3 >= tlo1, f3, key1, fgroup, fbelow, fl1, fc1);
         }
       }
       float x[4];
@@ -400,9 +413,16 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    // a NaN logit: the selection from the lists would not see it
-    if (FILTER && __any_sync(0xffffffffu, fbad) && lane == 0)
-      report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x104);
+    if (FILTER) {
+      // a NaN logit: the selection from the lists would not see it
+      if (__any_sync(0xffffffffu, fbad) && lane == 0)
+        report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x104);
+      // sub-list lengths, one writer per (row, split, warp)
+      if (gid == 0) {
+        if (hv0) a.fcount[(static_cast<size_t>(row_h0) * a.S + split) * NW + warp] = fc0;
+        if (hv1) a.fcount[(static_cast<size_t>(row_h1) * a.S + split) * NW + warp] = fc1;
+      }
+    }
   }
   __syncthreads();
   finish_cta<D>(a, st, warp < NW ? warp : -1, NW, reinterpret_cast<float*>(smem), b, g, split);
@@ -775,7 +795,7 @@ cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
 // Launch shapes: 4 consumer warps (64-key tiles) per CTA. Dense decode runs
 // 152 * 8 split CTAs (three resident per SM, so about 2.7 waves; 152 * 6 and
 // 152 * 12 were both slower); the union gather sizes its CTAs to one wave.
-constexpr int kDenseNW = 4;
+constexpr int kDenseNW = kDecodeConsumerWarps;
 constexpr int kUnionNW = 4;
 constexpr int kTargetCtas = 152 * 2 * 4;
 constexpr int kUnionTargetCtas = 152 * 2 * 4;

@@ -58,12 +58,14 @@ struct DecodeArgs {
   float scale;              // sigma
   float scale_log2;         // sigma * log2(e)
   int16_t heads[kMaxQHeads];  // heads[g*G + slot] = query head of slot in group g
-  // fused anchor decode (launch_decode_dense_bf16 with filter): append every
-  // spilled logit whose key is >= bracket[row].x to the row's list
+  // fused anchor decode (launch_decode_dense_bf16 with filter): every spilled
+  // logit whose key is >= bracket[row].x joins a list. Each (row, split,
+  // consumer warp) owns its own sub-list of chunk/NW entries (one warp sees at
+  // most that many keys of a row), so no atomics are needed: flist
+  // [B*Hq][S][chunk] (key, position), fcount [B*Hq][S][NW] entries written.
   const uint2* bracket;     // [B*Hq] (t_lo, t_hi)
-  unsigned int* fcount;     // [B*Hq] list lengths (zeroed by the bracket kernel)
-  uint2* flist;             // [B*Hq][fcap] (key, position)
-  int fcap;
+  unsigned int* fcount;
+  uint2* flist;
 };
 
 enum DecodeKind { kDense = 0, kAnchor = 1, kSparse = 2 };
@@ -108,30 +110,29 @@ struct TopkArgs {
   int prefill_tiles;       // 0: plain rows [rows, n]; >0: packed triangular tile rows
   int tile;                // prefill tile (128)
   // Fused anchor decode (plain rows only; null when unused): every score of
-  // row r whose key is >= bracket[r].x was appended by the attention kernel
-  // to flist[r * fcap ...] as (key, position), fcount[r] entries in all
-  // (more than fcap: the list overflowed). The selection is then made from
-  // the list; the row itself is read only when the bracket missed.
+  // row r whose key is >= bracket[r].x was filed by the attention kernel as
+  // (key, position) in one of the row's fsplits * fwarps sub-lists of
+  // fchunk / fwarps entries (flist + r * fsplits * fchunk; lengths in fcount
+  // [r][split][warp]). The selection is then made from the lists; the row
+  // itself is read only when the bracket missed.
   const uint2* bracket;    // (t_lo, t_hi) keys per row
   const unsigned int* fcount;
   const uint2* flist;
-  int fcap;
+  int fsplits, fwarps, fchunk;
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
 
 // Sample bracket of every decode logit row for the fused anchor decode:
 // row r = (b, h) takes an evenly spaced sample of its keys (runs of 32),
-// computes sigma q.k for them, and writes (t_lo, t_hi) such that the k-th
-// largest logit lies in [t_lo, t_hi] (order-preserving keys) with high
-// probability; also zeroes fcount[r]. bf16 q [B,Hq,d], k [B,Hkv,N,d].
-cudaError_t launch_anchor_bracket(const void* q, const void* k, const int16_t* head_kv, int B,
+// whose logits sigma q.k land in samp [B*Hq][anchor_sample_stride(N)] (as
+// order-preserving keys), then (t_lo, t_hi) such that the k-th largest logit
+// lies in [t_lo, t_hi] with high probability. bf16 q [B,Hq,d], k
+// [B,Hkv,N,d]; heads[g*G + slot] as in DecodeArgs.
+int anchor_sample_stride(int N);
+cudaError_t launch_anchor_bracket(const void* q, const void* k, const int16_t* heads, int B,
                                   int Hq, int Hkv, int N, int d, int topk, float scale,
-                                  uint2* bracket, unsigned int* fcount, cudaStream_t st);
-// Capacity of one row's candidate list in the fused anchor decode.
-inline int fused_list_cap(int N, int topk) {
-  const long long c = 2ll * topk + 8192;
-  return static_cast<int>(c < N ? c : N);
-}
+                                  uint32_t* samp, uint2* bracket, cudaStream_t st);
+constexpr int kDecodeConsumerWarps = 4;   // consumer warps of the dense decode kernel
 
 // prefill.cu
 struct PrefillArgs {

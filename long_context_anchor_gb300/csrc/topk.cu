@@ -279,22 +279,56 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__
       s_fc = 0;
     }
     __syncthreads();
-    const unsigned int cnt = a.fcount[r];
     const uint2 br = a.bracket[r];
-    if (cnt <= static_cast<unsigned int>(a.fcap)) {
-      const uint2* list = a.flist + static_cast<size_t>(r) * a.fcap;
+    {
+      // the row's sub-lists, one per (split, warp) of the attention kernel,
+      // taken by the warps in turn
+      const int nsub = a.fsplits * a.fwarps;
+      const int cap_sub = a.fchunk / a.fwarps;
+      const uint2* rl = a.flist + static_cast<size_t>(r) * a.fsplits * a.fchunk;
+      const unsigned int* rc = a.fcount + static_cast<size_t>(r) * nsub;
       int my_above = 0;
-      for (int e = tid; e < static_cast<int>(cnt); e += kThreads) {
-        const uint2 kp = list[e];
-        const int p = static_cast<int>(kp.y);
-        if (kp.x > br.y) {
-          atomicOr(&above[p >> 5], 1u << (p & 31));
-          ++my_above;
-        } else {
-          const int slot = atomicAdd(&s_fc, 1);
-          if (slot < cand_cap) {
-            cand_key[slot] = kp.x;
-            cand_pos[slot] = p;
+      // each warp's sub-list lengths in one round of loads (lane i holds the
+      // length of the warp's i-th sub-list), then every sub-list in batches
+      // of 4 entries per lane whose loads are all issued before any use
+      constexpr int kBatch = 4;
+      for (int sub0 = warp; sub0 < nsub; sub0 += 32 * kWarps) {
+        const int my_sub = sub0 + lane * kWarps;
+        const int my_cnt = my_sub < nsub ? min(static_cast<int>(rc[my_sub]), cap_sub) : 0;
+        for (int i = 0; i < 32 && sub0 + i * kWarps < nsub; ++i) {
+          const int sub = sub0 + i * kWarps;
+          const int cnt = __shfl_sync(0xffffffffu, my_cnt, i);
+          const uint2* list = rl + static_cast<size_t>(sub) * cap_sub;
+          for (int e0 = 0; e0 < cnt; e0 += 32 * kBatch) {
+            uint2 kp[kBatch];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+              kp[u] = list[min(e0 + u * 32 + lane, cnt - 1)];
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u) {
+              const bool valid = e0 + u * 32 + lane < cnt;
+              const int p = static_cast<int>(kp[u].y);
+              const bool is_above = valid && kp[u].x > br.y;
+              const bool is_mid = valid && !is_above;
+              if (is_above) {
+                atomicOr(&above[p >> 5], 1u << (p & 31));
+                ++my_above;
+              }
+              // candidates: one slot reservation per warp
+              const unsigned int mm = __ballot_sync(0xffffffffu, is_mid);
+              if (mm != 0u) {
+                int base = 0;
+                if (lane == __ffs(mm) - 1) base = atomicAdd(&s_fc, __popc(mm));
+                base = __shfl_sync(0xffffffffu, base, __ffs(mm) - 1);
+                if (is_mid) {
+                  const int slot = base + __popc(mm & ((1u << lane) - 1u));
+                  if (slot < cand_cap) {
+                    cand_key[slot] = kp[u].x;
+                    cand_pos[slot] = p;
+                  }
+                }
+              }
+            }
           }
         }
       }
@@ -521,106 +555,222 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__
 // ------------------------------------------------------------------------
 // Fused anchor decode, step 1: the sample bracket of every logit row, taken
 // before the attention kernel so that it can file each row's candidates as
-// it computes the logits. Row r = (b, h): the same evenly spaced sample of
-// the row as k_topk's (runs of 32 keys), its logits sigma q.k computed here
-// (fp32; only the bracket depends on them, the selection is made on the
-// attention kernel's own values), and the same two sample quantiles.
+// it computes the logits. The sample is k_topk's: `runs` evenly spaced runs
+// of 32 consecutive keys per row (every key of a row shorter than 2048).
+//   k_anchor_sample : the sample logits sigma q.k of one (sequence, KV head)
+//                     for all G heads of the group at once (each K row read
+//                     once), a few runs per CTA, as order-preserving keys;
+//   k_anchor_bracket: per row, the two sample quantiles -> (t_lo, t_hi).
+// The logits here are fp32 CUDA-core dot products: only the bracket depends
+// on them; the selection is made on the attention kernel's own values.
 // ------------------------------------------------------------------------
-struct BracketArgs {
+struct SampleGeom {
+  int S;        // sample size (a multiple of 32, or the whole row)
+  int runs;     // runs of 32 keys
+  bool whole;   // the whole row is the sample
+  float step;   // run spacing
+};
+
+__host__ __device__ inline SampleGeom sample_geom(int len) {
+  SampleGeom g;
+  g.whole = len < 2048;
+  const int s = len / 16 > 2048 ? len / 16 : 2048;
+  g.S = g.whole ? len : ((s < kSampleCap ? s : kSampleCap) / 32) * 32;
+  g.runs = (g.S + 31) / 32;
+  g.step = g.whole ? 32.f : static_cast<float>(len - 32) / static_cast<float>(g.runs > 1 ? g.runs - 1 : 1);
+  return g;
+}
+
+struct SampleArgs {
   const __nv_bfloat16* q;   // [B,Hq,D]
   const __nv_bfloat16* k;   // [B,Hkv,N,D]
-  uint2* bracket;           // [B*Hq]
-  unsigned int* fcount;     // [B*Hq]
-  int Hq, Hkv, N, topk;
+  uint32_t* samp;           // [B*Hq][S] sample keys
+  int Hq, Hkv, N, S_stride;
   float scale;
-  int16_t head_kv[kMaxQHeads];
+  int16_t heads[kMaxQHeads];   // heads[g*G + slot]
 };
+
+constexpr int kSampWarps = 4, kSampRunsPerWarp = 2;
+
+// One CTA: kSampWarps * kSampRunsPerWarp runs of one (sequence, KV head).
+// A warp reads a run as one contiguous block: lane l holds 16-byte chunk
+// l % CH of key row l / CH of each group of RPI rows (coalesced loads, all
+// issued before the arithmetic); the CH lanes of a row reduce their partial
+// dot products (G heads at once) by shuffles.
+template <int D, int G>
+__global__ void __launch_bounds__(kSampWarps * 32) k_anchor_sample(const __grid_constant__ SampleArgs a) {
+  pdl_wait();
+  pdl_trigger();
+  constexpr int CH = D / 8, RPI = 32 / CH, NI = 32 / RPI;
+  const int unit = blockIdx.y;
+  const int b = unit / a.Hkv, g = unit % a.Hkv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int cc = lane % CH, sub = lane / CH;
+  const int len = a.N;
+  const SampleGeom sg = sample_geom(len);
+  float qv[G][8];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(
+                              a.q + (static_cast<size_t>(b) * a.Hq + a.heads[g * G + h]) * D) + cc);
+    const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(p2[e]);
+      qv[h][2 * e] = f.x;
+      qv[h][2 * e + 1] = f.y;
+    }
+  }
+  const uint4* kb = reinterpret_cast<const uint4*>(a.k + static_cast<size_t>(unit) * a.N * D);
+  const int run0 = (blockIdx.x * kSampWarps + warp) * kSampRunsPerWarp;
+  for (int rr = 0; rr < kSampRunsPerWarp; ++rr) {
+    const int run = run0 + rr;
+    if (run >= sg.runs) break;
+    const int start = sg.whole ? 32 * run : min(len - 32, __float2int_rd(static_cast<float>(run) * sg.step));
+    uint4 w[NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      w[i] = __ldg(kb + static_cast<size_t>(min(start + i * RPI + sub, len - 1)) * CH + cc);
+    // partial dot products over this lane's 8 dimensions, two at a time
+    float part[G][NI];
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const __nv_bfloat162* p2 = reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+      uint64_t f[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(p2[e]);
+        f[e] = f2_pack(x.x, x.y);
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc = f2_fma(f[e], f2_pack(qv[h][2 * e], qv[h][2 * e + 1]), acc);
+        float lo, hi;
+        f2_unpack(acc, lo, hi);
+        part[h][i] = lo + hi;
+      }
+    }
+    // reduce-scatter over the CH lanes of each row: at every step a lane
+    // keeps half of its values and adds the partner's copy of that half, so
+    // after log2(CH) steps lane cc holds the full sum of load i = ri(cc)
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+#pragma unroll
+      for (int half = NI / 2; half >= 1; half >>= 1) {
+        const bool upper = (cc & half) != 0;
+#pragma unroll
+        for (int j = 0; j < half; ++j) {
+          const float send = upper ? part[h][j] : part[h][j + half];
+          const float keep = upper ? part[h][j + half] : part[h][j];
+          part[h][j] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+        }
+      }
+    }
+    // lane cc now owns load index i = cc (the bit of `half` chose the upper
+    // half at each step); its row is start + cc * RPI + sub
+    {
+      const int i = cc;
+      const int u = 32 * run + i * RPI + sub;   // sample slot
+      if (u < sg.S && start + i * RPI + sub < len) {
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+          a.samp[(static_cast<size_t>(b) * a.Hq + a.heads[g * G + h]) * a.S_stride + u] =
+              float_key(part[h][0] * a.scale);
+      }
+    }
+  }
+}
 
 constexpr int kBrThreads = 512;
 
-template <int D>
-__global__ void __launch_bounds__(kBrThreads) k_anchor_bracket(const __grid_constant__ BracketArgs a) {
+// One CTA per row: the two quantiles of its sample keys (as in k_topk).
+__global__ void __launch_bounds__(kBrThreads) k_anchor_bracket(const uint32_t* __restrict__ samp,
+                                                               int S_stride, int N, int topk,
+                                                               uint2* __restrict__ bracket) {
   pdl_wait();
   pdl_trigger();
   extern __shared__ uint32_t sm[];
   uint32_t* hist = sm;            // [2][2048]
-  uint32_t* samp = sm + 4096;     // [kSampleCap]
-  __shared__ float qs[D];
+  uint32_t* ss = sm + 4096;       // [kSampleCap]
   __shared__ int warp_tot[32];
   __shared__ int s_bin, s_above;
   const int r = blockIdx.x, tid = threadIdx.x;
-  const int b = r / a.Hq, h = r % a.Hq, g = a.head_kv[h];
-  const int len = a.N, k = min(a.topk, a.N);
-  if (tid == 0) a.fcount[r] = 0u;
+  const int len = N, k = min(topk, N);
   if (k >= len) {   // every key is selected (k_topk returns early)
-    if (tid == 0) a.bracket[r] = make_uint2(0u, 0xFFFFFFFFu);
+    if (tid == 0) bracket[r] = make_uint2(0u, 0xFFFFFFFFu);
     return;
   }
-  for (int c = tid; c < D; c += kBrThreads)
-    qs[c] = __bfloat162float(a.q[(static_cast<size_t>(b) * a.Hq + h) * D + c]);
-  __syncthreads();
-  const int S = min(len, max(2048, min(kSampleCap, len / 16)));
-  const int runs = S / 32;
-  const float step = static_cast<float>(len - 32) / static_cast<float>(max(runs - 1, 1));
-  const __nv_bfloat16* kb = a.k + (static_cast<size_t>(b) * a.Hkv + g) * a.N * D;
-  for (int u = tid; u < S; u += kBrThreads) {
-    const int j = min(len - 1, __float2int_rd(static_cast<float>(u >> 5) * step) + (u & 31));
-    const uint4* row = reinterpret_cast<const uint4*>(kb + static_cast<size_t>(j) * D);
-    float acc = 0.f;
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const uint4 w = __ldg(row + c);
-      const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162*>(&wv[e]);
-        const float2 f = __bfloat1622float2(p2);
-        acc = fmaf(f.x, qs[8 * c + 2 * e], acc);
-        acc = fmaf(f.y, qs[8 * c + 2 * e + 1], acc);
-      }
-    }
-    samp[u] = float_key(acc * a.scale);
-  }
+  const SampleGeom sg = sample_geom(len);
+  const int S = sg.S;
+  const uint32_t* row = samp + static_cast<size_t>(r) * S_stride;
+  for (int u = tid; u < S; u += kBrThreads) ss[u] = __ldg(row + u);
   __syncthreads();
   const float rc = static_cast<float>(k) * S / len;   // expected sample rank
   const float margin = 4.f * sqrtf(rc) + 16.f;
   const int r_hi = static_cast<int>(floorf(rc - margin));
   const int r_lo = static_cast<int>(ceilf(rc + margin));
   uint32_t p_hi, p_lo;
-  sample_bracket<kBrThreads>(samp, S, max(r_hi, 1), min(r_lo, S), hist, warp_tot, &s_bin,
+  sample_bracket<kBrThreads>(ss, S, max(r_hi, 1), min(r_lo, S), hist, warp_tot, &s_bin,
                              &s_above, p_hi, p_lo);
   if (tid == 0) {
     const uint32_t t_hi = r_hi >= 1 ? ((p_hi << 10) | 1023u) : 0xFFFFFFFFu;
     const uint32_t t_lo = r_lo <= S ? (p_lo << 10) : 0u;
-    a.bracket[r] = make_uint2(t_lo, t_hi);
+    bracket[r] = make_uint2(t_lo, t_hi);
   }
+}
+
+template <int D, int G>
+cudaError_t launch_sample_t(const SampleArgs& a, int units, int runs, cudaStream_t st) {
+  const int per_cta = kSampWarps * kSampRunsPerWarp;
+  return launch_pdl(k_anchor_sample<D, G>, dim3((runs + per_cta - 1) / per_cta, units),
+                    dim3(kSampWarps * 32), 0, st, a);
 }
 
 }  // namespace
 
-cudaError_t launch_anchor_bracket(const void* q, const void* k, const int16_t* head_kv, int B,
+int anchor_sample_stride(int N) { return sample_geom(N).S; }
+
+cudaError_t launch_anchor_bracket(const void* q, const void* k, const int16_t* heads, int B,
                                   int Hq, int Hkv, int N, int d, int topk, float scale,
-                                  uint2* bracket, unsigned int* fcount, cudaStream_t st) {
+                                  uint32_t* samp, uint2* bracket, cudaStream_t st) {
   const int rows = B * Hq;
   if (rows <= 0) return cudaSuccess;
-  BracketArgs a;
-  a.q = static_cast<const __nv_bfloat16*>(q);
-  a.k = static_cast<const __nv_bfloat16*>(k);
-  a.bracket = bracket;
-  a.fcount = fcount;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.N = N;
-  a.topk = topk;
-  a.scale = scale;
-  for (int h = 0; h < Hq; ++h) a.head_kv[h] = head_kv[h];
+  const int G = Hq / Hkv;
+  const SampleGeom sg = sample_geom(N);
+  if (topk < N) {
+    SampleArgs a;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.k = static_cast<const __nv_bfloat16*>(k);
+    a.samp = samp;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.N = N;
+    a.S_stride = sg.S;
+    a.scale = scale;
+    for (int h = 0; h < Hq; ++h) a.heads[h] = heads[h];
+    const int units = B * Hkv;
+    cudaError_t e = cudaErrorInvalidValue;
+    if (d == 128) {
+      if (G == 1) e = launch_sample_t<128, 1>(a, units, sg.runs, st);
+      if (G == 2) e = launch_sample_t<128, 2>(a, units, sg.runs, st);
+      if (G == 4) e = launch_sample_t<128, 4>(a, units, sg.runs, st);
+      if (G == 8) e = launch_sample_t<128, 8>(a, units, sg.runs, st);
+    } else if (d == 64) {
+      if (G == 1) e = launch_sample_t<64, 1>(a, units, sg.runs, st);
+      if (G == 2) e = launch_sample_t<64, 2>(a, units, sg.runs, st);
+      if (G == 4) e = launch_sample_t<64, 4>(a, units, sg.runs, st);
+      if (G == 8) e = launch_sample_t<64, 8>(a, units, sg.runs, st);
+    }
+    if (e != cudaSuccess) return e;
+  }
   const size_t smem = (4096 + kSampleCap) * sizeof(uint32_t);
-  auto kern = d == 128 ? k_anchor_bracket<128> : k_anchor_bracket<64>;
-  if (d != 128 && d != 64) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(k_anchor_bracket, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(rows), dim3(kBrThreads), smem, st, a);
+  return launch_pdl(k_anchor_bracket, dim3(rows), dim3(kBrThreads), smem, st,
+                    static_cast<const uint32_t*>(samp), sg.S, N, topk, bracket);
 }
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {

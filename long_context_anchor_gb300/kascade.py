@@ -46,6 +46,8 @@ _SIGS = {
     "kascade_check_wait_timeout": (ctypes.c_int, [_vp, _sz, _vp]),
     "kascade_dense_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kascade_anchor_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "kascade_anchor_decode_fused": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp,
+                                                   _sz, _vp]),
     "kascade_reuse_decode": (ctypes.c_int, [_DP, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _sz, _vp]),
     "kascade_topk": (ctypes.c_int, [_vp, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "kascade_dense_decode_noalloc": (ctypes.c_int, [_DP, _vp, _vp, _vp, _vp, _vp]),
@@ -291,11 +293,13 @@ def dense_decode(q, k, v, group_map=None, scale=None, out=None, ws=None, stream=
 
 
 def anchor_decode(q, k, v, topk, group_map=None, scale=None, return_scores=False, out=None,
-                  idx=None, ws=None, stream=None, pooled=False):
+                  idx=None, ws=None, stream=None, pooled=False, fused=False):
     """Anchor layer: (out [B,Hq,d], idx [B,H,topk] int32[, scores [B,H,N] fp32]).
 
     H = Hq: per-head sets, scores = the scaled logits. pooled: H = Hkv, one
-    set per KV head, scores = the group sums of the softmax weights."""
+    set per KV head, scores = the group sums of the softmax weights. fused:
+    the Top-k fused into the attention kernel (kascade_anchor_decode_fused;
+    bf16, per-head sets; the same results)."""
     B, Hq, Hkv, N, _ = _attn_inputs(q, k, v, prefill=False)
     H = Hkv if pooled else Hq
     extra = []
@@ -311,9 +315,10 @@ def anchor_decode(q, k, v, topk, group_map=None, scale=None, return_scores=False
     idx = torch.empty(B, H, topk, dtype=torch.int32, device=q.device) if idx is None else idx
     scores = torch.empty(B, H, N, dtype=torch.float32, device=q.device) if return_scores else None
     ws, buf = _ws(ws, q.device, workspace_size(desc, topk, DECODE), stream)
-    _check(_lib.kascade_anchor_decode(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk),
-                                      _ptr(out), _ptr(idx), _ptr(scores), _ptr(buf), buf.numel(),
-                                      _stream(stream)), "kascade_anchor_decode")
+    fn, name = ((_lib.kascade_anchor_decode_fused, "kascade_anchor_decode_fused") if fused
+                else (_lib.kascade_anchor_decode, "kascade_anchor_decode"))
+    _check(fn(ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), int(topk), _ptr(out), _ptr(idx),
+              _ptr(scores), _ptr(buf), buf.numel(), _stream(stream)), name)
     return (out, idx, scores) if return_scores else (out, idx)
 
 

@@ -111,12 +111,12 @@ def test_index_mode_validation_and_workspace(K):
     # pooled sets need room for the row statistics and the pooled weights
     # (decode: 8 B per query-head row + 4 B per (KV head, key)), and for the
     # pooled tile weights (prefill); bf16 per-head sets for the fused anchor
-    # Top-k's candidate lists (8 B per entry, min(N, 2k + 8192) entries per
-    # query-head row), which the fp32 path does not use
+    # Top-k's candidate lists (8 B per key and query-head row: every key has
+    # a slot in its (split, warp) sub-list), which the fp32 path does not use
     base = K.workspace_size(K.make_desc(2, 8, 2, 128, 4096, K.F32), 64, K.DECODE)
     d_ph, d_po = (K.workspace_size(x, 64, K.DECODE) for x in (per_head, pooled))
     assert d_po - base >= 2 * 8 * 8 + 2 * 2 * 4096 * 4
-    assert d_ph - base >= 2 * 8 * min(4096, 2 * 64 + 8192) * 8
+    assert d_ph - base >= 2 * 8 * 4096 * 8
     p_ph, p_po = (K.workspace_size(x, 64, K.PREFILL) for x in (per_head, pooled))
     nT = 4096 // 128
     assert p_po - p_ph >= 2 * 2 * (64 * (nT - 1) * nT + 4096) * 4

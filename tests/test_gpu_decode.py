@@ -301,9 +301,36 @@ def test_few_units_long_rows(K, shape):
     check_out(out_r, A.sparse_decode(f64(q2), f64(k2), f64(v2), idx_ref))
 
 
+FUSED_SHAPES = [  # B, Hq, Hkv, N, d, k
+    (8, 32, 8, 32768, 128, 4096),     # the 8B decode shape
+    (4, 64, 8, 131072, 64, 8192),     # the gpt-oss-20b-like long shape
+    (3, 8, 2, 3000, 128, 100),        # ragged splits, small k
+    (1, 16, 2, 1500, 64, 1400),       # short row: the sample is the whole row
+    (2, 8, 8, 70000, 128, 1),         # G = 1, k = 1
+]
+
+
+@pytest.mark.parametrize("shape", FUSED_SHAPES)
+def test_fused_anchor_equals_two_kernel_anchor(K, shape):
+    """kascade_anchor_decode_fused ranks the same fp32 logits under the same
+    rule as kascade_anchor_decode: its sets, logits and outputs are identical
+    bit for bit, and its sets follow the oracle rule on those logits."""
+    B, Hq, Hkv, N, d, k = shape
+    q, kk, v = _rand_layer(B, Hq, Hkv, N, d, torch.bfloat16, seed=N + k)
+    ws = K.Workspace(DEV)
+    out_f, idx_f, s_f = K.anchor_decode(q, kk, v, k, return_scores=True, ws=ws, fused=True)
+    out_d, idx_d, s_d = K.anchor_decode(q, kk, v, k, return_scores=True, ws=ws)
+    assert ws.device_error() == K.OK
+    assert torch.equal(idx_f, idx_d) and torch.equal(s_f, s_d) and torch.equal(out_f, out_d)
+    got, s_np = idx_f.cpu().numpy(), s_f.cpu().numpy()
+    rng = np.random.default_rng(k)
+    for b, h in [(0, 0), (B - 1, Hq - 1), (int(rng.integers(B)), int(rng.integers(Hq)))]:
+        check_topk_exact(got[b, h], s_np[b, h], k, what=("fused top-k", b, h))
+
+
 @pytest.mark.parametrize("kind", ["equal", "ties", "sampled_heavy", "nan"])
 def test_fused_anchor_topk_fallbacks(K, kind):
-    """The anchor decode selects from the candidate lists its attention kernel
+    """The fused anchor decode selects from the candidate lists its attention kernel
     files against a sample bracket; rows where the bracket misses take the
     full selection over the spilled logits. Every case must still equal the
     selection rule on the kernel's own fp32 logits: all logits equal (the
@@ -331,7 +358,7 @@ def test_fused_anchor_topk_fallbacks(K, kind):
     elif kind == "nan":
         kk[1, 0, 777] = float("nan")
     ws = K.Workspace(DEV)
-    out, idx, s_gpu = K.anchor_decode(q, kk, v, k, return_scores=True, ws=ws)
+    out, idx, s_gpu = K.anchor_decode(q, kk, v, k, return_scores=True, ws=ws, fused=True)
     if kind == "nan":
         assert ws.device_error() == K.BAD_INPUT
         return
