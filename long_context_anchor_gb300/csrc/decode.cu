@@ -565,6 +565,7 @@ __global__ void __launch_bounds__(NW * 32)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ int s_pref[kMaxChunksPerCta + 1];          // slice prefix over the CTA's chunks
+  __shared__ int s_cnt[kMaxChunksPerCta];               // plan entries of the CTA's chunks
   __shared__ uint32_t s_ent[NW][STAGES][16];            // entries of the slices in flight
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* wbuf = smem + warp * STAGES * 2 * SLICE;
@@ -573,13 +574,22 @@ __global__ void __launch_bounds__(NW * 32)
   const int b = unit / a.Hkv, g = unit % a.Hkv;
   const int c0 = split * a.chunks_per_cta;
   const int nc = max(0, min(a.plan_chunks - c0, a.chunks_per_cta));
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int c = 0; c < nc; ++c) {
-      s_pref[c] = acc;
-      acc += (min(kPlanCap, a.plan_count[unit * a.plan_chunks + c0 + c]) + 15) / 16;
+  if (warp == 0) {
+    // the chunks' entry counts in one round of loads, then a warp prefix sum
+    const int cnt = lane < nc ? min(kPlanCap, a.plan_count[unit * a.plan_chunks + c0 + lane]) : 0;
+    const int sl = (cnt + 15) / 16;
+    int incl = sl;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
     }
-    s_pref[nc] = acc;
+    if (lane < nc) {
+      s_cnt[lane] = cnt;
+      s_pref[lane] = incl - sl;
+    }
+    if (lane == nc - 1) s_pref[nc] = incl;
+    if (nc == 0 && lane == 0) s_pref[0] = 0;
   }
   __syncthreads();
   const int nslices = s_pref[nc];
@@ -589,9 +599,8 @@ __global__ void __launch_bounds__(NW * 32)
     int c = 0;
     while (c + 1 < nc && s_pref[c + 1] <= sl) ++c;
     const int e = (sl - s_pref[c]) * 16 + (lane & 15);
-    const int cnt = min(kPlanCap, a.plan_count[unit * a.plan_chunks + c0 + c]);
-    return e < cnt ? __ldg(a.plan + (static_cast<size_t>(unit) * a.plan_chunks + c0 + c) * kPlanCap + e)
-                   : 0u;
+    return e < s_cnt[c] ? __ldg(a.plan + (static_cast<size_t>(unit) * a.plan_chunks + c0 + c) * kPlanCap + e)
+                        : 0u;
   };
   const __nv_bfloat16* kbase =
       static_cast<const __nv_bfloat16*>(a.k) + static_cast<size_t>(unit) * a.N * D;

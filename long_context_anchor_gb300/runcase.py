@@ -3,8 +3,8 @@
     python -m long_context_anchor_gb300.runcase KIND [--batch B] [--kv-len N]
         [--heads HQ HKV] [--head-dim D] [--topk K] [--reps R] [--pooled]
 
-KIND: dense_decode, anchor_decode, reuse_decode, topk, dense_prefill,
-anchor_prefill, reuse_prefill. Defaults are the Llama-3.1-8B attention shape
+KIND: dense_decode, anchor_decode, anchor_decode_fused, reuse_decode, topk,
+dense_prefill, anchor_prefill, reuse_prefill. Defaults are the Llama-3.1-8B attention shape
 with batch 2 (decode: about 0.5 GB of K/V per layer, larger than L2), so a
 profiler capture of one launch stays small. Inputs are drawn once; every
 repetition runs the same launch sequence. --pooled uses one index set per KV
@@ -33,7 +33,7 @@ def main():
     B, N, (Hq, Hkv), d = a.batch, a.kv_len, a.heads, a.head_dim
     k_top = a.topk or max(1, N // 8)
     bf = torch.bfloat16
-    if a.kind.endswith("decode") or a.kind == "topk":
+    if "decode" in a.kind or a.kind == "topk":
         q = torch.randn(B, Hq, d, generator=g, device=dev).to(bf)
     else:
         q = torch.randn(B, Hq, N, d, generator=g, device=dev).to(bf)
@@ -55,6 +55,8 @@ def main():
             K.dense_decode(q, k, v, ws=ws)
         elif a.kind == "anchor_decode":
             K.anchor_decode(q, k, v, k_top, ws=ws, pooled=pl)
+        elif a.kind == "anchor_decode_fused":
+            K.anchor_decode(q, k, v, k_top, ws=ws, fused=True)
         elif a.kind == "reuse_decode":
             K.reuse_decode(q, k, v, idx, ws=ws, pooled=pl)
         elif a.kind == "topk":

@@ -41,8 +41,9 @@ def _rand_layer(B, Hq, Hkv, N, d, dtype, seed, scale_k=1.0):
 def _topk_cases():
     rng = np.random.default_rng(0)
     cases = []
+    # (32771: rows that do not start on a 16-byte boundary)
     for n, k in [(7, 3), (512, 32), (1000, 999), (4096, 512), (32768, 4096), (40000, 5000),
-                 (131072, 8192)]:
+                 (131072, 8192), (32771, 4000)]:
         rows = 6
         x = rng.standard_normal((rows, n)).astype(np.float32)
         x[1] = np.round(x[1] * 2) / 2                # heavy ties
@@ -54,7 +55,7 @@ def _topk_cases():
     return cases
 
 
-@pytest.mark.parametrize("case", range(7))
+@pytest.mark.parametrize("case", range(8))
 def test_topk_bit_exact_on_identical_scores(K, case):
     x, k = _topk_cases()[case]
     got = K.topk(torch.from_numpy(x).to(DEV), k).cpu().numpy()
