@@ -59,6 +59,21 @@ int main(void) {
          "k > n refused");
   expect(kascade_schedule_anchors(NULL, 4, 2, ip, NULL) == KASCADE_ERR_INVALID_ARG,
          "null similarity refused");
+  expect(kascade_anchor_prefill(&d, p, p, p, 512, p, ip, (float*)mis, p, ws_pre, NULL) ==
+             KASCADE_ERR_INVALID_ARG, "misaligned tile-weights buffer refused");
+  expect(kascade_anchor_decode_shard(&d, p, p, p, -1, 512, p, (float*)p, ip, (float*)p, p,
+                                     ws_dec, NULL) == KASCADE_ERR_INVALID_ARG,
+         "negative shard offset refused");
+  const size_t ws_merge = kascade_merge_workspace_size(&d, 4, 512);
+  expect(ws_merge > 0, "merge workspace size");
+  expect(kascade_merge_decode_shards(&d, 0, p, (float*)p, ip, (float*)p, 512, p, ip, p, ws_merge,
+                                     NULL) == KASCADE_ERR_INVALID_ARG, "zero shards refused");
+  expect(kascade_merge_decode_shards(&d, 4, p, (float*)p, ip, (float*)p, 512, p, ip, p, 256,
+                                     NULL) == KASCADE_ERR_WORKSPACE, "small merge workspace refused");
+  kascade_desc f32 = d;
+  f32.dtype = KASCADE_F32;
+  expect(kascade_anchor_decode_fused(&f32, p, p, p, 512, p, ip, NULL, p, ws_dec, NULL) ==
+             KASCADE_ERR_UNSUPPORTED, "fused anchor decode needs bf16");
 
   for (int s = KASCADE_OK; s <= KASCADE_ERR_TIMEOUT; ++s) {
     const char* msg = kascade_status_string((kascade_status)s);

@@ -66,6 +66,34 @@ def test_validation_before_launch(K):
     out_of_range = (ctypes.c_int32 * 1)(2)
     assert K._lib.kascade_run_stack(ctypes.byref(good), 0, 2, arr, arr, arr, 32, out_of_range, 1, arr, p, p, nws, None) == K.INVALID_ARG
     assert K._lib.kascade_topk(p, 4, 10, 11, p, p, 256, None) == K.INVALID_ARG
+    # anchor prefill: the optional weights buffer must be 16-byte aligned
+    pws = K.workspace_size(good, 32, K.PREFILL)
+    assert K._lib.kascade_anchor_prefill(ctypes.byref(good), p, p, p, 32, p, p,
+                                         ctypes.c_void_p(fake + 4), p, pws, None) == K.INVALID_ARG
+    # fused anchor decode: bf16 per query head only
+    assert K._lib.kascade_anchor_decode_fused(ctypes.byref(f32), p, p, p, 32, p, p, None, p,
+                                              1 << 30, None) == K.UNSUPPORTED
+    pooled = K.make_desc(1, 4, 2, 64, 512, K.BF16, pooled=True)
+    assert K._lib.kascade_anchor_decode_fused(ctypes.byref(pooled), p, p, p, 32, p, p, None, p,
+                                              1 << 30, None) == K.UNSUPPORTED
+    # sequence shards: topk within the shard, a non-negative offset, per-head sets;
+    # the merge: 1..1024 shards, aligned buffers, a large enough workspace
+    assert K._lib.kascade_anchor_decode_shard(ctypes.byref(good), p, p, p, 0, 513, p, p, p, p, p,
+                                              nws, None) == K.INVALID_ARG
+    assert K._lib.kascade_anchor_decode_shard(ctypes.byref(good), p, p, p, -1, 32, p, p, p, p, p,
+                                              nws, None) == K.INVALID_ARG
+    assert K._lib.kascade_anchor_decode_shard(ctypes.byref(pooled), p, p, p, 0, 32, p, p, p, p, p,
+                                              nws, None) == K.UNSUPPORTED
+    mws = K._lib.kascade_merge_workspace_size(ctypes.byref(good), 4, 32)
+    assert mws > 0 and K._lib.kascade_merge_workspace_size(ctypes.byref(good), 0, 32) == 0
+    assert K._lib.kascade_merge_decode_shards(ctypes.byref(good), 0, p, p, p, p, 32, p, p, p, mws,
+                                              None) == K.INVALID_ARG
+    assert K._lib.kascade_merge_decode_shards(ctypes.byref(good), 1025, p, p, p, p, 32, p, p, p,
+                                              1 << 30, None) == K.INVALID_ARG
+    assert K._lib.kascade_merge_decode_shards(ctypes.byref(good), 4, p, p, p, p, 32, p, p, p,
+                                              mws - 256, None) == K.WORKSPACE
+    assert K._lib.kascade_merge_decode_shards(ctypes.byref(good), 4, ctypes.c_void_p(fake + 8), p,
+                                              p, p, 32, p, p, p, mws, None) == K.INVALID_ARG
 
 
 def test_calibration_checks_every_layer_before_launching(K):

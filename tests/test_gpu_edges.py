@@ -9,7 +9,7 @@ import torch
 import __graft_entry__
 from oracle import attention as A
 from oracle.topk import topk_indices
-from gpu_helpers import check_index_set, check_out, f64
+from gpu_helpers import check_topk_exact, check_weights, log_w, packed_tile, check_index_set, check_out, f64
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0) if torch.cuda.is_available() else None
@@ -79,23 +79,38 @@ def test_decode_k_one_and_k_n(K, N):
     check_out(out1, A.sparse_decode(Q, Kh, V, idx1))
 
 
-@pytest.mark.parametrize("N", [1, 70, 129])
+@pytest.mark.parametrize("N", [1, 70, 129, 333])
 def test_prefill_shorter_than_a_tile_and_ragged(K, N):
+    """Rows shorter than a tile and ragged last tiles; the packed tile weights
+    then start off 16-byte boundaries for every (sequence, head) after the
+    first (their row length is not a multiple of 4)."""
     B, Hq, Hkv = 1, 4, 2
     q, k, v = _prefill_layer(B, Hq, Hkv, N, seed=7 + N)
     Q, Kh, V = f64(q), f64(k), f64(v)
     check_out(K.dense_prefill(q, k, v), A.dense_prefill(Q, Kh, V))
+    gm = A.default_group_map(Hq, Hkv)
+    scale = 1.0 / np.sqrt(128)
     for topk in sorted({1, min(N, 40), N}):
-        out, idx = K.anchor_prefill(q, k, v, topk)
+        out, idx, wts = K.anchor_prefill(q, k, v, topk, return_weights=True)
         o_ref, idx_ref = A.anchor_prefill(Q, Kh, V, topk)
         check_out(out, o_ref)
-        got = idx.cpu().numpy()
-        gm = A.default_group_map(Hq, Hkv)
+        got, w_gpu = idx.cpu().numpy(), wts.cpu().numpy()
         for h in range(Hq):
             for t in range(A.n_tiles(N)):
-                w = A.tile_weights(Q, Kh, 0, h, t, gm, 1.0 / np.sqrt(128))
+                w = A.tile_weights(Q, Kh, 0, h, t, gm, scale)
+                w_row = packed_tile(w_gpu[0, h], t, N)
+                check_weights(w_row, w, what=("tile weights", h, t))
                 kt = min(topk, w.shape[0])
-                assert (got[0, h, t, kt:] == -1).all()
-                check_index_set(got[0, h, t, :kt], w, kt)
+                check_topk_exact(got[0, h, t], w_row, kt, what=("tile top-k", h, t))
+                check_index_set(got[0, h, t, :kt], log_w(w), kt)
         out_r = K.reuse_prefill(q, k, v, _dev_idx(idx_ref))
         check_out(out_r, A.sparse_prefill(Q, Kh, V, idx_ref))
+        # pooled sets: the group sums of the same weights
+        _, idx_p, wts_p = K.anchor_prefill(q, k, v, topk, return_weights=True, pooled=True)
+        gp, wp = idx_p.cpu().numpy(), wts_p.cpu().numpy()
+        for g in range(Hkv):
+            for t in range(A.n_tiles(N)):
+                w = A.tile_weights_pooled(Q, Kh, 0, g, t, gm, scale)
+                w_row = packed_tile(wp[0, g], t, N)
+                check_weights(w_row, w, what=("pooled tile weights", g, t))
+                check_topk_exact(gp[0, g, t], w_row, min(topk, w.shape[0]), what=("pooled", g, t))
