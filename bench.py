@@ -317,15 +317,14 @@ def pooled_decode_bytes(w):
     """Algorithmic HBM bytes per layer with one index set per (sequence, KV head).
 
     anchor: dense + fp32 logits spill written and read back + the pooled
-            weights written and read by the Top-k + index sets written and
-            read once to build the plan;
-    reuse : K and V rows of the group's set (k rows, no union needed) + one
-            4-byte plan entry per row + q + out.
+            weights written and read by the Top-k + index sets written;
+    reuse : K and V rows of the group's set (k rows, no union needed) + the
+            4-byte set entry of each row (the set is the gather list) + q + out.
     """
     d, B, Hq, Hkv, N, k = w.head_dim, w.batch, w.n_q_heads, w.n_kv_heads, w.kv_len, w.topk
     qo = 2 * B * Hq * d * 2
     dense = B * Hkv * N * 2 * d * 2 + qo
-    anchor = dense + 2 * B * Hq * N * 4 + 2 * B * Hkv * N * 4 + 2 * B * Hkv * k * 4
+    anchor = dense + 2 * B * Hq * N * 4 + 2 * B * Hkv * N * 4 + B * Hkv * k * 4
     reuse = B * Hkv * k * (2 * d * 2 + 4) + qo
     return anchor, reuse
 
@@ -1017,7 +1016,8 @@ def run_ours(args):
             "reuse_hbm_gbs": round(pr_gbs, 1), "reuse_frac_of_copy": round(pr_gbs / hbm_peak, 4),
             "reuse_bytes_per_layer": int(pr_b), "anchor_bytes_per_layer": int(pa_b),
             "anchor_hbm_gbs": round(pa_b / (anchor_p * 1e-3) / 1e9, 1)}
-        result["gpu_launches_decode_pooled"] = args.steps * (5 * len(anchors) + len(reuse_layers))
+        # anchor: attention, row statistics, pooled weights, Top-k; reuse: one gather
+        result["gpu_launches_decode_pooled"] = args.steps * (4 * len(anchors) + len(reuse_layers))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
         result["cpu_baseline"] = time_oracle(w, lay01, n_groups=os.cpu_count() or 1, reps=2)

@@ -317,7 +317,7 @@ kascade_status run_reuse_decode(const Shape& s, const void* q, const void* k, co
   fill_decode_args(a, s, q, k, v, out, ws, L, topk);
   a.idx = idx;
   if (s.dtype == KASCADE_F32) return cuda_status(launch_decode_generic(a, s.d, s.dtype, kSparse, st));
-  if (!plan_ready) {
+  if (!plan_ready && !s.pooled) {   // pooled sets are gathered directly, with no plan
     kascade_status r = run_build_plan(s, idx, topk, ws, L, st);
     if (r != KASCADE_OK) return r;
   }
@@ -702,7 +702,8 @@ kascade_status kascade_run_stack_profiled(const kascade_desc* desc, int32_t mode
     if (mode == KASCADE_DECODE) {
       if (is_anchor) {
         r = run_anchor_decode(s, q[l], k[l], v[l], tk, out[l], idx_buf, nullptr, ws, L, st);
-        if (r == KASCADE_OK && s.dtype == KASCADE_BF16) r = run_build_plan(s, idx_buf, tk, ws, L, st);
+        if (r == KASCADE_OK && s.dtype == KASCADE_BF16 && !s.pooled)
+          r = run_build_plan(s, idx_buf, tk, ws, L, st);
         held = true;
       } else if (held) {
         r = run_reuse_decode(s, q[l], k[l], v[l], tk, idx_buf, out[l], ws, L, true, st);

@@ -545,15 +545,20 @@ __global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant_
 }
 
 // ------------------------------------------------------------------------
-// Reuse decode over the union plan. A CTA takes chunks_per_cta consecutive
-// plan chunks of one (sequence, KV head) as one stream of 16-row slices;
-// every warp gathers its own slices through a STAGES-deep cp.async pipeline
-// (no block barriers), reading each slice's plan entries from global memory
-// one slice ahead. Padding entries (mask 0) are zero-filled, never read.
+// Reuse decode over the union plan. A CTA takes an equal run of the 16-row
+// slices of one (sequence, KV head), numbered across the unit's plan chunks
+// in key order, as one stream; every warp gathers its own slices through a
+// STAGES-deep cp.async pipeline (no block barriers), reading each slice's
+// plan entries from global memory one slice ahead. Padding entries (mask 0)
+// are zero-filled, never read.
 // ------------------------------------------------------------------------
-constexpr int kMaxChunksPerCta = 8;
 
-template <int D, int NW, int STAGES>
+// DIRECT (pooled index sets): every head of a group shares the group's one
+// ascending set, so the set itself is the gather list, with every head's bit
+// in the mask, and no plan is built; a.S CTAs per (sequence, KV head) take
+// equal runs of its 16-row slices. Entries outside [0, N) or out of order
+// are reported as bad input and not read.
+template <int D, int NW, int STAGES, bool DIRECT>
 __global__ void __launch_bounds__(NW * 32)
     k_decode_union_bf16(const __grid_constant__ DecodeArgs a) {
   pdl_wait();
@@ -564,43 +569,66 @@ __global__ void __launch_bounds__(NW * 32)
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ int s_pref[kMaxChunksPerCta + 1];          // slice prefix over the CTA's chunks
-  __shared__ int s_cnt[kMaxChunksPerCta];               // plan entries of the CTA's chunks
+  __shared__ int s_pref[kMaxSplits + 1];                // slice prefix over the unit's chunks
+  __shared__ int s_cnt[kMaxSplits];                     // plan entries of the unit's chunks
   __shared__ uint32_t s_ent[NW][STAGES][16];            // entries of the slices in flight
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* wbuf = smem + warp * STAGES * 2 * SLICE;
 
   const int split = blockIdx.x, unit = blockIdx.y;
   const int b = unit / a.Hkv, g = unit % a.Hkv;
-  const int c0 = split * a.chunks_per_cta;
-  const int nc = max(0, min(a.plan_chunks - c0, a.chunks_per_cta));
-  if (warp == 0) {
-    // the chunks' entry counts in one round of loads, then a warp prefix sum
-    const int cnt = lane < nc ? min(kPlanCap, a.plan_count[unit * a.plan_chunks + c0 + lane]) : 0;
-    const int sl = (cnt + 15) / 16;
-    int incl = sl;
+  // The unit's 16-row slices, numbered across its plan chunks in key order
+  // (DIRECT: across its set), are split into a.S equal runs, one per CTA, so
+  // no CTA waits on a longer one of the same unit.
+  const int nch = DIRECT ? 0 : a.plan_chunks;
+  if (!DIRECT && warp == 0) {
+    // every chunk's entry count, 32 chunks per round, and a running prefix
+    int carry = 0;
+    for (int cb = 0; cb < nch; cb += 32) {
+      const int c = cb + lane;
+      const int cnt = c < nch ? min(kPlanCap, a.plan_count[unit * nch + c]) : 0;
+      const int sl = (cnt + 15) / 16;
+      int incl = sl;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (c < nch) {
+        s_cnt[c] = cnt;
+        s_pref[c] = carry + incl - sl;
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane < nc) {
-      s_cnt[lane] = cnt;
-      s_pref[lane] = incl - sl;
-    }
-    if (lane == nc - 1) s_pref[nc] = incl;
-    if (nc == 0 && lane == 0) s_pref[0] = 0;
+    if (lane == 0) s_pref[nch] = carry;
   }
   __syncthreads();
-  const int nslices = s_pref[nc];
+  const int total = DIRECT ? (a.topk + 15) / 16 : s_pref[nch];
+  const int per = (total + a.S - 1) / a.S;
+  const int g0 = min(total, split * per);
+  const int nslices = min(total, g0 + per) - g0;
   const int my = warp < nslices ? (nslices - warp + NW - 1) / NW : 0;
-  // this lane's plan entry of slice sl (lanes 16..31 repeat lanes 0..15)
+  const int32_t* dset = DIRECT ? a.idx + static_cast<size_t>(unit) * a.topk : nullptr;
+  const uint32_t dmask = (1u << a.G) - 1u;
+  int fc = 0;   // chunk cursor: a warp's slices only move forward
+  // this lane's plan entry of slice sl of the CTA (lanes 16..31 repeat 0..15)
   auto fetch = [&](int sl) -> uint32_t {
-    int c = 0;
-    while (c + 1 < nc && s_pref[c + 1] <= sl) ++c;
-    const int e = (sl - s_pref[c]) * 16 + (lane & 15);
-    return e < s_cnt[c] ? __ldg(a.plan + (static_cast<size_t>(unit) * a.plan_chunks + c0 + c) * kPlanCap + e)
-                        : 0u;
+    const int gs = g0 + sl;
+    if (DIRECT) {
+      const int e = gs * 16 + (lane & 15);
+      if (e >= a.topk) return 0u;
+      const int key = __ldg(dset + e);
+      const int prev = e > 0 ? __ldg(dset + e - 1) : -1;
+      if (key < 0 || key >= a.N || key <= prev) {
+        report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x203);
+        return 0u;   // padding: not read
+      }
+      return static_cast<uint32_t>(key) | (dmask << 24);
+    }
+    while (fc + 1 < nch && s_pref[fc + 1] <= gs) ++fc;
+    const int e = (gs - s_pref[fc]) * 16 + (lane & 15);
+    return e < s_cnt[fc] ? __ldg(a.plan + (static_cast<size_t>(unit) * nch + fc) * kPlanCap + e)
+                         : 0u;
   };
   const __nv_bfloat16* kbase =
       static_cast<const __nv_bfloat16*>(a.k) + static_cast<size_t>(unit) * a.N * D;
@@ -759,22 +787,11 @@ cudaError_t launch_dense_t(const DecodeArgs& a, cudaStream_t st) {
   return launch_pdl(kern, grid, dim3((NW + 1) * 32), smem, st, tk, tv, a);
 }
 
-// Plan chunks per reuse CTA: the fewest that fit all CTAs in one wave of
-// resident CTAs (`slots`); a second, partial wave costs more than CTAs that
-// leave some slots idle.
-int union_chunks_per_cta(int plan_chunks, int units, int slots) {
-  const int ctas_per_unit = slots / units > 1 ? slots / units : 1;
-  int m = (plan_chunks + ctas_per_unit - 1) / ctas_per_unit;
-  if (m < 1) m = 1;
-  if (m > kMaxChunksPerCta) m = kMaxChunksPerCta;
-  return m;
-}
-
-template <int D, int NW, int STAGES>
+template <int D, int NW, int STAGES, bool DIRECT>
 cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
   constexpr int SLICE = (D / 64) * 16 * 128;
   const size_t smem = 1024 + static_cast<size_t>(NW) * STAGES * 2 * SLICE;
-  auto kern = k_decode_union_bf16<D, NW, STAGES>;
+  auto kern = k_decode_union_bf16<D, NW, STAGES, DIRECT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));
   if (e != cudaSuccess) return e;
@@ -791,10 +808,15 @@ cudaError_t launch_union_t(const DecodeArgs& a, cudaStream_t st) {
     cached_slots = max(1, sms * per_sm);
     cached_dev = dev;
   }
-  DecodeArgs u = a;   // a.S plan chunks per unit, regrouped into fewer, longer CTAs
-  u.plan_chunks = a.S;
-  u.chunks_per_cta = union_chunks_per_cta(a.S, a.B * a.Hkv, cached_slots);
-  u.S = (a.S + u.chunks_per_cta - 1) / u.chunks_per_cta;
+  // equal runs of each unit's slices, as many CTAs per unit as fill one
+  // wave of resident CTAs (a second, partial wave costs more than slots left
+  // idle); a.S is the unit's plan chunks (unused with DIRECT)
+  DecodeArgs u = a;
+  const int units = a.B * a.Hkv;
+  const int max_slices = DIRECT ? (a.topk + 15) / 16 : a.S * (kPlanCap / 16);
+  u.plan_chunks = DIRECT ? 0 : a.S;
+  u.chunks_per_cta = 0;
+  u.S = max(1, min(cached_slots / units, min(max_slices, kMaxSplits)));
   dim3 grid(u.S, a.B * a.Hkv);
   return launch_pdl(kern, grid, dim3(NW * 32), smem, st, u);
 }
@@ -860,10 +882,14 @@ cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spi
 
 cudaError_t launch_decode_union_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st) {
   // pooled sets carry k rows per unit instead of the ~G k / 2 of a union, so
-  // their CTAs are shorter: one more stage in flight per warp pays there
+  // their CTAs are shorter: one more stage in flight per warp pays there;
+  // they are gathered straight from the sets (no plan)
   if (head_dim == 128)
-    return a.pooled ? launch_union_t<128, kUnionNW, 3>(a, st) : launch_union_t<128, kUnionNW, 2>(a, st);
-  if (head_dim == 64) return launch_union_t<64, kUnionNW, 3>(a, st);
+    return a.pooled ? launch_union_t<128, kUnionNW, 3, true>(a, st)
+                    : launch_union_t<128, kUnionNW, 2, false>(a, st);
+  if (head_dim == 64)
+    return a.pooled ? launch_union_t<64, kUnionNW, 3, true>(a, st)
+                    : launch_union_t<64, kUnionNW, 3, false>(a, st);
   return cudaErrorInvalidValue;
 }
 

@@ -53,7 +53,7 @@ struct DecodeArgs {
   int B, Hq, Hkv, N, G;
   int S;                    // splits per (sequence, KV head)
   int plan_chunks;          // union plan: key-range chunks per (sequence, KV head)
-  int chunks_per_cta;       // union plan chunks one reuse CTA takes in turn
+  int chunks_per_cta;       // unused (kept zero)
   int chunk;                // keys (dense) per split
   float scale;              // sigma
   float scale_log2;         // sigma * log2(e)

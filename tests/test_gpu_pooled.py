@@ -151,6 +151,33 @@ def test_pooled_nan_logit_reported(K):
     assert ws.device_error() == K.OK
 
 
+@pytest.mark.parametrize("bad", ["out_of_range", "negative", "not_ascending", "repeated"])
+def test_pooled_reuse_decode_bad_set_reported(K, bad):
+    """Pooled sets are gathered as they are (no plan); an entry outside
+    [0, N), or a set that does not strictly ascend, is reported as bad input
+    and the entry is not read; a valid set afterwards reports nothing."""
+    ws = K.Workspace(DEV)
+    B, Hq, Hkv, N, topk = 2, 8, 2, 3000, 100
+    q, k, v = _rand_layer(B, Hq, Hkv, N, 128, torch.bfloat16, seed=23)
+    rng = np.random.default_rng(3)
+    idx = np.stack([np.stack([np.sort(rng.choice(N, topk, replace=False)) for _ in range(Hkv)])
+                    for _ in range(B)]).astype(np.int32)
+    good = _dev_idx(idx)
+    if bad == "out_of_range":
+        idx[1, 0, -1] = N
+    elif bad == "negative":
+        idx[0, 1, 0] = -5
+    elif bad == "not_ascending":
+        idx[0, 0, 10], idx[0, 0, 11] = idx[0, 0, 11], idx[0, 0, 10]
+    else:
+        idx[1, 1, 40] = idx[1, 1, 39]
+    K.reuse_decode(q, k, v, _dev_idx(idx), ws=ws, pooled=True)
+    assert ws.device_error() == K.BAD_INPUT
+    out = K.reuse_decode(q, k, v, good, ws=ws, pooled=True)
+    assert ws.device_error() == K.OK
+    check_out(out, A.sparse_decode_pooled(f64(q), f64(k), f64(v), good.cpu().numpy()))
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_pooled_decode_stack_matches_layer_calls(K, dtype):
     w = configs.TINY_DECODE.with_(dtype=dtype, n_layers=4, anchors=(0, 2))
