@@ -730,6 +730,42 @@ def stacked_layers(w, dev):
     return q_all, k_all, v_all
 
 
+def run_decode_tiny(args, dev, world, stream):
+    """The tiny fp32 decode stack used for bring-up (B=1, 2 layers: anchor then
+    reuse, Hq=4 / Hkv=2, d=64, N=512, k=32): its time is informational (launch
+    latency bound), against the library's own dense decode on the same inputs."""
+    import torch
+    from long_context_anchor_gb300 import configs
+    from long_context_anchor_gb300 import kascade as K
+    from long_context_anchor_gb300.workloads import make_layers
+    w = configs.TINY_DECODE
+    qs, ks, vs = make_layers(w, device=dev)
+    outs = [torch.empty_like(q) for q in qs]
+    ws = K.Workspace(dev)
+    anchors = list(w.anchors)
+
+    def timed(anch, steps):
+        for _ in range(args.warmup):
+            K.run_stack(K.DECODE, qs, ks, vs, w.topk, anch, outs=outs, ws=ws)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            K.run_stack(K.DECODE, qs, ks, vs, w.topk, anch, outs=outs, ws=ws)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert ws.device_error() == K.OK
+        return max_over_ranks([e0.elapsed_time(e1) / steps], world, dev)[0]
+
+    steps = max(10, args.steps)
+    ms_k, ms_d = timed(anchors, steps), timed([], steps)
+    return {"workload": w.name, "layers": w.n_layers, "dtype": w.dtype,
+            "kascade_us_per_layer": round(1e3 * ms_k / w.n_layers, 2),
+            "dense_us_per_layer": round(1e3 * ms_d / w.n_layers, 2),
+            "note": "bring-up size: launch latency, not bandwidth, sets these times"}
+
+
 def run_decode_long(args, dev, world, stream, clocks):
     """Decode stack of the gpt-oss-20b-like attention shape (24 layers, 64/8
     heads, d=64, B=4, N=131072, k=8192, anchors every 3rd): Kascade vs the
@@ -1023,6 +1059,7 @@ def run_ours(args):
         result["cpu_baseline"] = time_oracle(w, lay01, n_groups=os.cpu_count() or 1, reps=2)
     del qs, ks, vs, outs, q_all, k_all, v_all, out_all, idx_buf, ws
     torch.cuda.empty_cache()
+    result["decode_tiny"] = run_decode_tiny(args, dev, world, stream)
     # Prefill stack: Llama-3.1-8B shape at N = 16384.
     if not args.no_prefill:
         pre, pre_launches, pre_ms, _ = run_prefill(args, dev, world, stream, clocks)
