@@ -409,6 +409,7 @@ def decode_e2e(K, w, q_all, k_all, v_all, out_all, anchors, idx_buf, ws, stream,
     vnew_host = v_all[:, :, :, N - 1].contiguous().cpu().pin_memory()
     out_host = [torch.empty(out_all.shape, dtype=out_all.dtype).pin_memory() for _ in range(2)]
     copy_stream = torch.cuda.Stream(device=dev)
+    down_stream = copy_stream   # the copies are small: one stream for both directions
     q_stage = [torch.empty_like(q_all) for _ in range(2)]
     kn_stage = [torch.empty(knew_host.shape, dtype=knew_host.dtype, device=dev) for _ in range(2)]
     vn_stage = [torch.empty(vnew_host.shape, dtype=vnew_host.dtype, device=dev) for _ in range(2)]
@@ -438,10 +439,10 @@ def decode_e2e(K, w, q_all, k_all, v_all, out_all, anchors, idx_buf, ws, stream,
         step_done[slot].record(stream)
 
     def download(slot):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(step_done[slot])
+        with torch.cuda.stream(down_stream):
+            down_stream.wait_event(step_done[slot])
             out_host[slot].copy_(out_stage[slot], non_blocking=True)
-            down_done[slot].record(copy_stream)
+            down_done[slot].record(down_stream)
 
     def run(n):
         upload(0)
@@ -460,6 +461,7 @@ def decode_e2e(K, w, q_all, k_all, v_all, out_all, anchors, idx_buf, ws, stream,
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     copy_stream.wait_event(e0)
+    down_stream.wait_event(e0)
     run(steps)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -474,7 +476,8 @@ def decode_e2e(K, w, q_all, k_all, v_all, out_all, anchors, idx_buf, ws, stream,
                       "per step"}
 
 
-def prefill_e2e(K, w, qs, ks, vs, anchors, ws, stream, steps, warmup, world, dev):
+def prefill_e2e(K, w, qs, ks, vs, anchors, ws, stream, steps, warmup, world, dev,
+                copy_streams=2):
     """Prefill stack end to end through kascade_run_stack with host buffers.
 
     Each step copies every layer's Q, K and V (the whole prompt) from pinned
@@ -487,10 +490,12 @@ def prefill_e2e(K, w, qs, ks, vs, anchors, ws, stream, steps, warmup, world, dev
     stack_h = lambda ts: torch.stack(ts).cpu().pin_memory()
     q_host, k_host, v_host = stack_h(qs), stack_h(ks), stack_h(vs)
     out_host = [torch.empty(q_host.shape, dtype=q_host.dtype).pin_memory() for _ in range(2)]
-    # one copy stream for both directions: a second stream for the downloads
-    # made the step slower (83 against 54 ms), the two large transfers
-    # contending rather than overlapping
+    # uploads on one copy stream; downloads on their own (copy_streams=2), so
+    # that both directions of the host link carry data at once (48 against
+    # 54 ms per stack with one stream for both, measured on one box), or on
+    # the same one (copy_streams=1)
     copy_stream = torch.cuda.Stream(device=dev)
+    down_stream = torch.cuda.Stream(device=dev) if copy_streams == 2 else copy_stream
     stage = [[torch.empty(h.shape, dtype=h.dtype, device=dev) for h in (q_host, k_host, v_host)]
              for _ in range(2)]
     out_stage = [torch.empty(q_host.shape, dtype=q_host.dtype, device=dev) for _ in range(2)]
@@ -518,10 +523,10 @@ def prefill_e2e(K, w, qs, ks, vs, anchors, ws, stream, steps, warmup, world, dev
         step_done[slot].record(stream)
 
     def download(slot):
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(step_done[slot])
+        with torch.cuda.stream(down_stream):
+            down_stream.wait_event(step_done[slot])
             out_host[slot].copy_(out_stage[slot], non_blocking=True)
-            down_done[slot].record(copy_stream)
+            down_done[slot].record(down_stream)
 
     def run(n):
         upload(0)
@@ -540,6 +545,7 @@ def prefill_e2e(K, w, qs, ks, vs, anchors, ws, stream, steps, warmup, world, dev
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     copy_stream.wait_event(e0)
+    down_stream.wait_event(e0)
     run(steps)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -549,7 +555,8 @@ def prefill_e2e(K, w, qs, ks, vs, anchors, ws, stream, steps, warmup, world, dev
     h2d = sum(h.numel() * h.element_size() for h in (q_host, k_host, v_host))
     res = {"value": round(ms, 3), "unit": "ms/stack", "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(out_host[0].numel() * out_host[0].element_size()),
-           "copies": "second stream, double-buffered staging of every layer's Q, K, V and output"}
+           "copies": ("second stream" if copy_streams == 1 else "upload and download streams") +
+                     ", double-buffered staging of every layer's Q, K, V and output"}
     del stage, out_stage, out_host, q_host, k_host, v_host
     torch.cuda.empty_cache()
     return res
