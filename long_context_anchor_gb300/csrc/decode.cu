@@ -635,11 +635,17 @@ __global__ void __launch_bounds__(NW * 32)
   const __nv_bfloat16* vbase =
       static_cast<const __nv_bfloat16*>(a.v) + static_cast<size_t>(unit) * a.N * D;
 
-  auto issue = [&](int i, uint32_t ent) {
+  // Per-head sets: slice i's K rows go to K buffer i % STAGES and its V rows
+  // to V buffer i % STAGES, each as its own cp.async group. A K buffer is free
+  // once the scores of its slice are formed and a V buffer once its P V
+  // product is, so slice i + STAGES's K copies start in the middle of slice
+  // i's work and its V copies at the end: STAGES slices stay in flight per
+  // warp (8B decode shape: 81.7 -> 80.6 us per reuse layer).
+  auto issue_half = [&](int i, uint32_t ent, bool is_v) {
     const int stg = i % STAGES;
-    if (lane < 16) s_ent[warp][stg][lane] = ent;
-    unsigned char* kd = wbuf + stg * 2 * SLICE;
-    unsigned char* vd = kd + SLICE;
+    if (!is_v && lane < 16) s_ent[warp][stg][lane] = ent;
+    unsigned char* dst = wbuf + stg * 2 * SLICE + (is_v ? SLICE : 0);
+    const __nv_bfloat16* src = is_v ? vbase : kbase;
 #pragma unroll
     for (int it = 0; it < 16 / ROWS_PER_INSTR; ++it) {
       const int row = it * ROWS_PER_INSTR + lane / CHUNKS;
@@ -647,8 +653,7 @@ __global__ void __launch_bounds__(NW * 32)
       const uint32_t ent_r = __shfl_sync(0xffffffffu, ent, row);
       const bool ok = (ent_r >> 24) != 0u;   // padding: mask 0
       const size_t off = static_cast<size_t>(ent_r & 0xFFFFFFu) * D + ch * 8;
-      cp_async16(kd + sw128_offset(16, row, ch), kbase + off, ok ? 16u : 0u);
-      cp_async16(vd + sw128_offset(16, row, ch), vbase + off, ok ? 16u : 0u);
+      cp_async16(dst + sw128_offset(16, row, ch), src + off, ok ? 16u : 0u);
     }
   };
 
@@ -658,38 +663,86 @@ __global__ void __launch_bounds__(NW * 32)
   load_q_frags<D>(a, b, g, qf);
   const int gid = lane >> 2, c4 = lane & 3;
 
-  uint32_t nxt = my > 0 ? fetch(warp) : 0u;   // entries of the next slice to issue
+  if constexpr (!DIRECT) {
+  #pragma unroll
+    for (int i = 0; i < STAGES; ++i) {
+      const uint32_t e = i < my ? fetch(warp + i * NW) : 0u;
+      if (i < my) issue_half(i, e, false);
+      cp_async_commit();
+      if (i < my) issue_half(i, e, true);
+      cp_async_commit();
+    }
+    // entries of the next slice to issue, read one iteration before its copies
+    uint32_t nxt = STAGES < my ? fetch(warp + STAGES * NW) : 0u;
+    for (int i = 0; i < my; ++i) {
+      // slice i's K and V groups have landed once at most the 2 (STAGES - 1)
+      // groups issued after them are pending
+      cp_async_wait<2 * (STAGES - 1)>();
+      __syncwarp();
+      const int stg = i % STAGES;
+      const uint32_t kd = smem_u32(wbuf + stg * 2 * SLICE);
+      float sc[4];
+      slice_scores<D>(kd, 16, 0, qf, sc);
+      const uint32_t ent = s_ent[warp][stg][lane & 15];
+      const uint32_t m0 = __shfl_sync(0xffffffffu, ent, gid) >> 24;
+      const uint32_t m1 = __shfl_sync(0xffffffffu, ent, gid + 8) >> 24;
+      // the K buffer and this stage's entries are free: slice i + STAGES's K
+      const int nx = i + STAGES;
+      const uint32_t ent_n = nxt;
+      nxt = nx + 1 < my ? fetch(warp + (nx + 1) * NW) : 0u;
+      __syncwarp();
+      if (nx < my) issue_half(nx, ent_n, false);
+      cp_async_commit();
+      float x[4];
+      x[0] = ((m0 >> (2 * c4)) & 1u) ? sc[0] * a.scale_log2 : kNegInf;
+      x[1] = ((m0 >> (2 * c4 + 1)) & 1u) ? sc[1] * a.scale_log2 : kNegInf;
+      x[2] = ((m1 >> (2 * c4)) & 1u) ? sc[2] * a.scale_log2 : kNegInf;
+      x[3] = ((m1 >> (2 * c4 + 1)) & 1u) ? sc[3] * a.scale_log2 : kNegInf;
+      slice_softmax_pv<D>(st, x, kd + SLICE, 16, 0);
+      // the V buffer is free: slice i + STAGES's V
+      __syncwarp();
+      if (nx < my) issue_half(nx, ent_n, true);
+      cp_async_commit();
+    }
+  } else {
+    // pooled sets: slice i + STAGES - 1 (K and V together) is requested at the
+    // top of iteration i into the buffers slice i - 1 used (measured faster
+    // here than the split requests: 35.5 against 37.0 us per pooled layer)
+    uint32_t nxt = my > 0 ? fetch(warp) : 0u;
 #pragma unroll
-  for (int i = 0; i < STAGES - 1; ++i) {
-    if (i < my) {
-      const uint32_t e = nxt;
-      nxt = (i + 1 < my) ? fetch(warp + (i + 1) * NW) : 0u;
-      issue(i, e);
+    for (int i = 0; i < STAGES - 1; ++i) {
+      if (i < my) {
+        const uint32_t e = nxt;
+        nxt = (i + 1 < my) ? fetch(warp + (i + 1) * NW) : 0u;
+        issue_half(i, e, false);
+        issue_half(i, e, true);
+      }
+      cp_async_commit();
     }
-    cp_async_commit();
-  }
-  for (int i = 0; i < my; ++i) {
-    if (i + STAGES - 1 < my) {
-      const uint32_t e = nxt;
-      nxt = (i + STAGES < my) ? fetch(warp + (i + STAGES) * NW) : 0u;
-      issue(i + STAGES - 1, e);
+    for (int i = 0; i < my; ++i) {
+      if (i + STAGES - 1 < my) {
+        const uint32_t e = nxt;
+        nxt = (i + STAGES < my) ? fetch(warp + (i + STAGES) * NW) : 0u;
+        issue_half(i + STAGES - 1, e, false);
+        issue_half(i + STAGES - 1, e, true);
+      }
+      cp_async_commit();
+      cp_async_wait<STAGES - 1>();
+      __syncwarp();
+      const uint32_t kd = smem_u32(wbuf + (i % STAGES) * 2 * SLICE);
+      float sc[4];
+      slice_scores<D>(kd, 16, 0, qf, sc);
+      const uint32_t ent = s_ent[warp][i % STAGES][lane & 15];
+      const uint32_t m0 = __shfl_sync(0xffffffffu, ent, gid) >> 24;
+      const uint32_t m1 = __shfl_sync(0xffffffffu, ent, gid + 8) >> 24;
+      float x[4];
+      x[0] = ((m0 >> (2 * c4)) & 1u) ? sc[0] * a.scale_log2 : kNegInf;
+      x[1] = ((m0 >> (2 * c4 + 1)) & 1u) ? sc[1] * a.scale_log2 : kNegInf;
+      x[2] = ((m1 >> (2 * c4)) & 1u) ? sc[2] * a.scale_log2 : kNegInf;
+      x[3] = ((m1 >> (2 * c4 + 1)) & 1u) ? sc[3] * a.scale_log2 : kNegInf;
+      slice_softmax_pv<D>(st, x, kd + SLICE, 16, 0);
+      __syncwarp();
     }
-    cp_async_commit();
-    cp_async_wait<STAGES - 1>();
-    __syncwarp();
-    const uint32_t kd = smem_u32(wbuf + (i % STAGES) * 2 * SLICE);
-    float sc[4];
-    slice_scores<D>(kd, 16, 0, qf, sc);
-    const uint32_t ent = s_ent[warp][i % STAGES][lane & 15];
-    const uint32_t m0 = __shfl_sync(0xffffffffu, ent, gid) >> 24;
-    const uint32_t m1 = __shfl_sync(0xffffffffu, ent, gid + 8) >> 24;
-    float x[4];
-    x[0] = ((m0 >> (2 * c4)) & 1u) ? sc[0] * a.scale_log2 : kNegInf;
-    x[1] = ((m0 >> (2 * c4 + 1)) & 1u) ? sc[1] * a.scale_log2 : kNegInf;
-    x[2] = ((m1 >> (2 * c4)) & 1u) ? sc[2] * a.scale_log2 : kNegInf;
-    x[3] = ((m1 >> (2 * c4 + 1)) & 1u) ? sc[3] * a.scale_log2 : kNegInf;
-    slice_softmax_pv<D>(st, x, kd + SLICE, 16, 0);
-    __syncwarp();
   }
   cp_async_wait<0>();
   __syncthreads();
