@@ -410,6 +410,12 @@ __global__ void __launch_bounds__((NW + 1) * 32)
       x[2] = kv1 ? sc[2] * a.scale_log2 : kNegInf;
       x[3] = kv1 ? sc[3] * a.scale_log2 : kNegInf;
       slice_softmax_pv<D>(st, x, smem_u32(vtile + s * TILE_BYTES), TK, row0);
+      // The stage is refilled by TMA (the async proxy) once every consumer
+      // warp has released it; the mbarrier alone did not order this warp's
+      // ldmatrix reads (generic proxy) before that write: without the fence
+      // a refill occasionally overwrote the last V columns still being read
+      // (about one long-shape anchor layer in sixteen came out wrong).
+      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
@@ -614,21 +620,28 @@ __global__ void __launch_bounds__(NW * 32)
   // this lane's plan entry of slice sl of the CTA (lanes 16..31 repeat 0..15)
   auto fetch = [&](int sl) -> uint32_t {
     const int gs = g0 + sl;
-    if (DIRECT) {
-      const int e = gs * 16 + (lane & 15);
-      if (e >= a.topk) return 0u;
-      const int key = __ldg(dset + e);
-      const int prev = e > 0 ? __ldg(dset + e - 1) : -1;
-      if (key < 0 || key >= a.N || key <= prev) {
-        report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x203);
-        return 0u;   // padding: not read
-      }
-      return static_cast<uint32_t>(key) | (dmask << 24);
-    }
     while (fc + 1 < nch && s_pref[fc + 1] <= gs) ++fc;
     const int e = (gs - s_pref[fc]) * 16 + (lane & 15);
     return e < s_cnt[fc] ? __ldg(a.plan + (static_cast<size_t>(unit) * nch + fc) * kPlanCap + e)
                          : 0u;
+  };
+  // DIRECT: this lane's set entry of slice sl and the entry before it, loaded
+  // here but checked (direct_entry) only when the slice's copies are issued a
+  // slice later; checking right after the loads stalled every warp a whole
+  // load latency per slice (pooled 8B decode shape: 34 us, DRAM half busy)
+  auto fetch_direct = [&](int sl) -> int2 {
+    const int e = (g0 + sl) * 16 + (lane & 15);
+    if (e >= a.topk) return make_int2(0, 0);
+    return make_int2(__ldg(dset + e), e > 0 ? __ldg(dset + e - 1) : -1);
+  };
+  auto direct_entry = [&](int sl, int2 r) -> uint32_t {
+    const int e = (g0 + sl) * 16 + (lane & 15);
+    if (e >= a.topk) return 0u;   // past the set: padding
+    if (r.x < 0 || r.x >= a.N || r.x <= r.y) {
+      report_error(a.err, KASCADE_ERR_BAD_INPUT, 0x203);
+      return 0u;   // padding: not read
+    }
+    return static_cast<uint32_t>(r.x) | (dmask << 24);
   };
   const __nv_bfloat16* kbase =
       static_cast<const __nv_bfloat16*>(a.k) + static_cast<size_t>(unit) * a.N * D;
@@ -708,12 +721,12 @@ __global__ void __launch_bounds__(NW * 32)
     // pooled sets: slice i + STAGES - 1 (K and V together) is requested at the
     // top of iteration i into the buffers slice i - 1 used (measured faster
     // here than the split requests: 35.5 against 37.0 us per pooled layer)
-    uint32_t nxt = my > 0 ? fetch(warp) : 0u;
+    int2 raw = my > 0 ? fetch_direct(warp) : make_int2(0, 0);
 #pragma unroll
     for (int i = 0; i < STAGES - 1; ++i) {
       if (i < my) {
-        const uint32_t e = nxt;
-        nxt = (i + 1 < my) ? fetch(warp + (i + 1) * NW) : 0u;
+        const uint32_t e = direct_entry(warp + i * NW, raw);
+        raw = (i + 1 < my) ? fetch_direct(warp + (i + 1) * NW) : make_int2(0, 0);
         issue_half(i, e, false);
         issue_half(i, e, true);
       }
@@ -721,8 +734,8 @@ __global__ void __launch_bounds__(NW * 32)
     }
     for (int i = 0; i < my; ++i) {
       if (i + STAGES - 1 < my) {
-        const uint32_t e = nxt;
-        nxt = (i + STAGES < my) ? fetch(warp + (i + STAGES) * NW) : 0u;
+        const uint32_t e = direct_entry(warp + (i + STAGES - 1) * NW, raw);
+        raw = (i + STAGES < my) ? fetch_direct(warp + (i + STAGES) * NW) : make_int2(0, 0);
         issue_half(i + STAGES - 1, e, false);
         issue_half(i + STAGES - 1, e, true);
       }

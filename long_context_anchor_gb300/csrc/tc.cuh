@@ -54,9 +54,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // MMA issue is warp-collective: all 32 lanes of a converged warp call these
 // with the same (warp-uniform) operands and one lane, chosen by elect.sync,

@@ -329,6 +329,27 @@ def test_fused_anchor_equals_two_kernel_anchor(K, shape):
         check_topk_exact(got[b, h], s_np[b, h], k, what=("fused top-k", b, h))
 
 
+def test_anchor_decode_repeatable(K):
+    """Every decode path that streams K/V through the TMA stage ring gives the
+    same output bit for bit on every call. A stage refilled by TMA while a
+    consumer warp still read its last V columns (no proxy fence between the
+    warp's ldmatrix reads and the refill) made about one long-shape fused
+    anchor layer in sixteen differ in one split's last output dims."""
+    B, Hq, Hkv, N, d, k = FUSED_SHAPES[1]
+    q, kk, v = _rand_layer(B, Hq, Hkv, N, d, torch.bfloat16, seed=N + k)
+    ws = K.Workspace(DEV)
+    ref = K.dense_decode(q, kk, v, ws=ws).clone()
+    bad = []
+    for rep in range(24):
+        for name, o in (("fused", K.anchor_decode(q, kk, v, k, ws=ws, fused=True)[0]),
+                        ("two-kernel", K.anchor_decode(q, kk, v, k, ws=ws)[0]),
+                        ("dense", K.dense_decode(q, kk, v, ws=ws))):
+            if not torch.equal(o, ref):
+                bad.append((rep, name, int((o != ref).sum())))
+    assert ws.device_error() == K.OK
+    assert not bad, bad
+
+
 @pytest.mark.parametrize("kind", ["equal", "ties", "sampled_heavy", "nan"])
 def test_fused_anchor_topk_fallbacks(K, kind):
     """The fused anchor decode selects from the candidate lists its attention kernel
