@@ -63,6 +63,48 @@ def test_topk_bit_exact_on_identical_scores(K, case):
         assert got[r].tolist() == topk_indices(x[r], k).tolist(), (case, r)
 
 
+def test_topk_long_row_fallbacks(K):
+    """Long rows whose sample bracket cannot settle the k-th key: an 8192-key
+    run set to the expected k-th value (its warps' candidate lists overflow),
+    heavy keys placed only where the sample never looks (the k-th key lies
+    above the bracket), few distinct values, and a NaN (reported as bad
+    input). k = 1 and k = n rows ride along; every row must still follow the
+    rule exactly."""
+    rng = np.random.default_rng(23)
+    n = 65536
+    x = rng.standard_normal((5, n)).astype(np.float32)
+    k = 4096
+    # row 0: one 8192-key segment set to the expected k-th value (all candidates)
+    kth = np.sort(x[0])[::-1][k - 1]
+    x[0, 8192:16384] = kth
+    # row 1: k + 100 heavy keys between the sample's runs (runs of 32 keys
+    # start at multiples of (n - 32) / (runs - 1); keys 40..479 after each run
+    # start are never sampled)
+    runs = max(2048, min(8192, n // 16)) // 32
+    step = (n - 32) / (runs - 1)
+    starts = np.floor(np.arange(runs) * step).astype(np.int64)
+    heavy = (starts[:, None] + np.arange(40, 480)[None, :]).ravel()
+    heavy = heavy[heavy < n][: k + 100]
+    x[1, heavy] = 50.0 + rng.random(heavy.size).astype(np.float32)
+    # row 2: ties everywhere (a few distinct values)
+    x[2] = np.round(x[2])
+    got = K.topk(torch.from_numpy(x).to(DEV), k).cpu().numpy()
+    for r in range(5):
+        assert got[r].tolist() == topk_indices(x[r], k).tolist(), r
+    for kk in (1, n):
+        got = K.topk(torch.from_numpy(x[3:5].copy()).to(DEV), kk).cpu().numpy()
+        for r in range(2):
+            assert got[r].tolist() == topk_indices(x[3 + r], kk).tolist(), (kk, r)
+    ws = K.Workspace(DEV)
+    xn = torch.from_numpy(x[3:5].copy()).to(DEV)
+    xn[1, 40000] = float("nan")
+    K.topk(xn, k, ws=ws)
+    assert ws.device_error() == K.BAD_INPUT
+    got = K.topk(torch.from_numpy(x[3:5].copy()).to(DEV), k, ws=ws).cpu().numpy()
+    assert ws.device_error() == K.OK
+    assert got[0].tolist() == topk_indices(x[3], k).tolist()
+
+
 def test_topk_many_short_rows_bit_exact(K):
     """1100 rows of 6000 keys take the 256-thread CTAs (the launch shape of the
     prefill tile rows); every row pattern of the cases above recurs across them,
