@@ -142,7 +142,8 @@ kascade_status kascade_anchor_decode(const kascade_desc* desc, const void* q, co
 
 /* The anchor layer of kascade_anchor_decode (bf16, per query head sets; other
  * modes return KASCADE_ERR_UNSUPPORTED) with the Top-k fused into the
- * attention kernel (the survey's "fused score spill" with a threshold pass):
+ * attention kernel (the logit spill fused with a threshold pass; euno.news
+ * summary, Methodology 2: the anchor's exact attention and its Top-k):
  * a first kernel brackets each row's k-th logit from an evenly spaced sample
  * of its keys; the attention kernel then files every logit at or above the
  * bracket's lower end, as (key, position), in per-(row, split, warp) lists
