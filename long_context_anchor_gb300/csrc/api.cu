@@ -105,6 +105,7 @@ inline bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<
 struct Layout {
   size_t counters, part, spill, plan, plan_count;   // decode
   size_t bracket, fcount, flist, fsamp;             // decode, fused anchor Top-k
+  size_t selbits;                                   // decode: the anchor rows' selection bitmaps
   size_t row_stat, pool;                            // decode, pooled sets
   size_t lse, w, w_pool;                            // prefill (w_pool: pooled sets)
   size_t total;
@@ -138,6 +139,10 @@ Layout layout(const Shape& s, int topk, int mode) {
       off = align256(off + rows * splits * kDecodeConsumerWarps * 4);
       L.flist = off;
       off = align256(off + rows * splits * static_cast<size_t>(chunk) * 8);
+      // the anchor's selection per logit row as a bitmap, from which a layer
+      // stack builds the reuse layers' union plan without searching the sets
+      L.selbits = off;
+      off = align256(off + rows * static_cast<size_t>((s.N + 31) / 32) * 4);
     }
     if (s.pooled) {
       L.row_stat = off;
@@ -225,8 +230,9 @@ kascade_status run_dense_decode(const Shape& s, const void* q, const void* k, co
 }
 
 kascade_status run_topk_rows(const float* scores, int rows, int n, int k, int32_t* idx,
-                             unsigned int* err, cudaStream_t st) {
+                             unsigned int* err, cudaStream_t st, uint32_t* sel_bits = nullptr) {
   TopkArgs t{};
+  t.sel_bits = sel_bits;
   t.scores = scores;
   t.idx_out = idx;
   t.err = err;
@@ -291,12 +297,27 @@ kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, c
     t.fsplits = a.S;
     t.fwarps = kDecodeConsumerWarps;
     t.fchunk = a.chunk;
+    t.sel_bits = at<uint32_t>(ws, L.selbits);
     const cudaError_t e = launch_topk(t, st);
     return e == cudaErrorNotSupported ? KASCADE_ERR_UNSUPPORTED : cuda_status(e);
   }
   kascade_status r = run_dense_decode(s, q, k, v, out, ws, L, topk, spill, st);
   if (r != KASCADE_OK) return r;
-  return run_topk_rows(spill, s.B * s.Hq, s.N, topk, idx_out, at<unsigned int>(ws, 0), st);
+  return run_topk_rows(spill, s.B * s.Hq, s.N, topk, idx_out, at<unsigned int>(ws, 0), st,
+                       L.selbits ? at<uint32_t>(ws, L.selbits) : nullptr);
+}
+
+// The union plan from the selection bitmaps the last anchor decode call on
+// this workspace left (per-head bf16 sets; the plan of its sets).
+kascade_status run_build_plan_bits(const Shape& s, int topk, void* ws, const Layout& L,
+                                   cudaStream_t st) {
+  if (!L.selbits) return KASCADE_ERR_UNSUPPORTED;
+  DecodeArgs a;
+  fill_decode_args(a, s, nullptr, nullptr, nullptr, nullptr, ws, L, topk);
+  const cudaError_t e = launch_build_union_plan_bits(a, at<uint32_t>(ws, L.selbits),
+                                                     (s.N + 31) / 32, at<uint32_t>(ws, L.plan),
+                                                     at<int32_t>(ws, L.plan_count), st);
+  return e == cudaErrorNotSupported ? KASCADE_ERR_UNSUPPORTED : cuda_status(e);
 }
 
 // Build the per-(sequence, KV head) union of the group's sets (bf16 path).
@@ -702,8 +723,9 @@ kascade_status kascade_run_stack_profiled(const kascade_desc* desc, int32_t mode
     if (mode == KASCADE_DECODE) {
       if (is_anchor) {
         r = run_anchor_decode(s, q[l], k[l], v[l], tk, out[l], idx_buf, nullptr, ws, L, st);
+        // the reuse layers' union plan, from the anchor's selection bitmaps
         if (r == KASCADE_OK && s.dtype == KASCADE_BF16 && !s.pooled)
-          r = run_build_plan(s, idx_buf, tk, ws, L, st);
+          r = run_build_plan_bits(s, tk, ws, L, st);
         held = true;
       } else if (held) {
         r = run_reuse_decode(s, q[l], k[l], v[l], tk, idx_buf, out[l], ws, L, true, st);

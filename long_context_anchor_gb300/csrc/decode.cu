@@ -550,6 +550,67 @@ __global__ void __launch_bounds__(256) k_build_union_plan(const __grid_constant_
   if (threadIdx.x == blockDim.x - 1) plan_count[unit * nch + c] = s_scan[threadIdx.x];
 }
 
+// The same plan from the heads' selection bitmaps (one word per 32 keys per
+// query-head row, as the anchor layer's Top-k emits them): CTA (c, unit)
+// ORs the G rows' words of keys [c*R, (c+1)*R) and emits the union in key
+// order with each entry's head mask, exactly as k_build_union_plan does from
+// the sets, without searching them. Per-head sets only.
+__global__ void __launch_bounds__(256) k_build_union_plan_bits(const __grid_constant__ DecodeArgs a,
+                                                               const uint32_t* __restrict__ sel,
+                                                               int words_per_row,
+                                                               uint32_t* __restrict__ plan,
+                                                               int32_t* __restrict__ plan_count,
+                                                               int R) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ int s_scan[256];
+  const int c = blockIdx.x, unit = blockIdx.y, nch = gridDim.x;
+  const int b = unit / a.Hkv, g = unit % a.Hkv;
+  const int G = a.G;
+  const int n0 = c * R, n1 = min(a.N, n0 + R);
+  const int words = (n1 - n0 + 31) / 32;   // R is a multiple of 32
+  const int w_base = n0 / 32;
+  // contiguous word runs per thread (at most one word for R <= 8192)
+  const int per = (words + blockDim.x - 1) / blockDim.x;
+  const int w0 = min(words, static_cast<int>(threadIdx.x) * per), w1 = min(words, w0 + per);
+  auto word_of = [&](int slot, int w) {
+    const size_t row = static_cast<size_t>(b) * a.Hq + a.heads[g * G + slot];
+    return __ldg(sel + row * words_per_row + w_base + w);
+  };
+  int cnt = 0;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t u = 0;
+    for (int slot = 0; slot < G; ++slot) u |= word_of(slot, w);
+    cnt += __popc(u);
+  }
+  s_scan[threadIdx.x] = cnt;
+  __syncthreads();
+  for (int off = 1; off < static_cast<int>(blockDim.x); off <<= 1) {
+    const int v = static_cast<int>(threadIdx.x) >= off ? s_scan[threadIdx.x - off] : 0;
+    __syncthreads();
+    s_scan[threadIdx.x] += v;
+    __syncthreads();
+  }
+  int pos = s_scan[threadIdx.x] - cnt;
+  uint32_t* out = plan + (static_cast<size_t>(unit) * nch + c) * kPlanCap;
+  for (int w = w0; w < w1; ++w) {
+    uint32_t bw[8];
+    uint32_t u = 0;
+    for (int slot = 0; slot < G; ++slot) {
+      bw[slot] = word_of(slot, w);
+      u |= bw[slot];
+    }
+    while (u) {
+      const int bit = __ffs(u) - 1;
+      u &= u - 1;
+      uint32_t mask = 0u;
+      for (int slot = 0; slot < G; ++slot) mask |= ((bw[slot] >> bit) & 1u) << slot;
+      out[pos++] = static_cast<uint32_t>(n0 + w * 32 + bit) | (mask << 24);
+    }
+  }
+  if (threadIdx.x == blockDim.x - 1) plan_count[unit * nch + c] = s_scan[threadIdx.x];
+}
+
 // ------------------------------------------------------------------------
 // Reuse decode over the union plan. A CTA takes an equal run of the 16-row
 // slices of one (sequence, KV head), numbered across the unit's plan chunks
@@ -959,6 +1020,16 @@ cudaError_t launch_decode_union_bf16(const DecodeArgs& a, int head_dim, cudaStre
     return a.pooled ? launch_union_t<64, kUnionNW, 3, true>(a, st)
                     : launch_union_t<64, kUnionNW, 3, false>(a, st);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_build_union_plan_bits(const DecodeArgs& a, const uint32_t* sel, int words,
+                                         uint32_t* plan, int32_t* plan_count, cudaStream_t st) {
+  if (a.G > 8 || a.pooled) return cudaErrorInvalidValue;
+  const int R = decode_union_range(a.B * a.Hkv, a.N);
+  const int S = (a.N + R - 1) / R;
+  if (S > kMaxSplits) return cudaErrorNotSupported;
+  return launch_pdl(k_build_union_plan_bits, dim3(S, a.B * a.Hkv), dim3(256), 0, st, a, sel,
+                    words, plan, plan_count, R);
 }
 
 cudaError_t launch_build_union_plan(const DecodeArgs& a, uint32_t* plan, int32_t* plan_count,

@@ -89,6 +89,10 @@ kascade_status check_desc(const kascade_desc* desc, Shape& s);
 cudaError_t launch_decode_dense_bf16(const DecodeArgs& a, int head_dim, bool spill,
                                      cudaStream_t st, bool filter = false);
 cudaError_t launch_decode_union_bf16(const DecodeArgs& a, int head_dim, cudaStream_t st);
+// The same plan from the rows' selection bitmaps (TopkArgs::sel_bits of
+// the group heads' rows, `words` words per row) instead of their index sets.
+cudaError_t launch_build_union_plan_bits(const DecodeArgs& a, const uint32_t* sel, int words,
+                                         uint32_t* plan, int32_t* plan_count, cudaStream_t st);
 cudaError_t launch_build_union_plan(const DecodeArgs& a, uint32_t* plan, int32_t* plan_count,
                                     cudaStream_t st);
 cudaError_t launch_decode_generic(const DecodeArgs& a, int head_dim, int dtype, DecodeKind kind,
@@ -119,6 +123,9 @@ struct TopkArgs {
   const unsigned int* fcount;
   const uint2* flist;
   int fsplits, fwarps, fchunk;
+  // Plain rows (null when unused): row r's selection as a bitmap of its n
+  // positions, sel_bits + r * ceil(n / 32) (bit p % 32 of word p / 32).
+  uint32_t* sel_bits;
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
 

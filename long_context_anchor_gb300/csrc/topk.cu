@@ -254,6 +254,13 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__
 
   if (rd.k >= rd.len) {   // the whole prefix is selected
     for (int j = tid; j < a.k_stride; j += kThreads) out[j] = (j < rd.len) ? j : -1;
+    if (a.sel_bits != nullptr) {
+      const int Ws = (rd.len + 31) >> 5;
+      for (int w = tid; w < Ws; w += kThreads) {
+        const int rest = rd.len - 32 * w;
+        a.sel_bits[static_cast<size_t>(r) * Ws + w] = rest >= 32 ? 0xFFFFFFFFu : (1u << rest) - 1u;
+      }
+    }
     return;
   }
   const int W = (rd.len + 31) >> 5;
@@ -535,19 +542,27 @@ __global__ void __launch_bounds__(NT, MIN_BLOCKS) k_topk(const __grid_constant__
   for (int w = w0; w < w1; ++w) {
     const uint32_t ab = above[w], eb = eqbm[w];
     uint32_t u = ab | eb;
+    uint32_t sel = 0u;   // the positions of this word that were emitted
     while (u) {
       const int bit = __ffs(u) - 1;
       u &= u - 1;
       const int pos = w * 32 + bit;
       if ((ab >> bit) & 1u) {
         const int o = pa + min(pe, need_eq);
-        if (o < rd.k) out[o] = pos;
+        if (o < rd.k) {
+          out[o] = pos;
+          sel |= 1u << bit;
+        }
         ++pa;
       } else {
-        if (pe < need_eq && pa + pe < rd.k) out[pa + pe] = pos;
+        if (pe < need_eq && pa + pe < rd.k) {
+          out[pa + pe] = pos;
+          sel |= 1u << bit;
+        }
         ++pe;
       }
     }
+    if (a.sel_bits != nullptr) a.sel_bits[static_cast<size_t>(r) * W + w] = sel;
   }
   for (int j = rd.k + tid; j < a.k_stride; j += kThreads) out[j] = -1;
 }
