@@ -49,7 +49,7 @@ TRAFFIC = {
     "k_prefill_fa2_reuse": 383.524e6,   # profiles/k_prefill_fa2_reuse_n16384.md
     # captured at B=1 (8 of the 32 units) and scaled by units to B=4:
     # profiles/k_decode_union_bf16_gptoss_b4_n131072.md
-    "k_decode_union_bf16_long": 4 * 110.809e6,
+    "k_decode_union_bf16_long": 4 * 110.981e6,
 }
 UNIT = "us/layer"
 NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s HBM3e figure the decode targets are quoted against
