@@ -252,6 +252,30 @@ def test_reuse_bad_index_reported(K):
 
 # ------------------------------------------------------------------- stack --
 
+PLAN_SHAPES = [  # B, Hq, Hkv, N, d, k
+    (2, 8, 2, 40000, 128, 1000),   # G = 4, many key-range chunks, a ragged last one
+    (1, 16, 2, 5000, 64, 5000),    # G = 8, k = N: every key selected
+    (3, 4, 4, 3001, 128, 7),       # G = 1, tiny k, ragged N
+]
+
+
+@pytest.mark.parametrize("shape", PLAN_SHAPES)
+def test_stack_bitmap_plan_matches_layer_calls(K, shape):
+    """In a bf16 per-head stack the reuse layers' union plan is built from the
+    anchor Top-k's selection bitmaps; the single reuse call builds it from the
+    index sets it is given. Both plans, and so the outputs, must be identical."""
+    B, Hq, Hkv, N, d, k = shape
+    layers = [_rand_layer(B, Hq, Hkv, N, d, torch.bfloat16, seed=N + 3 * l) for l in range(3)]
+    qs, ks, vs = ([lay[i] for lay in layers] for i in range(3))
+    outs, idx_buf = K.run_stack(K.DECODE, qs, ks, vs, k, [0])
+    o0, i0 = K.anchor_decode(qs[0], ks[0], vs[0], k)
+    o1 = K.reuse_decode(qs[1], ks[1], vs[1], i0)
+    o2 = K.reuse_decode(qs[2], ks[2], vs[2], i0)
+    assert torch.equal(idx_buf, i0)
+    for a, b in zip(outs, [o0, o1, o2]):
+        assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_stack_matches_layer_calls_and_oracle(K, dtype):
     w = configs.TINY_DECODE.with_(dtype=dtype, n_layers=5, anchors=(1, 3))
