@@ -218,10 +218,11 @@ namespace {
 
 kascade_status run_dense_decode(const Shape& s, const void* q, const void* k, const void* v,
                                 void* out, void* ws, const Layout& L, int topk, float* spill,
-                                cudaStream_t st) {
+                                cudaStream_t st, float2* row_stat = nullptr) {
   DecodeArgs a;
   fill_decode_args(a, s, q, k, v, out, ws, L, topk);
   if (spill != nullptr) a.spill = spill;
+  a.row_stat = row_stat;
   if (s.dtype == KASCADE_F32)
     return cuda_status(launch_decode_generic(a, s.d, s.dtype, spill ? kAnchor : kDense, st));
   a.chunk = decode_chunk_dense(s.B * s.Hkv, s.N);
@@ -252,11 +253,16 @@ kascade_status run_anchor_decode(const Shape& s, const void* q, const void* k, c
   if (s.pooled) {
     // logits to the workspace, then the group sums of their softmax weights
     float* spill = at<float>(ws, L.spill);
-    kascade_status r = run_dense_decode(s, q, k, v, out, ws, L, topk, spill, st);
+    // bf16: the attention kernel's split merge also leaves each row's softmax
+    // statistics, so no separate pass over the logits computes them
+    const bool bf16 = s.dtype == KASCADE_BF16;
+    float2* row_stat = at<float2>(ws, L.row_stat);
+    kascade_status r = run_dense_decode(s, q, k, v, out, ws, L, topk, spill, st,
+                                        bf16 ? row_stat : nullptr);
     if (r != KASCADE_OK) return r;
     float* pool = scores_out ? scores_out : at<float>(ws, L.pool);
-    r = cuda_status(launch_pool_decode(spill, at<float2>(ws, L.row_stat), pool, s.heads, s.B,
-                                       s.Hq, s.Hkv, s.G, s.N, st));
+    r = cuda_status(launch_pool_decode(spill, row_stat, pool, bf16, s.heads, s.B, s.Hq, s.Hkv,
+                                       s.G, s.N, st));
     if (r != KASCADE_OK) return r;
     return run_topk_rows(pool, s.B * s.Hkv, s.N, topk, idx_out, at<unsigned int>(ws, 0), st);
   }

@@ -34,6 +34,7 @@ namespace {
 constexpr int kPlanCap = kPlanCapEntries;   // plan entries of one reuse CTA (shared staging)
 
 #define kNegInf (-CUDART_INF_F)
+constexpr float kLn2 = 0.6931471805599453f;   // log2-domain maxima back to logit units
 
 // ------------------------------------------------------------------------
 // Consumer math on one 16-key slice held in swizzled shared memory. Thread
@@ -190,6 +191,9 @@ __device__ void finish_cta(const DecodeArgs& a, WarpState<D>& st, int cw, int n_
     }
     cm[h] = M;
     cl[h] = L;
+    if (a.S == 1 && a.row_stat != nullptr)   // the row's softmax statistics, in logit units
+      a.row_stat[static_cast<size_t>(b) * a.Hq + a.heads[g * G + h]] =
+          make_float2(M * kLn2, L > 0.f ? 1.f / L : 0.f);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
@@ -251,6 +255,8 @@ __device__ void finish_cta(const DecodeArgs& a, WarpState<D>& st, int cw, int n_
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     for (int s = 0; s < a.S; ++s) wts[h * a.S + s] *= inv;
+    if (a.row_stat != nullptr)   // the row's softmax statistics, in logit units
+      a.row_stat[static_cast<size_t>(b) * a.Hq + a.heads[g * G + h]] = make_float2(M * kLn2, inv);
   }
   __syncthreads();
   for (int e = threadIdx.x; e < G * D; e += blockDim.x) {

@@ -41,6 +41,8 @@ struct DecodeArgs {
   const void* v;            // [B,Hkv,N,d]
   void* out;                // [B,Hq,d]
   float* spill;             // [B,Hq,N] scaled logits (anchor), or null
+  float2* row_stat;         // [B*Hq] (max logit, 1 / sum exp(logit - max)) per row,
+                            // written by the split merge (pooled anchor), or null
   float* part;              // [B*Hq][S][d+4]: m (log2 units), l, -, -, o[d]
   unsigned int* counters;   // [B*Hkv] split arrival counters (self-resetting)
   unsigned int* err;        // workspace error word
@@ -166,7 +168,10 @@ cudaError_t launch_prefill_reuse(const PrefillArgs& a, int head_dim, cudaStream_
 // Decode: w[b,g,j] = sum over the group's heads h of softmax_j(s[b,h,:]),
 // from the anchor's logit spill s [B,Hq,N]; row_stat [B*Hq] holds each row's
 // (max, 1/sum exp(s - max)).
-cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w,
+// Pooled decode weights from the logit spill; row_stat holds each row's
+// (max, 1 / sum exp) already when stats_given (the bf16 attention kernel
+// writes them), else k_row_stat computes it first.
+cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w, bool stats_given,
                                const int16_t* heads, int B, int Hq, int Hkv, int G, int N,
                                cudaStream_t st);
 // Row statistics alone: row_stat[r] = (max_j s_rj, 1 / sum_j exp(s_rj - max)).

@@ -155,15 +155,17 @@ HeadTable make_table(const int16_t* heads, int Hq) {
 
 }  // namespace
 
-cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w,
+cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w, bool stats_given,
                                const int16_t* heads, int B, int Hq, int Hkv, int G, int N,
                                cudaStream_t st) {
   if (B < 1 || Hq < 1 || Hkv < 1 || G < 1 || N < 1 || Hq != Hkv * G || Hq > kMaxQHeads)
     return cudaErrorInvalidValue;
   const HeadTable ht = make_table(heads, Hq);
-  cudaError_t e = launch_pdl(k_row_stat, dim3(B * Hq), dim3(kStatThreads), 0, st, spill, N,
-                             row_stat);
-  if (e != cudaSuccess) return e;
+  if (!stats_given) {
+    const cudaError_t e = launch_pdl(k_row_stat, dim3(B * Hq), dim3(kStatThreads), 0, st, spill,
+                                     N, row_stat);
+    if (e != cudaSuccess) return e;
+  }
   return launch_pdl(k_pool_decode, dim3((N + 1023) / 1024, B * Hkv), dim3(256), 0, st, spill,
                     static_cast<const float2*>(row_stat), w, ht, Hq, Hkv, G, N);
 }
