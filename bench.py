@@ -45,11 +45,11 @@ METRIC = "decode attn µs/layer + HBM GB/s at 32K ctx; prefill attn TFLOP/s; vs 
 # ncu capture of the kernel as it stands (profiles/<kernel>_*.md); None when no
 # capture of the current kernel at the bench's size exists.
 TRAFFIC = {
-    "k_decode_union_bf16": 450.561e6,   # profiles/k_decode_union_bf16_llama8b_b8_n32768.md
+    "k_decode_union_bf16": 450.881e6,   # profiles/k_decode_union_bf16_llama8b_b8_n32768.md
     "k_prefill_fa2_reuse": 383.524e6,   # profiles/k_prefill_fa2_reuse_n16384.md
     # captured at B=1 (8 of the 32 units) and scaled by units to B=4:
     # profiles/k_decode_union_bf16_gptoss_b4_n131072.md
-    "k_decode_union_bf16_long": 4 * 110.981e6,
+    "k_decode_union_bf16_long": 4 * 111.014e6,
 }
 UNIT = "us/layer"
 NOMINAL_HBM_GBS = 8000.0   # the ~8 TB/s HBM3e figure the decode targets are quoted against
