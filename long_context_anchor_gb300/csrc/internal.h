@@ -167,10 +167,8 @@ cudaError_t launch_prefill_reuse(const PrefillArgs& a, int head_dim, cudaStream_
 // pool.cu — GQA-pooled scores (one index set per KV head).
 // Decode: w[b,g,j] = sum over the group's heads h of softmax_j(s[b,h,:]),
 // from the anchor's logit spill s [B,Hq,N]; row_stat [B*Hq] holds each row's
-// (max, 1/sum exp(s - max)).
-// Pooled decode weights from the logit spill; row_stat holds each row's
-// (max, 1 / sum exp) already when stats_given (the bf16 attention kernel
-// writes them), else k_row_stat computes it first.
+// (max, 1/sum exp(s - max)): already when stats_given (the bf16 attention
+// kernel's split merge writes it), else k_row_stat computes it first.
 cudaError_t launch_pool_decode(const float* spill, float2* row_stat, float* w, bool stats_given,
                                const int16_t* heads, int B, int Hq, int Hkv, int G, int N,
                                cudaStream_t st);
