@@ -120,6 +120,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsign
   return false;
 }
 
+// mbar_wait for code that every lane of a warp runs and that goes on to
+// warp-collective instructions (tcgen05.mma issue, tcgen05.ld, ldmatrix,
+// mma.sync): every lane gets the same answer, so a wait that gave up in some
+// lanes only cannot split the warp before such an instruction.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, unsigned int* err,
+                                               unsigned int where) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err, where));
+}
+
 // ------------------------------------------------------------------- TMA --
 // 2-D tiled bulk-tensor load into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, uint64_t* bar, int c0,

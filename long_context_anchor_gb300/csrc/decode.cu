@@ -381,7 +381,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     bool fbad = false;
     for (int t = 0; t < ntiles; ++t) {
       const int s = t % STAGES;
-      if (!mbar_wait(&full[s], (t / STAGES) & 1, a.err, 0x103)) break;
+      if (!mbar_wait_warp(&full[s], (t / STAGES) & 1, a.err, 0x103)) break;
       float sc[4];
       slice_scores<D>(smem_u32(ktile + s * TILE_BYTES), TK, row0, qf, sc);
       const int key0 = n0 + t * TK + row0 + gid, key1 = key0 + 8;
