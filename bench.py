@@ -1062,8 +1062,9 @@ def run_ours(args):
             "reuse_hbm_gbs": round(pr_gbs, 1), "reuse_frac_of_copy": round(pr_gbs / hbm_peak, 4),
             "reuse_bytes_per_layer": int(pr_b), "anchor_bytes_per_layer": int(pa_b),
             "anchor_hbm_gbs": round(pa_b / (anchor_p * 1e-3) / 1e9, 1)}
-        # anchor: attention, row statistics, pooled weights, Top-k; reuse: one gather
-        result["gpu_launches_decode_pooled"] = args.steps * (4 * len(anchors) + len(reuse_layers))
+        # anchor: attention (which also leaves the row statistics), pooled
+        # weights, Top-k; reuse: one gather
+        result["gpu_launches_decode_pooled"] = args.steps * (3 * len(anchors) + len(reuse_layers))
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         lay01 = [(qs[0], ks[0], vs[0]), (qs[1], ks[1], vs[1])]
         result["cpu_baseline"] = time_oracle(w, lay01, n_groups=os.cpu_count() or 1, reps=2)
